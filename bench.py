@@ -1,0 +1,370 @@
+"""Benchmark: goinfer's turn-9 suffix prefill on one GB300 (or N replicas).
+
+Workload (default): Qwen2.5-7B-shaped 28-layer stack, random int4 g32 weights,
+4 slots of 16384 bf16 KV.  Slot 0 holds a conversation whose first 1668 tokens
+match every timed prompt; slots 1-3 hold conversations that share only the
+7-token chat-template start.  One step = kvr_slot_match(1922-token prompt)
+-> slot 0, reused 1668 -> kvr_prefill_suffix(254 rows).  Each step's prompt
+has a fresh 254-token tail, so every step is a complete turn-9 (match,
+cut back, prefill) and no state is reset between steps.
+
+value       = suffix rows/s over the timed steps (device time, inputs resident).
+e2e         = the same through the public API with pinned host buffers: the
+              step's hidden rows copied in, the output copied back.
+roofline    = the projection kernels (the dominant class) against the measured
+              bf16 tensor peak; attended-KV GB/s of the attention kernels is
+              reported beside it.
+cpu_baseline= the oracle (float64 numpy) on a bounded sample of the same
+              workload: one layer, the 254 suffix rows, over a 1668-row prefix.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl kvr|reference]
+For N > 1, launch under torch.distributed.run: each rank runs an independent
+replica (slots shard by conversation; no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import workloads  # noqa: E402
+
+PEAKS_PATH = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+P_CACHED, M_ROWS, PROMPT = 1668, 254, 1922
+
+
+def peaks():
+    try:
+        with open(PEAKS_PATH) as f:
+            d = json.load(f)
+        return d, "measured"
+    except Exception:
+        return dict(FALLBACK), "fallback"
+
+
+def dist_setup(n_gpus):
+    rank, world = 0, 1
+    if n_gpus > 1 or "RANK" in os.environ:
+        import torch.distributed as dist
+        rank = int(os.environ.get("RANK", 0))
+        world = int(os.environ.get("WORLD_SIZE", 1))
+        local = int(os.environ.get("LOCAL_RANK", 0))
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    return rank, world
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def max_over_ranks(x: float) -> float:
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        t = torch.tensor([x], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+    return x
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{index}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.15)
+        self.proc.terminate()
+        self.proc.wait()
+        self.f.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1])); mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# the GPU arm
+# ---------------------------------------------------------------------------
+
+def build_turn9(device, steps_total):
+    from prefix_reused_prefill_gb300 import Kvr, config_for_shape
+    shape = workloads.SHAPES["qwen7b"]
+    seed = workloads.config_seed(2)
+    tk = workloads.turn9_tokens(seed)
+    t0 = time.time()
+    lws = workloads.stack_weights(shape, seed, device=device)
+    kv = Kvr(config_for_shape(shape, 4, 16384, 256), device=device)
+    w = kv.weights(lws)
+    for s in (1, 2, 3):
+        kv.kvr_slot_assign(s, tk[f"slot{s}"])   # their K/V are never read by the timed steps
+    slot0 = tk["slot0"]
+    assert kv.kvr_slot_match(slot0[:1]) == (0, 0)
+    for a in range(0, len(slot0), 256):
+        chunk = slot0[a:a + 256]
+        kv.kvr_prefill_suffix(0, chunk, workloads.hidden_for_tokens(chunk, shape.hidden, seed).to(device), w)
+    kv.kvr_sync_status()
+    rng = np.random.Generator(np.random.PCG64(seed + 7))
+    common = tk["prompt"][:P_CACHED]
+    tails, xs = [], []
+    for _ in range(steps_total):
+        tail = rng.integers(0, workloads.VOCAB, size=M_ROWS).tolist()
+        if tail[0] == slot0[P_CACHED]:
+            tail[0] = (tail[0] + 1) % workloads.VOCAB
+        tails.append(common + tail)
+        xs.append(workloads.hidden_for_tokens(tail, shape.hidden, seed))
+    setup_s = time.time() - t0
+    return shape, kv, w, tails, xs, setup_s
+
+
+def run_gpu(args, rank, world):
+    device = torch.device("cuda", torch.cuda.current_device())
+    pk, pk_kind = peaks()
+    total = args.warmup + args.steps
+    shape, kv, w, prompts, xs_host, setup_s = build_turn9(device, 2 * total + 2)
+    xs_dev = [x.to(device) for x in xs_host[:total]]
+    out = torch.empty((M_ROWS, shape.hidden), dtype=torch.bfloat16, device=device)
+    stream = torch.cuda.current_stream()
+
+    def step(i):
+        slot, reused = kv.kvr_slot_match(prompts[i])
+        assert (slot, reused) == (0, P_CACHED), (slot, reused)
+        kv.kvr_prefill_suffix(0, prompts[i][P_CACHED:], xs_dev[i], w, out=out)
+
+    for i in range(args.warmup):
+        step(i)
+    kv.kvr_sync_status()
+    kv.kvr_profile_read()  # reset counters
+    # ---------------- timed region (device time)
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for i in range(args.warmup, total):
+        step(i)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    ms = ev0.elapsed_time(ev1)
+    clk = clocks.stop()
+    kv.kvr_sync_status()
+    _, launches = kv.kvr_profile_read()
+    ms = max_over_ranks(ms)
+    ms_step = ms / args.steps
+    value = world * M_ROWS * args.steps / (ms / 1e3)
+
+    # ---------------- the same steps with per-kernel-class events (roofline)
+    kv.kvr_profile_enable(True)
+    for i in range(args.warmup, total):
+        step(i)
+    torch.cuda.synchronize()
+    cls_ms, cls_n = kv.kvr_profile_read()
+    kv.kvr_profile_enable(False)
+
+    # ---------------- end to end through the public API with host buffers
+    pinned_in = [x.pin_memory() for x in xs_host[total:2 * total]]
+    pinned_out = torch.empty((M_ROWS, shape.hidden), dtype=torch.bfloat16).pin_memory()
+    dev_in = torch.empty((M_ROWS, shape.hidden), dtype=torch.bfloat16, device=device)
+
+    def e2e_step(j):
+        p = prompts[total + j]
+        slot, reused = kv.kvr_slot_match(p)
+        dev_in.copy_(pinned_in[j], non_blocking=True)
+        kv.kvr_prefill_suffix(slot, p[reused:], dev_in, w, out=out)
+        pinned_out.copy_(out, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    for j in range(min(args.warmup, total)):
+        e2e_step(j)
+    barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for j in range(args.warmup, total):
+        e2e_step(j)
+    torch.cuda.synchronize()
+    barrier()
+    e2e_s = max_over_ranks(time.perf_counter() - t0)
+    kv.kvr_sync_status()
+    bytes_io = M_ROWS * shape.hidden * 2
+
+    # ---------------- roofline of the dominant class (projections)
+    L = shape.n_layers
+    proj_flops = 2.0 * M_ROWS * shape.params_per_layer() * L          # per step
+    proj_ms = cls_ms[0] / args.steps
+    n_proj = cls_n[0] / args.steps
+    achieved_tf = proj_flops / (proj_ms / 1e3) / 1e12
+    peak_tf = pk.get("bf16_tflops_sustained", pk.get("bf16_tflops"))
+    attn_bytes = (P_CACHED + M_ROWS) * shape.n_kv_heads * shape.head_dim * 2 * 2 * L
+    attn_ms = cls_ms[1] / args.steps
+    attn_gbs = attn_bytes / (attn_ms / 1e3) / 1e9
+    weight_bytes = shape.params_per_layer() * L * 0.5625
+    line = {
+        "metric": "suffix-prefill rows/s",
+        "value": round(value, 1),
+        "unit": "rows/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": "turn-9 suffix prefill: Qwen2.5-7B-shaped 28-layer int4-g32 stack, "
+                               "1922-token prompt, 1668 cached, 254 suffix rows, 4 slots x 16384",
+                   "global_batch": M_ROWS * world, "seq_len": PROMPT, "parallelism": f"replicas{world}",
+                   "l2": "inputs larger than L2: 3.67 GB of int4 weights streamed per step"},
+        "attended_kv_gbs": round(attn_gbs, 1),
+        "attended_kv_frac_hbm": round(attn_gbs / pk["hbm_gbs"], 4),
+        "roofline": {"bound": "tensor", "achieved": round(achieved_tf, 2),
+                     "peak": peak_tf, "unit": "TFLOP/s",
+                     "frac": round(achieved_tf / peak_tf, 4), "traffic": None,
+                     "peak_kind": f"bf16 sustained ({pk_kind})",
+                     "kernel": "projections (gemv_int4 / gemm_int4)",
+                     "launches_per_step": n_proj, "ms_per_step": round(proj_ms, 4),
+                     "weight_gbs": round(weight_bytes / (proj_ms / 1e3) / 1e9, 1)},
+        "kernel_ms_per_step": {"projections": round(cls_ms[0] / args.steps, 4),
+                               "attention": round(cls_ms[1] / args.steps, 4),
+                               "epilogues": round(cls_ms[2] / args.steps, 4),
+                               "prefix_match": round(cls_ms[3] / args.steps, 4)},
+        "e2e": {"value": round(world * M_ROWS * args.steps / e2e_s, 1), "unit": "rows/s",
+                "h2d_bytes_per_step": bytes_io + PROMPT * 4, "d2h_bytes_per_step": bytes_io + 4 * 4 * 4},
+        "gpu_launches": int(sum(launches)),
+        "clocks": clk,
+        "setup_s": round(setup_s, 1),
+    }
+    if rank == 0 and not args.no_cpu:
+        line["cpu_baseline"] = cpu_baseline(args.cpu_rows)
+    return line, rank
+
+
+# ---------------------------------------------------------------------------
+# the oracle, timed on the host cores
+# ---------------------------------------------------------------------------
+
+def cpu_baseline(rows: int, layers_timed: int = 1):
+    """Oracle (float64 numpy, as it stands) on one layer of the turn-9 workload:
+    `rows` suffix rows over a 1668-row cached prefix (K/V drawn N(0,1)), scaled to
+    rows/s of the full 28-layer stack.  Weight decoding happens before timing."""
+    from oracle import model as om
+    from oracle import formats
+    shape = workloads.SHAPES["qwen7b"]
+    seed = workloads.config_seed(2)
+    lw = workloads.layer_weights(shape, seed, 0, device="cpu")
+    W = {}
+    for k, v in lw.items():
+        if hasattr(v, "packed"):
+            W[k] = formats.dequant_int4(v.packed.numpy(), v.scales.numpy())
+        else:
+            W[k] = v.to(torch.float64).numpy()
+    dims = om.Dims(shape.hidden, shape.n_q_heads, shape.n_kv_heads, shape.head_dim, shape.ffn, False,
+                   shape.rope_theta, shape.rms_eps)
+    cache = om.SlotKV(1, shape.n_kv_heads, P_CACHED + rows, shape.head_dim)
+    k, v = workloads.random_kv(shape.n_kv_heads, P_CACHED, shape.head_dim, seed)
+    cache.K[0][:, :P_CACHED] = workloads.bf16_to_f64(k)
+    cache.V[0][:, :P_CACHED] = workloads.bf16_to_f64(v)
+    x = workloads.bf16_to_f64(workloads.hidden_for_tokens(list(range(rows)), shape.hidden, seed))
+    t0 = time.perf_counter()
+    om.layer(dims, W, x, cache.K[0], cache.V[0], om.plain_rows(P_CACHED, rows))
+    dt = time.perf_counter() - t0
+    per_row_stack = dt / rows * shape.n_layers
+    cores = int(os.environ.get("OMP_NUM_THREADS", 0)) or os.cpu_count()
+    return {"value": round(1.0 / per_row_stack, 3), "unit": "rows/s", "cores": cores,
+            "kind": "oracle",
+            "sample": f"1 of 28 layers, {rows} suffix rows over 1668 cached rows, float64 numpy "
+                      f"({dt:.2f} s), scaled to the 28-layer stack"}
+
+
+def run_reference(args, rank, world):
+    """--impl reference: the oracle as the reference arm (host cores)."""
+    if rank != 0:
+        return None, rank
+    vals = []
+    for _ in range(args.warmup):
+        cpu_baseline(args.cpu_rows)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        vals.append(cpu_baseline(args.cpu_rows))
+    dt = time.perf_counter() - t0
+    v = statistics.median(x["value"] for x in vals)
+    cb = dict(vals[0]); cb["value"] = v
+    line = {"impl": "reference", "metric": "suffix-prefill rows/s", "value": v, "unit": "rows/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1000 * M_ROWS / v, 1), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "turn-9 suffix prefill: Qwen2.5-7B-shaped 28-layer int4-g32 stack, "
+                                   "1922-token prompt, 1668 cached, 254 suffix rows, 4 slots x 16384"},
+            "cpu_baseline": cb, "e2e": {"value": v, "unit": "rows/s", "h2d_bytes_per_step": 0,
+                                        "d2h_bytes_per_step": 0},
+            "wall_s": round(dt, 1)}
+    return line, rank
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="kvr", choices=["kvr", "reference"])
+    ap.add_argument("--cpu-rows", type=int, default=64)
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3) if args.impl == "kvr" else max(args.warmup, 0)
+    rank, world = dist_setup(args.gpus)
+    if args.impl == "reference":
+        line, rank = run_reference(args, rank, world)
+    else:
+        line, rank = run_gpu(args, rank, world)
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,247 @@
+/*
+ * kvr.h -- prefix-reused (suffix) prefill against a resident GPU KV slot.
+ *
+ * One process, one GB300 (sm_103a).  The library keeps a table of KV-cache
+ * slots, one conversation each, and runs only the un-cached suffix of a
+ * prompt (or the m = k+1 rows of a speculative verify) through a decoder
+ * stack whose K/V for the cached prefix already sit in the slot.
+ *
+ * Sources (page title, section):
+ *   goinfer "Turn nine in under half a second":
+ *     "What goinfer does"  -- keep the KV cache (two vectors per token in each
+ *                             layer) of recent conversations; process only the
+ *                             tokens after the conversation's stored start.
+ *     "How it works"       -- longest shared start; a match must be longer
+ *                             than what the session shares with the other
+ *                             sessions; cut back to the shared point; on a GPU
+ *                             model, --kv-sessions slots, empty slot else LRU;
+ *                             usage.prefill_reused_tokens.
+ *     "Use it"             -- --kv-sessions N (0 turns reuse off); the memory
+ *                             check may grant fewer slots than asked for.
+ *     "What we got wrong"  -- the one-token-short cache after speculation.
+ *   thinkspread "The economics of speculative decoding", cost model -- the
+ *     m = k+1 verify rows run as one batched pass that reads each weight once.
+ *   OpenJev "Latency", What changed / Repeated state -- several questions
+ *     resume from one checkpoint placed exactly at the end of a shared state.
+ *
+ * ---------------------------------------------------------------------------
+ * Ownership.  The caller allocates every device buffer (the KV arena, the
+ * scratch area, weights, inputs, outputs) and owns the CUDA stream.  The
+ * library allocates no device memory; it owns only host state (the slot token
+ * lists, lengths, LRU stamps, cached TMA descriptors).  All calls that take a
+ * stream are asynchronous on it, except kvr_slot_match, which waits for the
+ * stream to read back the match lengths, and kvr_sync_status.
+ *
+ * Errors.  Every int-returning call returns KVR_OK (0) or a negative code;
+ * kvr_last_error() says why.  A failed call leaves every slot's length and
+ * tokens unchanged and launches nothing (validation precedes any launch).
+ *
+ * Threads.  A context is not thread-safe; serialise calls on one context.
+ * ---------------------------------------------------------------------------
+ */
+#ifndef KVR_H
+#define KVR_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define KVR_OK 0
+#define KVR_ERR_ARG (-1)         /* null pointer, bad slot, n <= 0, m <= 0, bad config   */
+#define KVR_ERR_CAPACITY (-2)    /* len + m > capacity, m > max_rows, small arena/scratch */
+#define KVR_ERR_CUDA (-3)        /* a CUDA runtime / driver call failed                   */
+#define KVR_ERR_TIMEOUT (-4)     /* a device-side wait gave up (status word set)          */
+#define KVR_ERR_FAULT (-5)       /* injected through the KVR_FAULT environment variable   */
+#define KVR_ERR_UNSUPPORTED (-6) /* a shape the kernels do not handle (see kvr_config)    */
+
+#define KVR_WEIGHTS_BF16 0
+#define KVR_WEIGHTS_INT4_G32 1
+
+#define KVR_MAX_SLOTS 16
+#define KVR_MAX_BRANCHES 16
+
+/*
+ * Model and table configuration.
+ *   n_slots        requested KV slots (--kv-sessions).  0 = reuse off: one
+ *                  working slot, every kvr_slot_match returns slot 0 with
+ *                  reused = 0.  At most KVR_MAX_SLOTS.
+ *   capacity       tokens per slot; a multiple of 64.
+ *   n_layers, hidden, n_q_heads, n_kv_heads, head_dim, ffn
+ *                  decoder shape.  head_dim is 64 or 128; n_q_heads is a
+ *                  multiple of n_kv_heads (grouped-query attention: query head
+ *                  h reads KV head h / (n_q_heads / n_kv_heads)).
+ *   weight_format  KVR_WEIGHTS_BF16 or KVR_WEIGHTS_INT4_G32 (layouts below).
+ *                  For int4 every projection's input width K must be a
+ *                  multiple of 256.
+ *   attn_only      1: a layer is out = Attn(x) Wo^T (no norms, no FFN, no
+ *                  residual).  0: the pre-norm decoder layer
+ *                    a = RMSNorm(h); h += Attn(a) Wo^T;
+ *                    b = RMSNorm(h); h += (silu(b Wg^T) * (b Wu^T)) Wd^T.
+ *   match_threshold 1 (default): the anti-theft rule of kvr_slot_match.
+ *   max_rows       largest m of one prefill / verify / branches call; sizes
+ *                  the scratch area.
+ *   rope_theta     rotate-half RoPE base; rows sit at absolute slot positions.
+ *   rms_eps        RMSNorm epsilon.
+ */
+typedef struct kvr_config {
+  int n_slots;
+  int capacity;
+  int n_layers;
+  int hidden;
+  int n_q_heads;
+  int n_kv_heads;
+  int head_dim;
+  int ffn;
+  int weight_format;
+  int attn_only;
+  int match_threshold;
+  int max_rows;
+  float rope_theta;
+  float rms_eps;
+} kvr_config;
+
+/*
+ * Weights of one layer: device pointers owned by the caller, stable while a
+ * call that uses them is in flight.  Matrices are in the torch Linear
+ * orientation [N][K] (output row n, input k):
+ *   wq [Hq*d][H], wk [Hkv*d][H], wv [Hkv*d][H], wo [H][Hq*d],
+ *   wg [F][H], wu [F][H], wd [H][F]   (wg/wu/wd unused when attn_only).
+ * KVR_WEIGHTS_BF16: w* are bf16 [N][K] row-major; s* unused.
+ * KVR_WEIGHTS_INT4_G32 (symmetric int4, one fp16 scale per 32 inputs):
+ *   w* are uint8 [N][K/2]: row n is K/2 bytes.  Group g of row n (inputs
+ *   32g .. 32g+31) is the 16 bytes at row offset 16g, read as four
+ *   little-endian 32-bit words.  Input k' = k - 32g (0..31) is held in word
+ *   (k' mod 8) div 2, in the 4-bit field number (k' div 8) + 4*(k' mod 2)
+ *   counted from the least significant bits.  A field holds code + 8 with
+ *   code in [-8, 7].
+ *   s* are fp16 [N][K/32] row-major; weight(n, k) = code(n, k) * s[n][k/32].
+ *   (The field order lets one 32-bit shared-memory load give a tensor-core
+ *   fragment its eight inputs of one group.)
+ * norm_attn, norm_ffn: bf16 [H] RMSNorm gains (unused when attn_only).
+ * Every pointer must be 16-byte aligned.
+ */
+typedef struct kvr_layer_weights {
+  const void *wq, *wk, *wv, *wo, *wg, *wu, *wd;
+  const void *sq, *sk, *sv, *so, *sg, *su, *sd;
+  const void *norm_attn, *norm_ffn;
+} kvr_layer_weights;
+
+typedef struct kvr_ctx kvr_ctx;
+
+/*
+ * Device bytes the caller must provide.
+ * KV arena (slot-major; a slot's region is contiguous):
+ *   slot s, layer l, kind c (0 = K, 1 = V), KV head j, position p, element e at
+ *   bf16 index ((((s*L + l)*2 + c)*Hkv + j)*capacity + p)*head_dim + e,
+ *   followed by the device token mirror int32 [n_slots][capacity].
+ *   kvr_arena_bytes(cfg, n) is the size for n slots (n = cfg->n_slots, or 1
+ *   when n_slots is 0).
+ * Scratch: activations, partial sums, RoPE tables, the match buffers and the
+ *   device status word; its contents do not outlive a call.
+ * Both return 0 for an invalid configuration.
+ */
+size_t kvr_arena_bytes(const kvr_config* cfg, int n_slots);
+size_t kvr_scratch_bytes(const kvr_config* cfg);
+
+/*
+ * Create a context over caller-allocated device memory (256-byte aligned).
+ * If arena_bytes holds fewer slots than cfg->n_slots (but at least one) the
+ * context grants that many and kvr_ctx_info reports both numbers ("Use it":
+ * the memory check may allow fewer slots than asked for).  Fails with
+ * KVR_ERR_CAPACITY if not even one slot or the scratch area fits.  Must be
+ * called with the device that owns the buffers current.
+ */
+int kvr_ctx_create(const kvr_config* cfg, void* kv_arena, size_t arena_bytes, void* scratch,
+                   size_t scratch_bytes, kvr_ctx** out);
+int kvr_ctx_info(const kvr_ctx* ctx, int* slots_granted, int* slots_requested, int* capacity);
+int kvr_ctx_destroy(kvr_ctx* ctx);
+
+/*
+ * Choose the slot for a prompt (tokens: host int32[n], n >= 1) and cut it
+ * back to the shared point.  Prefix lengths are computed on the device by the
+ * prefix-match kernel on `stream`; the call then synchronises on the stream
+ * and applies the policy on the host:
+ *   l(s) = longest common token prefix of slot s and the prompt;
+ *   o(s) = longest common prefix of slot s and any other occupied slot;
+ *   s* = the occupied slot with the largest l (lowest index on ties).
+ *   With match_threshold = 1, s* is accepted iff l(s*) > 0, l(s*) > o(s*), and
+ *   it would not cut s* back (l(s*) < len(s*)) while another slot is empty.
+ *   With match_threshold = 0, s* is accepted iff l(s*) > 0.
+ *   Accepted: reused = min(l(s*), n-1); the slot is truncated to reused.
+ *   Otherwise the lowest-index empty slot, else the least recently used slot,
+ *   restarts empty: reused = 0.
+ * *slot receives the slot, *reused the count to report as
+ * usage.prefill_reused_tokens.  The caller then prefills tokens[reused:].
+ */
+int kvr_slot_match(kvr_ctx* ctx, const int32_t* tokens, int n, int* slot, int* reused,
+                   void* stream);
+/* Cut a slot back to new_len <= len (a host length update; K/V beyond it are
+ * simply ignored from then on).  Used after a verify to keep p0+1+accepted. */
+int kvr_slot_truncate(kvr_ctx* ctx, int slot, int new_len);
+int kvr_slot_len(const kvr_ctx* ctx, int slot, int* len);
+/* Copy of the first min(n, len) tokens of a slot into host tokens[]. */
+int kvr_slot_tokens(const kvr_ctx* ctx, int slot, int32_t* tokens, int n);
+/* Declare that slot `slot` holds tokens[0..n) whose K/V the caller has
+ * written into the arena (restoring a saved slot, or synthetic K/V).  Uploads
+ * the token mirror on `stream`. */
+int kvr_slot_assign(kvr_ctx* ctx, int slot, const int32_t* tokens, int n, void* stream);
+/* Device addresses of a slot's K and V for one layer: [Hkv][capacity][head_dim] bf16. */
+int kvr_slot_kv(const kvr_ctx* ctx, int slot, int layer, void** k, void** v);
+
+/*
+ * Suffix prefill: run m rows (tokens: host int32[m]; hidden: device bf16
+ * [m][hidden], the rows' input hidden states) at positions p0 .. p0+m-1 of
+ * slot `slot`, p0 = the slot's length.  Each row attends causally to the
+ * slot's cached K/V [0, p0) and to the new rows up to itself; the new rows'
+ * K/V are appended.  w: host array of n_layers kvr_layer_weights.  out:
+ * device bf16 [m][hidden], the last layer's output (the residual stream for a
+ * full layer, Attn(x) Wo^T for attn_only).  On success the slot's length is
+ * p0+m and its tokens gain tokens[0..m).
+ * KVR_ERR_CAPACITY if p0+m > capacity or m > max_rows.
+ */
+int kvr_prefill_suffix(kvr_ctx* ctx, int slot, const int32_t* tokens, int m, const void* hidden,
+                       const kvr_layer_weights* w, void* out, void* stream);
+
+/* Speculative verify: the same computation for the m = k+1 rows (the last
+ * accepted token plus k drafts).  The rows are appended; the caller then calls
+ * kvr_slot_truncate(slot, p0 + 1 + accepted) so the cache holds exactly the
+ * committed tokens (the "one token short" fix).  1 <= m <= 64. */
+int kvr_verify(kvr_ctx* ctx, int slot, const int32_t* tokens, int m, const void* hidden,
+               const kvr_layer_weights* w, void* out, void* stream);
+
+/*
+ * Several questions resuming from one checkpoint in one batch.  The slot's
+ * length P is the checkpoint.  Branch b has lens[b] rows (rows are
+ * concatenated in branch order: tokens host int32[sum], hidden device bf16
+ * [sum][hidden]).  Row i of branch b sits at position P+i, as if it were the
+ * only question, and attends to [0, P) plus its own branch's rows up to
+ * itself.  The branches' K/V are written after position P (in branch order)
+ * but are not committed: the slot keeps length P and its tokens.
+ * 1 <= n_branch <= KVR_MAX_BRANCHES; P + sum(lens) <= capacity.
+ */
+int kvr_prefill_branches(kvr_ctx* ctx, int slot, int n_branch, const int* lens,
+                         const int32_t* tokens, const void* hidden, const kvr_layer_weights* w,
+                         void* out, void* stream);
+
+/* Wait for `stream` and check the device status word that kernels set when a
+ * bounded device-side wait gives up.  Returns KVR_ERR_TIMEOUT (and clears the
+ * word) if one did. */
+int kvr_sync_status(kvr_ctx* ctx, void* stream);
+
+/* Per-kernel-class timing with CUDA events recorded on the launch stream.
+ * While enabled, every launch is bracketed by an event pair; kvr_profile_read
+ * synchronises and returns milliseconds summed since the last read for
+ * classes: 0 projections (GEMV/GEMM), 1 attention (incl. split merge),
+ * 2 epilogues / norms / RoPE tables, 3 prefix match; and launch counts. */
+int kvr_profile_enable(kvr_ctx* ctx, int on);
+int kvr_profile_read(kvr_ctx* ctx, float ms[4], int launches[4]);
+
+const char* kvr_last_error(const kvr_ctx* ctx);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KVR_H */

@@ -1,0 +1,345 @@
+// Causal grouped-query attention of the new rows over a slot's cached prefix
+// plus the new rows themselves, split across the key axis.
+//
+// goinfer, "Turn nine in under half a second" ("The problem", "What goinfer
+// does"): prefill cost grows with the conversation; the cached rows' K/V are
+// kept, so the m new rows attend to them instead of recomputing them.
+// OpenJev "Latency" ("What changed"): several questions resume from one
+// checkpoint -- each row sees the shared state plus its own question's rows.
+//
+// One CTA = (row tile, key split, KV head).  All G = Hq/Hkv query heads of a
+// KV head and all m tokens are packed as rows (row = token*G + head-in-group),
+// so each K/V tile is read from HBM once per (tile, split) for every query
+// head that uses it.  A producer warp streams 64-key K and V tiles through TMA
+// (128B-swizzled) into a 3-stage mbarrier ring; each consumer warp owns 16
+// rows: S = Q K^T and O += P V run as bf16 m16n8k16 tensor-core fragments
+// (ldmatrix / ldmatrix.trans from the swizzled tiles), the online softmax runs
+// in fp32 registers in the log2 domain with quad shuffles.  With several
+// splits, unnormalised partials (O, running max, running sum) are merged by
+// attn_combine in a fixed split order.
+#include "kvr_internal.cuh"
+
+namespace kvr {
+
+namespace {
+
+template <int D>
+struct AttnCfg {
+  static constexpr int kHalves = D / 64;                 // 64-element TMA boxes per row
+  static constexpr int kTileBytes = kAttnKeys * D * 2;   // one K (or V) tile
+  static constexpr int kStageBytes = 2 * kTileBytes;
+  static constexpr int kStages = D == 128 ? 3 : 4;
+  static constexpr int kSmem = kStages * kStageBytes + 1024;
+};
+
+struct RowInfo {
+  int tok;      // token index, -1 for padding rows
+  int head;     // query head
+  int lo, hi;   // own-branch visible slot indices [lo, hi]
+};
+
+__device__ __forceinline__ RowInfo row_info(const AttnParams& p, int kv, int rho) {
+  RowInfo ri;
+  const int R = p.G * p.rows.m;
+  if (rho >= R) {
+    ri.tok = -1; ri.head = 0; ri.lo = 1; ri.hi = 0;
+    return ri;
+  }
+  ri.tok = rho / p.G;
+  ri.head = kv * p.G + rho % p.G;
+  const int b = row_branch(p.rows, ri.tok);
+  ri.lo = p.rows.P + p.rows.off[b];
+  ri.hi = p.rows.P + ri.tok;
+  return ri;
+}
+
+__device__ __forceinline__ bool visible(const AttnParams& p, const RowInfo& ri, int j) {
+  return ri.tok >= 0 && (j < p.rows.P || (j >= ri.lo && j <= ri.hi));
+}
+
+template <int D, int RW>
+__global__ void __launch_bounds__((RW + 1) * 32) attn_kernel(const __grid_constant__ AttnParams p) {
+  using C = AttnCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t full_bar[C::kStages];
+  __shared__ __align__(8) uint64_t empty_bar[C::kStages];
+  __shared__ int abort_flag;
+  volatile int* abort_v = &abort_flag;
+
+  const uint32_t base = (dev::smem_u32(smem_raw) + 1023u) & ~1023u;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int rt = blockIdx.x, split = blockIdx.y, kv = blockIdx.z;
+  const int R = p.G * p.rows.m;
+  const int row_lo = rt * 16 * RW;
+  const int row_hi = min(R, row_lo + 16 * RW);        // exclusive
+  const int last_tok = (row_hi - 1) / p.G;
+  const int kend = p.rows.P + last_tok + 1;            // keys [0, kend) may be visible
+  const int nb = (kend + kAttnKeys - 1) / kAttnKeys;
+  const int b0 = (int)((long long)nb * split / p.nsplit);
+  const int b1 = (int)((long long)nb * (split + 1) / p.nsplit);
+  const int nblk = b1 - b0;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::kStages; ++i) {
+      dev::mbar_init(dev::smem_u32(&full_bar[i]), 1);
+      dev::mbar_init(dev::smem_u32(&empty_bar[i]), RW);
+    }
+    *abort_v = 0;
+    dev::fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == RW) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      dev::prefetch_tmap(&p.tkv);
+      int issued = 0;
+      for (int it = 0; it < nblk; ++it) {
+        const int st = it % C::kStages;
+        const uint32_t use = (uint32_t)(it / C::kStages);
+        if (it >= C::kStages) {
+          if (!dev::mbar_wait(dev::smem_u32(&empty_bar[st]), (use - 1) & 1, p.status) ||
+              *abort_v) {
+            *abort_v = 1;
+            break;
+          }
+        }
+        const uint32_t sb = base + st * C::kStageBytes;
+        const uint32_t fb = dev::smem_u32(&full_bar[st]);
+        dev::mbar_arrive_expect_tx(fb, C::kStageBytes);
+        const int key0 = (b0 + it) * kAttnKeys;
+#pragma unroll
+        for (int h = 0; h < C::kHalves; ++h) {
+          dev::tma_load_2d(sb + h * (kAttnKeys * 128), &p.tkv, 64 * h, p.kbase + kv * p.cap + key0, fb);
+          dev::tma_load_2d(sb + C::kTileBytes + h * (kAttnKeys * 128), &p.tkv, 64 * h,
+                           p.vbase + kv * p.cap + key0, fb);
+        }
+        ++issued;
+      }
+      for (int st = 0; st < C::kStages && st < issued; ++st) {
+        const int last = ((issued - 1 - st) / C::kStages) * C::kStages + st;
+        dev::mbar_wait(dev::smem_u32(&full_bar[st]), (uint32_t)(last / C::kStages) & 1, nullptr);
+      }
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  const int r = lane >> 2, c = lane & 3;
+  const int rho0 = row_lo + warp * 16 + r;
+  const RowInfo ri0 = row_info(p, kv, rho0);
+  const RowInfo ri1 = row_info(p, kv, rho0 + 8);
+
+  // Q fragments (A operand of S = Q K^T), loaded once
+  uint32_t qa[D / 16][4];
+  {
+    const __nv_bfloat16* q0 = ri0.tok >= 0 ? p.q + ((long long)ri0.tok * p.Hq + ri0.head) * D : nullptr;
+    const __nv_bfloat16* q1 = ri1.tok >= 0 ? p.q + ((long long)ri1.tok * p.Hq + ri1.head) * D : nullptr;
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      const int d0 = kk * 16 + 2 * c;
+      qa[kk][0] = q0 ? *reinterpret_cast<const uint32_t*>(q0 + d0) : 0u;
+      qa[kk][1] = q1 ? *reinterpret_cast<const uint32_t*>(q1 + d0) : 0u;
+      qa[kk][2] = q0 ? *reinterpret_cast<const uint32_t*>(q0 + d0 + 8) : 0u;
+      qa[kk][3] = q1 ? *reinterpret_cast<const uint32_t*>(q1 + d0 + 8) : 0u;
+    }
+  }
+
+  float o[D / 8][4];
+#pragma unroll
+  for (int i = 0; i < D / 8; ++i)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) o[i][e] = 0.f;
+  float mrow[2] = {-INFINITY, -INFINITY};
+  float lrow[2] = {0.f, 0.f};
+  const float zero4[4] = {0.f, 0.f, 0.f, 0.f};
+
+  for (int it = 0; it < nblk; ++it) {
+    const int st = it % C::kStages;
+    const uint32_t use = (uint32_t)(it / C::kStages);
+    if (!dev::mbar_wait(dev::smem_u32(&full_bar[st]), use & 1, p.status) || *abort_v) {
+      *abort_v = 1;
+      break;
+    }
+    const uint32_t kt = base + st * C::kStageBytes;
+    const uint32_t vt = kt + C::kTileBytes;
+    const int key0 = (b0 + it) * kAttnKeys;
+
+    // S = Q K^T for 64 keys: 8 n-tiles of 8 keys
+    float s[8][4];
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) s[nt][e] = 0.f;
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+#pragma unroll
+      for (int np = 0; np < 4; ++np) {
+        const int q = lane >> 3;
+        const int key = 8 * (2 * np + (q >> 1)) + (lane & 7);
+        const int chunk = 2 * kk + (q & 1);
+        uint32_t b0r, b1r, b2r, b3r;
+        dev::ldmatrix_x4(kt + (chunk >> 3) * (kAttnKeys * 128) + dev::swz128(key, chunk & 7), b0r,
+                         b1r, b2r, b3r);
+        dev::mma_bf16_16816(s[2 * np], qa[kk], b0r, b1r, s[2 * np]);
+        dev::mma_bf16_16816(s[2 * np + 1], qa[kk], b2r, b3r, s[2 * np + 1]);
+      }
+    }
+
+    // mask, scale to log2 units, online softmax
+    float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int j = key0 + 8 * nt + 2 * c + (e & 1);
+        const bool vis = (e < 2) ? visible(p, ri0, j) : visible(p, ri1, j);
+        const float v = vis ? s[nt][e] * p.scale_log2 : -INFINITY;
+        s[nt][e] = v;
+        mx[e >> 1] = fmaxf(mx[e >> 1], v);
+      }
+    }
+    float corr[2], muse[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 1));
+      mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 2));
+      const float mnew = fmaxf(mrow[h], mx[h]);
+      muse[h] = mnew == -INFINITY ? 0.f : mnew;
+      corr[h] = exp2f(mrow[h] - muse[h]);
+      mrow[h] = mnew;
+      lrow[h] *= corr[h];
+    }
+#pragma unroll
+    for (int i = 0; i < D / 8; ++i) {
+      o[i][0] *= corr[0]; o[i][1] *= corr[0];
+      o[i][2] *= corr[1]; o[i][3] *= corr[1];
+    }
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float pv = exp2f(s[nt][e] - muse[e >> 1]);
+        s[nt][e] = pv;
+        lrow[e >> 1] += pv;
+      }
+    }
+
+    // O += P V: P as the A operand (16 keys per k-step), V^T fragments by ldmatrix.trans
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks) {
+      uint32_t pa[4];
+      pa[0] = dev::pack_bf16x2(s[2 * ks][0], s[2 * ks][1]);
+      pa[1] = dev::pack_bf16x2(s[2 * ks][2], s[2 * ks][3]);
+      pa[2] = dev::pack_bf16x2(s[2 * ks + 1][0], s[2 * ks + 1][1]);
+      pa[3] = dev::pack_bf16x2(s[2 * ks + 1][2], s[2 * ks + 1][3]);
+#pragma unroll
+      for (int dp = 0; dp < D / 16; ++dp) {
+        const int q = lane >> 3;
+        const int key = 16 * ks + 8 * (q & 1) + (lane & 7);
+        const int chunk = 2 * dp + (q >> 1);
+        uint32_t b0r, b1r, b2r, b3r;
+        dev::ldmatrix_x4_trans(vt + (chunk >> 3) * (kAttnKeys * 128) + dev::swz128(key, chunk & 7),
+                               b0r, b1r, b2r, b3r);
+        dev::mma_bf16_16816(o[2 * dp], pa, b0r, b1r, o[2 * dp]);
+        dev::mma_bf16_16816(o[2 * dp + 1], pa, b2r, b3r, o[2 * dp + 1]);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) dev::mbar_arrive(dev::smem_u32(&empty_bar[st]));
+  }
+  if (*abort_v) return;
+  (void)zero4;
+
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    lrow[h] += __shfl_xor_sync(0xffffffffu, lrow[h], 1);
+    lrow[h] += __shfl_xor_sync(0xffffffffu, lrow[h], 2);
+  }
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const RowInfo& ri = h == 0 ? ri0 : ri1;
+    if (ri.tok < 0) continue;
+    const long long rowidx = (long long)ri.tok * p.Hq + ri.head;
+    if (p.nsplit == 1) {
+      const float inv = 1.f / lrow[h];
+      __nv_bfloat16* dst = p.o + rowidx * D;
+#pragma unroll
+      for (int i = 0; i < D / 8; ++i)
+        *reinterpret_cast<uint32_t*>(dst + 8 * i + 2 * c) =
+            dev::pack_bf16x2(o[i][2 * h] * inv, o[i][2 * h + 1] * inv);
+    } else {
+      const long long plane = (long long)p.rows.m * p.Hq;
+      float* dst = p.opart + ((long long)split * plane + rowidx) * D;
+#pragma unroll
+      for (int i = 0; i < D / 8; ++i)
+        *reinterpret_cast<float2*>(dst + 8 * i + 2 * c) = make_float2(o[i][2 * h], o[i][2 * h + 1]);
+      if (c == 0) p.ml[split * plane + rowidx] = make_float2(mrow[h], lrow[h]);
+    }
+  }
+}
+
+template <int D>
+__global__ void attn_combine_kernel(const __grid_constant__ AttnParams p) {
+  const long long rowidx = blockIdx.x;  // token * Hq + head
+  const int d = threadIdx.x;
+  const long long plane = (long long)p.rows.m * p.Hq;
+  float M = -INFINITY;
+  for (int s = 0; s < p.nsplit; ++s) M = fmaxf(M, p.ml[s * plane + rowidx].x);
+  float num = 0.f, den = 0.f;
+  for (int s = 0; s < p.nsplit; ++s) {
+    const float2 ml = p.ml[s * plane + rowidx];
+    const float w = ml.x == -INFINITY ? 0.f : exp2f(ml.x - M);
+    num += w * p.opart[(s * plane + rowidx) * D + d];
+    den += w * ml.y;
+  }
+  p.o[rowidx * D + d] = __float2bfloat16_rn(num / den);
+}
+
+template <int D, int RW>
+cudaError_t launch_t(const AttnParams& p, cudaStream_t st) {
+  const dim3 grid(p.row_tiles, p.nsplit, p.Hkv);
+  attn_kernel<D, RW><<<grid, (RW + 1) * 32, AttnCfg<D>::kSmem, st>>>(p);
+  return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t setup_d() {
+  cudaError_t e;
+  e = cudaFuncSetAttribute(attn_kernel<D, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, AttnCfg<D>::kSmem);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(attn_kernel<D, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, AttnCfg<D>::kSmem);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(attn_kernel<D, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize, AttnCfg<D>::kSmem);
+}
+
+}  // namespace
+
+int attn_smem(int d) { return d == 128 ? AttnCfg<128>::kSmem : AttnCfg<64>::kSmem; }
+
+cudaError_t attn_setup() {
+  cudaError_t e = setup_d<64>();
+  if (e != cudaSuccess) return e;
+  return setup_d<128>();
+}
+
+cudaError_t launch_attention(const AttnParams& p, int d, int row_warps, cudaStream_t st) {
+  if (d == 128) {
+    if (row_warps == 1) return launch_t<128, 1>(p, st);
+    if (row_warps == 2) return launch_t<128, 2>(p, st);
+    return launch_t<128, 4>(p, st);
+  }
+  if (row_warps == 1) return launch_t<64, 1>(p, st);
+  if (row_warps == 2) return launch_t<64, 2>(p, st);
+  return launch_t<64, 4>(p, st);
+}
+
+cudaError_t launch_attn_combine(const AttnParams& p, int d, cudaStream_t st) {
+  const unsigned rows = (unsigned)(p.rows.m * p.Hq);
+  if (d == 128) attn_combine_kernel<128><<<rows, 128, 0, st>>>(p);
+  else attn_combine_kernel<64><<<rows, 64, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace kvr

@@ -1,0 +1,873 @@
+// C-ABI of libkvr: the slot table and the suffix-prefill driver.
+//
+// Host policy (goinfer, "Turn nine in under half a second", "How it works" and
+// "Use it"): longest shared start, the anti-theft rule, empty slot else LRU,
+// cut back to the shared point, reused-token count; --kv-sessions 0 turns
+// reuse off; the memory check may grant fewer slots than requested.
+// Device work is enqueued on the caller's stream; the library owns no device
+// memory -- it carves the caller's arena and scratch buffers.
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <map>
+#include <string>
+#include <tuple>
+#include <vector>
+
+#include <cudaTypedefs.h>
+
+#include "kvr_internal.cuh"
+
+using namespace kvr;
+
+namespace {
+
+constexpr size_t kAlign = 256;
+inline size_t align_up(size_t x, size_t a = kAlign) { return (x + a - 1) / a * a; }
+
+enum ProfClass { kProj = 0, kAttn = 1, kEpi = 2, kMatch = 3 };
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+bool valid_config(const kvr_config* c, std::string* why) {
+  auto bad = [&](const char* m) { if (why) *why = m; return false; };
+  if (!c) return bad("config is null");
+  if (c->n_slots < 0 || c->n_slots > KVR_MAX_SLOTS) return bad("n_slots must be in [0, 16]");
+  if (c->capacity <= 0 || c->capacity % kAttnKeys) return bad("capacity must be a positive multiple of 64");
+  if (c->n_layers <= 0 || c->hidden <= 0 || c->n_q_heads <= 0 || c->n_kv_heads <= 0)
+    return bad("layer shape must be positive");
+  if (c->head_dim != 64 && c->head_dim != 128) return bad("head_dim must be 64 or 128");
+  if (c->n_q_heads % c->n_kv_heads) return bad("n_q_heads must be a multiple of n_kv_heads");
+  if (c->hidden % 8) return bad("hidden must be a multiple of 8");
+  if (!c->attn_only && (c->ffn <= 0 || c->ffn % 8)) return bad("ffn must be a positive multiple of 8");
+  if (c->weight_format != KVR_WEIGHTS_BF16 && c->weight_format != KVR_WEIGHTS_INT4_G32)
+    return bad("weight_format must be 0 (bf16) or 1 (int4 g32)");
+  if (c->weight_format == KVR_WEIGHTS_INT4_G32) {
+    if (c->hidden % kGemvKStep || (c->n_q_heads * c->head_dim) % kGemvKStep ||
+        (!c->attn_only && c->ffn % kGemvKStep))
+      return bad("int4 weights need every projection input width to be a multiple of 256");
+  }
+  if (c->max_rows <= 0) return bad("max_rows must be positive");
+  if (c->max_rows > c->capacity) return bad("max_rows must not exceed capacity");
+  if ((long long)c->max_rows * c->n_q_heads / c->n_kv_heads > (1 << 20)) return bad("max_rows too large");
+  return true;
+}
+
+size_t slot_kv_bytes(const kvr_config* c) {
+  return (size_t)c->n_layers * 2 * c->n_kv_heads * (size_t)c->capacity * c->head_dim * 2;
+}
+
+int qkv_cols(const kvr_config* c) { return (c->n_q_heads + 2 * c->n_kv_heads) * c->head_dim; }
+int max_ldo(const kvr_config* c) {
+  int v = std::max(qkv_cols(c), c->hidden);
+  if (!c->attn_only) v = std::max(v, 2 * c->ffn);
+  return v;
+}
+
+int attn_row_warps(int R) { return R <= 16 ? 1 : (R <= 32 ? 2 : 4); }
+
+int attn_nsplit(int Hkv, int R, int kend_max, int target) {
+  const int rw = attn_row_warps(R);
+  const int rt = (R + 16 * rw - 1) / (16 * rw);
+  const int nb = (kend_max + kAttnKeys - 1) / kAttnKeys;
+  int ns = (target + Hkv * rt - 1) / (Hkv * rt);
+  ns = std::min(ns, std::max(1, nb / 2));
+  return std::max(1, std::min(ns, kMaxSplits));
+}
+
+struct ScratchLayout {
+  size_t status, prompt, slot_len, match_out, rope, h, a, q, o, z, part, opart, ml, total;
+  size_t part_floats, opart_floats, ml_count;
+};
+
+ScratchLayout scratch_layout(const kvr_config* c) {
+  ScratchLayout L{};
+  const int S = std::max(c->n_slots, 1);
+  const size_t M = c->max_rows, H = c->hidden, QD = (size_t)c->n_q_heads * c->head_dim;
+  const size_t F = c->attn_only ? 0 : c->ffn;
+  size_t off = 0;
+  auto take = [&](size_t bytes) { size_t at = off; off = align_up(off + std::max<size_t>(bytes, 1)); return at; };
+  L.status = take(64);
+  L.prompt = take((size_t)c->capacity * 4);
+  L.slot_len = take(KVR_MAX_SLOTS * 4);
+  L.match_out = take((size_t)(S + 1) * S * 4);
+  L.rope = take(M * (c->head_dim / 2) * 8);
+  L.h = take(M * H * 4);
+  L.a = take(M * H * 2);
+  L.q = take(M * QD * 2);
+  L.o = take(M * QD * 2);
+  L.z = take(M * F * 2);
+  L.part_floats = (size_t)kMaxKSplit * kGemvMaxCols * max_ldo(c);
+  L.part = take(L.part_floats * 4);
+  size_t worst = 0;
+  const int G = c->n_q_heads / c->n_kv_heads;
+  for (int m = 1; m <= c->max_rows; ++m) {
+    const int ns = attn_nsplit(c->n_kv_heads, G * m, c->capacity, kSplitTargetCtas);
+    if (ns > 1) worst = std::max(worst, (size_t)ns * m);
+  }
+  L.opart_floats = worst * c->n_q_heads * c->head_dim;
+  L.ml_count = worst * c->n_q_heads;
+  L.opart = take(L.opart_floats * 4);
+  L.ml = take(L.ml_count * 8);
+  L.total = off;
+  return L;
+}
+
+struct WKey {
+  const void* p;
+  int N, K;
+  bool operator<(const WKey& o) const { return std::tie(p, N, K) < std::tie(o.p, o.N, o.K); }
+};
+struct WMap {
+  CUtensorMap w, s;
+};
+
+struct SlotState {
+  bool occupied = false;
+  std::vector<int32_t> tokens;
+  unsigned long long stamp = 0;
+};
+
+struct EventPair {
+  int cls;
+  cudaEvent_t a, b;
+};
+
+}  // namespace
+
+struct kvr_ctx {
+  kvr_config cfg{};
+  int requested = 0, granted = 0;
+  bool reuse = true;
+  int n_sms = 148;
+  int fault = 0;  // 1 alloc, 2 launch, 3 capacity
+  uint8_t* arena = nullptr;
+  size_t arena_bytes = 0;
+  int32_t* tok_mirror = nullptr;
+  uint8_t* scratch = nullptr;
+  ScratchLayout sl{};
+  // scratch views
+  int* status = nullptr;
+  int32_t* prompt = nullptr;
+  int* slot_len = nullptr;
+  int32_t* match_out = nullptr;
+  float2* rope = nullptr;
+  float* h = nullptr;
+  __nv_bfloat16 *a = nullptr, *q = nullptr, *o = nullptr, *z = nullptr;
+  float* part = nullptr;
+  float* opart = nullptr;
+  float2* ml = nullptr;
+  // TMA descriptors
+  CUtensorMap tm_kv{};
+  CUtensorMap tm_a[3]{}, tm_o[3]{}, tm_z[3]{};
+  std::map<WKey, WMap> wmaps;
+  // slot table
+  SlotState slots[KVR_MAX_SLOTS];
+  unsigned long long clock = 0;
+  std::vector<int32_t> host_match;
+  // profiling
+  bool prof = false;
+  std::vector<EventPair> pending;
+  std::vector<cudaEvent_t> free_events;
+  float prof_ms[4] = {0, 0, 0, 0};
+  int prof_launches[4] = {0, 0, 0, 0};
+  std::string err;
+};
+
+namespace {
+
+int fail(kvr_ctx* c, int code, const char* fmt, ...) {
+  if (c) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    c->err = buf;
+  }
+  return code;
+}
+
+int cuda_fail(kvr_ctx* c, cudaError_t e, const char* what) {
+  return fail(c, KVR_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+cudaEvent_t get_event(kvr_ctx* c) {
+  if (!c->free_events.empty()) {
+    cudaEvent_t e = c->free_events.back();
+    c->free_events.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  cudaEventCreate(&e);
+  return e;
+}
+
+// Brackets one launch with an event pair when profiling is on.
+struct Timed {
+  kvr_ctx* c;
+  int cls;
+  cudaStream_t st;
+  cudaEvent_t a = nullptr;
+  Timed(kvr_ctx* c_, int cls_, cudaStream_t st_) : c(c_), cls(cls_), st(st_) {
+    c->prof_launches[cls]++;
+    if (c->prof) {
+      a = get_event(c);
+      cudaEventRecord(a, st);
+    }
+  }
+  ~Timed() {
+    if (c->prof && a) {
+      cudaEvent_t b = get_event(c);
+      cudaEventRecord(b, st);
+      c->pending.push_back({cls, a, b});
+    }
+  }
+};
+
+bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* ptr, uint64_t inner,
+               uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
+               CUtensorMapSwizzle sw) {
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = g_encode(m, dt, 2, const_cast<void*>(ptr), dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool act_maps(CUtensorMap out[3], const void* buf, int K, int rows) {
+  const int nts[3] = {1, 2, 4};
+  for (int i = 0; i < 3; ++i)
+    if (!encode_2d(&out[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, buf, K, rows, (uint64_t)K * 2, 64,
+                   8 * nts[i], CU_TENSOR_MAP_SWIZZLE_128B))
+      return false;
+  return true;
+}
+
+const WMap* weight_map(kvr_ctx* c, const void* w, const void* s, int N, int K) {
+  WKey key{w, N, K};
+  auto it = c->wmaps.find(key);
+  if (it != c->wmaps.end()) return &it->second;
+  WMap m;
+  if (!encode_2d(&m.w, CU_TENSOR_MAP_DATA_TYPE_UINT8, w, K / 2, N, K / 2, 128, kGemvRows,
+                 CU_TENSOR_MAP_SWIZZLE_128B))
+    return nullptr;
+  if (!encode_2d(&m.s, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, s, K / 32, N, (uint64_t)K / 32 * 2, 8,
+                 kGemvRows, CU_TENSOR_MAP_SWIZZLE_NONE))
+    return nullptr;
+  if (c->wmaps.size() > 4096) c->wmaps.clear();
+  return &(c->wmaps[key] = m);
+}
+
+// ---------------------------------------------------------------------------
+// projections
+// ---------------------------------------------------------------------------
+struct Seg {
+  const void* w;
+  const void* s;
+  int N;
+};
+
+enum class Act { A, O, Z };
+
+template <class Epi>
+int project(kvr_ctx* c, cudaStream_t st, const Seg* segs, int nseg, Act act, int K, int m, Epi epi) {
+  const kvr_config& cfg = c->cfg;
+  GemvParams p;
+  memset(&p, 0, sizeof p);
+  p.nseg = nseg;
+  p.K = K;
+  p.status = c->status;
+  int col = 0, tiles = 0;
+  for (int i = 0; i < nseg; ++i) {
+    GemvSeg& g = p.seg[i];
+    g.N = segs[i].N;
+    g.col0 = col;
+    g.tile0 = tiles;
+    g.tiles = (segs[i].N + kGemvRows - 1) / kGemvRows;
+    col += segs[i].N;
+    tiles += g.tiles;
+    if (cfg.weight_format == KVR_WEIGHTS_INT4_G32) {
+      const WMap* wm = weight_map(c, segs[i].w, segs[i].s, segs[i].N, K);
+      if (!wm) return fail(c, KVR_ERR_CUDA, "cuTensorMapEncodeTiled failed for a weight matrix");
+      g.tw = wm->w;
+      g.ts = wm->s;
+    } else {
+      g.wbf = static_cast<const __nv_bfloat16*>(segs[i].w);
+    }
+  }
+  p.ldo = col;
+  p.part = c->part;
+  const __nv_bfloat16* xbuf = act == Act::A ? c->a : (act == Act::O ? c->o : c->z);
+  const CUtensorMap* tmx = act == Act::A ? c->tm_a : (act == Act::O ? c->tm_o : c->tm_z);
+  p.x = xbuf;
+  p.ksteps = K / kGemvKStep;
+  for (int c0 = 0; c0 < m; c0 += kGemvMaxCols) {
+    const int mb = std::min(kGemvMaxCols, m - c0);
+    p.c0 = c0;
+    p.mb = mb;
+    if (cfg.weight_format == KVR_WEIGHTS_INT4_G32) {
+      const int nt = mb <= 8 ? 1 : (mb <= 16 ? 2 : 4);
+      const int per_sm = nt == 4 ? 1 : 2;
+      int ks = (c->n_sms * per_sm + tiles / 2) / std::max(tiles, 1);
+      ks = std::max(1, std::min(ks, std::min(p.ksteps, kMaxKSplit)));
+      p.ksplit = ks;
+      p.plane = (long long)kGemvMaxCols * p.ldo;
+      p.tx = tmx[nt == 1 ? 0 : (nt == 2 ? 1 : 2)];
+      cudaError_t e;
+      {
+        Timed t(c, kProj, st);
+        e = launch_gemv_int4(p, tiles, nt, st);
+      }
+      if (e != cudaSuccess) return cuda_fail(c, e, "gemv_int4 launch");
+    } else {
+      p.ksplit = 1;
+      p.plane = (long long)kGemvMaxCols * p.ldo;
+      cudaError_t e;
+      {
+        Timed t(c, kProj, st);
+        e = launch_gemv_bf16(p, col, st);
+      }
+      if (e != cudaSuccess) return cuda_fail(c, e, "gemv_bf16 launch");
+    }
+    cudaError_t e;
+    {
+      Timed t(c, kEpi, st);
+      e = epi(p.part, p.plane, p.ksplit, p.ldo, c0, mb);
+    }
+    if (e != cudaSuccess) return cuda_fail(c, e, "epilogue launch");
+  }
+  return KVR_OK;
+}
+
+long long kv_offset(const kvr_ctx* c, int slot, int layer, int kind) {
+  const kvr_config& k = c->cfg;
+  return ((((long long)slot * k.n_layers + layer) * 2 + kind) * k.n_kv_heads) * (long long)k.capacity *
+         k.head_dim;
+}
+
+int kv_row(const kvr_ctx* c, int slot, int layer, int kind) {
+  const kvr_config& k = c->cfg;
+  return (int)((((long long)slot * k.n_layers + layer) * 2 + kind) * k.n_kv_heads * (long long)k.capacity);
+}
+
+int attention(kvr_ctx* c, cudaStream_t st, int slot, int layer, const RowMap& rows) {
+  const kvr_config& k = c->cfg;
+  AttnParams p;
+  memset(&p, 0, sizeof p);
+  p.tkv = c->tm_kv;
+  p.q = c->q;
+  p.o = c->o;
+  p.opart = c->opart;
+  p.ml = c->ml;
+  p.rows = rows;
+  p.Hq = k.n_q_heads;
+  p.Hkv = k.n_kv_heads;
+  p.G = k.n_q_heads / k.n_kv_heads;
+  p.kbase = kv_row(c, slot, layer, 0);
+  p.vbase = kv_row(c, slot, layer, 1);
+  p.cap = k.capacity;
+  p.scale_log2 = 1.4426950408889634f / sqrtf((float)k.head_dim);
+  p.status = c->status;
+  const int R = p.G * rows.m;
+  const int rw = attn_row_warps(R);
+  p.row_tiles = (R + 16 * rw - 1) / (16 * rw);
+  const int kend = rows.P + rows.m;
+  int ns = attn_nsplit(k.n_kv_heads, R, kend, kSplitTargetCtas);
+  while (ns > 1 && (size_t)ns * rows.m * k.n_q_heads * k.head_dim > c->sl.opart_floats) --ns;
+  p.nsplit = ns;
+  cudaError_t e;
+  {
+    Timed t(c, kAttn, st);
+    e = launch_attention(p, k.head_dim, rw, st);
+  }
+  if (e != cudaSuccess) return cuda_fail(c, e, "attention launch");
+  if (ns > 1) {
+    Timed t(c, kAttn, st);
+    e = launch_attn_combine(p, k.head_dim, st);
+    if (e != cudaSuccess) return cuda_fail(c, e, "attention combine launch");
+  }
+  return KVR_OK;
+}
+
+// The layer stack for the rows of one call.
+int run_stack(kvr_ctx* c, int slot, const RowMap& rows, const void* hidden,
+              const kvr_layer_weights* w, void* out, cudaStream_t st) {
+  const kvr_config& k = c->cfg;
+  const int m = rows.m, H = k.hidden, d = k.head_dim;
+  const int Hq = k.n_q_heads, Hkv = k.n_kv_heads, F = k.ffn;
+  const bool i4 = k.weight_format == KVR_WEIGHTS_INT4_G32;
+  cudaError_t e;
+  {
+    Timed t(c, kEpi, st);
+    e = launch_rope_table(rows, d, k.rope_theta, c->rope, st);
+  }
+  if (e != cudaSuccess) return cuda_fail(c, e, "rope table launch");
+  if (k.attn_only) {
+    e = cudaMemcpyAsync(c->a, hidden, (size_t)m * H * 2, cudaMemcpyDeviceToDevice, st);
+    if (e != cudaSuccess) return cuda_fail(c, e, "input copy");
+  } else {
+    Timed t(c, kEpi, st);
+    e = launch_embed(static_cast<const __nv_bfloat16*>(hidden), m, H,
+                     static_cast<const __nv_bfloat16*>(w[0].norm_attn), k.rms_eps, c->h, c->a, st);
+    if (e != cudaSuccess) return cuda_fail(c, e, "embed launch");
+  }
+  __nv_bfloat16* arena = reinterpret_cast<__nv_bfloat16*>(c->arena);
+  for (int l = 0; l < k.n_layers; ++l) {
+    const kvr_layer_weights& W = w[l];
+    const bool last = l == k.n_layers - 1;
+    // Q, K, V (+ RoPE, append)
+    {
+      Seg segs[3] = {{W.wq, W.sq, Hq * d}, {W.wk, W.sk, Hkv * d}, {W.wv, W.sv, Hkv * d}};
+      const long long koff = kv_offset(c, slot, l, 0), voff = kv_offset(c, slot, l, 1);
+      int rc = project(c, st, segs, 3, Act::A, H, m, [&](const float* part, long long plane, int ks,
+                                                          int ldo, int c0, int mb) {
+        return launch_epi_qkv(part, plane, ks, ldo, c0, mb, rows, Hq, Hkv, d, c->rope, c->q, arena,
+                              koff, voff, k.capacity, st);
+      });
+      if (rc) return rc;
+    }
+    int rc = attention(c, st, slot, l, rows);
+    if (rc) return rc;
+    // O projection
+    {
+      Seg so = {W.wo, W.so, H};
+      if (k.attn_only) {
+        __nv_bfloat16* dst = last ? static_cast<__nv_bfloat16*>(out) : c->a;
+        rc = project(c, st, &so, 1, Act::O, Hq * d, m,
+                     [&](const float* part, long long plane, int ks, int ldo, int c0, int mb) {
+                       return launch_epi_cast(part, plane, ks, ldo, c0, mb, H, dst, st);
+                     });
+        if (rc) return rc;
+        continue;
+      }
+      rc = project(c, st, &so, 1, Act::O, Hq * d, m,
+                   [&](const float* part, long long plane, int ks, int ldo, int c0, int mb) {
+                     return launch_epi_resid(part, plane, ks, ldo, c0, mb, H, c->h,
+                                             static_cast<const __nv_bfloat16*>(W.norm_ffn),
+                                             k.rms_eps, c->a, nullptr, st);
+                   });
+      if (rc) return rc;
+    }
+    // gate | up -> SwiGLU
+    {
+      Seg gu[2] = {{W.wg, W.sg, F}, {W.wu, W.su, F}};
+      rc = project(c, st, gu, 2, Act::A, H, m,
+                   [&](const float* part, long long plane, int ks, int ldo, int c0, int mb) {
+                     return launch_epi_swiglu(part, plane, ks, ldo, c0, mb, F, c->z, st);
+                   });
+      if (rc) return rc;
+    }
+    // down + residual, then the next layer's attention norm (or the output)
+    {
+      Seg sd = {W.wd, W.sd, H};
+      const __nv_bfloat16* gain = last ? nullptr : static_cast<const __nv_bfloat16*>(w[l + 1].norm_attn);
+      rc = project(c, st, &sd, 1, Act::Z, F, m,
+                   [&](const float* part, long long plane, int ks, int ldo, int c0, int mb) {
+                     return launch_epi_resid(part, plane, ks, ldo, c0, mb, H, c->h, gain, k.rms_eps,
+                                             last ? nullptr : c->a,
+                                             last ? static_cast<__nv_bfloat16*>(out) : nullptr, st);
+                   });
+      if (rc) return rc;
+    }
+  }
+  (void)i4;
+  return KVR_OK;
+}
+
+bool weights_ok(const kvr_ctx* c, const kvr_layer_weights* w) {
+  if (!w) return false;
+  const bool i4 = c->cfg.weight_format == KVR_WEIGHTS_INT4_G32;
+  for (int l = 0; l < c->cfg.n_layers; ++l) {
+    const kvr_layer_weights& W = w[l];
+    const void* need[] = {W.wq, W.wk, W.wv, W.wo};
+    for (const void* p : need)
+      if (!p || (reinterpret_cast<uintptr_t>(p) & 15)) return false;
+    if (i4) {
+      const void* sc[] = {W.sq, W.sk, W.sv, W.so};
+      for (const void* p : sc)
+        if (!p || (reinterpret_cast<uintptr_t>(p) & 15)) return false;
+    }
+    if (!c->cfg.attn_only) {
+      const void* ff[] = {W.wg, W.wu, W.wd, W.norm_attn, W.norm_ffn};
+      for (const void* p : ff)
+        if (!p || (reinterpret_cast<uintptr_t>(p) & 15)) return false;
+      if (i4) {
+        const void* sf[] = {W.sg, W.su, W.sd};
+        for (const void* p : sf)
+          if (!p || (reinterpret_cast<uintptr_t>(p) & 15)) return false;
+      }
+    }
+  }
+  return true;
+}
+
+void touch(kvr_ctx* c, int s) { c->slots[s].stamp = ++c->clock; }
+
+int upload_tokens(kvr_ctx* c, int slot, int at, const int32_t* toks, int n, cudaStream_t st) {
+  if (n <= 0) return KVR_OK;
+  cudaError_t e = cudaMemcpyAsync(c->tok_mirror + (size_t)slot * c->cfg.capacity + at, toks,
+                                  (size_t)n * 4, cudaMemcpyHostToDevice, st);
+  return e == cudaSuccess ? KVR_OK : cuda_fail(c, e, "token mirror upload");
+}
+
+int prefill_common(kvr_ctx* c, int slot, const int32_t* tokens, int m, const void* hidden,
+                   const kvr_layer_weights* w, void* out, void* stream, int max_m) {
+  if (!c) return KVR_ERR_ARG;
+  if (slot < 0 || slot >= c->granted) return fail(c, KVR_ERR_ARG, "bad slot %d", slot);
+  if (!tokens || !hidden || !out || m <= 0) return fail(c, KVR_ERR_ARG, "null pointer or m <= 0");
+  if (m > max_m) return fail(c, KVR_ERR_ARG, "m = %d exceeds %d for this call", m, max_m);
+  if (((uintptr_t)hidden & 15) || ((uintptr_t)out & 15)) return fail(c, KVR_ERR_ARG, "hidden/out must be 16-byte aligned");
+  if (!weights_ok(c, w)) return fail(c, KVR_ERR_ARG, "missing or misaligned weight pointer");
+  const int p0 = (int)c->slots[slot].tokens.size();
+  if (m > c->cfg.max_rows || p0 + m > c->cfg.capacity || c->fault == 3)
+    return fail(c, KVR_ERR_CAPACITY, "slot %d: %d + %d rows exceed capacity %d (max_rows %d)", slot,
+                p0, m, c->cfg.capacity, c->cfg.max_rows);
+  if (c->fault == 2) return fail(c, KVR_ERR_FAULT, "injected launch fault");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  RowMap rows;
+  memset(&rows, 0, sizeof rows);
+  rows.P = p0;
+  rows.m = m;
+  rows.n_branch = 1;
+  rows.off[0] = 0;
+  rows.off[1] = m;
+  int rc = run_stack(c, slot, rows, hidden, w, out, st);
+  if (rc) return rc;
+  rc = upload_tokens(c, slot, p0, tokens, m, st);
+  if (rc) return rc;
+  SlotState& S = c->slots[slot];
+  S.occupied = true;
+  S.tokens.insert(S.tokens.end(), tokens, tokens + m);
+  touch(c, slot);
+  return KVR_OK;
+}
+
+}  // namespace
+
+// ===========================================================================
+// C ABI
+// ===========================================================================
+extern "C" {
+
+size_t kvr_arena_bytes(const kvr_config* cfg, int n_slots) {
+  if (!valid_config(cfg, nullptr) || n_slots <= 0) return 0;
+  return (size_t)n_slots * (slot_kv_bytes(cfg) + (size_t)cfg->capacity * 4);
+}
+
+size_t kvr_scratch_bytes(const kvr_config* cfg) {
+  if (!valid_config(cfg, nullptr)) return 0;
+  return scratch_layout(cfg).total;
+}
+
+int kvr_ctx_create(const kvr_config* cfg, void* kv_arena, size_t arena_bytes, void* scratch,
+                   size_t scratch_bytes, kvr_ctx** out) {
+  if (!out) return KVR_ERR_ARG;
+  *out = nullptr;
+  std::string why;
+  if (!valid_config(cfg, &why)) return KVR_ERR_ARG;
+  if (!kv_arena || !scratch || ((uintptr_t)kv_arena & 255) || ((uintptr_t)scratch & 255))
+    return KVR_ERR_ARG;
+  kvr_ctx* c = new kvr_ctx();
+  c->cfg = *cfg;
+  const char* f = getenv("KVR_FAULT");
+  if (f) {
+    if (!strcmp(f, "alloc")) c->fault = 1;
+    else if (!strcmp(f, "launch")) c->fault = 2;
+    else if (!strcmp(f, "capacity")) c->fault = 3;
+  }
+  if (c->fault == 1) {
+    delete c;
+    return KVR_ERR_FAULT;
+  }
+  c->requested = cfg->n_slots;
+  c->reuse = cfg->n_slots > 0;
+  const int want = std::max(cfg->n_slots, 1);
+  const size_t per = slot_kv_bytes(cfg) + (size_t)cfg->capacity * 4;
+  c->granted = (int)std::min<size_t>(want, arena_bytes / per);
+  c->sl = scratch_layout(cfg);
+  if (c->granted < 1 || scratch_bytes < c->sl.total) {
+    delete c;
+    return KVR_ERR_CAPACITY;
+  }
+  c->arena = static_cast<uint8_t*>(kv_arena);
+  c->arena_bytes = arena_bytes;
+  c->tok_mirror = reinterpret_cast<int32_t*>(c->arena + (size_t)c->granted * slot_kv_bytes(cfg));
+  c->scratch = static_cast<uint8_t*>(scratch);
+  uint8_t* s = c->scratch;
+  c->status = reinterpret_cast<int*>(s + c->sl.status);
+  c->prompt = reinterpret_cast<int32_t*>(s + c->sl.prompt);
+  c->slot_len = reinterpret_cast<int*>(s + c->sl.slot_len);
+  c->match_out = reinterpret_cast<int32_t*>(s + c->sl.match_out);
+  c->rope = reinterpret_cast<float2*>(s + c->sl.rope);
+  c->h = reinterpret_cast<float*>(s + c->sl.h);
+  c->a = reinterpret_cast<__nv_bfloat16*>(s + c->sl.a);
+  c->q = reinterpret_cast<__nv_bfloat16*>(s + c->sl.q);
+  c->o = reinterpret_cast<__nv_bfloat16*>(s + c->sl.o);
+  c->z = reinterpret_cast<__nv_bfloat16*>(s + c->sl.z);
+  c->part = reinterpret_cast<float*>(s + c->sl.part);
+  c->opart = reinterpret_cast<float*>(s + c->sl.opart);
+  c->ml = reinterpret_cast<float2*>(s + c->sl.ml);
+
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&c->n_sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess) e = gemv_setup();
+  if (e == cudaSuccess) e = attn_setup();
+  if (e == cudaSuccess && !g_encode) {
+    cudaDriverEntryPointQueryResult q;
+    void* fn = nullptr;
+    e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+    if (e == cudaSuccess && q == cudaDriverEntryPointSuccess) g_encode = (PFN_cuTensorMapEncodeTiled_v12000)fn;
+    else if (e == cudaSuccess) e = cudaErrorNotSupported;
+  }
+  if (e != cudaSuccess) {
+    delete c;
+    return KVR_ERR_CUDA;
+  }
+  const kvr_config& k = *cfg;
+  const uint64_t kv_rows = (uint64_t)c->granted * k.n_layers * 2 * k.n_kv_heads * k.capacity;
+  bool ok = encode_2d(&c->tm_kv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, c->arena, k.head_dim, kv_rows,
+                      (uint64_t)k.head_dim * 2, 64, kAttnKeys, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (k.weight_format == KVR_WEIGHTS_INT4_G32) {
+    ok = ok && act_maps(c->tm_a, c->a, k.hidden, k.max_rows);
+    ok = ok && act_maps(c->tm_o, c->o, k.n_q_heads * k.head_dim, k.max_rows);
+    if (!k.attn_only) ok = ok && act_maps(c->tm_z, c->z, k.ffn, k.max_rows);
+  }
+  if (!ok) {
+    delete c;
+    return KVR_ERR_CUDA;
+  }
+  e = cudaMemset(c->status, 0, 64);
+  if (e != cudaSuccess) {
+    delete c;
+    return KVR_ERR_CUDA;
+  }
+  c->host_match.resize((size_t)(c->granted + 1) * c->granted);
+  *out = c;
+  return KVR_OK;
+}
+
+int kvr_ctx_info(const kvr_ctx* c, int* slots_granted, int* slots_requested, int* capacity) {
+  if (!c) return KVR_ERR_ARG;
+  if (slots_granted) *slots_granted = c->granted;
+  if (slots_requested) *slots_requested = c->requested;
+  if (capacity) *capacity = c->cfg.capacity;
+  return KVR_OK;
+}
+
+int kvr_ctx_destroy(kvr_ctx* c) {
+  if (!c) return KVR_ERR_ARG;
+  for (auto& p : c->pending) {
+    cudaEventDestroy(p.a);
+    cudaEventDestroy(p.b);
+  }
+  for (auto e : c->free_events) cudaEventDestroy(e);
+  delete c;
+  return KVR_OK;
+}
+
+int kvr_slot_match(kvr_ctx* c, const int32_t* tokens, int n, int* slot, int* reused, void* stream) {
+  if (!c) return KVR_ERR_ARG;
+  if (!tokens || !slot || !reused || n <= 0) return fail(c, KVR_ERR_ARG, "null pointer or n <= 0");
+  if (n > c->cfg.capacity) return fail(c, KVR_ERR_CAPACITY, "prompt of %d tokens exceeds capacity %d", n, c->cfg.capacity);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int S = c->granted;
+  if (!c->reuse) {
+    c->slots[0].occupied = true;
+    c->slots[0].tokens.clear();
+    touch(c, 0);
+    *slot = 0;
+    *reused = 0;
+    return KVR_OK;
+  }
+  int lens[KVR_MAX_SLOTS];
+  for (int s = 0; s < S; ++s) lens[s] = c->slots[s].occupied ? (int)c->slots[s].tokens.size() : -1;
+  cudaError_t e = cudaMemcpyAsync(c->prompt, tokens, (size_t)n * 4, cudaMemcpyHostToDevice, st);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(c->slot_len, lens, (size_t)S * 4, cudaMemcpyHostToDevice, st);
+  if (e != cudaSuccess) return cuda_fail(c, e, "match upload");
+  {
+    Timed t(c, kMatch, st);
+    e = launch_prefix_match(c->tok_mirror, c->slot_len, S, c->cfg.capacity, c->prompt, n,
+                            c->match_out, st);
+  }
+  if (e != cudaSuccess) return cuda_fail(c, e, "prefix match launch");
+  e = cudaMemcpyAsync(c->host_match.data(), c->match_out, c->host_match.size() * 4,
+                      cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(c, e, "match readback");
+  const int W = S + 1;
+  auto pair = [&](int a, int b) { return a < b ? c->host_match[a * W + b] : c->host_match[b * W + a]; };
+  int l[KVR_MAX_SLOTS];
+  int best = -1;
+  bool any_empty = false;
+  for (int s = 0; s < S; ++s) {
+    l[s] = c->slots[s].occupied ? c->host_match[s * W + S] : 0;
+    if (!c->slots[s].occupied) any_empty = true;
+    if (c->slots[s].occupied && (best < 0 || l[s] > l[best])) best = s;
+  }
+  bool accept = best >= 0 && l[best] > 0;
+  if (accept && c->cfg.match_threshold) {
+    int o = 0;
+    for (int t = 0; t < S; ++t)
+      if (t != best && c->slots[t].occupied) o = std::max(o, pair(best, t));
+    accept = l[best] > o;
+    if (accept && any_empty && l[best] < (int)c->slots[best].tokens.size()) accept = false;
+  }
+  if (accept) {
+    const int r = std::min(l[best], n - 1);
+    c->slots[best].tokens.resize(r);
+    touch(c, best);
+    *slot = best;
+    *reused = r;
+    return KVR_OK;
+  }
+  int pick = -1;
+  for (int s = 0; s < S && pick < 0; ++s)
+    if (!c->slots[s].occupied) pick = s;
+  if (pick < 0) {
+    pick = 0;
+    for (int s = 1; s < S; ++s)
+      if (c->slots[s].stamp < c->slots[pick].stamp) pick = s;
+  }
+  c->slots[pick].occupied = true;
+  c->slots[pick].tokens.clear();
+  touch(c, pick);
+  *slot = pick;
+  *reused = 0;
+  return KVR_OK;
+}
+
+int kvr_slot_truncate(kvr_ctx* c, int slot, int new_len) {
+  if (!c) return KVR_ERR_ARG;
+  if (slot < 0 || slot >= c->granted) return fail(c, KVR_ERR_ARG, "bad slot %d", slot);
+  const int len = (int)c->slots[slot].tokens.size();
+  if (new_len < 0 || new_len > len) return fail(c, KVR_ERR_ARG, "truncate to %d outside [0, %d]", new_len, len);
+  c->slots[slot].tokens.resize(new_len);
+  return KVR_OK;
+}
+
+int kvr_slot_len(const kvr_ctx* c, int slot, int* len) {
+  if (!c || !len || slot < 0 || slot >= c->granted) return KVR_ERR_ARG;
+  *len = (int)c->slots[slot].tokens.size();
+  return KVR_OK;
+}
+
+int kvr_slot_tokens(const kvr_ctx* c, int slot, int32_t* tokens, int n) {
+  if (!c || !tokens || n < 0 || slot < 0 || slot >= c->granted) return KVR_ERR_ARG;
+  const int k = std::min(n, (int)c->slots[slot].tokens.size());
+  if (k > 0) memcpy(tokens, c->slots[slot].tokens.data(), (size_t)k * 4);
+  return KVR_OK;
+}
+
+int kvr_slot_assign(kvr_ctx* c, int slot, const int32_t* tokens, int n, void* stream) {
+  if (!c) return KVR_ERR_ARG;
+  if (slot < 0 || slot >= c->granted) return fail(c, KVR_ERR_ARG, "bad slot %d", slot);
+  if (n < 0 || (n > 0 && !tokens)) return fail(c, KVR_ERR_ARG, "bad token list");
+  if (n > c->cfg.capacity) return fail(c, KVR_ERR_CAPACITY, "%d tokens exceed capacity %d", n, c->cfg.capacity);
+  int rc = upload_tokens(c, slot, 0, tokens, n, static_cast<cudaStream_t>(stream));
+  if (rc) return rc;
+  c->slots[slot].occupied = true;
+  c->slots[slot].tokens.assign(tokens, tokens + n);
+  touch(c, slot);
+  return KVR_OK;
+}
+
+int kvr_slot_kv(const kvr_ctx* c, int slot, int layer, void** k, void** v) {
+  if (!c || slot < 0 || slot >= c->granted || layer < 0 || layer >= c->cfg.n_layers) return KVR_ERR_ARG;
+  __nv_bfloat16* base = reinterpret_cast<__nv_bfloat16*>(c->arena);
+  if (k) *k = base + kv_offset(c, slot, layer, 0);
+  if (v) *v = base + kv_offset(c, slot, layer, 1);
+  return KVR_OK;
+}
+
+int kvr_prefill_suffix(kvr_ctx* c, int slot, const int32_t* tokens, int m, const void* hidden,
+                       const kvr_layer_weights* w, void* out, void* stream) {
+  return prefill_common(c, slot, tokens, m, hidden, w, out, stream, 1 << 30);
+}
+
+int kvr_verify(kvr_ctx* c, int slot, const int32_t* tokens, int m, const void* hidden,
+               const kvr_layer_weights* w, void* out, void* stream) {
+  return prefill_common(c, slot, tokens, m, hidden, w, out, stream, 64);
+}
+
+int kvr_prefill_branches(kvr_ctx* c, int slot, int n_branch, const int* lens, const int32_t* tokens,
+                         const void* hidden, const kvr_layer_weights* w, void* out, void* stream) {
+  if (!c) return KVR_ERR_ARG;
+  if (slot < 0 || slot >= c->granted) return fail(c, KVR_ERR_ARG, "bad slot %d", slot);
+  if (n_branch < 1 || n_branch > KVR_MAX_BRANCHES || !lens || !tokens || !hidden || !out)
+    return fail(c, KVR_ERR_ARG, "bad branch arguments");
+  if (((uintptr_t)hidden & 15) || ((uintptr_t)out & 15)) return fail(c, KVR_ERR_ARG, "hidden/out must be 16-byte aligned");
+  if (!weights_ok(c, w)) return fail(c, KVR_ERR_ARG, "missing or misaligned weight pointer");
+  RowMap rows;
+  memset(&rows, 0, sizeof rows);
+  rows.P = (int)c->slots[slot].tokens.size();
+  rows.n_branch = n_branch;
+  int total = 0;
+  for (int b = 0; b < n_branch; ++b) {
+    if (lens[b] <= 0) return fail(c, KVR_ERR_ARG, "branch %d has %d rows", b, lens[b]);
+    rows.off[b] = total;
+    total += lens[b];
+  }
+  rows.off[n_branch] = total;
+  rows.m = total;
+  if (total > c->cfg.max_rows || rows.P + total > c->cfg.capacity || c->fault == 3)
+    return fail(c, KVR_ERR_CAPACITY, "%d branch rows after %d exceed capacity %d (max_rows %d)", total,
+                rows.P, c->cfg.capacity, c->cfg.max_rows);
+  if (c->fault == 2) return fail(c, KVR_ERR_FAULT, "injected launch fault");
+  int rc = run_stack(c, slot, rows, hidden, w, out, static_cast<cudaStream_t>(stream));
+  if (rc) return rc;
+  c->slots[slot].occupied = true;
+  touch(c, slot);
+  return KVR_OK;
+}
+
+int kvr_sync_status(kvr_ctx* c, void* stream) {
+  if (!c) return KVR_ERR_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int word = 0;
+  cudaError_t e = cudaMemcpyAsync(&word, c->status, 4, cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(c, e, "status readback");
+  if (word) {
+    cudaMemsetAsync(c->status, 0, 4, st);
+    cudaStreamSynchronize(st);
+    return fail(c, KVR_ERR_TIMEOUT, "a device-side wait gave up (status %d)", word);
+  }
+  return KVR_OK;
+}
+
+int kvr_profile_enable(kvr_ctx* c, int on) {
+  if (!c) return KVR_ERR_ARG;
+  c->prof = on != 0;
+  return KVR_OK;
+}
+
+int kvr_profile_read(kvr_ctx* c, float ms[4], int launches[4]) {
+  if (!c) return KVR_ERR_ARG;
+  for (auto& p : c->pending) {
+    cudaError_t e = cudaEventSynchronize(p.b);
+    float t = 0.f;
+    if (e == cudaSuccess) e = cudaEventElapsedTime(&t, p.a, p.b);
+    if (e == cudaSuccess) c->prof_ms[p.cls] += t;
+    c->free_events.push_back(p.a);
+    c->free_events.push_back(p.b);
+  }
+  c->pending.clear();
+  for (int i = 0; i < 4; ++i) {
+    if (ms) ms[i] = c->prof_ms[i];
+    if (launches) launches[i] = c->prof_launches[i];
+    c->prof_ms[i] = 0.f;
+    c->prof_launches[i] = 0;
+  }
+  return KVR_OK;
+}
+
+const char* kvr_last_error(const kvr_ctx* c) { return c ? c->err.c_str() : "null context"; }
+
+}  // extern "C"

@@ -1,0 +1,268 @@
+// Internal declarations shared by the kvr kernels and the C-ABI host code.
+// sm_103a only: TMA (cp.async.bulk.tensor), mbarrier transaction counts,
+// ldmatrix and bf16 tensor-core fragments are used directly through inline PTX.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/kvr.h"
+
+namespace kvr {
+
+// ----------------------------------------------------------------------------
+// constants
+// ----------------------------------------------------------------------------
+constexpr int kGemvRows = 128;     // weight rows per GEMV CTA (8 warps x 16 rows)
+constexpr int kGemvKStep = 256;    // inputs per pipeline stage (8 groups of 32)
+constexpr int kGemvMaxCols = 32;   // tokens per GEMV pass (4 tensor-core n-tiles)
+constexpr int kMaxKSplit = 16;
+constexpr int kAttnKeys = 64;      // keys per attention pipeline stage
+constexpr int kSplitTargetCtas = 320;
+constexpr int kMaxSplits = 64;
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s per bounded wait
+
+constexpr int kStatusTimeout = 1;
+
+// Rows of one call: P committed keys visible to every row; row i of branch b
+// (off[b] <= i < off[b+1]) sits at position P + i - off[b], is stored at slot
+// index P + i, and also sees slot indices [P + off[b], P + i].
+struct RowMap {
+  int P;
+  int m;
+  int n_branch;
+  int off[KVR_MAX_BRANCHES + 1];
+};
+
+__host__ __device__ inline int row_branch(const RowMap& r, int i) {
+  int b = 0;
+  while (b + 1 < r.n_branch && i >= r.off[b + 1]) ++b;
+  return b;
+}
+
+// ----------------------------------------------------------------------------
+// kernel parameter blocks
+// ----------------------------------------------------------------------------
+struct GemvSeg {
+  CUtensorMap tw;   // int4: uint8 [N][K/2], box {128 B, 128 rows}, 128B swizzle
+  CUtensorMap ts;   // int4: fp16 scales [N][K/32], box {8, 128 rows}
+  const __nv_bfloat16* wbf;  // bf16 weights [N][K] (bf16 format only)
+  int N;
+  int col0;         // first output column of this segment
+  int tile0;        // first CTA tile of this segment
+  int tiles;
+};
+
+struct GemvParams {
+  GemvSeg seg[3];
+  CUtensorMap tx;   // activations bf16 [max_rows][K], box {64, 8*NT}, 128B swizzle
+  const __nv_bfloat16* x;  // same activations, plain pointer (bf16 kernel)
+  int nseg;
+  int K;
+  int ksteps;
+  int ksplit;
+  int c0;           // first token of this pass
+  int mb;           // tokens in this pass (<= kGemvMaxCols)
+  int ldo;          // partial row stride (total output columns)
+  long long plane;  // floats per split plane of the partials
+  float* part;      // [ksplit][kGemvMaxCols][ldo]
+  int* status;
+};
+
+struct AttnParams {
+  CUtensorMap tkv;           // arena as bf16 [rows][head_dim], box {64, 64}, 128B swizzle
+  const __nv_bfloat16* q;    // [m][Hq][d] after RoPE
+  __nv_bfloat16* o;          // [m][Hq*d] (nsplit == 1)
+  float* opart;              // [nsplit][m][Hq][d]
+  float2* ml;                // [nsplit][m][Hq]  (running max in log2 units, sum)
+  RowMap rows;
+  int Hq, Hkv, G;
+  int kbase;                 // arena row of (slot, layer, K, head 0, position 0)
+  int vbase;                 // arena row of (slot, layer, V, head 0, position 0)
+  int cap;
+  int nsplit;
+  int row_tiles;
+  float scale_log2;          // log2(e) / sqrt(d)
+  int* status;
+};
+
+// ----------------------------------------------------------------------------
+// launchers (each returns cudaGetLastError() of its launch)
+// ----------------------------------------------------------------------------
+cudaError_t launch_prefix_match(const int32_t* slot_tokens, const int* slot_len, int n_slots,
+                                int cap, const int32_t* prompt, int n, int32_t* out,
+                                cudaStream_t st);
+cudaError_t launch_gemv_int4(const GemvParams& p, int total_tiles, int nt, cudaStream_t st);
+cudaError_t launch_gemv_bf16(const GemvParams& p, int total_cols, cudaStream_t st);
+cudaError_t launch_attention(const AttnParams& p, int d, int row_warps, cudaStream_t st);
+cudaError_t launch_attn_combine(const AttnParams& p, int d, cudaStream_t st);
+cudaError_t launch_rope_table(const RowMap& rows, int d, float theta, float2* table,
+                              cudaStream_t st);
+cudaError_t launch_embed(const __nv_bfloat16* hidden, int m, int H, const __nv_bfloat16* gain,
+                         float eps, float* h, __nv_bfloat16* a, cudaStream_t st);
+cudaError_t launch_epi_qkv(const float* part, long long plane, int ksplit, int ldo, int c0,
+                           int mb, const RowMap& rows, int Hq, int Hkv, int d,
+                           const float2* rope, __nv_bfloat16* q, __nv_bfloat16* arena,
+                           long long k_off, long long v_off, int cap, cudaStream_t st);
+cudaError_t launch_epi_resid(const float* part, long long plane, int ksplit, int ldo, int c0,
+                             int mb, int H, float* h, const __nv_bfloat16* gain, float eps,
+                             __nv_bfloat16* a_out, __nv_bfloat16* final_out, cudaStream_t st);
+cudaError_t launch_epi_swiglu(const float* part, long long plane, int ksplit, int ldo, int c0,
+                              int mb, int F, __nv_bfloat16* z, cudaStream_t st);
+cudaError_t launch_epi_cast(const float* part, long long plane, int ksplit, int ldo, int c0,
+                            int mb, int N, __nv_bfloat16* out, cudaStream_t st);
+
+// dynamic shared memory the launchers need (for cudaFuncSetAttribute at setup)
+int gemv_int4_smem(int nt);
+int attn_smem(int d);
+cudaError_t gemv_setup();
+cudaError_t attn_setup();
+
+}  // namespace kvr
+
+// ----------------------------------------------------------------------------
+// device helpers (inline PTX)
+// ----------------------------------------------------------------------------
+#ifdef __CUDACC__
+namespace kvr {
+namespace dev {
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ unsigned long long globaltimer_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for the phase of `parity` to complete; give up after kWaitLimitNs,
+// record the timeout in the device status word and return false.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      if (status) atomicExch(status, kStatusTimeout);
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap* m) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
+}
+
+// 2-D tiled TMA load global -> shared, completion counted on an mbarrier.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* m, int x, int y,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+// Same with an L2 eviction-priority hint (weights are streamed once).
+__device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap* m, int x, int y,
+                                                 uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(bar), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& r0, uint32_t& r1,
+                                            uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t addr, uint32_t& r0, uint32_t& r1,
+                                                  uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+// D = A(16x16 bf16, row) * B(16x8 bf16, col) + C, fp32 accumulate.
+__device__ __forceinline__ void mma_bf16_16816(float d[4], const uint32_t a[4], uint32_t b0,
+                                               uint32_t b1, const float c[4]) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
+      "{%4, %5, %6, %7}, {%8, %9}, {%10, %11, %12, %13};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]),
+        "f"(c[2]), "f"(c[3]));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// 128-byte TMA swizzle: 16-byte chunk j of a 128-byte row r lands at j ^ (r % 8)
+// (tile base 1024-byte aligned).
+__device__ __forceinline__ uint32_t swz128(uint32_t row, uint32_t chunk) {
+  return row * 128u + ((chunk ^ (row & 7u)) << 4);
+}
+
+}  // namespace dev
+}  // namespace kvr
+#endif

@@ -1,0 +1,82 @@
+"""The C-ABI library builds, loads and exports every symbol include/kvr.h
+declares; host-only calls behave (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+import workloads
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__
+    __graft_entry__.build()
+    from prefix_reused_prefill_gb300 import kvr
+    return kvr.load_library()
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "kvr.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(kvr_[a-z_]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 17
+    for n in names:
+        assert hasattr(lib, n), n
+    from prefix_reused_prefill_gb300 import kvr
+    assert sorted(kvr.EXPORTED) == names
+
+
+def test_sizes_match_documented_layout(lib):
+    from prefix_reused_prefill_gb300 import kvr
+    shape = workloads.SHAPES["qwen7b"]
+    cfg = kvr.config_for_shape(shape, 4, 16384, 256)
+    per_slot = shape.n_layers * 2 * shape.n_kv_heads * 16384 * shape.head_dim * 2 + 16384 * 4
+    assert lib.kvr_arena_bytes(ctypes.byref(cfg), 4) == 4 * per_slot
+    assert lib.kvr_arena_bytes(ctypes.byref(cfg), 1) == per_slot
+    assert lib.kvr_scratch_bytes(ctypes.byref(cfg)) > 0
+
+
+@pytest.mark.parametrize("field,value", [("capacity", 100), ("head_dim", 96), ("n_kv_heads", 3),
+                                         ("n_slots", 17), ("max_rows", 0), ("weight_format", 7)])
+def test_invalid_configs_are_refused(lib, field, value):
+    from prefix_reused_prefill_gb300 import kvr
+    cfg = kvr.config_for_shape(workloads.SHAPES["qwen7b"], 4, 16384, 256)
+    setattr(cfg, field, value)
+    assert lib.kvr_arena_bytes(ctypes.byref(cfg), 1) == 0
+    assert lib.kvr_scratch_bytes(ctypes.byref(cfg)) == 0
+    out = ctypes.c_void_p()
+    assert lib.kvr_ctx_create(ctypes.byref(cfg), None, 0, None, 0, ctypes.byref(out)) == -1
+
+
+def test_int4_width_rule(lib):
+    from prefix_reused_prefill_gb300 import kvr
+    cfg = kvr.config_for_shape(workloads.SHAPES["small"], 2, 256, 32)
+    assert lib.kvr_scratch_bytes(ctypes.byref(cfg)) > 0
+    cfg.hidden = 640  # not a multiple of 256
+    assert lib.kvr_scratch_bytes(ctypes.byref(cfg)) == 0
+
+
+def test_null_context_calls_return_arg_errors(lib):
+    n = ctypes.c_int()
+    assert lib.kvr_slot_len(None, 0, ctypes.byref(n)) == -1
+    assert lib.kvr_slot_truncate(None, 0, 0) == -1
+    assert lib.kvr_ctx_destroy(None) == -1
+    assert lib.kvr_last_error(None) == b"null context"
+
+
+def test_binding_fails_loudly_without_library(tmp_path):
+    from prefix_reused_prefill_gb300 import kvr
+    saved = kvr._lib
+    try:
+        kvr._lib = None
+        with pytest.raises(ImportError):
+            kvr.load_library(str(tmp_path / "missing.so"))
+    finally:
+        kvr._lib = saved
