@@ -27,8 +27,9 @@
  * ---------------------------------------------------------------------------
  * Ownership.  The caller allocates every device buffer (the KV arena, the
  * scratch area, weights, inputs, outputs) and owns the CUDA stream.  The
- * library allocates no device memory; it owns only host state (the slot token
- * lists, lengths, LRU stamps, cached TMA descriptors).  All calls that take a
+ * library makes no device allocation; it owns host state (the slot token
+ * lists, lengths, LRU stamps, cached TMA descriptors) and, on each GPU that
+ * loads it, the fixed staging array of kvr_slot_match_static.  All calls that take a
  * stream are asynchronous on it, except kvr_slot_match, which waits for the
  * stream to read back the match lengths, and kvr_sync_status.
  *
@@ -178,6 +179,39 @@ int kvr_ctx_destroy(kvr_ctx* ctx);
  */
 int kvr_slot_match(kvr_ctx* ctx, const int32_t* tokens, int n, int* slot, int* reused,
                    void* stream);
+/*
+ * kvr_slot_match_static -- kvr_slot_match for callers that cannot allocate
+ * device memory for it.  (The pages have no counterpart: this is a property
+ * of the library, not of the method.)
+ *
+ * kvr_slot_match stages the prompt and its match lengths in the scratch area
+ * handed to kvr_ctx_create.  Some callers have no device memory to hand over
+ * when they match: a request router or scheduler thread whose process leaves
+ * every device byte to another component's caching allocator (calling
+ * cudaMalloc behind that allocator's back breaks its accounting and can fail
+ * when it holds the whole device), or code that must not allocate while
+ * another stream is being captured into a CUDA graph.  This call computes the
+ * same (slot, reused) with the same policy, but stages everything in a fixed
+ * array inside the library: KVR_STATIC_MATCH_MAX_TOKENS prompt tokens plus
+ * the slot and match lengths (about 66 KB), held by every GPU that loads the
+ * library until the process exits.  It calls no cudaMalloc/cudaFree.
+ *
+ * Limits and rules:
+ *  - n > KVR_STATIC_MATCH_MAX_TOKENS (or > capacity) fails with
+ *    KVR_ERR_CAPACITY and a message saying so; nothing is launched.
+ *  - The first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress) with that device current; make that first call
+ *    before any stream capture on the device.
+ *  - Every call, from every context on the device, shares the one array and
+ *    leaves its contents behind.  Each call writes every word it reads
+ *    before reading it, so nothing needs clearing; but calls that overlap on
+ *    the GPU (different streams or threads without ordering) race on the
+ *    array and may return wrong results.  Serialise them.
+ */
+#define KVR_STATIC_MATCH_MAX_TOKENS 16384
+int kvr_slot_match_static(kvr_ctx* ctx, const int32_t* tokens, int n, int* slot, int* reused,
+                          void* stream);
+
 /* Cut a slot back to new_len <= len (a host length update; K/V beyond it are
  * simply ignored from then on).  Used after a verify to keep p0+1+accepted. */
 int kvr_slot_truncate(kvr_ctx* ctx, int slot, int new_len);

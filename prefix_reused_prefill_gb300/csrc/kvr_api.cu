@@ -870,4 +870,85 @@ int kvr_profile_read(kvr_ctx* c, float ms[4], int launches[4]) {
 
 const char* kvr_last_error(const kvr_ctx* c) { return c ? c->err.c_str() : "null context"; }
 
+// kvr_slot_match with its device staging in the library's static array
+// (k_match_static.cu) instead of the context's scratch area; the policy applied
+// to the match lengths is the one of kvr_slot_match.
+int kvr_slot_match_static(kvr_ctx* c, const int32_t* tokens, int n, int* slot, int* reused,
+                          void* stream) {
+  if (!c) return KVR_ERR_ARG;
+  if (!tokens || !slot || !reused || n <= 0) return fail(c, KVR_ERR_ARG, "null pointer or n <= 0");
+  if (n > KVR_STATIC_MATCH_MAX_TOKENS)
+    return fail(c, KVR_ERR_CAPACITY, "prompt of %d tokens exceeds the static match limit of %d tokens",
+                n, KVR_STATIC_MATCH_MAX_TOKENS);
+  if (n > c->cfg.capacity) return fail(c, KVR_ERR_CAPACITY, "prompt of %d tokens exceeds capacity %d", n, c->cfg.capacity);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int S = c->granted;
+  if (!c->reuse) {
+    c->slots[0].occupied = true;
+    c->slots[0].tokens.clear();
+    touch(c, 0);
+    *slot = 0;
+    *reused = 0;
+    return KVR_OK;
+  }
+  int32_t *d_prompt = nullptr, *d_out = nullptr;
+  int* d_len = nullptr;
+  cudaError_t e = static_match_scratch(&d_prompt, &d_len, &d_out);
+  if (e != cudaSuccess) return cuda_fail(c, e, "static match scratch lookup");
+  int lens[KVR_MAX_SLOTS];
+  for (int s = 0; s < S; ++s) lens[s] = c->slots[s].occupied ? (int)c->slots[s].tokens.size() : -1;
+  e = cudaMemcpyAsync(d_prompt, tokens, (size_t)n * 4, cudaMemcpyHostToDevice, st);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(d_len, lens, (size_t)S * 4, cudaMemcpyHostToDevice, st);
+  if (e != cudaSuccess) return cuda_fail(c, e, "static match upload");
+  {
+    Timed t(c, kMatch, st);
+    e = launch_prefix_match(c->tok_mirror, d_len, S, c->cfg.capacity, d_prompt, n, d_out, st);
+  }
+  if (e != cudaSuccess) return cuda_fail(c, e, "prefix match launch");
+  std::vector<int32_t> res((size_t)(S + 1) * S);
+  e = cudaMemcpyAsync(res.data(), d_out, res.size() * 4, cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(c, e, "static match readback");
+  const int W = S + 1;
+  auto pair = [&](int a, int b) { return a < b ? res[a * W + b] : res[b * W + a]; };
+  int l[KVR_MAX_SLOTS];
+  int best = -1;
+  bool any_empty = false;
+  for (int s = 0; s < S; ++s) {
+    l[s] = c->slots[s].occupied ? res[s * W + S] : 0;
+    if (!c->slots[s].occupied) any_empty = true;
+    if (c->slots[s].occupied && (best < 0 || l[s] > l[best])) best = s;
+  }
+  bool accept = best >= 0 && l[best] > 0;
+  if (accept && c->cfg.match_threshold) {
+    int o = 0;
+    for (int t = 0; t < S; ++t)
+      if (t != best && c->slots[t].occupied) o = std::max(o, pair(best, t));
+    accept = l[best] > o;
+    if (accept && any_empty && l[best] < (int)c->slots[best].tokens.size()) accept = false;
+  }
+  if (accept) {
+    const int r = std::min(l[best], n - 1);
+    c->slots[best].tokens.resize(r);
+    touch(c, best);
+    *slot = best;
+    *reused = r;
+    return KVR_OK;
+  }
+  int pick = -1;
+  for (int s = 0; s < S && pick < 0; ++s)
+    if (!c->slots[s].occupied) pick = s;
+  if (pick < 0) {
+    pick = 0;
+    for (int s = 1; s < S; ++s)
+      if (c->slots[s].stamp < c->slots[pick].stamp) pick = s;
+  }
+  c->slots[pick].occupied = true;
+  c->slots[pick].tokens.clear();
+  touch(c, pick);
+  *slot = pick;
+  *reused = 0;
+  return KVR_OK;
+}
+
 }  // extern "C"

@@ -120,6 +120,7 @@ int gemv_int4_smem(int nt);
 int attn_smem(int d);
 cudaError_t gemv_setup();
 cudaError_t attn_setup();
+cudaError_t static_match_scratch(int32_t** prompt, int** slot_len, int32_t** match_out);
 
 }  // namespace kvr
 

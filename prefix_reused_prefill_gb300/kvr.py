@@ -25,7 +25,7 @@ EXPORTED = ["kvr_arena_bytes", "kvr_scratch_bytes", "kvr_ctx_create", "kvr_ctx_i
             "kvr_ctx_destroy", "kvr_slot_match", "kvr_slot_truncate", "kvr_slot_len",
             "kvr_slot_tokens", "kvr_slot_assign", "kvr_slot_kv", "kvr_prefill_suffix", "kvr_verify",
             "kvr_prefill_branches", "kvr_sync_status", "kvr_profile_enable", "kvr_profile_read",
-            "kvr_last_error"]
+            "kvr_last_error", "kvr_slot_match_static"]
 
 
 class KvrError(RuntimeError):
@@ -82,6 +82,7 @@ def load_library(path: str = LIB_PATH):
         "kvr_profile_enable": (I, [V, I]),
         "kvr_profile_read": (I, [V, P(ctypes.c_float), P(I)]),
         "kvr_last_error": (ctypes.c_char_p, [V]),
+        "kvr_slot_match_static": (I, [V, i32p, I, P(I), P(I), V]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -188,6 +189,14 @@ class Kvr:
         s, r = ctypes.c_int(), ctypes.c_int()
         self._check(self.lib.kvr_slot_match(self.ctx, _i32(tokens), len(tokens), ctypes.byref(s),
                                             ctypes.byref(r), self._stream(stream)))
+        return s.value, r.value
+
+    def kvr_slot_match_static(self, tokens, stream=None) -> Tuple[int, int]:
+        """kvr_slot_match staged in the library's fixed device array (no caller scratch)."""
+        s, r = ctypes.c_int(), ctypes.c_int()
+        self._check(self.lib.kvr_slot_match_static(self.ctx, _i32(tokens), len(tokens),
+                                                   ctypes.byref(s), ctypes.byref(r),
+                                                   self._stream(stream)))
         return s.value, r.value
 
     def kvr_slot_truncate(self, slot: int, new_len: int):
