@@ -131,9 +131,12 @@ class ClockSampler:
 # the GPU arm
 # ---------------------------------------------------------------------------
 
-def build_turn9(device, steps_total):
+def build_turn9(device, steps_total, layers=None):
+    import dataclasses
     from prefix_reused_prefill_gb300 import Kvr, config_for_shape
     shape = workloads.SHAPES["qwen7b"]
+    if layers:
+        shape = dataclasses.replace(shape, n_layers=layers)
     seed = workloads.config_seed(2)
     tk = workloads.turn9_tokens(seed)
     t0 = time.time()
@@ -165,8 +168,8 @@ def run_gpu(args, rank, world):
     device = torch.device("cuda", torch.cuda.current_device())
     pk, pk_kind = peaks()
     total = args.warmup + args.steps
-    shape, kv, w, prompts, xs_host, setup_s = build_turn9(device, 2 * total + 2)
-    xs_dev = [x.to(device) for x in xs_host[:total]]
+    shape, kv, w, prompts, xs_host, setup_s = build_turn9(device, 3 * total + 2, args.layers)
+    xs_dev = [x.to(device) for x in xs_host[:2 * total]]
     out = torch.empty((M_ROWS, shape.hidden), dtype=torch.bfloat16, device=device)
     stream = torch.cuda.current_stream()
 
@@ -201,19 +204,19 @@ def run_gpu(args, rank, world):
 
     # ---------------- the same steps with per-kernel-class events (roofline)
     kv.kvr_profile_enable(True)
-    for i in range(args.warmup, total):
+    for i in range(total + args.warmup, 2 * total):
         step(i)
     torch.cuda.synchronize()
     cls_ms, cls_n = kv.kvr_profile_read()
     kv.kvr_profile_enable(False)
 
     # ---------------- end to end through the public API with host buffers
-    pinned_in = [x.pin_memory() for x in xs_host[total:2 * total]]
+    pinned_in = [x.pin_memory() for x in xs_host[2 * total:3 * total]]
     pinned_out = torch.empty((M_ROWS, shape.hidden), dtype=torch.bfloat16).pin_memory()
     dev_in = torch.empty((M_ROWS, shape.hidden), dtype=torch.bfloat16, device=device)
 
     def e2e_step(j):
-        p = prompts[total + j]
+        p = prompts[2 * total + j]
         slot, reused = kv.kvr_slot_match(p)
         dev_in.copy_(pinned_in[j], non_blocking=True)
         kv.kvr_prefill_suffix(slot, p[reused:], dev_in, w, out=out)
@@ -280,6 +283,8 @@ def run_gpu(args, rank, world):
         "clocks": clk,
         "setup_s": round(setup_s, 1),
     }
+    if args.layers:
+        line["config"]["workload"] += f" (REDUCED to {args.layers} layers: profiling case, not the bench line)"
     if rank == 0 and not args.no_cpu:
         line["cpu_baseline"] = cpu_baseline(args.cpu_rows)
     return line, rank
@@ -355,6 +360,8 @@ def main():
     ap.add_argument("--impl", default="kvr", choices=["kvr", "reference"])
     ap.add_argument("--cpu-rows", type=int, default=64)
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="profiling aid: run a reduced stack of this many layers")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3) if args.impl == "kvr" else max(args.warmup, 0)
     rank, world = dist_setup(args.gpus)

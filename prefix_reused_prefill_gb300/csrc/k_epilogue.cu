@@ -100,23 +100,56 @@ __global__ void epi_qkv_kernel(const float* part, long long plane, int ksplit, i
   }
 }
 
-__global__ void epi_resid_kernel(const float* part, long long plane, int ksplit, int ldo, int c0,
-                                 int H, float* h, const __nv_bfloat16* gain, float eps,
-                                 __nv_bfloat16* a_out, __nv_bfloat16* final_out) {
+// One CTA per token row: h += sum of the split partials (fixed split order),
+// then RMSNorm of the new row for the next projection, or the bf16 output.
+// float4 accesses; the row stays in registers between the two passes.
+template <int V>  // float4 per thread (H <= 4 * 256 * V)
+__global__ void __launch_bounds__(256) epi_resid_kernel(const float* part, long long plane, int ksplit,
+                                                        int ldo, int c0, int H, float* h,
+                                                        const __nv_bfloat16* gain, float eps,
+                                                        __nv_bfloat16* a_out, __nv_bfloat16* final_out) {
   __shared__ float red[32];
   const int t = blockIdx.x;
   const long long i = c0 + t;
+  const int H4 = H >> 2;
+  float4 v[V];
   float ss = 0.f;
-  for (int k = threadIdx.x; k < H; k += blockDim.x) {
-    const float v = h[i * H + k] + split_sum(part, plane, ksplit, (long long)t * ldo + k);
-    h[i * H + k] = v;
-    ss += v * v;
-    if (final_out) final_out[i * H + k] = __float2bfloat16_rn(v);
+#pragma unroll
+  for (int u = 0; u < V; ++u) {
+    const int k4 = threadIdx.x + u * 256;
+    if (k4 < H4) {
+      float4 acc = reinterpret_cast<const float4*>(h + i * H)[k4];
+      const float4* pp = reinterpret_cast<const float4*>(part + (long long)t * ldo) + k4;
+      for (int s = 0; s < ksplit; ++s) {
+        const float4 q = pp[s * (plane >> 2)];
+        acc.x += q.x; acc.y += q.y; acc.z += q.z; acc.w += q.w;
+      }
+      reinterpret_cast<float4*>(h + i * H)[k4] = acc;
+      ss += acc.x * acc.x + acc.y * acc.y + acc.z * acc.z + acc.w * acc.w;
+      v[u] = acc;
+      if (final_out) {
+        uint2 o;
+        o.x = dev::pack_bf16x2(acc.x, acc.y);
+        o.y = dev::pack_bf16x2(acc.z, acc.w);
+        reinterpret_cast<uint2*>(final_out + i * H)[k4] = o;
+      }
+    }
   }
   if (a_out) {
     const float rs = rsqrtf(block_sum(ss, red) / H + eps);
-    for (int k = threadIdx.x; k < H; k += blockDim.x)
-      a_out[i * H + k] = __float2bfloat16_rn(h[i * H + k] * rs * __bfloat162float(gain[k]));
+#pragma unroll
+    for (int u = 0; u < V; ++u) {
+      const int k4 = threadIdx.x + u * 256;
+      if (k4 < H4) {
+        const uint2 gw = reinterpret_cast<const uint2*>(gain)[k4];
+        const __nv_bfloat162 g01 = *reinterpret_cast<const __nv_bfloat162*>(&gw.x);
+        const __nv_bfloat162 g23 = *reinterpret_cast<const __nv_bfloat162*>(&gw.y);
+        uint2 o;
+        o.x = dev::pack_bf16x2(v[u].x * rs * __bfloat162float(g01.x), v[u].y * rs * __bfloat162float(g01.y));
+        o.y = dev::pack_bf16x2(v[u].z * rs * __bfloat162float(g23.x), v[u].w * rs * __bfloat162float(g23.y));
+        reinterpret_cast<uint2*>(a_out + i * H)[k4] = o;
+      }
+    }
   }
 }
 
@@ -169,8 +202,15 @@ cudaError_t launch_epi_qkv(const float* part, long long plane, int ksplit, int l
 cudaError_t launch_epi_resid(const float* part, long long plane, int ksplit, int ldo, int c0,
                              int mb, int H, float* h, const __nv_bfloat16* gain, float eps,
                              __nv_bfloat16* a_out, __nv_bfloat16* final_out, cudaStream_t st) {
-  epi_resid_kernel<<<mb, 256, 0, st>>>(part, plane, ksplit, ldo, c0, H, h, gain, eps, a_out,
-                                       final_out);
+  const int v = (H / 4 + 255) / 256;
+  if (v <= 2)
+    epi_resid_kernel<2><<<mb, 256, 0, st>>>(part, plane, ksplit, ldo, c0, H, h, gain, eps, a_out, final_out);
+  else if (v <= 4)
+    epi_resid_kernel<4><<<mb, 256, 0, st>>>(part, plane, ksplit, ldo, c0, H, h, gain, eps, a_out, final_out);
+  else if (v <= 8)
+    epi_resid_kernel<8><<<mb, 256, 0, st>>>(part, plane, ksplit, ldo, c0, H, h, gain, eps, a_out, final_out);
+  else
+    return cudaErrorInvalidValue;
   return cudaGetLastError();
 }
 

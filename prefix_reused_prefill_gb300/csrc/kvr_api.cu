@@ -40,7 +40,7 @@ bool valid_config(const kvr_config* c, std::string* why) {
     return bad("layer shape must be positive");
   if (c->head_dim != 64 && c->head_dim != 128) return bad("head_dim must be 64 or 128");
   if (c->n_q_heads % c->n_kv_heads) return bad("n_q_heads must be a multiple of n_kv_heads");
-  if (c->hidden % 8) return bad("hidden must be a multiple of 8");
+  if (c->hidden % 8 || c->hidden > 8192) return bad("hidden must be a multiple of 8, at most 8192");
   if (!c->attn_only && (c->ffn <= 0 || c->ffn % 8)) return bad("ffn must be a positive multiple of 8");
   if (c->weight_format != KVR_WEIGHTS_BF16 && c->weight_format != KVR_WEIGHTS_INT4_G32)
     return bad("weight_format must be 0 (bf16) or 1 (int4 g32)");
@@ -100,6 +100,9 @@ ScratchLayout scratch_layout(const kvr_config* c) {
   L.o = take(M * QD * 2);
   L.z = take(M * F * 2);
   L.part_floats = (size_t)kMaxKSplit * kGemvMaxCols * max_ldo(c);
+  if (c->weight_format == KVR_WEIGHTS_INT4_G32)
+    L.part_floats = std::max(L.part_floats, (size_t)kGemmMaxSplit * kGemmMaxTok *
+                                                std::max(qkv_cols(c), c->hidden));
   L.part = take(L.part_floats * 4);
   size_t worst = 0;
   const int G = c->n_q_heads / c->n_kv_heads;
@@ -117,8 +120,8 @@ ScratchLayout scratch_layout(const kvr_config* c) {
 
 struct WKey {
   const void* p;
-  int N, K;
-  bool operator<(const WKey& o) const { return std::tie(p, N, K) < std::tie(o.p, o.N, o.K); }
+  int N, K, box;
+  bool operator<(const WKey& o) const { return std::tie(p, N, K, box) < std::tie(o.p, o.N, o.K, o.box); }
 };
 struct WMap {
   CUtensorMap w, s;
@@ -161,7 +164,7 @@ struct kvr_ctx {
   float2* ml = nullptr;
   // TMA descriptors
   CUtensorMap tm_kv{};
-  CUtensorMap tm_a[3]{}, tm_o[3]{}, tm_z[3]{};
+  CUtensorMap tm_a[6]{}, tm_o[6]{}, tm_z[6]{};
   std::map<WKey, WMap> wmaps;
   // slot table
   SlotState slots[KVR_MAX_SLOTS];
@@ -169,6 +172,7 @@ struct kvr_ctx {
   std::vector<int32_t> host_match;
   // profiling
   bool prof = false;
+  bool force_gemv = false;  // KVR_FORCE_GEMV=1: keep every m on the GEMV path
   std::vector<EventPair> pending;
   std::vector<cudaEvent_t> free_events;
   float prof_ms[4] = {0, 0, 0, 0};
@@ -240,25 +244,26 @@ bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* ptr, uint64_t
   return r == CUDA_SUCCESS;
 }
 
-bool act_maps(CUtensorMap out[3], const void* buf, int K, int rows) {
-  const int nts[3] = {1, 2, 4};
-  for (int i = 0; i < 3; ++i)
+// boxes of 8/16/32 rows (GEMV passes) and 64/128/256 rows (GEMM passes)
+bool act_maps(CUtensorMap out[6], const void* buf, int K, int rows) {
+  const int box[6] = {8, 16, 32, 64, 128, 256};
+  for (int i = 0; i < 6; ++i)
     if (!encode_2d(&out[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, buf, K, rows, (uint64_t)K * 2, 64,
-                   8 * nts[i], CU_TENSOR_MAP_SWIZZLE_128B))
+                   box[i], CU_TENSOR_MAP_SWIZZLE_128B))
       return false;
   return true;
 }
 
-const WMap* weight_map(kvr_ctx* c, const void* w, const void* s, int N, int K) {
-  WKey key{w, N, K};
+const WMap* weight_map(kvr_ctx* c, const void* w, const void* s, int N, int K, int box = kGemvRows) {
+  WKey key{w, N, K, box};
   auto it = c->wmaps.find(key);
   if (it != c->wmaps.end()) return &it->second;
   WMap m;
-  if (!encode_2d(&m.w, CU_TENSOR_MAP_DATA_TYPE_UINT8, w, K / 2, N, K / 2, 128, kGemvRows,
+  if (!encode_2d(&m.w, CU_TENSOR_MAP_DATA_TYPE_UINT8, w, K / 2, N, K / 2, 128, box,
                  CU_TENSOR_MAP_SWIZZLE_128B))
     return nullptr;
   if (!encode_2d(&m.s, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, s, K / 32, N, (uint64_t)K / 32 * 2, 8,
-                 kGemvRows, CU_TENSOR_MAP_SWIZZLE_NONE))
+                 box, CU_TENSOR_MAP_SWIZZLE_NONE))
     return nullptr;
   if (c->wmaps.size() > 4096) c->wmaps.clear();
   return &(c->wmaps[key] = m);
@@ -275,9 +280,80 @@ struct Seg {
 
 enum class Act { A, O, Z };
 
+// Large-m passes on the tcgen05 GEMM; swiglu = 1 fuses silu(gate)*up into its epilogue.
 template <class Epi>
-int project(kvr_ctx* c, cudaStream_t st, const Seg* segs, int nseg, Act act, int K, int m, Epi epi) {
+int project_gemm(kvr_ctx* c, cudaStream_t st, const Seg* segs, int nseg, const CUtensorMap* tmx,
+                 int K, int m, bool swiglu, Epi epi) {
+  GemmParams p;
+  memset(&p, 0, sizeof p);
+  p.K = K;
+  p.kchunks = K / kGemvKStep;
+  p.status = c->status;
+  p.part = c->part;
+  p.z = c->z;
+  p.F = c->cfg.ffn;
+  int col = 0, tiles = 0;
+  if (swiglu) {
+    const WMap* g = weight_map(c, segs[0].w, segs[0].s, segs[0].N, K, 64);
+    const WMap* u = weight_map(c, segs[1].w, segs[1].s, segs[1].N, K, 64);
+    if (!g || !u) return fail(c, KVR_ERR_CUDA, "cuTensorMapEncodeTiled failed for a weight matrix");
+    p.nseg = 1;
+    p.seg[0].tw = g->w; p.seg[0].ts = g->s;
+    p.seg[1].tw = u->w; p.seg[1].ts = u->s;
+    p.seg[0].N = segs[0].N;
+    p.seg[0].tiles = (segs[0].N + 63) / 64;
+    tiles = p.seg[0].tiles;
+    col = 2 * segs[0].N;
+  } else {
+    p.nseg = nseg;
+    for (int i = 0; i < nseg; ++i) {
+      const WMap* wm = weight_map(c, segs[i].w, segs[i].s, segs[i].N, K, 128);
+      if (!wm) return fail(c, KVR_ERR_CUDA, "cuTensorMapEncodeTiled failed for a weight matrix");
+      GemmSeg& g = p.seg[i];
+      g.tw = wm->w; g.ts = wm->s;
+      g.N = segs[i].N; g.col0 = col; g.tile0 = tiles; g.tiles = (segs[i].N + 127) / 128;
+      col += segs[i].N;
+      tiles += g.tiles;
+    }
+  }
+  p.ldo = col;
+  p.plane = (long long)kGemmMaxTok * p.ldo;
+  p.swiglu = swiglu ? 1 : 0;
+  int ks = 1;
+  if (!swiglu) {
+    ks = (c->n_sms + tiles / 2) / std::max(tiles, 1);
+    ks = std::max(1, std::min(ks, std::min(p.kchunks, kGemmMaxSplit)));
+  }
+  p.ksplit = ks;
+  for (int t0 = 0; t0 < m; t0 += kGemmMaxTok) {
+    const int mp = std::min(kGemmMaxTok, m - t0);
+    p.t0 = t0;
+    p.m = mp;
+    p.n_tok = (mp + 15) / 16 * 16;
+    p.xrows = p.n_tok <= 64 ? 64 : (p.n_tok <= 128 ? 128 : 256);
+    p.tx = tmx[p.xrows == 64 ? 3 : (p.xrows == 128 ? 4 : 5)];
+    cudaError_t e;
+    {
+      Timed t(c, kProj, st);
+      e = launch_gemm_int4_tc(p, tiles, st);
+    }
+    if (e != cudaSuccess) return cuda_fail(c, e, "gemm_int4_tc launch");
+    if (!swiglu) {
+      Timed t(c, kEpi, st);
+      e = epi(p.part, p.plane, p.ksplit, p.ldo, t0, mp);
+      if (e != cudaSuccess) return cuda_fail(c, e, "epilogue launch");
+    }
+  }
+  return KVR_OK;
+}
+
+template <class Epi>
+int project(kvr_ctx* c, cudaStream_t st, const Seg* segs, int nseg, Act act, int K, int m, Epi epi,
+            bool swiglu = false) {
   const kvr_config& cfg = c->cfg;
+  const CUtensorMap* tmx = act == Act::A ? c->tm_a : (act == Act::O ? c->tm_o : c->tm_z);
+  if (cfg.weight_format == KVR_WEIGHTS_INT4_G32 && m > kGemvMaxCols && !c->force_gemv)
+    return project_gemm(c, st, segs, nseg, tmx, K, m, swiglu, epi);
   GemvParams p;
   memset(&p, 0, sizeof p);
   p.nseg = nseg;
@@ -304,7 +380,6 @@ int project(kvr_ctx* c, cudaStream_t st, const Seg* segs, int nseg, Act act, int
   p.ldo = col;
   p.part = c->part;
   const __nv_bfloat16* xbuf = act == Act::A ? c->a : (act == Act::O ? c->o : c->z);
-  const CUtensorMap* tmx = act == Act::A ? c->tm_a : (act == Act::O ? c->tm_o : c->tm_z);
   p.x = xbuf;
   p.ksteps = K / kGemvKStep;
   for (int c0 = 0; c0 < m; c0 += kGemvMaxCols) {
@@ -460,7 +535,8 @@ int run_stack(kvr_ctx* c, int slot, const RowMap& rows, const void* hidden,
       rc = project(c, st, gu, 2, Act::A, H, m,
                    [&](const float* part, long long plane, int ks, int ldo, int c0, int mb) {
                      return launch_epi_swiglu(part, plane, ks, ldo, c0, mb, F, c->z, st);
-                   });
+                   },
+                   /*swiglu=*/true);
       if (rc) return rc;
     }
     // down + residual, then the next layer's attention norm (or the output)
@@ -585,6 +661,8 @@ int kvr_ctx_create(const kvr_config* cfg, void* kv_arena, size_t arena_bytes, vo
     delete c;
     return KVR_ERR_FAULT;
   }
+  const char* fg = getenv("KVR_FORCE_GEMV");
+  c->force_gemv = fg && fg[0] == '1';
   c->requested = cfg->n_slots;
   c->reuse = cfg->n_slots > 0;
   const int want = std::max(cfg->n_slots, 1);
@@ -618,6 +696,7 @@ int kvr_ctx_create(const kvr_config* cfg, void* kv_arena, size_t arena_bytes, vo
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&c->n_sms, cudaDevAttrMultiProcessorCount, dev);
   if (e == cudaSuccess) e = gemv_setup();
+  if (e == cudaSuccess) e = gemm_tc_setup();
   if (e == cudaSuccess) e = attn_setup();
   if (e == cudaSuccess && !g_encode) {
     cudaDriverEntryPointQueryResult q;

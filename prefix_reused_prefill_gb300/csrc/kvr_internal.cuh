@@ -20,6 +20,8 @@ constexpr int kGemvRows = 128;     // weight rows per GEMV CTA (8 warps x 16 row
 constexpr int kGemvKStep = 256;    // inputs per pipeline stage (8 groups of 32)
 constexpr int kGemvMaxCols = 32;   // tokens per GEMV pass (4 tensor-core n-tiles)
 constexpr int kMaxKSplit = 16;
+constexpr int kGemmMaxTok = 256;   // tokens per tcgen05 GEMM pass (MMA N <= 256)
+constexpr int kGemmMaxSplit = 8;
 constexpr int kAttnKeys = 64;      // keys per attention pipeline stage
 constexpr int kSplitTargetCtas = 320;
 constexpr int kMaxSplits = 64;
@@ -72,6 +74,35 @@ struct GemvParams {
   int* status;
 };
 
+struct GemmSeg {
+  CUtensorMap tw;   // uint8 [N][K/2], box {128 B, 128 rows} (64 rows for SwiGLU), 128B swizzle
+  CUtensorMap ts;   // fp16 scales [N][K/32], box {8, 128 rows} (64 rows for SwiGLU)
+  int N;
+  int col0;
+  int tile0;
+  int tiles;
+};
+
+struct GemmParams {
+  GemmSeg seg[3];   // SwiGLU mode: seg[0] = gate, seg[1] = up (nseg = 1 for tiling)
+  CUtensorMap tx;   // activations bf16 [max_rows][K], box {64, xrows}, 128B swizzle
+  int nseg;
+  int K;
+  int kchunks;      // K / 256
+  int ksplit;
+  int n_tok;        // MMA N: tokens of this pass rounded up to 16 (<= 256)
+  int xrows;        // activation box rows (64, 128 or 256) >= n_tok
+  int m;            // valid tokens of this pass
+  int t0;           // first token of this pass
+  int swiglu;       // 1: write z = silu(gate) * up; 0: write fp32 partial sums
+  int ldo;
+  int F;
+  long long plane;
+  float* part;      // [ksplit][256][ldo]
+  __nv_bfloat16* z; // [max_rows][F]
+  int* status;
+};
+
 struct AttnParams {
   CUtensorMap tkv;           // arena as bf16 [rows][head_dim], box {64, 64}, 128B swizzle
   const __nv_bfloat16* q;    // [m][Hq][d] after RoPE
@@ -97,6 +128,7 @@ cudaError_t launch_prefix_match(const int32_t* slot_tokens, const int* slot_len,
                                 cudaStream_t st);
 cudaError_t launch_gemv_int4(const GemvParams& p, int total_tiles, int nt, cudaStream_t st);
 cudaError_t launch_gemv_bf16(const GemvParams& p, int total_cols, cudaStream_t st);
+cudaError_t launch_gemm_int4_tc(const GemmParams& p, int total_tiles, cudaStream_t st);
 cudaError_t launch_attention(const AttnParams& p, int d, int row_warps, cudaStream_t st);
 cudaError_t launch_attn_combine(const AttnParams& p, int d, cudaStream_t st);
 cudaError_t launch_rope_table(const RowMap& rows, int d, float theta, float2* table,
@@ -119,6 +151,7 @@ cudaError_t launch_epi_cast(const float* part, long long plane, int ksplit, int 
 int gemv_int4_smem(int nt);
 int attn_smem(int d);
 cudaError_t gemv_setup();
+cudaError_t gemm_tc_setup();
 cudaError_t attn_setup();
 cudaError_t static_match_scratch(int32_t** prompt, int** slot_len, int32_t** match_out);
 

@@ -87,17 +87,18 @@ def test_tiny_config_exact():
 
 # --------------------------------------------------------------------------- stacks
 
-@pytest.mark.parametrize("shape_name,P,ms", [
-    ("small", 70, [1, 3, 8, 9, 17, 40]),
-    ("small_d128", 45, [1, 5, 16, 33]),
-    ("small_bf16", 33, [2, 11, 35]),
+@pytest.mark.parametrize("shape_name,P,ms,cap", [
+    ("small", 70, [1, 3, 8, 9, 17, 40, 130], 256),
+    ("small_d128", 45, [1, 5, 16, 33, 100], 256),
+    ("small_bf16", 33, [2, 11, 35], 256),
+    ("small", 150, [300], 512),
 ])
-def test_suffix_prefill_matches_oracle(shape_name, P, ms):
-    shape, kv, w, W, _ = make(shape_name, 2, 256, 128)
+def test_suffix_prefill_matches_oracle(shape_name, P, ms, cap):
+    shape, kv, w, W, _ = make(shape_name, 2, cap, min(cap, 320))
     dims = oracle_dims(shape)
     toks = list(range(1000, 1000 + P + max(ms)))
     x = hidden(toks, shape)
-    cache = om.SlotKV(shape.n_layers, shape.n_kv_heads, 256, shape.head_dim)
+    cache = om.SlotKV(shape.n_layers, shape.n_kv_heads, cap, shape.head_dim)
     whole = om.prefill(dims, W, cache, workloads.bf16_to_f64(x), 0)
 
     assert kv.kvr_slot_match(toks[:P]) == (0, 0)
