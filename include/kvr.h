@@ -134,9 +134,12 @@ typedef struct kvr_ctx kvr_ctx;
 
 /*
  * Device bytes the caller must provide.
- * KV arena (slot-major; a slot's region is contiguous):
- *   slot s, layer l, kind c (0 = K, 1 = V), KV head j, position p, element e at
- *   bf16 index ((((s*L + l)*2 + c)*Hkv + j)*capacity + p)*head_dim + e,
+ * KV arena (slot-major; a slot's region is contiguous), bf16:
+ *   K of slot s, layer l, KV head j, position p, element e at
+ *     ((((s*L + l)*2 + 0)*Hkv + j)*capacity + p)*head_dim + e   ([capacity][head_dim] per head);
+ *   V is stored transposed, element e of position p at
+ *     ((((s*L + l)*2 + 1)*Hkv + j)*head_dim + e)*capacity + p   ([head_dim][capacity] per head),
+ *   so that both tensor-core operands of P.V are K-major tiles;
  *   followed by the device token mirror int32 [n_slots][capacity].
  *   kvr_arena_bytes(cfg, n) is the size for n slots (n = cfg->n_slots, or 1
  *   when n_slots is 0).
@@ -222,7 +225,8 @@ int kvr_slot_tokens(const kvr_ctx* ctx, int slot, int32_t* tokens, int n);
  * written into the arena (restoring a saved slot, or synthetic K/V).  Uploads
  * the token mirror on `stream`. */
 int kvr_slot_assign(kvr_ctx* ctx, int slot, const int32_t* tokens, int n, void* stream);
-/* Device addresses of a slot's K and V for one layer: [Hkv][capacity][head_dim] bf16. */
+/* Device addresses of a slot's K and V for one layer: K is [Hkv][capacity][head_dim] bf16,
+ * V is [Hkv][head_dim][capacity] bf16 (transposed, see the arena layout). */
 int kvr_slot_kv(const kvr_ctx* ctx, int slot, int layer, void** k, void** v);
 
 /*

@@ -10,10 +10,11 @@
 // One CTA = (row tile, key split, KV head).  All G = Hq/Hkv query heads of a
 // KV head and all m tokens are packed as rows (row = token*G + head-in-group),
 // so each K/V tile is read from HBM once per (tile, split) for every query
-// head that uses it.  A producer warp streams 64-key K and V tiles through TMA
-// (128B-swizzled) into a 3-stage mbarrier ring; each consumer warp owns 16
-// rows: S = Q K^T and O += P V run as bf16 m16n8k16 tensor-core fragments
-// (ldmatrix / ldmatrix.trans from the swizzled tiles), the online softmax runs
+// head that uses it.  A producer warp streams 64-key K tiles and V^T tiles (V
+// is stored transposed in the slot) through TMA (128B-swizzled) into a
+// 3-stage mbarrier ring; each consumer warp owns 16 rows: S = Q K^T and
+// O += P V run as bf16 m16n8k16 tensor-core fragments (ldmatrix from the
+// swizzled tiles), the online softmax runs
 // in fp32 registers in the log2 domain with quad shuffles.  With several
 // splits, unnormalised partials (O, running max, running sum) are merged by
 // attn_combine in a fixed split order.
@@ -26,7 +27,7 @@ namespace {
 template <int D>
 struct AttnCfg {
   static constexpr int kHalves = D / 64;                 // 64-element TMA boxes per row
-  static constexpr int kTileBytes = kAttnKeys * D * 2;   // one K (or V) tile
+  static constexpr int kTileBytes = kAttnKeys * D * 2;   // one K tile ([64 keys][D]) or V^T tile ([D][64 keys])
   static constexpr int kStageBytes = 2 * kTileBytes;
   static constexpr int kStages = D == 128 ? 3 : 4;
   static constexpr int kSmem = kStages * kStageBytes + 1024;
@@ -112,9 +113,9 @@ __global__ void __launch_bounds__((RW + 1) * 32) attn_kernel(const __grid_consta
 #pragma unroll
         for (int h = 0; h < C::kHalves; ++h) {
           dev::tma_load_2d(sb + h * (kAttnKeys * 128), &p.tkv, 64 * h, p.kbase + kv * p.cap + key0, fb);
-          dev::tma_load_2d(sb + C::kTileBytes + h * (kAttnKeys * 128), &p.tkv, 64 * h,
-                           p.vbase + kv * p.cap + key0, fb);
         }
+        // V^T tile: D rows (head elements) x 64 keys
+        dev::tma_load_2d(sb + C::kTileBytes, &p.tvt, key0, p.vtbase + kv * D, fb);
         ++issued;
       }
       for (int st = 0; st < C::kStages && st < issued; ++st) {
@@ -134,8 +135,10 @@ __global__ void __launch_bounds__((RW + 1) * 32) attn_kernel(const __grid_consta
   // Q fragments (A operand of S = Q K^T), loaded once
   uint32_t qa[D / 16][4];
   {
-    const __nv_bfloat16* q0 = ri0.tok >= 0 ? p.q + ((long long)ri0.tok * p.Hq + ri0.head) * D : nullptr;
-    const __nv_bfloat16* q1 = ri1.tok >= 0 ? p.q + ((long long)ri1.tok * p.Hq + ri1.head) * D : nullptr;
+    const __nv_bfloat16* q0 =
+        ri0.tok >= 0 ? p.q + (((long long)kv * p.rows.m + ri0.tok) * p.G + ri0.head % p.G) * D : nullptr;
+    const __nv_bfloat16* q1 =
+        ri1.tok >= 0 ? p.q + (((long long)kv * p.rows.m + ri1.tok) * p.G + ri1.head % p.G) * D : nullptr;
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
       const int d0 = kk * 16 + 2 * c;
@@ -226,7 +229,8 @@ __global__ void __launch_bounds__((RW + 1) * 32) attn_kernel(const __grid_consta
       }
     }
 
-    // O += P V: P as the A operand (16 keys per k-step), V^T fragments by ldmatrix.trans
+    // O += P V: P as the A operand (16 keys per k-step); V^T rows are head elements,
+    // so plain ldmatrix of the V^T tile yields the B fragments
 #pragma unroll
     for (int ks = 0; ks < 4; ++ks) {
       uint32_t pa[4];
@@ -237,11 +241,10 @@ __global__ void __launch_bounds__((RW + 1) * 32) attn_kernel(const __grid_consta
 #pragma unroll
       for (int dp = 0; dp < D / 16; ++dp) {
         const int q = lane >> 3;
-        const int key = 16 * ks + 8 * (q & 1) + (lane & 7);
-        const int chunk = 2 * dp + (q >> 1);
+        const int drow = 16 * dp + 8 * (q >> 1) + (lane & 7);
+        const int chunk = 2 * ks + (q & 1);
         uint32_t b0r, b1r, b2r, b3r;
-        dev::ldmatrix_x4_trans(vt + (chunk >> 3) * (kAttnKeys * 128) + dev::swz128(key, chunk & 7),
-                               b0r, b1r, b2r, b3r);
+        dev::ldmatrix_x4(vt + dev::swz128(drow, chunk), b0r, b1r, b2r, b3r);
         dev::mma_bf16_16816(o[2 * dp], pa, b0r, b1r, o[2 * dp]);
         dev::mma_bf16_16816(o[2 * dp + 1], pa, b2r, b3r, o[2 * dp + 1]);
       }
@@ -280,21 +283,39 @@ __global__ void __launch_bounds__((RW + 1) * 32) attn_kernel(const __grid_consta
   }
 }
 
+// One warp per (token, head) row: merge the key splits' (O, max, sum) partials
+// in split order; each lane owns D/32 consecutive elements.
 template <int D>
-__global__ void attn_combine_kernel(const __grid_constant__ AttnParams p) {
-  const long long rowidx = blockIdx.x;  // token * Hq + head
-  const int d = threadIdx.x;
-  const long long plane = (long long)p.rows.m * p.Hq;
+__global__ void __launch_bounds__(256) attn_combine_kernel(const __grid_constant__ AttnParams p) {
+  const long long rows = (long long)p.rows.m * p.Hq;
+  const long long rowidx = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (rowidx >= rows) return;
+  const int lane = threadIdx.x & 31;
+  constexpr int E = D / 32;
   float M = -INFINITY;
-  for (int s = 0; s < p.nsplit; ++s) M = fmaxf(M, p.ml[s * plane + rowidx].x);
-  float num = 0.f, den = 0.f;
+  for (int s = 0; s < p.nsplit; ++s) M = fmaxf(M, p.ml[s * rows + rowidx].x);
+  float acc[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) acc[e] = 0.f;
+  float den = 0.f;
   for (int s = 0; s < p.nsplit; ++s) {
-    const float2 ml = p.ml[s * plane + rowidx];
+    const float2 ml = p.ml[s * rows + rowidx];
     const float w = ml.x == -INFINITY ? 0.f : exp2f(ml.x - M);
-    num += w * p.opart[(s * plane + rowidx) * D + d];
     den += w * ml.y;
+    const float* src = p.opart + (s * rows + rowidx) * D + lane * E;
+    if (E == 4) {
+      const float4 v = *reinterpret_cast<const float4*>(src);
+      acc[0] += w * v.x; acc[1] += w * v.y; acc[2] += w * v.z; acc[3 % E] += w * v.w;
+    } else {
+      const float2 v = *reinterpret_cast<const float2*>(src);
+      acc[0] += w * v.x; acc[1 % E] += w * v.y;
+    }
   }
-  p.o[rowidx * D + d] = __float2bfloat16_rn(num / den);
+  const float inv = 1.f / den;
+  __nv_bfloat16* dst = p.o + rowidx * D + lane * E;
+#pragma unroll
+  for (int e = 0; e < E; e += 2)
+    *reinterpret_cast<uint32_t*>(dst + e) = dev::pack_bf16x2(acc[e] * inv, acc[e + 1] * inv);
 }
 
 template <int D, int RW>
@@ -336,9 +357,9 @@ cudaError_t launch_attention(const AttnParams& p, int d, int row_warps, cudaStre
 }
 
 cudaError_t launch_attn_combine(const AttnParams& p, int d, cudaStream_t st) {
-  const unsigned rows = (unsigned)(p.rows.m * p.Hq);
-  if (d == 128) attn_combine_kernel<128><<<rows, 128, 0, st>>>(p);
-  else attn_combine_kernel<64><<<rows, 64, 0, st>>>(p);
+  const unsigned blocks = (unsigned)((p.rows.m * p.Hq + 7) / 8);
+  if (d == 128) attn_combine_kernel<128><<<blocks, 256, 0, st>>>(p);
+  else attn_combine_kernel<64><<<blocks, 256, 0, st>>>(p);
   return cudaGetLastError();
 }
 

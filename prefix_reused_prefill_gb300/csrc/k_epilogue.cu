@@ -85,7 +85,8 @@ __global__ void epi_qkv_kernel(const float* part, long long plane, int ksplit, i
     const float y1 = x1 * cs.x - x2 * cs.y;
     const float y2 = x2 * cs.x + x1 * cs.y;
     if (hd < Hq) {
-      __nv_bfloat16* dst = q + ((long long)i * Hq + hd) * d;
+      const int G = Hq / Hkv;
+      __nv_bfloat16* dst = q + (((long long)(hd / G) * rows.m + i) * G + hd % G) * d;
       dst[j] = __float2bfloat16_rn(y1);
       dst[j + half] = __float2bfloat16_rn(y2);
     } else {
@@ -94,9 +95,10 @@ __global__ void epi_qkv_kernel(const float* part, long long plane, int ksplit, i
       dst[j + half] = __float2bfloat16_rn(y2);
     }
   } else {
-    __nv_bfloat16* dst = arena + v_off + ((long long)(hd - Hq - Hkv) * cap + store) * d;
-    dst[j] = __float2bfloat16_rn(x1);
-    dst[j + half] = __float2bfloat16_rn(x2);
+    // V is kept transposed in the slot: [Hkv][d][capacity]
+    __nv_bfloat16* dst = arena + v_off + (long long)(hd - Hq - Hkv) * d * cap + store;
+    dst[(long long)j * cap] = __float2bfloat16_rn(x1);
+    dst[(long long)(j + half) * cap] = __float2bfloat16_rn(x2);
   }
 }
 

@@ -309,7 +309,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_int4_tc_kernel(const __grid_
     if (!ok) *abort_v = 1;
 
     // ---------------------------------------------------------------- epilogue
-    const bool have = dev::mbar_wait(dev::smem_u32(&acc_full), 0, p.status) && !*abort_v;
+    const bool have = __all_sync(0xffffffffu, dev::mbar_wait(dev::smem_u32(&acc_full), 0, p.status) && !*abort_v);
     tc_fence_after();
     if (have) {
       const int q = warp & 3;              // TMEM lane quarter this warp may read

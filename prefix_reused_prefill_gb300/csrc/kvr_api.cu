@@ -163,7 +163,7 @@ struct kvr_ctx {
   float* opart = nullptr;
   float2* ml = nullptr;
   // TMA descriptors
-  CUtensorMap tm_kv{};
+  CUtensorMap tm_kv{}, tm_vt{}, tm_q{};
   CUtensorMap tm_a[6]{}, tm_o[6]{}, tm_z[6]{};
   std::map<WKey, WMap> wmaps;
   // slot table
@@ -426,9 +426,16 @@ long long kv_offset(const kvr_ctx* c, int slot, int layer, int kind) {
          k.head_dim;
 }
 
-int kv_row(const kvr_ctx* c, int slot, int layer, int kind) {
+// row of (slot, layer, K, head 0, position 0) in the [rows][head_dim] view of the arena
+int k_row(const kvr_ctx* c, int slot, int layer) {
   const kvr_config& k = c->cfg;
-  return (int)((((long long)slot * k.n_layers + layer) * 2 + kind) * k.n_kv_heads * (long long)k.capacity);
+  return (int)((((long long)slot * k.n_layers + layer) * 2) * k.n_kv_heads * (long long)k.capacity);
+}
+
+// row of (slot, layer, V^T, head 0, element 0) in the [rows][capacity] view of the arena
+int vt_row(const kvr_ctx* c, int slot, int layer) {
+  const kvr_config& k = c->cfg;
+  return (int)((((long long)slot * k.n_layers + layer) * 2 + 1) * k.n_kv_heads * (long long)k.head_dim);
 }
 
 int attention(kvr_ctx* c, cudaStream_t st, int slot, int layer, const RowMap& rows) {
@@ -436,6 +443,8 @@ int attention(kvr_ctx* c, cudaStream_t st, int slot, int layer, const RowMap& ro
   AttnParams p;
   memset(&p, 0, sizeof p);
   p.tkv = c->tm_kv;
+  p.tvt = c->tm_vt;
+  p.tq = c->tm_q;
   p.q = c->q;
   p.o = c->o;
   p.opart = c->opart;
@@ -444,22 +453,33 @@ int attention(kvr_ctx* c, cudaStream_t st, int slot, int layer, const RowMap& ro
   p.Hq = k.n_q_heads;
   p.Hkv = k.n_kv_heads;
   p.G = k.n_q_heads / k.n_kv_heads;
-  p.kbase = kv_row(c, slot, layer, 0);
-  p.vbase = kv_row(c, slot, layer, 1);
+  p.kbase = k_row(c, slot, layer);
+  p.vtbase = vt_row(c, slot, layer);
   p.cap = k.capacity;
   p.scale_log2 = 1.4426950408889634f / sqrtf((float)k.head_dim);
   p.status = c->status;
   const int R = p.G * rows.m;
-  const int rw = attn_row_warps(R);
-  p.row_tiles = (R + 16 * rw - 1) / (16 * rw);
   const int kend = rows.P + rows.m;
-  int ns = attn_nsplit(k.n_kv_heads, R, kend, kSplitTargetCtas);
+  const bool tc = R > kAttnTcMinRows && !c->force_gemv;
+  int ns;
+  if (tc) {
+    // tcgen05 path: 128-row tiles; split the keys until the grid covers the SMs
+    p.row_tiles = (R + 127) / 128;
+    const int nb = (kend + kAttnKeys - 1) / kAttnKeys;
+    ns = (c->n_sms + p.row_tiles * k.n_kv_heads - 1) / (p.row_tiles * k.n_kv_heads);
+    ns = std::max(1, std::min(std::min(ns, std::max(1, nb / 4)), kMaxSplits));
+  } else {
+    const int rw = attn_row_warps(R);
+    p.row_tiles = (R + 16 * rw - 1) / (16 * rw);
+    ns = attn_nsplit(k.n_kv_heads, R, kend, kSplitTargetCtas);
+  }
   while (ns > 1 && (size_t)ns * rows.m * k.n_q_heads * k.head_dim > c->sl.opart_floats) --ns;
   p.nsplit = ns;
   cudaError_t e;
   {
     Timed t(c, kAttn, st);
-    e = launch_attention(p, k.head_dim, rw, st);
+    e = tc ? launch_attention_tc(p, k.head_dim, st)
+           : launch_attention(p, k.head_dim, attn_row_warps(R), st);
   }
   if (e != cudaSuccess) return cuda_fail(c, e, "attention launch");
   if (ns > 1) {
@@ -698,6 +718,7 @@ int kvr_ctx_create(const kvr_config* cfg, void* kv_arena, size_t arena_bytes, vo
   if (e == cudaSuccess) e = gemv_setup();
   if (e == cudaSuccess) e = gemm_tc_setup();
   if (e == cudaSuccess) e = attn_setup();
+  if (e == cudaSuccess) e = attn_tc_setup();
   if (e == cudaSuccess && !g_encode) {
     cudaDriverEntryPointQueryResult q;
     void* fn = nullptr;
@@ -713,6 +734,13 @@ int kvr_ctx_create(const kvr_config* cfg, void* kv_arena, size_t arena_bytes, vo
   const uint64_t kv_rows = (uint64_t)c->granted * k.n_layers * 2 * k.n_kv_heads * k.capacity;
   bool ok = encode_2d(&c->tm_kv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, c->arena, k.head_dim, kv_rows,
                       (uint64_t)k.head_dim * 2, 64, kAttnKeys, CU_TENSOR_MAP_SWIZZLE_128B);
+  // the same arena as [rows][capacity]: V^T tiles of head_dim rows x 64 keys
+  ok = ok && encode_2d(&c->tm_vt, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, c->arena, k.capacity,
+                       kv_rows * k.head_dim / k.capacity, (uint64_t)k.capacity * 2, 64, k.head_dim,
+                       CU_TENSOR_MAP_SWIZZLE_128B);
+  ok = ok && encode_2d(&c->tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, c->q, k.head_dim,
+                       (uint64_t)k.max_rows * k.n_q_heads, (uint64_t)k.head_dim * 2, 64, 128,
+                       CU_TENSOR_MAP_SWIZZLE_128B);
   if (k.weight_format == KVR_WEIGHTS_INT4_G32) {
     ok = ok && act_maps(c->tm_a, c->a, k.hidden, k.max_rows);
     ok = ok && act_maps(c->tm_o, c->o, k.n_q_heads * k.head_dim, k.max_rows);

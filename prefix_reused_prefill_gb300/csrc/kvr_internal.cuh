@@ -23,6 +23,7 @@ constexpr int kMaxKSplit = 16;
 constexpr int kGemmMaxTok = 256;   // tokens per tcgen05 GEMM pass (MMA N <= 256)
 constexpr int kGemmMaxSplit = 8;
 constexpr int kAttnKeys = 64;      // keys per attention pipeline stage
+constexpr int kAttnTcMinRows = 96; // G*m above this: tcgen05 attention (128-row tiles)
 constexpr int kSplitTargetCtas = 320;
 constexpr int kMaxSplits = 64;
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s per bounded wait
@@ -104,15 +105,17 @@ struct GemmParams {
 };
 
 struct AttnParams {
-  CUtensorMap tkv;           // arena as bf16 [rows][head_dim], box {64, 64}, 128B swizzle
-  const __nv_bfloat16* q;    // [m][Hq][d] after RoPE
+  CUtensorMap tkv;           // arena as bf16 [rows][head_dim], box {64, 64}, 128B swizzle (K tiles)
+  CUtensorMap tvt;           // arena as bf16 [rows][capacity], box {64, head_dim} (V^T tiles)
+  CUtensorMap tq;            // q as bf16 [Hkv*max_rows*G][head_dim], box {64, 128}
+  const __nv_bfloat16* q;    // [Hkv][m][G][d] after RoPE (KV-head-major rows)
   __nv_bfloat16* o;          // [m][Hq*d] (nsplit == 1)
   float* opart;              // [nsplit][m][Hq][d]
   float2* ml;                // [nsplit][m][Hq]  (running max in log2 units, sum)
   RowMap rows;
   int Hq, Hkv, G;
-  int kbase;                 // arena row of (slot, layer, K, head 0, position 0)
-  int vbase;                 // arena row of (slot, layer, V, head 0, position 0)
+  int kbase;                 // [rows][d] view row of (slot, layer, K, head 0, position 0)
+  int vtbase;                // [rows][cap] view row of (slot, layer, V^T, head 0, element 0)
   int cap;
   int nsplit;
   int row_tiles;
@@ -130,6 +133,7 @@ cudaError_t launch_gemv_int4(const GemvParams& p, int total_tiles, int nt, cudaS
 cudaError_t launch_gemv_bf16(const GemvParams& p, int total_cols, cudaStream_t st);
 cudaError_t launch_gemm_int4_tc(const GemmParams& p, int total_tiles, cudaStream_t st);
 cudaError_t launch_attention(const AttnParams& p, int d, int row_warps, cudaStream_t st);
+cudaError_t launch_attention_tc(const AttnParams& p, int d, cudaStream_t st);
 cudaError_t launch_attn_combine(const AttnParams& p, int d, cudaStream_t st);
 cudaError_t launch_rope_table(const RowMap& rows, int d, float theta, float2* table,
                               cudaStream_t st);
@@ -153,6 +157,7 @@ int attn_smem(int d);
 cudaError_t gemv_setup();
 cudaError_t gemm_tc_setup();
 cudaError_t attn_setup();
+cudaError_t attn_tc_setup();
 cudaError_t static_match_scratch(int32_t** prompt, int** slot_len, int32_t** match_out);
 
 }  // namespace kvr

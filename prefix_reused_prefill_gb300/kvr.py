@@ -218,7 +218,8 @@ class Kvr:
                                              self._stream(stream)))
 
     def kvr_slot_kv(self, slot: int, layer: int) -> Tuple[torch.Tensor, torch.Tensor]:
-        """K, V views [Hkv][capacity][head_dim] bf16 of one slot and layer."""
+        """K view [Hkv][capacity][head_dim] and V view [Hkv][head_dim][capacity] (V is
+        stored transposed) of one slot and layer, bf16."""
         k, v = ctypes.c_void_p(), ctypes.c_void_p()
         self._check(self.lib.kvr_slot_kv(self.ctx, slot, layer, ctypes.byref(k), ctypes.byref(v)))
         c = self.cfg
@@ -226,8 +227,8 @@ class Kvr:
         flat = self.arena.view(torch.bfloat16)
         base = self.arena.data_ptr()
         ko, vo = (k.value - base) // 2, (v.value - base) // 2
-        shape = (c.n_kv_heads, c.capacity, c.head_dim)
-        return flat[ko:ko + n].view(shape), flat[vo:vo + n].view(shape)
+        return (flat[ko:ko + n].view(c.n_kv_heads, c.capacity, c.head_dim),
+                flat[vo:vo + n].view(c.n_kv_heads, c.head_dim, c.capacity))
 
     def _rows_call(self, fn, slot, tokens, hidden, weights, out, stream):
         arr = weights[0] if isinstance(weights, tuple) else weights

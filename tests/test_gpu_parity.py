@@ -50,8 +50,9 @@ def hidden(tokens, shape, seed=5):
 
 
 def slot_kv_f64(kv, slot, layer, n):
+    """K, V of a slot as [Hkv][n][d] (V is stored transposed in the arena)."""
     k, v = kv.kvr_slot_kv(slot, layer)
-    return workloads.bf16_to_f64(k[:, :n]), workloads.bf16_to_f64(v[:, :n])
+    return workloads.bf16_to_f64(k[:, :n]), workloads.bf16_to_f64(v[:, :, :n].transpose(1, 2))
 
 
 # --------------------------------------------------------------------------- config 1
@@ -143,10 +144,10 @@ def test_verify_then_truncate_equals_single_steps():
         kv.kvr_verify(0, list(range(65)), torch.zeros(65, shape.hidden, dtype=torch.bfloat16).cuda(), w)
 
 
-def test_branches_match_oracle_and_leave_checkpoint():
-    shape, kv, w, W, gw = make("small", 2, 256, 64)
+@pytest.mark.parametrize("P,lens", [(40, [5, 9, 1, 7]), (70, [30, 50, 1, 40])])
+def test_branches_match_oracle_and_leave_checkpoint(P, lens):
+    shape, kv, w, W, gw = make("small", 2, 256, 128)
     dims = oracle_dims(shape)
-    P, lens = 40, [5, 9, 1, 7]
     state = list(range(7, 7 + P))
     qs = [list(range(2000 + 100 * b, 2000 + 100 * b + n)) for b, n in enumerate(lens)]
     xs = hidden(state, shape)
@@ -178,7 +179,7 @@ def test_attention_only_7b_layer_with_given_kv():
     kk, vv = workloads.random_kv(shape.n_kv_heads, P, shape.head_dim, 77)
     k, v = kv.kvr_slot_kv(2, 0)
     k[:, :P] = kk.cuda()
-    v[:, :P] = vv.cuda()
+    v[:, :, :P] = vv.transpose(1, 2).cuda()
     state = list(range(P))
     kv.kvr_slot_assign(2, state)
     cache = om.SlotKV(1, shape.n_kv_heads, 1024, shape.head_dim)
