@@ -160,9 +160,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     }
     for (int i = 0; i < 2; ++i) {
       dev::mbar_init(dev::smem_u32(&s_full[i]), 1);
-      dev::mbar_init(dev::smem_u32(&s_empty[i]), 128);
+      dev::mbar_init(dev::smem_u32(&s_empty[i]), 4);
     }
-    dev::mbar_init(dev::smem_u32(&p_full), 128);
+    dev::mbar_init(dev::smem_u32(&p_full), 4);
     dev::mbar_init(dev::smem_u32(&pv_done), 1);
     *abort_v = 0;
     dev::fence_mbar_init();
@@ -284,7 +284,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       tmem_ld32_nowait(tmem + tlane + C::scol(sb) + 32, sr + 32);
       tmem_wait_ld();
       tc_fence_before();
-      dev::mbar_arrive(dev::smem_u32(&s_empty[sb]));
+      __syncwarp();
+      if (lane == 0) dev::mbar_arrive(dev::smem_u32(&s_empty[sb]));
       const int key0 = (b0 + j) * kKeys;
       // visible keys of this row within the block: [0, P) and [lo, hi]
       const int pe = min(max(P0 - key0, 0), kKeys);            // keys k < pe are in [0, P)
@@ -344,7 +345,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       }
       fence_proxy_async();
       tc_fence_before();
-      dev::mbar_arrive(dev::smem_u32(&p_full));
+      __syncwarp();
+      if (lane == 0) dev::mbar_arrive(dev::smem_u32(&p_full));
     }
     if (ok && nblk > 0) {
       ok = dev::mbar_wait(dev::smem_u32(&pv_done), (nblk - 1) & 1, p.status) && !*abort_v;

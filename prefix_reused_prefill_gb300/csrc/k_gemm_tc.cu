@@ -14,14 +14,17 @@
 //              tokens, 128B-swizzled K-major, 3 stages);
 //   warp 1     allocates the TMEM accumulator; one thread issues tcgen05.mma
 //              and tcgen05.commit (which frees the smem stages it read);
-//   warps 2-9  converters: int4 codes -> bf16 weights (code * scale, exact for
+//   warps 2-17 converters: int4 codes -> bf16 weights (code * scale, exact for
 //              scales with at most 8 significant bits) written as 128B-swizzled
-//              K-major A tiles (4 stages); thread = (tile row, one of the two
-//              32-input groups of a 64-input atom).  Then the epilogue, the two
-//              sets of four warps taking alternate 32-token chunks: tcgen05.ld of
-//              the accumulator, and either fp32 partial sums (reduced row-wise
-//              by the epilogue kernels) or, for the gate|up projection, the
-//              fused SwiGLU product silu(gate) * up written as bf16.
+//              K-major A tiles.  Four groups of four warps: group g converts
+//              atom g (inputs 64g..64g+63) of every 256-input chunk into its
+//              own A stage, so four atoms are in flight at once and the latency
+//              of one conversion (dequant, stores, proxy fence) is overlapped;
+//              thread = (tile row, one of the atom's two 32-input groups).
+//              Then the epilogue, the four groups taking 32-token chunks in
+//              turn: tcgen05.ld of the accumulator, and either fp32 partial
+//              sums (reduced row-wise by the epilogue kernels) or, for the
+//              gate|up projection, the fused SwiGLU product silu(gate) * up.
 // Every wait is bounded; on a timeout the CTA records it in the status word,
 // drains its own copies and frees its TMEM before returning.
 #include "kvr_internal.cuh"
@@ -30,9 +33,11 @@ namespace kvr {
 
 namespace {
 
-constexpr int kThreads = 320;
-constexpr int kConv = 256;  // converter threads
-constexpr int kRawStages = 2;
+constexpr int kConvGroups = 4;                  // one per 64-input atom of a 256-input chunk
+constexpr int kConvWarps = 4 * kConvGroups;      // 4 warps (128 rows x 2 groups) per atom
+constexpr int kThreads = 64 + 32 * kConvWarps;   // + producer warp + MMA warp
+constexpr int kRawStages = 3;
+constexpr int kPrefetch = 2;   // int4 chunks prefetched into L2 ahead of their TMA load
 constexpr int kAStages = 4;
 constexpr int kXStages = 3;
 constexpr int kRawWBytes = 128 * 128;   // 128 rows x 256 inputs of int4
@@ -143,10 +148,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_int4_tc_kernel(const __grid_
   if (threadIdx.x == 0) {
     for (int i = 0; i < kRawStages; ++i) {
       dev::mbar_init(dev::smem_u32(&raw_full[i]), 1);
-      dev::mbar_init(dev::smem_u32(&raw_empty[i]), kConv);
+      dev::mbar_init(dev::smem_u32(&raw_empty[i]), kConvWarps);
     }
     for (int i = 0; i < kAStages; ++i) {
-      dev::mbar_init(dev::smem_u32(&a_full[i]), kConv);
+      dev::mbar_init(dev::smem_u32(&a_full[i]), kConvWarps / kConvGroups);
       dev::mbar_init(dev::smem_u32(&a_empty[i]), 1);
     }
     for (int i = 0; i < kXStages; ++i) {
@@ -169,22 +174,33 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_int4_tc_kernel(const __grid_
   const uint32_t tmem = tmem_slot;
 
   if (warp == 0) {
-    // ---------------------------------------------------------------- producer
+    // ---------------------------------------------------------------- producers
+    // lane 0 streams int4 tiles + scales, lane 1 streams activation tiles; the
+    // two rings are independent so neither stream waits behind the other.
     if (lane == 0) {
       dev::prefetch_tmap(&seg.tw);
       dev::prefetch_tmap(&seg.ts);
-      dev::prefetch_tmap(&p.tx);
       const uint64_t pol = dev::policy_evict_first();
-      int raw_issued = 0, x_issued = 0;
-      bool ok = true;
-      for (int i = 0; i < nkc && ok; ++i) {
+      auto prefetch_chunk = [&](int i) {
+        const int kc = kc0 + i;
+        if (p.swiglu) {
+          dev::tma_prefetch_2d(&p.seg[0].tw, kc * 128, row0);
+          dev::tma_prefetch_2d(&p.seg[1].tw, kc * 128, row0);
+        } else {
+          dev::tma_prefetch_2d(&seg.tw, kc * 128, row0);
+        }
+      };
+      for (int i = 0; i < kPrefetch && i < nkc; ++i) prefetch_chunk(i);
+      int raw_issued = 0;
+      for (int i = 0; i < nkc; ++i) {
+        if (i + kPrefetch < nkc) prefetch_chunk(i + kPrefetch);
         const int rs = i % kRawStages;
         if (i >= kRawStages &&
-            !dev::mbar_wait(dev::smem_u32(&raw_empty[rs]), ((i / kRawStages) - 1) & 1, p.status)) {
-          ok = false;
+            (!dev::mbar_wait(dev::smem_u32(&raw_empty[rs]), ((i / kRawStages) - 1) & 1, p.status) ||
+             *abort_v)) {
+          *abort_v = 1;
           break;
         }
-        if (*abort_v) { ok = false; break; }
         const uint32_t rb = raw_base + rs * kRawBytes;
         const uint32_t fb = dev::smem_u32(&raw_full[rs]);
         dev::mbar_arrive_expect_tx(fb, kRawBytes);
@@ -200,26 +216,26 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_int4_tc_kernel(const __grid_
           dev::tma_load_2d_hint(rb + kRawWBytes, &seg.ts, kc * 8, row0, fb, pol);
         }
         ++raw_issued;
-        for (int a = 0; a < 4; ++a) {
-          const int j = 4 * i + a;
-          const int xs = j % kXStages;
-          if (j >= kXStages &&
-              !dev::mbar_wait(dev::smem_u32(&x_empty[xs]), ((j / kXStages) - 1) & 1, p.status)) {
-            ok = false;
-            break;
-          }
-          if (*abort_v) { ok = false; break; }
-          const uint32_t xb = dev::smem_u32(&x_full[xs]);
-          dev::mbar_arrive_expect_tx(xb, xbytes);
-          dev::tma_load_2d(x_base + xs * kXMaxBytes, &p.tx, kc * 256 + 64 * a, p.t0, xb);
-          ++x_issued;
-        }
       }
-      if (!ok) *abort_v = 1;
-      // drain: wait (bounded) for the last fill of every stage that was filled
       for (int st = 0; st < kRawStages && st < raw_issued; ++st) {
         const int last = ((raw_issued - 1 - st) / kRawStages) * kRawStages + st;
         dev::mbar_wait(dev::smem_u32(&raw_full[st]), (uint32_t)(last / kRawStages) & 1, nullptr);
+      }
+    } else if (lane == 1) {
+      dev::prefetch_tmap(&p.tx);
+      int x_issued = 0;
+      for (int j = 0; j < natoms; ++j) {
+        const int xs = j % kXStages;
+        if (j >= kXStages &&
+            (!dev::mbar_wait(dev::smem_u32(&x_empty[xs]), ((j / kXStages) - 1) & 1, p.status) ||
+             *abort_v)) {
+          *abort_v = 1;
+          break;
+        }
+        const uint32_t xb = dev::smem_u32(&x_full[xs]);
+        dev::mbar_arrive_expect_tx(xb, xbytes);
+        dev::tma_load_2d(x_base + xs * kXMaxBytes, &p.tx, (kc0 + (j >> 2)) * 256 + 64 * (j & 3), p.t0, xb);
+        ++x_issued;
       }
       for (int st = 0; st < kXStages && st < x_issued; ++st) {
         const int last = ((x_issued - 1 - st) / kXStages) * kXStages + st;
@@ -252,59 +268,52 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_int4_tc_kernel(const __grid_
     }
   } else {
     // ---------------------------------------------------------------- converters
-    const int cv = threadIdx.x - 64;  // 0..255
-    const int t = cv & 127;           // tile row
-    const int half = cv >> 7;         // which 32-input group of each 64-input atom
+    const int cw = warp - 2;                 // 0..15
+    const int grp = cw >> 2;                 // atom within each 256-input chunk = A stage
+    const int cv = ((cw & 3) << 5) | lane;   // 0..127 within the group
+    const int t = cv & 127;                  // tile row; the thread converts both 32-input groups
     bool ok = true;
-    int j = 0;
     for (int i = 0; i < nkc && ok; ++i) {
       const int rs = i % kRawStages;
-      if (!dev::mbar_wait(dev::smem_u32(&raw_full[rs]), (i / kRawStages) & 1, p.status) || *abort_v) {
-        ok = false;
-        break;
-      }
+      ok = dev::mbar_wait(dev::smem_u32(&raw_full[rs]), (i / kRawStages) & 1, p.status) && !*abort_v;
+      if (ok && i >= 1)
+        ok = dev::mbar_wait(dev::smem_u32(&a_empty[grp]), (i - 1) & 1, p.status) && !*abort_v;
+      if (!ok) break;
       const uint32_t rb = raw_base + rs * kRawBytes;
-      const uint4 sc = dev::lds128(rb + kRawWBytes + t * 16);
-      const uint32_t scw[4] = {sc.x, sc.y, sc.z, sc.w};
-      uint4 wv[4];
+      uint32_t scw;  // fp16 scales of groups 2*grp (low half) and 2*grp+1 (high half)
+      asm volatile("ld.shared.b32 %0, [%1];" : "=r"(scw) : "r"(rb + kRawWBytes + t * 16 + grp * 4));
+      const uint4 w0 = dev::lds128(rb + dev::swz128(t, 2 * grp));
+      const uint4 w1 = dev::lds128(rb + dev::swz128(t, 2 * grp + 1));
+      const uint32_t ab = a_base + grp * kABytes + t * 128;
 #pragma unroll
-      for (int a = 0; a < 4; ++a) wv[a] = dev::lds128(rb + dev::swz128(t, 2 * a + half));
-#pragma unroll
-      for (int a = 0; a < 4; ++a) {
-        const int jj4 = j + a;
-        const int as = jj4 % kAStages;
-        if (!ok) continue;
-        if (jj4 >= kAStages &&
-            (!dev::mbar_wait(dev::smem_u32(&a_empty[as]), ((jj4 / kAStages) - 1) & 1, p.status) ||
-             *abort_v)) {
-          ok = false;
-          continue;
-        }
-        const uint32_t ab = a_base + as * kABytes + t * 128;
-        const uint16_t sbits = (uint16_t)(half ? (scw[a] >> 16) : (scw[a] & 0xFFFFu));
+      for (int h = 0; h < 2; ++h) {
+        const uint4 wv = h ? w1 : w0;
+        const uint16_t sbits = (uint16_t)(h ? (scw >> 16) : (scw & 0xFFFFu));
         const float sf = __half2float(__ushort_as_half(sbits));
         const __nv_bfloat162 s2 = __floats2bfloat162_rn(sf, sf);
         __nv_bfloat162 c0[4], c1[4], c2[4], c3[4];
-        codes_of_word(wv[a].x, c0);
-        codes_of_word(wv[a].y, c1);
-        codes_of_word(wv[a].z, c2);
-        codes_of_word(wv[a].w, c3);
+        codes_of_word(wv.x, c0);
+        codes_of_word(wv.y, c1);
+        codes_of_word(wv.z, c2);
+        codes_of_word(wv.w, c3);
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj) {
           __nv_bfloat162 v0 = __hmul2(c0[jj], s2), v1 = __hmul2(c1[jj], s2);
           __nv_bfloat162 v2 = __hmul2(c2[jj], s2), v3 = __hmul2(c3[jj], s2);
-          const uint32_t chunk = (uint32_t)(4 * half + jj);
+          const uint32_t chunk = (uint32_t)(4 * h + jj);
           const uint32_t addr = ab + ((chunk ^ (uint32_t)(t & 7)) << 4);
           asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr),
                        "r"(*reinterpret_cast<uint32_t*>(&v0)), "r"(*reinterpret_cast<uint32_t*>(&v1)),
                        "r"(*reinterpret_cast<uint32_t*>(&v2)), "r"(*reinterpret_cast<uint32_t*>(&v3))
                        : "memory");
         }
-        fence_proxy_async();
-        dev::mbar_arrive(dev::smem_u32(&a_full[as]));
       }
-      j += 4;
-      dev::mbar_arrive(dev::smem_u32(&raw_empty[rs]));
+      fence_proxy_async();
+      __syncwarp();
+      if (lane == 0) {
+        dev::mbar_arrive(dev::smem_u32(&a_full[grp]));
+        dev::mbar_arrive(dev::smem_u32(&raw_empty[rs]));
+      }
     }
     if (!ok) *abort_v = 1;
 
@@ -313,13 +322,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_int4_tc_kernel(const __grid_
     tc_fence_after();
     if (have) {
       const int q = warp & 3;              // TMEM lane quarter this warp may read
-      const int set = (warp - 2) >> 2;     // 0: warps 2-5, 1: warps 6-9
+      const int set = (warp - 2) >> 2;     // 0..3: the converter group of this warp
       const int trow = 32 * q + lane;      // tile row of this thread
       const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16);
       if (!p.swiglu) {
         const int row = row0 + trow;
         float* out = p.part + (long long)split * p.plane + seg.col0 + row;
-        for (int c0 = 32 * set; c0 < p.n_tok; c0 += 64) {
+        for (int c0 = 32 * set; c0 < p.n_tok; c0 += 32 * kConvGroups) {
           uint32_t r[32];
           tmem_ld32(taddr + c0, r);
           if (row < seg.N) {
@@ -332,7 +341,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_int4_tc_kernel(const __grid_
         // rows 0..63 are gate, 64..127 the matching up rows: exchange through smem
         float* xch = reinterpret_cast<float*>(smem_raw + (a_base - dev::smem_u32(smem_raw))) + set * 64 * 33;
         const int n = row0 + (trow & 63);
-        for (int c0 = 32 * set; c0 < p.n_tok; c0 += 64) {
+        for (int c0 = 32 * set; c0 < p.n_tok; c0 += 32 * kConvGroups) {
           uint32_t r[32];
           tmem_ld32(taddr + c0, r);
           if (q >= 2) {
