@@ -8,23 +8,26 @@
 //
 // One CTA = 128 weight rows x up to 256 tokens (one tcgen05.mma M=128, N<=256
 // tile, K = 16 per instruction), over a range of the K dimension (split-K for
-// narrow projections).  Warp roles:
-//   warp 0     TMA producer: int4 tile + fp16 scales (256 inputs per stage,
-//              128B-swizzled, 2 stages) and activation tiles (64 inputs x N
-//              tokens, 128B-swizzled K-major, 3 stages);
+// narrow projections).  The pipeline stage is 128 inputs, so the MMA thread
+// issues 8 MMAs (1024 tensor cycles at N=256) per pair of barrier waits: a
+// single issuing thread pays ~100-250 cycles per wait and ~60 per MMA, so
+// smaller stages leave the tensor pipe idle.  Warp roles:
+//   warp 0     lane 0 streams int4 tiles (128 inputs x 128 rows, 64B-swizzled,
+//              3 stages, prefetched into L2 two stages ahead), lane 1 streams
+//              activation tiles (128 inputs x N tokens as two 128B-swizzled
+//              K-major atoms, 2 stages); the two rings are independent;
 //   warp 1     allocates the TMEM accumulator; one thread issues tcgen05.mma
 //              and tcgen05.commit (which frees the smem stages it read);
 //   warps 2-17 converters: int4 codes -> bf16 weights (code * scale, exact for
-//              scales with at most 8 significant bits) written as 128B-swizzled
-//              K-major A tiles.  Four groups of four warps: group g converts
-//              atom g (inputs 64g..64g+63) of every 256-input chunk into its
-//              own A stage, so four atoms are in flight at once and the latency
-//              of one conversion (dequant, stores, proxy fence) is overlapped;
-//              thread = (tile row, one of the atom's two 32-input groups).
-//              Then the epilogue, the four groups taking 32-token chunks in
-//              turn: tcgen05.ld of the accumulator, and either fp32 partial
-//              sums (reduced row-wise by the epilogue kernels) or, for the
-//              gate|up projection, the fused SwiGLU product silu(gate) * up.
+//              scales with at most 8 significant bits; the fp16 scales are read
+//              from global memory) written as 128B-swizzled K-major A tiles.
+//              Two groups of eight warps, one per A stage (stages alternate),
+//              so one stage is converted while the other feeds the MMAs;
+//              thread = (tile row, one 64-input half of the stage).
+//              Then the epilogue, four sets of four warps taking 32-token
+//              chunks in turn: tcgen05.ld of the accumulator, and either fp32
+//              partial sums (reduced row-wise by the epilogue kernels) or, for
+//              the gate|up projection, the fused SwiGLU product silu(gate)*up.
 // Every wait is bounded; on a timeout the CTA records it in the status word,
 // drains its own copies and frees its TMEM before returning.
 #include "kvr_internal.cuh"
@@ -33,20 +36,20 @@ namespace kvr {
 
 namespace {
 
-constexpr int kConvGroups = 4;                  // one per 64-input atom of a 256-input chunk
-constexpr int kConvWarps = 4 * kConvGroups;      // 4 warps (128 rows x 2 groups) per atom
+constexpr int kConvGroups = 2;                  // one per A stage
+constexpr int kGroupWarps = 8;                   // 128 rows x two 64-input halves
+constexpr int kConvWarps = kConvGroups * kGroupWarps;
 constexpr int kThreads = 64 + 32 * kConvWarps;   // + producer warp + MMA warp
 constexpr int kRawStages = 3;
-constexpr int kPrefetch = 2;   // int4 chunks prefetched into L2 ahead of their TMA load
-constexpr int kAStages = 4;
-constexpr int kXStages = 3;
-constexpr int kRawWBytes = 128 * 128;   // 128 rows x 256 inputs of int4
-constexpr int kRawSBytes = 128 * 16;    // 128 rows x 8 fp16 scales
-constexpr int kRawBytes = kRawWBytes + kRawSBytes;
-constexpr int kABytes = 128 * 128;      // 128 rows x 64 inputs bf16
-constexpr int kXMaxBytes = 256 * 128;   // 256 tokens x 64 inputs bf16
+constexpr int kStages = 2;                       // A and activation stages
+constexpr int kPrefetch = 2;                     // int4 stages prefetched into L2 ahead
+constexpr int kRawBytes = 128 * 64;              // 128 rows x 128 inputs of int4
+constexpr int kABytes = 128 * 128 * 2;           // 128 rows x 128 inputs bf16 (2 atoms)
+constexpr int kAAtom = 128 * 128;                // one 64-input atom of A
+constexpr int kXAtom = 256 * 128;                // one 64-input atom of up to 256 tokens
+constexpr int kXBytes = 2 * kXAtom;
 constexpr int kTmemCols = 256;
-constexpr int kSmem = kRawStages * kRawBytes + kAStages * kABytes + kXStages * kXMaxBytes + 1024;
+constexpr int kSmem = kRawStages * kRawBytes + kStages * kABytes + kStages * kXBytes + 1024;
 
 __device__ __forceinline__ void fence_proxy_async() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -118,8 +121,8 @@ __device__ __forceinline__ void codes_of_word(uint32_t w, __nv_bfloat162 out[4])
 __global__ void __launch_bounds__(kThreads, 1) gemm_int4_tc_kernel(const __grid_constant__ GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t raw_full[kRawStages], raw_empty[kRawStages];
-  __shared__ __align__(8) uint64_t a_full[kAStages], a_empty[kAStages];
-  __shared__ __align__(8) uint64_t x_full[kXStages], x_empty[kXStages];
+  __shared__ __align__(8) uint64_t a_full[kStages], a_empty[kStages];
+  __shared__ __align__(8) uint64_t x_full[kStages], x_empty[kStages];
   __shared__ __align__(8) uint64_t acc_full;
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
@@ -128,10 +131,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_int4_tc_kernel(const __grid_
   const uint32_t base = (dev::smem_u32(smem_raw) + 1023u) & ~1023u;
   const uint32_t raw_base = base;
   const uint32_t a_base = raw_base + kRawStages * kRawBytes;
-  const uint32_t x_base = a_base + kAStages * kABytes;
+  const uint32_t x_base = a_base + kStages * kABytes;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  // tile -> segment / rows; split -> range of 256-input chunks
+  // tile -> segment / rows; split -> range of 128-input stages
   const int tile = blockIdx.x;
   int s = 0;
   while (s + 1 < p.nseg && tile >= p.seg[s + 1].tile0) ++s;
@@ -142,19 +145,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_int4_tc_kernel(const __grid_
   const int kc0 = (int)((long long)split * p.kchunks / p.ksplit);
   const int kc1 = (int)((long long)(split + 1) * p.kchunks / p.ksplit);
   const int nkc = kc1 - kc0;
-  const int natoms = 4 * nkc;
-  const uint32_t xbytes = (uint32_t)p.xrows * 128u;
+  const uint32_t xbytes = 2u * (uint32_t)p.xrows * 128u;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kRawStages; ++i) {
       dev::mbar_init(dev::smem_u32(&raw_full[i]), 1);
-      dev::mbar_init(dev::smem_u32(&raw_empty[i]), kConvWarps);
+      dev::mbar_init(dev::smem_u32(&raw_empty[i]), kGroupWarps);
     }
-    for (int i = 0; i < kAStages; ++i) {
-      dev::mbar_init(dev::smem_u32(&a_full[i]), kConvWarps / kConvGroups);
+    for (int i = 0; i < kStages; ++i) {
+      dev::mbar_init(dev::smem_u32(&a_full[i]), kGroupWarps);
       dev::mbar_init(dev::smem_u32(&a_empty[i]), 1);
-    }
-    for (int i = 0; i < kXStages; ++i) {
       dev::mbar_init(dev::smem_u32(&x_full[i]), 1);
       dev::mbar_init(dev::smem_u32(&x_empty[i]), 1);
     }
@@ -175,25 +175,24 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_int4_tc_kernel(const __grid_
 
   if (warp == 0) {
     // ---------------------------------------------------------------- producers
-    // lane 0 streams int4 tiles + scales, lane 1 streams activation tiles; the
-    // two rings are independent so neither stream waits behind the other.
     if (lane == 0) {
-      dev::prefetch_tmap(&seg.tw);
-      dev::prefetch_tmap(&seg.ts);
+      dev::prefetch_tmap(&p.seg[0].tw);
+      if (p.swiglu) dev::prefetch_tmap(&p.seg[1].tw);
+      else dev::prefetch_tmap(&seg.tw);
       const uint64_t pol = dev::policy_evict_first();
-      auto prefetch_chunk = [&](int i) {
-        const int kc = kc0 + i;
+      auto prefetch_stage = [&](int i) {
+        const int x = (kc0 + i) * 64;
         if (p.swiglu) {
-          dev::tma_prefetch_2d(&p.seg[0].tw, kc * 128, row0);
-          dev::tma_prefetch_2d(&p.seg[1].tw, kc * 128, row0);
+          dev::tma_prefetch_2d(&p.seg[0].tw, x, row0);
+          dev::tma_prefetch_2d(&p.seg[1].tw, x, row0);
         } else {
-          dev::tma_prefetch_2d(&seg.tw, kc * 128, row0);
+          dev::tma_prefetch_2d(&seg.tw, x, row0);
         }
       };
-      for (int i = 0; i < kPrefetch && i < nkc; ++i) prefetch_chunk(i);
-      int raw_issued = 0;
+      for (int i = 0; i < kPrefetch && i < nkc; ++i) prefetch_stage(i);
+      int issued = 0;
       for (int i = 0; i < nkc; ++i) {
-        if (i + kPrefetch < nkc) prefetch_chunk(i + kPrefetch);
+        if (i + kPrefetch < nkc) prefetch_stage(i + kPrefetch);
         const int rs = i % kRawStages;
         if (i >= kRawStages &&
             (!dev::mbar_wait(dev::smem_u32(&raw_empty[rs]), ((i / kRawStages) - 1) & 1, p.status) ||
@@ -204,42 +203,39 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_int4_tc_kernel(const __grid_
         const uint32_t rb = raw_base + rs * kRawBytes;
         const uint32_t fb = dev::smem_u32(&raw_full[rs]);
         dev::mbar_arrive_expect_tx(fb, kRawBytes);
-        const int kc = kc0 + i;
+        const int x = (kc0 + i) * 64;
         if (p.swiglu) {
-          const GemmSeg& up = p.seg[1];
-          dev::tma_load_2d_hint(rb, &p.seg[0].tw, kc * 128, row0, fb, pol);
-          dev::tma_load_2d_hint(rb + kRawWBytes / 2, &up.tw, kc * 128, row0, fb, pol);
-          dev::tma_load_2d_hint(rb + kRawWBytes, &p.seg[0].ts, kc * 8, row0, fb, pol);
-          dev::tma_load_2d_hint(rb + kRawWBytes + kRawSBytes / 2, &up.ts, kc * 8, row0, fb, pol);
+          dev::tma_load_2d_hint(rb, &p.seg[0].tw, x, row0, fb, pol);
+          dev::tma_load_2d_hint(rb + kRawBytes / 2, &p.seg[1].tw, x, row0, fb, pol);
         } else {
-          dev::tma_load_2d_hint(rb, &seg.tw, kc * 128, row0, fb, pol);
-          dev::tma_load_2d_hint(rb + kRawWBytes, &seg.ts, kc * 8, row0, fb, pol);
+          dev::tma_load_2d_hint(rb, &seg.tw, x, row0, fb, pol);
         }
-        ++raw_issued;
+        ++issued;
       }
-      for (int st = 0; st < kRawStages && st < raw_issued; ++st) {
-        const int last = ((raw_issued - 1 - st) / kRawStages) * kRawStages + st;
+      for (int st = 0; st < kRawStages && st < issued; ++st) {
+        const int last = ((issued - 1 - st) / kRawStages) * kRawStages + st;
         dev::mbar_wait(dev::smem_u32(&raw_full[st]), (uint32_t)(last / kRawStages) & 1, nullptr);
       }
     } else if (lane == 1) {
       dev::prefetch_tmap(&p.tx);
-      int x_issued = 0;
-      for (int j = 0; j < natoms; ++j) {
-        const int xs = j % kXStages;
-        if (j >= kXStages &&
-            (!dev::mbar_wait(dev::smem_u32(&x_empty[xs]), ((j / kXStages) - 1) & 1, p.status) ||
-             *abort_v)) {
+      int issued = 0;
+      for (int i = 0; i < nkc; ++i) {
+        const int st = i & 1;
+        if (i >= kStages &&
+            (!dev::mbar_wait(dev::smem_u32(&x_empty[st]), ((i >> 1) - 1) & 1, p.status) || *abort_v)) {
           *abort_v = 1;
           break;
         }
-        const uint32_t xb = dev::smem_u32(&x_full[xs]);
+        const uint32_t xb = dev::smem_u32(&x_full[st]);
         dev::mbar_arrive_expect_tx(xb, xbytes);
-        dev::tma_load_2d(x_base + xs * kXMaxBytes, &p.tx, (kc0 + (j >> 2)) * 256 + 64 * (j & 3), p.t0, xb);
-        ++x_issued;
+        const uint32_t dst = x_base + st * kXBytes;
+        dev::tma_load_2d(dst, &p.tx, (kc0 + i) * 128, p.t0, xb);
+        dev::tma_load_2d(dst + kXAtom, &p.tx, (kc0 + i) * 128 + 64, p.t0, xb);
+        ++issued;
       }
-      for (int st = 0; st < kXStages && st < x_issued; ++st) {
-        const int last = ((x_issued - 1 - st) / kXStages) * kXStages + st;
-        dev::mbar_wait(dev::smem_u32(&x_full[st]), (uint32_t)(last / kXStages) & 1, nullptr);
+      for (int st = 0; st < kStages && st < issued; ++st) {
+        const int last = ((issued - 1 - st) / kStages) * kStages + st;
+        dev::mbar_wait(dev::smem_u32(&x_full[st]), (uint32_t)(last / kStages) & 1, nullptr);
       }
     }
   } else if (warp == 1) {
@@ -247,44 +243,56 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_int4_tc_kernel(const __grid_
     if (lane == 0) {
       const uint32_t idesc = idesc_bf16(128, p.n_tok);
       bool ok = true;
-      for (int j = 0; j < natoms; ++j) {
-        const int as = j % kAStages, xs = j % kXStages;
-        if (!dev::mbar_wait(dev::smem_u32(&a_full[as]), (j / kAStages) & 1, p.status) ||
-            !dev::mbar_wait(dev::smem_u32(&x_full[xs]), (j / kXStages) & 1, p.status) || *abort_v) {
+      for (int i = 0; i < nkc; ++i) {
+        const int st = i & 1;
+        if (!dev::mbar_wait(dev::smem_u32(&a_full[st]), (i >> 1) & 1, p.status) ||
+            !dev::mbar_wait(dev::smem_u32(&x_full[st]), (i >> 1) & 1, p.status) || *abort_v) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint64_t ad = sw128_desc(a_base + as * kABytes);
-        const uint64_t bd = sw128_desc(x_base + xs * kXMaxBytes);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          mma_f16(tmem, ad + 2 * kk, bd + 2 * kk, idesc, (j > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(dev::smem_u32(&a_empty[as]));
-        mma_commit(dev::smem_u32(&x_empty[xs]));
+        for (int atom = 0; atom < 2; ++atom) {
+          const uint64_t ad = sw128_desc(a_base + st * kABytes + atom * kAAtom);
+          const uint64_t bd = sw128_desc(x_base + st * kXBytes + atom * kXAtom);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_f16(tmem, ad + 2 * kk, bd + 2 * kk, idesc, (i > 0 || atom > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(dev::smem_u32(&a_empty[st]));
+        mma_commit(dev::smem_u32(&x_empty[st]));
       }
       if (!ok) *abort_v = 1;
       mma_commit(dev::smem_u32(&acc_full));
     }
   } else {
     // ---------------------------------------------------------------- converters
-    const int cw = warp - 2;                 // 0..15
-    const int grp = cw >> 2;                 // atom within each 256-input chunk = A stage
-    const int cv = ((cw & 3) << 5) | lane;   // 0..127 within the group
-    const int t = cv & 127;                  // tile row; the thread converts both 32-input groups
+    const int cw = warp - 2;                      // 0..15
+    const int grp = cw / kGroupWarps;             // A stage this group fills
+    const int cv = ((cw % kGroupWarps) << 5) | lane;  // 0..255
+    const int t = cv & 127;                       // tile row
+    const int hq = cv >> 7;                       // 64-input half of the stage
+    // fp16 scales of this row: gate / up rows for the SwiGLU tile
+    const GemmSeg& sseg = (p.swiglu && t >= 64) ? p.seg[1] : seg;
+    const int srow = p.swiglu ? row0 + (t & 63) : row0 + t;
+    const bool srow_ok = srow < sseg.N;
+    const int G = p.K / 32;
+    const uint32_t* sptr = reinterpret_cast<const uint32_t*>(sseg.scales + (long long)(srow_ok ? srow : 0) * G);
     bool ok = true;
-    for (int i = 0; i < nkc && ok; ++i) {
+    for (int i = grp; i < nkc; i += kConvGroups) {
       const int rs = i % kRawStages;
+      // scales of groups 4*(kc0+i) + 2*hq and +1 (one aligned 32-bit load)
+      const uint32_t scw = srow_ok ? __ldg(sptr + 2 * (kc0 + i) + hq) : 0u;
       ok = dev::mbar_wait(dev::smem_u32(&raw_full[rs]), (i / kRawStages) & 1, p.status) && !*abort_v;
-      if (ok && i >= 1)
-        ok = dev::mbar_wait(dev::smem_u32(&a_empty[grp]), (i - 1) & 1, p.status) && !*abort_v;
+      if (ok && i >= kConvGroups)
+        ok = dev::mbar_wait(dev::smem_u32(&a_empty[grp]), ((i / kConvGroups) - 1) & 1, p.status) &&
+             !*abort_v;
       if (!ok) break;
-      const uint32_t rb = raw_base + rs * kRawBytes;
-      uint32_t scw;  // fp16 scales of groups 2*grp (low half) and 2*grp+1 (high half)
-      asm volatile("ld.shared.b32 %0, [%1];" : "=r"(scw) : "r"(rb + kRawWBytes + t * 16 + grp * 4));
-      const uint4 w0 = dev::lds128(rb + dev::swz128(t, 2 * grp));
-      const uint4 w1 = dev::lds128(rb + dev::swz128(t, 2 * grp + 1));
-      const uint32_t ab = a_base + grp * kABytes + t * 128;
+      const uint32_t rb = raw_base + rs * kRawBytes + t * 64;
+      const uint32_t sw = (uint32_t)((t >> 1) & 3);  // 64-byte swizzle of this row
+      const uint4 w0 = dev::lds128(rb + (((uint32_t)(2 * hq) ^ sw) << 4));
+      const uint4 w1 = dev::lds128(rb + (((uint32_t)(2 * hq + 1) ^ sw) << 4));
+      const uint32_t ab = a_base + grp * kABytes + hq * kAAtom + t * 128;
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const uint4 wv = h ? w1 : w0;
@@ -322,13 +330,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_int4_tc_kernel(const __grid_
     tc_fence_after();
     if (have) {
       const int q = warp & 3;              // TMEM lane quarter this warp may read
-      const int set = (warp - 2) >> 2;     // 0..3: the converter group of this warp
+      const int set = cw >> 2;             // 0..3
       const int trow = 32 * q + lane;      // tile row of this thread
       const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16);
       if (!p.swiglu) {
         const int row = row0 + trow;
         float* out = p.part + (long long)split * p.plane + seg.col0 + row;
-        for (int c0 = 32 * set; c0 < p.n_tok; c0 += 32 * kConvGroups) {
+        for (int c0 = 32 * set; c0 < p.n_tok; c0 += 128) {
           uint32_t r[32];
           tmem_ld32(taddr + c0, r);
           if (row < seg.N) {
@@ -341,7 +349,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_int4_tc_kernel(const __grid_
         // rows 0..63 are gate, 64..127 the matching up rows: exchange through smem
         float* xch = reinterpret_cast<float*>(smem_raw + (a_base - dev::smem_u32(smem_raw))) + set * 64 * 33;
         const int n = row0 + (trow & 63);
-        for (int c0 = 32 * set; c0 < p.n_tok; c0 += 32 * kConvGroups) {
+        for (int c0 = 32 * set; c0 < p.n_tok; c0 += 128) {
           uint32_t r[32];
           tmem_ld32(taddr + c0, r);
           if (q >= 2) {

@@ -120,8 +120,10 @@ ScratchLayout scratch_layout(const kvr_config* c) {
 
 struct WKey {
   const void* p;
-  int N, K, box;
-  bool operator<(const WKey& o) const { return std::tie(p, N, K, box) < std::tie(o.p, o.N, o.K, o.box); }
+  int N, K, box, inner;
+  bool operator<(const WKey& o) const {
+    return std::tie(p, N, K, box, inner) < std::tie(o.p, o.N, o.K, o.box, o.inner);
+  }
 };
 struct WMap {
   CUtensorMap w, s;
@@ -254,13 +256,16 @@ bool act_maps(CUtensorMap out[6], const void* buf, int K, int rows) {
   return true;
 }
 
-const WMap* weight_map(kvr_ctx* c, const void* w, const void* s, int N, int K, int box = kGemvRows) {
-  WKey key{w, N, K, box};
+// int4 weight (and scale) tensor maps: box of `box` rows x `inner` bytes (128: 128-byte
+// swizzle, GEMV; 64: 64-byte swizzle, tcgen05 GEMM), cached per matrix.
+const WMap* weight_map(kvr_ctx* c, const void* w, const void* s, int N, int K, int box = kGemvRows,
+                       int inner = 128) {
+  WKey key{w, N, K, box, inner};
   auto it = c->wmaps.find(key);
   if (it != c->wmaps.end()) return &it->second;
   WMap m;
-  if (!encode_2d(&m.w, CU_TENSOR_MAP_DATA_TYPE_UINT8, w, K / 2, N, K / 2, 128, box,
-                 CU_TENSOR_MAP_SWIZZLE_128B))
+  if (!encode_2d(&m.w, CU_TENSOR_MAP_DATA_TYPE_UINT8, w, K / 2, N, K / 2, inner, box,
+                 inner == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B))
     return nullptr;
   if (!encode_2d(&m.s, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, s, K / 32, N, (uint64_t)K / 32 * 2, 8,
                  box, CU_TENSOR_MAP_SWIZZLE_NONE))
@@ -287,19 +292,20 @@ int project_gemm(kvr_ctx* c, cudaStream_t st, const Seg* segs, int nseg, const C
   GemmParams p;
   memset(&p, 0, sizeof p);
   p.K = K;
-  p.kchunks = K / kGemvKStep;
+  p.kchunks = K / 128;
   p.status = c->status;
   p.part = c->part;
   p.z = c->z;
   p.F = c->cfg.ffn;
   int col = 0, tiles = 0;
   if (swiglu) {
-    const WMap* g = weight_map(c, segs[0].w, segs[0].s, segs[0].N, K, 64);
-    const WMap* u = weight_map(c, segs[1].w, segs[1].s, segs[1].N, K, 64);
+    const WMap* g = weight_map(c, segs[0].w, segs[0].s, segs[0].N, K, 64, 64);
+    const WMap* u = weight_map(c, segs[1].w, segs[1].s, segs[1].N, K, 64, 64);
     if (!g || !u) return fail(c, KVR_ERR_CUDA, "cuTensorMapEncodeTiled failed for a weight matrix");
     p.nseg = 1;
-    p.seg[0].tw = g->w; p.seg[0].ts = g->s;
-    p.seg[1].tw = u->w; p.seg[1].ts = u->s;
+    p.seg[0].tw = g->w; p.seg[0].scales = static_cast<const __half*>(segs[0].s);
+    p.seg[1].tw = u->w; p.seg[1].scales = static_cast<const __half*>(segs[1].s);
+    p.seg[1].N = segs[1].N;
     p.seg[0].N = segs[0].N;
     p.seg[0].tiles = (segs[0].N + 63) / 64;
     tiles = p.seg[0].tiles;
@@ -307,10 +313,10 @@ int project_gemm(kvr_ctx* c, cudaStream_t st, const Seg* segs, int nseg, const C
   } else {
     p.nseg = nseg;
     for (int i = 0; i < nseg; ++i) {
-      const WMap* wm = weight_map(c, segs[i].w, segs[i].s, segs[i].N, K, 128);
+      const WMap* wm = weight_map(c, segs[i].w, segs[i].s, segs[i].N, K, 128, 64);
       if (!wm) return fail(c, KVR_ERR_CUDA, "cuTensorMapEncodeTiled failed for a weight matrix");
       GemmSeg& g = p.seg[i];
-      g.tw = wm->w; g.ts = wm->s;
+      g.tw = wm->w; g.scales = static_cast<const __half*>(segs[i].s);
       g.N = segs[i].N; g.col0 = col; g.tile0 = tiles; g.tiles = (segs[i].N + 127) / 128;
       col += segs[i].N;
       tiles += g.tiles;

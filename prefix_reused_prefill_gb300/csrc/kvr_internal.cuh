@@ -76,8 +76,8 @@ struct GemvParams {
 };
 
 struct GemmSeg {
-  CUtensorMap tw;   // uint8 [N][K/2], box {128 B, 128 rows} (64 rows for SwiGLU), 128B swizzle
-  CUtensorMap ts;   // fp16 scales [N][K/32], box {8, 128 rows} (64 rows for SwiGLU)
+  CUtensorMap tw;        // uint8 [N][K/2], box {64 B, 128 rows} (64 rows for SwiGLU), 64B swizzle
+  const __half* scales;  // fp16 [N][K/32]
   int N;
   int col0;
   int tile0;
@@ -89,7 +89,7 @@ struct GemmParams {
   CUtensorMap tx;   // activations bf16 [max_rows][K], box {64, xrows}, 128B swizzle
   int nseg;
   int K;
-  int kchunks;      // K / 256
+  int kchunks;      // K / 128 (pipeline stages)
   int ksplit;
   int n_tok;        // MMA N: tokens of this pass rounded up to 16 (<= 256)
   int xrows;        // activation box rows (64, 128 or 256) >= n_tok
