@@ -11,19 +11,21 @@
 // narrow projections).  The pipeline stage is 128 inputs, so the MMA thread
 // issues 8 MMAs (1024 tensor cycles at N=256) per pair of barrier waits: a
 // single issuing thread pays ~100-250 cycles per wait and ~60 per MMA, so
-// smaller stages leave the tensor pipe idle.  Warp roles:
+// smaller stages leave the tensor pipe idle.  The dequantised weights (the A
+// operand) live in tensor memory, which keeps shared memory for a 3-deep
+// activation ring.  Warp roles:
 //   warp 0     lane 0 streams int4 tiles (128 inputs x 128 rows, 64B-swizzled,
-//              3 stages, prefetched into L2 two stages ahead), lane 1 streams
+//              4 stages, prefetched into L2 two stages ahead), lane 1 streams
 //              activation tiles (128 inputs x N tokens as two 128B-swizzled
-//              K-major atoms, 2 stages); the two rings are independent;
+//              K-major atoms, 3 stages); the two rings are independent;
 //   warp 1     allocates the TMEM accumulator; one thread issues tcgen05.mma
 //              and tcgen05.commit (which frees the smem stages it read);
 //   warps 2-17 converters: int4 codes -> bf16 weights (code * scale, exact for
 //              scales with at most 8 significant bits; the fp16 scales are read
-//              from global memory) written as 128B-swizzled K-major A tiles.
-//              Two groups of eight warps, one per A stage (stages alternate),
-//              so one stage is converted while the other feeds the MMAs;
-//              thread = (tile row, one 64-input half of the stage).
+//              from global memory) stored straight into a TMEM A stage with one
+//              tcgen05.st per thread (thread = TMEM lane / tile row, one
+//              64-input half of the stage).  Two groups of eight warps take
+//              alternate stages of a 4-deep A ring in TMEM.
 //              Then the epilogue, four sets of four warps taking 32-token
 //              chunks in turn: tcgen05.ld of the accumulator, and either fp32
 //              partial sums (reduced row-wise by the epilogue kernels) or, for
@@ -40,20 +42,21 @@ constexpr int kConvGroups = 2;                  // one per A stage
 constexpr int kGroupWarps = 8;                   // 128 rows x two 64-input halves
 constexpr int kConvWarps = kConvGroups * kGroupWarps;
 constexpr int kThreads = 64 + 32 * kConvWarps;   // + producer warp + MMA warp
-constexpr int kRawStages = 3;
-constexpr int kStages = 2;                       // A and activation stages
+// The two converter groups take alternate stages, so the int4 ring has an even
+// number of slots: each slot is then always consumed by the same group, one use
+// after the other (a group never waits on a slot whose previous use belongs to
+// the other group, which the mbarrier phase parity could not tell apart).
+constexpr int kRawStages = 4;
+constexpr int kStages = 3;                       // activation stages (shared memory)
+constexpr int kAStages = 4;                      // A stages (tensor memory)
 constexpr int kPrefetch = 2;                     // int4 stages prefetched into L2 ahead
 constexpr int kRawBytes = 128 * 64;              // 128 rows x 128 inputs of int4
-constexpr int kABytes = 128 * 128 * 2;           // 128 rows x 128 inputs bf16 (2 atoms)
-constexpr int kAAtom = 128 * 128;                // one 64-input atom of A
 constexpr int kXAtom = 256 * 128;                // one 64-input atom of up to 256 tokens
 constexpr int kXBytes = 2 * kXAtom;
-constexpr int kTmemCols = 256;
-constexpr int kSmem = kRawStages * kRawBytes + kStages * kABytes + kStages * kXBytes + 1024;
+constexpr int kTmemCols = 512;                   // accumulator 256 + 4 A stages x 64 columns
+constexpr uint32_t kACol = 256;                  // first A stage column; stage s at kACol + 64 s
+constexpr int kSmem = kRawStages * kRawBytes + kStages * kXBytes + 1024;
 
-__device__ __forceinline__ void fence_proxy_async() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
@@ -73,13 +76,26 @@ __device__ __forceinline__ uint32_t idesc_bf16(int M, int N) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
-__device__ __forceinline__ void mma_f16(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc,
-                                        uint32_t accumulate) {
+// D (TMEM) += A (TMEM) * B (shared memory)
+__device__ __forceinline__ void mma_f16_ta(uint32_t tmem_d, uint32_t tmem_a, uint64_t b, uint32_t idesc,
+                                           uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(tmem_d),
-      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(tmem_d),
+      "r"(tmem_a), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t r[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
+      "%12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, "
+      "%30, %31, %32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]),
+      "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]),
+      "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
       : "memory");
 }
 
@@ -121,7 +137,7 @@ __device__ __forceinline__ void codes_of_word(uint32_t w, __nv_bfloat162 out[4])
 __global__ void __launch_bounds__(kThreads, 1) gemm_int4_tc_kernel(const __grid_constant__ GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t raw_full[kRawStages], raw_empty[kRawStages];
-  __shared__ __align__(8) uint64_t a_full[kStages], a_empty[kStages];
+  __shared__ __align__(8) uint64_t a_full[kAStages], a_empty[kAStages];
   __shared__ __align__(8) uint64_t x_full[kStages], x_empty[kStages];
   __shared__ __align__(8) uint64_t acc_full;
   __shared__ uint32_t tmem_slot;
@@ -130,8 +146,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_int4_tc_kernel(const __grid_
 
   const uint32_t base = (dev::smem_u32(smem_raw) + 1023u) & ~1023u;
   const uint32_t raw_base = base;
-  const uint32_t a_base = raw_base + kRawStages * kRawBytes;
-  const uint32_t x_base = a_base + kStages * kABytes;
+  const uint32_t x_base = raw_base + kRawStages * kRawBytes;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   // tile -> segment / rows; split -> range of 128-input stages
@@ -152,9 +167,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_int4_tc_kernel(const __grid_
       dev::mbar_init(dev::smem_u32(&raw_full[i]), 1);
       dev::mbar_init(dev::smem_u32(&raw_empty[i]), kGroupWarps);
     }
-    for (int i = 0; i < kStages; ++i) {
+    for (int i = 0; i < kAStages; ++i) {
       dev::mbar_init(dev::smem_u32(&a_full[i]), kGroupWarps);
       dev::mbar_init(dev::smem_u32(&a_empty[i]), 1);
+    }
+    for (int i = 0; i < kStages; ++i) {
       dev::mbar_init(dev::smem_u32(&x_full[i]), 1);
       dev::mbar_init(dev::smem_u32(&x_empty[i]), 1);
     }
@@ -220,9 +237,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_int4_tc_kernel(const __grid_
       dev::prefetch_tmap(&p.tx);
       int issued = 0;
       for (int i = 0; i < nkc; ++i) {
-        const int st = i & 1;
+        const int st = i % kStages;
         if (i >= kStages &&
-            (!dev::mbar_wait(dev::smem_u32(&x_empty[st]), ((i >> 1) - 1) & 1, p.status) || *abort_v)) {
+            (!dev::mbar_wait(dev::smem_u32(&x_empty[st]), ((i / kStages) - 1) & 1, p.status) || *abort_v)) {
           *abort_v = 1;
           break;
         }
@@ -244,23 +261,24 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_int4_tc_kernel(const __grid_
       const uint32_t idesc = idesc_bf16(128, p.n_tok);
       bool ok = true;
       for (int i = 0; i < nkc; ++i) {
-        const int st = i & 1;
-        if (!dev::mbar_wait(dev::smem_u32(&a_full[st]), (i >> 1) & 1, p.status) ||
-            !dev::mbar_wait(dev::smem_u32(&x_full[st]), (i >> 1) & 1, p.status) || *abort_v) {
+        const int xs = i % kStages, as = i % kAStages;
+        if (!dev::mbar_wait(dev::smem_u32(&a_full[as]), (i / kAStages) & 1, p.status) ||
+            !dev::mbar_wait(dev::smem_u32(&x_full[xs]), (i / kStages) & 1, p.status) || *abort_v) {
           ok = false;
           break;
         }
         tc_fence_after();
+        const uint32_t ta = tmem + kACol + 64u * (uint32_t)as;
 #pragma unroll
         for (int atom = 0; atom < 2; ++atom) {
-          const uint64_t ad = sw128_desc(a_base + st * kABytes + atom * kAAtom);
-          const uint64_t bd = sw128_desc(x_base + st * kXBytes + atom * kXAtom);
+          const uint64_t bd = sw128_desc(x_base + xs * kXBytes + atom * kXAtom);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_f16(tmem, ad + 2 * kk, bd + 2 * kk, idesc, (i > 0 || atom > 0 || kk > 0) ? 1u : 0u);
+            mma_f16_ta(tmem, ta + 32u * atom + 8u * kk, bd + 2 * kk, idesc,
+                       (i > 0 || atom > 0 || kk > 0) ? 1u : 0u);
         }
-        mma_commit(dev::smem_u32(&a_empty[st]));
-        mma_commit(dev::smem_u32(&x_empty[st]));
+        mma_commit(dev::smem_u32(&a_empty[as]));
+        mma_commit(dev::smem_u32(&x_empty[xs]));
       }
       if (!ok) *abort_v = 1;
       mma_commit(dev::smem_u32(&acc_full));
@@ -268,31 +286,34 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_int4_tc_kernel(const __grid_
   } else {
     // ---------------------------------------------------------------- converters
     const int cw = warp - 2;                      // 0..15
-    const int grp = cw / kGroupWarps;             // A stage this group fills
-    const int cv = ((cw % kGroupWarps) << 5) | lane;  // 0..255
-    const int t = cv & 127;                       // tile row
-    const int hq = cv >> 7;                       // 64-input half of the stage
+    const int grp = cw / kGroupWarps;             // stages grp, grp+2, ... (A stage i % 4)
+    const int q = warp & 3;                       // TMEM lane quarter this warp may write
+    const int hq = ((cw % kGroupWarps) >> 2) & 1; // 64-input half of the stage
+    const int t = 32 * q + lane;                  // tile row = TMEM lane
     // fp16 scales of this row: gate / up rows for the SwiGLU tile
     const GemmSeg& sseg = (p.swiglu && t >= 64) ? p.seg[1] : seg;
     const int srow = p.swiglu ? row0 + (t & 63) : row0 + t;
     const bool srow_ok = srow < sseg.N;
     const int G = p.K / 32;
     const uint32_t* sptr = reinterpret_cast<const uint32_t*>(sseg.scales + (long long)(srow_ok ? srow : 0) * G);
+    const uint32_t tlane = (uint32_t)(32 * q) << 16;
     bool ok = true;
     for (int i = grp; i < nkc; i += kConvGroups) {
-      const int rs = i % kRawStages;
+      const int rs = i % kRawStages, as = i % kAStages;
       // scales of groups 4*(kc0+i) + 2*hq and +1 (one aligned 32-bit load)
       const uint32_t scw = srow_ok ? __ldg(sptr + 2 * (kc0 + i) + hq) : 0u;
       ok = dev::mbar_wait(dev::smem_u32(&raw_full[rs]), (i / kRawStages) & 1, p.status) && !*abort_v;
-      if (ok && i >= kConvGroups)
-        ok = dev::mbar_wait(dev::smem_u32(&a_empty[grp]), ((i / kConvGroups) - 1) & 1, p.status) &&
-             !*abort_v;
-      if (!ok) break;
+      if (ok && i >= kAStages)
+        ok = dev::mbar_wait(dev::smem_u32(&a_empty[as]), ((i / kAStages) - 1) & 1, p.status) && !*abort_v;
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
       const uint32_t rb = raw_base + rs * kRawBytes + t * 64;
       const uint32_t sw = (uint32_t)((t >> 1) & 3);  // 64-byte swizzle of this row
       const uint4 w0 = dev::lds128(rb + (((uint32_t)(2 * hq) ^ sw) << 4));
       const uint4 w1 = dev::lds128(rb + (((uint32_t)(2 * hq + 1) ^ sw) << 4));
-      const uint32_t ab = a_base + grp * kABytes + hq * kAAtom + t * 128;
+      uint32_t outv[32];   // 64 bf16 inputs of this row, k order, two per column
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const uint4 wv = h ? w1 : w0;
@@ -306,20 +327,21 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_int4_tc_kernel(const __grid_
         codes_of_word(wv.w, c3);
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj) {
+          // inputs 8*jj .. 8*jj+7 of this 32-input group: words 0..3 give pairs (2w, 2w+1)
           __nv_bfloat162 v0 = __hmul2(c0[jj], s2), v1 = __hmul2(c1[jj], s2);
           __nv_bfloat162 v2 = __hmul2(c2[jj], s2), v3 = __hmul2(c3[jj], s2);
-          const uint32_t chunk = (uint32_t)(4 * h + jj);
-          const uint32_t addr = ab + ((chunk ^ (uint32_t)(t & 7)) << 4);
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr),
-                       "r"(*reinterpret_cast<uint32_t*>(&v0)), "r"(*reinterpret_cast<uint32_t*>(&v1)),
-                       "r"(*reinterpret_cast<uint32_t*>(&v2)), "r"(*reinterpret_cast<uint32_t*>(&v3))
-                       : "memory");
+          outv[16 * h + 4 * jj + 0] = *reinterpret_cast<uint32_t*>(&v0);
+          outv[16 * h + 4 * jj + 1] = *reinterpret_cast<uint32_t*>(&v1);
+          outv[16 * h + 4 * jj + 2] = *reinterpret_cast<uint32_t*>(&v2);
+          outv[16 * h + 4 * jj + 3] = *reinterpret_cast<uint32_t*>(&v3);
         }
       }
-      fence_proxy_async();
+      tmem_st32(tmem + tlane + kACol + 64u * (uint32_t)as + 32u * (uint32_t)hq, outv);
+      asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+      tc_fence_before();
       __syncwarp();
       if (lane == 0) {
-        dev::mbar_arrive(dev::smem_u32(&a_full[grp]));
+        dev::mbar_arrive(dev::smem_u32(&a_full[as]));
         dev::mbar_arrive(dev::smem_u32(&raw_empty[rs]));
       }
     }
@@ -329,7 +351,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_int4_tc_kernel(const __grid_
     const bool have = __all_sync(0xffffffffu, dev::mbar_wait(dev::smem_u32(&acc_full), 0, p.status) && !*abort_v);
     tc_fence_after();
     if (have) {
-      const int q = warp & 3;              // TMEM lane quarter this warp may read
       const int set = cw >> 2;             // 0..3
       const int trow = 32 * q + lane;      // tile row of this thread
       const uint32_t taddr = tmem + ((uint32_t)(32 * q) << 16);
@@ -347,7 +368,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_int4_tc_kernel(const __grid_
         }
       } else {
         // rows 0..63 are gate, 64..127 the matching up rows: exchange through smem
-        float* xch = reinterpret_cast<float*>(smem_raw + (a_base - dev::smem_u32(smem_raw))) + set * 64 * 33;
+        float* xch = reinterpret_cast<float*>(smem_raw + (x_base - dev::smem_u32(smem_raw))) + set * 64 * 33;
         const int n = row0 + (trow & 63);
         for (int c0 = 32 * set; c0 < p.n_tok; c0 += 128) {
           uint32_t r[32];
