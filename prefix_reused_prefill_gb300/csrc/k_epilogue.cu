@@ -64,41 +64,85 @@ __global__ void embed_kernel(const __nv_bfloat16* hidden, int H, const __nv_bflo
     a[row * H + k] = __float2bfloat16_rn(h[row * H + k] * rs * __bfloat162float(gain[k]));
 }
 
-__global__ void epi_qkv_kernel(const float* part, long long plane, int ksplit, int ldo, int c0,
-                               int mb, RowMap rows, int Hq, int Hkv, int d, const float2* rope,
-                               __nv_bfloat16* q, __nv_bfloat16* arena, long long k_off,
-                               long long v_off, int cap) {
-  const int half = d / 2;
-  const int heads = Hq + 2 * Hkv;
-  const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  if (idx >= (long long)mb * heads * half) return;
-  const int t = (int)(idx / (heads * half));
-  const int rem = (int)(idx % (heads * half));
-  const int hd = rem / half, j = rem % half;
+// One CTA per (tile of tokens, head): sum the split partials, rotate q/k
+// (pair j, j + d/2), round to bf16; q rows go to the KV-head-major q buffer,
+// K rows to the slot, and V through a shared-memory transpose to the slot's
+// V^T rows so every global write is contiguous.  Thread = (token, 8-pair chunk).
+template <int D>
+__global__ void __launch_bounds__(256) epi_qkv_kernel(const float* part, long long plane, int ksplit,
+                                                      int ldo, int c0, int mb, RowMap rows, int Hq,
+                                                      int Hkv, const float2* rope, __nv_bfloat16* q,
+                                                      __nv_bfloat16* arena, long long k_off,
+                                                      long long v_off, int cap) {
+  constexpr int kHalf = D / 2;
+  constexpr int kChunks = kHalf / 8;          // threads per token
+  constexpr int kTok = 256 / kChunks;         // tokens per CTA
+  __shared__ __nv_bfloat16 vt[kTok][D + 8];
+  const int hd = blockIdx.y;
+  const int tl = threadIdx.x / kChunks, ch = threadIdx.x % kChunks;
+  const int t = blockIdx.x * kTok + tl;
+  const bool live = t < mb;
   const int i = c0 + t;
-  const long long col = (long long)hd * d + j;
-  const float x1 = split_sum(part, plane, ksplit, (long long)t * ldo + col);
-  const float x2 = split_sum(part, plane, ksplit, (long long)t * ldo + col + half);
+  const int j0 = 8 * ch;
+  float x1[8], x2[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) x1[e] = x2[e] = 0.f;
+  if (live) {
+    const float* src = part + (long long)t * ldo + (long long)hd * D + j0;
+    for (int s = 0; s < ksplit; ++s) {
+      const float4 a0 = *reinterpret_cast<const float4*>(src + s * plane);
+      const float4 a1 = *reinterpret_cast<const float4*>(src + s * plane + 4);
+      const float4 b0 = *reinterpret_cast<const float4*>(src + s * plane + kHalf);
+      const float4 b1 = *reinterpret_cast<const float4*>(src + s * plane + kHalf + 4);
+      x1[0] += a0.x; x1[1] += a0.y; x1[2] += a0.z; x1[3] += a0.w;
+      x1[4] += a1.x; x1[5] += a1.y; x1[6] += a1.z; x1[7] += a1.w;
+      x2[0] += b0.x; x2[1] += b0.y; x2[2] += b0.z; x2[3] += b0.w;
+      x2[4] += b1.x; x2[5] += b1.y; x2[6] += b1.z; x2[7] += b1.w;
+    }
+  }
   const int store = rows.P + i;
   if (hd < Hq + Hkv) {
-    const float2 cs = rope[(long long)i * half + j];
-    const float y1 = x1 * cs.x - x2 * cs.y;
-    const float y2 = x2 * cs.x + x1 * cs.y;
-    if (hd < Hq) {
-      const int G = Hq / Hkv;
-      __nv_bfloat16* dst = q + (((long long)(hd / G) * rows.m + i) * G + hd % G) * d;
-      dst[j] = __float2bfloat16_rn(y1);
-      dst[j + half] = __float2bfloat16_rn(y2);
-    } else {
-      __nv_bfloat16* dst = arena + k_off + ((long long)(hd - Hq) * cap + store) * d;
-      dst[j] = __float2bfloat16_rn(y1);
-      dst[j + half] = __float2bfloat16_rn(y2);
+    if (live) {
+      const float4* cs4 = reinterpret_cast<const float4*>(rope + (long long)i * kHalf + j0);
+      float y1[8], y2[8];
+#pragma unroll
+      for (int e = 0; e < 8; e += 2) {
+        const float4 cs = cs4[e / 2];   // (cos, sin) of pairs j0+e and j0+e+1
+        y1[e] = x1[e] * cs.x - x2[e] * cs.y;
+        y2[e] = x2[e] * cs.x + x1[e] * cs.y;
+        y1[e + 1] = x1[e + 1] * cs.z - x2[e + 1] * cs.w;
+        y2[e + 1] = x2[e + 1] * cs.z + x1[e + 1] * cs.w;
+      }
+      __nv_bfloat16* dst;
+      if (hd < Hq) {
+        const int G = Hq / Hkv;
+        dst = q + (((long long)(hd / G) * rows.m + i) * G + hd % G) * D;
+      } else {
+        dst = arena + k_off + ((long long)(hd - Hq) * cap + store) * D;
+      }
+      uint4 lo, hi;
+      lo.x = dev::pack_bf16x2(y1[0], y1[1]); lo.y = dev::pack_bf16x2(y1[2], y1[3]);
+      lo.z = dev::pack_bf16x2(y1[4], y1[5]); lo.w = dev::pack_bf16x2(y1[6], y1[7]);
+      hi.x = dev::pack_bf16x2(y2[0], y2[1]); hi.y = dev::pack_bf16x2(y2[2], y2[3]);
+      hi.z = dev::pack_bf16x2(y2[4], y2[5]); hi.w = dev::pack_bf16x2(y2[6], y2[7]);
+      *reinterpret_cast<uint4*>(dst + j0) = lo;
+      *reinterpret_cast<uint4*>(dst + kHalf + j0) = hi;
     }
   } else {
-    // V is kept transposed in the slot: [Hkv][d][capacity]
-    __nv_bfloat16* dst = arena + v_off + (long long)(hd - Hq - Hkv) * d * cap + store;
-    dst[(long long)j * cap] = __float2bfloat16_rn(x1);
-    dst[(long long)(j + half) * cap] = __float2bfloat16_rn(x2);
+    // V: stage the tile, then write V^T rows [d][positions] of this head
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      vt[tl][j0 + e] = __float2bfloat16_rn(x1[e]);
+      vt[tl][kHalf + j0 + e] = __float2bfloat16_rn(x2[e]);
+    }
+    __syncthreads();
+    const int ntok = min(kTok, mb - (int)blockIdx.x * kTok);
+    const int store0 = rows.P + c0 + blockIdx.x * kTok;
+    __nv_bfloat16* base = arena + v_off + (long long)(hd - Hq - Hkv) * D * cap + store0;
+    for (int idx = threadIdx.x; idx < D * kTok; idx += 256) {
+      const int e = idx / kTok, tt = idx % kTok;
+      if (tt < ntok) base[(long long)e * cap + tt] = vt[tt][e];
+    }
   }
 }
 
@@ -195,9 +239,18 @@ cudaError_t launch_epi_qkv(const float* part, long long plane, int ksplit, int l
                            const RowMap& rows, int Hq, int Hkv, int d, const float2* rope,
                            __nv_bfloat16* q, __nv_bfloat16* arena, long long k_off,
                            long long v_off, int cap, cudaStream_t st) {
-  const long long n = (long long)mb * (Hq + 2 * Hkv) * (d / 2);
-  epi_qkv_kernel<<<blocks_for(n, 256), 256, 0, st>>>(part, plane, ksplit, ldo, c0, mb, rows, Hq,
-                                                     Hkv, d, rope, q, arena, k_off, v_off, cap);
+  const int heads = Hq + 2 * Hkv;
+  if (d == 128) {
+    const dim3 grid((mb + 15) / 16, heads);
+    epi_qkv_kernel<128><<<grid, 256, 0, st>>>(part, plane, ksplit, ldo, c0, mb, rows, Hq, Hkv, rope, q,
+                                              arena, k_off, v_off, cap);
+  } else if (d == 64) {
+    const dim3 grid((mb + 31) / 32, heads);
+    epi_qkv_kernel<64><<<grid, 256, 0, st>>>(part, plane, ksplit, ldo, c0, mb, rows, Hq, Hkv, rope, q,
+                                             arena, k_off, v_off, cap);
+  } else {
+    return cudaErrorInvalidValue;
+  }
   return cudaGetLastError();
 }
 
