@@ -141,6 +141,10 @@ typedef struct kvr_ctx kvr_ctx;
  *     ((((s*L + l)*2 + 1)*Hkv + j)*head_dim + e)*capacity + p   ([head_dim][capacity] per head),
  *   so that both tensor-core operands of P.V are K-major tiles;
  *   followed by the device token mirror int32 [n_slots][capacity].
+ *   kvr_ctx_create zeroes the K/V part once.  Attention reads whole 64-key
+ *   blocks, so positions past a slot's length (weighted by zero) must hold
+ *   finite values: everything the library writes is finite, and K/V a caller
+ *   writes itself (kvr_slot_assign) must be finite too.
  *   kvr_arena_bytes(cfg, n) is the size for n slots (n = cfg->n_slots, or 1
  *   when n_slots is 0).
  * Scratch: activations, partial sums, RoPE tables, the match buffers and the
@@ -268,6 +272,15 @@ int kvr_prefill_branches(kvr_ctx* ctx, int slot, int n_branch, const int* lens,
  * bounded device-side wait gives up.  Returns KVR_ERR_TIMEOUT (and clears the
  * word) if one did. */
 int kvr_sync_status(kvr_ctx* ctx, void* stream);
+
+/* Per-layer trace for checking a long stack one layer at a time.  While a
+ * buffer is set (dev: device float32 [n_layers + 1][max_rows][hidden],
+ * bytes >= that size; NULL clears it), every prefill / verify / branches call
+ * of a full-layer model (attn_only = 0) copies the float32 residual stream of
+ * its m rows into it on the call's stream: entry 0 after the first RMSNorm's
+ * input load, entry l+1 after layer l (row i of entry e at
+ * (e*max_rows + i)*hidden).  Returns KVR_ERR_CAPACITY if bytes is too small. */
+int kvr_trace_set(kvr_ctx* ctx, void* dev, size_t bytes);
 
 /* Per-kernel-class timing with CUDA events recorded on the launch stream.
  * While enabled, every launch is bracketed by an event pair; kvr_profile_read

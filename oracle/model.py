@@ -166,6 +166,38 @@ def layer(dims: Dims, W: Dict[str, np.ndarray], h: np.ndarray, K: np.ndarray, V:
     return h + linear(z, W["wd"])
 
 
+def layer_rows(dims: Dims, W: Dict[str, np.ndarray], h: np.ndarray, K: np.ndarray, V: np.ndarray,
+               rows: List[Row], out_rows: Sequence[int]) -> np.ndarray:
+    """The same layer, evaluated only for the rows listed in out_rows.
+
+    A row's output depends on the other rows only through their K/V, so K/V
+    are computed (and written into K, V) for every row, and the query,
+    attention, O projection and FFN only for out_rows.  Returns
+    [len(out_rows)][H].  Bit-identical to ``layer`` on those rows (pinned).
+    """
+    Hq, Hkv, d = dims.n_q_heads, dims.n_kv_heads, dims.head_dim
+    if dims.attn_only:
+        a = h
+    else:
+        a = round_bf16(rmsnorm(h, W["norm_attn"], dims.rms_eps))
+    k = linear(a, W["wk"]).reshape(-1, Hkv, d)
+    v = linear(a, W["wv"]).reshape(-1, Hkv, d)
+    for i, r in enumerate(rows):
+        K[:, r.store] = round_bf16(rope(k[i], r.pos, dims.rope_theta))
+        V[:, r.store] = round_bf16(v[i])
+    sel = list(out_rows)
+    q = linear(a[sel], W["wq"]).reshape(-1, Hq, d)
+    o = np.stack([round_bf16(attend(round_bf16(rope(q[n], rows[i].pos, dims.rope_theta)), K, V,
+                                    rows[i].visible, dims.group)).reshape(Hq * d)
+                  for n, i in enumerate(sel)])
+    if dims.attn_only:
+        return round_bf16(linear(o, W["wo"]))
+    hs = h[sel] + linear(o, W["wo"])
+    b = round_bf16(rmsnorm(hs, W["norm_ffn"], dims.rms_eps))
+    z = round_bf16(silu(linear(b, W["wg"])) * linear(b, W["wu"]))
+    return hs + linear(z, W["wd"])
+
+
 def forward(dims: Dims, weights: List[Dict[str, np.ndarray]], kv: SlotKV, hidden: np.ndarray,
             rows: List[Row]) -> np.ndarray:
     """Run the rows through every layer; K/V land in ``kv``.  Returns the

@@ -174,6 +174,7 @@ struct kvr_ctx {
   std::vector<int32_t> host_match;
   // profiling
   bool prof = false;
+  float* trace = nullptr;   // [n_layers + 1][max_rows][hidden] float32, or null
   bool force_gemv = false;  // KVR_FORCE_GEMV=1: keep every m on the GEMV path
   std::vector<EventPair> pending;
   std::vector<cudaEvent_t> free_events;
@@ -518,6 +519,13 @@ int run_stack(kvr_ctx* c, int slot, const RowMap& rows, const void* hidden,
                      static_cast<const __nv_bfloat16*>(w[0].norm_attn), k.rms_eps, c->h, c->a, st);
     if (e != cudaSuccess) return cuda_fail(c, e, "embed launch");
   }
+  auto trace = [&](int entry) -> cudaError_t {
+    if (!c->trace || k.attn_only) return cudaSuccess;
+    return cudaMemcpyAsync(c->trace + (size_t)entry * k.max_rows * H, c->h, (size_t)m * H * 4,
+                           cudaMemcpyDeviceToDevice, st);
+  };
+  e = trace(0);
+  if (e != cudaSuccess) return cuda_fail(c, e, "trace copy");
   __nv_bfloat16* arena = reinterpret_cast<__nv_bfloat16*>(c->arena);
   for (int l = 0; l < k.n_layers; ++l) {
     const kvr_layer_weights& W = w[l];
@@ -576,6 +584,8 @@ int run_stack(kvr_ctx* c, int slot, const RowMap& rows, const void* hidden,
                                              last ? static_cast<__nv_bfloat16*>(out) : nullptr, st);
                    });
       if (rc) return rc;
+      e = trace(l + 1);
+      if (e != cudaSuccess) return cuda_fail(c, e, "trace copy");
     }
   }
   (void)i4;
@@ -756,7 +766,11 @@ int kvr_ctx_create(const kvr_config* cfg, void* kv_arena, size_t arena_bytes, vo
     delete c;
     return KVR_ERR_CUDA;
   }
+  // Positions past a slot's length are read (and multiplied by a zero weight)
+  // when a key block is partly visible; zero the arena once so they are finite.
   e = cudaMemset(c->status, 0, 64);
+  if (e == cudaSuccess) e = cudaMemset(c->arena, 0, (size_t)c->granted * slot_kv_bytes(cfg));
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e != cudaSuccess) {
     delete c;
     return KVR_ERR_CUDA;
@@ -952,6 +966,19 @@ int kvr_sync_status(kvr_ctx* c, void* stream) {
     cudaStreamSynchronize(st);
     return fail(c, KVR_ERR_TIMEOUT, "a device-side wait gave up (status %d)", word);
   }
+  return KVR_OK;
+}
+
+int kvr_trace_set(kvr_ctx* c, void* dev, size_t bytes) {
+  if (!c) return KVR_ERR_ARG;
+  if (!dev) {
+    c->trace = nullptr;
+    return KVR_OK;
+  }
+  const size_t need = (size_t)(c->cfg.n_layers + 1) * c->cfg.max_rows * c->cfg.hidden * 4;
+  if (bytes < need) return fail(c, KVR_ERR_CAPACITY, "trace buffer needs %zu bytes", need);
+  if ((uintptr_t)dev & 15) return fail(c, KVR_ERR_ARG, "trace buffer must be 16-byte aligned");
+  c->trace = static_cast<float*>(dev);
   return KVR_OK;
 }
 

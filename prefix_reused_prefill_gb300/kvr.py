@@ -25,7 +25,7 @@ EXPORTED = ["kvr_arena_bytes", "kvr_scratch_bytes", "kvr_ctx_create", "kvr_ctx_i
             "kvr_ctx_destroy", "kvr_slot_match", "kvr_slot_truncate", "kvr_slot_len",
             "kvr_slot_tokens", "kvr_slot_assign", "kvr_slot_kv", "kvr_prefill_suffix", "kvr_verify",
             "kvr_prefill_branches", "kvr_sync_status", "kvr_profile_enable", "kvr_profile_read",
-            "kvr_last_error", "kvr_slot_match_static"]
+            "kvr_last_error", "kvr_slot_match_static", "kvr_trace_set"]
 
 
 class KvrError(RuntimeError):
@@ -83,6 +83,7 @@ def load_library(path: str = LIB_PATH):
         "kvr_profile_read": (I, [V, P(ctypes.c_float), P(I)]),
         "kvr_last_error": (ctypes.c_char_p, [V]),
         "kvr_slot_match_static": (I, [V, i32p, I, P(I), P(I), V]),
+        "kvr_trace_set": (I, [V, V, Z]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -261,6 +262,15 @@ class Kvr:
 
     def kvr_sync_status(self, stream=None):
         self._check(self.lib.kvr_sync_status(self.ctx, self._stream(stream)))
+
+    def kvr_trace_set(self, buf: Optional[torch.Tensor]):
+        """buf: float32 device tensor [n_layers + 1][max_rows][hidden], or None to clear."""
+        if buf is None:
+            self._check(self.lib.kvr_trace_set(self.ctx, None, 0))
+        else:
+            assert buf.dtype == torch.float32 and buf.is_cuda and buf.is_contiguous()
+            self._check(self.lib.kvr_trace_set(self.ctx, buf.data_ptr(), buf.numel() * 4))
+        self._trace = buf
 
     def kvr_profile_enable(self, on: bool):
         self._check(self.lib.kvr_profile_enable(self.ctx, 1 if on else 0))

@@ -28,7 +28,7 @@ def close(got, ref, what=""):
     got = np.asarray(got, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
     err = np.abs(got - ref)
-    bad = err > ATOL + RTOL * np.abs(ref)
+    bad = ~(err <= ATOL + RTOL * np.abs(ref))   # NaN fails
     assert not bad.any(), (f"{what}: {int(bad.sum())}/{bad.size} out of tolerance, max err "
                            f"{err.max():.4g} at {np.unravel_index(err.argmax(), err.shape)}")
     return float(err.max())

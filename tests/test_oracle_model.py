@@ -213,3 +213,23 @@ def test_attn_only_layer_structure(rng):
     W["wv"] = np.zeros((d, H)); kv.V[0, 0, :10] = 0.0
     out0 = model.layer(dims, W, x, kv.K[0], kv.V[0], model.plain_rows(10, 3))
     np.testing.assert_array_equal(out0, 0.0)
+
+
+@pytest.mark.parametrize("name", ["small", "small_attn"])
+def test_layer_rows_equals_layer_on_selected_rows(name, rng):
+    shape = workloads.SHAPES[name]
+    dims = oracle_dims(shape)
+    W = oracle_weights(shape, workloads.layer_weights(shape, 4, 0))
+    m, P = 11, 9
+    h = rng.standard_normal((m, shape.hidden))
+    kv1 = SlotKV(1, shape.n_kv_heads, 32, shape.head_dim)
+    kv1.K[0][:, :P] = round_bf16(rng.standard_normal((shape.n_kv_heads, P, shape.head_dim)))
+    kv1.V[0][:, :P] = round_bf16(rng.standard_normal((shape.n_kv_heads, P, shape.head_dim)))
+    kv2 = SlotKV(1, shape.n_kv_heads, 32, shape.head_dim)
+    kv2.K[:] = kv1.K; kv2.V[:] = kv1.V
+    full = model.layer(dims, W, h, kv1.K[0], kv1.V[0], model.plain_rows(P, m))
+    sel = [0, 4, 10]
+    part = model.layer_rows(dims, W, h, kv2.K[0], kv2.V[0], model.plain_rows(P, m), sel)
+    np.testing.assert_array_equal(part, full[sel])
+    np.testing.assert_array_equal(kv2.K, kv1.K)
+    np.testing.assert_array_equal(kv2.V, kv1.V)
