@@ -291,13 +291,205 @@ def run_gpu(args, rank, world):
 
 
 # ---------------------------------------------------------------------------
+# the other measured workloads (verify sweep, priming, attention crossover)
+# ---------------------------------------------------------------------------
+
+def _event_ms(call, reps, warm, before=None, after=None):
+    """Median device time of `call` over `reps` runs (CUDA events on the
+    launching stream); `before`/`after` run outside the timed region."""
+    stream = torch.cuda.current_stream()
+    for _ in range(warm):
+        if before: before()
+        call()
+        if after: after()
+    ts = []
+    for _ in range(reps):
+        if before: before()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        call()
+        e1.record(stream)
+        e1.synchronize()
+        ts.append(e0.elapsed_time(e1))
+        if after: after()
+    return statistics.median(ts)
+
+
+def _prefill_state(kv, slot, toks, shape, seed, w, device, chunk=256):
+    for a in range(0, len(toks), chunk):
+        c = toks[a:a + chunk]
+        kv.kvr_prefill_suffix(slot, c, workloads.hidden_for_tokens(c, shape.hidden, seed).to(device), w)
+    kv.kvr_sync_status()
+
+
+def run_verify(args):
+    """Speculative verify: 36 layers (H 4096, 32/8 heads, F 12288), one slot
+    holding 4096 tokens, m = k+1 in {1,2,3,4,6,8}; the slot is cut back to
+    4096 after each call (outside the timed region).  Reports t(m) and the
+    least-squares fit a + b m, and the HBM fraction of each m against the
+    bytes one call must move (weights once, K/V once per KV head, the append)."""
+    from prefix_reused_prefill_gb300 import Kvr, config_for_shape
+    device = torch.device("cuda", torch.cuda.current_device())
+    pk, pk_kind = peaks()
+    shape = workloads.SHAPES["dense9b"]
+    seed = workloads.config_seed(3)
+    tk = workloads.verify_tokens(seed)
+    P = len(tk["state"])
+    lws = workloads.stack_weights(shape, seed, device=device)
+    kv = Kvr(config_for_shape(shape, 1, P + 256, 256), device=device)
+    w = kv.weights(lws)
+    assert kv.kvr_slot_match(tk["state"][:1]) == (0, 0)
+    _prefill_state(kv, 0, tk["state"], shape, seed, w, device)
+    L = shape.n_layers
+    table = []
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    for m in (1, 2, 3, 4, 6, 8):
+        draft = tk["draft"][:m]
+        x = workloads.hidden_for_tokens(draft, shape.hidden, seed).to(device)
+        out = torch.empty((m, shape.hidden), dtype=torch.bfloat16, device=device)
+        ms = _event_ms(lambda: kv.kvr_verify(0, draft, x, w, out=out), args.steps, args.warmup,
+                       after=lambda: kv.kvr_slot_truncate(0, P))
+        kv.kvr_sync_status()
+        nbytes = (shape.params_per_layer() * 0.5625 * L
+                  + (P + m) * shape.n_kv_heads * shape.head_dim * 2 * 2 * L
+                  + m * shape.n_kv_heads * shape.head_dim * 4 * L)
+        gbs = nbytes / (ms / 1e3) / 1e9
+        table.append({"m": m, "ms": round(ms, 4), "rows_per_s": round(m / (ms / 1e3), 1),
+                      "algorithmic_gb": round(nbytes / 1e9, 4), "gbs": round(gbs, 1),
+                      "frac_hbm": round(gbs / pk["hbm_gbs"], 4)})
+    clk = clocks.stop()
+    ms_ = np.array([r["m"] for r in table], dtype=np.float64)
+    ts = np.array([r["ms"] for r in table])
+    b, a = np.polyfit(ms_, ts, 1)
+    kv.close()
+    return {"metric": "verify ms per call", "workload": "speculative verify: 36 x (H 4096, 32/8 heads, F 12288) "
+            "int4-g32, 4096 cached tokens, m = k+1 rows", "unit": "ms", "higher_is_better": False,
+            "fit_ms": {"a": round(float(a), 4), "b_per_row": round(float(b), 4)},
+            "page_fit_ms": {"a": 9.0, "b_per_row": 5.5, "hardware": "the page's own (not a GB300)"},
+            "per_m": table, "peak_hbm_gbs": pk["hbm_gbs"], "peak_kind": pk_kind,
+            "l2": "inputs larger than L2 (3.9 GB of weights and 0.6 GB of K/V per call)",
+            "reps": args.steps, "warmup": args.warmup, "clocks": clk, "dtype": "bf16", "data": "synthetic"}
+
+
+def run_priming(args):
+    """Multi-branch priming: 36 layers (H 2560, 16/8 heads, F 9728), a 1200-token
+    state, 4 questions of 40 tokens in one kvr_prefill_branches call, against the
+    same 4 questions as 4 separate kvr_prefill_suffix calls (each followed by a
+    cut back to 1200, a host-only step)."""
+    from prefix_reused_prefill_gb300 import Kvr, config_for_shape
+    device = torch.device("cuda", torch.cuda.current_device())
+    shape = workloads.SHAPES["dense4b"]
+    seed = workloads.config_seed(4)
+    tk = workloads.priming_tokens(seed)
+    P = len(tk["state"])
+    lws = workloads.stack_weights(shape, seed, device=device)
+    kv = Kvr(config_for_shape(shape, 1, P + 272, 256), device=device)
+    w = kv.weights(lws)
+    assert kv.kvr_slot_match(tk["state"][:1]) == (0, 0)
+    _prefill_state(kv, 0, tk["state"], shape, seed, w, device)
+    qs = tk["questions"]
+    lens = [len(q) for q in qs]
+    allq = sum(qs, [])
+    xq = workloads.hidden_for_tokens(allq, shape.hidden, seed).to(device)
+    xs = [xq[sum(lens[:b]):sum(lens[:b + 1])].contiguous() for b in range(len(qs))]
+    out = torch.empty((sum(lens), shape.hidden), dtype=torch.bfloat16, device=device)
+    outs = [torch.empty((n, shape.hidden), dtype=torch.bfloat16, device=device) for n in lens]
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    ms_batched = _event_ms(lambda: kv.kvr_prefill_branches(0, lens, allq, xq, w, out=out),
+                           args.steps, args.warmup)
+
+    def separate():
+        for b in range(len(qs)):
+            kv.kvr_prefill_suffix(0, qs[b], xs[b], w, out=outs[b])
+            kv.kvr_slot_truncate(0, P)
+    ms_sep = _event_ms(separate, args.steps, args.warmup)
+    clk = clocks.stop()
+    kv.kvr_sync_status()
+    assert kv.kvr_slot_len(0) == P
+    kv.close()
+    rows = sum(lens)
+    return {"metric": "priming rows/s", "workload": "multi-branch priming: 36 x (H 2560, 16/8 heads, F 9728) "
+            "int4-g32, 1200-token state, 4 questions x 40 tokens", "unit": "rows/s", "higher_is_better": True,
+            "value": round(rows / (ms_batched / 1e3), 1), "ms_batched": round(ms_batched, 4),
+            "ms_separate_4_calls": round(ms_sep, 4), "speedup": round(ms_sep / ms_batched, 3),
+            "l2": "inputs larger than L2 (1.83 GB of weights per call)",
+            "reps": args.steps, "warmup": args.warmup, "clocks": clk, "dtype": "bf16", "data": "synthetic"}
+
+
+def run_crossover(args):
+    """Attention crossover: one 7B-shaped attention + QKV/O layer, 4 slots of
+    16384; the target slot holds P cached tokens (K/V drawn N(0,1)); m rows are
+    prefilled after them.  L2 is flushed (a 2 x L2 write) before every timed
+    call.  Reports the call time, the attention kernels' time (per-class
+    events) and the attended-KV GB/s for each (P, m)."""
+    from prefix_reused_prefill_gb300 import Kvr, config_for_shape
+    device = torch.device("cuda", torch.cuda.current_device())
+    pk, pk_kind = peaks()
+    shape = workloads.SHAPES["qwen7b_attn"]
+    seed = workloads.config_seed(5)
+    lw = workloads.layer_weights(shape, seed, 0, device=device)
+    kv = Kvr(config_for_shape(shape, 4, 16384, 1024), device=device)
+    w = kv.weights([lw])
+    flush_buf = torch.empty(2 * 129 * 2 ** 20 // 4, dtype=torch.float32, device=device)  # 2 x L2
+    Hkv, d, Hq = shape.n_kv_heads, shape.head_dim, shape.n_q_heads
+    table = []
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    for P in (512, 2048, 8192, 15360):
+        kk, vv = workloads.random_kv(Hkv, P, d, seed + P)
+        k, v = kv.kvr_slot_kv(3, 0)
+        k[:, :P] = kk.to(device)
+        v[:, :, :P] = vv.transpose(1, 2).to(device)
+        kv.kvr_slot_assign(3, list(range(P)))
+        for m in (1, 4, 16, 64, 256, 1024):
+            new = list(range(40000, 40000 + m))
+            x = workloads.hidden_for_tokens(new, shape.hidden, seed).to(device)
+            out = torch.empty((m, shape.hidden), dtype=torch.bfloat16, device=device)
+            call = lambda: kv.kvr_prefill_suffix(3, new, x, w, out=out)  # noqa: E731
+            flush = lambda: flush_buf.fill_(1.0)  # noqa: E731
+            cut = lambda: kv.kvr_slot_truncate(3, P)  # noqa: E731
+            ms = _event_ms(call, args.steps, args.warmup, before=flush, after=cut)
+            kv.kvr_profile_read()
+            kv.kvr_profile_enable(True)
+            for _ in range(args.steps):
+                flush()
+                call()
+                cut()
+            torch.cuda.synchronize()
+            cls_ms, _ = kv.kvr_profile_read()
+            kv.kvr_profile_enable(False)
+            attn_ms = cls_ms[1] / args.steps
+            kv_bytes = (P + m) * Hkv * d * 2 * 2
+            flops = 4.0 * d * Hq * sum(P + i + 1 for i in range(m))
+            table.append({"P": P, "m": m, "ms": round(ms, 4), "attn_ms": round(attn_ms, 4),
+                          "proj_ms": round(cls_ms[0] / args.steps, 4),
+                          "attended_kv_gbs": round(kv_bytes / (attn_ms / 1e3) / 1e9, 1),
+                          "attn_tflops": round(flops / (attn_ms / 1e3) / 1e12, 2)})
+        kv.kvr_sync_status()
+    clk = clocks.stop()
+    kv.close()
+    return {"metric": "attention crossover", "workload": "one 7B-shaped attention + QKV/O layer (H 3584, 28/4 "
+            "heads, int4-g32), 4 slots x 16384, P cached x m new rows", "unit": "ms",
+            "higher_is_better": False, "per_case": table, "peak_hbm_gbs": pk["hbm_gbs"],
+            "peak_bf16_tflops": pk.get("bf16_tflops"), "peak_kind": pk_kind,
+            "l2": "flushed before every timed call (2 x L2 write)",
+            "reps": args.steps, "warmup": args.warmup, "clocks": clk, "dtype": "bf16", "data": "synthetic"}
+
+
+# ---------------------------------------------------------------------------
 # the oracle, timed on the host cores
 # ---------------------------------------------------------------------------
 
-def cpu_baseline(rows: int, layers_timed: int = 1):
-    """Oracle (float64 numpy, as it stands) on one layer of the turn-9 workload:
-    `rows` suffix rows over a 1668-row cached prefix (K/V drawn N(0,1)), scaled to
-    rows/s of the full 28-layer stack.  Weight decoding happens before timing."""
+_ORACLE_SETUP = {}
+
+
+def _oracle_turn9_layer(rows: int):
+    """Decoded layer-0 weights, the cached prefix and the suffix rows (built once)."""
+    if rows in _ORACLE_SETUP:
+        return _ORACLE_SETUP[rows]
     from oracle import model as om
     from oracle import formats
     shape = workloads.SHAPES["qwen7b"]
@@ -316,15 +508,31 @@ def cpu_baseline(rows: int, layers_timed: int = 1):
     cache.K[0][:, :P_CACHED] = workloads.bf16_to_f64(k)
     cache.V[0][:, :P_CACHED] = workloads.bf16_to_f64(v)
     x = workloads.bf16_to_f64(workloads.hidden_for_tokens(list(range(rows)), shape.hidden, seed))
+    _ORACLE_SETUP[rows] = (shape, dims, W, cache, x)
+    return _ORACLE_SETUP[rows]
+
+
+def cpu_baseline(rows: int, min_seconds: float = 10.0):
+    """Oracle (float64 numpy, as it stands) on the turn-9 workload: the layer
+    evaluated for `rows` suffix rows over a 1668-row cached prefix (K/V drawn
+    N(0,1)), repeated until at least `min_seconds` of CPU work, scaled to rows/s
+    of the full 28-layer stack.  Weight decoding happens before timing."""
+    from oracle import model as om
+    shape, dims, W, cache, x = _oracle_turn9_layer(rows)
+    n_eval = 0
     t0 = time.perf_counter()
-    om.layer(dims, W, x, cache.K[0], cache.V[0], om.plain_rows(P_CACHED, rows))
-    dt = time.perf_counter() - t0
-    per_row_stack = dt / rows * shape.n_layers
+    while True:
+        om.layer(dims, W, x, cache.K[0], cache.V[0], om.plain_rows(P_CACHED, rows))
+        n_eval += 1
+        dt = time.perf_counter() - t0
+        if dt >= min_seconds:
+            break
+    per_row_stack = dt / (n_eval * rows) * shape.n_layers
     cores = int(os.environ.get("OMP_NUM_THREADS", 0)) or os.cpu_count()
     return {"value": round(1.0 / per_row_stack, 3), "unit": "rows/s", "cores": cores,
             "kind": "oracle",
-            "sample": f"1 of 28 layers, {rows} suffix rows over 1668 cached rows, float64 numpy "
-                      f"({dt:.2f} s), scaled to the 28-layer stack"}
+            "sample": f"{n_eval} layer evaluation(s) of {rows} suffix rows over 1668 cached rows "
+                      f"(float64 numpy, {dt:.1f} s), scaled to the 28-layer stack"}
 
 
 def run_reference(args, rank, world):
@@ -333,10 +541,10 @@ def run_reference(args, rank, world):
         return None, rank
     vals = []
     for _ in range(args.warmup):
-        cpu_baseline(args.cpu_rows)
+        cpu_baseline(args.cpu_rows, min_seconds=0.0)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        vals.append(cpu_baseline(args.cpu_rows))
+        vals.append(cpu_baseline(args.cpu_rows, min_seconds=0.0))
     dt = time.perf_counter() - t0
     v = statistics.median(x["value"] for x in vals)
     cb = dict(vals[0]); cb["value"] = v
@@ -358,8 +566,10 @@ def main():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="kvr", choices=["kvr", "reference"])
-    ap.add_argument("--cpu-rows", type=int, default=64)
+    ap.add_argument("--cpu-rows", type=int, default=M_ROWS)
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--workload", default="turn9", choices=["turn9", "verify", "priming", "crossover"],
+                    help="turn9 is the bench line; the others print their own measurement line")
     ap.add_argument("--layers", type=int, default=0,
                     help="profiling aid: run a reduced stack of this many layers")
     args = ap.parse_args()
@@ -367,6 +577,9 @@ def main():
     rank, world = dist_setup(args.gpus)
     if args.impl == "reference":
         line, rank = run_reference(args, rank, world)
+    elif args.workload != "turn9":
+        runner = {"verify": run_verify, "priming": run_priming, "crossover": run_crossover}[args.workload]
+        line = runner(args) if rank == 0 else None
     else:
         line, rank = run_gpu(args, rank, world)
     if rank == 0 and line is not None:

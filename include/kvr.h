@@ -290,6 +290,13 @@ int kvr_trace_set(kvr_ctx* ctx, void* dev, size_t bytes);
 int kvr_profile_enable(kvr_ctx* ctx, int on);
 int kvr_profile_read(kvr_ctx* ctx, float ms[4], int launches[4]);
 
+/* The launches recorded since the last kvr_profile_read, in launch order:
+ * cls[i] (as above) and ms[i], the time between the event pair around launch
+ * i (the kernel plus any wait for the host to issue it).  Synchronises; fills
+ * at most max_n entries and sets *n to the number recorded.  Does not reset:
+ * kvr_profile_read still returns (and clears) the sums. */
+int kvr_profile_launches(kvr_ctx* ctx, int* cls, float* ms, int max_n, int* n);
+
 const char* kvr_last_error(const kvr_ctx* ctx);
 
 #ifdef __cplusplus

@@ -81,6 +81,8 @@ __global__ void __launch_bounds__((RW + 1) * 32) attn_kernel(const __grid_consta
   const int b1 = (int)((long long)nb * (split + 1) / p.nsplit);
   const int nblk = b1 - b0;
 
+  dev::pdl_trigger();
+  dev::pdl_wait();   // q and the appended K/V come from the previous launch
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kStages; ++i) {
       dev::mbar_init(dev::smem_u32(&full_bar[i]), 1);
@@ -287,6 +289,8 @@ __global__ void __launch_bounds__((RW + 1) * 32) attn_kernel(const __grid_consta
 // in split order; each lane owns D/32 consecutive elements.
 template <int D>
 __global__ void __launch_bounds__(256) attn_combine_kernel(const __grid_constant__ AttnParams p) {
+  dev::pdl_trigger();
+  dev::pdl_wait();
   const long long rows = (long long)p.rows.m * p.Hq;
   const long long rowidx = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
   if (rowidx >= rows) return;
@@ -321,8 +325,7 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const __grid_constant
 template <int D, int RW>
 cudaError_t launch_t(const AttnParams& p, cudaStream_t st) {
   const dim3 grid(p.row_tiles, p.nsplit, p.Hkv);
-  attn_kernel<D, RW><<<grid, (RW + 1) * 32, AttnCfg<D>::kSmem, st>>>(p);
-  return cudaGetLastError();
+  return launch_k(attn_kernel<D, RW>, grid, (RW + 1) * 32, AttnCfg<D>::kSmem, st, p);
 }
 
 template <int D>
@@ -358,9 +361,8 @@ cudaError_t launch_attention(const AttnParams& p, int d, int row_warps, cudaStre
 
 cudaError_t launch_attn_combine(const AttnParams& p, int d, cudaStream_t st) {
   const unsigned blocks = (unsigned)((p.rows.m * p.Hq + 7) / 8);
-  if (d == 128) attn_combine_kernel<128><<<blocks, 256, 0, st>>>(p);
-  else attn_combine_kernel<64><<<blocks, 256, 0, st>>>(p);
-  return cudaGetLastError();
+  if (d == 128) return launch_k(attn_combine_kernel<128>, blocks, 256, 0, st, p);
+  return launch_k(attn_combine_kernel<64>, blocks, 256, 0, st, p);
 }
 
 }  // namespace kvr

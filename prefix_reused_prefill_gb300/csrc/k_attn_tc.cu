@@ -152,6 +152,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
   const int b1 = (int)((long long)nb * (split + 1) / p.nsplit);
   const int nblk = b1 - b0;
 
+  dev::pdl_trigger();
+  dev::pdl_wait();   // q and the appended K/V come from the previous launch
   if (threadIdx.x == 0) {
     dev::mbar_init(dev::smem_u32(&q_full), 1);
     for (int i = 0; i < C::kStages; ++i) {
@@ -411,9 +413,8 @@ cudaError_t attn_tc_setup() {
 
 cudaError_t launch_attention_tc(const AttnParams& p, int d, cudaStream_t st) {
   const dim3 grid(p.row_tiles, p.nsplit, p.Hkv);
-  if (d == 128) attn_tc_kernel<128><<<grid, kThreads, TcCfg<128>::kSmem, st>>>(p);
-  else attn_tc_kernel<64><<<grid, kThreads, TcCfg<64>::kSmem, st>>>(p);
-  return cudaGetLastError();
+  if (d == 128) return launch_k(attn_tc_kernel<128>, grid, kThreads, TcCfg<128>::kSmem, st, p);
+  return launch_k(attn_tc_kernel<64>, grid, kThreads, TcCfg<64>::kSmem, st, p);
 }
 
 }  // namespace kvr

@@ -37,6 +37,8 @@ __device__ __forceinline__ float split_sum(const float* part, long long plane, i
 
 // cos/sin of pos * theta^(-2j/d), evaluated in double and rounded once.
 __global__ void rope_table_kernel(RowMap rows, int d, double theta, float2* table) {
+  dev::pdl_trigger();
+  dev::pdl_wait();
   const int half = d / 2;
   const int idx = blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= rows.m * half) return;
@@ -51,6 +53,8 @@ __global__ void rope_table_kernel(RowMap rows, int d, double theta, float2* tabl
 
 __global__ void embed_kernel(const __nv_bfloat16* hidden, int H, const __nv_bfloat16* gain,
                              float eps, float* h, __nv_bfloat16* a) {
+  dev::pdl_trigger();
+  dev::pdl_wait();
   __shared__ float red[32];
   const long long row = blockIdx.x;
   float ss = 0.f;
@@ -74,6 +78,8 @@ __global__ void __launch_bounds__(256) epi_qkv_kernel(const float* part, long lo
                                                       int Hkv, const float2* rope, __nv_bfloat16* q,
                                                       __nv_bfloat16* arena, long long k_off,
                                                       long long v_off, int cap) {
+  dev::pdl_trigger();
+  dev::pdl_wait();
   constexpr int kHalf = D / 2;
   constexpr int kChunks = kHalf / 8;          // threads per token
   constexpr int kTok = 256 / kChunks;         // tokens per CTA
@@ -154,6 +160,8 @@ __global__ void __launch_bounds__(256) epi_resid_kernel(const float* part, long 
                                                         int ldo, int c0, int H, float* h,
                                                         const __nv_bfloat16* gain, float eps,
                                                         __nv_bfloat16* a_out, __nv_bfloat16* final_out) {
+  dev::pdl_trigger();
+  dev::pdl_wait();
   __shared__ float red[32];
   const int t = blockIdx.x;
   const long long i = c0 + t;
@@ -201,6 +209,8 @@ __global__ void __launch_bounds__(256) epi_resid_kernel(const float* part, long 
 
 __global__ void epi_swiglu_kernel(const float* part, long long plane, int ksplit, int ldo, int c0,
                                   int mb, int F, __nv_bfloat16* z) {
+  dev::pdl_trigger();
+  dev::pdl_wait();
   const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= (long long)mb * F) return;
   const int t = (int)(idx / F), n = (int)(idx % F);
@@ -212,6 +222,8 @@ __global__ void epi_swiglu_kernel(const float* part, long long plane, int ksplit
 
 __global__ void epi_cast_kernel(const float* part, long long plane, int ksplit, int ldo, int c0,
                                 int mb, int N, __nv_bfloat16* out) {
+  dev::pdl_trigger();
+  dev::pdl_wait();
   const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= (long long)mb * N) return;
   const int t = (int)(idx / N), n = (int)(idx % N);
@@ -225,14 +237,12 @@ inline unsigned blocks_for(long long n, int threads) { return (unsigned)((n + th
 
 cudaError_t launch_rope_table(const RowMap& rows, int d, float theta, float2* table, cudaStream_t st) {
   const long long n = (long long)rows.m * (d / 2);
-  rope_table_kernel<<<blocks_for(n, 256), 256, 0, st>>>(rows, d, (double)theta, table);
-  return cudaGetLastError();
+  return launch_k(rope_table_kernel, blocks_for(n, 256), 256, 0, st, rows, d, (double)theta, table);
 }
 
 cudaError_t launch_embed(const __nv_bfloat16* hidden, int m, int H, const __nv_bfloat16* gain,
                          float eps, float* h, __nv_bfloat16* a, cudaStream_t st) {
-  embed_kernel<<<m, 256, 0, st>>>(hidden, H, gain, eps, h, a);
-  return cudaGetLastError();
+  return launch_k(embed_kernel, m, 256, 0, st, hidden, H, gain, eps, h, a);
 }
 
 cudaError_t launch_epi_qkv(const float* part, long long plane, int ksplit, int ldo, int c0, int mb,
@@ -242,16 +252,14 @@ cudaError_t launch_epi_qkv(const float* part, long long plane, int ksplit, int l
   const int heads = Hq + 2 * Hkv;
   if (d == 128) {
     const dim3 grid((mb + 15) / 16, heads);
-    epi_qkv_kernel<128><<<grid, 256, 0, st>>>(part, plane, ksplit, ldo, c0, mb, rows, Hq, Hkv, rope, q,
-                                              arena, k_off, v_off, cap);
+    return launch_k(epi_qkv_kernel<128>, grid, 256, 0, st, part, plane, ksplit, ldo, c0, mb, rows, Hq,
+                    Hkv, rope, q, arena, k_off, v_off, cap);
   } else if (d == 64) {
     const dim3 grid((mb + 31) / 32, heads);
-    epi_qkv_kernel<64><<<grid, 256, 0, st>>>(part, plane, ksplit, ldo, c0, mb, rows, Hq, Hkv, rope, q,
-                                             arena, k_off, v_off, cap);
-  } else {
-    return cudaErrorInvalidValue;
+    return launch_k(epi_qkv_kernel<64>, grid, 256, 0, st, part, plane, ksplit, ldo, c0, mb, rows, Hq,
+                    Hkv, rope, q, arena, k_off, v_off, cap);
   }
-  return cudaGetLastError();
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_epi_resid(const float* part, long long plane, int ksplit, int ldo, int c0,
@@ -259,28 +267,27 @@ cudaError_t launch_epi_resid(const float* part, long long plane, int ksplit, int
                              __nv_bfloat16* a_out, __nv_bfloat16* final_out, cudaStream_t st) {
   const int v = (H / 4 + 255) / 256;
   if (v <= 2)
-    epi_resid_kernel<2><<<mb, 256, 0, st>>>(part, plane, ksplit, ldo, c0, H, h, gain, eps, a_out, final_out);
-  else if (v <= 4)
-    epi_resid_kernel<4><<<mb, 256, 0, st>>>(part, plane, ksplit, ldo, c0, H, h, gain, eps, a_out, final_out);
-  else if (v <= 8)
-    epi_resid_kernel<8><<<mb, 256, 0, st>>>(part, plane, ksplit, ldo, c0, H, h, gain, eps, a_out, final_out);
-  else
-    return cudaErrorInvalidValue;
-  return cudaGetLastError();
+    return launch_k(epi_resid_kernel<2>, mb, 256, 0, st, part, plane, ksplit, ldo, c0, H, h, gain, eps,
+                    a_out, final_out);
+  if (v <= 4)
+    return launch_k(epi_resid_kernel<4>, mb, 256, 0, st, part, plane, ksplit, ldo, c0, H, h, gain, eps,
+                    a_out, final_out);
+  if (v <= 8)
+    return launch_k(epi_resid_kernel<8>, mb, 256, 0, st, part, plane, ksplit, ldo, c0, H, h, gain, eps,
+                    a_out, final_out);
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_epi_swiglu(const float* part, long long plane, int ksplit, int ldo, int c0,
                               int mb, int F, __nv_bfloat16* z, cudaStream_t st) {
-  epi_swiglu_kernel<<<blocks_for((long long)mb * F, 256), 256, 0, st>>>(part, plane, ksplit, ldo,
-                                                                         c0, mb, F, z);
-  return cudaGetLastError();
+  return launch_k(epi_swiglu_kernel, blocks_for((long long)mb * F, 256), 256, 0, st, part, plane,
+                  ksplit, ldo, c0, mb, F, z);
 }
 
 cudaError_t launch_epi_cast(const float* part, long long plane, int ksplit, int ldo, int c0,
                             int mb, int N, __nv_bfloat16* out, cudaStream_t st) {
-  epi_cast_kernel<<<blocks_for((long long)mb * N, 256), 256, 0, st>>>(part, plane, ksplit, ldo, c0,
-                                                                      mb, N, out);
-  return cudaGetLastError();
+  return launch_k(epi_cast_kernel, blocks_for((long long)mb * N, 256), 256, 0, st, part, plane,
+                  ksplit, ldo, c0, mb, N, out);
 }
 
 }  // namespace kvr

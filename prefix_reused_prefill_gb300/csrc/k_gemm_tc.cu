@@ -162,6 +162,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_int4_tc_kernel(const __grid_
   const int nkc = kc1 - kc0;
   const uint32_t xbytes = 2u * (uint32_t)p.xrows * 128u;
 
+  dev::pdl_trigger();
   if (threadIdx.x == 0) {
     for (int i = 0; i < kRawStages; ++i) {
       dev::mbar_init(dev::smem_u32(&raw_full[i]), 1);
@@ -189,6 +190,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_int4_tc_kernel(const __grid_
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
+  // The int4 weight stream (warp 0, lane 0) reads only weights and may run
+  // ahead of the previous launch; every other role waits for it.
+  if (warp != 0 || lane != 0) dev::pdl_wait();
 
   if (warp == 0) {
     // ---------------------------------------------------------------- producers
@@ -413,8 +417,7 @@ cudaError_t gemm_tc_setup() {
 
 cudaError_t launch_gemm_int4_tc(const GemmParams& p, int total_tiles, cudaStream_t st) {
   const dim3 grid(total_tiles, p.ksplit);
-  gemm_int4_tc_kernel<<<grid, kThreads, kSmem, st>>>(p);
-  return cudaGetLastError();
+  return launch_k(gemm_int4_tc_kernel, grid, kThreads, kSmem, st, p);
 }
 
 }  // namespace kvr

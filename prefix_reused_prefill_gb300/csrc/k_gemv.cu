@@ -84,6 +84,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_int4_kernel(const __grid_con
   const int ks1 = (int)((long long)(split + 1) * p.ksteps / p.ksplit);
   const int nk = ks1 - ks0;
 
+  dev::pdl_trigger();
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kStages; ++i) {
       dev::mbar_init(dev::smem_u32(&full_bar[i]), 1);
@@ -101,16 +102,37 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_int4_kernel(const __grid_con
       dev::prefetch_tmap(&seg.ts);
       dev::prefetch_tmap(&p.tx);
       const uint64_t pol = dev::policy_evict_first();
-      int issued = 0;
-      for (int it = 0; it < nk; ++it) {
+      // Weights do not depend on earlier launches: fill the ring's weight and
+      // scale tiles and pull the rest of this CTA's weights toward L2 before
+      // waiting for the previous launch; the activations follow the wait.
+      const int pre = nk < C::kStages ? nk : C::kStages;
+      for (int it = 0; it < pre; ++it) {
+        const uint32_t sb = base + it * C::kStageBytes;
+        const uint32_t fb = dev::smem_u32(&full_bar[it]);
+        dev::mbar_arrive_expect_tx(fb, C::kStageBytes);
+        dev::tma_load_2d_hint(sb, &seg.tw, (ks0 + it) * 128, row0, fb, pol);
+        dev::tma_load_2d_hint(sb + kWTileBytes + C::kXTileBytes, &seg.ts, (ks0 + it) * 8, row0, fb, pol);
+      }
+      for (int it = pre; it < nk; ++it) {
+        dev::tma_prefetch_2d(&seg.tw, (ks0 + it) * 128, row0);
+        dev::tma_prefetch_2d(&seg.ts, (ks0 + it) * 8, row0);
+      }
+      dev::pdl_wait();
+      for (int it = 0; it < pre; ++it) {
+        const uint32_t sb = base + it * C::kStageBytes;
+        const uint32_t fb = dev::smem_u32(&full_bar[it]);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          dev::tma_load_2d(sb + kWTileBytes + j * C::kXBoxBytes, &p.tx, (ks0 + it) * kGemvKStep + 64 * j,
+                           p.c0, fb);
+      }
+      int issued = pre;
+      for (int it = pre; it < nk; ++it) {
         const int st = it % C::kStages;
         const uint32_t use = (uint32_t)(it / C::kStages);
-        if (it >= C::kStages) {
-          if (!dev::mbar_wait(dev::smem_u32(&empty_bar[st]), (use - 1) & 1, p.status) ||
-              *abort_v) {
-            *abort_v = 1;
-            break;
-          }
+        if (!dev::mbar_wait(dev::smem_u32(&empty_bar[st]), (use - 1) & 1, p.status) || *abort_v) {
+          *abort_v = 1;
+          break;
         }
         const uint32_t sb = base + st * C::kStageBytes;
         const uint32_t fb = dev::smem_u32(&full_bar[st]);
@@ -135,6 +157,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_int4_kernel(const __grid_con
   }
 
   // -------------------------------------------------------------- consumers
+  dev::pdl_wait();                  // the partial sums are written below
   const int r = lane >> 2;          // fragment row 0..7
   const int c = lane & 3;           // fragment column pair
   const int rho0 = warp * 16 + r;   // tile rows of this thread: rho0 and rho0+8
@@ -210,6 +233,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_int4_kernel(const __grid_con
 // per output column, 16-byte loads along K, every token of the pass per warp.
 __global__ void __launch_bounds__(256) gemv_bf16_kernel(const __grid_constant__ GemvParams p,
                                                         int total_cols) {
+  dev::pdl_trigger();
+  dev::pdl_wait();
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (warp >= total_cols) return;
@@ -272,17 +297,15 @@ cudaError_t gemv_setup() {
 cudaError_t launch_gemv_int4(const GemvParams& p, int total_tiles, int nt, cudaStream_t st) {
   const dim3 grid(total_tiles, p.ksplit);
   switch (nt) {
-    case 1: gemv_int4_kernel<1><<<grid, kThreads, GemvCfg<1>::kSmem, st>>>(p); break;
-    case 2: gemv_int4_kernel<2><<<grid, kThreads, GemvCfg<2>::kSmem, st>>>(p); break;
-    default: gemv_int4_kernel<4><<<grid, kThreads, GemvCfg<4>::kSmem, st>>>(p); break;
+    case 1: return launch_k(gemv_int4_kernel<1>, grid, kThreads, GemvCfg<1>::kSmem, st, p);
+    case 2: return launch_k(gemv_int4_kernel<2>, grid, kThreads, GemvCfg<2>::kSmem, st, p);
+    default: return launch_k(gemv_int4_kernel<4>, grid, kThreads, GemvCfg<4>::kSmem, st, p);
   }
-  return cudaGetLastError();
 }
 
 cudaError_t launch_gemv_bf16(const GemvParams& p, int total_cols, cudaStream_t st) {
   const int blocks = (total_cols * 32 + 255) / 256;
-  gemv_bf16_kernel<<<blocks, 256, 0, st>>>(p, total_cols);
-  return cudaGetLastError();
+  return launch_k(gemv_bf16_kernel, blocks, 256, 0, st, p, total_cols);
 }
 
 }  // namespace kvr

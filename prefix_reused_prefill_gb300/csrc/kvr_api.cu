@@ -22,6 +22,14 @@
 
 using namespace kvr;
 
+bool kvr::pdl_enabled() {
+  static const bool on = [] {
+    const char* v = getenv("KVR_PDL");
+    return !(v && v[0] == '0');
+  }();
+  return on;
+}
+
 namespace {
 
 constexpr size_t kAlign = 256;
@@ -985,6 +993,24 @@ int kvr_trace_set(kvr_ctx* c, void* dev, size_t bytes) {
 int kvr_profile_enable(kvr_ctx* c, int on) {
   if (!c) return KVR_ERR_ARG;
   c->prof = on != 0;
+  return KVR_OK;
+}
+
+int kvr_profile_launches(kvr_ctx* c, int* cls, float* ms, int max_n, int* n) {
+  if (!c || !n || max_n < 0 || (max_n > 0 && (!cls || !ms))) return KVR_ERR_ARG;
+  int k = 0;
+  for (auto& p : c->pending) {
+    cudaError_t e = cudaEventSynchronize(p.b);
+    float t = 0.f;
+    if (e == cudaSuccess) e = cudaEventElapsedTime(&t, p.a, p.b);
+    if (e != cudaSuccess) return cuda_fail(c, e, "profile events");
+    if (k < max_n) {
+      cls[k] = p.cls;
+      ms[k] = t;
+    }
+    ++k;
+  }
+  *n = k;
   return KVR_OK;
 }
 

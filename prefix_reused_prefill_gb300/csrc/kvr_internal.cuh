@@ -124,8 +124,35 @@ struct AttnParams {
 };
 
 // ----------------------------------------------------------------------------
-// launchers (each returns cudaGetLastError() of its launch)
+// launchers (each returns the error of its launch)
 // ----------------------------------------------------------------------------
+// Every kernel of a call is launched with programmatic stream serialization:
+// it may be scheduled while its predecessor on the stream is still running.
+// Each kernel therefore signals griddepcontrol.launch_dependents on entry and
+// executes griddepcontrol.wait (which returns once the predecessor grid has
+// completed and its memory is visible) before it reads anything an earlier
+// launch wrote or writes anything at all.  Only reads of data no launch of a
+// call writes (weights, tensor maps) may precede the wait.  KVR_PDL=0 in the
+// environment turns the attribute off (every launch then waits in full).
+bool pdl_enabled();
+
+#ifdef __CUDACC__
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                            cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl_enabled() ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+#endif
 cudaError_t launch_prefix_match(const int32_t* slot_tokens, const int* slot_len, int n_slots,
                                 int cap, const int32_t* prompt, int n, int32_t* out,
                                 cudaStream_t st);
@@ -178,6 +205,13 @@ __device__ __forceinline__ unsigned long long globaltimer_ns() {
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
 }
+
+// Programmatic dependent launch: let the next kernel on the stream be
+// scheduled, and wait for the previous one to complete.
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");

@@ -25,6 +25,7 @@ EXPORTED = ["kvr_arena_bytes", "kvr_scratch_bytes", "kvr_ctx_create", "kvr_ctx_i
             "kvr_ctx_destroy", "kvr_slot_match", "kvr_slot_truncate", "kvr_slot_len",
             "kvr_slot_tokens", "kvr_slot_assign", "kvr_slot_kv", "kvr_prefill_suffix", "kvr_verify",
             "kvr_prefill_branches", "kvr_sync_status", "kvr_profile_enable", "kvr_profile_read",
+            "kvr_profile_launches",
             "kvr_last_error", "kvr_slot_match_static", "kvr_trace_set"]
 
 
@@ -81,6 +82,7 @@ def load_library(path: str = LIB_PATH):
         "kvr_sync_status": (I, [V, V]),
         "kvr_profile_enable": (I, [V, I]),
         "kvr_profile_read": (I, [V, P(ctypes.c_float), P(I)]),
+        "kvr_profile_launches": (I, [V, P(I), P(ctypes.c_float), I, P(I)]),
         "kvr_last_error": (ctypes.c_char_p, [V]),
         "kvr_slot_match_static": (I, [V, i32p, I, P(I), P(I), V]),
         "kvr_trace_set": (I, [V, V, Z]),
@@ -280,3 +282,11 @@ class Kvr:
         n = (ctypes.c_int * 4)()
         self._check(self.lib.kvr_profile_read(self.ctx, ms, n))
         return list(ms), list(n)
+
+    def kvr_profile_launches(self, max_n: int = 65536):
+        """[(class, ms)] of the launches recorded since the last kvr_profile_read."""
+        cls = (ctypes.c_int * max_n)()
+        ms = (ctypes.c_float * max_n)()
+        n = ctypes.c_int()
+        self._check(self.lib.kvr_profile_launches(self.ctx, cls, ms, max_n, ctypes.byref(n)))
+        return [(cls[i], ms[i]) for i in range(min(n.value, max_n))]
