@@ -1,15 +1,17 @@
 // m-row batched GEMV: Y[t][n] = sum_k X[t][k] * W[n][k] for up to 32 token rows,
-// each weight byte read from HBM once for all rows.
+// each weight byte read from HBM once for all rows, with the projection's
+// epilogue applied in the same launch.
 //
 // thinkspread, "The economics of speculative decoding" (cost model): the m
 // verify rows run as a batched GEMV whose weights are read once and shared by
 // the rows, so an extra row costs far less than a full weight read.
 //
-// int4 group-32 path (the hot one).  A CTA owns 128 weight rows and a range of
-// 256-input k-steps.  One producer warp streams, per k-step, a 128 x 128-byte
-// int4 tile (128B-swizzled), its 128 x 8 fp16 scales and the 8*NT x 256 bf16
-// activation tile through TMA into a multi-stage shared-memory ring guarded by
-// mbarriers.  Eight consumer warps each own 16 weight rows:
+// int4 group-32 path (the hot one).  A CTA owns a 128-row weight tile and a
+// range of 256-input k-steps.  One producer warp streams, per k-step, a
+// 128 x 128-byte int4 tile (128B-swizzled), its 128 x 8 fp16 scales and the
+// 8*NT x 256 bf16 activation tile through TMA into a multi-stage
+// shared-memory ring guarded by mbarriers.  Eight consumer warps each own 16
+// weight rows:
 //   * one 32-bit shared load per row gives a thread the eight 4-bit codes it
 //     needs for the two m16n8k16 fragments of one 32-input group (the byte
 //     layout of include/kvr.h is chosen for this);
@@ -21,8 +23,20 @@
 //     never rounded to bf16.
 // Plain CUDA-core FMAs would need 32*m FMAs per 16 weight bytes, more than the
 // SM issues at HBM rate once m > 2; the tensor cores keep the kernel HBM-bound.
-// Partial sums for each k-split go to a fp32 buffer; a row-wise epilogue
-// kernel adds the splits in a fixed order and applies the fused epilogue.
+//
+// Split k-steps: each CTA writes its fp32 partial tile, and the last CTA of
+// the tile to arrive (an arrival counter per tile) adds the splits in split
+// order -- the result does not depend on which CTA finishes last -- and runs
+// the epilogue on the tile in shared memory:
+//   * QKV: a tile is one head (d = 128) or two (d = 64), so each rotate-half
+//     pair (j, j + d/2) is in the tile: RoPE at the row's position, bf16,
+//     q to the KV-head-major q buffer, K rows and V^T columns to the slot
+//     (goinfer "What goinfer does": two vectors per token per layer);
+//   * Resid: h += y in fp32 (the RMSNorm that follows needs the whole row and
+//     runs as its own small launch), and on the last layer out = bf16(h);
+//   * Swiglu: the tile holds gate rows n0..n0+63 and the same up rows, so
+//     z = bf16(silu(g) * u) is local to the tile;
+//   * Cast: out = bf16(y) (attention-only layers).
 #include "kvr_internal.cuh"
 
 namespace kvr {
@@ -30,9 +44,11 @@ namespace kvr {
 namespace {
 
 constexpr int kConsumerWarps = kGemvRows / 16;   // 8
-constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kConsumers = kConsumerWarps * 32;  // 256
+constexpr int kThreads = kConsumers + 32;
 constexpr int kWTileBytes = kGemvRows * 128;       // 16 KB
 constexpr int kSTileBytes = kGemvRows * 16;        // 2 KB
+constexpr int kTileLd = kGemvRows + 4;             // fp32 result tile row stride (bank spread)
 
 template <int NT>
 struct GemvCfg {
@@ -42,6 +58,8 @@ struct GemvCfg {
   static constexpr int kStageBytes = kWTileBytes + kXTileBytes + kSTileBytes;
   static constexpr int kStages = 4;
   static constexpr int kSmem = kStages * kStageBytes + 1024;  // + alignment slack
+  // the result tile reuses stage 0 once every stage has been consumed
+  static_assert(kXRows * kTileLd * 4 <= kStageBytes, "result tile must fit in one stage");
 };
 
 // 8 int4 codes of one 32-bit word -> 4 bf16x2 registers holding code values.
@@ -60,29 +78,126 @@ __device__ __forceinline__ void dequant_word(uint32_t w, uint32_t r[4]) {
   }
 }
 
-template <int NT>
-__global__ void __launch_bounds__(kThreads, 1) gemv_int4_kernel(const __grid_constant__ GemvParams p) {
+// barrier of the eight consumer warps (the producer warp has left)
+__device__ __forceinline__ void consumers_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+
+// ---------------------------------------------------------------- epilogues
+// ct: the tile's fp32 results [token][kTileLd] for tokens < p.mb
+
+__device__ __forceinline__ void epi_qkv(const GemvParams& p, const GemvSeg& seg, int s, int row0,
+                                        const float* ct, int tid) {
+  const int d = p.d, half = d >> 1;
+  const int nv = min(kGemvRows, seg.N - row0);
+  const int hd0 = row0 / d;
+  if (s < 2) {
+    const int npairs = nv >> 1;
+    const int G = p.Hq / p.Hkv;
+    for (int idx = tid; idx < p.mb * npairs; idx += kConsumers) {
+      const int t = idx / npairs, pr = idx % npairs;
+      const int hh = pr / half, j = pr % half;
+      const int col = hh * d + j;
+      const float x1 = ct[t * kTileLd + col];
+      const float x2 = ct[t * kTileLd + col + half];
+      const int i = p.c0 + t;
+      const float2 cs = p.rope[(long long)i * half + j];
+      const float y1 = x1 * cs.x - x2 * cs.y;
+      const float y2 = x2 * cs.x + x1 * cs.y;
+      const int hd = hd0 + hh;
+      __nv_bfloat16* dst =
+          s == 0 ? p.q + (((long long)(hd / G) * p.rows.m + i) * G + hd % G) * d
+                 : p.arena + p.k_off + ((long long)hd * p.cap + p.rows.P + i) * d;
+      dst[j] = __float2bfloat16_rn(y1);
+      dst[j + half] = __float2bfloat16_rn(y2);
+    }
+  } else {
+    // V^T: row (head, element) of the slot holds consecutive positions
+    for (int idx = tid; idx < p.mb * nv; idx += kConsumers) {
+      const int t = idx % p.mb, col = idx / p.mb;
+      const int hd = hd0 + col / d, e = col % d;
+      p.arena[p.v_off + ((long long)hd * d + e) * p.cap + p.rows.P + p.c0 + t] =
+          __float2bfloat16_rn(ct[t * kTileLd + col]);
+    }
+  }
+}
+
+__device__ __forceinline__ void epi_resid(const GemvParams& p, int row0, const float* ct, int tid) {
+  const int nv = min(kGemvRows, p.H - row0);
+  for (int idx = tid; idx < p.mb * (kGemvRows / 4); idx += kConsumers) {
+    const int t = idx / (kGemvRows / 4), c4 = (idx % (kGemvRows / 4)) * 4;
+    if (c4 >= nv) continue;
+    const long long i = p.c0 + t;
+    float4* hp = reinterpret_cast<float4*>(p.h + i * p.H + row0 + c4);
+    const float4 y = *reinterpret_cast<const float4*>(ct + t * kTileLd + c4);
+    float4 hv = *hp;
+    hv.x += y.x; hv.y += y.y; hv.z += y.z; hv.w += y.w;
+    *hp = hv;
+    if (p.out) {
+      uint2 o;
+      o.x = dev::pack_bf16x2(hv.x, hv.y);
+      o.y = dev::pack_bf16x2(hv.z, hv.w);
+      *reinterpret_cast<uint2*>(p.out + i * p.ldout + row0 + c4) = o;
+    }
+  }
+}
+
+__device__ __forceinline__ void epi_swiglu(const GemvParams& p, int row0, const float* ct, int tid) {
+  const int nv = min(64, p.F - row0);
+  for (int idx = tid; idx < p.mb * 64; idx += kConsumers) {
+    const int t = idx >> 6, j = idx & 63;
+    if (j >= nv) continue;
+    const float g = ct[t * kTileLd + j], u = ct[t * kTileLd + 64 + j];
+    const float sg = g / (1.f + expf(-g));
+    p.z[(long long)(p.c0 + t) * p.F + row0 + j] = __float2bfloat16_rn(sg * u);
+  }
+}
+
+__device__ __forceinline__ void epi_cast(const GemvParams& p, const GemvSeg& seg, int row0,
+                                         const float* ct, int tid) {
+  const int nv = min(kGemvRows, seg.N - row0);
+  for (int idx = tid; idx < p.mb * kGemvRows; idx += kConsumers) {
+    const int t = idx / kGemvRows, j = idx % kGemvRows;
+    if (j >= nv) continue;
+    p.out[(long long)(p.c0 + t) * p.ldout + seg.col0 + row0 + j] = __float2bfloat16_rn(ct[t * kTileLd + j]);
+  }
+}
+
+// CTA owning unit u of the launch (units are tile-major: u = tile * ksteps + step)
+__device__ __forceinline__ int unit_owner(long long u, int units, int ctas) {
+  return (int)(((u + 1) * ctas - 1) / units);
+}
+
+constexpr int kMaxOwnTiles = 16;   // tiles one CTA may finish (host keeps it below)
+
+// two CTAs per SM for up to 16 tokens (the host sizes the grid for it)
+template <int NT, int EPI>
+__global__ void __launch_bounds__(kThreads, NT == 4 ? 1 : 2) gemv_int4_kernel(const __grid_constant__ GemvParams p) {
   using C = GemvCfg<NT>;
+  constexpr bool kPair = EPI == kGemvEpiSwiglu;   // tile = 64 gate rows + 64 up rows
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[C::kStages];
   __shared__ __align__(8) uint64_t empty_bar[C::kStages];
   __shared__ int abort_flag;
+  __shared__ int n_own;
+  __shared__ int own_tiles[kMaxOwnTiles];
   volatile int* abort_v = &abort_flag;
 
   const uint32_t base = (dev::smem_u32(smem_raw) + 1023u) & ~1023u;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // which segment / row tile / k range
-  const int tile = blockIdx.x;
-  int s = 0;
-  while (s + 1 < p.nseg && tile >= p.seg[s + 1].tile0) ++s;
-  const GemvSeg& seg = p.seg[s];
-  const int row0 = (tile - seg.tile0) * kGemvRows;
-  const int split = blockIdx.y;
-  const int ks0 = (int)((long long)split * p.ksteps / p.ksplit);
-  const int ks1 = (int)((long long)(split + 1) * p.ksteps / p.ksplit);
-  const int nk = ks1 - ks0;
+  // this CTA's contiguous range of (tile, k-step) units
+  const int units = p.tiles * p.ksteps;
+  const int u0 = (int)((long long)blockIdx.x * units / p.ctas);
+  const int u1 = (int)((long long)(blockIdx.x + 1) * units / p.ctas);
+  const int nk = u1 - u0;
+  // segment and first weight row of a tile
+  auto tile_seg = [&](int tile) {
+    int s = 0;
+    if (!kPair)
+      while (s + 1 < p.nseg && tile >= p.seg[s + 1].tile0) ++s;
+    return s;
+  };
+  auto tile_row0 = [&](int tile, int s) { return kPair ? tile * 64 : (tile - p.seg[s].tile0) * kGemvRows; };
 
   dev::pdl_trigger();
   if (threadIdx.x == 0) {
@@ -91,6 +206,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_int4_kernel(const __grid_con
       dev::mbar_init(dev::smem_u32(&empty_bar[i]), kConsumerWarps);
     }
     *abort_v = 0;
+    n_own = 0;
     dev::fence_mbar_init();
   }
   __syncthreads();
@@ -98,34 +214,64 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_int4_kernel(const __grid_con
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      dev::prefetch_tmap(&seg.tw);
-      dev::prefetch_tmap(&seg.ts);
+      for (int i = 0; i < p.nseg; ++i) {
+        dev::prefetch_tmap(&p.seg[i].tw);
+        dev::prefetch_tmap(&p.seg[i].ts);
+      }
+      if (kPair) {
+        dev::prefetch_tmap(&p.seg[1].tw);
+        dev::prefetch_tmap(&p.seg[1].ts);
+      }
       dev::prefetch_tmap(&p.tx);
       const uint64_t pol = dev::policy_evict_first();
+      auto load_w = [&](uint32_t sb, uint32_t fb, int u) {
+        const int tile = u / p.ksteps, ks = u % p.ksteps;
+        const int s = tile_seg(tile);
+        const int row0 = tile_row0(tile, s);
+        const uint32_t sc = sb + kWTileBytes + C::kXTileBytes;
+        if (kPair) {
+          dev::tma_load_2d_hint(sb, &p.seg[0].tw, ks * 128, row0, fb, pol);
+          dev::tma_load_2d_hint(sb + kWTileBytes / 2, &p.seg[1].tw, ks * 128, row0, fb, pol);
+          dev::tma_load_2d_hint(sc, &p.seg[0].ts, ks * 8, row0, fb, pol);
+          dev::tma_load_2d_hint(sc + kSTileBytes / 2, &p.seg[1].ts, ks * 8, row0, fb, pol);
+        } else {
+          dev::tma_load_2d_hint(sb, &p.seg[s].tw, ks * 128, row0, fb, pol);
+          dev::tma_load_2d_hint(sc, &p.seg[s].ts, ks * 8, row0, fb, pol);
+        }
+      };
+      auto prefetch_w = [&](int u) {
+        const int tile = u / p.ksteps, ks = u % p.ksteps;
+        const int s = tile_seg(tile);
+        const int row0 = tile_row0(tile, s);
+        if (kPair) {
+          dev::tma_prefetch_2d(&p.seg[0].tw, ks * 128, row0);
+          dev::tma_prefetch_2d(&p.seg[1].tw, ks * 128, row0);
+          dev::tma_prefetch_2d(&p.seg[0].ts, ks * 8, row0);
+          dev::tma_prefetch_2d(&p.seg[1].ts, ks * 8, row0);
+        } else {
+          dev::tma_prefetch_2d(&p.seg[s].tw, ks * 128, row0);
+          dev::tma_prefetch_2d(&p.seg[s].ts, ks * 8, row0);
+        }
+      };
+      auto load_x = [&](uint32_t sb, uint32_t fb, int u) {
+        const int ks = u % p.ksteps;
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          dev::tma_load_2d(sb + kWTileBytes + j * C::kXBoxBytes, &p.tx, ks * kGemvKStep + 64 * j, p.c0, fb);
+      };
       // Weights do not depend on earlier launches: fill the ring's weight and
       // scale tiles and pull the rest of this CTA's weights toward L2 before
       // waiting for the previous launch; the activations follow the wait.
       const int pre = nk < C::kStages ? nk : C::kStages;
       for (int it = 0; it < pre; ++it) {
-        const uint32_t sb = base + it * C::kStageBytes;
         const uint32_t fb = dev::smem_u32(&full_bar[it]);
         dev::mbar_arrive_expect_tx(fb, C::kStageBytes);
-        dev::tma_load_2d_hint(sb, &seg.tw, (ks0 + it) * 128, row0, fb, pol);
-        dev::tma_load_2d_hint(sb + kWTileBytes + C::kXTileBytes, &seg.ts, (ks0 + it) * 8, row0, fb, pol);
+        load_w(base + it * C::kStageBytes, fb, u0 + it);
       }
-      for (int it = pre; it < nk; ++it) {
-        dev::tma_prefetch_2d(&seg.tw, (ks0 + it) * 128, row0);
-        dev::tma_prefetch_2d(&seg.ts, (ks0 + it) * 8, row0);
-      }
+      for (int it = pre; it < nk; ++it) prefetch_w(u0 + it);
       dev::pdl_wait();
-      for (int it = 0; it < pre; ++it) {
-        const uint32_t sb = base + it * C::kStageBytes;
-        const uint32_t fb = dev::smem_u32(&full_bar[it]);
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          dev::tma_load_2d(sb + kWTileBytes + j * C::kXBoxBytes, &p.tx, (ks0 + it) * kGemvKStep + 64 * j,
-                           p.c0, fb);
-      }
+      for (int it = 0; it < pre; ++it)
+        load_x(base + it * C::kStageBytes, dev::smem_u32(&full_bar[it]), u0 + it);
       int issued = pre;
       for (int it = pre; it < nk; ++it) {
         const int st = it % C::kStages;
@@ -137,13 +283,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_int4_kernel(const __grid_con
         const uint32_t sb = base + st * C::kStageBytes;
         const uint32_t fb = dev::smem_u32(&full_bar[st]);
         dev::mbar_arrive_expect_tx(fb, C::kStageBytes);
-        const int ks = ks0 + it;
-        dev::tma_load_2d_hint(sb, &seg.tw, ks * 128, row0, fb, pol);
-        dev::tma_load_2d_hint(sb + kWTileBytes + C::kXTileBytes, &seg.ts, ks * 8, row0, fb, pol);
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          dev::tma_load_2d(sb + kWTileBytes + j * C::kXBoxBytes, &p.tx, ks * kGemvKStep + 64 * j,
-                           p.c0, fb);
+        load_w(sb, fb, u0 + it);
+        load_x(sb, fb, u0 + it);
         ++issued;
       }
       // never leave the CTA with copies in flight: wait (bounded) for the last
@@ -157,7 +298,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_int4_kernel(const __grid_con
   }
 
   // -------------------------------------------------------------- consumers
-  dev::pdl_wait();                  // the partial sums are written below
+  dev::pdl_wait();                  // results are written below
+  const int tid = threadIdx.x;      // 0..255 over the consumer warps
   const int r = lane >> 2;          // fragment row 0..7
   const int c = lane & 3;           // fragment column pair
   const int rho0 = warp * 16 + r;   // tile rows of this thread: rho0 and rho0+8
@@ -168,64 +310,119 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_int4_kernel(const __grid_con
     for (int e = 0; e < 4; ++e) acc[t][e] = 0.f;
 
   const float zero4[4] = {0.f, 0.f, 0.f, 0.f};
+  // A wait that gives up marks the CTA aborted; from then on the warps skip
+  // the work and the waits but still pass every consumer barrier, so no warp
+  // is left waiting for one that has stopped.
+  bool ok = true;                   // warp-uniform
   for (int it = 0; it < nk; ++it) {
     const int st = it % C::kStages;
     const uint32_t use = (uint32_t)(it / C::kStages);
-    if (!dev::mbar_wait(dev::smem_u32(&full_bar[st]), use & 1, p.status) || *abort_v) {
-      *abort_v = 1;
-      break;
+    if (ok) {
+      const bool got = dev::mbar_wait(dev::smem_u32(&full_bar[st]), use & 1, p.status) && !*abort_v;
+      ok = __all_sync(0xffffffffu, got);
+      if (!ok && lane == 0) *abort_v = 1;
     }
-    const uint32_t wt = base + st * C::kStageBytes;
-    const uint32_t xt = wt + kWTileBytes;
-    const uint32_t stile = xt + C::kXTileBytes;
-    const uint4 sc0 = dev::lds128(stile + rho0 * 16);
-    const uint4 sc1 = dev::lds128(stile + (rho0 + 8) * 16);
-    const __half* s0h = reinterpret_cast<const __half*>(&sc0);
-    const __half* s1h = reinterpret_cast<const __half*>(&sc1);
+    if (ok) {
+      const uint32_t wt = base + st * C::kStageBytes;
+      const uint32_t xt = wt + kWTileBytes;
+      const uint32_t stile = xt + C::kXTileBytes;
+      const uint4 sc0 = dev::lds128(stile + rho0 * 16);
+      const uint4 sc1 = dev::lds128(stile + (rho0 + 8) * 16);
+      const __half* s0h = reinterpret_cast<const __half*>(&sc0);
+      const __half* s1h = reinterpret_cast<const __half*>(&sc1);
 #pragma unroll
-    for (int g = 0; g < 8; ++g) {
-      const uint32_t w0 = dev::lds32(wt + dev::swz128(rho0, g) + 4 * c);
-      const uint32_t w1 = dev::lds32(wt + dev::swz128(rho0 + 8, g) + 4 * c);
-      uint32_t q0[4], q1[4];
-      dequant_word(w0, q0);
-      dequant_word(w1, q1);
-      const uint32_t a_lo[4] = {q0[0], q1[0], q0[1], q1[1]};  // inputs 0..15 of the group
-      const uint32_t a_hi[4] = {q0[2], q1[2], q0[3], q1[3]};  // inputs 16..31
-      const float sr0 = __half2float(s0h[g]);
-      const float sr1 = __half2float(s1h[g]);
+      for (int g = 0; g < 8; ++g) {
+        const uint32_t w0 = dev::lds32(wt + dev::swz128(rho0, g) + 4 * c);
+        const uint32_t w1 = dev::lds32(wt + dev::swz128(rho0 + 8, g) + 4 * c);
+        uint32_t q0[4], q1[4];
+        dequant_word(w0, q0);
+        dequant_word(w1, q1);
+        const uint32_t a_lo[4] = {q0[0], q1[0], q0[1], q1[1]};  // inputs 0..15 of the group
+        const uint32_t a_hi[4] = {q0[2], q1[2], q0[3], q1[3]};  // inputs 16..31
+        const float sr0 = __half2float(s0h[g]);
+        const float sr1 = __half2float(s1h[g]);
 #pragma unroll
-      for (int t = 0; t < NT; ++t) {
-        // B fragments: tokens t*8 .. t*8+7, inputs 32g + 8q .. +7 for q = 0..3
-        const int n = t * 8 + (lane & 7);
-        const int q = lane >> 3;
-        const int box = g >> 1;
-        const int chunk = 4 * (g & 1) + q;
-        uint32_t b0, b1, b2, b3;
-        dev::ldmatrix_x4(xt + box * C::kXBoxBytes + dev::swz128(n, chunk), b0, b1, b2, b3);
-        float tmp[4];
-        dev::mma_bf16_16816(tmp, a_lo, b0, b1, zero4);
-        dev::mma_bf16_16816(tmp, a_hi, b2, b3, tmp);
-        acc[t][0] = fmaf(sr0, tmp[0], acc[t][0]);
-        acc[t][1] = fmaf(sr0, tmp[1], acc[t][1]);
-        acc[t][2] = fmaf(sr1, tmp[2], acc[t][2]);
-        acc[t][3] = fmaf(sr1, tmp[3], acc[t][3]);
+        for (int t = 0; t < NT; ++t) {
+          // B fragments: tokens t*8 .. t*8+7, inputs 32g + 8q .. +7 for q = 0..3
+          const int n = t * 8 + (lane & 7);
+          const int q = lane >> 3;
+          const int box = g >> 1;
+          const int chunk = 4 * (g & 1) + q;
+          uint32_t b0, b1, b2, b3;
+          dev::ldmatrix_x4(xt + box * C::kXBoxBytes + dev::swz128(n, chunk), b0, b1, b2, b3);
+          float tmp[4];
+          dev::mma_bf16_16816(tmp, a_lo, b0, b1, zero4);
+          dev::mma_bf16_16816(tmp, a_hi, b2, b3, tmp);
+          acc[t][0] = fmaf(sr0, tmp[0], acc[t][0]);
+          acc[t][1] = fmaf(sr0, tmp[1], acc[t][1]);
+          acc[t][2] = fmaf(sr1, tmp[2], acc[t][2]);
+          acc[t][3] = fmaf(sr1, tmp[3], acc[t][3]);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) dev::mbar_arrive(dev::smem_u32(&empty_bar[st]));
+    }
+
+    // end of this CTA's part of a tile: publish it as one contribution
+    const int u = u0 + it;
+    const int tile = u / p.ksteps;
+    if (u % p.ksteps == p.ksteps - 1 || it == nk - 1) {
+      const long long tu0 = (long long)tile * p.ksteps;
+      const int first = unit_owner(tu0, units, p.ctas);
+      const int ncon = unit_owner(tu0 + p.ksteps - 1, units, p.ctas) - first + 1;
+      float* tp = p.part + ((long long)tile * p.maxc + (blockIdx.x - first)) * (kGemvMaxCols * kGemvRows);
+#pragma unroll
+      for (int t = 0; t < NT; ++t)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int tok = t * 8 + 2 * c + (e & 1);
+          if (ok && tok < p.mb) tp[tok * kGemvRows + rho0 + (e >> 1) * 8] = acc[t][e];
+          acc[t][e] = 0.f;
+        }
+      __threadfence();
+      consumers_sync();
+      if (tid == 0 && !*abort_v) {
+        const int done = atomicAdd(p.counters + tile, 1) + 1;
+        if (done == ncon) {
+          p.counters[tile] = 0;   // ready for the next launch
+          if (n_own < kMaxOwnTiles) own_tiles[n_own] = tile;
+          ++n_own;
+        }
       }
     }
-    __syncwarp();
-    if (lane == 0) dev::mbar_arrive(dev::smem_u32(&empty_bar[st]));
   }
-  if (*abort_v) return;
-
-  // write this split's partial sums: part[split][token][col0 + row]
-  float* out = p.part + (long long)split * p.plane;
-#pragma unroll
-  for (int t = 0; t < NT; ++t) {
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int tok = t * 8 + 2 * c + (e & 1);
-      const int row = row0 + rho0 + (e >> 1) * 8;
-      if (tok < p.mb && row < seg.N) out[(long long)tok * p.ldo + seg.col0 + row] = acc[t][e];
+  consumers_sync();
+  if (tid == 0 && *abort_v) n_own = 0;          // an aborted CTA finishes nothing
+  // ----------------------- tiles this CTA finished last: reduce, then epilogue
+  consumers_sync();                            // every stage read; own_tiles visible
+  float* ct = reinterpret_cast<float*>(smem_raw + (base - dev::smem_u32(smem_raw)));
+  const int n_done = min(n_own, kMaxOwnTiles);
+  for (int k = 0; k < n_done; ++k) {
+    const int tile = own_tiles[k];
+    const long long tu0 = (long long)tile * p.ksteps;
+    const int first = unit_owner(tu0, units, p.ctas);
+    const int ncon = unit_owner(tu0 + p.ksteps - 1, units, p.ctas) - first + 1;
+    __threadfence();
+    const float* t0p = p.part + (long long)tile * p.maxc * (kGemvMaxCols * kGemvRows);
+    for (int idx = tid; idx < p.mb * (kGemvRows / 4); idx += kConsumers) {
+      const int tok = idx / (kGemvRows / 4), r4 = (idx % (kGemvRows / 4)) * 4;
+      // contributions in contributor order: the sum does not depend on timing
+      float4 v = __ldcg(reinterpret_cast<const float4*>(t0p + tok * kGemvRows + r4));
+      for (int j = 1; j < ncon; ++j) {
+        const float4 w = __ldcg(reinterpret_cast<const float4*>(t0p + (long long)j * (kGemvMaxCols * kGemvRows) +
+                                                                tok * kGemvRows + r4));
+        v.x += w.x; v.y += w.y; v.z += w.z; v.w += w.w;
+      }
+      *reinterpret_cast<float4*>(ct + tok * kTileLd + r4) = v;
     }
+    consumers_sync();
+    const int s = tile_seg(tile);
+    const int row0 = tile_row0(tile, s);
+    if (EPI == kGemvEpiQKV) epi_qkv(p, p.seg[s], s, row0, ct, tid);
+    else if (EPI == kGemvEpiResid) epi_resid(p, row0, ct, tid);
+    else if (EPI == kGemvEpiSwiglu) epi_swiglu(p, row0, ct, tid);
+    else epi_cast(p, p.seg[s], row0, ct, tid);
+    consumers_sync();
   }
 }
 
@@ -282,24 +479,45 @@ int gemv_int4_smem(int nt) {
   }
 }
 
-cudaError_t gemv_setup() {
-  cudaError_t e;
-  e = cudaFuncSetAttribute(gemv_int4_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           GemvCfg<1>::kSmem);
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(gemv_int4_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           GemvCfg<2>::kSmem);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(gemv_int4_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              GemvCfg<4>::kSmem);
+namespace {
+
+template <int NT>
+cudaError_t setup_nt() {
+  void (*ks[4])(GemvParams) = {gemv_int4_kernel<NT, 0>, gemv_int4_kernel<NT, 1>, gemv_int4_kernel<NT, 2>,
+                               gemv_int4_kernel<NT, 3>};
+  for (auto k : ks) {
+    const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, GemvCfg<NT>::kSmem);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
-cudaError_t launch_gemv_int4(const GemvParams& p, int total_tiles, int nt, cudaStream_t st) {
-  const dim3 grid(total_tiles, p.ksplit);
+template <int NT>
+cudaError_t launch_nt(const GemvParams& p, dim3 grid, cudaStream_t st) {
+  switch (p.epi) {
+    case kGemvEpiQKV: return launch_k(gemv_int4_kernel<NT, 0>, grid, kThreads, GemvCfg<NT>::kSmem, st, p);
+    case kGemvEpiResid: return launch_k(gemv_int4_kernel<NT, 1>, grid, kThreads, GemvCfg<NT>::kSmem, st, p);
+    case kGemvEpiSwiglu: return launch_k(gemv_int4_kernel<NT, 2>, grid, kThreads, GemvCfg<NT>::kSmem, st, p);
+    case kGemvEpiCast: return launch_k(gemv_int4_kernel<NT, 3>, grid, kThreads, GemvCfg<NT>::kSmem, st, p);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+cudaError_t gemv_setup() {
+  cudaError_t e = setup_nt<1>();
+  if (e == cudaSuccess) e = setup_nt<2>();
+  if (e == cudaSuccess) e = setup_nt<4>();
+  return e;
+}
+
+cudaError_t launch_gemv_int4(const GemvParams& p, int nt, cudaStream_t st) {
+  const dim3 grid(p.ctas);
   switch (nt) {
-    case 1: return launch_k(gemv_int4_kernel<1>, grid, kThreads, GemvCfg<1>::kSmem, st, p);
-    case 2: return launch_k(gemv_int4_kernel<2>, grid, kThreads, GemvCfg<2>::kSmem, st, p);
-    default: return launch_k(gemv_int4_kernel<4>, grid, kThreads, GemvCfg<4>::kSmem, st, p);
+    case 1: return launch_nt<1>(p, grid, st);
+    case 2: return launch_nt<2>(p, grid, st);
+    default: return launch_nt<4>(p, grid, st);
   }
 }
 

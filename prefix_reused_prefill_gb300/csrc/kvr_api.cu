@@ -33,6 +33,7 @@ bool kvr::pdl_enabled() {
 namespace {
 
 constexpr size_t kAlign = 256;
+constexpr int kCounters = 16384;   // per-tile arrival counters of the fused GEMV epilogues
 inline size_t align_up(size_t x, size_t a = kAlign) { return (x + a - 1) / a * a; }
 
 enum ProfClass { kProj = 0, kAttn = 1, kEpi = 2, kMatch = 3 };
@@ -86,7 +87,7 @@ int attn_nsplit(int Hkv, int R, int kend_max, int target) {
 }
 
 struct ScratchLayout {
-  size_t status, prompt, slot_len, match_out, rope, h, a, q, o, z, part, opart, ml, total;
+  size_t status, counters, prompt, slot_len, match_out, rope, h, a, q, o, z, part, opart, ml, total;
   size_t part_floats, opart_floats, ml_count;
 };
 
@@ -98,6 +99,7 @@ ScratchLayout scratch_layout(const kvr_config* c) {
   size_t off = 0;
   auto take = [&](size_t bytes) { size_t at = off; off = align_up(off + std::max<size_t>(bytes, 1)); return at; };
   L.status = take(64);
+  L.counters = take(kCounters * 4);
   L.prompt = take((size_t)c->capacity * 4);
   L.slot_len = take(KVR_MAX_SLOTS * 4);
   L.match_out = take((size_t)(S + 1) * S * 4);
@@ -107,7 +109,8 @@ ScratchLayout scratch_layout(const kvr_config* c) {
   L.q = take(M * QD * 2);
   L.o = take(M * QD * 2);
   L.z = take(M * F * 2);
-  L.part_floats = (size_t)kMaxKSplit * kGemvMaxCols * max_ldo(c);
+  // GEMV: [ksplit][tiles][32][128] tile-major partials (tiles round each segment up)
+  L.part_floats = (size_t)kMaxKSplit * kGemvMaxCols * (max_ldo(c) + 3 * kGemvRows);
   if (c->weight_format == KVR_WEIGHTS_INT4_G32)
     L.part_floats = std::max(L.part_floats, (size_t)kGemmMaxSplit * kGemmMaxTok *
                                                 std::max(qkv_cols(c), c->hidden));
@@ -163,6 +166,7 @@ struct kvr_ctx {
   ScratchLayout sl{};
   // scratch views
   int* status = nullptr;
+  int* counters = nullptr;
   int32_t* prompt = nullptr;
   int* slot_len = nullptr;
   int32_t* match_out = nullptr;
@@ -362,70 +366,153 @@ int project_gemm(kvr_ctx* c, cudaStream_t st, const Seg* segs, int nseg, const C
   return KVR_OK;
 }
 
+// The epilogue the small-m int4 GEMV applies itself (see GemvEpi).
+struct Fused {
+  int epi = kGemvEpiResid;
+  const RowMap* rows = nullptr;           // QKV
+  long long k_off = 0, v_off = 0;         // QKV
+  __nv_bfloat16* out = nullptr;           // Resid (last layer) / Cast
+  const __nv_bfloat16* norm_gain = nullptr;  // Resid: RMSNorm the new rows into c->a
+};
+
+// Small-m int4 passes: the GEMV with its fused epilogue (plus the RMSNorm of
+// the finished rows after a residual projection).
+int project_gemv_int4(kvr_ctx* c, cudaStream_t st, const Seg* segs, int nseg, const CUtensorMap* tmx,
+                      int K, int m, const Fused& fz) {
+  const kvr_config& cfg = c->cfg;
+  const bool pair = fz.epi == kGemvEpiSwiglu;
+  GemvParams p;
+  memset(&p, 0, sizeof p);
+  p.K = K;
+  p.ksteps = K / kGemvKStep;
+  p.status = c->status;
+  p.part = c->part;
+  p.epi = fz.epi;
+  p.counters = c->counters;
+  int tiles = 0;
+  if (pair) {
+    const WMap* g = weight_map(c, segs[0].w, segs[0].s, segs[0].N, K, 64);
+    const WMap* u = weight_map(c, segs[1].w, segs[1].s, segs[1].N, K, 64);
+    if (!g || !u) return fail(c, KVR_ERR_CUDA, "cuTensorMapEncodeTiled failed for a weight matrix");
+    p.nseg = 1;
+    p.seg[0].tw = g->w; p.seg[0].ts = g->s; p.seg[0].N = segs[0].N;
+    p.seg[1].tw = u->w; p.seg[1].ts = u->s; p.seg[1].N = segs[1].N;
+    tiles = (segs[0].N + 63) / 64;
+    p.seg[0].tiles = tiles;
+  } else {
+    p.nseg = nseg;
+    int col = 0;
+    for (int i = 0; i < nseg; ++i) {
+      GemvSeg& g = p.seg[i];
+      const WMap* wm = weight_map(c, segs[i].w, segs[i].s, segs[i].N, K);
+      if (!wm) return fail(c, KVR_ERR_CUDA, "cuTensorMapEncodeTiled failed for a weight matrix");
+      g.tw = wm->w;
+      g.ts = wm->s;
+      g.N = segs[i].N;
+      g.col0 = col;
+      g.tile0 = tiles;
+      g.tiles = (segs[i].N + kGemvRows - 1) / kGemvRows;
+      col += segs[i].N;
+      tiles += g.tiles;
+    }
+  }
+  if (tiles > kCounters) return fail(c, KVR_ERR_UNSUPPORTED, "projection has %d tiles (max %d)", tiles, kCounters);
+  p.tiles = tiles;
+  if (fz.rows) p.rows = *fz.rows;
+  p.rope = c->rope;
+  p.q = c->q;
+  p.arena = reinterpret_cast<__nv_bfloat16*>(c->arena);
+  p.k_off = fz.k_off;
+  p.v_off = fz.v_off;
+  p.cap = cfg.capacity;
+  p.Hq = cfg.n_q_heads;
+  p.Hkv = cfg.n_kv_heads;
+  p.d = cfg.head_dim;
+  p.h = c->h;
+  p.H = cfg.hidden;
+  p.out = fz.out;
+  p.ldout = cfg.hidden;
+  p.z = c->z;
+  p.F = cfg.ffn;
+  for (int c0 = 0; c0 < m; c0 += kGemvMaxCols) {
+    const int mb = std::min(kGemvMaxCols, m - c0);
+    p.c0 = c0;
+    p.mb = mb;
+    const int nt = mb <= 8 ? 1 : (mb <= 16 ? 2 : 4);
+    const int per_sm = nt == 4 ? 1 : 2;   // CTAs resident per SM (shared memory, registers)
+    // one resident wave of CTAs, each an equal run of (tile, k-step) units
+    const int units = tiles * p.ksteps;
+    int ctas = std::min(units, c->n_sms * per_sm);
+    int maxc = 0;
+    for (int tries = 0;; ++tries) {
+      if (tries == 64) return fail(c, KVR_ERR_UNSUPPORTED, "no GEMV decomposition fits the scratch buffer");
+      const int upc = units / ctas;                       // fewest units of a CTA
+      maxc = (p.ksteps + upc - 1) / upc + 1;              // most contributors of a tile
+      const int most_tiles = ((units + ctas - 1) / ctas + p.ksteps - 1) / p.ksteps + 1;
+      const bool fits = (size_t)tiles * maxc * kGemvMaxCols * kGemvRows <= c->sl.part_floats;
+      if (fits && most_tiles <= 16) break;
+      if (!fits && ctas > 1) ctas = std::max(1, ctas * 3 / 4);
+      else if (most_tiles > 16 && ctas < units) ctas = std::min(units, ctas * 2);
+      else return fail(c, KVR_ERR_UNSUPPORTED, "no GEMV decomposition fits the scratch buffer");
+    }
+    p.ctas = ctas;
+    p.maxc = maxc;
+    p.ksplit = 1;
+    p.tx = tmx[nt == 1 ? 0 : (nt == 2 ? 1 : 2)];
+    cudaError_t e;
+    {
+      Timed t(c, kProj, st);
+      e = launch_gemv_int4(p, nt, st);
+    }
+    if (e != cudaSuccess) return cuda_fail(c, e, "gemv_int4 launch");
+    if (fz.epi == kGemvEpiResid && fz.norm_gain) {
+      Timed t(c, kEpi, st);
+      e = launch_rmsnorm(c->h, c0, mb, cfg.hidden, fz.norm_gain, cfg.rms_eps, c->a, st);
+      if (e != cudaSuccess) return cuda_fail(c, e, "rmsnorm launch");
+    }
+  }
+  return KVR_OK;
+}
+
 template <class Epi>
 int project(kvr_ctx* c, cudaStream_t st, const Seg* segs, int nseg, Act act, int K, int m, Epi epi,
-            bool swiglu = false) {
+            const Fused& fz, bool swiglu = false) {
   const kvr_config& cfg = c->cfg;
   const CUtensorMap* tmx = act == Act::A ? c->tm_a : (act == Act::O ? c->tm_o : c->tm_z);
-  if (cfg.weight_format == KVR_WEIGHTS_INT4_G32 && m > kGemvMaxCols && !c->force_gemv)
-    return project_gemm(c, st, segs, nseg, tmx, K, m, swiglu, epi);
+  if (cfg.weight_format == KVR_WEIGHTS_INT4_G32) {
+    if (m > kGemvMaxCols && !c->force_gemv)
+      return project_gemm(c, st, segs, nseg, tmx, K, m, swiglu, epi);
+    return project_gemv_int4(c, st, segs, nseg, tmx, K, m, fz);
+  }
+  // bf16 weights: plain GEMV into partials, then the row-wise epilogue kernel
   GemvParams p;
   memset(&p, 0, sizeof p);
   p.nseg = nseg;
   p.K = K;
   p.status = c->status;
-  int col = 0, tiles = 0;
+  int col = 0;
   for (int i = 0; i < nseg; ++i) {
     GemvSeg& g = p.seg[i];
     g.N = segs[i].N;
     g.col0 = col;
-    g.tile0 = tiles;
-    g.tiles = (segs[i].N + kGemvRows - 1) / kGemvRows;
+    g.wbf = static_cast<const __nv_bfloat16*>(segs[i].w);
     col += segs[i].N;
-    tiles += g.tiles;
-    if (cfg.weight_format == KVR_WEIGHTS_INT4_G32) {
-      const WMap* wm = weight_map(c, segs[i].w, segs[i].s, segs[i].N, K);
-      if (!wm) return fail(c, KVR_ERR_CUDA, "cuTensorMapEncodeTiled failed for a weight matrix");
-      g.tw = wm->w;
-      g.ts = wm->s;
-    } else {
-      g.wbf = static_cast<const __nv_bfloat16*>(segs[i].w);
-    }
   }
   p.ldo = col;
   p.part = c->part;
-  const __nv_bfloat16* xbuf = act == Act::A ? c->a : (act == Act::O ? c->o : c->z);
-  p.x = xbuf;
-  p.ksteps = K / kGemvKStep;
+  p.x = act == Act::A ? c->a : (act == Act::O ? c->o : c->z);
+  p.ksplit = 1;
+  p.plane = (long long)kGemvMaxCols * p.ldo;
   for (int c0 = 0; c0 < m; c0 += kGemvMaxCols) {
     const int mb = std::min(kGemvMaxCols, m - c0);
     p.c0 = c0;
     p.mb = mb;
-    if (cfg.weight_format == KVR_WEIGHTS_INT4_G32) {
-      const int nt = mb <= 8 ? 1 : (mb <= 16 ? 2 : 4);
-      const int per_sm = nt == 4 ? 1 : 2;
-      int ks = (c->n_sms * per_sm + tiles / 2) / std::max(tiles, 1);
-      ks = std::max(1, std::min(ks, std::min(p.ksteps, kMaxKSplit)));
-      p.ksplit = ks;
-      p.plane = (long long)kGemvMaxCols * p.ldo;
-      p.tx = tmx[nt == 1 ? 0 : (nt == 2 ? 1 : 2)];
-      cudaError_t e;
-      {
-        Timed t(c, kProj, st);
-        e = launch_gemv_int4(p, tiles, nt, st);
-      }
-      if (e != cudaSuccess) return cuda_fail(c, e, "gemv_int4 launch");
-    } else {
-      p.ksplit = 1;
-      p.plane = (long long)kGemvMaxCols * p.ldo;
-      cudaError_t e;
-      {
-        Timed t(c, kProj, st);
-        e = launch_gemv_bf16(p, col, st);
-      }
-      if (e != cudaSuccess) return cuda_fail(c, e, "gemv_bf16 launch");
-    }
     cudaError_t e;
+    {
+      Timed t(c, kProj, st);
+      e = launch_gemv_bf16(p, col, st);
+    }
+    if (e != cudaSuccess) return cuda_fail(c, e, "gemv_bf16 launch");
     {
       Timed t(c, kEpi, st);
       e = epi(p.part, p.plane, p.ksplit, p.ldo, c0, mb);
@@ -542,11 +629,16 @@ int run_stack(kvr_ctx* c, int slot, const RowMap& rows, const void* hidden,
     {
       Seg segs[3] = {{W.wq, W.sq, Hq * d}, {W.wk, W.sk, Hkv * d}, {W.wv, W.sv, Hkv * d}};
       const long long koff = kv_offset(c, slot, l, 0), voff = kv_offset(c, slot, l, 1);
+      Fused fz;
+      fz.epi = kGemvEpiQKV;
+      fz.rows = &rows;
+      fz.k_off = koff;
+      fz.v_off = voff;
       int rc = project(c, st, segs, 3, Act::A, H, m, [&](const float* part, long long plane, int ks,
                                                           int ldo, int c0, int mb) {
         return launch_epi_qkv(part, plane, ks, ldo, c0, mb, rows, Hq, Hkv, d, c->rope, c->q, arena,
                               koff, voff, k.capacity, st);
-      });
+      }, fz);
       if (rc) return rc;
     }
     int rc = attention(c, st, slot, l, rows);
@@ -556,41 +648,53 @@ int run_stack(kvr_ctx* c, int slot, const RowMap& rows, const void* hidden,
       Seg so = {W.wo, W.so, H};
       if (k.attn_only) {
         __nv_bfloat16* dst = last ? static_cast<__nv_bfloat16*>(out) : c->a;
+        Fused fz;
+        fz.epi = kGemvEpiCast;
+        fz.out = dst;
         rc = project(c, st, &so, 1, Act::O, Hq * d, m,
                      [&](const float* part, long long plane, int ks, int ldo, int c0, int mb) {
                        return launch_epi_cast(part, plane, ks, ldo, c0, mb, H, dst, st);
-                     });
+                     }, fz);
         if (rc) return rc;
         continue;
       }
+      Fused fz;
+      fz.epi = kGemvEpiResid;
+      fz.norm_gain = static_cast<const __nv_bfloat16*>(W.norm_ffn);
       rc = project(c, st, &so, 1, Act::O, Hq * d, m,
                    [&](const float* part, long long plane, int ks, int ldo, int c0, int mb) {
                      return launch_epi_resid(part, plane, ks, ldo, c0, mb, H, c->h,
                                              static_cast<const __nv_bfloat16*>(W.norm_ffn),
                                              k.rms_eps, c->a, nullptr, st);
-                   });
+                   }, fz);
       if (rc) return rc;
     }
     // gate | up -> SwiGLU
     {
       Seg gu[2] = {{W.wg, W.sg, F}, {W.wu, W.su, F}};
+      Fused fz;
+      fz.epi = kGemvEpiSwiglu;
       rc = project(c, st, gu, 2, Act::A, H, m,
                    [&](const float* part, long long plane, int ks, int ldo, int c0, int mb) {
                      return launch_epi_swiglu(part, plane, ks, ldo, c0, mb, F, c->z, st);
                    },
-                   /*swiglu=*/true);
+                   fz, /*swiglu=*/true);
       if (rc) return rc;
     }
     // down + residual, then the next layer's attention norm (or the output)
     {
       Seg sd = {W.wd, W.sd, H};
       const __nv_bfloat16* gain = last ? nullptr : static_cast<const __nv_bfloat16*>(w[l + 1].norm_attn);
+      Fused fz;
+      fz.epi = kGemvEpiResid;
+      fz.norm_gain = gain;
+      fz.out = last ? static_cast<__nv_bfloat16*>(out) : nullptr;
       rc = project(c, st, &sd, 1, Act::Z, F, m,
                    [&](const float* part, long long plane, int ks, int ldo, int c0, int mb) {
                      return launch_epi_resid(part, plane, ks, ldo, c0, mb, H, c->h, gain, k.rms_eps,
                                              last ? nullptr : c->a,
                                              last ? static_cast<__nv_bfloat16*>(out) : nullptr, st);
-                   });
+                   }, fz);
       if (rc) return rc;
       e = trace(l + 1);
       if (e != cudaSuccess) return cuda_fail(c, e, "trace copy");
@@ -723,6 +827,7 @@ int kvr_ctx_create(const kvr_config* cfg, void* kv_arena, size_t arena_bytes, vo
   c->scratch = static_cast<uint8_t*>(scratch);
   uint8_t* s = c->scratch;
   c->status = reinterpret_cast<int*>(s + c->sl.status);
+  c->counters = reinterpret_cast<int*>(s + c->sl.counters);
   c->prompt = reinterpret_cast<int32_t*>(s + c->sl.prompt);
   c->slot_len = reinterpret_cast<int*>(s + c->sl.slot_len);
   c->match_out = reinterpret_cast<int32_t*>(s + c->sl.match_out);
@@ -777,6 +882,7 @@ int kvr_ctx_create(const kvr_config* cfg, void* kv_arena, size_t arena_bytes, vo
   // Positions past a slot's length are read (and multiplied by a zero weight)
   // when a key block is partly visible; zero the arena once so they are finite.
   e = cudaMemset(c->status, 0, 64);
+  if (e == cudaSuccess) e = cudaMemset(c->counters, 0, kCounters * 4);
   if (e == cudaSuccess) e = cudaMemset(c->arena, 0, (size_t)c->granted * slot_kv_bytes(cfg));
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e != cudaSuccess) {
@@ -970,6 +1076,8 @@ int kvr_sync_status(kvr_ctx* c, void* stream) {
   if (e == cudaSuccess) e = cudaStreamSynchronize(st);
   if (e != cudaSuccess) return cuda_fail(c, e, "status readback");
   if (word) {
+    // a launch that gave up may have left tile counters behind
+    cudaMemsetAsync(c->counters, 0, kCounters * 4, st);
     cudaMemsetAsync(c->status, 0, 4, st);
     cudaStreamSynchronize(st);
     return fail(c, KVR_ERR_TIMEOUT, "a device-side wait gave up (status %d)", word);

@@ -59,20 +59,47 @@ struct GemvSeg {
   int tiles;
 };
 
+// Epilogue the int4 GEMV applies itself (the last CTA of a tile to finish
+// adds the k-split partials in split order and then):
+enum GemvEpi : int {
+  kGemvEpiQKV = 0,     // RoPE q and k, round to bf16, write q, append K and V^T to the slot
+  kGemvEpiResid = 1,   // h += y (fp32 residual stream); optionally out = bf16(h)
+  kGemvEpiSwiglu = 2,  // tile = 64 gate rows + the same 64 up rows: z = bf16(silu(g) * u)
+  kGemvEpiCast = 3,    // out = bf16(y)
+};
+
 struct GemvParams {
-  GemvSeg seg[3];
+  GemvSeg seg[3];   // SwiGLU: seg[0] = gate, seg[1] = up (64-row boxes), nseg = 1
   CUtensorMap tx;   // activations bf16 [max_rows][K], box {64, 8*NT}, 128B swizzle
   const __nv_bfloat16* x;  // same activations, plain pointer (bf16 kernel)
   int nseg;
   int K;
-  int ksteps;
-  int ksplit;
+  int ksteps;       // 256-input steps along K
+  int ksplit;       // bf16 kernel only (always 1)
+  int ctas;         // int4 kernel: CTA i takes units [i*U/ctas, (i+1)*U/ctas), U = tiles*ksteps
+  int maxc;         // int4 kernel: partial slots per tile (>= contributors of any tile)
   int c0;           // first token of this pass
   int mb;           // tokens in this pass (<= kGemvMaxCols)
-  int ldo;          // partial row stride (total output columns)
-  long long plane;  // floats per split plane of the partials
-  float* part;      // [ksplit][kGemvMaxCols][ldo]
+  int ldo;          // partial row stride (total output columns; bf16 kernel)
+  long long plane;  // floats per split plane of the partials (bf16 kernel)
+  float* part;      // bf16 kernel: [kGemvMaxCols][ldo]; int4 kernel: [tiles][maxc][32][128]
   int* status;
+  // fused epilogue of the int4 kernel
+  int epi;          // GemvEpi
+  int tiles;        // tiles of this launch
+  int* counters;    // [tiles] contributor arrival counters; zero between launches
+  RowMap rows;      // QKV: row positions (row i is stored at rows.P + i)
+  const float2* rope;   // QKV: (cos, sin) [m][d/2]
+  __nv_bfloat16* q;     // QKV: [Hkv][m][G][d]
+  __nv_bfloat16* arena; // QKV: the slot arena
+  long long k_off, v_off;
+  int cap, Hq, Hkv, d;
+  float* h;             // Resid: [max_rows][H]
+  int H;
+  __nv_bfloat16* out;   // Resid (last layer) / Cast: bf16 [m][ldout], or null
+  int ldout;
+  __nv_bfloat16* z;     // Swiglu: [max_rows][F]
+  int F;
 };
 
 struct GemmSeg {
@@ -156,7 +183,7 @@ inline cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_
 cudaError_t launch_prefix_match(const int32_t* slot_tokens, const int* slot_len, int n_slots,
                                 int cap, const int32_t* prompt, int n, int32_t* out,
                                 cudaStream_t st);
-cudaError_t launch_gemv_int4(const GemvParams& p, int total_tiles, int nt, cudaStream_t st);
+cudaError_t launch_gemv_int4(const GemvParams& p, int nt, cudaStream_t st);
 cudaError_t launch_gemv_bf16(const GemvParams& p, int total_cols, cudaStream_t st);
 cudaError_t launch_gemm_int4_tc(const GemmParams& p, int total_tiles, cudaStream_t st);
 cudaError_t launch_attention(const AttnParams& p, int d, int row_warps, cudaStream_t st);
@@ -166,6 +193,9 @@ cudaError_t launch_rope_table(const RowMap& rows, int d, float theta, float2* ta
                               cudaStream_t st);
 cudaError_t launch_embed(const __nv_bfloat16* hidden, int m, int H, const __nv_bfloat16* gain,
                          float eps, float* h, __nv_bfloat16* a, cudaStream_t st);
+// a[c0 + t] = bf16(RMSNorm(h[c0 + t]) * gain) for t < mb
+cudaError_t launch_rmsnorm(const float* h, int c0, int mb, int H, const __nv_bfloat16* gain,
+                           float eps, __nv_bfloat16* a, cudaStream_t st);
 cudaError_t launch_epi_qkv(const float* part, long long plane, int ksplit, int ldo, int c0,
                            int mb, const RowMap& rows, int Hq, int Hkv, int d,
                            const float2* rope, __nv_bfloat16* q, __nv_bfloat16* arena,
