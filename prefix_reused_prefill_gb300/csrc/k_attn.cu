@@ -82,7 +82,6 @@ __global__ void __launch_bounds__((RW + 1) * 32) attn_kernel(const __grid_consta
   const int nblk = b1 - b0;
 
   dev::pdl_trigger();
-  dev::pdl_wait();   // q and the appended K/V come from the previous launch
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kStages; ++i) {
       dev::mbar_init(dev::smem_u32(&full_bar[i]), 1);
@@ -97,8 +96,24 @@ __global__ void __launch_bounds__((RW + 1) * 32) attn_kernel(const __grid_consta
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       dev::prefetch_tmap(&p.tkv);
-      int issued = 0;
-      for (int it = 0; it < nblk; ++it) {
+      dev::prefetch_tmap(&p.tvt);
+      // Blocks wholly inside the cached prefix were written by earlier calls:
+      // load them before waiting for the launch that appends this call's K/V.
+      int pre = 0;
+      while (pre < nblk && pre < C::kStages && (b0 + pre + 1) * kAttnKeys <= p.rows.P) {
+        const uint32_t sb = base + pre * C::kStageBytes;
+        const uint32_t fb = dev::smem_u32(&full_bar[pre]);
+        dev::mbar_arrive_expect_tx(fb, C::kStageBytes);
+        const int key0 = (b0 + pre) * kAttnKeys;
+#pragma unroll
+        for (int h = 0; h < C::kHalves; ++h)
+          dev::tma_load_2d(sb + h * (kAttnKeys * 128), &p.tkv, 64 * h, p.kbase + kv * p.cap + key0, fb);
+        dev::tma_load_2d(sb + C::kTileBytes, &p.tvt, key0, p.vtbase + kv * D, fb);
+        ++pre;
+      }
+      dev::pdl_wait();
+      int issued = pre;
+      for (int it = pre; it < nblk; ++it) {
         const int st = it % C::kStages;
         const uint32_t use = (uint32_t)(it / C::kStages);
         if (it >= C::kStages) {
@@ -129,6 +144,7 @@ __global__ void __launch_bounds__((RW + 1) * 32) attn_kernel(const __grid_consta
   }
 
   // -------------------------------------------------------------- consumers
+  dev::pdl_wait();   // q comes from the previous launch
   const int r = lane >> 2, c = lane & 3;
   const int rho0 = row_lo + warp * 16 + r;
   const RowInfo ri0 = row_info(p, kv, rho0);
@@ -285,8 +301,10 @@ __global__ void __launch_bounds__((RW + 1) * 32) attn_kernel(const __grid_consta
   }
 }
 
-// One warp per (token, head) row: merge the key splits' (O, max, sum) partials
-// in split order; each lane owns D/32 consecutive elements.
+// One warp per (token, head) row: merge the key splits' (O, max, sum)
+// partials.  Lane s holds split s's (max, sum) (and lane s-32 split s for
+// nsplit > 32); the split weights are broadcast with shuffles and each lane
+// accumulates D/32 consecutive elements over the splits in split order.
 template <int D>
 __global__ void __launch_bounds__(256) attn_combine_kernel(const __grid_constant__ AttnParams p) {
   dev::pdl_trigger();
@@ -296,22 +314,31 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const __grid_constant
   if (rowidx >= rows) return;
   const int lane = threadIdx.x & 31;
   constexpr int E = D / 32;
-  float M = -INFINITY;
-  for (int s = 0; s < p.nsplit; ++s) M = fmaxf(M, p.ml[s * rows + rowidx].x);
+  static_assert(kMaxSplits <= 64, "two split records per lane");
+  const int ns = p.nsplit;
+  const float2 ml0 = lane < ns ? p.ml[lane * rows + rowidx] : make_float2(-INFINITY, 0.f);
+  const float2 ml1 = lane + 32 < ns ? p.ml[(lane + 32) * rows + rowidx] : make_float2(-INFINITY, 0.f);
+  float M = fmaxf(ml0.x, ml1.x);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  const float w0 = ml0.x == -INFINITY ? 0.f : exp2f(ml0.x - M);
+  const float w1 = ml1.x == -INFINITY ? 0.f : exp2f(ml1.x - M);
+  float den = w0 * ml0.y + w1 * ml1.y;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
   float acc[E];
 #pragma unroll
   for (int e = 0; e < E; ++e) acc[e] = 0.f;
-  float den = 0.f;
-  for (int s = 0; s < p.nsplit; ++s) {
-    const float2 ml = p.ml[s * rows + rowidx];
-    const float w = ml.x == -INFINITY ? 0.f : exp2f(ml.x - M);
-    den += w * ml.y;
-    const float* src = p.opart + (s * rows + rowidx) * D + lane * E;
+  const float* src = p.opart + rowidx * D + lane * E;
+  const long long sstride = rows * D;
+#pragma unroll 8
+  for (int s = 0; s < ns; ++s) {
+    const float w = __shfl_sync(0xffffffffu, s < 32 ? w0 : w1, s & 31);
     if (E == 4) {
-      const float4 v = *reinterpret_cast<const float4*>(src);
-      acc[0] += w * v.x; acc[1] += w * v.y; acc[2] += w * v.z; acc[3 % E] += w * v.w;
+      const float4 v = *reinterpret_cast<const float4*>(src + s * sstride);
+      acc[0] += w * v.x; acc[1 % E] += w * v.y; acc[2 % E] += w * v.z; acc[3 % E] += w * v.w;
     } else {
-      const float2 v = *reinterpret_cast<const float2*>(src);
+      const float2 v = *reinterpret_cast<const float2*>(src + s * sstride);
       acc[0] += w * v.x; acc[1 % E] += w * v.y;
     }
   }

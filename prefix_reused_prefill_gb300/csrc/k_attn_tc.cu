@@ -153,7 +153,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
   const int nblk = b1 - b0;
 
   dev::pdl_trigger();
-  dev::pdl_wait();   // q and the appended K/V come from the previous launch
   if (threadIdx.x == 0) {
     dev::mbar_init(dev::smem_u32(&q_full), 1);
     for (int i = 0; i < C::kStages; ++i) {
@@ -179,20 +178,37 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
+  // q and this call's K/V come from the previous launch; only the producer's
+  // loads of cached-prefix K/V may run ahead of it.
+  if (warp != 0 || lane != 0) dev::pdl_wait();
 
   if (warp == 0) {
     // ---------------------------------------------------------------- producer
+    if (lane == 0 && nblk == 0) dev::pdl_wait();
     if (lane == 0 && nblk > 0) {
       dev::prefetch_tmap(&p.tq);
       dev::prefetch_tmap(&p.tkv);
       dev::prefetch_tmap(&p.tvt);
+      int pre = 0;
+      while (pre < nblk && pre < C::kStages && (b0 + pre + 1) * kKeys <= p.rows.P) {
+        const uint32_t sb = kv_base + pre * C::kStageBytes;
+        const uint32_t fb = dev::smem_u32(&kv_full[pre]);
+        dev::mbar_arrive_expect_tx(fb, C::kStageBytes);
+        const int key0 = (b0 + pre) * kKeys;
+#pragma unroll
+        for (int a = 0; a < D / 64; ++a)
+          dev::tma_load_2d(sb + a * (kKeys * 128), &p.tkv, 64 * a, p.kbase + kv * p.cap + key0, fb);
+        dev::tma_load_2d(sb + C::kKBytes, &p.tvt, key0, p.vtbase + kv * D, fb);
+        ++pre;
+      }
+      dev::pdl_wait();
       const uint32_t qb = dev::smem_u32(&q_full);
       dev::mbar_arrive_expect_tx(qb, C::kQBytes);
       const int qrow = kv * R + row_lo;
 #pragma unroll
       for (int a = 0; a < D / 64; ++a) dev::tma_load_2d(q_base + a * 16384, &p.tq, 64 * a, qrow, qb);
-      int issued = 0;
-      for (int j = 0; j < nblk; ++j) {
+      int issued = pre;
+      for (int j = pre; j < nblk; ++j) {
         const int st = j % C::kStages;
         if (j >= C::kStages &&
             (!dev::mbar_wait(dev::smem_u32(&kv_empty[st]), ((j / C::kStages) - 1) & 1, p.status) ||

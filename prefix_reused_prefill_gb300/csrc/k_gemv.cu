@@ -167,6 +167,7 @@ __device__ __forceinline__ int unit_owner(long long u, int units, int ctas) {
 }
 
 constexpr int kMaxOwnTiles = 16;   // tiles one CTA may finish (host keeps it below)
+constexpr int kConBatch = 8;       // contribution loads kept in flight by the reduction
 
 // two CTAs per SM for up to 16 tokens (the host sizes the grid for it)
 template <int NT, int EPI>
@@ -363,13 +364,12 @@ __global__ void __launch_bounds__(kThreads, NT == 4 ? 1 : 2) gemv_int4_kernel(co
       if (lane == 0) dev::mbar_arrive(dev::smem_u32(&empty_bar[st]));
     }
 
-    // end of this CTA's part of a tile: publish it as one contribution
+    // end of this CTA's part of a tile: store it as one contribution (the
+    // arrivals are counted once, after the loop)
     const int u = u0 + it;
     const int tile = u / p.ksteps;
     if (u % p.ksteps == p.ksteps - 1 || it == nk - 1) {
-      const long long tu0 = (long long)tile * p.ksteps;
-      const int first = unit_owner(tu0, units, p.ctas);
-      const int ncon = unit_owner(tu0 + p.ksteps - 1, units, p.ctas) - first + 1;
+      const int first = unit_owner((long long)tile * p.ksteps, units, p.ctas);
       float* tp = p.part + ((long long)tile * p.maxc + (blockIdx.x - first)) * (kGemvMaxCols * kGemvRows);
 #pragma unroll
       for (int t = 0; t < NT; ++t)
@@ -379,22 +379,31 @@ __global__ void __launch_bounds__(kThreads, NT == 4 ? 1 : 2) gemv_int4_kernel(co
           if (ok && tok < p.mb) tp[tok * kGemvRows + rho0 + (e >> 1) * 8] = acc[t][e];
           acc[t][e] = 0.f;
         }
-      __threadfence();
-      consumers_sync();
-      if (tid == 0 && !*abort_v) {
-        const int done = atomicAdd(p.counters + tile, 1) + 1;
-        if (done == ncon) {
-          p.counters[tile] = 0;   // ready for the next launch
-          if (n_own < kMaxOwnTiles) own_tiles[n_own] = tile;
-          ++n_own;
-        }
+    }
+  }
+  // publish every contribution of this CTA, then count one arrival per tile
+  // touched (one thread per tile); the last arrival owns the tile's epilogue
+  __threadfence();
+  consumers_sync();
+  {
+    const int t_first = u0 / p.ksteps, t_last = (u1 - 1) / p.ksteps;
+    const int tile = t_first + tid;
+    if (tile <= t_last && !*abort_v) {
+      const long long tu0 = (long long)tile * p.ksteps;
+      const int ncon = unit_owner(tu0 + p.ksteps - 1, units, p.ctas) - unit_owner(tu0, units, p.ctas) + 1;
+      const int done = atomicAdd(p.counters + tile, 1) + 1;
+      if (done == ncon) {
+        p.counters[tile] = 0;   // ready for the next launch
+        const int k = atomicAdd(&n_own, 1);
+        if (k < kMaxOwnTiles) own_tiles[k] = tile;
       }
     }
   }
   consumers_sync();
   if (tid == 0 && *abort_v) n_own = 0;          // an aborted CTA finishes nothing
+
   // ----------------------- tiles this CTA finished last: reduce, then epilogue
-  consumers_sync();                            // every stage read; own_tiles visible
+  consumers_sync();                            // own_tiles visible
   float* ct = reinterpret_cast<float*>(smem_raw + (base - dev::smem_u32(smem_raw)));
   const int n_done = min(n_own, kMaxOwnTiles);
   for (int k = 0; k < n_done; ++k) {
@@ -406,12 +415,21 @@ __global__ void __launch_bounds__(kThreads, NT == 4 ? 1 : 2) gemv_int4_kernel(co
     const float* t0p = p.part + (long long)tile * p.maxc * (kGemvMaxCols * kGemvRows);
     for (int idx = tid; idx < p.mb * (kGemvRows / 4); idx += kConsumers) {
       const int tok = idx / (kGemvRows / 4), r4 = (idx % (kGemvRows / 4)) * 4;
-      // contributions in contributor order: the sum does not depend on timing
-      float4 v = __ldcg(reinterpret_cast<const float4*>(t0p + tok * kGemvRows + r4));
-      for (int j = 1; j < ncon; ++j) {
-        const float4 w = __ldcg(reinterpret_cast<const float4*>(t0p + (long long)j * (kGemvMaxCols * kGemvRows) +
-                                                                tok * kGemvRows + r4));
-        v.x += w.x; v.y += w.y; v.z += w.z; v.w += w.w;
+      const float* src = t0p + tok * kGemvRows + r4;
+      // all contributions in flight at once, then added in contributor order
+      // (the sum does not depend on which CTA arrived last)
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int j0 = 0; j0 < ncon; j0 += kConBatch) {
+        float4 w[kConBatch];
+#pragma unroll
+        for (int j = 0; j < kConBatch; ++j)
+          if (j0 + j < ncon)
+            w[j] = __ldcg(reinterpret_cast<const float4*>(src + (long long)(j0 + j) * (kGemvMaxCols * kGemvRows)));
+#pragma unroll
+        for (int j = 0; j < kConBatch; ++j)
+          if (j0 + j < ncon) {
+            v.x += w[j].x; v.y += w[j].y; v.z += w[j].z; v.w += w[j].w;
+          }
       }
       *reinterpret_cast<float4*>(ct + tok * kTileLd + r4) = v;
     }
