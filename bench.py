@@ -29,6 +29,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -43,6 +44,10 @@ PEAKS_PATH = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 P_CACHED, M_ROWS, PROMPT = 1668, 254, 1922
+# DRAM bytes (read + write) of the four projection GEMMs of one layer of this workload, from one
+# ncu capture (dram__bytes_read.sum + dram__bytes_write.sum, cold L2): 11.18 + 9.11 + 80.30 + 48.41 MB.
+# Re-take the capture whenever gemm_int4_tc_kernel changes.
+PROJ_TRAFFIC_PER_LAYER = 148.99e6
 
 
 def peaks():
@@ -90,7 +95,8 @@ class ClockSampler:
     def __init__(self, index: int):
         self.index = index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{index}.csv")
+        out_dir = os.environ.get("KVR_CLOCKS_DIR") or tempfile.gettempdir()
+        self.path = os.path.join(out_dir, f"clocks_rank{index}.csv")
 
     def start(self):
         try:
@@ -246,6 +252,7 @@ def run_gpu(args, rank, world):
     attn_bytes = (P_CACHED + M_ROWS) * shape.n_kv_heads * shape.head_dim * 2 * 2 * L
     attn_ms = cls_ms[1] / args.steps
     attn_gbs = attn_bytes / (attn_ms / 1e3) / 1e9
+    attn_flops = 4.0 * shape.head_dim * shape.n_q_heads * sum(P_CACHED + i + 1 for i in range(M_ROWS)) * L
     weight_bytes = shape.params_per_layer() * L * 0.5625
     line = {
         "metric": "suffix-prefill rows/s",
@@ -266,9 +273,13 @@ def run_gpu(args, rank, world):
                    "l2": "inputs larger than L2: 3.67 GB of int4 weights streamed per step"},
         "attended_kv_gbs": round(attn_gbs, 1),
         "attended_kv_frac_hbm": round(attn_gbs / pk["hbm_gbs"], 4),
+        "attention_causal_tflops": round(attn_flops / (attn_ms / 1e3) / 1e12, 1),
+        "attention_frac_tensor": round(attn_flops / (attn_ms / 1e3) / 1e12 / peak_tf, 4),
         "roofline": {"bound": "tensor", "achieved": round(achieved_tf, 2),
                      "peak": peak_tf, "unit": "TFLOP/s",
-                     "frac": round(achieved_tf / peak_tf, 4), "traffic": None,
+                     "frac": round(achieved_tf / peak_tf, 4),
+                     "traffic": None if args.layers else round(PROJ_TRAFFIC_PER_LAYER * L),
+                     "traffic_per": "step (the class's 112 launches)",
                      "peak_kind": f"bf16 sustained ({pk_kind})",
                      "kernel": "projections (gemv_int4 / gemm_int4)",
                      "launches_per_step": n_proj, "ms_per_step": round(proj_ms, 4),
@@ -352,13 +363,23 @@ def run_verify(args):
         ms = _event_ms(lambda: kv.kvr_verify(0, draft, x, w, out=out), args.steps, args.warmup,
                        after=lambda: kv.kvr_slot_truncate(0, P))
         kv.kvr_sync_status()
+        kv.kvr_profile_read()
+        kv.kvr_profile_enable(True)
+        for _ in range(3):
+            kv.kvr_verify(0, draft, x, w, out=out)
+            kv.kvr_slot_truncate(0, P)
+        cls_ms, cls_n = kv.kvr_profile_read()
+        kv.kvr_profile_enable(False)
         nbytes = (shape.params_per_layer() * 0.5625 * L
                   + (P + m) * shape.n_kv_heads * shape.head_dim * 2 * 2 * L
                   + m * shape.n_kv_heads * shape.head_dim * 4 * L)
         gbs = nbytes / (ms / 1e3) / 1e9
         table.append({"m": m, "ms": round(ms, 4), "rows_per_s": round(m / (ms / 1e3), 1),
                       "algorithmic_gb": round(nbytes / 1e9, 4), "gbs": round(gbs, 1),
-                      "frac_hbm": round(gbs / pk["hbm_gbs"], 4)})
+                      "frac_hbm": round(gbs / pk["hbm_gbs"], 4),
+                      "class_ms_serialised": {k: round(v / 3, 4) for k, v in
+                                              zip(("projections", "attention", "epilogues"), cls_ms)},
+                      "launches": cls_n[0] // 3 + cls_n[1] // 3 + cls_n[2] // 3})
     clk = clocks.stop()
     ms_ = np.array([r["m"] for r in table], dtype=np.float64)
     ts = np.array([r["ms"] for r in table])

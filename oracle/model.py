@@ -28,7 +28,8 @@ matches a worked example (tests/golden/rope_fixture.txt); RMSNorm is
 invariant to positive scaling and maps a constant vector to ~1; a layer whose
 Wo and Wd are zero is the identity; prefill(whole) == prefill(prefix) then
 prefill(suffix), bit for bit; the branch rows of a priming batch equal
-separate truncate-and-prefill runs, bit for bit.  The stack as a whole beyond
+separate truncate-and-prefill runs, bit for bit; layer_rows equals layer on
+the rows it evaluates, bit for bit.  The stack as a whole beyond
 these invariants is "parity unpinned": no page prints a worked numeric
 example of a layer.
 """
