@@ -60,13 +60,16 @@ def peaks():
 
 
 def dist_setup(n_gpus):
+    """One process per GPU under torch.distributed.run (RANK / WORLD_SIZE /
+    LOCAL_RANK / MASTER_* from the environment): NCCL with a GPU, gloo without."""
     rank, world = 0, 1
     if n_gpus > 1 or "RANK" in os.environ:
         import torch.distributed as dist
         rank = int(os.environ.get("RANK", 0))
         world = int(os.environ.get("WORLD_SIZE", 1))
         local = int(os.environ.get("LOCAL_RANK", 0))
-        torch.cuda.set_device(local)
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
         dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
     return rank, world
 
@@ -78,12 +81,19 @@ def barrier():
 
 
 def max_over_ranks(x: float) -> float:
+    """The slowest rank's time: every rank's clock brackets the same barrier-aligned region."""
     import torch.distributed as dist
     if dist.is_available() and dist.is_initialized():
-        t = torch.tensor([x], device="cuda")
+        on_gpu = dist.get_backend() == "nccl"
+        t = torch.tensor([x], dtype=torch.float64, device="cuda" if on_gpu else "cpu")
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         return float(t.item())
     return x
+
+
+def whole_job_rate(world: int, rows_per_rank: int, steps: int, ms_max: float) -> float:
+    """Rows/s of the whole job: every rank's rows over the slowest rank's time."""
+    return world * rows_per_rank * steps / (ms_max / 1e3)
 
 
 class ClockSampler:
@@ -206,7 +216,7 @@ def run_gpu(args, rank, world):
     _, launches = kv.kvr_profile_read()
     ms = max_over_ranks(ms)
     ms_step = ms / args.steps
-    value = world * M_ROWS * args.steps / (ms / 1e3)
+    value = whole_job_rate(world, M_ROWS, args.steps, ms)
 
     # ---------------- the same steps with per-kernel-class events (roofline)
     kv.kvr_profile_enable(True)
