@@ -133,6 +133,7 @@ __global__ void __launch_bounds__(256) epi_qkv_kernel(const float* part, long lo
   for (int e = 0; e < 8; ++e) x1[e] = x2[e] = 0.f;
   if (live) {
     const float* src = part + (long long)t * ldo + (long long)hd * D + j0;
+#pragma unroll 2
     for (int s = 0; s < ksplit; ++s) {
       const float4 a0 = *reinterpret_cast<const float4*>(src + s * plane);
       const float4 a1 = *reinterpret_cast<const float4*>(src + s * plane + 4);
@@ -206,19 +207,32 @@ __global__ void __launch_bounds__(256) epi_resid_kernel(const float* part, long 
   const int H4 = H >> 2;
   float4 v[V];
   float ss = 0.f;
+  // splits outermost, this thread's columns innermost: V independent loads
+  // per split (two splits in flight); each element still adds h + p0 + p1 + ...
+  const float4* pp = reinterpret_cast<const float4*>(part + (long long)t * ldo);
+#pragma unroll
+  for (int u = 0; u < V; ++u) {
+    const int k4 = threadIdx.x + u * 256;
+    v[u] = k4 < H4 ? reinterpret_cast<const float4*>(h + i * H)[k4] : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+#pragma unroll 2
+  for (int s = 0; s < ksplit; ++s) {
+#pragma unroll
+    for (int u = 0; u < V; ++u) {
+      const int k4 = threadIdx.x + u * 256;
+      if (k4 < H4) {
+        const float4 q = pp[s * (plane >> 2) + k4];
+        v[u].x += q.x; v[u].y += q.y; v[u].z += q.z; v[u].w += q.w;
+      }
+    }
+  }
 #pragma unroll
   for (int u = 0; u < V; ++u) {
     const int k4 = threadIdx.x + u * 256;
     if (k4 < H4) {
-      float4 acc = reinterpret_cast<const float4*>(h + i * H)[k4];
-      const float4* pp = reinterpret_cast<const float4*>(part + (long long)t * ldo) + k4;
-      for (int s = 0; s < ksplit; ++s) {
-        const float4 q = pp[s * (plane >> 2)];
-        acc.x += q.x; acc.y += q.y; acc.z += q.z; acc.w += q.w;
-      }
+      const float4 acc = v[u];
       reinterpret_cast<float4*>(h + i * H)[k4] = acc;
       ss += acc.x * acc.x + acc.y * acc.y + acc.z * acc.z + acc.w * acc.w;
-      v[u] = acc;
       if (final_out) {
         uint2 o;
         o.x = dev::pack_bf16x2(acc.x, acc.y);

@@ -190,9 +190,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_int4_tc_kernel(const __grid_
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
-  // The int4 weight stream (warp 0, lane 0) reads only weights and may run
-  // ahead of the previous launch; every other role waits for it.
-  if (warp != 0 || lane != 0) dev::pdl_wait();
+  // Only the activation stream (warp 0, lane 1) and, before it writes, the
+  // epilogue depend on the previous launch: the int4 stream, the converters
+  // (weights and scales) and the MMA issuer (fed by the two streams) run
+  // ahead, so the A stages are full when the activations arrive.
+  if (warp == 0 && lane == 1) dev::pdl_wait();
 
   if (warp == 0) {
     // ---------------------------------------------------------------- producers
@@ -354,6 +356,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_int4_tc_kernel(const __grid_
     // ---------------------------------------------------------------- epilogue
     const bool have = __all_sync(0xffffffffu, dev::mbar_wait(dev::smem_u32(&acc_full), 0, p.status) && !*abort_v);
     tc_fence_after();
+    dev::pdl_wait();   // the outputs below may still be read by the previous launch
     if (have) {
       const int set = cw >> 2;             // 0..3
       const int trow = 32 * q + lane;      // tile row of this thread
@@ -371,24 +374,26 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_int4_tc_kernel(const __grid_
           }
         }
       } else {
-        // rows 0..63 are gate, 64..127 the matching up rows: exchange through smem
-        float* xch = reinterpret_cast<float*>(smem_raw + (x_base - dev::smem_u32(smem_raw))) + set * 64 * 33;
-        const int n = row0 + (trow & 63);
+        // rows 0..63 are gate, 64..127 the matching up rows: each warp stages
+        // its 32 rows x 32 tokens in shared memory, then the set's 128 threads
+        // form z = silu(g) * u for 64 rows x 32 tokens (thread = row, token parity)
+        float* xch = reinterpret_cast<float*>(smem_raw + (x_base - dev::smem_u32(smem_raw))) + set * 128 * 33;
+        const int tid = 32 * q + lane;       // 0..127 within the set
+        const int r = tid & 63, kp = tid >> 6;
+        const int n = row0 + r;
         for (int c0 = 32 * set; c0 < p.n_tok; c0 += 128) {
-          uint32_t r[32];
-          tmem_ld32(taddr + c0, r);
-          if (q >= 2) {
+          uint32_t v[32];
+          tmem_ld32(taddr + c0, v);
 #pragma unroll
-            for (int k = 0; k < 32; ++k) xch[(trow - 64) * 33 + k] = __uint_as_float(r[k]);
-          }
+          for (int k = 0; k < 32; ++k) xch[trow * 33 + k] = __uint_as_float(v[k]);
           named_sync(1 + set, 128);
-          if (q < 2 && n < seg.N) {
+          if (n < seg.N) {
 #pragma unroll
-            for (int k = 0; k < 32; ++k) {
+            for (int k = kp; k < 32; k += 2) {
               if (c0 + k < p.m) {
-                const float g = __uint_as_float(r[k]);
-                const float u = xch[trow * 33 + k];
-                const float sg = g / (1.f + expf(-g));
+                const float g = xch[r * 33 + k];
+                const float u = xch[(64 + r) * 33 + k];
+                const float sg = __fdividef(g, 1.f + __expf(-g));
                 p.z[(long long)(p.t0 + c0 + k) * p.F + n] = __float2bfloat16_rn(sg * u);
               }
             }
