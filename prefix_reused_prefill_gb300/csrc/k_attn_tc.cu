@@ -6,24 +6,34 @@
 // all G query heads of a KV head packed as rows (row = token*G + head in the
 // group), one KV head's rows form a real dense contraction.
 //
-// One CTA = (128-row tile of one KV head, key split).  Warp roles:
-//   warp 0     TMA: the Q tile once (128 rows x d, 128B-swizzled K-major), then
-//              per 64-key block a K tile ([64 keys][d]) and a V^T tile
-//              ([d][64 keys]; V is stored transposed in the slot), 3 stages;
-//   warp 1     allocates TMEM; one thread issues S_j = Q K_j^T (M=128, N=64)
-//              into a double-buffered S accumulator and O += P_j V_j (M=128,
-//              N=d) into one O accumulator that stays in TMEM for the whole
-//              key range, software-pipelined so S_{j+1} is computed while the
-//              softmax works on block j;
-//   warps 2-5  one thread per row: tcgen05.ld of S_j, causal mask, online
-//              softmax in fp32 (log2 units) and P_j written to shared memory as
-//              a 128B-swizzled K-major bf16 tile.  The running-max correction of
-//              O is lazy: P_j is taken relative to a per-row reference max, and
-//              only when a block's max exceeds the reference by more than 8
-//              (P would exceed 2^8) does the warp rescale its rows of O in TMEM
-//              (tcgen05.ld / tcgen05.st) and move the reference.  At the end
-//              O / l is written (or, with several key splits, the unnormalised
-//              partials merged by attn_combine).
+// One CTA = (128-row tile of one KV head, key split); keys go in blocks of
+// 128, so S_j = Q K_j^T is M=128, N=128 (the MMA count of a block, not its
+// size, bounds a small-tile tensor pipe).  Tensor memory holds three S
+// buffers of 128 columns and the O accumulator (512 columns).  Warp roles:
+//   warp 0     TMA, two independent streams: lane 0 the Q tile once (128 rows x
+//              d, 128B-swizzled K-major) and per block a K tile ([128 keys][d],
+//              3 stages, a stage freed by the S that read it), lane 1 per block
+//              a V^T tile ([d][128 keys]; V is stored transposed in the slot; 2
+//              stages, freed by the P V that read it);
+//   warp 1     allocates TMEM; one thread issues S_j into S buffer j % 3 as
+//              soon as its K tile is in and P V of the buffer's previous block
+//              has completed;
+//   warp 10    one thread issues O += P_j V_j (M=128, N=d) with P_j read from
+//              tensor memory, in block order;
+//   warps 2-9  two threads per row, one per 64-key half of the block (warps
+//              w and w+4 share a TMEM lane quarter): tcgen05.ld of their half of
+//              S_j, causal mask, the block max exchanged through shared memory
+//              (a named barrier per warp pair), online softmax in fp32 (log2
+//              units), and P_j (bf16) stored back over the first half of its own
+//              S buffer with tcgen05.st.  Each thread keeps the running sum of
+//              its half; the halves are added at the end.  The running-max
+//              correction of O is lazy: P_j is taken relative to a per-row
+//              reference max, and only when a block's max exceeds the reference
+//              by more than 8 (P would exceed 2^8) do the two threads rescale
+//              their halves of the row of O in TMEM (after P V of the previous
+//              block) and move the reference.  At the end O / l is written (or,
+//              with several key splits, the unnormalised partials merged by
+//              attn_combine).
 // Every wait is bounded; a timed-out CTA records it, drains its copies and
 // frees its TMEM.
 #include "kvr_internal.cuh"
@@ -32,22 +42,26 @@ namespace kvr {
 
 namespace {
 
-constexpr int kKeys = 64;
-constexpr int kThreads = 192;
+constexpr int kKeys = kAttnTcKeys;               // 128 keys per block
+constexpr int kSoftmaxWarps = 8;                  // warps 2..9
+constexpr int kPvWarp = 2 + kSoftmaxWarps;        // warp 10
+constexpr int kThreads = 32 * (kPvWarp + 1);
 
 template <int D>
 struct TcCfg {
-  static constexpr int kQBytes = 128 * D * 2;
-  static constexpr int kKBytes = kKeys * D * 2;   // D/64 atoms of [64 keys][64 elems]
-  static constexpr int kVBytes = D * kKeys * 2;   // one atom of [D rows][64 keys]
-  static constexpr int kStageBytes = kKBytes + kVBytes;
-  static constexpr int kStages = 3;
-  static constexpr int kPBytes = 128 * kKeys * 2;
-  static constexpr int kSmem = kQBytes + kStages * kStageBytes + kPBytes + 1024;
-  // TMEM columns: S buffers at 0 and 64, the O accumulator at 128
-  static __device__ __forceinline__ uint32_t scol(int b) { return (uint32_t)(64 * b); }
-  static constexpr uint32_t kOCol = 128;
-  static constexpr int kTmemCols = 256;
+  static constexpr int kQBytes = 128 * D * 2;    // D/64 atoms of [128 rows][64 elems]
+  static constexpr int kKAtom = kKeys * 128;     // [128 keys][64 elems]
+  static constexpr int kKBytes = kKeys * D * 2;  // D/64 atoms
+  static constexpr int kVAtom = D * 128;         // [D rows][64 keys]
+  static constexpr int kVBytes = D * kKeys * 2;  // 2 atoms
+  static constexpr int kKStages = 3;
+  static constexpr int kVStages = 2;
+  static constexpr int kSmem = kQBytes + kKStages * kKBytes + kVStages * kVBytes + 1024;
+  // TMEM columns: S (then P) buffers at 0, 128, 256; the O accumulator at 384
+  static constexpr int kSBufs = 3;
+  static __device__ __forceinline__ uint32_t scol(int b) { return (uint32_t)(128 * b); }
+  static constexpr uint32_t kOCol = 384;
+  static constexpr int kTmemCols = 512;
 };
 
 __device__ __forceinline__ void tc_fence_before() {
@@ -55,9 +69,6 @@ __device__ __forceinline__ void tc_fence_before() {
 }
 __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void fence_proxy_async() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
   return (uint64_t)((saddr >> 4) & 0x3FFFu) | (1ull << 16) | (64ull << 32) | (1ull << 46) |
@@ -75,9 +86,28 @@ __device__ __forceinline__ void mma_f16(uint32_t tmem_d, uint64_t a, uint64_t b,
       "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// D (TMEM) += A (TMEM) * B (shared memory)
+__device__ __forceinline__ void mma_f16_ta(uint32_t tmem_d, uint32_t tmem_a, uint64_t b, uint32_t idesc,
+                                           uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(tmem_d),
+      "r"(tmem_a), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                : "memory");
+}
+__device__ __forceinline__ void named_sync(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+// 2^x with the PTX approximate base-2 exponential (ex2.approx.ftz.f32; 2^-inf = 0)
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 constexpr float kLazyMax = 8.0f;  // rescale O only when a block max passes the reference by this (log2)
 
@@ -130,16 +160,19 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
   using C = TcCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t q_full;
-  __shared__ __align__(8) uint64_t kv_full[C::kStages], kv_empty[C::kStages];
-  __shared__ __align__(8) uint64_t s_full[2], s_empty[2], p_full, pv_done;
+  __shared__ __align__(8) uint64_t k_full[C::kKStages], k_empty[C::kKStages];
+  __shared__ __align__(8) uint64_t v_full[C::kVStages], v_empty[C::kVStages];
+  __shared__ __align__(8) uint64_t s_full[C::kSBufs], p_full[C::kSBufs], pv_done[C::kSBufs];
+  __shared__ float xmax[2][2][128];   // [block parity][key half][row]
+  __shared__ float xsum[2][128];
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
   volatile int* abort_v = &abort_flag;
 
   const uint32_t base = (dev::smem_u32(smem_raw) + 1023u) & ~1023u;
   const uint32_t q_base = base;
-  const uint32_t kv_base = q_base + C::kQBytes;
-  const uint32_t p_base = kv_base + C::kStages * C::kStageBytes;
+  const uint32_t k_base = q_base + C::kQBytes;
+  const uint32_t v_base = k_base + C::kKStages * C::kKBytes;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rt = blockIdx.x, split = blockIdx.y, kv = blockIdx.z;
   const int R = p.G * p.rows.m;
@@ -155,16 +188,19 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
   dev::pdl_trigger();
   if (threadIdx.x == 0) {
     dev::mbar_init(dev::smem_u32(&q_full), 1);
-    for (int i = 0; i < C::kStages; ++i) {
-      dev::mbar_init(dev::smem_u32(&kv_full[i]), 1);
-      dev::mbar_init(dev::smem_u32(&kv_empty[i]), 1);
+    for (int i = 0; i < C::kKStages; ++i) {
+      dev::mbar_init(dev::smem_u32(&k_full[i]), 1);
+      dev::mbar_init(dev::smem_u32(&k_empty[i]), 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < C::kVStages; ++i) {
+      dev::mbar_init(dev::smem_u32(&v_full[i]), 1);
+      dev::mbar_init(dev::smem_u32(&v_empty[i]), 1);
+    }
+    for (int i = 0; i < C::kSBufs; ++i) {
       dev::mbar_init(dev::smem_u32(&s_full[i]), 1);
-      dev::mbar_init(dev::smem_u32(&s_empty[i]), 4);
+      dev::mbar_init(dev::smem_u32(&p_full[i]), kSoftmaxWarps);
+      dev::mbar_init(dev::smem_u32(&pv_done[i]), 1);
     }
-    dev::mbar_init(dev::smem_u32(&p_full), 4);
-    dev::mbar_init(dev::smem_u32(&pv_done), 1);
     *abort_v = 0;
     dev::fence_mbar_init();
   }
@@ -178,105 +214,145 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
-  // q and this call's K/V come from the previous launch; only the producer's
+  // q and this call's K/V come from the previous launch; only the producers'
   // loads of cached-prefix K/V may run ahead of it.
-  if (warp != 0 || lane != 0) dev::pdl_wait();
+  if (warp != 0 || lane > 1) dev::pdl_wait();
 
   if (warp == 0) {
-    // ---------------------------------------------------------------- producer
-    if (lane == 0 && nblk == 0) dev::pdl_wait();
-    if (lane == 0 && nblk > 0) {
-      dev::prefetch_tmap(&p.tq);
-      dev::prefetch_tmap(&p.tkv);
-      dev::prefetch_tmap(&p.tvt);
-      int pre = 0;
-      while (pre < nblk && pre < C::kStages && (b0 + pre + 1) * kKeys <= p.rows.P) {
-        const uint32_t sb = kv_base + pre * C::kStageBytes;
-        const uint32_t fb = dev::smem_u32(&kv_full[pre]);
-        dev::mbar_arrive_expect_tx(fb, C::kStageBytes);
-        const int key0 = (b0 + pre) * kKeys;
+    // ---------------------------------------------------------------- producers
+    if (lane <= 1 && nblk == 0) dev::pdl_wait();
+    if (lane <= 1 && nblk > 0) {
+      const bool is_k = lane == 0;
+      const int stages = is_k ? C::kKStages : C::kVStages;
+      dev::prefetch_tmap(is_k ? &p.tkv : &p.tvt);
+      if (is_k) dev::prefetch_tmap(&p.tq);
+      uint64_t* fullb = is_k ? k_full : v_full;
+      uint64_t* emptyb = is_k ? k_empty : v_empty;
+      const uint32_t ring = is_k ? k_base : v_base;
+      const uint32_t bytes = is_k ? C::kKBytes : C::kVBytes;
+      // a block = two 64-key halves: K atoms of 128 rows (two 64-row boxes each),
+      // V^T atoms of 64 keys
+      auto load = [&](int j, uint32_t dst, uint32_t fb) {
+        const int key0 = (b0 + j) * kKeys;
 #pragma unroll
-        for (int a = 0; a < D / 64; ++a)
-          dev::tma_load_2d(sb + a * (kKeys * 128), &p.tkv, 64 * a, p.kbase + kv * p.cap + key0, fb);
-        dev::tma_load_2d(sb + C::kKBytes, &p.tvt, key0, p.vtbase + kv * D, fb);
+        for (int h = 0; h < 2; ++h) {
+          if (is_k) {
+#pragma unroll
+            for (int a = 0; a < D / 64; ++a)
+              dev::tma_load_2d(dst + a * C::kKAtom + h * (64 * 128), &p.tkv, 64 * a,
+                               p.kbase + kv * p.cap + key0 + 64 * h, fb);
+          } else {
+            dev::tma_load_2d(dst + h * C::kVAtom, &p.tvt, key0 + 64 * h, p.vtbase + kv * D, fb);
+          }
+        }
+      };
+      auto prefetch = [&](int j) {
+        const int key0 = (b0 + j) * kKeys;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          if (is_k) {
+#pragma unroll
+            for (int a = 0; a < D / 64; ++a)
+              dev::tma_prefetch_2d(&p.tkv, 64 * a, p.kbase + kv * p.cap + key0 + 64 * h);
+          } else {
+            dev::tma_prefetch_2d(&p.tvt, key0 + 64 * h, p.vtbase + kv * D);
+          }
+        }
+      };
+      int pre = 0;
+      while (pre < nblk && pre < stages && (b0 + pre + 1) * kKeys <= p.rows.P) {
+        const uint32_t fb = dev::smem_u32(&fullb[pre]);
+        dev::mbar_arrive_expect_tx(fb, bytes);
+        load(pre, ring + pre * bytes, fb);
         ++pre;
       }
+      // the rest of the cached-prefix blocks of this split toward L2
+      for (int j = pre; j < nblk && (b0 + j + 1) * kKeys <= p.rows.P; ++j) prefetch(j);
       dev::pdl_wait();
       const uint32_t qb = dev::smem_u32(&q_full);
-      dev::mbar_arrive_expect_tx(qb, C::kQBytes);
-      const int qrow = kv * R + row_lo;
+      if (is_k) {
+        dev::mbar_arrive_expect_tx(qb, C::kQBytes);
+        const int qrow = kv * R + row_lo;
 #pragma unroll
-      for (int a = 0; a < D / 64; ++a) dev::tma_load_2d(q_base + a * 16384, &p.tq, 64 * a, qrow, qb);
+        for (int a = 0; a < D / 64; ++a) dev::tma_load_2d(q_base + a * 16384, &p.tq, 64 * a, qrow, qb);
+      }
       int issued = pre;
       for (int j = pre; j < nblk; ++j) {
-        const int st = j % C::kStages;
-        if (j >= C::kStages &&
-            (!dev::mbar_wait(dev::smem_u32(&kv_empty[st]), ((j / C::kStages) - 1) & 1, p.status) ||
-             *abort_v)) {
+        const int st = j % stages;
+        if (j >= stages &&
+            (!dev::mbar_wait(dev::smem_u32(&emptyb[st]), ((j / stages) - 1) & 1, p.status) || *abort_v)) {
           *abort_v = 1;
           break;
         }
-        const uint32_t sb = kv_base + st * C::kStageBytes;
-        const uint32_t fb = dev::smem_u32(&kv_full[st]);
-        dev::mbar_arrive_expect_tx(fb, C::kStageBytes);
-        const int key0 = (b0 + j) * kKeys;
-#pragma unroll
-        for (int a = 0; a < D / 64; ++a)
-          dev::tma_load_2d(sb + a * (kKeys * 128), &p.tkv, 64 * a, p.kbase + kv * p.cap + key0, fb);
-        dev::tma_load_2d(sb + C::kKBytes, &p.tvt, key0, p.vtbase + kv * D, fb);
+        const uint32_t fb = dev::smem_u32(&fullb[st]);
+        dev::mbar_arrive_expect_tx(fb, bytes);
+        load(j, ring + st * bytes, fb);
         ++issued;
       }
-      dev::mbar_wait(qb, 0, nullptr);
-      for (int st = 0; st < C::kStages && st < issued; ++st) {
-        const int last = ((issued - 1 - st) / C::kStages) * C::kStages + st;
-        dev::mbar_wait(dev::smem_u32(&kv_full[st]), (uint32_t)(last / C::kStages) & 1, nullptr);
+      if (is_k) dev::mbar_wait(qb, 0, nullptr);
+      for (int st = 0; st < stages && st < issued; ++st) {
+        const int last = ((issued - 1 - st) / stages) * stages + st;
+        dev::mbar_wait(dev::smem_u32(&fullb[st]), (uint32_t)(last / stages) & 1, nullptr);
       }
     }
   } else if (warp == 1) {
-    // ---------------------------------------------------------------- MMA issuer
+    // ---------------------------------------------------------------- S issuer
     if (lane == 0 && nblk > 0) {
       const uint32_t id_qk = idesc_bf16(128, kKeys);
-      const uint32_t id_pv = idesc_bf16(128, D);
       bool ok = dev::mbar_wait(dev::smem_u32(&q_full), 0, p.status);
-      auto pv = [&](int b) -> bool {
-        const int st = b % C::kStages;
-        if (!dev::mbar_wait(dev::smem_u32(&p_full), b & 1, p.status) || *abort_v) return false;
-        tc_fence_after();
-        const uint64_t pd = sw128_desc(p_base);
-        const uint64_t vd = sw128_desc(kv_base + st * C::kStageBytes + C::kKBytes);
-#pragma unroll
-        for (int kk = 0; kk < kKeys / 16; ++kk)
-          mma_f16(tmem + C::kOCol, pd + 2 * kk, vd + 2 * kk, id_pv, (b > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(dev::smem_u32(&pv_done));
-        mma_commit(dev::smem_u32(&kv_empty[st]));
-        return true;
-      };
+      const uint64_t qd = sw128_desc(q_base);
       for (int j = 0; j < nblk && ok; ++j) {
-        const int st = j % C::kStages, sb = j & 1;
-        if (!dev::mbar_wait(dev::smem_u32(&kv_full[st]), (j / C::kStages) & 1, p.status) ||
-            (j >= 2 && !dev::mbar_wait(dev::smem_u32(&s_empty[sb]), ((j - 2) >> 1) & 1, p.status)) ||
+        const int st = j % C::kKStages, sb = j % C::kSBufs;
+        if (!dev::mbar_wait(dev::smem_u32(&k_full[st]), (j / C::kKStages) & 1, p.status) ||
+            (j >= C::kSBufs &&
+             !dev::mbar_wait(dev::smem_u32(&pv_done[sb]), ((j / C::kSBufs) - 1) & 1, p.status)) ||
             *abort_v) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint64_t kd = sw128_desc(kv_base + st * C::kStageBytes);
-        const uint64_t qd = sw128_desc(q_base);
+        const uint64_t kd = sw128_desc(k_base + st * C::kKBytes);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
           mma_f16(tmem + C::scol(sb), qd + (kk >> 2) * (16384 >> 4) + 2 * (kk & 3),
-                  kd + (kk >> 2) * ((kKeys * 128) >> 4) + 2 * (kk & 3), id_qk, kk > 0 ? 1u : 0u);
+                  kd + (kk >> 2) * (C::kKAtom >> 4) + 2 * (kk & 3), id_qk, kk > 0 ? 1u : 0u);
         mma_commit(dev::smem_u32(&s_full[sb]));
-        if (j >= 1 && !pv(j - 1)) ok = false;
+        mma_commit(dev::smem_u32(&k_empty[st]));
       }
-      if (ok) ok = pv(nblk - 1);
+      if (!ok) *abort_v = 1;
+    }
+  } else if (warp == kPvWarp) {
+    // ---------------------------------------------------------------- P V issuer
+    // O += P_j V_j in block order, P_j from tensor memory; the commit frees
+    // the V stage and, for the S issuer, the S / P buffer
+    if (lane == 0 && nblk > 0) {
+      const uint32_t id_pv = idesc_bf16(128, D);
+      bool ok = true;
+      for (int b = 0; b < nblk && ok; ++b) {
+        const int st = b % C::kVStages, sb = b % C::kSBufs;
+        if (!dev::mbar_wait(dev::smem_u32(&v_full[st]), (b / C::kVStages) & 1, p.status) ||
+            !dev::mbar_wait(dev::smem_u32(&p_full[sb]), (b / C::kSBufs) & 1, p.status) || *abort_v) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint64_t vd = sw128_desc(v_base + st * C::kVBytes);
+#pragma unroll
+        for (int kk = 0; kk < kKeys / 16; ++kk)
+          mma_f16_ta(tmem + C::kOCol, tmem + C::scol(sb) + 8u * (uint32_t)kk,
+                     vd + (kk >> 2) * (C::kVAtom >> 4) + 2 * (kk & 3), id_pv, (b > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(dev::smem_u32(&pv_done[sb]));
+        mma_commit(dev::smem_u32(&v_empty[st]));
+      }
       if (!ok) *abort_v = 1;
     }
   } else {
     // ---------------------------------------------------------------- softmax
-    const int q4 = warp & 3;
+    const int q4 = warp & 3;                  // TMEM lane quarter
+    const int half = (warp - 2) >> 2;         // keys [64 half, 64 half + 64) of each block
     const int r = 32 * q4 + lane;
     const uint32_t tlane = (uint32_t)(32 * q4) << 16;
+    const int pair_bar = 1 + q4;              // warps q4+2 and q4+6 (64 threads)
     const int rho = row_lo + r;
     int tok = -1, head = 0, lo = 1, hi = 0;
     if (rho < R) {
@@ -288,96 +364,113 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     }
     const int P0 = p.rows.P;
     float m_ref = -INFINITY, l = 0.f;
+    // warp-uniform; once false the warp skips work and waits but still meets
+    // its partner at every pair barrier
     bool ok = true;
-    for (int j = 0; j < nblk && ok; ++j) {
-      const int sb = j & 1;
-      ok = dev::mbar_wait(dev::smem_u32(&s_full[sb]), (j >> 1) & 1, p.status) && !*abort_v;
-      if (!__all_sync(0xffffffffu, ok)) {
-        ok = false;
-        break;
+    for (int j = 0; j < nblk; ++j) {
+      const int xb = j & 1;                // exchange slot
+      const int sb = j % C::kSBufs;        // S / P buffer
+      if (ok) {
+        const bool got = dev::mbar_wait(dev::smem_u32(&s_full[sb]), (j / C::kSBufs) & 1, p.status) && !*abort_v;
+        ok = __all_sync(0xffffffffu, got);
       }
-      tc_fence_after();
-      uint32_t sr[kKeys];
-      tmem_ld32_nowait(tmem + tlane + C::scol(sb), sr);
-      tmem_ld32_nowait(tmem + tlane + C::scol(sb) + 32, sr + 32);
-      tmem_wait_ld();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) dev::mbar_arrive(dev::smem_u32(&s_empty[sb]));
-      const int key0 = (b0 + j) * kKeys;
-      // visible keys of this row within the block: [0, P) and [lo, hi]
-      const int pe = min(max(P0 - key0, 0), kKeys);            // keys k < pe are in [0, P)
-      const int la = min(max(lo - key0, 0), kKeys);            // own range k in [la, hb)
-      const int hb = tok >= 0 ? min(max(hi - key0 + 1, 0), kKeys) : 0;
-      float s[kKeys];
+      float sv[64];
       float mx = -INFINITY;
+      const int key0 = (b0 + j) * kKeys + 64 * half;
+      if (ok) {
+        tc_fence_after();
+        uint32_t sr[64];
+        tmem_ld32_nowait(tmem + tlane + C::scol(sb) + 64 * half, sr);
+        tmem_ld32_nowait(tmem + tlane + C::scol(sb) + 64 * half + 32, sr + 32);
+        tmem_wait_ld();
+        // visible keys of this row within the half block: [0, P) and [lo, hi]
+        const int pe = min(max(P0 - key0, 0), 64);
+        const int la = min(max(lo - key0, 0), 64);
+        const int hb = tok >= 0 ? min(max(hi - key0 + 1, 0), 64) : 0;
+        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        if (tok >= 0 && pe == 64) {
+          // wholly inside the cached prefix: every key visible
 #pragma unroll
-      for (int k = 0; k < kKeys; ++k) {
-        const bool vis = tok >= 0 && (k < pe || (k >= la && k < hb));
-        s[k] = vis ? __uint_as_float(sr[k]) * p.scale_log2 : -INFINITY;
-        mx = fmaxf(mx, s[k]);
+          for (int k = 0; k < 64; ++k) {
+            sv[k] = __uint_as_float(sr[k]) * p.scale_log2;
+            m4[k & 3] = fmaxf(m4[k & 3], sv[k]);
+          }
+        } else {
+#pragma unroll
+          for (int k = 0; k < 64; ++k) {
+            const bool vis = tok >= 0 && (k < pe || (k >= la && k < hb));
+            sv[k] = vis ? __uint_as_float(sr[k]) * p.scale_log2 : -INFINITY;
+            m4[k & 3] = fmaxf(m4[k & 3], sv[k]);
+          }
+        }
+        mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
       }
+      // the row's block max from both halves; after this barrier both halves
+      // have read their S, so P may overwrite the buffer
+      xmax[xb][half][r] = mx;
+      named_sync(pair_bar, 64);
+      mx = fmaxf(mx, xmax[xb][half ^ 1][r]);
+      if (!ok) continue;
       // lazy reference max: move it (and rescale O) only when P would exceed 2^8
       const bool move = mx > m_ref + kLazyMax;
       const float m_new = move ? mx : m_ref;
       const float factor = (move && m_ref != -INFINITY) ? exp2f(m_ref - m_new) : 1.f;
       const float muse = m_new == -INFINITY ? 0.f : m_new;
-      uint32_t pk[kKeys / 2];
-      float sum = 0.f;
+      uint32_t pk[32];
+      float s4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int k = 0; k < kKeys; k += 2) {
-        const float e0 = exp2f(s[k] - muse), e1 = exp2f(s[k + 1] - muse);
-        sum += e0 + e1;
+      for (int k = 0; k < 64; k += 2) {
+        const float e0 = ex2_approx(sv[k] - muse), e1 = ex2_approx(sv[k + 1] - muse);
+        s4[(k >> 1) & 3] += e0 + e1;
         pk[k / 2] = dev::pack_bf16x2(e0, e1);
       }
-      // P V of block j-1 must be done: it reads the P buffer and accumulates into O
-      if (j >= 1) {
-        ok = dev::mbar_wait(dev::smem_u32(&pv_done), (j - 1) & 1, p.status) && !*abort_v;
-        if (!__all_sync(0xffffffffu, ok)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        if (__any_sync(0xffffffffu, factor != 1.f)) {
+      const float sum = (s4[0] + s4[1]) + (s4[2] + s4[3]);
+      // P_j (bf16, keys in order, two per column) over the first half of S_j
+      tmem_st32(tmem + tlane + C::scol(sb) + 32 * half, pk);
+      // an O rescale waits for P V of the previous block
+      const bool rescale = j >= 1 && __any_sync(0xffffffffu, factor != 1.f);
+      if (rescale) {
+        const bool got = dev::mbar_wait(dev::smem_u32(&pv_done[(j - 1) % C::kSBufs]),
+                                        ((j - 1) / C::kSBufs) & 1, p.status);
+        ok = __all_sync(0xffffffffu, got && !*abort_v);
+        if (ok) {
+          tc_fence_after();
 #pragma unroll
-          for (int c0 = 0; c0 < D; c0 += 32) {
+          for (int c0 = 0; c0 < D / 2; c0 += 32) {
             uint32_t v[32];
-            tmem_ld32_nowait(tmem + tlane + C::kOCol + c0, v);
+            const uint32_t oaddr = tmem + tlane + C::kOCol + (D / 2) * half + c0;
+            tmem_ld32_nowait(oaddr, v);
             tmem_wait_ld();
 #pragma unroll
             for (int k = 0; k < 32; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * factor);
-            tmem_st32(tmem + tlane + C::kOCol + c0, v);
+            tmem_st32(oaddr, v);
           }
-          tmem_wait_st();
         }
       }
+      tmem_wait_st();
       l = l * factor + sum;
       m_ref = m_new;
-      const uint32_t prow = p_base + r * 128;
-#pragma unroll
-      for (int ch = 0; ch < 8; ++ch) {
-        const uint32_t addr = prow + (((uint32_t)ch ^ (uint32_t)(r & 7)) << 4);
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(pk[4 * ch]),
-                     "r"(pk[4 * ch + 1]), "r"(pk[4 * ch + 2]), "r"(pk[4 * ch + 3])
-                     : "memory");
-      }
-      fence_proxy_async();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) dev::mbar_arrive(dev::smem_u32(&p_full));
+      if (ok && lane == 0) dev::mbar_arrive(dev::smem_u32(&p_full[sb]));
     }
     if (ok && nblk > 0) {
-      ok = dev::mbar_wait(dev::smem_u32(&pv_done), (nblk - 1) & 1, p.status) && !*abort_v;
-      ok = __all_sync(0xffffffffu, ok);
+      const bool got = dev::mbar_wait(dev::smem_u32(&pv_done[(nblk - 1) % C::kSBufs]),
+                                      ((nblk - 1) / C::kSBufs) & 1, p.status) && !*abort_v;
+      ok = __all_sync(0xffffffffu, got);
     }
     if (!ok) *abort_v = 1;
+    // the row sum from both halves
+    xsum[half][r] = l;
+    named_sync(pair_bar, 64);
+    l += xsum[half ^ 1][r];
     if (ok) {
       tc_fence_after();
       const long long rowidx = (long long)tok * p.Hq + head;
       const long long plane = (long long)p.rows.m * p.Hq;
       const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
-      for (int c0 = 0; c0 < D; c0 += 32) {
+      for (int c0 = (D / 2) * half; c0 < (D / 2) * (half + 1); c0 += 32) {
         float v[32];
         if (nblk > 0) {
           tmem_ld32(tmem + tlane + C::kOCol + c0, v);
@@ -405,7 +498,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
           }
         }
       }
-      if (tok >= 0 && p.nsplit > 1) p.ml[split * plane + rowidx] = make_float2(m_ref, l);
+      if (tok >= 0 && p.nsplit > 1 && half == 0) p.ml[split * plane + rowidx] = make_float2(m_ref, l);
     }
   }
 

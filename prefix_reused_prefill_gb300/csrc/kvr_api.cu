@@ -188,6 +188,7 @@ struct kvr_ctx {
   bool prof = false;
   float* trace = nullptr;   // [n_layers + 1][max_rows][hidden] float32, or null
   bool force_gemv = false;  // KVR_FORCE_GEMV=1: keep every m on the GEMV path
+  int attn_splits = 0;      // KVR_ATTN_SPLITS=n: fixed key-split count of the tcgen05 attention
   std::vector<EventPair> pending;
   std::vector<cudaEvent_t> free_events;
   float prof_ms[4] = {0, 0, 0, 0};
@@ -565,11 +566,13 @@ int attention(kvr_ctx* c, cudaStream_t st, int slot, int layer, const RowMap& ro
   const bool tc = R > kAttnTcMinRows && !c->force_gemv;
   int ns;
   if (tc) {
-    // tcgen05 path: 128-row tiles; split the keys until the grid covers the SMs
+    // tcgen05 path: 128-row tiles (one CTA per SM); split the keys as far as
+    // one wave allows -- a partial second wave costs as much as a full one
     p.row_tiles = (R + 127) / 128;
-    const int nb = (kend + kAttnKeys - 1) / kAttnKeys;
-    ns = (c->n_sms + p.row_tiles * k.n_kv_heads - 1) / (p.row_tiles * k.n_kv_heads);
+    const int nb = (kend + kAttnTcKeys - 1) / kAttnTcKeys;
+    ns = std::max(1, c->n_sms / (p.row_tiles * k.n_kv_heads));
     ns = std::max(1, std::min(std::min(ns, std::max(1, nb / 4)), kMaxSplits));
+    if (c->attn_splits > 0) ns = std::min(c->attn_splits, std::min(nb, kMaxSplits));
   } else {
     const int rw = attn_row_warps(R);
     p.row_tiles = (R + 16 * rw - 1) / (16 * rw);
@@ -811,6 +814,8 @@ int kvr_ctx_create(const kvr_config* cfg, void* kv_arena, size_t arena_bytes, vo
   }
   const char* fg = getenv("KVR_FORCE_GEMV");
   c->force_gemv = fg && fg[0] == '1';
+  const char* as = getenv("KVR_ATTN_SPLITS");
+  c->attn_splits = as ? atoi(as) : 0;
   c->requested = cfg->n_slots;
   c->reuse = cfg->n_slots > 0;
   const int want = std::max(cfg->n_slots, 1);

@@ -24,6 +24,7 @@ constexpr int kGemmMaxTok = 256;   // tokens per tcgen05 GEMM pass (MMA N <= 256
 constexpr int kGemmMaxSplit = 8;
 constexpr int kAttnKeys = 64;      // keys per attention pipeline stage
 constexpr int kAttnTcMinRows = 96; // G*m above this: tcgen05 attention (128-row tiles)
+constexpr int kAttnTcKeys = 128;   // keys per block of the tcgen05 attention
 constexpr int kSplitTargetCtas = 320;
 constexpr int kMaxSplits = 64;
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s per bounded wait
