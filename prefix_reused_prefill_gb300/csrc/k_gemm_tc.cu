@@ -142,6 +142,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_int4_tc_kernel(const __grid_
   __shared__ __align__(8) uint64_t acc_full;
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
+  __shared__ int epi_bad;
   volatile int* abort_v = &abort_flag;
 
   const uint32_t base = (dev::smem_u32(smem_raw) + 1023u) & ~1023u;
@@ -178,6 +179,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_int4_tc_kernel(const __grid_
     }
     dev::mbar_init(dev::smem_u32(&acc_full), 1);
     *abort_v = 0;
+    epi_bad = 0;
     dev::fence_mbar_init();
   }
   if (warp == 1) {
@@ -354,9 +356,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_int4_tc_kernel(const __grid_
     if (!ok) *abort_v = 1;
 
     // ---------------------------------------------------------------- epilogue
-    const bool have = __all_sync(0xffffffffu, dev::mbar_wait(dev::smem_u32(&acc_full), 0, p.status) && !*abort_v);
+    // one decision for all sixteen epilogue warps (the SwiGLU sets' barriers
+    // need all of their warps)
+    const bool have_w = __all_sync(0xffffffffu, dev::mbar_wait(dev::smem_u32(&acc_full), 0, p.status) && !*abort_v);
+    if (!have_w && lane == 0) epi_bad = 1;
     tc_fence_after();
     dev::pdl_wait();   // the outputs below may still be read by the previous launch
+    named_sync(5, 32 * kConvWarps);
+    const bool have = epi_bad == 0;
     if (have) {
       const int set = cw >> 2;             // 0..3
       const int trow = 32 * q + lane;      // tile row of this thread
