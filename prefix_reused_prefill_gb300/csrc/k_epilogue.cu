@@ -133,7 +133,7 @@ __global__ void __launch_bounds__(256) epi_qkv_kernel(const float* part, long lo
   for (int e = 0; e < 8; ++e) x1[e] = x2[e] = 0.f;
   if (live) {
     const float* src = part + (long long)t * ldo + (long long)hd * D + j0;
-#pragma unroll 2
+#pragma unroll 4
     for (int s = 0; s < ksplit; ++s) {
       const float4 a0 = *reinterpret_cast<const float4*>(src + s * plane);
       const float4 a1 = *reinterpret_cast<const float4*>(src + s * plane + 4);
@@ -193,42 +193,54 @@ __global__ void __launch_bounds__(256) epi_qkv_kernel(const float* part, long lo
 
 // One CTA per token row: h += sum of the split partials (fixed split order),
 // then RMSNorm of the new row for the next projection, or the bf16 output.
-// float4 accesses; the row stays in registers between the two passes.
-template <int V>  // float4 per thread (H <= 4 * 256 * V)
-__global__ void __launch_bounds__(256) epi_resid_kernel(const float* part, long long plane, int ksplit,
-                                                        int ldo, int c0, int H, float* h,
-                                                        const __nv_bfloat16* gain, float eps,
-                                                        __nv_bfloat16* a_out, __nv_bfloat16* final_out) {
+// 512 threads x V float4; every split's loads of a thread are issued before
+// any of them is added (the kernel is L2-latency-bound), and the row stays in
+// registers between the two passes.
+constexpr int kResidThreads = 512;
+template <int V>  // float4 per thread (H <= 4 * 512 * V)
+__global__ void __launch_bounds__(kResidThreads) epi_resid_kernel(const float* part, long long plane, int ksplit,
+                                                                  int ldo, int c0, int H, float* h,
+                                                                  const __nv_bfloat16* gain, float eps,
+                                                                  __nv_bfloat16* a_out, __nv_bfloat16* final_out) {
   dev::pdl_trigger();
   dev::pdl_wait();
   __shared__ float red[32];
   const int t = blockIdx.x;
   const long long i = c0 + t;
   const int H4 = H >> 2;
-  float4 v[V];
-  float ss = 0.f;
-  // splits outermost, this thread's columns innermost: V independent loads
-  // per split (two splits in flight); each element still adds h + p0 + p1 + ...
+  const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
   const float4* pp = reinterpret_cast<const float4*>(part + (long long)t * ldo);
+  const long long pl4 = plane >> 2;
+  // splits in flight at once: all of them for up to two float4 per thread
+  constexpr int kB = V <= 2 ? kGemmMaxSplit : kGemmMaxSplit / 2;
+  float4 v[V];
 #pragma unroll
   for (int u = 0; u < V; ++u) {
-    const int k4 = threadIdx.x + u * 256;
-    v[u] = k4 < H4 ? reinterpret_cast<const float4*>(h + i * H)[k4] : make_float4(0.f, 0.f, 0.f, 0.f);
+    const int k4 = threadIdx.x + u * kResidThreads;
+    v[u] = k4 < H4 ? reinterpret_cast<const float4*>(h + i * H)[k4] : zero;
   }
-#pragma unroll 2
-  for (int s = 0; s < ksplit; ++s) {
+  for (int s0 = 0; s0 < ksplit; s0 += kB) {
+    float4 q[kB][V];
 #pragma unroll
-    for (int u = 0; u < V; ++u) {
-      const int k4 = threadIdx.x + u * 256;
-      if (k4 < H4) {
-        const float4 q = pp[s * (plane >> 2) + k4];
-        v[u].x += q.x; v[u].y += q.y; v[u].z += q.z; v[u].w += q.w;
+    for (int s = 0; s < kB; ++s)
+#pragma unroll
+      for (int u = 0; u < V; ++u) {
+        const int k4 = threadIdx.x + u * kResidThreads;
+        q[s][u] = (s0 + s < ksplit && k4 < H4) ? pp[(s0 + s) * pl4 + k4] : zero;
       }
-    }
+    // h + p0 + p1 + ... in split order
+#pragma unroll
+    for (int s = 0; s < kB; ++s)
+#pragma unroll
+      for (int u = 0; u < V; ++u)
+        if (s0 + s < ksplit) {
+          v[u].x += q[s][u].x; v[u].y += q[s][u].y; v[u].z += q[s][u].z; v[u].w += q[s][u].w;
+        }
   }
+  float ss = 0.f;
 #pragma unroll
   for (int u = 0; u < V; ++u) {
-    const int k4 = threadIdx.x + u * 256;
+    const int k4 = threadIdx.x + u * kResidThreads;
     if (k4 < H4) {
       const float4 acc = v[u];
       reinterpret_cast<float4*>(h + i * H)[k4] = acc;
@@ -245,7 +257,7 @@ __global__ void __launch_bounds__(256) epi_resid_kernel(const float* part, long 
     const float rs = rsqrtf(block_sum(ss, red) / H + eps);
 #pragma unroll
     for (int u = 0; u < V; ++u) {
-      const int k4 = threadIdx.x + u * 256;
+      const int k4 = threadIdx.x + u * kResidThreads;
       if (k4 < H4) {
         const uint2 gw = reinterpret_cast<const uint2*>(gain)[k4];
         const __nv_bfloat162 g01 = *reinterpret_cast<const __nv_bfloat162*>(&gw.x);
@@ -326,16 +338,17 @@ cudaError_t launch_epi_qkv(const float* part, long long plane, int ksplit, int l
 cudaError_t launch_epi_resid(const float* part, long long plane, int ksplit, int ldo, int c0,
                              int mb, int H, float* h, const __nv_bfloat16* gain, float eps,
                              __nv_bfloat16* a_out, __nv_bfloat16* final_out, cudaStream_t st) {
-  const int v = (H / 4 + 255) / 256;
+  if (ksplit > kGemmMaxSplit) return cudaErrorInvalidValue;
+  const int v = (H / 4 + kResidThreads - 1) / kResidThreads;
+  if (v <= 1)
+    return launch_k(epi_resid_kernel<1>, mb, kResidThreads, 0, st, part, plane, ksplit, ldo, c0, H, h, gain,
+                    eps, a_out, final_out);
   if (v <= 2)
-    return launch_k(epi_resid_kernel<2>, mb, 256, 0, st, part, plane, ksplit, ldo, c0, H, h, gain, eps,
-                    a_out, final_out);
+    return launch_k(epi_resid_kernel<2>, mb, kResidThreads, 0, st, part, plane, ksplit, ldo, c0, H, h, gain,
+                    eps, a_out, final_out);
   if (v <= 4)
-    return launch_k(epi_resid_kernel<4>, mb, 256, 0, st, part, plane, ksplit, ldo, c0, H, h, gain, eps,
-                    a_out, final_out);
-  if (v <= 8)
-    return launch_k(epi_resid_kernel<8>, mb, 256, 0, st, part, plane, ksplit, ldo, c0, H, h, gain, eps,
-                    a_out, final_out);
+    return launch_k(epi_resid_kernel<4>, mb, kResidThreads, 0, st, part, plane, ksplit, ldo, c0, H, h, gain,
+                    eps, a_out, final_out);
   return cudaErrorInvalidValue;
 }
 
