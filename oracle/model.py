@@ -4,9 +4,10 @@ TEST INFRASTRUCTURE ONLY (see the package header).
 
 Sources: goinfer, "Turn nine in under half a second" ("What goinfer does": the
 KV cache is two vectors per token in each layer, kept per conversation; only
-the tokens after the shared start are processed); the spec-decode post
-("cost model": the m = k+1 verify rows run as one batched pass over weights
-read once); OpenJev "What changed" (several questions resume from one shared
+the tokens after the shared start are processed; "What we got wrong": a
+speculative step checks the guessed tokens and must give the same words as
+plain decoding); the spec-decode post ("cost model": the m = k+1 verify rows
+run as one batched pass over weights read once); OpenJev "What changed" (several questions resume from one shared
 checkpoint).  The pages do not print the layer; the layer below is the
 pre-norm Qwen2-style decoder those pages serve (RMSNorm, GQA attention with
 rotate-half RoPE, SwiGLU), with the readings listed in the design notes:
@@ -29,7 +30,9 @@ invariant to positive scaling and maps a constant vector to ~1; a layer whose
 Wo and Wd are zero is the identity; prefill(whole) == prefill(prefix) then
 prefill(suffix), bit for bit; the branch rows of a priming batch equal
 separate truncate-and-prefill runs, bit for bit; layer_rows equals layer on
-the rows it evaluates, bit for bit.  The stack as a whole beyond
+the rows it evaluates, bit for bit; greedy acceptance on hand-worked token
+lists; the head with an identity LM head ranks the normed stream, and a
+one-row head is that row's dot product.  The stack as a whole beyond
 these invariants is "parity unpinned": no page prints a worked numeric
 example of a layer.
 """
@@ -200,13 +203,50 @@ def layer_rows(dims: Dims, W: Dict[str, np.ndarray], h: np.ndarray, K: np.ndarra
 
 
 def forward(dims: Dims, weights: List[Dict[str, np.ndarray]], kv: SlotKV, hidden: np.ndarray,
-            rows: List[Row]) -> np.ndarray:
+            rows: List[Row], rounded: bool = True) -> np.ndarray:
     """Run the rows through every layer; K/V land in ``kv``.  Returns the
-    bf16-valued output [m][H] (the final residual stream, rounded once)."""
+    bf16-valued output [m][H] (the final residual stream, rounded once), or
+    the unrounded stream with rounded=False."""
     h = np.asarray(hidden, dtype=np.float64)
     for l, W in enumerate(weights):
         h = layer(dims, W, h, kv.K[l], kv.V[l], rows)
-    return round_bf16(h)
+    return round_bf16(h) if rounded else h
+
+
+# ----------------------------------------------------------------------------
+# the output head and greedy verification
+# ----------------------------------------------------------------------------
+
+def head_logits(dims: Dims, h: np.ndarray, gain: np.ndarray, w_lm: np.ndarray) -> np.ndarray:
+    """Logits [m][vocab] of output rows: the final RMSNorm (rounded to bf16, as
+    every normed activation) times the LM head."""
+    b = round_bf16(rmsnorm(np.asarray(h, dtype=np.float64), gain, dims.rms_eps))
+    return linear(b, w_lm)
+
+
+def greedy_argmax(logits: np.ndarray) -> np.ndarray:
+    """Index of each row's largest logit; ties go to the lowest index."""
+    return np.argmax(logits, axis=-1)
+
+
+def greedy_accept(tokens: Sequence[int], argmax: Sequence[int]) -> int:
+    """Verify rows hold [t0, d1 .. dk]: draft d_(j+1) is accepted while it
+    equals the argmax of row j (greedy decoding would have produced it).
+    Returns the number of accepted drafts; the next token is argmax[accepted]."""
+    a = 0
+    while a + 1 < len(tokens) and int(tokens[a + 1]) == int(argmax[a]):
+        a += 1
+    return a
+
+
+def verify_accept(dims: Dims, weights, kv: SlotKV, hidden: np.ndarray, p0: int, tokens: Sequence[int],
+                  gain: np.ndarray, w_lm: np.ndarray):
+    """Verify the m rows at p0 .. p0+m-1 and take the greedy decision.
+    Returns (logits, argmax, accepted)."""
+    h = forward(dims, weights, kv, hidden, plain_rows(p0, len(hidden)), rounded=False)
+    logits = head_logits(dims, h, gain, w_lm)
+    am = greedy_argmax(logits)
+    return logits, am, greedy_accept(tokens, am)
 
 
 def prefill(dims: Dims, weights, kv: SlotKV, hidden: np.ndarray, p0: int) -> np.ndarray:

@@ -233,3 +233,42 @@ def test_layer_rows_equals_layer_on_selected_rows(name, rng):
     np.testing.assert_array_equal(part, full[sel])
     np.testing.assert_array_equal(kv2.K, kv1.K)
     np.testing.assert_array_equal(kv2.V, kv1.V)
+
+
+# ---------------------------------------------------------------- head and greedy acceptance
+
+def test_greedy_accept_hand_worked():
+    acc = model.greedy_accept
+    # rows [t0, d1, d2, d3]; argmax[j] is the model's next token after row j
+    assert acc([5, 7, 9, 11], [7, 9, 11, 3]) == 3          # every draft agrees
+    assert acc([5, 7, 9, 11], [8, 9, 11, 3]) == 0          # the first draft is rejected
+    assert acc([5, 7, 9, 11], [7, 9, 2, 3]) == 2           # d3 differs from argmax of row 2
+    assert acc([5, 7, 9, 11], [7, 1, 11, 3]) == 1          # later agreement does not count
+    assert acc([5], [4]) == 0                              # m = 1: nothing to accept
+
+
+def test_greedy_argmax_takes_lowest_index_on_ties():
+    logits = np.array([[1.0, 3.0, 3.0, -1.0], [0.0, 0.0, 0.0, 0.0]])
+    assert model.greedy_argmax(logits).tolist() == [1, 0]
+
+
+def test_head_with_identity_lm_ranks_the_normed_stream(rng):
+    dims = Dims(64, 4, 2, 16, 128, False)
+    h = rng.standard_normal((3, 64)) * 7.0
+    gain = np.ones(64)
+    logits = model.head_logits(dims, h, gain, np.eye(64))
+    normed = h / np.sqrt(np.mean(h * h, axis=-1, keepdims=True) + dims.rms_eps)
+    np.testing.assert_array_equal(logits, round_bf16(normed))
+    assert (model.greedy_argmax(logits) == np.argmax(h, axis=-1)).all()
+
+
+def test_head_single_row_is_its_dot_product(rng):
+    dims = Dims(32, 4, 2, 8, 64, False)
+    h = rng.standard_normal((2, 32))
+    gain = rng.uniform(0.5, 1.5, 32)
+    w = np.zeros((10, 32))
+    w[6] = rng.standard_normal(32)
+    logits = model.head_logits(dims, h, gain, w)
+    b = round_bf16(rmsnorm(h, gain, dims.rms_eps))
+    assert np.count_nonzero(logits[:, [0, 1, 2, 3, 4, 5, 7, 8, 9]]) == 0
+    np.testing.assert_allclose(logits[:, 6], b @ w[6], rtol=0, atol=1e-12)

@@ -91,6 +91,13 @@ MUTATIONS = [
     (model, "branch_rows", "Row(P + i, P + off + i, vis)", "Row(P + off + i, P + off + i, vis)"),
     (model, "branch_rows", "np.concatenate([np.arange(P), P + off + np.arange(i + 1)])",
      "np.concatenate([np.arange(P + off), P + off + np.arange(i + 1)])"),      # sees earlier branches
+    # output head and greedy acceptance
+    (model, "head_logits", "rmsnorm(np.asarray(h, dtype=np.float64), gain, dims.rms_eps)",
+     "np.asarray(h, dtype=np.float64)"),                                         # final norm dropped
+    (model, "greedy_argmax", "np.argmax(logits, axis=-1)",
+     "logits.shape[-1] - 1 - np.argmax(logits[..., ::-1], axis=-1)"),           # ties to the highest index
+    (model, "greedy_accept", "int(tokens[a + 1]) == int(argmax[a])", "int(tokens[a]) == int(argmax[a])"),
+    (model, "greedy_accept", "while a + 1 < len(tokens)", "while a + 2 < len(tokens)"),  # last draft never taken
     # scalar numerics and formats
     (numerics, "round_bf16", "np.rint(", "np.trunc("),                          # truncation
     (numerics, "silu", "1.0 + np.exp(-x)", "1.0 + np.exp(x)"),

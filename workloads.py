@@ -211,6 +211,22 @@ def layer_weights(shape: ModelShape, seed: int, layer: int, device="cpu",
     return out
 
 
+def head_weights(shape: ModelShape, seed: int, device="cpu", vocab: int = VOCAB, keep_codes: bool = False,
+                 std: float = 0.02) -> Dict[str, object]:
+    """The output head: 'norm' (bf16 ones, the final RMSNorm gain) and 'lm', the
+    LM head [vocab][H] in the shape's weight format (int4 g32 or bf16)."""
+    H = shape.hidden
+    if str(device) == "cpu":
+        rng = np.random.Generator(np.random.PCG64([seed, 10_000, 0]))
+        w = torch.from_numpy(rng.standard_normal((vocab, H), dtype=np.float32) * np.float32(std))
+    else:
+        g = torch.Generator(device=device)
+        g.manual_seed(seed * 1_000_003 + 10_000 * 101)
+        w = torch.randn((vocab, H), generator=g, device=device, dtype=torch.float32) * std
+    lm = w.to(torch.bfloat16).contiguous() if shape.weight_format == "bf16" else make_int4(w, keep_codes=keep_codes)
+    return {"norm": torch.ones(H, dtype=torch.bfloat16, device=device), "lm": lm}
+
+
 def stack_weights(shape: ModelShape, seed: int, device="cpu", keep_codes=False,
                   n_layers: Optional[int] = None) -> List[Dict[str, object]]:
     L = shape.n_layers if n_layers is None else n_layers
