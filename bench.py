@@ -358,8 +358,9 @@ def run_verify(args):
     tk = workloads.verify_tokens(seed)
     P = len(tk["state"])
     lws = workloads.stack_weights(shape, seed, device=device)
-    kv = Kvr(config_for_shape(shape, 1, P + 256, 256), device=device)
+    kv = Kvr(config_for_shape(shape, 1, P + 256, 256, vocab=workloads.VOCAB), device=device)
     w = kv.weights(lws)
+    head = workloads.head_weights(shape, seed, device=device)
     assert kv.kvr_slot_match(tk["state"][:1]) == (0, 0)
     _prefill_state(kv, 0, tk["state"], shape, seed, w, device)
     L = shape.n_layers
@@ -373,6 +374,10 @@ def run_verify(args):
         ms = _event_ms(lambda: kv.kvr_verify(0, draft, x, w, out=out), args.steps, args.warmup,
                        after=lambda: kv.kvr_slot_truncate(0, P))
         kv.kvr_sync_status()
+        # the same rows, then the output head, the argmax and the acceptance count
+        # (one device-to-host read of m token ids and a stream synchronisation inside)
+        ms_acc = _event_ms(lambda: kv.kvr_verify_accept(0, draft, x, w, head, out=out), args.steps,
+                           args.warmup, after=lambda: kv.kvr_slot_truncate(0, P))
         kv.kvr_profile_read()
         kv.kvr_profile_enable(True)
         for _ in range(3):
@@ -384,7 +389,8 @@ def run_verify(args):
                   + (P + m) * shape.n_kv_heads * shape.head_dim * 2 * 2 * L
                   + m * shape.n_kv_heads * shape.head_dim * 4 * L)
         gbs = nbytes / (ms / 1e3) / 1e9
-        table.append({"m": m, "ms": round(ms, 4), "rows_per_s": round(m / (ms / 1e3), 1),
+        table.append({"m": m, "ms": round(ms, 4), "accept_ms": round(ms_acc, 4),
+                      "rows_per_s": round(m / (ms / 1e3), 1),
                       "algorithmic_gb": round(nbytes / 1e9, 4), "gbs": round(gbs, 1),
                       "frac_hbm": round(gbs / pk["hbm_gbs"], 4),
                       "class_ms_serialised": {k: round(v / 3, 4) for k, v in
@@ -398,6 +404,8 @@ def run_verify(args):
     return {"metric": "verify ms per call", "workload": "speculative verify: 36 x (H 4096, 32/8 heads, F 12288) "
             "int4-g32, 4096 cached tokens, m = k+1 rows", "unit": "ms", "higher_is_better": False,
             "fit_ms": {"a": round(float(a), 4), "b_per_row": round(float(b), 4)},
+            "accept": {"vocab": workloads.VOCAB, "what": "accept_ms: kvr_verify_accept (verify + final "
+                       "RMSNorm + int4 LM head + argmax + acceptance, read back to the host)"},
             "page_fit_ms": {"a": 9.0, "b_per_row": 5.5, "hardware": "the page's own (not a GB300)"},
             "per_m": table, "peak_hbm_gbs": pk["hbm_gbs"], "peak_kind": pk_kind,
             "l2": "inputs larger than L2 (3.9 GB of weights and 0.6 GB of K/V per call)",

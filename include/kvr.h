@@ -86,7 +86,11 @@ extern "C" {
  *                  the scratch area.
  *   rope_theta     rotate-half RoPE base; rows sit at absolute slot positions.
  *   rms_eps        RMSNorm epsilon.
+ *   vocab          largest output-head vocabulary (kvr_verify_accept); 0 for
+ *                  none.  Sizes the scratch area; at most KVR_MAX_VOCAB.
  */
+#define KVR_MAX_VOCAB 262144
+
 typedef struct kvr_config {
   int n_slots;
   int capacity;
@@ -102,6 +106,7 @@ typedef struct kvr_config {
   int max_rows;
   float rope_theta;
   float rms_eps;
+  int vocab;
 } kvr_config;
 
 /*
@@ -281,6 +286,34 @@ int kvr_sync_status(kvr_ctx* ctx, void* stream);
  * input load, entry l+1 after layer l (row i of entry e at
  * (e*max_rows + i)*hidden).  Returns KVR_ERR_CAPACITY if bytes is too small. */
 int kvr_trace_set(kvr_ctx* ctx, void* dev, size_t bytes);
+
+/* The output head for greedy verification: the final RMSNorm gain and the
+ * LM head in the layer weights' int4 group-32 layout (device pointers, caller-
+ * owned, 16-byte aligned). */
+typedef struct {
+  const void* norm;  /* bf16 [hidden]                              */
+  const void* w;     /* int4 bytes [vocab][hidden/2]               */
+  const void* s;     /* fp16 group scales [vocab][hidden/32]       */
+  int vocab;         /* 1 .. the context's configured vocab        */
+} kvr_head_weights;
+
+/* Speculative verify with the greedy decision (goinfer "What we got wrong":
+ * a speculative step checks the guessed tokens and must give the same words
+ * as plain decoding; thinkspread, cost model: the m = k+1 rows run as one
+ * batched pass).  tokens (host, m <= 64) are [t0, d1 .. dk]: t0 the last
+ * committed token, d the drafts; rows sit at p0 .. p0+m-1, p0 = the slot's
+ * length.  Runs kvr_verify, then logits = RMSNorm(h) * lm^T per row (the
+ * normed rows rounded to bf16), next_tokens[i] = argmax of row i (lowest
+ * index on ties), *accepted = the number of leading drafts with
+ * d_(j+1) == next_tokens[j].  The slot is cut back to p0 + 1 + accepted (the
+ * next token, next_tokens[accepted], is not in the cache).  out (device bf16
+ * [m][hidden]) receives the rows' outputs as kvr_verify's, or may be null.
+ * next_tokens (host, m entries) and accepted are written after the call has
+ * synchronised the stream.  int4 weights only (KVR_ERR_UNSUPPORTED otherwise).
+ * On error the slot keeps its length before the call. */
+int kvr_verify_accept(kvr_ctx* ctx, int slot, const int32_t* tokens, int m, const void* hidden,
+                      const kvr_layer_weights* weights, const kvr_head_weights* head, void* out,
+                      int32_t* next_tokens, int* accepted, void* stream);
 
 /* Per-kernel-class timing with CUDA events recorded on the launch stream.
  * While enabled, every launch is bracketed by an event pair; kvr_profile_read

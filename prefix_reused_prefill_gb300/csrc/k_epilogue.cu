@@ -309,6 +309,32 @@ cudaError_t launch_embed(const __nv_bfloat16* hidden, int m, int H, const __nv_b
   return launch_k(embed_kernel, m, 256, 0, st, hidden, H, gain, eps, h, a);
 }
 
+// One warp per token: the largest of the tiles' bests, lowest row on ties.
+__global__ void __launch_bounds__(256) head_argmax_kernel(const float2* best, int tiles, int m, int32_t* out) {
+  dev::pdl_trigger();
+  dev::pdl_wait();
+  const int t = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (t >= m) return;
+  float bv = -INFINITY;
+  int bi = 0x7fffffff;
+  for (int k = lane; k < tiles; k += 32) {
+    const float2 v = best[(long long)t * tiles + k];
+    const int i = (int)v.y;
+    if (v.x > bv || (v.x == bv && i < bi)) { bv = v.x; bi = i; }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+    if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
+  }
+  if (lane == 0) out[t] = bi;
+}
+
+cudaError_t launch_head_argmax(const float2* best, int tiles, int m, int32_t* out, cudaStream_t st) {
+  return launch_k(head_argmax_kernel, (m + 7) / 8, 256, 0, st, best, tiles, m, out);
+}
+
 cudaError_t launch_rmsnorm(const float* h, int c0, int mb, int H, const __nv_bfloat16* gain,
                            float eps, __nv_bfloat16* a, cudaStream_t st) {
   const int v = (H / 4 + 255) / 256;

@@ -36,7 +36,9 @@
 //     runs as its own small launch), and on the last layer out = bf16(h);
 //   * Swiglu: the tile holds gate rows n0..n0+63 and the same up rows, so
 //     z = bf16(silu(g) * u) is local to the tile;
-//   * Cast: out = bf16(y) (attention-only layers).
+//   * Cast: out = bf16(y) (attention-only layers);
+//   * Argmax: per token, the tile's largest logit and its row (the LM head of
+//     greedy verification; a small launch reduces the tiles).
 #include "kvr_internal.cuh"
 
 namespace kvr {
@@ -168,6 +170,31 @@ __device__ __forceinline__ int unit_owner(long long u, int units, int ctas) {
 
 constexpr int kMaxOwnTiles = 16;   // tiles one CTA may finish (host keeps it below)
 constexpr int kConBatch = 8;       // contribution loads kept in flight by the reduction
+
+// per token: the tile's largest logit and its row (lowest row on ties); warp w
+// takes tokens w, w+8, ..., lane l rows l, l+32, l+64, l+96
+__device__ __forceinline__ void epi_argmax(const GemvParams& p, const GemvSeg& seg, int tile, int row0,
+                                           const float* ct, int tid) {
+  const int warp = tid >> 5, lane = tid & 31;
+  const int nv = min(kGemvRows, seg.N - row0);
+  for (int t = warp; t < p.mb; t += kConsumerWarps) {
+    float bv = -INFINITY;
+    int bi = 0x7fffffff;
+#pragma unroll
+    for (int r = 0; r < kGemvRows / 32; ++r) {
+      const int j = lane + 32 * r;
+      const float v = j < nv ? ct[t * kTileLd + j] : -INFINITY;
+      if (j < nv && (v > bv || (v == bv && j < bi))) { bv = v; bi = j; }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
+    }
+    if (lane == 0) p.best[(long long)(p.c0 + t) * p.tiles + tile] = make_float2(bv, (float)(row0 + bi));
+  }
+}
 
 // two CTAs per SM for up to 16 tokens (the host sizes the grid for it)
 template <int NT, int EPI>
@@ -439,6 +466,7 @@ __global__ void __launch_bounds__(kThreads, NT == 4 ? 1 : 2) gemv_int4_kernel(co
     if (EPI == kGemvEpiQKV) epi_qkv(p, p.seg[s], s, row0, ct, tid);
     else if (EPI == kGemvEpiResid) epi_resid(p, row0, ct, tid);
     else if (EPI == kGemvEpiSwiglu) epi_swiglu(p, row0, ct, tid);
+    else if (EPI == kGemvEpiArgmax) epi_argmax(p, p.seg[s], tile, row0, ct, tid);
     else epi_cast(p, p.seg[s], row0, ct, tid);
     consumers_sync();
   }
@@ -501,8 +529,8 @@ namespace {
 
 template <int NT>
 cudaError_t setup_nt() {
-  void (*ks[4])(GemvParams) = {gemv_int4_kernel<NT, 0>, gemv_int4_kernel<NT, 1>, gemv_int4_kernel<NT, 2>,
-                               gemv_int4_kernel<NT, 3>};
+  void (*ks[5])(GemvParams) = {gemv_int4_kernel<NT, 0>, gemv_int4_kernel<NT, 1>, gemv_int4_kernel<NT, 2>,
+                               gemv_int4_kernel<NT, 3>, gemv_int4_kernel<NT, 4>};
   for (auto k : ks) {
     const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, GemvCfg<NT>::kSmem);
     if (e != cudaSuccess) return e;
@@ -517,6 +545,7 @@ cudaError_t launch_nt(const GemvParams& p, dim3 grid, cudaStream_t st) {
     case kGemvEpiResid: return launch_k(gemv_int4_kernel<NT, 1>, grid, kThreads, GemvCfg<NT>::kSmem, st, p);
     case kGemvEpiSwiglu: return launch_k(gemv_int4_kernel<NT, 2>, grid, kThreads, GemvCfg<NT>::kSmem, st, p);
     case kGemvEpiCast: return launch_k(gemv_int4_kernel<NT, 3>, grid, kThreads, GemvCfg<NT>::kSmem, st, p);
+    case kGemvEpiArgmax: return launch_k(gemv_int4_kernel<NT, 4>, grid, kThreads, GemvCfg<NT>::kSmem, st, p);
   }
   return cudaErrorInvalidValue;
 }

@@ -34,6 +34,7 @@ namespace {
 
 constexpr size_t kAlign = 256;
 constexpr int kCounters = 16384;   // per-tile arrival counters of the fused GEMV epilogues
+constexpr int kVerifyMaxRows = 64; // rows of one verify call
 inline size_t align_up(size_t x, size_t a = kAlign) { return (x + a - 1) / a * a; }
 
 enum ProfClass { kProj = 0, kAttn = 1, kEpi = 2, kMatch = 3 };
@@ -61,6 +62,7 @@ bool valid_config(const kvr_config* c, std::string* why) {
   if (c->max_rows <= 0) return bad("max_rows must be positive");
   if (c->max_rows > c->capacity) return bad("max_rows must not exceed capacity");
   if ((long long)c->max_rows * c->n_q_heads / c->n_kv_heads > (1 << 20)) return bad("max_rows too large");
+  if (c->vocab < 0 || c->vocab > KVR_MAX_VOCAB) return bad("vocab must be in [0, 262144]");
   return true;
 }
 
@@ -87,7 +89,7 @@ int attn_nsplit(int Hkv, int R, int kend_max, int target) {
 }
 
 struct ScratchLayout {
-  size_t status, counters, prompt, slot_len, match_out, rope, h, a, q, o, z, part, opart, ml, total;
+  size_t status, counters, prompt, slot_len, match_out, rope, h, a, q, o, z, part, opart, ml, best, next, total;
   size_t part_floats, opart_floats, ml_count;
 };
 
@@ -114,6 +116,10 @@ ScratchLayout scratch_layout(const kvr_config* c) {
   if (c->weight_format == KVR_WEIGHTS_INT4_G32)
     L.part_floats = std::max(L.part_floats, (size_t)kGemmMaxSplit * kGemmMaxTok *
                                                 std::max(qkv_cols(c), c->hidden));
+  // the output head's GEMV: up to three contributions per 128-row tile
+  const size_t head_tiles = ((size_t)c->vocab + kGemvRows - 1) / kGemvRows;
+  if (c->weight_format == KVR_WEIGHTS_INT4_G32)
+    L.part_floats = std::max(L.part_floats, head_tiles * 3 * kGemvMaxCols * kGemvRows);
   L.part = take(L.part_floats * 4);
   size_t worst = 0;
   const int G = c->n_q_heads / c->n_kv_heads;
@@ -125,6 +131,8 @@ ScratchLayout scratch_layout(const kvr_config* c) {
   L.ml_count = worst * c->n_q_heads;
   L.opart = take(L.opart_floats * 4);
   L.ml = take(L.ml_count * 8);
+  L.best = take((size_t)kVerifyMaxRows * head_tiles * 8);
+  L.next = take((size_t)kVerifyMaxRows * 4);
   L.total = off;
   return L;
 }
@@ -176,6 +184,8 @@ struct kvr_ctx {
   float* part = nullptr;
   float* opart = nullptr;
   float2* ml = nullptr;
+  float2* best = nullptr;   // output head: per row and tile, the largest logit and its index
+  int32_t* next = nullptr;  // output head: per row, the argmax
   // TMA descriptors
   CUtensorMap tm_kv{}, tm_vt{}, tm_q{};
   CUtensorMap tm_a[6]{}, tm_o[6]{}, tm_z[6]{};
@@ -374,6 +384,7 @@ struct Fused {
   long long k_off = 0, v_off = 0;         // QKV
   __nv_bfloat16* out = nullptr;           // Resid (last layer) / Cast
   const __nv_bfloat16* norm_gain = nullptr;  // Resid: RMSNorm the new rows into c->a
+  float2* best = nullptr;                 // Argmax
 };
 
 // Small-m int4 passes: the GEMV with its fused epilogue (plus the RMSNorm of
@@ -435,6 +446,7 @@ int project_gemv_int4(kvr_ctx* c, cudaStream_t st, const Seg* segs, int nseg, co
   p.ldout = cfg.hidden;
   p.z = c->z;
   p.F = cfg.ffn;
+  p.best = fz.best;
   for (int c0 = 0; c0 < m; c0 += kGemvMaxCols) {
     const int mb = std::min(kGemvMaxCols, m - c0);
     p.c0 = c0;
@@ -596,8 +608,11 @@ int attention(kvr_ctx* c, cudaStream_t st, int slot, int layer, const RowMap& ro
 }
 
 // The layer stack for the rows of one call.
+// out (bf16 [m][hidden]) may be null; head_gain: RMSNorm the last layer's rows
+// with it into c->a (the output head's input)
 int run_stack(kvr_ctx* c, int slot, const RowMap& rows, const void* hidden,
-              const kvr_layer_weights* w, void* out, cudaStream_t st) {
+              const kvr_layer_weights* w, void* out, cudaStream_t st,
+              const __nv_bfloat16* head_gain = nullptr) {
   const kvr_config& k = c->cfg;
   const int m = rows.m, H = k.hidden, d = k.head_dim;
   const int Hq = k.n_q_heads, Hkv = k.n_kv_heads, F = k.ffn;
@@ -684,10 +699,11 @@ int run_stack(kvr_ctx* c, int slot, const RowMap& rows, const void* hidden,
                    fz, /*swiglu=*/true);
       if (rc) return rc;
     }
-    // down + residual, then the next layer's attention norm (or the output)
+    // down + residual, then the next layer's attention norm (the output head's
+    // norm after the last layer), and the output
     {
       Seg sd = {W.wd, W.sd, H};
-      const __nv_bfloat16* gain = last ? nullptr : static_cast<const __nv_bfloat16*>(w[l + 1].norm_attn);
+      const __nv_bfloat16* gain = last ? head_gain : static_cast<const __nv_bfloat16*>(w[l + 1].norm_attn);
       Fused fz;
       fz.epi = kGemvEpiResid;
       fz.norm_gain = gain;
@@ -695,7 +711,7 @@ int run_stack(kvr_ctx* c, int slot, const RowMap& rows, const void* hidden,
       rc = project(c, st, &sd, 1, Act::Z, F, m,
                    [&](const float* part, long long plane, int ks, int ldo, int c0, int mb) {
                      return launch_epi_resid(part, plane, ks, ldo, c0, mb, H, c->h, gain, k.rms_eps,
-                                             last ? nullptr : c->a,
+                                             gain ? c->a : nullptr,
                                              last ? static_cast<__nv_bfloat16*>(out) : nullptr, st);
                    }, fz);
       if (rc) return rc;
@@ -744,10 +760,12 @@ int upload_tokens(kvr_ctx* c, int slot, int at, const int32_t* toks, int n, cuda
 }
 
 int prefill_common(kvr_ctx* c, int slot, const int32_t* tokens, int m, const void* hidden,
-                   const kvr_layer_weights* w, void* out, void* stream, int max_m) {
+                   const kvr_layer_weights* w, void* out, void* stream, int max_m,
+                   const __nv_bfloat16* head_gain = nullptr) {
   if (!c) return KVR_ERR_ARG;
   if (slot < 0 || slot >= c->granted) return fail(c, KVR_ERR_ARG, "bad slot %d", slot);
-  if (!tokens || !hidden || !out || m <= 0) return fail(c, KVR_ERR_ARG, "null pointer or m <= 0");
+  if (!tokens || !hidden || (!out && !head_gain) || m <= 0)
+    return fail(c, KVR_ERR_ARG, "null pointer or m <= 0");
   if (m > max_m) return fail(c, KVR_ERR_ARG, "m = %d exceeds %d for this call", m, max_m);
   if (((uintptr_t)hidden & 15) || ((uintptr_t)out & 15)) return fail(c, KVR_ERR_ARG, "hidden/out must be 16-byte aligned");
   if (!weights_ok(c, w)) return fail(c, KVR_ERR_ARG, "missing or misaligned weight pointer");
@@ -764,7 +782,7 @@ int prefill_common(kvr_ctx* c, int slot, const int32_t* tokens, int m, const voi
   rows.n_branch = 1;
   rows.off[0] = 0;
   rows.off[1] = m;
-  int rc = run_stack(c, slot, rows, hidden, w, out, st);
+  int rc = run_stack(c, slot, rows, hidden, w, out, st, head_gain);
   if (rc) return rc;
   rc = upload_tokens(c, slot, p0, tokens, m, st);
   if (rc) return rc;
@@ -845,6 +863,8 @@ int kvr_ctx_create(const kvr_config* cfg, void* kv_arena, size_t arena_bytes, vo
   c->part = reinterpret_cast<float*>(s + c->sl.part);
   c->opart = reinterpret_cast<float*>(s + c->sl.opart);
   c->ml = reinterpret_cast<float2*>(s + c->sl.ml);
+  c->best = reinterpret_cast<float2*>(s + c->sl.best);
+  c->next = reinterpret_cast<int32_t*>(s + c->sl.next);
 
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -1039,7 +1059,53 @@ int kvr_prefill_suffix(kvr_ctx* c, int slot, const int32_t* tokens, int m, const
 
 int kvr_verify(kvr_ctx* c, int slot, const int32_t* tokens, int m, const void* hidden,
                const kvr_layer_weights* w, void* out, void* stream) {
-  return prefill_common(c, slot, tokens, m, hidden, w, out, stream, 64);
+  return prefill_common(c, slot, tokens, m, hidden, w, out, stream, kVerifyMaxRows);
+}
+
+int kvr_verify_accept(kvr_ctx* c, int slot, const int32_t* tokens, int m, const void* hidden,
+                      const kvr_layer_weights* w, const kvr_head_weights* head, void* out,
+                      int32_t* next_tokens, int* accepted, void* stream) {
+  if (!c) return KVR_ERR_ARG;
+  const kvr_config& k = c->cfg;
+  if (!head || !next_tokens || !accepted) return fail(c, KVR_ERR_ARG, "null head or result pointer");
+  if (k.weight_format != KVR_WEIGHTS_INT4_G32 || k.attn_only)
+    return fail(c, KVR_ERR_UNSUPPORTED, "the output head needs int4 weights and the full decoder layer");
+  if (head->vocab <= 0 || head->vocab > k.vocab)
+    return fail(c, KVR_ERR_ARG, "head vocab %d outside [1, %d] (the configured vocab)", head->vocab, k.vocab);
+  for (const void* q : {head->norm, head->w, head->s})
+    if (!q || (reinterpret_cast<uintptr_t>(q) & 15)) return fail(c, KVR_ERR_ARG, "missing or misaligned head pointer");
+  if (slot < 0 || slot >= c->granted) return fail(c, KVR_ERR_ARG, "bad slot %d", slot);
+  const int p0 = (int)c->slots[slot].tokens.size();
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int rc = prefill_common(c, slot, tokens, m, hidden, w, out, stream, kVerifyMaxRows,
+                          static_cast<const __nv_bfloat16*>(head->norm));
+  if (rc) return rc;
+  // logits = a * lm^T (a = the normed rows), each tile's best, then each row's
+  Seg seg = {head->w, head->s, head->vocab};
+  Fused fz;
+  fz.epi = kGemvEpiArgmax;
+  fz.best = c->best;
+  rc = project_gemv_int4(c, st, &seg, 1, c->tm_a, k.hidden, m, fz);
+  cudaError_t e = cudaSuccess;
+  if (!rc) {
+    Timed t(c, kEpi, st);
+    e = launch_head_argmax(c->best, (head->vocab + kGemvRows - 1) / kGemvRows, m, c->next, st);
+    if (e != cudaSuccess) rc = cuda_fail(c, e, "head argmax launch");
+  }
+  if (!rc) {
+    e = cudaMemcpyAsync(next_tokens, c->next, (size_t)m * 4, cudaMemcpyDeviceToHost, st);
+    if (e != cudaSuccess) rc = cuda_fail(c, e, "next-token readback");
+  }
+  if (!rc) rc = kvr_sync_status(c, stream);
+  if (rc) {
+    c->slots[slot].tokens.resize(p0);
+    return rc;
+  }
+  int a = 0;
+  while (a + 1 < m && tokens[a + 1] == next_tokens[a]) ++a;
+  *accepted = a;
+  c->slots[slot].tokens.resize(p0 + 1 + a);
+  return KVR_OK;
 }
 
 int kvr_prefill_branches(kvr_ctx* c, int slot, int n_branch, const int* lens, const int32_t* tokens,

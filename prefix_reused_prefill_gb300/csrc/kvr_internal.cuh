@@ -67,6 +67,7 @@ enum GemvEpi : int {
   kGemvEpiResid = 1,   // h += y (fp32 residual stream); optionally out = bf16(h)
   kGemvEpiSwiglu = 2,  // tile = 64 gate rows + the same 64 up rows: z = bf16(silu(g) * u)
   kGemvEpiCast = 3,    // out = bf16(y)
+  kGemvEpiArgmax = 4,  // per token, the tile's largest y and its row (lowest on ties) -> best
 };
 
 struct GemvParams {
@@ -101,6 +102,7 @@ struct GemvParams {
   int ldout;
   __nv_bfloat16* z;     // Swiglu: [max_rows][F]
   int F;
+  float2* best;         // Argmax: [token][tiles] (value, row)
 };
 
 struct GemmSeg {
@@ -194,6 +196,9 @@ cudaError_t launch_rope_table(const RowMap& rows, int d, float theta, float2* ta
                               cudaStream_t st);
 cudaError_t launch_embed(const __nv_bfloat16* hidden, int m, int H, const __nv_bfloat16* gain,
                          float eps, float* h, __nv_bfloat16* a, cudaStream_t st);
+// out[t] = the row of the largest value over the tiles' bests of token t
+// (lowest row on ties), t < m
+cudaError_t launch_head_argmax(const float2* best, int tiles, int m, int32_t* out, cudaStream_t st);
 // a[c0 + t] = bf16(RMSNorm(h[c0 + t]) * gain) for t < mb
 cudaError_t launch_rmsnorm(const float* h, int c0, int mb, int H, const __nv_bfloat16* gain,
                            float eps, __nv_bfloat16* a, cudaStream_t st);

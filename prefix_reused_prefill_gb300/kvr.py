@@ -26,7 +26,7 @@ EXPORTED = ["kvr_arena_bytes", "kvr_scratch_bytes", "kvr_ctx_create", "kvr_ctx_i
             "kvr_slot_tokens", "kvr_slot_assign", "kvr_slot_kv", "kvr_prefill_suffix", "kvr_verify",
             "kvr_prefill_branches", "kvr_sync_status", "kvr_profile_enable", "kvr_profile_read",
             "kvr_profile_launches",
-            "kvr_last_error", "kvr_slot_match_static", "kvr_trace_set"]
+            "kvr_last_error", "kvr_slot_match_static", "kvr_trace_set", "kvr_verify_accept"]
 
 
 class KvrError(RuntimeError):
@@ -41,7 +41,7 @@ class KvrConfig(ctypes.Structure):
                 ("head_dim", ctypes.c_int), ("ffn", ctypes.c_int), ("weight_format", ctypes.c_int),
                 ("attn_only", ctypes.c_int), ("match_threshold", ctypes.c_int),
                 ("max_rows", ctypes.c_int), ("rope_theta", ctypes.c_float),
-                ("rms_eps", ctypes.c_float)]
+                ("rms_eps", ctypes.c_float), ("vocab", ctypes.c_int)]
 
 
 _W_FIELDS = ["wq", "wk", "wv", "wo", "wg", "wu", "wd", "sq", "sk", "sv", "so", "sg", "su", "sd",
@@ -50,6 +50,11 @@ _W_FIELDS = ["wq", "wk", "wv", "wo", "wg", "wu", "wd", "sq", "sk", "sv", "so", "
 
 class KvrLayerWeights(ctypes.Structure):
     _fields_ = [(f, ctypes.c_void_p) for f in _W_FIELDS]
+
+
+class KvrHeadWeights(ctypes.Structure):
+    _fields_ = [("norm", ctypes.c_void_p), ("w", ctypes.c_void_p), ("s", ctypes.c_void_p),
+                ("vocab", ctypes.c_int)]
 
 
 _lib = None
@@ -78,6 +83,8 @@ def load_library(path: str = LIB_PATH):
         "kvr_slot_kv": (I, [V, I, I, P(V), P(V)]),
         "kvr_prefill_suffix": (I, [V, I, i32p, I, V, P(KvrLayerWeights), V, V]),
         "kvr_verify": (I, [V, I, i32p, I, V, P(KvrLayerWeights), V, V]),
+        "kvr_verify_accept": (I, [V, I, i32p, I, V, P(KvrLayerWeights), P(KvrHeadWeights), V, i32p,
+                                  P(I), V]),
         "kvr_prefill_branches": (I, [V, I, I, P(I), i32p, V, P(KvrLayerWeights), V, V]),
         "kvr_sync_status": (I, [V, V]),
         "kvr_profile_enable": (I, [V, I]),
@@ -95,12 +102,13 @@ def load_library(path: str = LIB_PATH):
 
 
 def config_for_shape(shape, n_slots: int, capacity: int, max_rows: int,
-                     match_threshold: bool = True, n_layers: Optional[int] = None) -> KvrConfig:
+                     match_threshold: bool = True, n_layers: Optional[int] = None,
+                     vocab: int = 0) -> KvrConfig:
     return KvrConfig(n_slots, capacity, shape.n_layers if n_layers is None else n_layers,
                      shape.hidden, shape.n_q_heads, shape.n_kv_heads, shape.head_dim,
                      shape.ffn, WEIGHTS_INT4_G32 if shape.weight_format == "int4" else WEIGHTS_BF16,
                      1 if shape.attn_only else 0, 1 if match_threshold else 0, max_rows,
-                     shape.rope_theta, shape.rms_eps)
+                     shape.rope_theta, shape.rms_eps, vocab)
 
 
 def _ptr(t) -> Optional[int]:
@@ -128,6 +136,15 @@ def layer_weight_structs(layers: Sequence[Dict[str, object]]):
                 setattr(arr[i], name, _ptr(lw[name]))
                 keep.append(lw[name])
     return arr, keep
+
+
+def head_weight_struct(head: Dict[str, object]):
+    """{"norm": bf16 [H], "lm": Int4Matrix [vocab][H]} -> (ctypes struct, tensors kept alive)."""
+    lm = head["lm"]
+    if not hasattr(lm, "packed"):
+        raise KvrError(-6, "the output head needs int4 weights")
+    st = KvrHeadWeights(_ptr(head["norm"]), _ptr(lm.packed), _ptr(lm.scales), int(lm.packed.shape[0]))
+    return st, [head["norm"], lm.packed, lm.scales]
 
 
 def _i32(tokens) -> ctypes.Array:
@@ -249,6 +266,21 @@ class Kvr:
 
     def kvr_verify(self, slot, tokens, hidden, weights, out=None, stream=None):
         return self._rows_call(self.lib.kvr_verify, slot, tokens, hidden, weights, out, stream)
+
+    def kvr_verify_accept(self, slot, tokens, hidden, weights, head, out=None, stream=None):
+        """Verify [t0, d1 .. dk] and take the greedy decision.  Returns
+        (next_tokens: the argmax of every row, accepted: the drafts kept)."""
+        arr = weights[0] if isinstance(weights, tuple) else weights
+        hs, _keep = head_weight_struct(head)
+        m = len(tokens)
+        assert hidden.dtype == torch.bfloat16 and hidden.is_cuda and hidden.is_contiguous()
+        assert hidden.shape == (m, self.cfg.hidden)
+        nxt = (ctypes.c_int32 * max(m, 1))()
+        acc = ctypes.c_int()
+        self._check(self.lib.kvr_verify_accept(self.ctx, slot, _i32(tokens), m, hidden.data_ptr(), arr,
+                                               ctypes.byref(hs), _ptr(out), nxt, ctypes.byref(acc),
+                                               self._stream(stream)))
+        return list(nxt[:m]), acc.value
 
     def kvr_prefill_branches(self, slot, lens, tokens, hidden, weights, out=None, stream=None):
         arr = weights[0] if isinstance(weights, tuple) else weights

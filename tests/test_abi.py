@@ -44,7 +44,8 @@ def test_sizes_match_documented_layout(lib):
 
 
 @pytest.mark.parametrize("field,value", [("capacity", 100), ("head_dim", 96), ("n_kv_heads", 3),
-                                         ("n_slots", 17), ("max_rows", 0), ("weight_format", 7)])
+                                         ("n_slots", 17), ("max_rows", 0), ("weight_format", 7),
+                                         ("vocab", -1), ("vocab", 262145)])
 def test_invalid_configs_are_refused(lib, field, value):
     from prefix_reused_prefill_gb300 import kvr
     cfg = kvr.config_for_shape(workloads.SHAPES["qwen7b"], 4, 16384, 256)
@@ -63,11 +64,27 @@ def test_int4_width_rule(lib):
     assert lib.kvr_scratch_bytes(ctypes.byref(cfg)) == 0
 
 
+def test_output_head_scratch_grows_with_vocab(lib):
+    """The scratch holds, per verify row and 128-row LM-head tile, one (value, index) pair,
+    and the head GEMV's partial sums (three contributions per tile at most)."""
+    from prefix_reused_prefill_gb300 import kvr
+    shape = workloads.SHAPES["small"]
+    base = lib.kvr_scratch_bytes(ctypes.byref(kvr.config_for_shape(shape, 2, 256, 32)))
+    for vocab in (1000, 32000, 262144):
+        cfg = kvr.config_for_shape(shape, 2, 256, 32, vocab=vocab)
+        tiles = -(-vocab // 128)
+        grow = lib.kvr_scratch_bytes(ctypes.byref(cfg)) - base
+        assert grow >= 64 * tiles * 8 - 256   # the vocab-0 layout keeps one aligned block
+        assert grow <= 64 * tiles * 8 + tiles * 3 * 32 * 128 * 4 + 4096
+
+
 def test_null_context_calls_return_arg_errors(lib):
     n = ctypes.c_int()
     assert lib.kvr_slot_len(None, 0, ctypes.byref(n)) == -1
     assert lib.kvr_slot_truncate(None, 0, 0) == -1
     assert lib.kvr_ctx_destroy(None) == -1
+    acc = ctypes.c_int()
+    assert lib.kvr_verify_accept(None, 0, None, 1, None, None, None, None, None, ctypes.byref(acc), None) == -1
     assert lib.kvr_last_error(None) == b"null context"
 
 
