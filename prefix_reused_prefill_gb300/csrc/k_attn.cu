@@ -331,8 +331,30 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const __grid_constant
   for (int e = 0; e < E; ++e) acc[e] = 0.f;
   const float* src = p.opart + rowidx * D + lane * E;
   const long long sstride = rows * D;
+  if (ns <= 32) {
+    // every split's slice in flight at once, then added in split order
+    float v[32][E];
+#pragma unroll
+    for (int s = 0; s < 32; ++s)
+      if (s < ns) {
+        if (E == 4) {
+          const float4 x = __ldcg(reinterpret_cast<const float4*>(src + s * sstride));
+          v[s][0] = x.x; v[s][1 % E] = x.y; v[s][2 % E] = x.z; v[s][3 % E] = x.w;
+        } else {
+          const float2 x = __ldcg(reinterpret_cast<const float2*>(src + s * sstride));
+          v[s][0] = x.x; v[s][1 % E] = x.y;
+        }
+      }
+#pragma unroll
+    for (int s = 0; s < 32; ++s)
+      if (s < ns) {
+        const float w = __shfl_sync(0xffffffffu, w0, s);
+#pragma unroll
+        for (int e = 0; e < E; ++e) acc[e] += w * v[s][e];
+      }
+  }
 #pragma unroll 8
-  for (int s = 0; s < ns; ++s) {
+  for (int s = ns <= 32 ? ns : 0; s < ns; ++s) {
     const float w = __shfl_sync(0xffffffffu, s < 32 ? w0 : w1, s & 31);
     if (E == 4) {
       const float4 v = *reinterpret_cast<const float4*>(src + s * sstride);
