@@ -57,6 +57,7 @@ extern "C" {
 #define KVR_ERR_TIMEOUT (-4)     /* a device-side wait gave up (status word set)          */
 #define KVR_ERR_FAULT (-5)       /* injected through the KVR_FAULT environment variable   */
 #define KVR_ERR_UNSUPPORTED (-6) /* a shape the kernels do not handle (see kvr_config)    */
+#define KVR_ERR_MISMATCH (-7)    /* a spilled slot from another model or KV layout        */
 
 #define KVR_WEIGHTS_BF16 0
 #define KVR_WEIGHTS_INT4_G32 1
@@ -237,6 +238,45 @@ int kvr_slot_assign(kvr_ctx* ctx, int slot, const int32_t* tokens, int n, void* 
 /* Device addresses of a slot's K and V for one layer: K is [Hkv][capacity][head_dim] bf16,
  * V is [Hkv][head_dim][capacity] bf16 (transposed, see the arena layout). */
 int kvr_slot_kv(const kvr_ctx* ctx, int slot, int layer, void** k, void** v);
+
+/*
+ * Slot spill and restore through host memory (Tempo9 docs, "KV cache spills
+ * to disk, by default": reusable prefixes leave device memory and come back
+ * later, and a record written for another model, dtype or KV layout is
+ * recognised by a configuration hash and refused instead of being served).
+ * Files, the size cap and eviction of records are the caller's.
+ *
+ * kvr_config_hash: FNV-1a (64-bit) over the fields that fix what a slot's K/V
+ * hold -- n_layers, hidden, n_q_heads, n_kv_heads, head_dim, ffn,
+ * weight_format, attn_only, rope_theta, rms_eps (as little-endian 32-bit
+ * words, in that order) -- followed by the caller's 64-bit model_tag (which
+ * names the weights).  n_slots, capacity, match_threshold, max_rows and vocab
+ * do not enter: a record restores into any context whose capacity holds it.
+ *
+ * Record (host bytes, written by kvr_slot_spill, 16-byte aligned sections):
+ *   64-byte header: magic "KVRSLOT1", the hash, len, n_layers, n_kv_heads,
+ *     head_dim, the byte size of the record;
+ *   tokens int32[len], padded to 16 bytes;
+ *   per layer l: K as [Hkv][len][head_dim] bf16, then V^T as
+ *     [Hkv][head_dim][len] bf16 (the arena's layout with capacity cut to len).
+ * kvr_slot_spill_bytes gives the record size of a slot's current length.
+ *
+ * kvr_slot_spill copies the slot into host (caller-owned, `bytes` long) on
+ * `stream`; the record is complete once the stream reaches that point (pinned
+ * host memory makes the copies asynchronous).  KVR_ERR_CAPACITY if bytes is
+ * too small.  The slot is unchanged.
+ * kvr_slot_restore checks the header (KVR_ERR_MISMATCH for another hash,
+ * KVR_ERR_ARG for a damaged header, KVR_ERR_CAPACITY if len > capacity), then
+ * copies the K/V into `slot` on `stream`, sets its tokens and refreshes its
+ * LRU stamp.  The host record must stay valid until the stream reaches the
+ * copies.  A refused record leaves the slot unchanged; a copy that fails
+ * leaves it empty (length 0).
+ */
+uint64_t kvr_config_hash(const kvr_config* cfg, uint64_t model_tag);
+size_t kvr_slot_spill_bytes(const kvr_ctx* ctx, int slot);
+int kvr_slot_spill(kvr_ctx* ctx, int slot, uint64_t model_tag, void* host, size_t bytes, void* stream);
+int kvr_slot_restore(kvr_ctx* ctx, int slot, uint64_t model_tag, const void* host, size_t bytes,
+                     void* stream);
 
 /*
  * Suffix prefill: run m rows (tokens: host int32[m]; hidden: device bf16

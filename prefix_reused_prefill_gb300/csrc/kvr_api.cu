@@ -793,6 +793,73 @@ int prefill_common(kvr_ctx* c, int slot, const int32_t* tokens, int m, const voi
   return KVR_OK;
 }
 
+// ---------------------------------------------------------------- spill/restore
+struct SpillHeader {
+  char magic[8];      // "KVRSLOT1"
+  uint64_t hash;      // kvr_config_hash of the writer
+  uint64_t bytes;     // size of the whole record
+  int32_t len, n_layers, n_kv_heads, head_dim;
+  uint8_t reserved[24];
+};
+static_assert(sizeof(SpillHeader) == 64, "spill header is 64 bytes");
+constexpr char kSpillMagic[8] = {'K', 'V', 'R', 'S', 'L', 'O', 'T', '1'};
+
+struct SpillLayout {
+  size_t tokens, kv, layer_bytes, half_bytes, total;
+};
+
+SpillLayout spill_layout(int len, int n_layers, int hkv, int d) {
+  SpillLayout L;
+  L.tokens = sizeof(SpillHeader);
+  L.kv = L.tokens + align_up((size_t)len * 4, 16);
+  L.half_bytes = (size_t)hkv * len * d * 2;   // K or V^T of one layer
+  L.layer_bytes = 2 * L.half_bytes;
+  L.total = L.kv + (size_t)n_layers * L.layer_bytes;
+  return L;
+}
+
+uint64_t fnv1a_words(const uint32_t* w, int n, uint64_t tag) {
+  uint64_t h = 0xcbf29ce484222325ull;
+  auto eat = [&](uint8_t b) { h = (h ^ b) * 0x100000001b3ull; };
+  for (int i = 0; i < n; ++i)
+    for (int k = 0; k < 4; ++k) eat((uint8_t)(w[i] >> (8 * k)));
+  for (int k = 0; k < 8; ++k) eat((uint8_t)(tag >> (8 * k)));
+  return h;
+}
+
+uint32_t float_word(float f) {
+  uint32_t u;
+  memcpy(&u, &f, 4);
+  return u;
+}
+
+// one 2-D copy per layer for K ([Hkv] blocks of len*d) and one for V^T
+// ([Hkv*d] rows of len); to_host picks the direction
+cudaError_t copy_slot_kv(kvr_ctx* c, int slot, int len, uint8_t* host, bool to_host, cudaStream_t st) {
+  const kvr_config& k = c->cfg;
+  const size_t cap = k.capacity, d = k.head_dim, hkv = k.n_kv_heads;
+  const SpillLayout L = spill_layout(len, k.n_layers, k.n_kv_heads, k.head_dim);
+  if (len == 0) return cudaSuccess;
+  uint8_t* arena = c->arena;
+  for (int l = 0; l < k.n_layers; ++l) {
+    uint8_t* kd = arena + kv_offset(c, slot, l, 0) * 2;
+    uint8_t* vd = arena + kv_offset(c, slot, l, 1) * 2;
+    uint8_t* kh = host + L.kv + l * L.layer_bytes;
+    uint8_t* vh = kh + L.half_bytes;
+    const size_t kw = (size_t)len * d * 2, vw = (size_t)len * 2;
+    cudaError_t e;
+    if (to_host) {
+      e = cudaMemcpy2DAsync(kh, kw, kd, cap * d * 2, kw, hkv, cudaMemcpyDeviceToHost, st);
+      if (e == cudaSuccess) e = cudaMemcpy2DAsync(vh, vw, vd, cap * 2, vw, hkv * d, cudaMemcpyDeviceToHost, st);
+    } else {
+      e = cudaMemcpy2DAsync(kd, cap * d * 2, kh, kw, kw, hkv, cudaMemcpyHostToDevice, st);
+      if (e == cudaSuccess) e = cudaMemcpy2DAsync(vd, cap * 2, vh, vw, vw, hkv * d, cudaMemcpyHostToDevice, st);
+    }
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
 }  // namespace
 
 // ===========================================================================
@@ -1040,6 +1107,75 @@ int kvr_slot_assign(kvr_ctx* c, int slot, const int32_t* tokens, int n, void* st
   if (rc) return rc;
   c->slots[slot].occupied = true;
   c->slots[slot].tokens.assign(tokens, tokens + n);
+  touch(c, slot);
+  return KVR_OK;
+}
+
+uint64_t kvr_config_hash(const kvr_config* cfg, uint64_t model_tag) {
+  if (!cfg) return 0;
+  const uint32_t w[10] = {(uint32_t)cfg->n_layers,      (uint32_t)cfg->hidden,   (uint32_t)cfg->n_q_heads,
+                          (uint32_t)cfg->n_kv_heads,    (uint32_t)cfg->head_dim, (uint32_t)cfg->ffn,
+                          (uint32_t)cfg->weight_format, (uint32_t)cfg->attn_only, float_word(cfg->rope_theta),
+                          float_word(cfg->rms_eps)};
+  return fnv1a_words(w, 10, model_tag);
+}
+
+size_t kvr_slot_spill_bytes(const kvr_ctx* c, int slot) {
+  if (!c || slot < 0 || slot >= c->granted) return 0;
+  return spill_layout((int)c->slots[slot].tokens.size(), c->cfg.n_layers, c->cfg.n_kv_heads, c->cfg.head_dim).total;
+}
+
+int kvr_slot_spill(kvr_ctx* c, int slot, uint64_t model_tag, void* host, size_t bytes, void* stream) {
+  if (!c) return KVR_ERR_ARG;
+  if (slot < 0 || slot >= c->granted || !host) return fail(c, KVR_ERR_ARG, "bad slot %d or null record", slot);
+  const kvr_config& k = c->cfg;
+  const int len = (int)c->slots[slot].tokens.size();
+  const SpillLayout L = spill_layout(len, k.n_layers, k.n_kv_heads, k.head_dim);
+  if (bytes < L.total) return fail(c, KVR_ERR_CAPACITY, "spill of slot %d needs %zu bytes", slot, L.total);
+  uint8_t* rec = static_cast<uint8_t*>(host);
+  SpillHeader hd;
+  memset(&hd, 0, sizeof hd);
+  memcpy(hd.magic, kSpillMagic, 8);
+  hd.hash = kvr_config_hash(&k, model_tag);
+  hd.bytes = L.total;
+  hd.len = len;
+  hd.n_layers = k.n_layers;
+  hd.n_kv_heads = k.n_kv_heads;
+  hd.head_dim = k.head_dim;
+  memcpy(rec, &hd, sizeof hd);
+  memset(rec + L.tokens, 0, L.kv - L.tokens);
+  if (len > 0) memcpy(rec + L.tokens, c->slots[slot].tokens.data(), (size_t)len * 4);
+  cudaError_t e = copy_slot_kv(c, slot, len, rec, true, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? KVR_OK : cuda_fail(c, e, "slot spill copy");
+}
+
+int kvr_slot_restore(kvr_ctx* c, int slot, uint64_t model_tag, const void* host, size_t bytes, void* stream) {
+  if (!c) return KVR_ERR_ARG;
+  if (slot < 0 || slot >= c->granted || !host) return fail(c, KVR_ERR_ARG, "bad slot %d or null record", slot);
+  const kvr_config& k = c->cfg;
+  if (bytes < sizeof(SpillHeader)) return fail(c, KVR_ERR_ARG, "record shorter than its header");
+  SpillHeader hd;
+  memcpy(&hd, host, sizeof hd);
+  if (memcmp(hd.magic, kSpillMagic, 8)) return fail(c, KVR_ERR_ARG, "not a slot record");
+  if (hd.hash != kvr_config_hash(&k, model_tag))
+    return fail(c, KVR_ERR_MISMATCH, "slot record from another model or KV layout");
+  if (hd.n_layers != k.n_layers || hd.n_kv_heads != k.n_kv_heads || hd.head_dim != k.head_dim || hd.len < 0)
+    return fail(c, KVR_ERR_ARG, "damaged slot record header");
+  const SpillLayout L = spill_layout(hd.len, k.n_layers, k.n_kv_heads, k.head_dim);
+  if (hd.bytes != L.total || bytes < L.total) return fail(c, KVR_ERR_ARG, "slot record truncated or damaged");
+  if (hd.len > k.capacity) return fail(c, KVR_ERR_CAPACITY, "record of %d tokens exceeds capacity %d", hd.len, k.capacity);
+  const uint8_t* rec = static_cast<const uint8_t*>(host);
+  const int32_t* toks = reinterpret_cast<const int32_t*>(rec + L.tokens);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  SlotState& S = c->slots[slot];
+  cudaError_t e = copy_slot_kv(c, slot, hd.len, const_cast<uint8_t*>(rec), false, st);
+  int rc = e == cudaSuccess ? upload_tokens(c, slot, 0, toks, hd.len, st) : cuda_fail(c, e, "slot restore copy");
+  if (rc) {   // the slot's K/V may be partly overwritten: leave it empty
+    S.tokens.clear();
+    return rc;
+  }
+  S.occupied = true;
+  S.tokens.assign(toks, toks + hd.len);
   touch(c, slot);
   return KVR_OK;
 }

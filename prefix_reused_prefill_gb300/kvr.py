@@ -17,7 +17,7 @@ LIB_PATH = os.path.join(HERE, "libkvr.so")
 
 KVR_OK = 0
 ERRORS = {-1: "KVR_ERR_ARG", -2: "KVR_ERR_CAPACITY", -3: "KVR_ERR_CUDA", -4: "KVR_ERR_TIMEOUT",
-          -5: "KVR_ERR_FAULT", -6: "KVR_ERR_UNSUPPORTED"}
+          -5: "KVR_ERR_FAULT", -6: "KVR_ERR_UNSUPPORTED", -7: "KVR_ERR_MISMATCH"}
 WEIGHTS_BF16, WEIGHTS_INT4_G32 = 0, 1
 MAX_SLOTS, MAX_BRANCHES = 16, 16
 
@@ -26,7 +26,8 @@ EXPORTED = ["kvr_arena_bytes", "kvr_scratch_bytes", "kvr_ctx_create", "kvr_ctx_i
             "kvr_slot_tokens", "kvr_slot_assign", "kvr_slot_kv", "kvr_prefill_suffix", "kvr_verify",
             "kvr_prefill_branches", "kvr_sync_status", "kvr_profile_enable", "kvr_profile_read",
             "kvr_profile_launches",
-            "kvr_last_error", "kvr_slot_match_static", "kvr_trace_set", "kvr_verify_accept"]
+            "kvr_last_error", "kvr_slot_match_static", "kvr_trace_set", "kvr_verify_accept",
+            "kvr_config_hash", "kvr_slot_spill_bytes", "kvr_slot_spill", "kvr_slot_restore"]
 
 
 class KvrError(RuntimeError):
@@ -93,6 +94,10 @@ def load_library(path: str = LIB_PATH):
         "kvr_last_error": (ctypes.c_char_p, [V]),
         "kvr_slot_match_static": (I, [V, i32p, I, P(I), P(I), V]),
         "kvr_trace_set": (I, [V, V, Z]),
+        "kvr_config_hash": (ctypes.c_uint64, [P(KvrConfig), ctypes.c_uint64]),
+        "kvr_slot_spill_bytes": (Z, [V, I]),
+        "kvr_slot_spill": (I, [V, I, ctypes.c_uint64, V, Z, V]),
+        "kvr_slot_restore": (I, [V, I, ctypes.c_uint64, V, Z, V]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -281,6 +286,27 @@ class Kvr:
                                                ctypes.byref(hs), _ptr(out), nxt, ctypes.byref(acc),
                                                self._stream(stream)))
         return list(nxt[:m]), acc.value
+
+    def kvr_slot_spill(self, slot: int, model_tag: int = 0, stream=None, sync: bool = True) -> torch.Tensor:
+        """The slot's record in pinned host memory (uint8); complete once the
+        stream has passed the copies (sync=True waits for it)."""
+        n = self.lib.kvr_slot_spill_bytes(self.ctx, slot)
+        if n == 0:
+            raise KvrError(-1, f"bad slot {slot}")
+        rec = torch.empty(n, dtype=torch.uint8, pin_memory=True)
+        st = self._stream(stream)
+        self._check(self.lib.kvr_slot_spill(self.ctx, slot, model_tag, rec.data_ptr(), n, st))
+        if sync:
+            (stream if stream is not None else torch.cuda.current_stream()).synchronize()
+        return rec
+
+    def kvr_slot_restore(self, slot: int, record: torch.Tensor, model_tag: int = 0, stream=None,
+                         sync: bool = True):
+        assert record.dtype == torch.uint8 and record.device.type == "cpu" and record.is_contiguous()
+        self._check(self.lib.kvr_slot_restore(self.ctx, slot, model_tag, record.data_ptr(), record.numel(),
+                                              self._stream(stream)))
+        if sync:
+            (stream if stream is not None else torch.cuda.current_stream()).synchronize()
 
     def kvr_prefill_branches(self, slot, lens, tokens, hidden, weights, out=None, stream=None):
         arr = weights[0] if isinstance(weights, tuple) else weights

@@ -78,6 +78,49 @@ def test_output_head_scratch_grows_with_vocab(lib):
         assert grow <= 64 * tiles * 8 + tiles * 3 * 32 * 128 * 4 + 4096
 
 
+def _fnv1a64(data: bytes) -> int:
+    """FNV-1a, 64-bit: offset basis 14695981039346656037, prime 1099511628211."""
+    h = 14695981039346656037
+    for byte in data:
+        h = ((h ^ byte) * 1099511628211) % (1 << 64)
+    return h
+
+
+def test_fnv1a_reference_vectors():
+    # the published FNV-1a 64-bit values of the empty string and of "a"
+    assert _fnv1a64(b"") == 0xcbf29ce484222325
+    assert _fnv1a64(b"a") == 0xaf63dc4c8601ec8c
+
+
+def test_config_hash_is_fnv1a_of_the_kv_fields(lib):
+    import struct
+    from prefix_reused_prefill_gb300 import kvr
+    cfg = kvr.config_for_shape(workloads.SHAPES["dense9b"], 4, 8192, 256)
+    for tag in (0, 1, 0x0123456789abcdef):
+        words = struct.pack("<8I", cfg.n_layers, cfg.hidden, cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim,
+                            cfg.ffn, cfg.weight_format, cfg.attn_only)
+        words += struct.pack("<2f", cfg.rope_theta, cfg.rms_eps) + struct.pack("<Q", tag)
+        assert lib.kvr_config_hash(ctypes.byref(cfg), tag) == _fnv1a64(words)
+
+
+def test_config_hash_sees_the_kv_fields_only(lib):
+    from prefix_reused_prefill_gb300 import kvr
+    base = kvr.config_for_shape(workloads.SHAPES["dense9b"], 4, 8192, 256)
+    h0 = lib.kvr_config_hash(ctypes.byref(base), 7)
+    assert lib.kvr_config_hash(ctypes.byref(base), 8) != h0
+    for field, value in [("n_layers", 35), ("hidden", 4352), ("n_q_heads", 16), ("n_kv_heads", 4),
+                         ("head_dim", 64), ("ffn", 12544), ("weight_format", 0), ("attn_only", 1),
+                         ("rope_theta", 5e5), ("rms_eps", 1e-5)]:
+        cfg = kvr.config_for_shape(workloads.SHAPES["dense9b"], 4, 8192, 256)
+        setattr(cfg, field, value)
+        assert lib.kvr_config_hash(ctypes.byref(cfg), 7) != h0, field
+    for field, value in [("n_slots", 1), ("capacity", 16384), ("max_rows", 64), ("match_threshold", 0),
+                         ("vocab", 32000)]:
+        cfg = kvr.config_for_shape(workloads.SHAPES["dense9b"], 4, 8192, 256)
+        setattr(cfg, field, value)
+        assert lib.kvr_config_hash(ctypes.byref(cfg), 7) == h0, field
+
+
 def test_null_context_calls_return_arg_errors(lib):
     n = ctypes.c_int()
     assert lib.kvr_slot_len(None, 0, ctypes.byref(n)) == -1
@@ -85,6 +128,9 @@ def test_null_context_calls_return_arg_errors(lib):
     assert lib.kvr_ctx_destroy(None) == -1
     acc = ctypes.c_int()
     assert lib.kvr_verify_accept(None, 0, None, 1, None, None, None, None, None, ctypes.byref(acc), None) == -1
+    assert lib.kvr_slot_spill_bytes(None, 0) == 0
+    assert lib.kvr_slot_spill(None, 0, 0, None, 0, None) == -1
+    assert lib.kvr_slot_restore(None, 0, 0, None, 0, None) == -1
     assert lib.kvr_last_error(None) == b"null context"
 
 
