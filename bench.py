@@ -458,6 +458,67 @@ def run_priming(args):
             "reps": args.steps, "warmup": args.warmup, "clocks": clk, "dtype": "bf16", "data": "synthetic"}
 
 
+def run_batch(args):
+    """Continuous batching across conversations: the verify shape (36 layers,
+    H 4096, 32/8 heads, F 12288, int4-g32), 4 slots each holding its own
+    4096-token conversation; m rows per conversation (m in {1, 4}) verified in
+    one kvr_prefill_batch call against 4 separate kvr_verify calls (the slots
+    are cut back outside the timed region).  Reports both times and the HBM
+    fraction of the batched call against its algorithmic bytes (weights once,
+    every conversation's K/V once per KV head, the appends)."""
+    from prefix_reused_prefill_gb300 import Kvr, config_for_shape
+    device = torch.device("cuda", torch.cuda.current_device())
+    pk, pk_kind = peaks()
+    shape = workloads.SHAPES["dense9b"]
+    n = 4
+    seed = workloads.config_seed(3)
+    tks = [workloads.verify_tokens(seed + 17 * j) for j in range(n)]
+    P = len(tks[0]["state"])
+    lws = workloads.stack_weights(shape, seed, device=device)
+    kv = Kvr(config_for_shape(shape, n, P + 256, 256), device=device)
+    w = kv.weights(lws)
+    for j in range(n):
+        _prefill_state(kv, j, tks[j]["state"], shape, seed + j, w, device)
+    L = shape.n_layers
+    table = []
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+
+    def cut():
+        for j in range(n):
+            kv.kvr_slot_truncate(j, P)
+    for m in (1, 4):
+        drafts = [tks[j]["draft"][:m] for j in range(n)]
+        xs = [workloads.hidden_for_tokens(d, shape.hidden, seed + j).to(device) for j, d in enumerate(drafts)]
+        xall = torch.cat(xs).contiguous()
+        out = torch.empty((n * m, shape.hidden), dtype=torch.bfloat16, device=device)
+        outs = [torch.empty((m, shape.hidden), dtype=torch.bfloat16, device=device) for _ in range(n)]
+        ms_b = _event_ms(lambda: kv.kvr_prefill_batch(list(range(n)), drafts, xall, w, out=out),
+                         args.steps, args.warmup, after=cut)
+
+        def separate():
+            for j in range(n):
+                kv.kvr_verify(j, drafts[j], xs[j], w, out=outs[j])
+        ms_s = _event_ms(separate, args.steps, args.warmup, after=cut)
+        kv.kvr_sync_status()
+        nbytes = (shape.params_per_layer() * 0.5625 * L
+                  + n * (P + m) * shape.n_kv_heads * shape.head_dim * 2 * 2 * L
+                  + n * m * shape.n_kv_heads * shape.head_dim * 4 * L)
+        gbs = nbytes / (ms_b / 1e3) / 1e9
+        table.append({"m_per_conversation": m, "rows": n * m, "ms_batched": round(ms_b, 4),
+                      "ms_separate_4_calls": round(ms_s, 4), "speedup": round(ms_s / ms_b, 3),
+                      "rows_per_s_batched": round(n * m / (ms_b / 1e3), 1),
+                      "algorithmic_gb": round(nbytes / 1e9, 4), "gbs": round(gbs, 1),
+                      "frac_hbm": round(gbs / pk["hbm_gbs"], 4)})
+    clk = clocks.stop()
+    kv.close()
+    return {"metric": "batched verify rows/s", "workload": "4 conversations x 4096 cached tokens, 36 x (H 4096, "
+            "32/8 heads, F 12288) int4-g32, m rows each in one call", "unit": "rows/s", "higher_is_better": True,
+            "per_m": table, "peak_hbm_gbs": pk["hbm_gbs"], "peak_kind": pk_kind,
+            "l2": "inputs larger than L2 (3.9 GB of weights and 2.4 GB of K/V per call)",
+            "reps": args.steps, "warmup": args.warmup, "clocks": clk, "dtype": "bf16", "data": "synthetic"}
+
+
 def run_crossover(args):
     """Attention crossover: one 7B-shaped attention + QKV/O layer, 4 slots of
     16384; the target slot holds P cached tokens (K/V drawn N(0,1)); m rows are
@@ -607,7 +668,7 @@ def main():
     ap.add_argument("--impl", default="kvr", choices=["kvr", "reference"])
     ap.add_argument("--cpu-rows", type=int, default=M_ROWS)
     ap.add_argument("--no-cpu", action="store_true")
-    ap.add_argument("--workload", default="turn9", choices=["turn9", "verify", "priming", "crossover"],
+    ap.add_argument("--workload", default="turn9", choices=["turn9", "verify", "priming", "crossover", "batch"],
                     help="turn9 is the bench line; the others print their own measurement line")
     ap.add_argument("--layers", type=int, default=0,
                     help="profiling aid: run a reduced stack of this many layers")
@@ -617,7 +678,8 @@ def main():
     if args.impl == "reference":
         line, rank = run_reference(args, rank, world)
     elif args.workload != "turn9":
-        runner = {"verify": run_verify, "priming": run_priming, "crossover": run_crossover}[args.workload]
+        runner = {"verify": run_verify, "priming": run_priming, "crossover": run_crossover,
+                  "batch": run_batch}[args.workload]
         line = runner(args) if rank == 0 else None
     else:
         line, rank = run_gpu(args, rank, world)

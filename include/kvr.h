@@ -313,6 +313,26 @@ int kvr_prefill_branches(kvr_ctx* ctx, int slot, int n_branch, const int* lens,
                          const int32_t* tokens, const void* hidden, const kvr_layer_weights* w,
                          void* out, void* stream);
 
+/*
+ * Several conversations in one call (continuous batching across requests:
+ * OpenJev "Next"; goinfer "What was measured", several clients each keeping
+ * their own history; the Tempo9 agents article, "concurrency").  Conversation
+ * j appends lens[j] rows to slot slots[j] after that slot's len_j cached
+ * tokens, with the same result as kvr_prefill_suffix(slots[j], ...) alone;
+ * the projections read each weight once for the rows of every conversation,
+ * and attention runs per conversation over its own slot.
+ *   n_seq          1 .. KVR_MAX_BRANCHES; slots[] distinct and granted.
+ *   lens           host [n_seq], each >= 1; sum <= max_rows and
+ *                  len_j + lens[j] <= capacity.
+ *   tokens         host int32 [sum lens], conversation-major.
+ *   hidden, out    device bf16 [sum lens][hidden] in the same order.
+ * A verify of several conversations is this call followed by one
+ * kvr_slot_truncate per slot.  Errors as kvr_prefill_suffix; on error no
+ * slot's length changes.
+ */
+int kvr_prefill_batch(kvr_ctx* ctx, int n_seq, const int* slots, const int* lens, const int32_t* tokens,
+                      const void* hidden, const kvr_layer_weights* weights, void* out, void* stream);
+
 /* Wait for `stream` and check the device status word that kernels set when a
  * bounded device-side wait gives up.  Returns KVR_ERR_TIMEOUT (and clears the
  * word) if one did. */

@@ -33,29 +33,63 @@ struct AttnCfg {
   static constexpr int kSmem = kStages * kStageBytes + 1024;
 };
 
+// The part of the call one CTA serves: the whole call, or in a batched
+// launch the conversation owning its row tile.
+struct AttnView {
+  int P, m;          // cached prefix, rows
+  int kbase, vtbase;
+  int nsplit;
+  int rt;            // row tile within the rows
+  const __nv_bfloat16* q;
+  __nv_bfloat16* o;
+  float* opart;
+  float2* ml;
+};
+
+template <int D>
+__device__ __forceinline__ AttnView attn_view(const AttnParams& p, int bx) {
+  AttnView v;
+  if (p.n_conv == 0) {
+    v.P = p.rows.P; v.m = p.rows.m; v.kbase = p.kbase; v.vtbase = p.vtbase; v.nsplit = p.nsplit;
+    v.rt = bx; v.q = p.q; v.o = p.o; v.opart = p.opart; v.ml = p.ml;
+    return v;
+  }
+  int b = 0;
+  while (b + 1 < p.n_conv && bx >= p.conv[b + 1].tile0) ++b;
+  const AttnConv& cv = p.conv[b];
+  v.P = cv.P; v.m = cv.m; v.kbase = cv.kbase; v.vtbase = cv.vtbase; v.nsplit = cv.nsplit;
+  v.rt = bx - cv.tile0;
+  const long long qd = (long long)cv.tok0 * p.Hq * D;
+  v.q = p.q + qd; v.o = p.o + qd;
+  v.opart = p.opart + cv.part0; v.ml = p.ml + cv.part0 / D;
+  return v;
+}
+
 struct RowInfo {
-  int tok;      // token index, -1 for padding rows
+  int tok;      // token index within the view, -1 for padding rows
   int head;     // query head
+  int pre;      // keys [0, pre) are the cached prefix
   int lo, hi;   // own-branch visible slot indices [lo, hi]
 };
 
-__device__ __forceinline__ RowInfo row_info(const AttnParams& p, int kv, int rho) {
+__device__ __forceinline__ RowInfo row_info(const AttnParams& p, const AttnView& v, int kv, int rho) {
   RowInfo ri;
-  const int R = p.G * p.rows.m;
+  const int R = p.G * v.m;
+  ri.pre = v.P;
   if (rho >= R) {
     ri.tok = -1; ri.head = 0; ri.lo = 1; ri.hi = 0;
     return ri;
   }
   ri.tok = rho / p.G;
   ri.head = kv * p.G + rho % p.G;
-  const int b = row_branch(p.rows, ri.tok);
-  ri.lo = p.rows.P + p.rows.off[b];
-  ri.hi = p.rows.P + ri.tok;
+  const int b = p.n_conv ? 0 : row_branch(p.rows, ri.tok);
+  ri.lo = v.P + (p.n_conv ? 0 : p.rows.off[b]);
+  ri.hi = v.P + ri.tok;
   return ri;
 }
 
-__device__ __forceinline__ bool visible(const AttnParams& p, const RowInfo& ri, int j) {
-  return ri.tok >= 0 && (j < p.rows.P || (j >= ri.lo && j <= ri.hi));
+__device__ __forceinline__ bool visible(const RowInfo& ri, int j) {
+  return ri.tok >= 0 && (j < ri.pre || (j >= ri.lo && j <= ri.hi));
 }
 
 template <int D, int RW>
@@ -70,15 +104,17 @@ __global__ void __launch_bounds__((RW + 1) * 32) attn_kernel(const __grid_consta
   const uint32_t base = (dev::smem_u32(smem_raw) + 1023u) & ~1023u;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int rt = blockIdx.x, split = blockIdx.y, kv = blockIdx.z;
-  const int R = p.G * p.rows.m;
-  const int row_lo = rt * 16 * RW;
+  const AttnView v = attn_view<D>(p, blockIdx.x);
+  const int split = blockIdx.y, kv = blockIdx.z;
+  if (split >= v.nsplit) return;   // a batched launch: this conversation uses fewer splits
+  const int R = p.G * v.m;
+  const int row_lo = v.rt * 16 * RW;
   const int row_hi = min(R, row_lo + 16 * RW);        // exclusive
   const int last_tok = (row_hi - 1) / p.G;
-  const int kend = p.rows.P + last_tok + 1;            // keys [0, kend) may be visible
+  const int kend = v.P + last_tok + 1;                 // keys [0, kend) may be visible
   const int nb = (kend + kAttnKeys - 1) / kAttnKeys;
-  const int b0 = (int)((long long)nb * split / p.nsplit);
-  const int b1 = (int)((long long)nb * (split + 1) / p.nsplit);
+  const int b0 = (int)((long long)nb * split / v.nsplit);
+  const int b1 = (int)((long long)nb * (split + 1) / v.nsplit);
   const int nblk = b1 - b0;
 
   dev::pdl_trigger();
@@ -100,15 +136,15 @@ __global__ void __launch_bounds__((RW + 1) * 32) attn_kernel(const __grid_consta
       // Blocks wholly inside the cached prefix were written by earlier calls:
       // load them before waiting for the launch that appends this call's K/V.
       int pre = 0;
-      while (pre < nblk && pre < C::kStages && (b0 + pre + 1) * kAttnKeys <= p.rows.P) {
+      while (pre < nblk && pre < C::kStages && (b0 + pre + 1) * kAttnKeys <= v.P) {
         const uint32_t sb = base + pre * C::kStageBytes;
         const uint32_t fb = dev::smem_u32(&full_bar[pre]);
         dev::mbar_arrive_expect_tx(fb, C::kStageBytes);
         const int key0 = (b0 + pre) * kAttnKeys;
 #pragma unroll
         for (int h = 0; h < C::kHalves; ++h)
-          dev::tma_load_2d(sb + h * (kAttnKeys * 128), &p.tkv, 64 * h, p.kbase + kv * p.cap + key0, fb);
-        dev::tma_load_2d(sb + C::kTileBytes, &p.tvt, key0, p.vtbase + kv * D, fb);
+          dev::tma_load_2d(sb + h * (kAttnKeys * 128), &p.tkv, 64 * h, v.kbase + kv * p.cap + key0, fb);
+        dev::tma_load_2d(sb + C::kTileBytes, &p.tvt, key0, v.vtbase + kv * D, fb);
         ++pre;
       }
       dev::pdl_wait();
@@ -129,10 +165,10 @@ __global__ void __launch_bounds__((RW + 1) * 32) attn_kernel(const __grid_consta
         const int key0 = (b0 + it) * kAttnKeys;
 #pragma unroll
         for (int h = 0; h < C::kHalves; ++h) {
-          dev::tma_load_2d(sb + h * (kAttnKeys * 128), &p.tkv, 64 * h, p.kbase + kv * p.cap + key0, fb);
+          dev::tma_load_2d(sb + h * (kAttnKeys * 128), &p.tkv, 64 * h, v.kbase + kv * p.cap + key0, fb);
         }
         // V^T tile: D rows (head elements) x 64 keys
-        dev::tma_load_2d(sb + C::kTileBytes, &p.tvt, key0, p.vtbase + kv * D, fb);
+        dev::tma_load_2d(sb + C::kTileBytes, &p.tvt, key0, v.vtbase + kv * D, fb);
         ++issued;
       }
       for (int st = 0; st < C::kStages && st < issued; ++st) {
@@ -147,16 +183,16 @@ __global__ void __launch_bounds__((RW + 1) * 32) attn_kernel(const __grid_consta
   dev::pdl_wait();   // q comes from the previous launch
   const int r = lane >> 2, c = lane & 3;
   const int rho0 = row_lo + warp * 16 + r;
-  const RowInfo ri0 = row_info(p, kv, rho0);
-  const RowInfo ri1 = row_info(p, kv, rho0 + 8);
+  const RowInfo ri0 = row_info(p, v, kv, rho0);
+  const RowInfo ri1 = row_info(p, v, kv, rho0 + 8);
 
   // Q fragments (A operand of S = Q K^T), loaded once
   uint32_t qa[D / 16][4];
   {
     const __nv_bfloat16* q0 =
-        ri0.tok >= 0 ? p.q + (((long long)kv * p.rows.m + ri0.tok) * p.G + ri0.head % p.G) * D : nullptr;
+        ri0.tok >= 0 ? v.q + (((long long)kv * v.m + ri0.tok) * p.G + ri0.head % p.G) * D : nullptr;
     const __nv_bfloat16* q1 =
-        ri1.tok >= 0 ? p.q + (((long long)kv * p.rows.m + ri1.tok) * p.G + ri1.head % p.G) * D : nullptr;
+        ri1.tok >= 0 ? v.q + (((long long)kv * v.m + ri1.tok) * p.G + ri1.head % p.G) * D : nullptr;
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
       const int d0 = kk * 16 + 2 * c;
@@ -215,7 +251,7 @@ __global__ void __launch_bounds__((RW + 1) * 32) attn_kernel(const __grid_consta
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int j = key0 + 8 * nt + 2 * c + (e & 1);
-        const bool vis = (e < 2) ? visible(p, ri0, j) : visible(p, ri1, j);
+        const bool vis = (e < 2) ? visible(ri0, j) : visible(ri1, j);
         const float v = vis ? s[nt][e] * p.scale_log2 : -INFINITY;
         s[nt][e] = v;
         mx[e >> 1] = fmaxf(mx[e >> 1], v);
@@ -283,20 +319,20 @@ __global__ void __launch_bounds__((RW + 1) * 32) attn_kernel(const __grid_consta
     const RowInfo& ri = h == 0 ? ri0 : ri1;
     if (ri.tok < 0) continue;
     const long long rowidx = (long long)ri.tok * p.Hq + ri.head;
-    if (p.nsplit == 1) {
+    if (v.nsplit == 1) {
       const float inv = 1.f / lrow[h];
-      __nv_bfloat16* dst = p.o + rowidx * D;
+      __nv_bfloat16* dst = v.o + rowidx * D;
 #pragma unroll
       for (int i = 0; i < D / 8; ++i)
         *reinterpret_cast<uint32_t*>(dst + 8 * i + 2 * c) =
             dev::pack_bf16x2(o[i][2 * h] * inv, o[i][2 * h + 1] * inv);
     } else {
-      const long long plane = (long long)p.rows.m * p.Hq;
-      float* dst = p.opart + ((long long)split * plane + rowidx) * D;
+      const long long plane = (long long)v.m * p.Hq;
+      float* dst = v.opart + ((long long)split * plane + rowidx) * D;
 #pragma unroll
       for (int i = 0; i < D / 8; ++i)
         *reinterpret_cast<float2*>(dst + 8 * i + 2 * c) = make_float2(o[i][2 * h], o[i][2 * h + 1]);
-      if (c == 0) p.ml[split * plane + rowidx] = make_float2(mrow[h], lrow[h]);
+      if (c == 0) v.ml[split * plane + rowidx] = make_float2(mrow[h], lrow[h]);
     }
   }
 }
@@ -309,15 +345,30 @@ template <int D>
 __global__ void __launch_bounds__(256) attn_combine_kernel(const __grid_constant__ AttnParams p) {
   dev::pdl_trigger();
   dev::pdl_wait();
-  const long long rows = (long long)p.rows.m * p.Hq;
-  const long long rowidx = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
-  if (rowidx >= rows) return;
+  const long long grow = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);   // (token, head) of the call
+  if (grow >= (long long)p.rows.m * p.Hq) return;
+  // the row's partials: of the whole call, or of its conversation in a batch
+  long long rows = (long long)p.rows.m * p.Hq, rowidx = grow;
+  int ns = p.nsplit;
+  const float* opart = p.opart;
+  const float2* mlp = p.ml;
+  if (p.n_conv) {
+    const int tok = (int)(grow / p.Hq);
+    int b = 0;
+    while (b + 1 < p.n_conv && tok >= p.conv[b + 1].tok0) ++b;
+    const AttnConv& cv = p.conv[b];
+    ns = cv.nsplit;
+    if (ns == 1) return;   // the attention kernel wrote this row itself
+    rows = (long long)cv.m * p.Hq;
+    rowidx = grow - (long long)cv.tok0 * p.Hq;
+    opart += cv.part0;
+    mlp += cv.part0 / D;
+  }
   const int lane = threadIdx.x & 31;
   constexpr int E = D / 32;
   static_assert(kMaxSplits <= 64, "two split records per lane");
-  const int ns = p.nsplit;
-  const float2 ml0 = lane < ns ? p.ml[lane * rows + rowidx] : make_float2(-INFINITY, 0.f);
-  const float2 ml1 = lane + 32 < ns ? p.ml[(lane + 32) * rows + rowidx] : make_float2(-INFINITY, 0.f);
+  const float2 ml0 = lane < ns ? mlp[lane * rows + rowidx] : make_float2(-INFINITY, 0.f);
+  const float2 ml1 = lane + 32 < ns ? mlp[(lane + 32) * rows + rowidx] : make_float2(-INFINITY, 0.f);
   float M = fmaxf(ml0.x, ml1.x);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
@@ -329,7 +380,7 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const __grid_constant
   float acc[E];
 #pragma unroll
   for (int e = 0; e < E; ++e) acc[e] = 0.f;
-  const float* src = p.opart + rowidx * D + lane * E;
+  const float* src = opart + rowidx * D + lane * E;
   const long long sstride = rows * D;
   if (ns <= 32) {
     // every split's slice in flight at once, then added in split order
@@ -365,7 +416,7 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const __grid_constant
     }
   }
   const float inv = 1.f / den;
-  __nv_bfloat16* dst = p.o + rowidx * D + lane * E;
+  __nv_bfloat16* dst = p.o + grow * D + lane * E;
 #pragma unroll
   for (int e = 0; e < E; e += 2)
     *reinterpret_cast<uint32_t*>(dst + e) = dev::pack_bf16x2(acc[e] * inv, acc[e + 1] * inv);

@@ -272,7 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       const uint32_t qb = dev::smem_u32(&q_full);
       if (is_k) {
         dev::mbar_arrive_expect_tx(qb, C::kQBytes);
-        const int qrow = kv * R + row_lo;
+        const int qrow = p.qrow0 + kv * R + row_lo;
 #pragma unroll
         for (int a = 0; a < D / 64; ++a) dev::tma_load_2d(q_base + a * 16384, &p.tq, 64 * a, qrow, qb);
       }

@@ -43,8 +43,7 @@ __global__ void rope_table_kernel(RowMap rows, int d, double theta, float2* tabl
   const int idx = blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= rows.m * half) return;
   const int i = idx / half, j = idx % half;
-  const int b = row_branch(rows, i);
-  const double pos = (double)(rows.P + i - rows.off[b]);
+  const double pos = (double)row_pos(rows, i);
   const double ang = pos * pow(theta, -2.0 * j / d);
   double sn, cs;
   sincos(ang, &sn, &cs);
@@ -115,7 +114,7 @@ __global__ void __launch_bounds__(256) epi_qkv_kernel(const float* part, long lo
                                                       int ldo, int c0, int mb, RowMap rows, int Hq,
                                                       int Hkv, const float2* rope, __nv_bfloat16* q,
                                                       __nv_bfloat16* arena, long long k_off,
-                                                      long long v_off, int cap) {
+                                                      long long v_off, long long slot_stride, int cap) {
   dev::pdl_trigger();
   dev::pdl_wait();
   constexpr int kHalf = D / 2;
@@ -145,7 +144,6 @@ __global__ void __launch_bounds__(256) epi_qkv_kernel(const float* part, long lo
       x2[4] += b1.x; x2[5] += b1.y; x2[6] += b1.z; x2[7] += b1.w;
     }
   }
-  const int store = rows.P + i;
   if (hd < Hq + Hkv) {
     if (live) {
       const float4* cs4 = reinterpret_cast<const float4*>(rope + (long long)i * kHalf + j0);
@@ -161,9 +159,9 @@ __global__ void __launch_bounds__(256) epi_qkv_kernel(const float* part, long lo
       __nv_bfloat16* dst;
       if (hd < Hq) {
         const int G = Hq / Hkv;
-        dst = q + (((long long)(hd / G) * rows.m + i) * G + hd % G) * D;
+        dst = q + q_row(rows, i, hd / G, hd % G, G, Hq) * D;
       } else {
-        dst = arena + k_off + ((long long)(hd - Hq) * cap + store) * D;
+        dst = arena + k_off + row_slot(rows, i) * slot_stride + ((long long)(hd - Hq) * cap + row_store(rows, i)) * D;
       }
       uint4 lo, hi;
       lo.x = dev::pack_bf16x2(y1[0], y1[1]); lo.y = dev::pack_bf16x2(y1[2], y1[3]);
@@ -182,11 +180,12 @@ __global__ void __launch_bounds__(256) epi_qkv_kernel(const float* part, long lo
     }
     __syncthreads();
     const int ntok = min(kTok, mb - (int)blockIdx.x * kTok);
-    const int store0 = rows.P + c0 + blockIdx.x * kTok;
-    __nv_bfloat16* base = arena + v_off + (long long)(hd - Hq - Hkv) * D * cap + store0;
+    const int t0 = c0 + blockIdx.x * kTok;
+    __nv_bfloat16* base = arena + v_off + (long long)(hd - Hq - Hkv) * D * cap;
     for (int idx = threadIdx.x; idx < D * kTok; idx += 256) {
       const int e = idx / kTok, tt = idx % kTok;
-      if (tt < ntok) base[(long long)e * cap + tt] = vt[tt][e];
+      if (tt < ntok)
+        base[row_slot(rows, t0 + tt) * slot_stride + (long long)e * cap + row_store(rows, t0 + tt)] = vt[tt][e];
     }
   }
 }
@@ -347,16 +346,16 @@ cudaError_t launch_rmsnorm(const float* h, int c0, int mb, int H, const __nv_bfl
 cudaError_t launch_epi_qkv(const float* part, long long plane, int ksplit, int ldo, int c0, int mb,
                            const RowMap& rows, int Hq, int Hkv, int d, const float2* rope,
                            __nv_bfloat16* q, __nv_bfloat16* arena, long long k_off,
-                           long long v_off, int cap, cudaStream_t st) {
+                           long long v_off, long long slot_stride, int cap, cudaStream_t st) {
   const int heads = Hq + 2 * Hkv;
   if (d == 128) {
     const dim3 grid((mb + 15) / 16, heads);
     return launch_k(epi_qkv_kernel<128>, grid, 256, 0, st, part, plane, ksplit, ldo, c0, mb, rows, Hq,
-                    Hkv, rope, q, arena, k_off, v_off, cap);
+                    Hkv, rope, q, arena, k_off, v_off, slot_stride, cap);
   } else if (d == 64) {
     const dim3 grid((mb + 31) / 32, heads);
     return launch_k(epi_qkv_kernel<64>, grid, 256, 0, st, part, plane, ksplit, ldo, c0, mb, rows, Hq,
-                    Hkv, rope, q, arena, k_off, v_off, cap);
+                    Hkv, rope, q, arena, k_off, v_off, slot_stride, cap);
   }
   return cudaErrorInvalidValue;
 }

@@ -106,8 +106,9 @@ __device__ __forceinline__ void epi_qkv(const GemvParams& p, const GemvSeg& seg,
       const float y2 = x2 * cs.x + x1 * cs.y;
       const int hd = hd0 + hh;
       __nv_bfloat16* dst =
-          s == 0 ? p.q + (((long long)(hd / G) * p.rows.m + i) * G + hd % G) * d
-                 : p.arena + p.k_off + ((long long)hd * p.cap + p.rows.P + i) * d;
+          s == 0 ? p.q + q_row(p.rows, i, hd / G, hd % G, G, p.Hq) * d
+                 : p.arena + p.k_off + row_slot(p.rows, i) * p.slot_stride +
+                       ((long long)hd * p.cap + row_store(p.rows, i)) * d;
       dst[j] = __float2bfloat16_rn(y1);
       dst[j + half] = __float2bfloat16_rn(y2);
     }
@@ -116,8 +117,9 @@ __device__ __forceinline__ void epi_qkv(const GemvParams& p, const GemvSeg& seg,
     for (int idx = tid; idx < p.mb * nv; idx += kConsumers) {
       const int t = idx % p.mb, col = idx / p.mb;
       const int hd = hd0 + col / d, e = col % d;
-      p.arena[p.v_off + ((long long)hd * d + e) * p.cap + p.rows.P + p.c0 + t] =
-          __float2bfloat16_rn(ct[t * kTileLd + col]);
+      const int i = p.c0 + t;
+      p.arena[p.v_off + row_slot(p.rows, i) * p.slot_stride + ((long long)hd * d + e) * p.cap +
+              row_store(p.rows, i)] = __float2bfloat16_rn(ct[t * kTileLd + col]);
     }
   }
 }

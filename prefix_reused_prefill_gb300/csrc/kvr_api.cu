@@ -377,6 +377,13 @@ int project_gemm(kvr_ctx* c, cudaStream_t st, const Seg* segs, int nseg, const C
   return KVR_OK;
 }
 
+// element offset of (slot, layer, K or V^T, head 0) in the arena
+long long kv_offset(const kvr_ctx* c, int slot, int layer, int kind) {
+  const kvr_config& k = c->cfg;
+  return ((((long long)slot * k.n_layers + layer) * 2 + kind) * k.n_kv_heads) * (long long)k.capacity *
+         k.head_dim;
+}
+
 // The epilogue the small-m int4 GEMV applies itself (see GemvEpi).
 struct Fused {
   int epi = kGemvEpiResid;
@@ -446,6 +453,7 @@ int project_gemv_int4(kvr_ctx* c, cudaStream_t st, const Seg* segs, int nseg, co
   p.ldout = cfg.hidden;
   p.z = c->z;
   p.F = cfg.ffn;
+  p.slot_stride = kv_offset(c, 1, 0, 0);
   p.best = fz.best;
   for (int c0 = 0; c0 < m; c0 += kGemvMaxCols) {
     const int mb = std::min(kGemvMaxCols, m - c0);
@@ -535,11 +543,6 @@ int project(kvr_ctx* c, cudaStream_t st, const Seg* segs, int nseg, Act act, int
   return KVR_OK;
 }
 
-long long kv_offset(const kvr_ctx* c, int slot, int layer, int kind) {
-  const kvr_config& k = c->cfg;
-  return ((((long long)slot * k.n_layers + layer) * 2 + kind) * k.n_kv_heads) * (long long)k.capacity *
-         k.head_dim;
-}
 
 // row of (slot, layer, K, head 0, position 0) in the [rows][head_dim] view of the arena
 int k_row(const kvr_ctx* c, int slot, int layer) {
@@ -553,15 +556,19 @@ int vt_row(const kvr_ctx* c, int slot, int layer) {
   return (int)((((long long)slot * k.n_layers + layer) * 2 + 1) * k.n_kv_heads * (long long)k.head_dim);
 }
 
-int attention(kvr_ctx* c, cudaStream_t st, int slot, int layer, const RowMap& rows) {
+// Attention of one slot's rows (tokens tok0 .. tok0 + rows.m of the call; a
+// batch runs one of these per conversation).
+int attention(kvr_ctx* c, cudaStream_t st, int slot, int layer, const RowMap& rows, int tok0 = 0) {
   const kvr_config& k = c->cfg;
   AttnParams p;
   memset(&p, 0, sizeof p);
   p.tkv = c->tm_kv;
   p.tvt = c->tm_vt;
   p.tq = c->tm_q;
-  p.q = c->q;
-  p.o = c->o;
+  const long long qd = (long long)tok0 * k.n_q_heads * k.head_dim;
+  p.q = c->q + qd;
+  p.qrow0 = tok0 * k.n_q_heads;
+  p.o = c->o + qd;
   p.opart = c->opart;
   p.ml = c->ml;
   p.rows = rows;
@@ -607,10 +614,93 @@ int attention(kvr_ctx* c, cudaStream_t st, int slot, int layer, const RowMap& ro
   return KVR_OK;
 }
 
+// Split-KV attention of several small conversations of a batch in one launch
+// (and one combine): each CTA serves a row tile of one conversation over its
+// own slot.  Every conversation takes the same split count (one wave of CTAs
+// over all their tiles), at most half its key blocks.
+int attention_batch(kvr_ctx* c, cudaStream_t st, int layer, const RowMap& rows, const int* bs, int nbs) {
+  const kvr_config& k = c->cfg;
+  AttnParams p;
+  memset(&p, 0, sizeof p);
+  p.tkv = c->tm_kv;
+  p.tvt = c->tm_vt;
+  p.tq = c->tm_q;
+  p.q = c->q;
+  p.o = c->o;
+  p.opart = c->opart;
+  p.ml = c->ml;
+  p.rows.m = rows.m;
+  p.Hq = k.n_q_heads;
+  p.Hkv = k.n_kv_heads;
+  p.G = k.n_q_heads / k.n_kv_heads;
+  p.cap = k.capacity;
+  p.scale_log2 = 1.4426950408889634f / sqrtf((float)k.head_dim);
+  p.status = c->status;
+  int rmax = 0;
+  for (int i = 0; i < nbs; ++i) rmax = std::max(rmax, p.G * (rows.off[bs[i] + 1] - rows.off[bs[i]]));
+  const int rw = attn_row_warps(rmax);
+  int tiles = 0;
+  for (int i = 0; i < nbs; ++i) {
+    const int b = bs[i];
+    AttnConv& cv = p.conv[i];
+    cv.kbase = k_row(c, rows.slot[b], layer);
+    cv.vtbase = vt_row(c, rows.slot[b], layer);
+    cv.P = rows.pre[b];
+    cv.m = rows.off[b + 1] - rows.off[b];
+    cv.tok0 = rows.off[b];
+    cv.tile0 = tiles;
+    tiles += (p.G * cv.m + 16 * rw - 1) / (16 * rw);
+  }
+  p.n_conv = nbs;
+  p.row_tiles = tiles;
+  const int ns = std::max(1, (kSplitTargetCtas + k.n_kv_heads * tiles - 1) / (k.n_kv_heads * tiles));
+  for (int i = 0; i < nbs; ++i) {
+    const int nb = (p.conv[i].P + p.conv[i].m + kAttnKeys - 1) / kAttnKeys;
+    p.conv[i].nsplit = std::max(1, std::min(std::min(ns, std::max(1, nb / 2)), kMaxSplits));
+  }
+  // the partials of every split conversation must fit the scratch
+  auto need = [&]() {
+    size_t f = 0;
+    for (int i = 0; i < nbs; ++i)
+      if (p.conv[i].nsplit > 1) f += (size_t)p.conv[i].nsplit * p.conv[i].m * k.n_q_heads * k.head_dim;
+    return f;
+  };
+  while (need() > c->sl.opart_floats) {   // need() > 0: some conversation still splits
+    int big = -1;
+    for (int i = 0; i < nbs; ++i)
+      if (p.conv[i].nsplit > 1 &&
+          (big < 0 || p.conv[i].nsplit * p.conv[i].m > p.conv[big].nsplit * p.conv[big].m))
+        big = i;
+    --p.conv[big].nsplit;
+  }
+  long long at = 0;
+  bool combine = false;
+  for (int i = 0; i < nbs; ++i) {
+    p.conv[i].part0 = at;
+    if (p.conv[i].nsplit > 1) {
+      at += (long long)p.conv[i].nsplit * p.conv[i].m * k.n_q_heads * k.head_dim;
+      combine = true;
+    }
+    p.nsplit = std::max(p.nsplit, p.conv[i].nsplit);
+  }
+  cudaError_t e;
+  {
+    Timed t(c, kAttn, st);
+    e = launch_attention(p, k.head_dim, rw, st);
+  }
+  if (e != cudaSuccess) return cuda_fail(c, e, "attention launch");
+  if (combine) {
+    Timed t(c, kAttn, st);
+    e = launch_attn_combine(p, k.head_dim, st);
+    if (e != cudaSuccess) return cuda_fail(c, e, "attention combine launch");
+  }
+  return KVR_OK;
+}
+
 // The layer stack for the rows of one call.
 // out (bf16 [m][hidden]) may be null; head_gain: RMSNorm the last layer's rows
 // with it into c->a (the output head's input)
-int run_stack(kvr_ctx* c, int slot, const RowMap& rows, const void* hidden,
+int run_stack(kvr_ctx* c, const RowMap& rows, const void* hidden,
               const kvr_layer_weights* w, void* out, cudaStream_t st,
               const __nv_bfloat16* head_gain = nullptr) {
   const kvr_config& k = c->cfg;
@@ -646,7 +736,9 @@ int run_stack(kvr_ctx* c, int slot, const RowMap& rows, const void* hidden,
     // Q, K, V (+ RoPE, append)
     {
       Seg segs[3] = {{W.wq, W.sq, Hq * d}, {W.wk, W.sk, Hkv * d}, {W.wv, W.sv, Hkv * d}};
-      const long long koff = kv_offset(c, slot, l, 0), voff = kv_offset(c, slot, l, 1);
+      // K/V of slot 0 of this layer; each row adds its slot's stride
+      const long long koff = kv_offset(c, 0, l, 0), voff = kv_offset(c, 0, l, 1);
+      const long long sstride = kv_offset(c, 1, 0, 0);
       Fused fz;
       fz.epi = kGemvEpiQKV;
       fz.rows = &rows;
@@ -655,11 +747,32 @@ int run_stack(kvr_ctx* c, int slot, const RowMap& rows, const void* hidden,
       int rc = project(c, st, segs, 3, Act::A, H, m, [&](const float* part, long long plane, int ks,
                                                           int ldo, int c0, int mb) {
         return launch_epi_qkv(part, plane, ks, ldo, c0, mb, rows, Hq, Hkv, d, c->rope, c->q, arena,
-                              koff, voff, k.capacity, st);
+                              koff, voff, sstride, k.capacity, st);
       }, fz);
       if (rc) return rc;
     }
-    int rc = attention(c, st, slot, l, rows);
+    int rc = KVR_OK;
+    if (!rows.batch) {
+      rc = attention(c, st, rows.slot[0], l, rows);
+    } else {
+      // conversations with many rows take the tcgen05 kernel one by one; the
+      // rest share one split-KV launch
+      int small[KVR_MAX_BRANCHES], n_small = 0;
+      for (int b = 0; b < rows.n_branch && !rc; ++b) {
+        RowMap one;
+        memset(&one, 0, sizeof one);
+        one.P = rows.pre[b];
+        one.m = rows.off[b + 1] - rows.off[b];
+        one.n_branch = 1;
+        one.off[1] = one.m;
+        one.slot[0] = rows.slot[b];
+        if ((k.n_q_heads / k.n_kv_heads) * one.m > kAttnTcMinRows && !c->force_gemv)
+          rc = attention(c, st, rows.slot[b], l, one, rows.off[b]);
+        else
+          small[n_small++] = b;
+      }
+      if (!rc && n_small) rc = attention_batch(c, st, l, rows, small, n_small);
+    }
     if (rc) return rc;
     // O projection
     {
@@ -782,7 +895,8 @@ int prefill_common(kvr_ctx* c, int slot, const int32_t* tokens, int m, const voi
   rows.n_branch = 1;
   rows.off[0] = 0;
   rows.off[1] = m;
-  int rc = run_stack(c, slot, rows, hidden, w, out, st, head_gain);
+  rows.slot[0] = slot;
+  int rc = run_stack(c, rows, hidden, w, out, st, head_gain);
   if (rc) return rc;
   rc = upload_tokens(c, slot, p0, tokens, m, st);
   if (rc) return rc;
@@ -1256,6 +1370,7 @@ int kvr_prefill_branches(kvr_ctx* c, int slot, int n_branch, const int* lens, co
   memset(&rows, 0, sizeof rows);
   rows.P = (int)c->slots[slot].tokens.size();
   rows.n_branch = n_branch;
+  rows.slot[0] = slot;
   int total = 0;
   for (int b = 0; b < n_branch; ++b) {
     if (lens[b] <= 0) return fail(c, KVR_ERR_ARG, "branch %d has %d rows", b, lens[b]);
@@ -1268,10 +1383,56 @@ int kvr_prefill_branches(kvr_ctx* c, int slot, int n_branch, const int* lens, co
     return fail(c, KVR_ERR_CAPACITY, "%d branch rows after %d exceed capacity %d (max_rows %d)", total,
                 rows.P, c->cfg.capacity, c->cfg.max_rows);
   if (c->fault == 2) return fail(c, KVR_ERR_FAULT, "injected launch fault");
-  int rc = run_stack(c, slot, rows, hidden, w, out, static_cast<cudaStream_t>(stream));
+  int rc = run_stack(c, rows, hidden, w, out, static_cast<cudaStream_t>(stream));
   if (rc) return rc;
   c->slots[slot].occupied = true;
   touch(c, slot);
+  return KVR_OK;
+}
+
+int kvr_prefill_batch(kvr_ctx* c, int n_seq, const int* slots, const int* lens, const int32_t* tokens,
+                      const void* hidden, const kvr_layer_weights* w, void* out, void* stream) {
+  if (!c) return KVR_ERR_ARG;
+  if (n_seq < 1 || n_seq > KVR_MAX_BRANCHES || !slots || !lens || !tokens || !hidden || !out)
+    return fail(c, KVR_ERR_ARG, "bad batch arguments");
+  if (((uintptr_t)hidden & 15) || ((uintptr_t)out & 15)) return fail(c, KVR_ERR_ARG, "hidden/out must be 16-byte aligned");
+  if (!weights_ok(c, w)) return fail(c, KVR_ERR_ARG, "missing or misaligned weight pointer");
+  RowMap rows;
+  memset(&rows, 0, sizeof rows);
+  rows.batch = 1;
+  rows.n_branch = n_seq;
+  int total = 0;
+  for (int j = 0; j < n_seq; ++j) {
+    const int s = slots[j];
+    if (s < 0 || s >= c->granted) return fail(c, KVR_ERR_ARG, "bad slot %d", s);
+    for (int i = 0; i < j; ++i)
+      if (slots[i] == s) return fail(c, KVR_ERR_ARG, "slot %d appears twice in the batch", s);
+    if (lens[j] <= 0) return fail(c, KVR_ERR_ARG, "conversation %d has %d rows", j, lens[j]);
+    rows.slot[j] = s;
+    rows.pre[j] = (int)c->slots[s].tokens.size();
+    rows.off[j] = total;
+    total += lens[j];
+    if (rows.pre[j] + lens[j] > c->cfg.capacity || c->fault == 3)
+      return fail(c, KVR_ERR_CAPACITY, "slot %d: %d + %d rows exceed capacity %d", s, rows.pre[j], lens[j],
+                  c->cfg.capacity);
+  }
+  rows.off[n_seq] = total;
+  rows.m = total;
+  if (total > c->cfg.max_rows) return fail(c, KVR_ERR_CAPACITY, "%d rows exceed max_rows %d", total, c->cfg.max_rows);
+  if (c->fault == 2) return fail(c, KVR_ERR_FAULT, "injected launch fault");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int rc = run_stack(c, rows, hidden, w, out, st);
+  if (rc) return rc;
+  for (int j = 0; j < n_seq; ++j) {
+    rc = upload_tokens(c, slots[j], rows.pre[j], tokens + rows.off[j], lens[j], st);
+    if (rc) return rc;
+  }
+  for (int j = 0; j < n_seq; ++j) {
+    SlotState& S = c->slots[slots[j]];
+    S.occupied = true;
+    S.tokens.insert(S.tokens.end(), tokens + rows.off[j], tokens + rows.off[j + 1]);
+    touch(c, slots[j]);
+  }
   return KVR_OK;
 }
 

@@ -34,17 +34,53 @@ constexpr int kStatusTimeout = 1;
 // Rows of one call: P committed keys visible to every row; row i of branch b
 // (off[b] <= i < off[b+1]) sits at position P + i - off[b], is stored at slot
 // index P + i, and also sees slot indices [P + off[b], P + i].
+// The m rows of one call, in branches b = rows [off[b], off[b+1]):
+//  * batch == 0 (one slot, slot[0]): keys [0, P) are the shared cached prefix;
+//    row i is stored at P + i and sits at position P + i - off[b]; it sees
+//    the prefix and its own branch's rows up to itself (a plain suffix is the
+//    one-branch case).
+//  * batch == 1 (one conversation per branch): branch b appends to slot[b]
+//    after that slot's pre[b] cached tokens, exactly as a one-branch call on
+//    that slot would (row i at position and index pre[b] + i - off[b]).
 struct RowMap {
   int P;
   int m;
   int n_branch;
+  int batch;
   int off[KVR_MAX_BRANCHES + 1];
+  int pre[KVR_MAX_BRANCHES];
+  int slot[KVR_MAX_BRANCHES];
 };
 
 __host__ __device__ inline int row_branch(const RowMap& r, int i) {
   int b = 0;
   while (b + 1 < r.n_branch && i >= r.off[b + 1]) ++b;
   return b;
+}
+
+// RoPE position of row i
+__host__ __device__ inline int row_pos(const RowMap& r, int i) {
+  const int b = row_branch(r, i);
+  return (r.batch ? r.pre[b] : r.P) + i - r.off[b];
+}
+
+// slot and slot index receiving row i's K/V
+__host__ __device__ inline int row_slot(const RowMap& r, int i) { return r.slot[r.batch ? row_branch(r, i) : 0]; }
+__host__ __device__ inline int row_store(const RowMap& r, int i) {
+  if (!r.batch) return r.P + i;
+  const int b = row_branch(r, i);
+  return r.pre[b] + i - r.off[b];
+}
+
+// q buffer row ([rows][head_dim]) of row i, query head g of KV head kv:
+// KV-head-major [Hkv][m][G] per call, or per conversation in a batch (the
+// block of branch b starts at row off[b] * Hq) so each conversation's
+// attention reads a [Hkv][len][G] block of its own
+__host__ __device__ inline long long q_row(const RowMap& r, int i, int kv, int g, int G, int Hq) {
+  if (!r.batch) return ((long long)kv * r.m + i) * G + g;
+  const int b = row_branch(r, i);
+  const int len = r.off[b + 1] - r.off[b];
+  return (long long)r.off[b] * Hq + ((long long)kv * len + (i - r.off[b])) * G + g;
 }
 
 // ----------------------------------------------------------------------------
@@ -94,7 +130,8 @@ struct GemvParams {
   const float2* rope;   // QKV: (cos, sin) [m][d/2]
   __nv_bfloat16* q;     // QKV: [Hkv][m][G][d]
   __nv_bfloat16* arena; // QKV: the slot arena
-  long long k_off, v_off;
+  long long k_off, v_off;   // QKV: the layer's K and V^T in slot 0
+  long long slot_stride;    // QKV: arena elements per slot
   int cap, Hq, Hkv, d;
   float* h;             // Resid: [max_rows][H]
   int H;
@@ -134,6 +171,16 @@ struct GemmParams {
   int* status;
 };
 
+// One conversation of a batched small-m attention launch.
+struct AttnConv {
+  int kbase, vtbase;   // its slot's K / V^T rows of the layer (as AttnParams)
+  int P, m;            // its cached tokens and new rows
+  int tok0;            // its first row in the call
+  int tile0;           // its first row tile (blockIdx.x)
+  int nsplit;
+  long long part0;     // float offset of its partials [nsplit][m][Hq][d] (ml: part0 / d)
+};
+
 struct AttnParams {
   CUtensorMap tkv;           // arena as bf16 [rows][head_dim], box {64, 64}, 128B swizzle (K tiles)
   CUtensorMap tvt;           // arena as bf16 [rows][capacity], box {64, head_dim} (V^T tiles)
@@ -144,6 +191,7 @@ struct AttnParams {
   float2* ml;                // [nsplit][m][Hq]  (running max in log2 units, sum)
   RowMap rows;
   int Hq, Hkv, G;
+  int qrow0;                 // first q buffer row of this launch (a conversation of a batch)
   int kbase;                 // [rows][d] view row of (slot, layer, K, head 0, position 0)
   int vtbase;                // [rows][cap] view row of (slot, layer, V^T, head 0, element 0)
   int cap;
@@ -151,6 +199,10 @@ struct AttnParams {
   int row_tiles;
   float scale_log2;          // log2(e) / sqrt(d)
   int* status;
+  // batched conversations (split-KV kernel and combine only): n_conv > 0
+  // replaces rows/kbase/vtbase/nsplit/q/o by each CTA's conversation
+  int n_conv;
+  AttnConv conv[KVR_MAX_BRANCHES];
 };
 
 // ----------------------------------------------------------------------------
@@ -205,7 +257,8 @@ cudaError_t launch_rmsnorm(const float* h, int c0, int mb, int H, const __nv_bfl
 cudaError_t launch_epi_qkv(const float* part, long long plane, int ksplit, int ldo, int c0,
                            int mb, const RowMap& rows, int Hq, int Hkv, int d,
                            const float2* rope, __nv_bfloat16* q, __nv_bfloat16* arena,
-                           long long k_off, long long v_off, int cap, cudaStream_t st);
+                           long long k_off, long long v_off, long long slot_stride, int cap,
+                           cudaStream_t st);
 cudaError_t launch_epi_resid(const float* part, long long plane, int ksplit, int ldo, int c0,
                              int mb, int H, float* h, const __nv_bfloat16* gain, float eps,
                              __nv_bfloat16* a_out, __nv_bfloat16* final_out, cudaStream_t st);

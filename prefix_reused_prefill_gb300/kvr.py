@@ -27,7 +27,8 @@ EXPORTED = ["kvr_arena_bytes", "kvr_scratch_bytes", "kvr_ctx_create", "kvr_ctx_i
             "kvr_prefill_branches", "kvr_sync_status", "kvr_profile_enable", "kvr_profile_read",
             "kvr_profile_launches",
             "kvr_last_error", "kvr_slot_match_static", "kvr_trace_set", "kvr_verify_accept",
-            "kvr_config_hash", "kvr_slot_spill_bytes", "kvr_slot_spill", "kvr_slot_restore"]
+            "kvr_config_hash", "kvr_slot_spill_bytes", "kvr_slot_spill", "kvr_slot_restore",
+            "kvr_prefill_batch"]
 
 
 class KvrError(RuntimeError):
@@ -87,6 +88,7 @@ def load_library(path: str = LIB_PATH):
         "kvr_verify_accept": (I, [V, I, i32p, I, V, P(KvrLayerWeights), P(KvrHeadWeights), V, i32p,
                                   P(I), V]),
         "kvr_prefill_branches": (I, [V, I, I, P(I), i32p, V, P(KvrLayerWeights), V, V]),
+        "kvr_prefill_batch": (I, [V, I, P(I), P(I), i32p, V, P(KvrLayerWeights), V, V]),
         "kvr_sync_status": (I, [V, V]),
         "kvr_profile_enable": (I, [V, I]),
         "kvr_profile_read": (I, [V, P(ctypes.c_float), P(I)]),
@@ -286,6 +288,23 @@ class Kvr:
                                                ctypes.byref(hs), _ptr(out), nxt, ctypes.byref(acc),
                                                self._stream(stream)))
         return list(nxt[:m]), acc.value
+
+    def kvr_prefill_batch(self, slots, token_lists, hidden, weights, out=None, stream=None):
+        """Conversation j's rows token_lists[j] (hidden rows concatenated in the
+        same order) appended to slot slots[j]; returns the rows' outputs."""
+        arr = weights[0] if isinstance(weights, tuple) else weights
+        lens = [len(t) for t in token_lists]
+        m = sum(lens)
+        assert hidden.dtype == torch.bfloat16 and hidden.is_cuda and hidden.is_contiguous()
+        assert hidden.shape == (m, self.cfg.hidden)
+        if out is None:
+            out = torch.empty((m, self.cfg.hidden), dtype=torch.bfloat16, device=self.device)
+        n = len(slots)
+        slots_c = (ctypes.c_int * max(n, 1))(*[int(s) for s in slots])
+        lens_c = (ctypes.c_int * max(n, 1))(*lens)
+        self._check(self.lib.kvr_prefill_batch(self.ctx, n, slots_c, lens_c, _i32(sum(token_lists, [])),
+                                               hidden.data_ptr(), arr, out.data_ptr(), self._stream(stream)))
+        return out
 
     def kvr_slot_spill(self, slot: int, model_tag: int = 0, stream=None, sync: bool = True) -> torch.Tensor:
         """The slot's record in pinned host memory (uint8); complete once the
