@@ -8,9 +8,21 @@ int4 group-32 (the layout statement of ``include/kvr.h``):
     significant bits; the field holds code + 8, code in [-8, 7].  The weight is
     code * scale[n][g], scale an fp16 number.
 
-This module decodes that statement element by element, independently of the
-packer in ``workloads``.  Pinned by: decode(pack(q)) == q for random q, and a
-hand-written byte fixture (tests/golden/int4_fixture.txt).
+K-quant 4-bit superblocks (KVR_WEIGHTS_Q4K; Tempo9 docs, "Models and
+quantizations": Q4_K keeps 256 weights in 144 bytes, a superblock scale plus
+per-sub-block scales and mins):
+    the codes use the int4 nibble layout above, but a field holds q in [0, 15]
+    with no offset; per row n and superblock s (inputs 256s .. 256s+255) a
+    16-byte record at byte 16s of row n holds fp16 d (bytes 0-1), fp16 dmin
+    (bytes 2-3) and a little-endian 96-bit string (bytes 4-15) of sixteen
+    6-bit fields, field f at bits 6f: fields 0-7 the sub-block scales sc_j,
+    fields 8-15 the mins mn_j, sub-block j = inputs 256s + 32j .. +31.  The
+    weight is d*sc_j*q - dmin*mn_j.  128 + 16 = 144 bytes per 256 weights; the
+    pages give that size only, so the layout inside is this library's.
+
+This module decodes both statements element by element, independently of the
+packers in ``workloads``.  Pinned by: decode(pack(q)) == q for random q, and
+hand-written byte fixtures (tests/golden/int4_fixture.txt, q4k_fixture.txt).
 """
 from __future__ import annotations
 
@@ -48,3 +60,32 @@ def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
     """uint16 bf16 bit patterns -> float64 values (bf16 is the top half of fp32)."""
     bits = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)
     return bits.view(np.float32).astype(np.float64)
+
+
+SUPER = 256
+
+
+def q4k_record_fields(meta: np.ndarray):
+    """uint8 [N][K/256*16] records -> (d, dmin) float64 [N][S] and (sc, mn) int64 [N][S][8]."""
+    meta = np.asarray(meta, dtype=np.uint8)
+    N = meta.shape[0]
+    rec = meta.reshape(N, -1, 16)
+    d = rec[..., 0:2].copy().view(np.float16)[..., 0].astype(np.float64)
+    dmin = rec[..., 2:4].copy().view(np.float16)[..., 0].astype(np.float64)
+    # the 96-bit string as an integer per record (byte b has weight 256**b)
+    bits = [[int.from_bytes(bytes(rec[n, s, 4:16]), "little") for s in range(rec.shape[1])] for n in range(N)]
+    fields = np.array([[[(x >> (6 * f)) & 63 for f in range(16)] for x in row] for row in bits],
+                      dtype=np.int64).reshape(N, rec.shape[1], 16)
+    return d, dmin, fields[..., :8], fields[..., 8:]
+
+
+def dequant_q4k(packed: np.ndarray, meta: np.ndarray) -> np.ndarray:
+    """Dequantised weight d*sc*q - dmin*mn, float64 [N][K] (exact: every term
+    is a short product of fp16 numbers and small integers)."""
+    packed = np.asarray(packed, dtype=np.uint8)
+    N, K = packed.shape[0], packed.shape[1] * 2
+    assert K % SUPER == 0
+    q = (int4_codes(packed, K) + 8).astype(np.float64).reshape(N, K // SUPER, 8, GROUP)
+    d, dmin, sc, mn = q4k_record_fields(meta)
+    w = (d[:, :, None, None] * sc[:, :, :, None] * q) - (dmin[:, :, None, None] * mn[:, :, :, None])
+    return w.reshape(N, K)

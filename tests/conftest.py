@@ -37,6 +37,8 @@ def oracle_weights(shape, lw):
     for name, v in lw.items():
         if isinstance(v, workloads.Int4Matrix):
             W[name] = formats.dequant_int4(v.packed.cpu().numpy(), v.scales.cpu().numpy())
+        elif isinstance(v, workloads.Q4KMatrix):
+            W[name] = formats.dequant_q4k(v.packed.cpu().numpy(), v.scales.cpu().numpy())
         else:
             W[name] = v.detach().cpu().to(torch.float64).numpy()
     return W

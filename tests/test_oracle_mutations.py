@@ -103,6 +103,11 @@ MUTATIONS = [
     (numerics, "silu", "1.0 + np.exp(-x)", "1.0 + np.exp(x)"),
     (formats, "int4_codes", ".astype(np.int64) - 8", ".astype(np.int64)"),     # missing offset
     (formats, "int4_codes", "field = kk // 8 + 4 * (kk % 2)", "field = kk % 8"),  # nibble order
+    (formats, "q4k_record_fields", "(x >> (6 * f)) & 63", "(x >> (6 * f)) & 31"),  # field width
+    (formats, "q4k_record_fields", "fields[..., :8], fields[..., 8:]", "fields[..., 8:], fields[..., :8]"),
+    (formats, "q4k_record_fields", "d = rec[..., 0:2]", "d = rec[..., 2:4]"),  # d from dmin's bytes
+    (formats, "dequant_q4k", "- (dmin[:, :, None, None]", "+ (dmin[:, :, None, None]"),  # min sign
+    (formats, "dequant_q4k", "int4_codes(packed, K) + 8", "int4_codes(packed, K)"),  # signed codes
     # slot policy
     (slots.SlotTable, "choose", "ok = l[best] > self.lcp_with_others(best)",
      "ok = l[best] >= self.lcp_with_others(best)"),                            # threshold

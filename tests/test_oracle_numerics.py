@@ -83,3 +83,78 @@ def test_bf16_bits_decode():
     bits = np.array([0x3F80, 0xC000, 0x0000, 0x3EAA], dtype=np.uint16)
     np.testing.assert_array_equal(formats.bf16_bits_to_f64(bits)[:3], [1.0, -2.0, 0.0])
     assert abs(formats.bf16_bits_to_f64(bits)[3] - 0.33203125) == 0
+
+
+# ---------------------------------------------------------------- K-quant superblocks
+
+def _q4k_fixture():
+    fx = read_fixture("q4k_fixture.txt")
+    group = [int(b, 16) for b in fx["group"]]
+    packed = np.array(group * 8, dtype=np.uint8)[None, :]
+    record = np.array([int(b, 16) for b in fx["record"]], dtype=np.uint8)[None, :]
+    return fx, packed, record
+
+
+def test_q4k_fixture_decodes():
+    fx, packed, record = _q4k_fixture()
+    d, dmin, sc, mn = formats.q4k_record_fields(record)
+    assert d[0, 0] == float(fx["d"][0]) and dmin[0, 0] == float(fx["dmin"][0])
+    np.testing.assert_array_equal(sc[0, 0], [int(v) for v in fx["sc"]])
+    np.testing.assert_array_equal(mn[0, 0], [int(v) for v in fx["mn"]])
+    w = formats.dequant_q4k(packed, record)[0]
+    for kv in fx["worked"]:
+        k, v = kv.split(":")
+        assert w[int(k)] == float(v), k
+
+
+def test_q4k_packer_matches_fixture():
+    fx, packed, record = _q4k_fixture()
+    d = torch.tensor([[float(fx["d"][0])]], dtype=torch.float16)
+    dmin = torch.tensor([[float(fx["dmin"][0])]], dtype=torch.float16)
+    sc = torch.tensor([[[int(v) for v in fx["sc"]]]])
+    mn = torch.tensor([[[int(v) for v in fx["mn"]]]])
+    np.testing.assert_array_equal(workloads.pack_q4k_records(d, dmin, sc, mn).numpy(), record)
+    q = torch.tensor([[k % 16 for k in range(256)]], dtype=torch.int16)
+    np.testing.assert_array_equal(workloads.pack_int4((q - 8).to(torch.int8)).numpy(), packed)
+
+
+def test_q4k_with_unit_scales_and_mins_of_eight_is_int4(rng):
+    # sc = 1, mn = 8, d = dmin = s gives s*q - 8s = s*(q - 8): the int4 decode of
+    # the same code bytes with scale s on every group of the superblock
+    N, S = 5, 2
+    packed = rng.integers(0, 256, size=(N, S * 128), dtype=np.uint8)
+    s = rng.uniform(0.01, 0.1, size=(N, S)).astype(np.float16)
+    bits = sum(1 << (6 * f) for f in range(8)) + sum(8 << (6 * f) for f in range(8, 16))
+    tail = np.frombuffer(bits.to_bytes(12, "little"), dtype=np.uint8)
+    record = np.zeros((N, S, 16), dtype=np.uint8)
+    record[..., 0:2] = s.view(np.uint8).reshape(N, S, 2)
+    record[..., 2:4] = s.view(np.uint8).reshape(N, S, 2)
+    record[..., 4:] = tail
+    got = formats.dequant_q4k(packed, record.reshape(N, S * 16))
+    want = formats.dequant_int4(packed, np.repeat(s, 8, axis=1))
+    np.testing.assert_array_equal(got, want)
+
+
+def test_q4k_single_field_lands_on_its_sub_block():
+    # one non-zero 6-bit field f: a scale (f < 8) scales sub-block f, a min
+    # (f >= 8) offsets sub-block f - 8; every other sub-block decodes to 0
+    packed = np.full((1, 128), 0x11, dtype=np.uint8)          # q = 1 everywhere
+    for f in range(16):
+        record = np.zeros((1, 16), dtype=np.uint8)
+        record[0, 0:2] = np.array([1.0], dtype=np.float16).view(np.uint8)
+        record[0, 2:4] = np.array([1.0], dtype=np.float16).view(np.uint8)
+        record[0, 4:] = np.frombuffer((37 << (6 * f)).to_bytes(12, "little"), dtype=np.uint8)
+        w = formats.dequant_q4k(packed, record)[0].reshape(8, 32)
+        want = np.zeros((8, 32))
+        want[f % 8] = 37.0 if f < 8 else -37.0
+        np.testing.assert_array_equal(w, want, err_msg=f"field {f}")
+
+
+def test_q4k_quantizer_error_bound(rng):
+    w = torch.from_numpy(rng.standard_normal((16, 512)).astype(np.float32) * 0.02)
+    m = workloads.make_q4k(w)
+    deq = formats.dequant_q4k(m.packed.numpy(), m.scales.numpy())
+    d, dmin, sc, mn = formats.q4k_record_fields(m.scales.numpy())
+    step = (d[:, :, None] * sc).repeat(32, axis=-1).reshape(16, 512)
+    assert np.all(np.abs(w.numpy() - deq) <= step / 2 * (1 + 1e-6) + 1e-12)
+    assert sc.max() <= 63 and mn.max() <= 63 and sc.min() >= 1

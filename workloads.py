@@ -85,6 +85,9 @@ SHAPES: Dict[str, ModelShape] = {
     "small_d128": ModelShape("small_d128", 768, 6, 2, 128, 768, 2, "int4"),
     "small_attn": ModelShape("small_attn", 512, 8, 2, 64, 0, 1, "int4", attn_only=True),
     "small_bf16": ModelShape("small_bf16", 256, 4, 2, 64, 512, 2, "bf16"),
+    "small_q4k": ModelShape("small_q4k", 512, 8, 2, 64, 1024, 2, "q4k"),
+    # the verify shape with K-quant superblock weights
+    "dense9b_q4k": ModelShape("dense9b_q4k", 4096, 32, 8, 128, 12288, 36, "q4k"),
 }
 
 
@@ -177,6 +180,74 @@ def make_int4(w: torch.Tensor, keep_codes: bool = False) -> Int4Matrix:
 
 
 # ----------------------------------------------------------------------------
+# K-quant 4-bit superblocks (256 inputs: fp16 d and dmin, 6-bit scale and min
+# per 32-input sub-block, unsigned 4-bit codes)
+# ----------------------------------------------------------------------------
+
+SUPER = 256
+
+
+def _fp16_up(x: torch.Tensor) -> torch.Tensor:
+    """Smallest fp16 value >= x (x >= 0), as float32."""
+    h = x.to(torch.float16)
+    low = h.to(torch.float32) < x
+    h = torch.where(low, torch.nextafter(h, torch.full_like(h, float("inf"))), h)
+    return h.to(torch.float32)
+
+
+def quantize_q4k(w: torch.Tensor) -> tuple:
+    """w float32 [N][K] -> (q uint [N][K] in [0, 15] as int8, d, dmin fp16 [N][K/256],
+    sc, mn int [N][K/256][8] in [0, 63]).
+
+    Per sub-block j: mn_j*dmin >= -min(w, 0) (every weight offset into [0, ...)),
+    sc_j*d*15 >= the offset range, so rne((w + dmin*mn_j) / (d*sc_j)) lies in
+    [0, 15] and the error is at most d*sc_j/2."""
+    N, K = w.shape
+    assert K % SUPER == 0
+    g = w.reshape(N, K // SUPER, 8, GROUP).to(torch.float32)
+    lo = torch.clamp(g.amin(dim=-1), max=0.0)
+    hi = g.amax(dim=-1)
+    dmin = _fp16_up(torch.clamp((-lo).amax(dim=-1) / 63.0, min=2.0 ** -24))
+    mn = torch.clamp(torch.ceil(-lo / dmin.unsqueeze(-1)), 0, 63)
+    off = mn * dmin.unsqueeze(-1)                          # exact: fp16 * small integer
+    span = torch.clamp(hi + off, min=0.0) / 15.0
+    d = _fp16_up(torch.clamp(span.amax(dim=-1) / 63.0, min=2.0 ** -24))
+    sc = torch.clamp(torch.ceil(span / d.unsqueeze(-1)), 1, 63)
+    step = (sc * d.unsqueeze(-1)).unsqueeze(-1)
+    q = torch.round((g + off.unsqueeze(-1)) / step).clamp_(0, 15)
+    return (q.to(torch.int8).reshape(N, K), d.to(torch.float16), dmin.to(torch.float16),
+            sc.to(torch.int64), mn.to(torch.int64))
+
+
+def pack_q4k_records(d: torch.Tensor, dmin: torch.Tensor, sc: torch.Tensor, mn: torch.Tensor) -> torch.Tensor:
+    """uint8 [N][S*16]: per superblock fp16 d, fp16 dmin, then sixteen 6-bit
+    fields (sc_0..7, mn_0..7), field f at bits 6f of a little-endian 96-bit string."""
+    N, S = d.shape
+    rec = torch.zeros((N, S, 16), dtype=torch.uint8, device=d.device)
+    rec[..., 0:2] = d.contiguous().view(torch.uint8).reshape(N, S, 2)
+    rec[..., 2:4] = dmin.contiguous().view(torch.uint8).reshape(N, S, 2)
+    fields = torch.cat([sc, mn], dim=-1).to(torch.int64)  # [N, S, 16]
+    # four fields per 24 bits -> 3 bytes
+    f = fields.reshape(N, S, 4, 4)
+    word = f[..., 0] | (f[..., 1] << 6) | (f[..., 2] << 12) | (f[..., 3] << 18)
+    for b in range(3):
+        rec[..., 4 + b::3][..., :4] = ((word >> (8 * b)) & 0xFF).to(torch.uint8)
+    return rec.reshape(N, S * 16).contiguous()
+
+
+@dataclasses.dataclass
+class Q4KMatrix:
+    packed: torch.Tensor   # uint8 [N][K/2]: the int4 nibble layout holding q in [0, 15]
+    scales: torch.Tensor   # uint8 [N][K/256*16]: the superblock records
+
+
+def make_q4k(w: torch.Tensor) -> Q4KMatrix:
+    q, d, dmin, sc, mn = quantize_q4k(w)
+    # pack_int4 stores code + 8: hand it q - 8
+    return Q4KMatrix(pack_int4(q.to(torch.int16).sub(8).to(torch.int8)), pack_q4k_records(d, dmin, sc, mn))
+
+
+# ----------------------------------------------------------------------------
 # layer weights
 # ----------------------------------------------------------------------------
 
@@ -201,6 +272,8 @@ def layer_weights(shape: ModelShape, seed: int, layer: int, device="cpu",
             w = torch.randn((n, k), generator=g, device=device, dtype=torch.float32) * std
         if shape.weight_format == "bf16":
             out[name] = w.to(torch.bfloat16).contiguous()
+        elif shape.weight_format == "q4k":
+            out[name] = make_q4k(w)
         else:
             out[name] = make_int4(w, keep_codes=keep_codes)
         del w
@@ -241,6 +314,8 @@ def weights_to(ws: List[Dict[str, object]], device) -> List[Dict[str, object]]:
             if isinstance(v, Int4Matrix):
                 d[k] = Int4Matrix(v.packed.to(device), v.scales.to(device),
                                   None if v.codes is None else v.codes.to(device))
+            elif isinstance(v, Q4KMatrix):
+                d[k] = Q4KMatrix(v.packed.to(device), v.scales.to(device))
             else:
                 d[k] = v.to(device)
         out.append(d)
