@@ -147,10 +147,13 @@ class ClockSampler:
 # the GPU arm
 # ---------------------------------------------------------------------------
 
-def build_turn9(device, steps_total, layers=None):
+FORMAT_LABEL = {"int4": "int4-g32", "q4k": "K-quant 4-bit superblocks"}
+
+
+def build_turn9(device, steps_total, layers=None, fmt="int4"):
     import dataclasses
     from prefix_reused_prefill_gb300 import Kvr, config_for_shape
-    shape = workloads.SHAPES["qwen7b"]
+    shape = workloads.SHAPES["qwen7b" if fmt == "int4" else "qwen7b_q4k"]
     if layers:
         shape = dataclasses.replace(shape, n_layers=layers)
     seed = workloads.config_seed(2)
@@ -184,7 +187,7 @@ def run_gpu(args, rank, world):
     device = torch.device("cuda", torch.cuda.current_device())
     pk, pk_kind = peaks()
     total = args.warmup + args.steps
-    shape, kv, w, prompts, xs_host, setup_s = build_turn9(device, 3 * total + 2, args.layers)
+    shape, kv, w, prompts, xs_host, setup_s = build_turn9(device, 3 * total + 2, args.layers, args.format)
     xs_dev = [x.to(device) for x in xs_host[:2 * total]]
     out = torch.empty((M_ROWS, shape.hidden), dtype=torch.bfloat16, device=device)
     stream = torch.cuda.current_stream()
@@ -277,10 +280,10 @@ def run_gpu(args, rank, world):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": "turn-9 suffix prefill: Qwen2.5-7B-shaped 28-layer int4-g32 stack, "
-                               "1922-token prompt, 1668 cached, 254 suffix rows, 4 slots x 16384",
+        "config": {"workload": f"turn-9 suffix prefill: Qwen2.5-7B-shaped 28-layer {FORMAT_LABEL[args.format]} "
+                               "stack, 1922-token prompt, 1668 cached, 254 suffix rows, 4 slots x 16384",
                    "global_batch": M_ROWS * world, "seq_len": PROMPT, "parallelism": f"replicas{world}",
-                   "l2": "inputs larger than L2: 3.67 GB of int4 weights streamed per step"},
+                   "l2": "inputs larger than L2: 3.67 GB of 4-bit weights streamed per step"},
         "attended_kv_gbs": round(attn_gbs, 1),
         "attended_kv_frac_hbm": round(attn_gbs / pk["hbm_gbs"], 4),
         "attention_causal_tflops": round(attn_flops / (attn_ms / 1e3) / 1e12, 1),
@@ -288,7 +291,8 @@ def run_gpu(args, rank, world):
         "roofline": {"bound": "tensor", "achieved": round(achieved_tf, 2),
                      "peak": peak_tf, "unit": "TFLOP/s",
                      "frac": round(achieved_tf / peak_tf, 4),
-                     "traffic": None if args.layers else round(PROJ_TRAFFIC_PER_LAYER * L),
+                     # DRAM bytes from an ncu capture of the int4 kernels
+                     "traffic": None if args.layers or args.format != "int4" else round(PROJ_TRAFFIC_PER_LAYER * L),
                      "traffic_per": "step (the class's 112 launches)",
                      "peak_kind": f"bf16 sustained ({pk_kind})",
                      "kernel": "projections (gemv_int4 / gemm_int4)",
@@ -353,7 +357,7 @@ def run_verify(args):
     from prefix_reused_prefill_gb300 import Kvr, config_for_shape
     device = torch.device("cuda", torch.cuda.current_device())
     pk, pk_kind = peaks()
-    shape = workloads.SHAPES["dense9b"]
+    shape = workloads.SHAPES["dense9b" if args.format == "int4" else "dense9b_q4k"]
     seed = workloads.config_seed(3)
     tk = workloads.verify_tokens(seed)
     P = len(tk["state"])
@@ -402,7 +406,7 @@ def run_verify(args):
     b, a = np.polyfit(ms_, ts, 1)
     kv.close()
     return {"metric": "verify ms per call", "workload": "speculative verify: 36 x (H 4096, 32/8 heads, F 12288) "
-            "int4-g32, 4096 cached tokens, m = k+1 rows", "unit": "ms", "higher_is_better": False,
+            f"{FORMAT_LABEL[args.format]}, 4096 cached tokens, m = k+1 rows", "unit": "ms", "higher_is_better": False,
             "fit_ms": {"a": round(float(a), 4), "b_per_row": round(float(b), 4)},
             "accept": {"vocab": workloads.VOCAB, "what": "accept_ms: kvr_verify_accept (verify + final "
                        "RMSNorm + int4 LM head + argmax + acceptance, read back to the host)"},
@@ -670,6 +674,8 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--workload", default="turn9", choices=["turn9", "verify", "priming", "crossover", "batch"],
                     help="turn9 is the bench line; the others print their own measurement line")
+    ap.add_argument("--format", default="int4", choices=["int4", "q4k"],
+                    help="weight format of the turn9 and verify workloads")
     ap.add_argument("--layers", type=int, default=0,
                     help="profiling aid: run a reduced stack of this many layers")
     args = ap.parse_args()

@@ -61,6 +61,7 @@ extern "C" {
 
 #define KVR_WEIGHTS_BF16 0
 #define KVR_WEIGHTS_INT4_G32 1
+#define KVR_WEIGHTS_Q4K 2
 
 #define KVR_MAX_SLOTS 16
 #define KVR_MAX_BRANCHES 16
@@ -75,7 +76,8 @@ extern "C" {
  *                  decoder shape.  head_dim is 64 or 128; n_q_heads is a
  *                  multiple of n_kv_heads (grouped-query attention: query head
  *                  h reads KV head h / (n_q_heads / n_kv_heads)).
- *   weight_format  KVR_WEIGHTS_BF16 or KVR_WEIGHTS_INT4_G32 (layouts below).
+ *   weight_format  KVR_WEIGHTS_BF16, KVR_WEIGHTS_INT4_G32 or KVR_WEIGHTS_Q4K
+ *                  (layouts below).
  *                  For int4 every projection's input width K must be a
  *                  multiple of 256.
  *   attn_only      1: a layer is out = Attn(x) Wo^T (no norms, no FFN, no
@@ -127,6 +129,19 @@ typedef struct kvr_config {
  *   s* are fp16 [N][K/32] row-major; weight(n, k) = code(n, k) * s[n][k/32].
  *   (The field order lets one 32-bit shared-memory load give a tensor-core
  *   fragment its eight inputs of one group.)
+ * KVR_WEIGHTS_Q4K (K-quant 4-bit superblocks; Tempo9 docs, "Models and
+ * quantizations": Q4_K keeps 256 weights in 144 bytes; the byte layout
+ * inside is this library's, the pages give only the size):
+ *   w* hold codes q in [0, 15] in the int4 layout above (a field holds q,
+ *   no offset).  s* are uint8 [N][K/256][16]: for row n and superblock s
+ *   (inputs 256s .. 256s+255) fp16 d (bytes 0-1), fp16 dmin (bytes 2-3) and
+ *   a little-endian 96-bit string (bytes 4-15) of sixteen 6-bit fields,
+ *   field f at bits 6f: fields 0-7 the scales sc_j, fields 8-15 the mins mn_j
+ *   of sub-block j (inputs 256s + 32j .. +31).
+ *   weight(n, k) = d*sc_j*q - dmin*mn_j.  The small-m GEMV applies d*sc_j
+ *   and dmin*mn_j to fp32 sums; the tcgen05 GEMM rounds each weight to the
+ *   nearest bf16 once.
+ *   Every projection input width must be a multiple of 256 (as for int4).
  * norm_attn, norm_ffn: bf16 [H] RMSNorm gains (unused when attn_only).
  * Every pointer must be 16-byte aligned.
  */

@@ -134,6 +134,25 @@ __device__ __forceinline__ void codes_of_word(uint32_t w, __nv_bfloat162 out[4])
   }
 }
 
+// K-quant: 8 unsigned 4-bit codes of one word -> 4 bf16x2 weights
+// bf16(d*sc*q - dmin*mn) (pair i: fields i and i+4, as codes_of_word), with
+// a = d*sc and b = dmin*mn in fp32 (q*a - b is formed exactly and rounded once)
+__device__ __forceinline__ void q4k_weights_of_word(uint32_t w, float a, float b, uint32_t out[4]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t v = (w >> (4 * i)) & 0x000F000Fu;
+    const float ql = (float)(v & 0xFFFFu), qh = (float)(v >> 16);
+    out[i] = dev::pack_bf16x2(fmaf(ql, a, -b), fmaf(qh, a, -b));
+  }
+}
+
+__device__ __forceinline__ uint32_t q4k_field6(const uint4& r, int f) {
+  const int p = 6 * f, word = p >> 5, off = p & 31;
+  const uint32_t lo = word == 0 ? r.y : (word == 1 ? r.z : r.w);
+  const uint32_t hi = word == 0 ? r.z : r.w;
+  return (off > 26 && word < 2 ? __funnelshift_r(lo, hi, off) : lo >> off) & 63u;
+}
+
 __global__ void __launch_bounds__(kThreads, 1) gemm_int4_tc_kernel(const __grid_constant__ GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t raw_full[kRawStages], raw_empty[kRawStages];
@@ -304,12 +323,21 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_int4_tc_kernel(const __grid_
     const bool srow_ok = srow < sseg.N;
     const int G = p.K / 32;
     const uint32_t* sptr = reinterpret_cast<const uint32_t*>(sseg.scales + (long long)(srow_ok ? srow : 0) * G);
+    // K-quant: the row's 16-byte superblock records (same row stride, K/32 halves)
+    const uint4* rptr = reinterpret_cast<const uint4*>(sptr);
     const uint32_t tlane = (uint32_t)(32 * q) << 16;
     bool ok = true;
     for (int i = grp; i < nkc; i += kConvGroups) {
       const int rs = i % kRawStages, as = i % kAStages;
-      // scales of groups 4*(kc0+i) + 2*hq and +1 (one aligned 32-bit load)
-      const uint32_t scw = srow_ok ? __ldg(sptr + 2 * (kc0 + i) + hq) : 0u;
+      // scales of groups 4*(kc0+i) + 2*hq and +1 (one aligned 32-bit load), or
+      // the K-quant record of superblock (kc0+i)/2 (sub-blocks 4*((kc0+i)&1) + 2*hq, +1)
+      uint32_t scw = 0u;
+      uint4 rec = make_uint4(0u, 0u, 0u, 0u);
+      if (p.fmt == kFmtQ4K) {
+        if (srow_ok) rec = __ldg(rptr + (kc0 + i) / 2);
+      } else {
+        scw = srow_ok ? __ldg(sptr + 2 * (kc0 + i) + hq) : 0u;
+      }
       ok = dev::mbar_wait(dev::smem_u32(&raw_full[rs]), (i / kRawStages) & 1, p.status) && !*abort_v;
       if (ok && i >= kAStages)
         ok = dev::mbar_wait(dev::smem_u32(&a_empty[as]), ((i / kAStages) - 1) & 1, p.status) && !*abort_v;
@@ -322,6 +350,28 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_int4_tc_kernel(const __grid_
       const uint4 w0 = dev::lds128(rb + (((uint32_t)(2 * hq) ^ sw) << 4));
       const uint4 w1 = dev::lds128(rb + (((uint32_t)(2 * hq + 1) ^ sw) << 4));
       uint32_t outv[32];   // 64 bf16 inputs of this row, k order, two per column
+      if (p.fmt == kFmtQ4K) {
+        const float d = __half2float(__ushort_as_half((unsigned short)(rec.x & 0xFFFFu)));
+        const float dmin = __half2float(__ushort_as_half((unsigned short)(rec.x >> 16)));
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const uint4 wv = h ? w1 : w0;
+          const int j = 4 * ((kc0 + i) & 1) + 2 * hq + h;   // sub-block of the superblock
+          const float a = d * (float)q4k_field6(rec, j), b = dmin * (float)q4k_field6(rec, 8 + j);
+          uint32_t c0[4], c1[4], c2[4], c3[4];
+          q4k_weights_of_word(wv.x, a, b, c0);
+          q4k_weights_of_word(wv.y, a, b, c1);
+          q4k_weights_of_word(wv.z, a, b, c2);
+          q4k_weights_of_word(wv.w, a, b, c3);
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) {
+            outv[16 * h + 4 * jj + 0] = c0[jj];
+            outv[16 * h + 4 * jj + 1] = c1[jj];
+            outv[16 * h + 4 * jj + 2] = c2[jj];
+            outv[16 * h + 4 * jj + 3] = c3[jj];
+          }
+        }
+      } else {
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const uint4 wv = h ? w1 : w0;
@@ -343,6 +393,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_int4_tc_kernel(const __grid_
           outv[16 * h + 4 * jj + 2] = *reinterpret_cast<uint32_t*>(&v2);
           outv[16 * h + 4 * jj + 3] = *reinterpret_cast<uint32_t*>(&v3);
         }
+      }
       }
       tmem_st32(tmem + tlane + kACol + 64u * (uint32_t)as + 32u * (uint32_t)hq, outv);
       asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");

@@ -64,11 +64,13 @@ struct GemvCfg {
   static_assert(kXRows * kTileLd * 4 <= kStageBytes, "result tile must fit in one stage");
 };
 
-// 8 int4 codes of one 32-bit word -> 4 bf16x2 registers holding code values.
+// 8 4-bit fields of one 32-bit word -> 4 bf16x2 registers holding field - OFF
+// (OFF = 8: the signed int4 code; 0: the unsigned K-quant code).
 // Register i holds fields i (low half) and i+4 (high half).
+template <int OFF>
 __device__ __forceinline__ void dequant_word(uint32_t w, uint32_t r[4]) {
   const uint32_t magic = 0x43004300u;  // bf16 128.0 in both halves
-  const __nv_bfloat162 bias = __floats2bfloat162_rn(136.0f, 136.0f);
+  const __nv_bfloat162 bias = __floats2bfloat162_rn(128.0f + OFF, 128.0f + OFF);
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     uint32_t v;
@@ -78,6 +80,21 @@ __device__ __forceinline__ void dequant_word(uint32_t w, uint32_t r[4]) {
     h = __hsub2(h, bias);
     r[i] = *reinterpret_cast<uint32_t*>(&h);
   }
+}
+
+// K-quant record (16 bytes: fp16 d, fp16 dmin, sixteen 6-bit fields at bits 6f
+// of the little-endian 96-bit string in words y, z, w): (d*sc_g, dmin*mn_g)
+__device__ __forceinline__ uint32_t q4k_field(const uint4& r, int f) {
+  const int p = 6 * f, word = p >> 5, off = p & 31;
+  const uint32_t lo = word == 0 ? r.y : (word == 1 ? r.z : r.w);
+  const uint32_t hi = word == 0 ? r.z : r.w;
+  return (off > 26 && word < 2 ? __funnelshift_r(lo, hi, off) : lo >> off) & 63u;
+}
+
+__device__ __forceinline__ float2 q4k_ab(const uint4& r, int g) {
+  const float d = __half2float(__ushort_as_half((unsigned short)(r.x & 0xFFFFu)));
+  const float dmin = __half2float(__ushort_as_half((unsigned short)(r.x >> 16)));
+  return make_float2(d * (float)q4k_field(r, g), dmin * (float)q4k_field(r, 8 + g));
 }
 
 // barrier of the eight consumer warps (the producer warp has left)
@@ -199,7 +216,7 @@ __device__ __forceinline__ void epi_argmax(const GemvParams& p, const GemvSeg& s
 }
 
 // two CTAs per SM for up to 16 tokens (the host sizes the grid for it)
-template <int NT, int EPI>
+template <int NT, int EPI, int FMT>
 __global__ void __launch_bounds__(kThreads, NT == 4 ? 1 : 2) gemv_int4_kernel(const __grid_constant__ GemvParams p) {
   using C = GemvCfg<NT>;
   constexpr bool kPair = EPI == kGemvEpiSwiglu;   // tile = 64 gate rows + 64 up rows
@@ -209,6 +226,8 @@ __global__ void __launch_bounds__(kThreads, NT == 4 ? 1 : 2) gemv_int4_kernel(co
   __shared__ int abort_flag;
   __shared__ int n_own;
   __shared__ int own_tiles[kMaxOwnTiles];
+  // K-quant: per warp and stage, (d*sc, dmin*mn) of its 16 rows x 8 sub-blocks
+  __shared__ float2 q4k_tab[FMT == kFmtQ4K ? kConsumerWarps * 128 : 1];
   volatile int* abort_v = &abort_flag;
 
   const uint32_t base = (dev::smem_u32(smem_raw) + 1023u) & ~1023u;
@@ -356,6 +375,50 @@ __global__ void __launch_bounds__(kThreads, NT == 4 ? 1 : 2) gemv_int4_kernel(co
       const uint32_t wt = base + st * C::kStageBytes;
       const uint32_t xt = wt + kWTileBytes;
       const uint32_t stile = xt + C::kXTileBytes;
+      if constexpr (FMT == kFmtQ4K) {
+        // one superblock per row and stage: the warp decodes (d*sc, dmin*mn)
+        // of its 16 rows x 8 sub-blocks once, then per sub-block
+        //   acc += d*sc * sum(q x) - dmin*mn * sum(x)
+        // with both sums on the tensor cores (q exact in bf16, A = 1 for sum(x))
+        float2* tab = q4k_tab + warp * 128;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int idx = lane + 32 * k;
+          tab[idx] = q4k_ab(dev::lds128(stile + (warp * 16 + (idx >> 3)) * 16), idx & 7);
+        }
+        __syncwarp();
+        const uint32_t one2 = 0x3F803F80u;   // bf16 1.0 in both halves
+        const uint32_t a_one[4] = {one2, one2, one2, one2};
+#pragma unroll
+        for (int g = 0; g < 8; ++g) {
+          const uint32_t w0 = dev::lds32(wt + dev::swz128(rho0, g) + 4 * c);
+          const uint32_t w1 = dev::lds32(wt + dev::swz128(rho0 + 8, g) + 4 * c);
+          uint32_t q0[4], q1[4];
+          dequant_word<0>(w0, q0);
+          dequant_word<0>(w1, q1);
+          const uint32_t a_lo[4] = {q0[0], q1[0], q0[1], q1[1]};
+          const uint32_t a_hi[4] = {q0[2], q1[2], q0[3], q1[3]};
+          const float2 ab0 = tab[r * 8 + g], ab1 = tab[(r + 8) * 8 + g];
+#pragma unroll
+          for (int t = 0; t < NT; ++t) {
+            const int n = t * 8 + (lane & 7);
+            const int q = lane >> 3;
+            const int box = g >> 1;
+            const int chunk = 4 * (g & 1) + q;
+            uint32_t b0, b1, b2, b3;
+            dev::ldmatrix_x4(xt + box * C::kXBoxBytes + dev::swz128(n, chunk), b0, b1, b2, b3);
+            float s1[4], s0[4];
+            dev::mma_bf16_16816(s1, a_lo, b0, b1, zero4);
+            dev::mma_bf16_16816(s1, a_hi, b2, b3, s1);
+            dev::mma_bf16_16816(s0, a_one, b0, b1, zero4);
+            dev::mma_bf16_16816(s0, a_one, b2, b3, s0);
+            acc[t][0] = fmaf(ab0.x, s1[0], fmaf(-ab0.y, s0[0], acc[t][0]));
+            acc[t][1] = fmaf(ab0.x, s1[1], fmaf(-ab0.y, s0[1], acc[t][1]));
+            acc[t][2] = fmaf(ab1.x, s1[2], fmaf(-ab1.y, s0[2], acc[t][2]));
+            acc[t][3] = fmaf(ab1.x, s1[3], fmaf(-ab1.y, s0[3], acc[t][3]));
+          }
+        }
+      } else {
       const uint4 sc0 = dev::lds128(stile + rho0 * 16);
       const uint4 sc1 = dev::lds128(stile + (rho0 + 8) * 16);
       const __half* s0h = reinterpret_cast<const __half*>(&sc0);
@@ -365,8 +428,8 @@ __global__ void __launch_bounds__(kThreads, NT == 4 ? 1 : 2) gemv_int4_kernel(co
         const uint32_t w0 = dev::lds32(wt + dev::swz128(rho0, g) + 4 * c);
         const uint32_t w1 = dev::lds32(wt + dev::swz128(rho0 + 8, g) + 4 * c);
         uint32_t q0[4], q1[4];
-        dequant_word(w0, q0);
-        dequant_word(w1, q1);
+        dequant_word<8>(w0, q0);
+        dequant_word<8>(w1, q1);
         const uint32_t a_lo[4] = {q0[0], q1[0], q0[1], q1[1]};  // inputs 0..15 of the group
         const uint32_t a_hi[4] = {q0[2], q1[2], q0[3], q1[3]};  // inputs 16..31
         const float sr0 = __half2float(s0h[g]);
@@ -388,6 +451,7 @@ __global__ void __launch_bounds__(kThreads, NT == 4 ? 1 : 2) gemv_int4_kernel(co
           acc[t][2] = fmaf(sr1, tmp[2], acc[t][2]);
           acc[t][3] = fmaf(sr1, tmp[3], acc[t][3]);
         }
+      }
       }
       __syncwarp();
       if (lane == 0) dev::mbar_arrive(dev::smem_u32(&empty_bar[st]));
@@ -531,8 +595,11 @@ namespace {
 
 template <int NT>
 cudaError_t setup_nt() {
-  void (*ks[5])(GemvParams) = {gemv_int4_kernel<NT, 0>, gemv_int4_kernel<NT, 1>, gemv_int4_kernel<NT, 2>,
-                               gemv_int4_kernel<NT, 3>, gemv_int4_kernel<NT, 4>};
+  void (*ks[10])(GemvParams) = {
+      gemv_int4_kernel<NT, 0, kFmtInt4>, gemv_int4_kernel<NT, 1, kFmtInt4>, gemv_int4_kernel<NT, 2, kFmtInt4>,
+      gemv_int4_kernel<NT, 3, kFmtInt4>, gemv_int4_kernel<NT, 4, kFmtInt4>, gemv_int4_kernel<NT, 0, kFmtQ4K>,
+      gemv_int4_kernel<NT, 1, kFmtQ4K>, gemv_int4_kernel<NT, 2, kFmtQ4K>, gemv_int4_kernel<NT, 3, kFmtQ4K>,
+      gemv_int4_kernel<NT, 4, kFmtQ4K>};
   for (auto k : ks) {
     const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, GemvCfg<NT>::kSmem);
     if (e != cudaSuccess) return e;
@@ -540,16 +607,21 @@ cudaError_t setup_nt() {
   return cudaSuccess;
 }
 
-template <int NT>
-cudaError_t launch_nt(const GemvParams& p, dim3 grid, cudaStream_t st) {
+template <int NT, int FMT>
+cudaError_t launch_fmt(const GemvParams& p, dim3 grid, cudaStream_t st) {
   switch (p.epi) {
-    case kGemvEpiQKV: return launch_k(gemv_int4_kernel<NT, 0>, grid, kThreads, GemvCfg<NT>::kSmem, st, p);
-    case kGemvEpiResid: return launch_k(gemv_int4_kernel<NT, 1>, grid, kThreads, GemvCfg<NT>::kSmem, st, p);
-    case kGemvEpiSwiglu: return launch_k(gemv_int4_kernel<NT, 2>, grid, kThreads, GemvCfg<NT>::kSmem, st, p);
-    case kGemvEpiCast: return launch_k(gemv_int4_kernel<NT, 3>, grid, kThreads, GemvCfg<NT>::kSmem, st, p);
-    case kGemvEpiArgmax: return launch_k(gemv_int4_kernel<NT, 4>, grid, kThreads, GemvCfg<NT>::kSmem, st, p);
+    case kGemvEpiQKV: return launch_k(gemv_int4_kernel<NT, 0, FMT>, grid, kThreads, GemvCfg<NT>::kSmem, st, p);
+    case kGemvEpiResid: return launch_k(gemv_int4_kernel<NT, 1, FMT>, grid, kThreads, GemvCfg<NT>::kSmem, st, p);
+    case kGemvEpiSwiglu: return launch_k(gemv_int4_kernel<NT, 2, FMT>, grid, kThreads, GemvCfg<NT>::kSmem, st, p);
+    case kGemvEpiCast: return launch_k(gemv_int4_kernel<NT, 3, FMT>, grid, kThreads, GemvCfg<NT>::kSmem, st, p);
+    case kGemvEpiArgmax: return launch_k(gemv_int4_kernel<NT, 4, FMT>, grid, kThreads, GemvCfg<NT>::kSmem, st, p);
   }
   return cudaErrorInvalidValue;
+}
+
+template <int NT>
+cudaError_t launch_nt(const GemvParams& p, dim3 grid, cudaStream_t st) {
+  return p.fmt == kFmtQ4K ? launch_fmt<NT, kFmtQ4K>(p, grid, st) : launch_fmt<NT, kFmtInt4>(p, grid, st);
 }
 
 }  // namespace

@@ -41,6 +41,12 @@ enum ProfClass { kProj = 0, kAttn = 1, kEpi = 2, kMatch = 3 };
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
+// int4 group-32 or K-quant: the 4-bit formats of the GEMV and the tcgen05 GEMM
+bool packed4(const kvr_config& c) {
+  return c.weight_format == KVR_WEIGHTS_INT4_G32 || c.weight_format == KVR_WEIGHTS_Q4K;
+}
+int weight_fmt(const kvr_config& c) { return c.weight_format == KVR_WEIGHTS_Q4K ? kFmtQ4K : kFmtInt4; }
+
 bool valid_config(const kvr_config* c, std::string* why) {
   auto bad = [&](const char* m) { if (why) *why = m; return false; };
   if (!c) return bad("config is null");
@@ -52,9 +58,10 @@ bool valid_config(const kvr_config* c, std::string* why) {
   if (c->n_q_heads % c->n_kv_heads) return bad("n_q_heads must be a multiple of n_kv_heads");
   if (c->hidden % 8 || c->hidden > 8192) return bad("hidden must be a multiple of 8, at most 8192");
   if (!c->attn_only && (c->ffn <= 0 || c->ffn % 8)) return bad("ffn must be a positive multiple of 8");
-  if (c->weight_format != KVR_WEIGHTS_BF16 && c->weight_format != KVR_WEIGHTS_INT4_G32)
-    return bad("weight_format must be 0 (bf16) or 1 (int4 g32)");
-  if (c->weight_format == KVR_WEIGHTS_INT4_G32) {
+  if (c->weight_format != KVR_WEIGHTS_BF16 && c->weight_format != KVR_WEIGHTS_INT4_G32 &&
+      c->weight_format != KVR_WEIGHTS_Q4K)
+    return bad("weight_format must be 0 (bf16), 1 (int4 g32) or 2 (q4k)");
+  if (packed4(*c)) {
     if (c->hidden % kGemvKStep || (c->n_q_heads * c->head_dim) % kGemvKStep ||
         (!c->attn_only && c->ffn % kGemvKStep))
       return bad("int4 weights need every projection input width to be a multiple of 256");
@@ -113,12 +120,12 @@ ScratchLayout scratch_layout(const kvr_config* c) {
   L.z = take(M * F * 2);
   // GEMV: [ksplit][tiles][32][128] tile-major partials (tiles round each segment up)
   L.part_floats = (size_t)kMaxKSplit * kGemvMaxCols * (max_ldo(c) + 3 * kGemvRows);
-  if (c->weight_format == KVR_WEIGHTS_INT4_G32)
+  if (packed4(*c))
     L.part_floats = std::max(L.part_floats, (size_t)kGemmMaxSplit * kGemmMaxTok *
                                                 std::max(qkv_cols(c), c->hidden));
   // the output head's GEMV: up to three contributions per 128-row tile
   const size_t head_tiles = ((size_t)c->vocab + kGemvRows - 1) / kGemvRows;
-  if (c->weight_format == KVR_WEIGHTS_INT4_G32)
+  if (packed4(*c))
     L.part_floats = std::max(L.part_floats, head_tiles * 3 * kGemvMaxCols * kGemvRows);
   L.part = take(L.part_floats * 4);
   size_t worst = 0;
@@ -349,6 +356,7 @@ int project_gemm(kvr_ctx* c, cudaStream_t st, const Seg* segs, int nseg, const C
   p.ldo = col;
   p.plane = (long long)kGemmMaxTok * p.ldo;
   p.swiglu = swiglu ? 1 : 0;
+  p.fmt = weight_fmt(c->cfg);
   int ks = 1;
   if (!swiglu) {
     ks = (c->n_sms + tiles / 2) / std::max(tiles, 1);
@@ -392,6 +400,7 @@ struct Fused {
   __nv_bfloat16* out = nullptr;           // Resid (last layer) / Cast
   const __nv_bfloat16* norm_gain = nullptr;  // Resid: RMSNorm the new rows into c->a
   float2* best = nullptr;                 // Argmax
+  int fmt = -1;                           // WeightFmt; -1: the layers' format
 };
 
 // Small-m int4 passes: the GEMV with its fused epilogue (plus the RMSNorm of
@@ -407,6 +416,7 @@ int project_gemv_int4(kvr_ctx* c, cudaStream_t st, const Seg* segs, int nseg, co
   p.status = c->status;
   p.part = c->part;
   p.epi = fz.epi;
+  p.fmt = fz.fmt >= 0 ? fz.fmt : weight_fmt(cfg);
   p.counters = c->counters;
   int tiles = 0;
   if (pair) {
@@ -500,7 +510,7 @@ int project(kvr_ctx* c, cudaStream_t st, const Seg* segs, int nseg, Act act, int
             const Fused& fz, bool swiglu = false) {
   const kvr_config& cfg = c->cfg;
   const CUtensorMap* tmx = act == Act::A ? c->tm_a : (act == Act::O ? c->tm_o : c->tm_z);
-  if (cfg.weight_format == KVR_WEIGHTS_INT4_G32) {
+  if (packed4(cfg)) {
     if (m > kGemvMaxCols && !c->force_gemv)
       return project_gemm(c, st, segs, nseg, tmx, K, m, swiglu, epi);
     return project_gemv_int4(c, st, segs, nseg, tmx, K, m, fz);
@@ -706,7 +716,6 @@ int run_stack(kvr_ctx* c, const RowMap& rows, const void* hidden,
   const kvr_config& k = c->cfg;
   const int m = rows.m, H = k.hidden, d = k.head_dim;
   const int Hq = k.n_q_heads, Hkv = k.n_kv_heads, F = k.ffn;
-  const bool i4 = k.weight_format == KVR_WEIGHTS_INT4_G32;
   cudaError_t e;
   {
     Timed t(c, kEpi, st);
@@ -832,13 +841,12 @@ int run_stack(kvr_ctx* c, const RowMap& rows, const void* hidden,
       if (e != cudaSuccess) return cuda_fail(c, e, "trace copy");
     }
   }
-  (void)i4;
   return KVR_OK;
 }
 
 bool weights_ok(const kvr_ctx* c, const kvr_layer_weights* w) {
   if (!w) return false;
-  const bool i4 = c->cfg.weight_format == KVR_WEIGHTS_INT4_G32;
+  const bool i4 = packed4(c->cfg);
   for (int l = 0; l < c->cfg.n_layers; ++l) {
     const kvr_layer_weights& W = w[l];
     const void* need[] = {W.wq, W.wk, W.wv, W.wo};
@@ -1076,7 +1084,7 @@ int kvr_ctx_create(const kvr_config* cfg, void* kv_arena, size_t arena_bytes, vo
   ok = ok && encode_2d(&c->tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, c->q, k.head_dim,
                        (uint64_t)k.max_rows * k.n_q_heads, (uint64_t)k.head_dim * 2, 64, 128,
                        CU_TENSOR_MAP_SWIZZLE_128B);
-  if (k.weight_format == KVR_WEIGHTS_INT4_G32) {
+  if (packed4(k)) {
     ok = ok && act_maps(c->tm_a, c->a, k.hidden, k.max_rows);
     ok = ok && act_maps(c->tm_o, c->o, k.n_q_heads * k.head_dim, k.max_rows);
     if (!k.attn_only) ok = ok && act_maps(c->tm_z, c->z, k.ffn, k.max_rows);
@@ -1318,7 +1326,7 @@ int kvr_verify_accept(kvr_ctx* c, int slot, const int32_t* tokens, int m, const 
   if (!c) return KVR_ERR_ARG;
   const kvr_config& k = c->cfg;
   if (!head || !next_tokens || !accepted) return fail(c, KVR_ERR_ARG, "null head or result pointer");
-  if (k.weight_format != KVR_WEIGHTS_INT4_G32 || k.attn_only)
+  if (!packed4(k) || k.attn_only)
     return fail(c, KVR_ERR_UNSUPPORTED, "the output head needs int4 weights and the full decoder layer");
   if (head->vocab <= 0 || head->vocab > k.vocab)
     return fail(c, KVR_ERR_ARG, "head vocab %d outside [1, %d] (the configured vocab)", head->vocab, k.vocab);
@@ -1334,6 +1342,7 @@ int kvr_verify_accept(kvr_ctx* c, int slot, const int32_t* tokens, int m, const 
   Seg seg = {head->w, head->s, head->vocab};
   Fused fz;
   fz.epi = kGemvEpiArgmax;
+  fz.fmt = kFmtInt4;   // the head is int4 group-32 in every configuration
   fz.best = c->best;
   rc = project_gemv_int4(c, st, &seg, 1, c->tm_a, k.hidden, m, fz);
   cudaError_t e = cudaSuccess;

@@ -106,6 +106,10 @@ enum GemvEpi : int {
   kGemvEpiArgmax = 4,  // per token, the tile's largest y and its row (lowest on ties) -> best
 };
 
+// int4 weight formats of the GEMV and the tcgen05 GEMM (include/kvr.h):
+// group-32 fp16 scales, or K-quant superblocks (16-byte records per 256 inputs)
+enum WeightFmt { kFmtInt4 = 0, kFmtQ4K = 1 };
+
 struct GemvParams {
   GemvSeg seg[3];   // SwiGLU: seg[0] = gate, seg[1] = up (64-row boxes), nseg = 1
   CUtensorMap tx;   // activations bf16 [max_rows][K], box {64, 8*NT}, 128B swizzle
@@ -124,6 +128,7 @@ struct GemvParams {
   int* status;
   // fused epilogue of the int4 kernel
   int epi;          // GemvEpi
+  int fmt;          // WeightFmt
   int tiles;        // tiles of this launch
   int* counters;    // [tiles] contributor arrival counters; zero between launches
   RowMap rows;      // QKV: row positions (row i is stored at rows.P + i)
@@ -163,6 +168,7 @@ struct GemmParams {
   int m;            // valid tokens of this pass
   int t0;           // first token of this pass
   int swiglu;       // 1: write z = silu(gate) * up; 0: write fp32 partial sums
+  int fmt;          // WeightFmt (scales: fp16 group scales or K-quant records)
   int ldo;
   int F;
   long long plane;

@@ -18,7 +18,8 @@ LIB_PATH = os.path.join(HERE, "libkvr.so")
 KVR_OK = 0
 ERRORS = {-1: "KVR_ERR_ARG", -2: "KVR_ERR_CAPACITY", -3: "KVR_ERR_CUDA", -4: "KVR_ERR_TIMEOUT",
           -5: "KVR_ERR_FAULT", -6: "KVR_ERR_UNSUPPORTED", -7: "KVR_ERR_MISMATCH"}
-WEIGHTS_BF16, WEIGHTS_INT4_G32 = 0, 1
+WEIGHTS_BF16, WEIGHTS_INT4_G32, WEIGHTS_Q4K = 0, 1, 2
+_FORMATS = {"bf16": WEIGHTS_BF16, "int4": WEIGHTS_INT4_G32, "q4k": WEIGHTS_Q4K}
 MAX_SLOTS, MAX_BRANCHES = 16, 16
 
 EXPORTED = ["kvr_arena_bytes", "kvr_scratch_bytes", "kvr_ctx_create", "kvr_ctx_info",
@@ -113,7 +114,7 @@ def config_for_shape(shape, n_slots: int, capacity: int, max_rows: int,
                      vocab: int = 0) -> KvrConfig:
     return KvrConfig(n_slots, capacity, shape.n_layers if n_layers is None else n_layers,
                      shape.hidden, shape.n_q_heads, shape.n_kv_heads, shape.head_dim,
-                     shape.ffn, WEIGHTS_INT4_G32 if shape.weight_format == "int4" else WEIGHTS_BF16,
+                     shape.ffn, _FORMATS[shape.weight_format],
                      1 if shape.attn_only else 0, 1 if match_threshold else 0, max_rows,
                      shape.rope_theta, shape.rms_eps, vocab)
 

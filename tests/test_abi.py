@@ -56,6 +56,17 @@ def test_invalid_configs_are_refused(lib, field, value):
     assert lib.kvr_ctx_create(ctypes.byref(cfg), None, 0, None, 0, ctypes.byref(out)) == -1
 
 
+def test_q4k_is_a_format(lib):
+    from prefix_reused_prefill_gb300 import kvr
+    cfg = kvr.config_for_shape(workloads.SHAPES["small_q4k"], 2, 256, 32)
+    assert cfg.weight_format == 2 and lib.kvr_scratch_bytes(ctypes.byref(cfg)) > 0
+    cfg.hidden = 640  # the input widths follow the int4 rule
+    assert lib.kvr_scratch_bytes(ctypes.byref(cfg)) == 0
+    cfg = kvr.config_for_shape(workloads.SHAPES["small_q4k"], 2, 256, 32)
+    cfg.weight_format = 3
+    assert lib.kvr_scratch_bytes(ctypes.byref(cfg)) == 0
+
+
 def test_int4_width_rule(lib):
     from prefix_reused_prefill_gb300 import kvr
     cfg = kvr.config_for_shape(workloads.SHAPES["small"], 2, 256, 32)

@@ -36,6 +36,7 @@ def close(got, ref, what):
     ("small", [20, 0, 130, 45], [30, 1, 40, 7]),       # 78 rows: tcgen05 GEMM; 30 and 40 rows take tcgen05 attention
     ("small_d128", [50, 11], [4, 2]),
     ("small_bf16", [33, 70, 5], [2, 9, 1]),
+    ("small_q4k", [40, 9], [3, 50]),
 ])
 def test_batch_matches_each_conversation_alone(shape_name, prefixes, lens):
     from prefix_reused_prefill_gb300 import Kvr, config_for_shape

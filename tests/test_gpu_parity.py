@@ -93,6 +93,7 @@ def test_tiny_config_exact():
     ("small_d128", 45, [1, 5, 16, 33, 100], 256),
     ("small_bf16", 33, [2, 11, 35], 256),
     ("small", 150, [300], 512),
+    ("small_q4k", 70, [1, 3, 9, 17, 40, 130], 256),   # K-quant: GEMV at 8/16/32 tokens, tcgen05 GEMM
 ])
 def test_suffix_prefill_matches_oracle(shape_name, P, ms, cap):
     shape, kv, w, W, _ = make(shape_name, 2, cap, min(cap, 320))
