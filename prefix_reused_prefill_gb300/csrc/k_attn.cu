@@ -340,8 +340,9 @@ __global__ void __launch_bounds__((RW + 1) * 32) attn_kernel(const __grid_consta
 // One warp per (token, head) row: merge the key splits' (O, max, sum)
 // partials.  Lane s holds split s's (max, sum) (and lane s-32 split s for
 // nsplit > 32); the split weights are broadcast with shuffles and each lane
-// accumulates D/32 consecutive elements over the splits in split order.
-template <int D>
+// accumulates D/32 consecutive elements over the splits in split order, NS
+// splits' loads in flight at a time.
+template <int D, int NS>   // NS: split slices loaded per batch
 __global__ void __launch_bounds__(256) attn_combine_kernel(const __grid_constant__ AttnParams p) {
   dev::pdl_trigger();
   dev::pdl_wait();
@@ -382,38 +383,28 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const __grid_constant
   for (int e = 0; e < E; ++e) acc[e] = 0.f;
   const float* src = opart + rowidx * D + lane * E;
   const long long sstride = rows * D;
-  if (ns <= 32) {
-    // every split's slice in flight at once, then added in split order
-    float v[32][E];
+  // NS splits' slices in flight at a time, added in split order
+  for (int s0 = 0; s0 < ns; s0 += NS) {
+    float v[NS][E];
 #pragma unroll
-    for (int s = 0; s < 32; ++s)
-      if (s < ns) {
+    for (int j = 0; j < NS; ++j)
+      if (s0 + j < ns) {
         if (E == 4) {
-          const float4 x = __ldcg(reinterpret_cast<const float4*>(src + s * sstride));
-          v[s][0] = x.x; v[s][1 % E] = x.y; v[s][2 % E] = x.z; v[s][3 % E] = x.w;
+          const float4 x = __ldcg(reinterpret_cast<const float4*>(src + (s0 + j) * sstride));
+          v[j][0] = x.x; v[j][1 % E] = x.y; v[j][2 % E] = x.z; v[j][3 % E] = x.w;
         } else {
-          const float2 x = __ldcg(reinterpret_cast<const float2*>(src + s * sstride));
-          v[s][0] = x.x; v[s][1 % E] = x.y;
+          const float2 x = __ldcg(reinterpret_cast<const float2*>(src + (s0 + j) * sstride));
+          v[j][0] = x.x; v[j][1 % E] = x.y;
         }
       }
 #pragma unroll
-    for (int s = 0; s < 32; ++s)
-      if (s < ns) {
-        const float w = __shfl_sync(0xffffffffu, w0, s);
+    for (int j = 0; j < NS; ++j)
+      if (s0 + j < ns) {
+        const int sp = s0 + j;
+        const float w = __shfl_sync(0xffffffffu, sp < 32 ? w0 : w1, sp & 31);
 #pragma unroll
-        for (int e = 0; e < E; ++e) acc[e] += w * v[s][e];
+        for (int e = 0; e < E; ++e) acc[e] += w * v[j][e];
       }
-  }
-#pragma unroll 8
-  for (int s = ns <= 32 ? ns : 0; s < ns; ++s) {
-    const float w = __shfl_sync(0xffffffffu, s < 32 ? w0 : w1, s & 31);
-    if (E == 4) {
-      const float4 v = *reinterpret_cast<const float4*>(src + s * sstride);
-      acc[0] += w * v.x; acc[1 % E] += w * v.y; acc[2 % E] += w * v.z; acc[3 % E] += w * v.w;
-    } else {
-      const float2 v = *reinterpret_cast<const float2*>(src + s * sstride);
-      acc[0] += w * v.x; acc[1 % E] += w * v.y;
-    }
   }
   const float inv = 1.f / den;
   __nv_bfloat16* dst = p.o + grow * D + lane * E;
@@ -461,8 +452,18 @@ cudaError_t launch_attention(const AttnParams& p, int d, int row_warps, cudaStre
 
 cudaError_t launch_attn_combine(const AttnParams& p, int d, cudaStream_t st) {
   const unsigned blocks = (unsigned)((p.rows.m * p.Hq + 7) / 8);
-  if (d == 128) return launch_k(attn_combine_kernel<128>, blocks, 256, 0, st, p);
-  return launch_k(attn_combine_kernel<64>, blocks, 256, 0, st, p);
+  // few splits (large m): a short batch keeps registers and occupancy; many
+  // splits (small m): all of them in flight
+  if (p.nsplit <= 4) {
+    if (d == 128) return launch_k(attn_combine_kernel<128, 4>, blocks, 256, 0, st, p);
+    return launch_k(attn_combine_kernel<64, 4>, blocks, 256, 0, st, p);
+  }
+  if (p.nsplit <= 8) {
+    if (d == 128) return launch_k(attn_combine_kernel<128, 8>, blocks, 256, 0, st, p);
+    return launch_k(attn_combine_kernel<64, 8>, blocks, 256, 0, st, p);
+  }
+  if (d == 128) return launch_k(attn_combine_kernel<128, 32>, blocks, 256, 0, st, p);
+  return launch_k(attn_combine_kernel<64, 32>, blocks, 256, 0, st, p);
 }
 
 }  // namespace kvr

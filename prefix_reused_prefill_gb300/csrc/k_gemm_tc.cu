@@ -135,14 +135,18 @@ __device__ __forceinline__ void codes_of_word(uint32_t w, __nv_bfloat162 out[4])
 }
 
 // K-quant: 8 unsigned 4-bit codes of one word -> 4 bf16x2 weights
-// bf16(d*sc*q - dmin*mn) (pair i: fields i and i+4, as codes_of_word), with
-// a = d*sc and b = dmin*mn in fp32 (q*a - b is formed exactly and rounded once)
-__device__ __forceinline__ void q4k_weights_of_word(uint32_t w, float a, float b, uint32_t out[4]) {
+// bf16(d*sc*q - dmin*mn) (pair i: fields i and i+4, as codes_of_word).  The
+// codes become exact fp32 values 128 + q (the bf16 pattern 128 + q shifted
+// into the high half), so w = (128 + q)*a + c with a = d*sc and
+// c = -(128*a + dmin*mn), one fp32 FMA per weight on the full-rate pipe (c
+// carries at most one fp32 rounding, far below the bf16 rounding that follows).
+__device__ __forceinline__ void q4k_weights_of_word(uint32_t w, float a, float c, uint32_t out[4]) {
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const uint32_t v = (w >> (4 * i)) & 0x000F000Fu;
-    const float ql = (float)(v & 0xFFFFu), qh = (float)(v >> 16);
-    out[i] = dev::pack_bf16x2(fmaf(ql, a, -b), fmaf(qh, a, -b));
+    uint32_t v;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(v) : "r"(w >> (4 * i)), "r"(0x000F000Fu), "r"(0x43004300u));
+    const float ql = __uint_as_float(v << 16), qh = __uint_as_float(v & 0xFFFF0000u);
+    out[i] = dev::pack_bf16x2(fmaf(ql, a, c), fmaf(qh, a, c));
   }
 }
 
@@ -357,12 +361,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_int4_tc_kernel(const __grid_
         for (int h = 0; h < 2; ++h) {
           const uint4 wv = h ? w1 : w0;
           const int j = 4 * ((kc0 + i) & 1) + 2 * hq + h;   // sub-block of the superblock
-          const float a = d * (float)q4k_field6(rec, j), b = dmin * (float)q4k_field6(rec, 8 + j);
+          const float a = d * (float)q4k_field6(rec, j);
+          const float c = -fmaf(128.f, a, dmin * (float)q4k_field6(rec, 8 + j));
           uint32_t c0[4], c1[4], c2[4], c3[4];
-          q4k_weights_of_word(wv.x, a, b, c0);
-          q4k_weights_of_word(wv.y, a, b, c1);
-          q4k_weights_of_word(wv.z, a, b, c2);
-          q4k_weights_of_word(wv.w, a, b, c3);
+          q4k_weights_of_word(wv.x, a, c, c0);
+          q4k_weights_of_word(wv.y, a, c, c1);
+          q4k_weights_of_word(wv.z, a, c, c2);
+          q4k_weights_of_word(wv.w, a, c, c3);
 #pragma unroll
           for (int jj = 0; jj < 4; ++jj) {
             outv[16 * h + 4 * jj + 0] = c0[jj];
