@@ -390,6 +390,13 @@ int kvr_verify_accept(kvr_ctx* ctx, int slot, const int32_t* tokens, int m, cons
                       const kvr_layer_weights* weights, const kvr_head_weights* head, void* out,
                       int32_t* next_tokens, int* accepted, void* stream);
 
+/* Self-test of the failure path, without a GPU fault: launches one device
+ * wait on an mbarrier that nothing completes.  Like every wait in the
+ * library's kernels it gives up after 1 s and records the timeout in the
+ * status word; the next kvr_sync_status returns KVR_ERR_TIMEOUT, clears the
+ * word and the GEMV arrival counters, and the context stays usable. */
+int kvr_selftest_wait(kvr_ctx* ctx, void* stream);
+
 /* Per-kernel-class timing with CUDA events recorded on the launch stream.
  * While enabled, every launch is bracketed by an event pair; kvr_profile_read
  * synchronises and returns milliseconds summed since the last read for

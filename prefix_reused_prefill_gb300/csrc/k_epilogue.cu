@@ -334,6 +334,21 @@ cudaError_t launch_head_argmax(const float2* best, int tiles, int m, int32_t* ou
   return launch_k(head_argmax_kernel, (m + 7) / 8, 256, 0, st, best, tiles, m, out);
 }
 
+// One bounded wait on an mbarrier that nothing completes: it gives up after
+// the wait limit and records the timeout in the status word.
+__global__ void wait_probe_kernel(int* status) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x != 0) return;
+  dev::mbar_init(dev::smem_u32(&bar), 1);
+  dev::fence_mbar_init();
+  dev::mbar_wait(dev::smem_u32(&bar), 0, status);
+}
+
+cudaError_t launch_wait_probe(int* status, cudaStream_t st) {
+  wait_probe_kernel<<<1, 32, 0, st>>>(status);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_rmsnorm(const float* h, int c0, int mb, int H, const __nv_bfloat16* gain,
                            float eps, __nv_bfloat16* a, cudaStream_t st) {
   const int v = (H / 4 + 255) / 256;

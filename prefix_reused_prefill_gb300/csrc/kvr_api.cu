@@ -1462,6 +1462,12 @@ int kvr_sync_status(kvr_ctx* c, void* stream) {
   return KVR_OK;
 }
 
+int kvr_selftest_wait(kvr_ctx* c, void* stream) {
+  if (!c) return KVR_ERR_ARG;
+  cudaError_t e = launch_wait_probe(c->status, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? KVR_OK : cuda_fail(c, e, "wait probe launch");
+}
+
 int kvr_trace_set(kvr_ctx* c, void* dev, size_t bytes) {
   if (!c) return KVR_ERR_ARG;
   if (!dev) {

@@ -256,6 +256,8 @@ cudaError_t launch_embed(const __nv_bfloat16* hidden, int m, int H, const __nv_b
                          float eps, float* h, __nv_bfloat16* a, cudaStream_t st);
 // out[t] = the row of the largest value over the tiles' bests of token t
 // (lowest row on ties), t < m
+// one device-side wait that runs out (the failure path, without a fault)
+cudaError_t launch_wait_probe(int* status, cudaStream_t st);
 cudaError_t launch_head_argmax(const float2* best, int tiles, int m, int32_t* out, cudaStream_t st);
 // a[c0 + t] = bf16(RMSNorm(h[c0 + t]) * gain) for t < mb
 cudaError_t launch_rmsnorm(const float* h, int c0, int mb, int H, const __nv_bfloat16* gain,

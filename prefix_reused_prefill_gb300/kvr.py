@@ -29,7 +29,7 @@ EXPORTED = ["kvr_arena_bytes", "kvr_scratch_bytes", "kvr_ctx_create", "kvr_ctx_i
             "kvr_profile_launches",
             "kvr_last_error", "kvr_slot_match_static", "kvr_trace_set", "kvr_verify_accept",
             "kvr_config_hash", "kvr_slot_spill_bytes", "kvr_slot_spill", "kvr_slot_restore",
-            "kvr_prefill_batch"]
+            "kvr_prefill_batch", "kvr_selftest_wait"]
 
 
 class KvrError(RuntimeError):
@@ -97,6 +97,7 @@ def load_library(path: str = LIB_PATH):
         "kvr_last_error": (ctypes.c_char_p, [V]),
         "kvr_slot_match_static": (I, [V, i32p, I, P(I), P(I), V]),
         "kvr_trace_set": (I, [V, V, Z]),
+        "kvr_selftest_wait": (I, [V, V]),
         "kvr_config_hash": (ctypes.c_uint64, [P(KvrConfig), ctypes.c_uint64]),
         "kvr_slot_spill_bytes": (Z, [V, I]),
         "kvr_slot_spill": (I, [V, I, ctypes.c_uint64, V, Z, V]),
@@ -306,6 +307,9 @@ class Kvr:
         self._check(self.lib.kvr_prefill_batch(self.ctx, n, slots_c, lens_c, _i32(sum(token_lists, [])),
                                                hidden.data_ptr(), arr, out.data_ptr(), self._stream(stream)))
         return out
+
+    def kvr_selftest_wait(self, stream=None):
+        self._check(self.lib.kvr_selftest_wait(self.ctx, self._stream(stream)))
 
     def kvr_slot_spill(self, slot: int, model_tag: int = 0, stream=None, sync: bool = True) -> torch.Tensor:
         """The slot's record in pinned host memory (uint8); complete once the
