@@ -80,6 +80,8 @@ def oracle_layer_weights(lw):
     for k, v in lw.items():
         if isinstance(v, workloads.Int4Matrix):
             W[k] = formats.dequant_int4(v.packed.cpu().numpy(), v.scales.cpu().numpy())
+        elif isinstance(v, workloads.Q4KMatrix):
+            W[k] = formats.dequant_q4k(v.packed.cpu().numpy(), v.scales.cpu().numpy())
         else:
             W[k] = v.detach().cpu().to(torch.float64).numpy()
     return W
@@ -150,6 +152,36 @@ def test_turn9_full_size():
     rows = om.plain_rows(1668, 254)
     for layer in (0, 13, 27):
         check_layer(shape, lws[layer], kv, 0, layer, tr, 1668, rows, [0, 1, 127, 253], "turn9")
+    kv.close()
+
+
+def test_q4k_full_size_turn9_then_verify():
+    """K-quant weights at the turn-9 shape: 254 rows after 1668 cached (tcgen05 GEMM),
+    then a verify of 8 rows (GEMV); sampled rows of the first and last layers."""
+    shape = workloads.SHAPES["qwen7b_q4k"]
+    seed = workloads.config_seed(2)
+    tk = workloads.turn9_tokens(seed)
+    lws = workloads.stack_weights(shape, seed, device="cuda")
+    kv = make_ctx(shape, 1, 2304, 256)
+    w = kv.weights(lws)
+    state = tk["prompt"][:1668]
+    assert kv.kvr_slot_match(state[:1]) == (0, 0)
+    prefill_chunks(kv, 0, state, shape, seed, w)
+    trace = torch.zeros((shape.n_layers + 1, 256, shape.hidden), dtype=torch.float32, device="cuda")
+    kv.kvr_trace_set(trace)
+    suffix = tk["prompt"][1668:]
+    kv.kvr_prefill_suffix(0, suffix, workloads.hidden_for_tokens(suffix, shape.hidden, seed).cuda(), w)
+    kv.kvr_sync_status()
+    tr = trace.cpu().numpy()
+    for layer in (0, shape.n_layers - 1):
+        check_layer(shape, lws[layer], kv, 0, layer, tr, 1668, om.plain_rows(1668, 254), [0, 253],
+                    "q4k turn9")
+    draft = list(range(7000, 7008))
+    kv.kvr_verify(0, draft, workloads.hidden_for_tokens(draft, shape.hidden, seed).cuda(), w)
+    kv.kvr_sync_status()
+    tr = trace.cpu().numpy()
+    check_layer(shape, lws[0], kv, 0, 0, tr, 1922, om.plain_rows(1922, 8), list(range(8)), "q4k verify m=8")
+    kv.kvr_trace_set(None)
     kv.close()
 
 
