@@ -8,14 +8,17 @@
  *
  * Sources (page title, section):
  *   goinfer "Turn nine in under half a second":
- *     "What goinfer does"  -- keep the KV cache (two vectors per token in each
- *                             layer) of recent conversations; process only the
- *                             tokens after the conversation's stored start.
- *     "How it works"       -- longest shared start; a match must be longer
- *                             than what the session shares with the other
- *                             sessions; cut back to the shared point; on a GPU
- *                             model, --kv-sessions slots, empty slot else LRU;
- *                             usage.prefill_reused_tokens.
+ *     "What goinfer does"  -- recent conversations keep their K and V rows
+ *                             (one key and one value row per token and
+ *                             layer); a prompt runs only past the part a
+ *                             conversation already holds.
+ *     "How it works"       -- the slot with the longest common token prefix
+ *                             wins, provided that prefix exceeds the longest
+ *                             prefix this slot has in common with any other
+ *                             slot; the slot is truncated to the common
+ *                             length; on a GPU model --kv-sessions slots,
+ *                             an empty one first, else the least recently
+ *                             used; usage.prefill_reused_tokens.
  *     "Use it"             -- --kv-sessions N (0 turns reuse off); the memory
  *                             check may grant fewer slots than asked for.
  *     "What we got wrong"  -- the one-token-short cache after speculation.
@@ -257,8 +260,8 @@ int kvr_slot_kv(const kvr_ctx* ctx, int slot, int layer, void** k, void** v);
 /*
  * Slot spill and restore through host memory (Tempo9 docs, "KV cache spills
  * to disk, by default": reusable prefixes leave device memory and come back
- * later, and a record written for another model, dtype or KV layout is
- * recognised by a configuration hash and refused instead of being served).
+ * later; a record made under a different model, number format or KV layout
+ * is detected through a configuration hash and discarded, never reused).
  * Files, the size cap and eviction of records are the caller's.
  *
  * kvr_config_hash: FNV-1a (64-bit) over the fields that fix what a slot's K/V

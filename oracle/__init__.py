@@ -10,8 +10,8 @@ input generator ``workloads``.
 What it computes (sources are the three pages the design cites):
 
 * ``slots``  -- the slot table's policy: longest-token-prefix match, the
-  "longer than what the session shares with the others" threshold, empty-slot-
-  then-LRU eviction, truncate to the shared point, reused-token count
+  threshold against the prefix a slot shares with the other slots, empty-slot-
+  then-LRU eviction, truncate to the common length, reused-token count
   (goinfer, "Turn nine in under half a second": "How it works").
 * ``formats`` -- decoding of the int4 group-32 weight bytes and of bf16 values,
   written from the layout statement in ``include/kvr.h``.

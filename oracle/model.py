@@ -2,9 +2,9 @@
 
 TEST INFRASTRUCTURE ONLY (see the package header).
 
-Sources: goinfer, "Turn nine in under half a second" ("What goinfer does": the
-KV cache is two vectors per token in each layer, kept per conversation; only
-the tokens after the shared start are processed; "What we got wrong": a
+Sources: goinfer, "Turn nine in under half a second" ("What goinfer does": each
+conversation keeps one key and one value row per token and layer, and a prompt
+runs only past the part the conversation already holds; "What we got wrong": a
 speculative step checks the guessed tokens and must give the same words as
 plain decoding); the spec-decode post ("cost model": the m = k+1 verify rows
 run as one batched pass over weights read once); OpenJev "What changed" (several questions resume from one shared

@@ -1,15 +1,16 @@
 """The slot table's policy, stated plainly.  Test infrastructure only.
 
 Source: goinfer, "Turn nine in under half a second":
-* "How it works" -- a new prompt takes the session sharing the longest start
-  with it; that match must be longer than what the session shares with the
-  other sessions; the session is cut back to the shared point and only the
-  rest is prefilled.  On the GPU the sessions are --kv-sessions KV slots, one
-  conversation each; a new conversation takes an empty slot, else the least
-  recently used one.
+* "How it works" -- the prompt goes to the session with the longest common
+  token prefix, but only when that prefix exceeds the longest prefix the
+  session has in common with any other session; the session is truncated to
+  the common length and only the remaining prompt tokens are prefilled.  On
+  the GPU the sessions are --kv-sessions KV slots, one conversation each; an
+  unmatched prompt fills a free slot if there is one and otherwise evicts the
+  slot used longest ago.
 * "Use it" -- --kv-sessions 0 turns reuse off.
-* "What goinfer does" / usage.prefill_reused_tokens -- how many prompt tokens
-  were skipped.
+* "What goinfer does" / usage.prefill_reused_tokens -- the count of prompt
+  tokens served from the slot instead of being prefilled.
 
 Readings (listed in the design notes):
 * R1  accept the best slot s* iff l(s*) > 0 and (threshold off or

@@ -7,8 +7,9 @@
 //             the next projection (or write the bf16 output);
 //   * swiglu: silu(gate) * up -> bf16;
 //   * cast:   bf16 output of an attention-only layer.
-// goinfer "What goinfer does": the KV cache is two vectors per token per
-// layer; a row's K/V land at its slot position so later turns reuse them.
+// goinfer "What goinfer does": a conversation keeps one key and one value row
+// per token and layer; a row's K/V land at its slot position so later turns
+// reuse them.
 #include "kvr_internal.cuh"
 
 namespace kvr {

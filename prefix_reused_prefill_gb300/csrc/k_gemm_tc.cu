@@ -1,8 +1,8 @@
 // Large-m projections on the 5th-generation tensor cores: Y = X W^T with int4
 // group-32 weights, X bf16 [tokens][K], fp32 accumulation in tensor memory.
 //
-// thinkspread, "The economics of speculative decoding" (cost model): weights
-// are read once and shared by all m rows.  At the m = 254 rows of goinfer's
+// thinkspread, "The economics of speculative decoding" (cost model): each
+// weight streams once for all m rows.  At the m = 254 rows of goinfer's
 // turn-9 replay the projections are a real dense contraction (3.3 TFLOP per
 // 28-layer step), so they run as tcgen05.mma instead of a GEMV.
 //

@@ -3,8 +3,8 @@
 // epilogue applied in the same launch.
 //
 // thinkspread, "The economics of speculative decoding" (cost model): the m
-// verify rows run as a batched GEMV whose weights are read once and shared by
-// the rows, so an extra row costs far less than a full weight read.
+// verify rows run as one batched GEMV that streams each weight a single time
+// for all of them, so an extra row costs far less than a full weight read.
 //
 // int4 group-32 path (the hot one).  A CTA owns a 128-row weight tile and a
 // range of 256-input k-steps.  One producer warp streams, per k-step, a
@@ -31,7 +31,7 @@
 //   * QKV: a tile is one head (d = 128) or two (d = 64), so each rotate-half
 //     pair (j, j + d/2) is in the tile: RoPE at the row's position, bf16,
 //     q to the KV-head-major q buffer, K rows and V^T columns to the slot
-//     (goinfer "What goinfer does": two vectors per token per layer);
+//     (goinfer "What goinfer does": one key and one value row per token and layer);
 //   * Resid: h += y in fp32 (the RMSNorm that follows needs the whole row and
 //     runs as its own small launch), and on the last layer out = bf16(h);
 //   * Swiglu: the tile holds gate rows n0..n0+63 and the same up rows, so

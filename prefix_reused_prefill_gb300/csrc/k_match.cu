@@ -1,9 +1,10 @@
 // Prefix match on the device: longest common token prefix of every occupied
 // slot with the prompt, and of every pair of occupied slots.
 //
-// goinfer, "Turn nine in under half a second" ("How it works"): a new prompt
-// takes the slot sharing the longest start with it, and that match must be
-// longer than what the slot shares with the other slots.  Both quantities are
+// goinfer, "Turn nine in under half a second" ("How it works"): the prompt
+// goes to the slot with the longest common token prefix, provided that prefix
+// exceeds the longest one the slot has in common with any other slot.  Both
+// quantities are
 // first-mismatch positions; one CTA computes one of them by scanning its two
 // token rows in 256-token chunks and stopping at the first chunk that holds a
 // mismatch (block-wide vote, then a shared-memory minimum).

@@ -1,8 +1,8 @@
 // C-ABI of libkvr: the slot table and the suffix-prefill driver.
 //
 // Host policy (goinfer, "Turn nine in under half a second", "How it works" and
-// "Use it"): longest shared start, the anti-theft rule, empty slot else LRU,
-// cut back to the shared point, reused-token count; --kv-sessions 0 turns
+// "Use it"): longest common prefix, the anti-theft rule, empty slot else LRU,
+// truncation to the common length, reused-token count; --kv-sessions 0 turns
 // reuse off; the memory check may grant fewer slots than requested.
 // Device work is enqueued on the caller's stream; the library owns no device
 // memory -- it carves the caller's arena and scratch buffers.

@@ -15,7 +15,7 @@ def brute_choice(slots, stamps, prompt, threshold=True):
     slot[:L] == prompt[:L]; a candidate must share more with the prompt than
     with any other occupied slot, and may not cut its slot back while another
     slot is empty; the longest candidate wins; otherwise the first empty
-    slot, else the least recently used one.
+    slot, and with none empty the slot whose last use is oldest.
     """
     def shared(a, b):
         return max(L for L in range(min(len(a), len(b)) + 1) if list(a[:L]) == list(b[:L]))
