@@ -148,8 +148,8 @@ def _copy_kv(kv):
     return c
 
 
-def test_two_verify_rounds_continue_from_the_kept_tokens():
-    """Round 2 starts from the next token of round 1 at P + 1 + accepted; the
+def test_two_verify_steps_continue_from_the_kept_tokens():
+    """The second verify starts from the first one's next token at P + 1 + accepted; the
     rejected rows' K/V (still in the arena past the slot's length) are overwritten."""
     vocab, P = 2000, 45
     shape, kv, w, W = make("small", 256, 128, vocab)
@@ -163,7 +163,7 @@ def test_two_verify_rounds_continue_from_the_kept_tokens():
     for t0 in range(1200, 1400):
         c1 = _copy_kv(base)
         toks1, lg1 = oracle_chain(dims, W, c1, P, t0, 5, 2, gain, lm, xseed)
-        # the kept rows (three) then round 2 from the next token, on a cache holding only them
+        # the kept rows (three), then the second verify from the next token, on a cache holding only them
         c2 = _copy_kv(base)
         om.forward(dims, W, c2, workloads.bf16_to_f64(workloads.hidden_for_tokens(toks1[:3], shape.hidden, xseed)),
                    om.plain_rows(P, 3), rounded=False)
@@ -178,7 +178,7 @@ def test_two_verify_rounds_continue_from_the_kept_tokens():
     n1, a1 = kv.kvr_verify_accept(0, toks1, workloads.hidden_for_tokens(toks1, shape.hidden, xseed).cuda(), w, head)
     assert a1 == 2 and n1[2] == t1
     n2, a2 = kv.kvr_verify_accept(0, toks2, workloads.hidden_for_tokens(toks2, shape.hidden, xseed).cuda(), w, head)
-    check_rows(n2, lg2, "round 2")
+    check_rows(n2, lg2, "second verify")
     assert a2 == 3
     assert kv.kvr_slot_tokens(0) == prefix + toks1[:3] + toks2
 
