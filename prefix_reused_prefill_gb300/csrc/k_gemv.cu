@@ -475,8 +475,9 @@ __global__ void __launch_bounds__(kThreads, NT == 4 ? 1 : 2) gemv_int4_kernel(co
     }
   }
   // publish every contribution of this CTA, then count one arrival per tile
-  // touched (one thread per tile); the last arrival owns the tile's epilogue
-  __threadfence();
+  // touched (one thread per tile); the last arrival owns the tile's epilogue.
+  // The barrier orders every consumer's partial stores before the counting
+  // threads' gpu-scope fence (fences are cumulative), so only they fence.
   consumers_sync();
   {
     const int t_first = u0 / p.ksteps, t_last = (u1 - 1) / p.ksteps;
@@ -484,6 +485,7 @@ __global__ void __launch_bounds__(kThreads, NT == 4 ? 1 : 2) gemv_int4_kernel(co
     if (tile <= t_last && !*abort_v) {
       const long long tu0 = (long long)tile * p.ksteps;
       const int ncon = unit_owner(tu0 + p.ksteps - 1, units, p.ctas) - unit_owner(tu0, units, p.ctas) + 1;
+      __threadfence();
       const int done = atomicAdd(p.counters + tile, 1) + 1;
       if (done == ncon) {
         p.counters[tile] = 0;   // ready for the next launch
