@@ -24,13 +24,17 @@ namespace kvr {
 
 namespace {
 
-template <int D>
+// KW > 1: KW consumer warps share one 16-row tile and take alternate key
+// blocks (their online-softmax states are merged at the end), with a deeper
+// ring so that every warp has a block in flight.
+template <int D, int KW = 1>
 struct AttnCfg {
   static constexpr int kHalves = D / 64;                 // 64-element TMA boxes per row
   static constexpr int kTileBytes = kAttnKeys * D * 2;   // one K tile ([64 keys][D]) or V^T tile ([D][64 keys])
   static constexpr int kStageBytes = 2 * kTileBytes;
-  static constexpr int kStages = D == 128 ? 3 : 4;
+  static constexpr int kStages = KW > 1 ? (D == 128 ? 6 : 8) : (D == 128 ? 3 : 4);
   static constexpr int kSmem = kStages * kStageBytes + 1024;
+  static_assert(KW * (16 * D + 32) * 4 <= kStages * kStageBytes, "warp merge buffer fits the ring");
 };
 
 // The part of the call one CTA serves: the whole call, or in a batched
@@ -92,9 +96,11 @@ __device__ __forceinline__ bool visible(const RowInfo& ri, int j) {
   return ri.tok >= 0 && (j < ri.pre || (j >= ri.lo && j <= ri.hi));
 }
 
-template <int D, int RW>
-__global__ void __launch_bounds__((RW + 1) * 32) attn_kernel(const __grid_constant__ AttnParams p) {
-  using C = AttnCfg<D>;
+template <int D, int RW, int KW>
+__global__ void __launch_bounds__((RW * KW + 1) * 32) attn_kernel(const __grid_constant__ AttnParams p) {
+  static_assert(KW == 1 || RW == 1, "key-parallel warps serve one row tile");
+  using C = AttnCfg<D, KW>;
+  constexpr int kCons = RW * KW;   // consumer warps
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[C::kStages];
   __shared__ __align__(8) uint64_t empty_bar[C::kStages];
@@ -128,7 +134,7 @@ __global__ void __launch_bounds__((RW + 1) * 32) attn_kernel(const __grid_consta
   }
   __syncthreads();
 
-  if (warp == RW) {
+  if (warp == kCons) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       dev::prefetch_tmap(&p.tkv);
@@ -182,7 +188,8 @@ __global__ void __launch_bounds__((RW + 1) * 32) attn_kernel(const __grid_consta
   // -------------------------------------------------------------- consumers
   dev::pdl_wait();   // q comes from the previous launch
   const int r = lane >> 2, c = lane & 3;
-  const int rho0 = row_lo + warp * 16 + r;
+  const int kw = KW > 1 ? warp : 0;                    // key-parallel warp
+  const int rho0 = row_lo + (KW > 1 ? 0 : warp) * 16 + r;
   const RowInfo ri0 = row_info(p, v, kv, rho0);
   const RowInfo ri1 = row_info(p, v, kv, rho0 + 8);
 
@@ -212,7 +219,7 @@ __global__ void __launch_bounds__((RW + 1) * 32) attn_kernel(const __grid_consta
   float lrow[2] = {0.f, 0.f};
   const float zero4[4] = {0.f, 0.f, 0.f, 0.f};
 
-  for (int it = 0; it < nblk; ++it) {
+  for (int it = kw; it < nblk; it += KW) {
     const int st = it % C::kStages;
     const uint32_t use = (uint32_t)(it / C::kStages);
     if (!dev::mbar_wait(dev::smem_u32(&full_bar[st]), use & 1, p.status) || *abort_v) {
@@ -306,7 +313,6 @@ __global__ void __launch_bounds__((RW + 1) * 32) attn_kernel(const __grid_consta
     __syncwarp();
     if (lane == 0) dev::mbar_arrive(dev::smem_u32(&empty_bar[st]));
   }
-  if (*abort_v) return;
   (void)zero4;
 
 #pragma unroll
@@ -314,6 +320,56 @@ __global__ void __launch_bounds__((RW + 1) * 32) attn_kernel(const __grid_consta
     lrow[h] += __shfl_xor_sync(0xffffffffu, lrow[h], 1);
     lrow[h] += __shfl_xor_sync(0xffffffffu, lrow[h], 2);
   }
+  if constexpr (KW > 1) {
+    // merge the KW warps' (O, max, sum) of the same rows in shared memory (the
+    // ring is drained: every block was consumed); warp 0 writes the result
+    asm volatile("bar.sync 1, %0;" ::"r"(kCons * 32) : "memory");
+    float* mb = reinterpret_cast<float*>(smem_raw + (base - dev::smem_u32(smem_raw)));
+    float* mine = mb + kw * (16 * D + 32);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int row = r + 8 * h;
+#pragma unroll
+      for (int i = 0; i < D / 8; ++i)
+        *reinterpret_cast<float2*>(mine + row * D + 8 * i + 2 * c) = make_float2(o[i][2 * h], o[i][2 * h + 1]);
+      if (c == 0) {
+        mine[16 * D + row] = mrow[h];
+        mine[16 * D + 16 + row] = lrow[h];
+      }
+    }
+    asm volatile("bar.sync 1, %0;" ::"r"(kCons * 32) : "memory");
+    if (kw != 0 || *abort_v) return;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int row = r + 8 * h;
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < KW; ++w) M = fmaxf(M, mb[w * (16 * D + 32) + 16 * D + row]);
+      float sc[KW];
+      float L = 0.f;
+#pragma unroll
+      for (int w = 0; w < KW; ++w) {
+        const float mw = mb[w * (16 * D + 32) + 16 * D + row];
+        sc[w] = mw == -INFINITY ? 0.f : exp2f(mw - M);
+        L += sc[w] * mb[w * (16 * D + 32) + 16 * D + 16 + row];
+      }
+#pragma unroll
+      for (int i = 0; i < D / 8; ++i) {
+        float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int w = 0; w < KW; ++w) {
+          const float2 x = *reinterpret_cast<const float2*>(mb + w * (16 * D + 32) + row * D + 8 * i + 2 * c);
+          acc.x += sc[w] * x.x;
+          acc.y += sc[w] * x.y;
+        }
+        o[i][2 * h] = acc.x;
+        o[i][2 * h + 1] = acc.y;
+      }
+      mrow[h] = M;
+      lrow[h] = L;
+    }
+  }
+  if (*abort_v) return;
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     const RowInfo& ri = h == 0 ? ri0 : ri1;
@@ -413,25 +469,25 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const __grid_constant
     *reinterpret_cast<uint32_t*>(dst + e) = dev::pack_bf16x2(acc[e] * inv, acc[e + 1] * inv);
 }
 
-template <int D, int RW>
+template <int D, int RW, int KW = 1>
 cudaError_t launch_t(const AttnParams& p, cudaStream_t st) {
   const dim3 grid(p.row_tiles, p.nsplit, p.Hkv);
-  return launch_k(attn_kernel<D, RW>, grid, (RW + 1) * 32, AttnCfg<D>::kSmem, st, p);
+  return launch_k(attn_kernel<D, RW, KW>, grid, (RW * KW + 1) * 32, AttnCfg<D, KW>::kSmem, st, p);
 }
 
 template <int D>
 cudaError_t setup_d() {
   cudaError_t e;
-  e = cudaFuncSetAttribute(attn_kernel<D, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, AttnCfg<D>::kSmem);
+  e = cudaFuncSetAttribute(attn_kernel<D, 1, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize, AttnCfg<D, 4>::kSmem);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(attn_kernel<D, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, AttnCfg<D>::kSmem);
+  e = cudaFuncSetAttribute(attn_kernel<D, 2, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, AttnCfg<D>::kSmem);
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(attn_kernel<D, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize, AttnCfg<D>::kSmem);
+  return cudaFuncSetAttribute(attn_kernel<D, 4, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, AttnCfg<D>::kSmem);
 }
 
 }  // namespace
 
-int attn_smem(int d) { return d == 128 ? AttnCfg<128>::kSmem : AttnCfg<64>::kSmem; }
+int attn_key_warps(int row_warps) { return row_warps == 1 ? 4 : 1; }
 
 cudaError_t attn_setup() {
   cudaError_t e = setup_d<64>();
@@ -439,13 +495,14 @@ cudaError_t attn_setup() {
   return setup_d<128>();
 }
 
+// one row tile (R <= 16): four key-parallel warps; more rows: 2 or 4 row warps
 cudaError_t launch_attention(const AttnParams& p, int d, int row_warps, cudaStream_t st) {
   if (d == 128) {
-    if (row_warps == 1) return launch_t<128, 1>(p, st);
+    if (row_warps == 1) return launch_t<128, 1, 4>(p, st);
     if (row_warps == 2) return launch_t<128, 2>(p, st);
     return launch_t<128, 4>(p, st);
   }
-  if (row_warps == 1) return launch_t<64, 1>(p, st);
+  if (row_warps == 1) return launch_t<64, 1, 4>(p, st);
   if (row_warps == 2) return launch_t<64, 2>(p, st);
   return launch_t<64, 4>(p, st);
 }

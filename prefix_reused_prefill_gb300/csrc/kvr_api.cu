@@ -86,12 +86,15 @@ int max_ldo(const kvr_config* c) {
 
 int attn_row_warps(int R) { return R <= 16 ? 1 : (R <= 32 ? 2 : 4); }
 
+// Key splits of the split-KV kernel: about `target` CTAs, each with at least
+// two 64-key blocks per consumer warp row, or one block per key-parallel warp
+// (one row tile: four warps take alternate blocks, one CTA per SM).
 int attn_nsplit(int Hkv, int R, int kend_max, int target) {
   const int rw = attn_row_warps(R);
   const int rt = (R + 16 * rw - 1) / (16 * rw);
   const int nb = (kend_max + kAttnKeys - 1) / kAttnKeys;
   int ns = (target + Hkv * rt - 1) / (Hkv * rt);
-  ns = std::min(ns, std::max(1, nb / 2));
+  ns = std::min(ns, std::max(1, rw == 1 ? nb / attn_key_warps(rw) : nb / 2));
   return std::max(1, std::min(ns, kMaxSplits));
 }
 
@@ -605,7 +608,8 @@ int attention(kvr_ctx* c, cudaStream_t st, int slot, int layer, const RowMap& ro
   } else {
     const int rw = attn_row_warps(R);
     p.row_tiles = (R + 16 * rw - 1) / (16 * rw);
-    ns = attn_nsplit(k.n_kv_heads, R, kend, kSplitTargetCtas);
+    // key-parallel warps (one row tile) run one CTA per SM: one wave of them
+    ns = attn_nsplit(k.n_kv_heads, R, kend, rw == 1 ? c->n_sms : kSplitTargetCtas);
   }
   while (ns > 1 && (size_t)ns * rows.m * k.n_q_heads * k.head_dim > c->sl.opart_floats) --ns;
   p.nsplit = ns;
@@ -663,10 +667,12 @@ int attention_batch(kvr_ctx* c, cudaStream_t st, int layer, const RowMap& rows, 
   }
   p.n_conv = nbs;
   p.row_tiles = tiles;
-  const int ns = std::max(1, (kSplitTargetCtas + k.n_kv_heads * tiles - 1) / (k.n_kv_heads * tiles));
+  const int target = rw == 1 ? c->n_sms : kSplitTargetCtas;
+  const int ns = std::max(1, (target + k.n_kv_heads * tiles - 1) / (k.n_kv_heads * tiles));
   for (int i = 0; i < nbs; ++i) {
     const int nb = (p.conv[i].P + p.conv[i].m + kAttnKeys - 1) / kAttnKeys;
-    p.conv[i].nsplit = std::max(1, std::min(std::min(ns, std::max(1, nb / 2)), kMaxSplits));
+    const int cap = rw == 1 ? nb / attn_key_warps(rw) : nb / 2;
+    p.conv[i].nsplit = std::max(1, std::min(std::min(ns, std::max(1, cap)), kMaxSplits));
   }
   // the partials of every split conversation must fit the scratch
   auto need = [&]() {

@@ -277,7 +277,7 @@ cudaError_t launch_epi_cast(const float* part, long long plane, int ksplit, int 
 
 // dynamic shared memory the launchers need (for cudaFuncSetAttribute at setup)
 int gemv_int4_smem(int nt);
-int attn_smem(int d);
+int attn_key_warps(int row_warps);   // consumer warps per row tile taking alternate key blocks
 cudaError_t gemv_setup();
 cudaError_t gemm_tc_setup();
 cudaError_t attn_setup();
