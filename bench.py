@@ -542,13 +542,15 @@ def run_crossover(args):
     table = []
     clocks = ClockSampler(torch.cuda.current_device())
     clocks.start()
-    for P in (512, 2048, 8192, 15360):
+    Ps = [int(v) for v in args.crossover_p.split(",")] if args.crossover_p else (512, 2048, 8192, 15360)
+    ms_list = [int(v) for v in args.crossover_m.split(",")] if args.crossover_m else (1, 4, 16, 64, 256, 1024)
+    for P in Ps:
         kk, vv = workloads.random_kv(Hkv, P, d, seed + P)
         k, v = kv.kvr_slot_kv(3, 0)
         k[:, :P] = kk.to(device)
         v[:, :, :P] = vv.transpose(1, 2).to(device)
         kv.kvr_slot_assign(3, list(range(P)))
-        for m in (1, 4, 16, 64, 256, 1024):
+        for m in ms_list:
             new = list(range(40000, 40000 + m))
             x = workloads.hidden_for_tokens(new, shape.hidden, seed).to(device)
             out = torch.empty((m, shape.hidden), dtype=torch.bfloat16, device=device)
@@ -676,6 +678,8 @@ def main():
                     help="turn9 is the bench line; the others print their own measurement line")
     ap.add_argument("--format", default="int4", choices=["int4", "q4k"],
                     help="weight format of the turn9 and verify workloads")
+    ap.add_argument("--crossover-p", default="", help="crossover: cached lengths to run (comma-separated)")
+    ap.add_argument("--crossover-m", default="", help="crossover: row counts to run (comma-separated)")
     ap.add_argument("--layers", type=int, default=0,
                     help="profiling aid: run a reduced stack of this many layers")
     args = ap.parse_args()

@@ -424,6 +424,25 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const __grid_constant
   const int lane = threadIdx.x & 31;
   constexpr int E = D / 32;
   static_assert(kMaxSplits <= 64, "two split records per lane");
+  const float* src = opart + rowidx * D + lane * E;
+  const long long sstride = rows * D;
+  // NS splits' slices in flight at a time, added in split order; the first
+  // batch is requested before the split weights are formed
+  float v[NS][E];
+  auto load = [&](int s0) {
+#pragma unroll
+    for (int j = 0; j < NS; ++j)
+      if (s0 + j < ns) {
+        if (E == 4) {
+          const float4 x = __ldcg(reinterpret_cast<const float4*>(src + (s0 + j) * sstride));
+          v[j][0] = x.x; v[j][1 % E] = x.y; v[j][2 % E] = x.z; v[j][3 % E] = x.w;
+        } else {
+          const float2 x = __ldcg(reinterpret_cast<const float2*>(src + (s0 + j) * sstride));
+          v[j][0] = x.x; v[j][1 % E] = x.y;
+        }
+      }
+  };
+  load(0);
   const float2 ml0 = lane < ns ? mlp[lane * rows + rowidx] : make_float2(-INFINITY, 0.f);
   const float2 ml1 = lane + 32 < ns ? mlp[(lane + 32) * rows + rowidx] : make_float2(-INFINITY, 0.f);
   float M = fmaxf(ml0.x, ml1.x);
@@ -437,22 +456,8 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const __grid_constant
   float acc[E];
 #pragma unroll
   for (int e = 0; e < E; ++e) acc[e] = 0.f;
-  const float* src = opart + rowidx * D + lane * E;
-  const long long sstride = rows * D;
-  // NS splits' slices in flight at a time, added in split order
   for (int s0 = 0; s0 < ns; s0 += NS) {
-    float v[NS][E];
-#pragma unroll
-    for (int j = 0; j < NS; ++j)
-      if (s0 + j < ns) {
-        if (E == 4) {
-          const float4 x = __ldcg(reinterpret_cast<const float4*>(src + (s0 + j) * sstride));
-          v[j][0] = x.x; v[j][1 % E] = x.y; v[j][2 % E] = x.z; v[j][3 % E] = x.w;
-        } else {
-          const float2 x = __ldcg(reinterpret_cast<const float2*>(src + (s0 + j) * sstride));
-          v[j][0] = x.x; v[j][1 % E] = x.y;
-        }
-      }
+    if (s0 > 0) load(s0);
 #pragma unroll
     for (int j = 0; j < NS; ++j)
       if (s0 + j < ns) {

@@ -208,6 +208,7 @@ struct kvr_ctx {
   bool prof = false;
   float* trace = nullptr;   // [n_layers + 1][max_rows][hidden] float32, or null
   bool force_gemv = false;  // KVR_FORCE_GEMV=1: keep every m on the GEMV path
+  bool force_gemm = false;  // KVR_FORCE_GEMM=1: every m on the tcgen05 GEMM (a GEMV-free process)
   int attn_splits = 0;      // KVR_ATTN_SPLITS=n: fixed key-split count of the tcgen05 attention
   std::vector<EventPair> pending;
   std::vector<cudaEvent_t> free_events;
@@ -514,7 +515,7 @@ int project(kvr_ctx* c, cudaStream_t st, const Seg* segs, int nseg, Act act, int
   const kvr_config& cfg = c->cfg;
   const CUtensorMap* tmx = act == Act::A ? c->tm_a : (act == Act::O ? c->tm_o : c->tm_z);
   if (packed4(cfg)) {
-    if (m > kGemvMaxCols && !c->force_gemv)
+    if ((m > kGemvMaxCols || c->force_gemm) && !c->force_gemv)
       return project_gemm(c, st, segs, nseg, tmx, K, m, swiglu, epi);
     return project_gemv_int4(c, st, segs, nseg, tmx, K, m, fz);
   }
@@ -1027,6 +1028,8 @@ int kvr_ctx_create(const kvr_config* cfg, void* kv_arena, size_t arena_bytes, vo
   }
   const char* fg = getenv("KVR_FORCE_GEMV");
   c->force_gemv = fg && fg[0] == '1';
+  const char* fm = getenv("KVR_FORCE_GEMM");
+  c->force_gemm = fm && fm[0] == '1';
   const char* as = getenv("KVR_ATTN_SPLITS");
   c->attn_splits = as ? atoi(as) : 0;
   c->requested = cfg->n_slots;

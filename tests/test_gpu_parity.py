@@ -118,6 +118,26 @@ def test_suffix_prefill_matches_oracle(shape_name, P, ms, cap):
     assert kv.kvr_slot_len(0) == P + ms[-1]
 
 
+@pytest.mark.parametrize("shape_name", ["small", "small_q4k"])
+def test_small_m_on_the_tensor_core_gemm_matches_oracle(monkeypatch, shape_name):
+    """KVR_FORCE_GEMM=1 sends every m to the tcgen05 GEMM (N = 16 for up to 16 rows)."""
+    monkeypatch.setenv("KVR_FORCE_GEMM", "1")
+    shape, kv, w, W, _ = make(shape_name, 2, 256, 64)
+    monkeypatch.delenv("KVR_FORCE_GEMM")
+    dims = oracle_dims(shape)
+    toks = list(range(900, 900 + 60))
+    x = hidden(toks, shape)
+    cache = om.SlotKV(shape.n_layers, shape.n_kv_heads, 256, shape.head_dim)
+    whole = om.prefill(dims, W, cache, workloads.bf16_to_f64(x), 0)
+    kv.kvr_slot_match(toks[:40])
+    kv.kvr_prefill_suffix(0, toks[:40], x[:40].cuda(), w)
+    for m in (1, 5, 17):
+        kv.kvr_slot_truncate(0, 40)
+        out = kv.kvr_prefill_suffix(0, toks[40:40 + m], x[40:40 + m].cuda(), w)
+        kv.kvr_sync_status()
+        close(workloads.bf16_to_f64(out), whole[40:40 + m], f"{shape_name} m={m} on the GEMM")
+
+
 def test_verify_then_truncate_equals_single_steps():
     shape, kv, w, W, _ = make("small", 2, 256, 64)
     dims = oracle_dims(shape)
