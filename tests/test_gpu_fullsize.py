@@ -185,6 +185,47 @@ def test_q4k_full_size_turn9_then_verify():
     kv.close()
 
 
+def test_batch_full_size_four_conversations():
+    """The batched-verify shape: 4 conversations of 4096 cached tokens (36 layers,
+    H 4096), one or three rows each in one kvr_prefill_batch call; every
+    conversation's rows against the oracle at the first and last layers."""
+    shape = workloads.SHAPES["dense9b"]
+    seed = workloads.config_seed(3)
+    tks = [workloads.verify_tokens(seed + 17 * j) for j in range(4)]
+    lws = workloads.stack_weights(shape, seed, device="cuda")
+    kv = make_ctx(shape, 4, 4160, 256)
+    w = kv.weights(lws)
+    for j in range(4):
+        prefill_chunks(kv, j, tks[j]["state"], shape, seed + j, w)
+    lens = [1, 3, 1, 3]
+    rows_tok = [tks[j]["draft"][:lens[j]] for j in range(4)]
+    x = torch.cat([workloads.hidden_for_tokens(t, shape.hidden, seed + j) for j, t in enumerate(rows_tok)])
+    trace = torch.zeros((shape.n_layers + 1, 256, shape.hidden), dtype=torch.float32, device="cuda")
+    kv.kvr_trace_set(trace)
+    kv.kvr_prefill_batch([0, 1, 2, 3], rows_tok, x.contiguous().cuda(), w)
+    kv.kvr_sync_status()
+    kv.kvr_trace_set(None)
+    tr = trace.cpu().numpy()
+    dims = oracle_dims(shape)
+    at = 0
+    for j in range(4):
+        assert kv.kvr_slot_len(j) == 4096 + lens[j]
+        for layer in (0, shape.n_layers - 1):
+            W = oracle_layer_weights(lws[layer])
+            K = np.zeros((shape.n_kv_heads, 4096 + lens[j], shape.head_dim))
+            V = np.zeros_like(K)
+            Kp, Vp = slot_prefix(kv, j, layer, 4096)
+            K[:, :4096], V[:, :4096] = Kp, Vp
+            h_in = tr[layer, at:at + lens[j]].astype(np.float64)
+            ref = om.layer_rows(dims, W, h_in, K, V, om.plain_rows(4096, lens[j]), list(range(lens[j])))
+            Kg, Vg = slot_prefix(kv, j, layer, 4096 + lens[j])
+            close(Kg[:, 4096:], K[:, 4096:], f"batch conversation {j} layer {layer} new K")
+            close(Vg[:, 4096:], V[:, 4096:], f"batch conversation {j} layer {layer} new V")
+            close_rows(tr[layer + 1, at:at + lens[j]], ref, f"batch conversation {j} layer {layer}")
+        at += lens[j]
+    kv.close()
+
+
 def test_verify_full_size_then_one_token_short_fix():
     """Config 3: 36 layers, 4096 cached; verify m = 8, keep 1 + 3 accepted, verify m = 1."""
     shape = workloads.SHAPES["dense9b"]
