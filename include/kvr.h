@@ -25,7 +25,11 @@
  *   thinkspread "The economics of speculative decoding", cost model -- the
  *     m = k+1 verify rows run as one batched pass that reads each weight once.
  *   OpenJev "Latency", What changed / Repeated state -- several questions
- *     resume from one checkpoint placed exactly at the end of a shared state.
+ *     resume from one checkpoint placed exactly at the end of a shared state;
+ *     Next -- continuous batching across requests.
+ *   Tempo9 docs: "KV cache spills to disk, by default" (slot spill/restore
+ *     with a configuration hash) and "Models and quantizations" (Q4_K: 256
+ *     weights in 144 bytes).
  *
  * ---------------------------------------------------------------------------
  * Ownership.  The caller allocates every device buffer (the KV arena, the
@@ -33,12 +37,15 @@
  * library makes no device allocation; it owns host state (the slot token
  * lists, lengths, LRU stamps, cached TMA descriptors) and, on each GPU that
  * loads it, the fixed staging array of kvr_slot_match_static.  All calls that take a
- * stream are asynchronous on it, except kvr_slot_match, which waits for the
- * stream to read back the match lengths, and kvr_sync_status.
+ * stream are asynchronous on it, except kvr_slot_match (it waits for the
+ * stream to read back the match lengths), kvr_verify_accept (it returns the
+ * decision to the host) and kvr_sync_status.
  *
  * Errors.  Every int-returning call returns KVR_OK (0) or a negative code;
- * kvr_last_error() says why.  A failed call leaves every slot's length and
- * tokens unchanged and launches nothing (validation precedes any launch).
+ * kvr_last_error() says why.  A call refused by its checks launches nothing
+ * and leaves every slot's length and tokens unchanged (validation precedes
+ * any launch); what a call leaves after a failure past that point is stated
+ * with the call.
  *
  * Threads.  A context is not thread-safe; serialise calls on one context.
  * ---------------------------------------------------------------------------
