@@ -400,6 +400,20 @@ int kvr_verify_accept(kvr_ctx* ctx, int slot, const int32_t* tokens, int m, cons
                       const kvr_layer_weights* weights, const kvr_head_weights* head, void* out,
                       int32_t* next_tokens, int* accepted, void* stream);
 
+/* Greedy verification of several conversations in one call: the rows of
+ * conversation j ([t0, d1 .. dk] of slot slots[j], lens[j] of them, in the
+ * order and layout of kvr_prefill_batch, at most 64 rows in all) run as one
+ * batch, then the output head decides every row.  next_tokens (host, sum of
+ * lens) receives every row's argmax and accepted (host, n_seq) each
+ * conversation's count of accepted drafts; slot slots[j] is cut back to its
+ * length before the call + 1 + accepted[j].  Conversation j's results equal
+ * kvr_verify_accept on its slot alone.  Synchronises the stream.  On an error
+ * after the rows ran every slot keeps its length before the call. */
+int kvr_verify_accept_batch(kvr_ctx* ctx, int n_seq, const int* slots, const int* lens,
+                            const int32_t* tokens, const void* hidden, const kvr_layer_weights* weights,
+                            const kvr_head_weights* head, void* out, int32_t* next_tokens, int* accepted,
+                            void* stream);
+
 /* Self-test of the failure path, without a GPU fault: launches one device
  * wait on an mbarrier that nothing completes.  Like every wait in the
  * library's kernels it gives up after 1 s and records the timeout in the

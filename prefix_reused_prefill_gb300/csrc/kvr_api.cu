@@ -922,6 +922,47 @@ int prefill_common(kvr_ctx* c, int slot, const int32_t* tokens, int m, const voi
   return KVR_OK;
 }
 
+// ---------------------------------------------------------------- output head
+int head_check(kvr_ctx* c, const kvr_head_weights* head, const void* next_tokens, const void* accepted) {
+  const kvr_config& k = c->cfg;
+  if (!head || !next_tokens || !accepted) return fail(c, KVR_ERR_ARG, "null head or result pointer");
+  if (!packed4(k) || k.attn_only)
+    return fail(c, KVR_ERR_UNSUPPORTED, "the output head needs int4 weights and the full decoder layer");
+  if (head->vocab <= 0 || head->vocab > k.vocab)
+    return fail(c, KVR_ERR_ARG, "head vocab %d outside [1, %d] (the configured vocab)", head->vocab, k.vocab);
+  for (const void* q : {head->norm, head->w, head->s})
+    if (!q || (reinterpret_cast<uintptr_t>(q) & 15)) return fail(c, KVR_ERR_ARG, "missing or misaligned head pointer");
+  return KVR_OK;
+}
+
+// logits = a * lm^T over the m normed rows in c->a, each tile's best, each
+// row's argmax, read back to next_tokens; synchronises the stream
+int head_decide(kvr_ctx* c, cudaStream_t st, int m, const kvr_head_weights* head, int32_t* next_tokens) {
+  Seg seg = {head->w, head->s, head->vocab};
+  Fused fz;
+  fz.epi = kGemvEpiArgmax;
+  fz.fmt = kFmtInt4;   // the head is int4 group-32 in every configuration
+  fz.best = c->best;
+  int rc = project_gemv_int4(c, st, &seg, 1, c->tm_a, c->cfg.hidden, m, fz);
+  if (rc) return rc;
+  cudaError_t e;
+  {
+    Timed t(c, kEpi, st);
+    e = launch_head_argmax(c->best, (head->vocab + kGemvRows - 1) / kGemvRows, m, c->next, st);
+  }
+  if (e != cudaSuccess) return cuda_fail(c, e, "head argmax launch");
+  e = cudaMemcpyAsync(next_tokens, c->next, (size_t)m * 4, cudaMemcpyDeviceToHost, st);
+  if (e != cudaSuccess) return cuda_fail(c, e, "next-token readback");
+  return kvr_sync_status(c, st);
+}
+
+// greedy acceptance of one conversation's rows [t0, d1 .. dk]
+int greedy_accept(const int32_t* tokens, const int32_t* next, int m) {
+  int a = 0;
+  while (a + 1 < m && tokens[a + 1] == next[a]) ++a;
+  return a;
+}
+
 // ---------------------------------------------------------------- spill/restore
 struct SpillHeader {
   char magic[8];      // "KVRSLOT1"
@@ -987,6 +1028,54 @@ cudaError_t copy_slot_kv(kvr_ctx* c, int slot, int len, uint8_t* host, bool to_h
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
+}
+
+int batch_common(kvr_ctx* c, int n_seq, const int* slots, const int* lens, const int32_t* tokens,
+                 const void* hidden, const kvr_layer_weights* w, void* out, void* stream, int max_m,
+                 const __nv_bfloat16* head_gain) {
+  if (!c) return KVR_ERR_ARG;
+  if (n_seq < 1 || n_seq > KVR_MAX_BRANCHES || !slots || !lens || !tokens || !hidden || (!out && !head_gain))
+    return fail(c, KVR_ERR_ARG, "bad batch arguments");
+  if (((uintptr_t)hidden & 15) || ((uintptr_t)out & 15)) return fail(c, KVR_ERR_ARG, "hidden/out must be 16-byte aligned");
+  if (!weights_ok(c, w)) return fail(c, KVR_ERR_ARG, "missing or misaligned weight pointer");
+  RowMap rows;
+  memset(&rows, 0, sizeof rows);
+  rows.batch = 1;
+  rows.n_branch = n_seq;
+  int total = 0;
+  for (int j = 0; j < n_seq; ++j) {
+    const int s = slots[j];
+    if (s < 0 || s >= c->granted) return fail(c, KVR_ERR_ARG, "bad slot %d", s);
+    for (int i = 0; i < j; ++i)
+      if (slots[i] == s) return fail(c, KVR_ERR_ARG, "slot %d appears twice in the batch", s);
+    if (lens[j] <= 0) return fail(c, KVR_ERR_ARG, "conversation %d has %d rows", j, lens[j]);
+    rows.slot[j] = s;
+    rows.pre[j] = (int)c->slots[s].tokens.size();
+    rows.off[j] = total;
+    total += lens[j];
+    if (rows.pre[j] + lens[j] > c->cfg.capacity || c->fault == 3)
+      return fail(c, KVR_ERR_CAPACITY, "slot %d: %d + %d rows exceed capacity %d", s, rows.pre[j], lens[j],
+                  c->cfg.capacity);
+  }
+  rows.off[n_seq] = total;
+  rows.m = total;
+  if (total > c->cfg.max_rows) return fail(c, KVR_ERR_CAPACITY, "%d rows exceed max_rows %d", total, c->cfg.max_rows);
+  if (total > max_m) return fail(c, KVR_ERR_ARG, "%d rows exceed %d for this call", total, max_m);
+  if (c->fault == 2) return fail(c, KVR_ERR_FAULT, "injected launch fault");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int rc = run_stack(c, rows, hidden, w, out, st, head_gain);
+  if (rc) return rc;
+  for (int j = 0; j < n_seq; ++j) {
+    rc = upload_tokens(c, slots[j], rows.pre[j], tokens + rows.off[j], lens[j], st);
+    if (rc) return rc;
+  }
+  for (int j = 0; j < n_seq; ++j) {
+    SlotState& S = c->slots[slots[j]];
+    S.occupied = true;
+    S.tokens.insert(S.tokens.end(), tokens + rows.off[j], tokens + rows.off[j + 1]);
+    touch(c, slots[j]);
+  }
+  return KVR_OK;
 }
 
 }  // namespace
@@ -1333,44 +1422,19 @@ int kvr_verify_accept(kvr_ctx* c, int slot, const int32_t* tokens, int m, const 
                       const kvr_layer_weights* w, const kvr_head_weights* head, void* out,
                       int32_t* next_tokens, int* accepted, void* stream) {
   if (!c) return KVR_ERR_ARG;
-  const kvr_config& k = c->cfg;
-  if (!head || !next_tokens || !accepted) return fail(c, KVR_ERR_ARG, "null head or result pointer");
-  if (!packed4(k) || k.attn_only)
-    return fail(c, KVR_ERR_UNSUPPORTED, "the output head needs int4 weights and the full decoder layer");
-  if (head->vocab <= 0 || head->vocab > k.vocab)
-    return fail(c, KVR_ERR_ARG, "head vocab %d outside [1, %d] (the configured vocab)", head->vocab, k.vocab);
-  for (const void* q : {head->norm, head->w, head->s})
-    if (!q || (reinterpret_cast<uintptr_t>(q) & 15)) return fail(c, KVR_ERR_ARG, "missing or misaligned head pointer");
+  int rc = head_check(c, head, next_tokens, accepted);
+  if (rc) return rc;
   if (slot < 0 || slot >= c->granted) return fail(c, KVR_ERR_ARG, "bad slot %d", slot);
   const int p0 = (int)c->slots[slot].tokens.size();
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  int rc = prefill_common(c, slot, tokens, m, hidden, w, out, stream, kVerifyMaxRows,
-                          static_cast<const __nv_bfloat16*>(head->norm));
+  rc = prefill_common(c, slot, tokens, m, hidden, w, out, stream, kVerifyMaxRows,
+                      static_cast<const __nv_bfloat16*>(head->norm));
   if (rc) return rc;
-  // logits = a * lm^T (a = the normed rows), each tile's best, then each row's
-  Seg seg = {head->w, head->s, head->vocab};
-  Fused fz;
-  fz.epi = kGemvEpiArgmax;
-  fz.fmt = kFmtInt4;   // the head is int4 group-32 in every configuration
-  fz.best = c->best;
-  rc = project_gemv_int4(c, st, &seg, 1, c->tm_a, k.hidden, m, fz);
-  cudaError_t e = cudaSuccess;
-  if (!rc) {
-    Timed t(c, kEpi, st);
-    e = launch_head_argmax(c->best, (head->vocab + kGemvRows - 1) / kGemvRows, m, c->next, st);
-    if (e != cudaSuccess) rc = cuda_fail(c, e, "head argmax launch");
-  }
-  if (!rc) {
-    e = cudaMemcpyAsync(next_tokens, c->next, (size_t)m * 4, cudaMemcpyDeviceToHost, st);
-    if (e != cudaSuccess) rc = cuda_fail(c, e, "next-token readback");
-  }
-  if (!rc) rc = kvr_sync_status(c, stream);
+  rc = head_decide(c, static_cast<cudaStream_t>(stream), m, head, next_tokens);
   if (rc) {
     c->slots[slot].tokens.resize(p0);
     return rc;
   }
-  int a = 0;
-  while (a + 1 < m && tokens[a + 1] == next_tokens[a]) ++a;
+  const int a = greedy_accept(tokens, next_tokens, m);
   *accepted = a;
   c->slots[slot].tokens.resize(p0 + 1 + a);
   return KVR_OK;
@@ -1410,46 +1474,36 @@ int kvr_prefill_branches(kvr_ctx* c, int slot, int n_branch, const int* lens, co
 
 int kvr_prefill_batch(kvr_ctx* c, int n_seq, const int* slots, const int* lens, const int32_t* tokens,
                       const void* hidden, const kvr_layer_weights* w, void* out, void* stream) {
+  return batch_common(c, n_seq, slots, lens, tokens, hidden, w, out, stream, 1 << 30, nullptr);
+}
+
+int kvr_verify_accept_batch(kvr_ctx* c, int n_seq, const int* slots, const int* lens, const int32_t* tokens,
+                            const void* hidden, const kvr_layer_weights* w, const kvr_head_weights* head,
+                            void* out, int32_t* next_tokens, int* accepted, void* stream) {
   if (!c) return KVR_ERR_ARG;
-  if (n_seq < 1 || n_seq > KVR_MAX_BRANCHES || !slots || !lens || !tokens || !hidden || !out)
-    return fail(c, KVR_ERR_ARG, "bad batch arguments");
-  if (((uintptr_t)hidden & 15) || ((uintptr_t)out & 15)) return fail(c, KVR_ERR_ARG, "hidden/out must be 16-byte aligned");
-  if (!weights_ok(c, w)) return fail(c, KVR_ERR_ARG, "missing or misaligned weight pointer");
-  RowMap rows;
-  memset(&rows, 0, sizeof rows);
-  rows.batch = 1;
-  rows.n_branch = n_seq;
-  int total = 0;
-  for (int j = 0; j < n_seq; ++j) {
-    const int s = slots[j];
-    if (s < 0 || s >= c->granted) return fail(c, KVR_ERR_ARG, "bad slot %d", s);
-    for (int i = 0; i < j; ++i)
-      if (slots[i] == s) return fail(c, KVR_ERR_ARG, "slot %d appears twice in the batch", s);
-    if (lens[j] <= 0) return fail(c, KVR_ERR_ARG, "conversation %d has %d rows", j, lens[j]);
-    rows.slot[j] = s;
-    rows.pre[j] = (int)c->slots[s].tokens.size();
-    rows.off[j] = total;
-    total += lens[j];
-    if (rows.pre[j] + lens[j] > c->cfg.capacity || c->fault == 3)
-      return fail(c, KVR_ERR_CAPACITY, "slot %d: %d + %d rows exceed capacity %d", s, rows.pre[j], lens[j],
-                  c->cfg.capacity);
-  }
-  rows.off[n_seq] = total;
-  rows.m = total;
-  if (total > c->cfg.max_rows) return fail(c, KVR_ERR_CAPACITY, "%d rows exceed max_rows %d", total, c->cfg.max_rows);
-  if (c->fault == 2) return fail(c, KVR_ERR_FAULT, "injected launch fault");
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  int rc = run_stack(c, rows, hidden, w, out, st);
+  int rc = head_check(c, head, next_tokens, accepted);
   if (rc) return rc;
+  if (n_seq < 1 || n_seq > KVR_MAX_BRANCHES || !slots || !lens) return fail(c, KVR_ERR_ARG, "bad batch arguments");
+  int p0[KVR_MAX_BRANCHES];
   for (int j = 0; j < n_seq; ++j) {
-    rc = upload_tokens(c, slots[j], rows.pre[j], tokens + rows.off[j], lens[j], st);
-    if (rc) return rc;
+    if (slots[j] < 0 || slots[j] >= c->granted) return fail(c, KVR_ERR_ARG, "bad slot %d", slots[j]);
+    p0[j] = (int)c->slots[slots[j]].tokens.size();
   }
+  rc = batch_common(c, n_seq, slots, lens, tokens, hidden, w, out, stream, kVerifyMaxRows,
+                    static_cast<const __nv_bfloat16*>(head->norm));
+  if (rc) return rc;
+  int total = 0;
+  for (int j = 0; j < n_seq; ++j) total += lens[j];
+  rc = head_decide(c, static_cast<cudaStream_t>(stream), total, head, next_tokens);
+  if (rc) {
+    for (int j = 0; j < n_seq; ++j) c->slots[slots[j]].tokens.resize(p0[j]);
+    return rc;
+  }
+  int at = 0;
   for (int j = 0; j < n_seq; ++j) {
-    SlotState& S = c->slots[slots[j]];
-    S.occupied = true;
-    S.tokens.insert(S.tokens.end(), tokens + rows.off[j], tokens + rows.off[j + 1]);
-    touch(c, slots[j]);
+    accepted[j] = greedy_accept(tokens + at, next_tokens + at, lens[j]);
+    c->slots[slots[j]].tokens.resize(p0[j] + 1 + accepted[j]);
+    at += lens[j];
   }
   return KVR_OK;
 }

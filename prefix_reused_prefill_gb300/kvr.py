@@ -29,7 +29,7 @@ EXPORTED = ["kvr_arena_bytes", "kvr_scratch_bytes", "kvr_ctx_create", "kvr_ctx_i
             "kvr_profile_launches",
             "kvr_last_error", "kvr_slot_match_static", "kvr_trace_set", "kvr_verify_accept",
             "kvr_config_hash", "kvr_slot_spill_bytes", "kvr_slot_spill", "kvr_slot_restore",
-            "kvr_prefill_batch", "kvr_selftest_wait"]
+            "kvr_prefill_batch", "kvr_selftest_wait", "kvr_verify_accept_batch"]
 
 
 class KvrError(RuntimeError):
@@ -98,6 +98,8 @@ def load_library(path: str = LIB_PATH):
         "kvr_slot_match_static": (I, [V, i32p, I, P(I), P(I), V]),
         "kvr_trace_set": (I, [V, V, Z]),
         "kvr_selftest_wait": (I, [V, V]),
+        "kvr_verify_accept_batch": (I, [V, I, P(I), P(I), i32p, V, P(KvrLayerWeights), P(KvrHeadWeights), V,
+                                        i32p, P(I), V]),
         "kvr_config_hash": (ctypes.c_uint64, [P(KvrConfig), ctypes.c_uint64]),
         "kvr_slot_spill_bytes": (Z, [V, I]),
         "kvr_slot_spill": (I, [V, I, ctypes.c_uint64, V, Z, V]),
@@ -290,6 +292,30 @@ class Kvr:
                                                ctypes.byref(hs), _ptr(out), nxt, ctypes.byref(acc),
                                                self._stream(stream)))
         return list(nxt[:m]), acc.value
+
+    def kvr_verify_accept_batch(self, slots, token_lists, hidden, weights, head, out=None, stream=None):
+        """Greedy verification of conversation j's rows token_lists[j] on slot
+        slots[j], all in one call.  Returns (per conversation: the argmax of
+        each of its rows, the drafts kept)."""
+        arr = weights[0] if isinstance(weights, tuple) else weights
+        hs, _keep = head_weight_struct(head)
+        lens = [len(t) for t in token_lists]
+        m = sum(lens)
+        assert hidden.dtype == torch.bfloat16 and hidden.is_cuda and hidden.is_contiguous()
+        assert hidden.shape == (m, self.cfg.hidden)
+        n = len(slots)
+        slots_c = (ctypes.c_int * max(n, 1))(*[int(s) for s in slots])
+        lens_c = (ctypes.c_int * max(n, 1))(*lens)
+        nxt = (ctypes.c_int32 * max(m, 1))()
+        acc = (ctypes.c_int * max(n, 1))()
+        self._check(self.lib.kvr_verify_accept_batch(self.ctx, n, slots_c, lens_c, _i32(sum(token_lists, [])),
+                                                     hidden.data_ptr(), arr, ctypes.byref(hs), _ptr(out),
+                                                     nxt, acc, self._stream(stream)))
+        out_next, at = [], 0
+        for L in lens:
+            out_next.append(list(nxt[at:at + L]))
+            at += L
+        return out_next, list(acc[:n])
 
     def kvr_prefill_batch(self, slots, token_lists, hidden, weights, out=None, stream=None):
         """Conversation j's rows token_lists[j] (hidden rows concatenated in the

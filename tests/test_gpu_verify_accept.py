@@ -47,11 +47,11 @@ def head_for(shape, vocab, seed):
     return dev, gain.to(torch.float64).numpy(), formats.dequant_int4(lm.packed.numpy(), lm.scales.numpy())
 
 
-def make(shape_name, cap, max_rows, vocab, seed=21):
+def make(shape_name, cap, max_rows, vocab, seed=21, n_slots=2):
     from prefix_reused_prefill_gb300 import Kvr, config_for_shape
     shape = workloads.SHAPES[shape_name]
     lws = workloads.stack_weights(shape, seed)
-    kv = Kvr(config_for_shape(shape, 2, cap, max_rows, vocab=vocab), device="cuda")
+    kv = Kvr(config_for_shape(shape, n_slots, cap, max_rows, vocab=vocab), device="cuda")
     w = kv.weights(workloads.weights_to(lws, "cuda"))
     W = [oracle_weights(shape, lw) for lw in lws]
     return shape, kv, w, W
@@ -200,3 +200,37 @@ def test_verify_accept_refuses_bad_heads():
     assert kv.kvr_slot_len(0) == 3
     nxt, acc = kv.kvr_verify_accept(0, [4, 5], x, w, head)
     assert kv.kvr_slot_len(0) == 3 + 1 + acc and len(nxt) == 2
+
+
+def test_batched_verify_accept_matches_each_conversation():
+    """Three conversations in one kvr_verify_accept_batch call: every row's
+    decision, each acceptance count and each slot's kept tokens as the oracle
+    gives them for the conversation alone."""
+    vocab = 1000
+    shape, kv, w, W = make("small", 256, 128, vocab, n_slots=3)
+    dims = oracle_dims(shape)
+    head, gain, lm = head_for(shape, vocab, 33)
+    xseed = 7
+    plan = [(2, 41, 5, 2), (0, 60, 1, 0), (1, 23, 4, 3)]   # (slot, P, m, a)
+    toks_all, logits_all, prefixes = [], [], []
+    for slot, P, m, a in plan:
+        prefix = list(range(100 * (slot + 1), 100 * (slot + 1) + P))
+        xp = workloads.hidden_for_tokens(prefix, shape.hidden, xseed)
+        base = om.SlotKV(shape.n_layers, shape.n_kv_heads, 256, shape.head_dim)
+        om.prefill(dims, W, base, workloads.bf16_to_f64(xp), 0)
+        for t0 in range(700 + 50 * slot, 900 + 50 * slot):
+            toks, logits = oracle_chain(dims, W, _copy_kv(base), P, t0, m, a, gain, lm, xseed)
+            if clear(toks, logits, a):
+                break
+        else:
+            pytest.fail("no draft chain with clear decisions")
+        kv.kvr_prefill_suffix(slot, prefix, xp.cuda(), w)
+        toks_all.append(toks)
+        logits_all.append(logits)
+        prefixes.append(prefix)
+    x = torch.cat([workloads.hidden_for_tokens(t, shape.hidden, xseed) for t in toks_all]).contiguous()
+    nxt, acc = kv.kvr_verify_accept_batch([p[0] for p in plan], toks_all, x.cuda(), w, head)
+    for (slot, P, m, a), toks, logits, prefix, n, got in zip(plan, toks_all, logits_all, prefixes, nxt, acc):
+        check_rows(n, logits, f"batched slot {slot}")
+        assert got == min(a, m - 1)
+        assert kv.kvr_slot_tokens(slot) == prefix + toks[:1 + got]
