@@ -495,8 +495,9 @@ def run_batch(args):
     tks = [workloads.verify_tokens(seed + 17 * j) for j in range(n)]
     P = len(tks[0]["state"])
     lws = workloads.stack_weights(shape, seed, device=device)
-    kv = Kvr(config_for_shape(shape, n, P + 256, 256), device=device)
+    kv = Kvr(config_for_shape(shape, n, P + 256, 256, vocab=workloads.VOCAB), device=device)
     w = kv.weights(lws)
+    head = workloads.head_weights(shape, seed, device=device)
     for j in range(n):
         _prefill_state(kv, j, tks[j]["state"], shape, seed + j, w, device)
     L = shape.n_layers
@@ -520,6 +521,10 @@ def run_batch(args):
             for j in range(n):
                 kv.kvr_verify(j, drafts[j], xs[j], w, out=outs[j])
         ms_s = _event_ms(separate, args.steps, args.warmup, after=cut)
+        # the same rows with the greedy decision for every conversation (one call,
+        # read back to the host)
+        ms_acc = _event_ms(lambda: kv.kvr_verify_accept_batch(list(range(n)), drafts, xall, w, head, out=out),
+                           args.steps, args.warmup, after=cut)
         kv.kvr_sync_status()
         nbytes = (shape.params_per_layer() * 0.5625 * L
                   + n * (P + m) * shape.n_kv_heads * shape.head_dim * 2 * 2 * L
@@ -527,6 +532,7 @@ def run_batch(args):
         gbs = nbytes / (ms_b / 1e3) / 1e9
         table.append({"m_per_conversation": m, "rows": n * m, "ms_batched": round(ms_b, 4),
                       "ms_separate_4_calls": round(ms_s, 4), "speedup": round(ms_s / ms_b, 3),
+                      "accept_batch_ms": round(ms_acc, 4),
                       "rows_per_s_batched": round(n * m / (ms_b / 1e3), 1),
                       "algorithmic_gb": round(nbytes / 1e9, 4), "gbs": round(gbs, 1),
                       "frac_hbm": round(gbs / pk["hbm_gbs"], 4)})
