@@ -20,7 +20,8 @@
 //   * the unscaled group product sum_k code*x runs on the tensor cores with an
 //     fp32 accumulator, and the fp16 group scale is applied afterwards in fp32:
 //     acc += scale * group_sum.  The weight is therefore exactly code*scale,
-//     never rounded to bf16.
+//     never rounded to bf16.  (K-quant codes stay biased, 128 + q: the offset
+//     folds into the sub-block's min term, which is formed anyway.)
 // Plain CUDA-core FMAs would need 32*m FMAs per 16 weight bytes, more than the
 // SM issues at HBM rate once m > 2; the tensor cores keep the kernel HBM-bound.
 //
@@ -67,17 +68,23 @@ struct GemvCfg {
 // 8 4-bit fields of one 32-bit word -> 4 bf16x2 registers holding field - OFF
 // (OFF = 8: the signed int4 code; 0: the unsigned K-quant code).
 // Register i holds fields i (low half) and i+4 (high half).
-template <int OFF>
-__device__ __forceinline__ void dequant_word(uint32_t w, uint32_t r[4]) {
+// 8 4-bit fields of one 32-bit word -> 4 bf16x2 registers holding 128 + field
+// (exact bf16 integers).  Register i holds fields i (low half) and i+4 (high
+// half).
+__device__ __forceinline__ void biased_word(uint32_t w, uint32_t r[4]) {
   const uint32_t magic = 0x43004300u;  // bf16 128.0 in both halves
-  const __nv_bfloat162 bias = __floats2bfloat162_rn(128.0f + OFF, 128.0f + OFF);
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r[i]) : "r"(w >> (4 * i)), "r"(0x000F000Fu), "r"(magic));
+}
+
+// the same fields as signed int4 codes: 128 + field - 136 = code
+__device__ __forceinline__ void code_word(uint32_t w, uint32_t r[4]) {
+  const __nv_bfloat162 bias = __floats2bfloat162_rn(136.0f, 136.0f);
+  biased_word(w, r);
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    uint32_t v;
-    const uint32_t s = w >> (4 * i);
-    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(v) : "r"(s), "r"(0x000F000Fu), "r"(magic));
-    __nv_bfloat162 h = *reinterpret_cast<__nv_bfloat162*>(&v);
-    h = __hsub2(h, bias);
+    __nv_bfloat162 h = __hsub2(*reinterpret_cast<__nv_bfloat162*>(&r[i]), bias);
     r[i] = *reinterpret_cast<uint32_t*>(&h);
   }
 }
@@ -91,10 +98,13 @@ __device__ __forceinline__ uint32_t q4k_field(const uint4& r, int f) {
   return (off > 26 && word < 2 ? __funnelshift_r(lo, hi, off) : lo >> off) & 63u;
 }
 
+// (a, c) = (d*sc_g, 128*d*sc_g + dmin*mn_g): with the biased codes 128 + q on
+// the tensor cores, sum(w x) = a * sum((128 + q) x) - c * sum(x)
 __device__ __forceinline__ float2 q4k_ab(const uint4& r, int g) {
   const float d = __half2float(__ushort_as_half((unsigned short)(r.x & 0xFFFFu)));
   const float dmin = __half2float(__ushort_as_half((unsigned short)(r.x >> 16)));
-  return make_float2(d * (float)q4k_field(r, g), dmin * (float)q4k_field(r, 8 + g));
+  const float a = d * (float)q4k_field(r, g);
+  return make_float2(a, fmaf(128.f, a, dmin * (float)q4k_field(r, 8 + g)));
 }
 
 // barrier of the eight consumer warps (the producer warp has left)
@@ -376,10 +386,10 @@ __global__ void __launch_bounds__(kThreads, NT == 4 ? 1 : 2) gemv_int4_kernel(co
       const uint32_t xt = wt + kWTileBytes;
       const uint32_t stile = xt + C::kXTileBytes;
       if constexpr (FMT == kFmtQ4K) {
-        // one superblock per row and stage: the warp decodes (d*sc, dmin*mn)
-        // of its 16 rows x 8 sub-blocks once, then per sub-block
-        //   acc += d*sc * sum(q x) - dmin*mn * sum(x)
-        // with both sums on the tensor cores (q exact in bf16, A = 1 for sum(x))
+        // one superblock per row and stage: the warp decodes (a, c) of its 16
+        // rows x 8 sub-blocks once, then per sub-block
+        //   acc += a * sum((128 + q) x) - c * sum(x)
+        // with both sums on the tensor cores (128 + q exact in bf16, A = 1 for sum(x))
         float2* tab = q4k_tab + warp * 128;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
@@ -394,8 +404,8 @@ __global__ void __launch_bounds__(kThreads, NT == 4 ? 1 : 2) gemv_int4_kernel(co
           const uint32_t w0 = dev::lds32(wt + dev::swz128(rho0, g) + 4 * c);
           const uint32_t w1 = dev::lds32(wt + dev::swz128(rho0 + 8, g) + 4 * c);
           uint32_t q0[4], q1[4];
-          dequant_word<0>(w0, q0);
-          dequant_word<0>(w1, q1);
+          biased_word(w0, q0);
+          biased_word(w1, q1);
           const uint32_t a_lo[4] = {q0[0], q1[0], q0[1], q1[1]};
           const uint32_t a_hi[4] = {q0[2], q1[2], q0[3], q1[3]};
           const float2 ab0 = tab[r * 8 + g], ab1 = tab[(r + 8) * 8 + g];
@@ -419,6 +429,8 @@ __global__ void __launch_bounds__(kThreads, NT == 4 ? 1 : 2) gemv_int4_kernel(co
           }
         }
       } else {
+      // (removing the offset with two extra MMAs instead of the subtraction
+      // measured slower here: the MMA issue, not the ALU, is the tighter limit)
       const uint4 sc0 = dev::lds128(stile + rho0 * 16);
       const uint4 sc1 = dev::lds128(stile + (rho0 + 8) * 16);
       const __half* s0h = reinterpret_cast<const __half*>(&sc0);
@@ -428,8 +440,8 @@ __global__ void __launch_bounds__(kThreads, NT == 4 ? 1 : 2) gemv_int4_kernel(co
         const uint32_t w0 = dev::lds32(wt + dev::swz128(rho0, g) + 4 * c);
         const uint32_t w1 = dev::lds32(wt + dev::swz128(rho0 + 8, g) + 4 * c);
         uint32_t q0[4], q1[4];
-        dequant_word<8>(w0, q0);
-        dequant_word<8>(w1, q1);
+        code_word(w0, q0);
+        code_word(w1, q1);
         const uint32_t a_lo[4] = {q0[0], q1[0], q0[1], q1[1]};  // inputs 0..15 of the group
         const uint32_t a_hi[4] = {q0[2], q1[2], q0[3], q1[3]};  // inputs 16..31
         const float sr0 = __half2float(s0h[g]);
