@@ -388,22 +388,24 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         const int la = min(max(lo - key0, 0), 64);
         const int hb = tok >= 0 ? min(max(hi - key0 + 1, 0), 64) : 0;
         float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        // raw scores here; the log2-domain scale is applied inside the
+        // exponent's FMA below (the scale is positive, so the max commutes)
         if (tok >= 0 && pe == 64) {
           // wholly inside the cached prefix: every key visible
 #pragma unroll
           for (int k = 0; k < 64; ++k) {
-            sv[k] = __uint_as_float(sr[k]) * p.scale_log2;
+            sv[k] = __uint_as_float(sr[k]);
             m4[k & 3] = fmaxf(m4[k & 3], sv[k]);
           }
         } else {
 #pragma unroll
           for (int k = 0; k < 64; ++k) {
             const bool vis = tok >= 0 && (k < pe || (k >= la && k < hb));
-            sv[k] = vis ? __uint_as_float(sr[k]) * p.scale_log2 : -INFINITY;
+            sv[k] = vis ? __uint_as_float(sr[k]) : -INFINITY;
             m4[k & 3] = fmaxf(m4[k & 3], sv[k]);
           }
         }
-        mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+        mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * p.scale_log2;
       }
       // the row's block max from both halves; after this barrier both halves
       // have read their S, so P may overwrite the buffer
@@ -420,7 +422,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       float s4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int k = 0; k < 64; k += 2) {
-        const float e0 = ex2_approx(sv[k] - muse), e1 = ex2_approx(sv[k + 1] - muse);
+        const float e0 = ex2_approx(fmaf(sv[k], p.scale_log2, -muse));
+        const float e1 = ex2_approx(fmaf(sv[k + 1], p.scale_log2, -muse));
         s4[(k >> 1) & 3] += e0 + e1;
         pk[k / 2] = dev::pack_bf16x2(e0, e1);
       }
