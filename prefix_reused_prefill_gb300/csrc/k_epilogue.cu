@@ -52,7 +52,7 @@ __global__ void rope_table_kernel(RowMap rows, int d, double theta, float2* tabl
 }
 
 __global__ void embed_kernel(const __nv_bfloat16* hidden, int H, const __nv_bfloat16* gain,
-                             float eps, float* h, __nv_bfloat16* a) {
+                             float eps, float* h, __nv_bfloat16* a, float* ss_out, int nss) {
   dev::pdl_trigger();
   dev::pdl_wait();
   __shared__ float red[32];
@@ -62,48 +62,16 @@ __global__ void embed_kernel(const __nv_bfloat16* hidden, int H, const __nv_bflo
     const float v = __bfloat162float(hidden[row * H + k]);
     h[row * H + k] = v;
     ss += v * v;
+    if (ss_out) a[row * H + k] = __float2bfloat16_rn(v * __bfloat162float(gain[k]));
   }
-  const float rs = rsqrtf(block_sum(ss, red) / H + eps);
+  const float sum = block_sum(ss, red);
+  if (ss_out) {
+    for (int j = threadIdx.x; j < nss; j += blockDim.x) ss_out[row * nss + j] = j == 0 ? sum : 0.f;
+    return;
+  }
+  const float rs = rsqrtf(sum / H + eps);
   for (int k = threadIdx.x; k < H; k += blockDim.x)
     a[row * H + k] = __float2bfloat16_rn(h[row * H + k] * rs * __bfloat162float(gain[k]));
-}
-
-// One CTA per token row: a = bf16(h * rsqrt(mean(h^2) + eps) * gain) over a
-// finished residual-stream row (the small-m path, where the GEMV epilogue has
-// already added the projection to h).  float4 accesses, the row in registers.
-template <int V>  // float4 per thread (H <= 4 * 256 * V)
-__global__ void __launch_bounds__(256) rmsnorm_kernel(const float* h, int c0, int H,
-                                                      const __nv_bfloat16* gain, float eps,
-                                                      __nv_bfloat16* a) {
-  dev::pdl_trigger();
-  dev::pdl_wait();
-  __shared__ float red[32];
-  const long long i = c0 + blockIdx.x;
-  const int H4 = H >> 2;
-  float4 v[V];
-  float ss = 0.f;
-#pragma unroll
-  for (int u = 0; u < V; ++u) {
-    const int k4 = threadIdx.x + u * 256;
-    if (k4 < H4) {
-      v[u] = reinterpret_cast<const float4*>(h + i * H)[k4];
-      ss += v[u].x * v[u].x + v[u].y * v[u].y + v[u].z * v[u].z + v[u].w * v[u].w;
-    }
-  }
-  const float rs = rsqrtf(block_sum(ss, red) / H + eps);
-#pragma unroll
-  for (int u = 0; u < V; ++u) {
-    const int k4 = threadIdx.x + u * 256;
-    if (k4 < H4) {
-      const uint2 gw = reinterpret_cast<const uint2*>(gain)[k4];
-      const __nv_bfloat162 g01 = *reinterpret_cast<const __nv_bfloat162*>(&gw.x);
-      const __nv_bfloat162 g23 = *reinterpret_cast<const __nv_bfloat162*>(&gw.y);
-      uint2 o;
-      o.x = dev::pack_bf16x2(v[u].x * rs * __bfloat162float(g01.x), v[u].y * rs * __bfloat162float(g01.y));
-      o.y = dev::pack_bf16x2(v[u].z * rs * __bfloat162float(g23.x), v[u].w * rs * __bfloat162float(g23.y));
-      reinterpret_cast<uint2*>(a + i * H)[k4] = o;
-    }
-  }
 }
 
 // One CTA per (tile of tokens, head): sum the split partials, rotate q/k
@@ -305,8 +273,9 @@ cudaError_t launch_rope_table(const RowMap& rows, int d, float theta, float2* ta
 }
 
 cudaError_t launch_embed(const __nv_bfloat16* hidden, int m, int H, const __nv_bfloat16* gain,
-                         float eps, float* h, __nv_bfloat16* a, cudaStream_t st) {
-  return launch_k(embed_kernel, m, 256, 0, st, hidden, H, gain, eps, h, a);
+                         float eps, float* h, __nv_bfloat16* a, float* ss_out, int nss,
+                         cudaStream_t st) {
+  return launch_k(embed_kernel, m, 256, 0, st, hidden, H, gain, eps, h, a, ss_out, nss);
 }
 
 // One warp per token: the largest of the tiles' bests, lowest row on ties.
@@ -348,15 +317,6 @@ __global__ void wait_probe_kernel(int* status) {
 cudaError_t launch_wait_probe(int* status, cudaStream_t st) {
   wait_probe_kernel<<<1, 32, 0, st>>>(status);
   return cudaGetLastError();
-}
-
-cudaError_t launch_rmsnorm(const float* h, int c0, int mb, int H, const __nv_bfloat16* gain,
-                           float eps, __nv_bfloat16* a, cudaStream_t st) {
-  const int v = (H / 4 + 255) / 256;
-  if (v <= 2) return launch_k(rmsnorm_kernel<2>, mb, 256, 0, st, h, c0, H, gain, eps, a);
-  if (v <= 4) return launch_k(rmsnorm_kernel<4>, mb, 256, 0, st, h, c0, H, gain, eps, a);
-  if (v <= 8) return launch_k(rmsnorm_kernel<8>, mb, 256, 0, st, h, c0, H, gain, eps, a);
-  return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_epi_qkv(const float* part, long long plane, int ksplit, int ldo, int c0, int mb,

@@ -33,8 +33,11 @@
 //     pair (j, j + d/2) is in the tile: RoPE at the row's position, bf16,
 //     q to the KV-head-major q buffer, K rows and V^T columns to the slot
 //     (goinfer "What goinfer does": one key and one value row per token and layer);
-//   * Resid: h += y in fp32 (the RMSNorm that follows needs the whole row and
-//     runs as its own small launch), and on the last layer out = bf16(h);
+//   * Resid: h += y in fp32, and on the last layer out = bf16(h).  The
+//     RMSNorm that follows needs the whole row, which no tile has; it is
+//     deferred instead: the tile writes a = bf16(h * gain) and its share of
+//     sum(h^2) per row, and the next projection, linear in a, multiplies its
+//     results by rsqrt(sum / H + eps) when it adds the tile's contributions;
 //   * Swiglu: the tile holds gate rows n0..n0+63 and the same up rows, so
 //     z = bf16(silu(g) * u) is local to the tile;
 //   * Cast: out = bf16(y) (attention-only layers);
@@ -151,22 +154,44 @@ __device__ __forceinline__ void epi_qkv(const GemvParams& p, const GemvSeg& seg,
   }
 }
 
+// h += y; with a gain, also the deferred RMSNorm input of the next projection:
+// a = bf16(h * gain) and this tile's sum of h^2 per row.  A warp covers one
+// row's 128 columns per pass, so the tile's sum is one warp reduction in a
+// fixed order.
 __device__ __forceinline__ void epi_resid(const GemvParams& p, int row0, const float* ct, int tid) {
+  static_assert(kGemvRows / 4 == 32, "one warp per row of the tile");
   const int nv = min(kGemvRows, p.H - row0);
   for (int idx = tid; idx < p.mb * (kGemvRows / 4); idx += kConsumers) {
     const int t = idx / (kGemvRows / 4), c4 = (idx % (kGemvRows / 4)) * 4;
-    if (c4 >= nv) continue;
     const long long i = p.c0 + t;
-    float4* hp = reinterpret_cast<float4*>(p.h + i * p.H + row0 + c4);
-    const float4 y = *reinterpret_cast<const float4*>(ct + t * kTileLd + c4);
-    float4 hv = *hp;
-    hv.x += y.x; hv.y += y.y; hv.z += y.z; hv.w += y.w;
-    *hp = hv;
-    if (p.out) {
-      uint2 o;
-      o.x = dev::pack_bf16x2(hv.x, hv.y);
-      o.y = dev::pack_bf16x2(hv.z, hv.w);
-      *reinterpret_cast<uint2*>(p.out + i * p.ldout + row0 + c4) = o;
+    float ss = 0.f;
+    if (c4 < nv) {
+      float4* hp = reinterpret_cast<float4*>(p.h + i * p.H + row0 + c4);
+      const float4 y = *reinterpret_cast<const float4*>(ct + t * kTileLd + c4);
+      float4 hv = *hp;
+      hv.x += y.x; hv.y += y.y; hv.z += y.z; hv.w += y.w;
+      *hp = hv;
+      if (p.out) {
+        uint2 o;
+        o.x = dev::pack_bf16x2(hv.x, hv.y);
+        o.y = dev::pack_bf16x2(hv.z, hv.w);
+        *reinterpret_cast<uint2*>(p.out + i * p.ldout + row0 + c4) = o;
+      }
+      if (p.gain) {
+        const uint2 gw = *reinterpret_cast<const uint2*>(p.gain + row0 + c4);
+        const __nv_bfloat162 g01 = *reinterpret_cast<const __nv_bfloat162*>(&gw.x);
+        const __nv_bfloat162 g23 = *reinterpret_cast<const __nv_bfloat162*>(&gw.y);
+        uint2 o;
+        o.x = dev::pack_bf16x2(hv.x * __bfloat162float(g01.x), hv.y * __bfloat162float(g01.y));
+        o.y = dev::pack_bf16x2(hv.z * __bfloat162float(g23.x), hv.w * __bfloat162float(g23.y));
+        *reinterpret_cast<uint2*>(p.a + i * p.H + row0 + c4) = o;
+        ss = hv.x * hv.x + hv.y * hv.y + hv.z * hv.z + hv.w * hv.w;
+      }
+    }
+    if (p.gain) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+      if ((tid & 31) == 0) p.ss_out[i * p.nss + row0 / kGemvRows] = ss;
     }
   }
 }
@@ -238,6 +263,7 @@ __global__ void __launch_bounds__(kThreads, NT == 4 ? 1 : 2) gemv_int4_kernel(co
   __shared__ int own_tiles[kMaxOwnTiles];
   // K-quant: per warp and stage, (d*sc, dmin*mn) of its 16 rows x 8 sub-blocks
   __shared__ float2 q4k_tab[FMT == kFmtQ4K ? kConsumerWarps * 128 : 1];
+  __shared__ float row_scale[kGemvMaxCols];   // deferred RMSNorm of the input rows
   volatile int* abort_v = &abort_flag;
 
   const uint32_t base = (dev::smem_u32(smem_raw) + 1023u) & ~1023u;
@@ -359,6 +385,17 @@ __global__ void __launch_bounds__(kThreads, NT == 4 ? 1 : 2) gemv_int4_kernel(co
   // -------------------------------------------------------------- consumers
   dev::pdl_wait();                  // results are written below
   const int tid = threadIdx.x;      // 0..255 over the consumer warps
+  // Input rows in the deferred form: each row's RMSNorm factor from its tile
+  // sums (fixed order), used when the tile's contributions are added.  The
+  // loads overlap the first activation copies.
+  if (p.ss_in)
+    for (int t = warp; t < p.mb; t += kConsumerWarps) {
+      float v = 0.f;
+      for (int j = lane; j < p.nss; j += 32) v += p.ss_in[(long long)(p.c0 + t) * p.nss + j];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+      if (lane == 0) row_scale[t] = rsqrtf(v / p.H + p.eps);
+    }
   const int r = lane >> 2;          // fragment row 0..7
   const int c = lane & 3;           // fragment column pair
   const int rho0 = warp * 16 + r;   // tile rows of this thread: rho0 and rho0+8
@@ -537,6 +574,10 @@ __global__ void __launch_bounds__(kThreads, NT == 4 ? 1 : 2) gemv_int4_kernel(co
           if (j0 + j < ncon) {
             v.x += w[j].x; v.y += w[j].y; v.z += w[j].z; v.w += w[j].w;
           }
+      }
+      if (p.ss_in) {
+        const float f = row_scale[tok];
+        v.x *= f; v.y *= f; v.z *= f; v.w *= f;
       }
       *reinterpret_cast<float4*>(ct + tok * kTileLd + r4) = v;
     }

@@ -99,7 +99,7 @@ int attn_nsplit(int Hkv, int R, int kend_max, int target) {
 }
 
 struct ScratchLayout {
-  size_t status, counters, prompt, slot_len, match_out, rope, h, a, q, o, z, part, opart, ml, best, next, total;
+  size_t status, counters, prompt, slot_len, match_out, rope, h, a, ss, q, o, z, part, opart, ml, best, next, total;
   size_t part_floats, opart_floats, ml_count;
 };
 
@@ -118,6 +118,7 @@ ScratchLayout scratch_layout(const kvr_config* c) {
   L.rope = take(M * (c->head_dim / 2) * 8);
   L.h = take(M * H * 4);
   L.a = take(M * H * 2);
+  L.ss = take(M * ((H + kGemvRows - 1) / kGemvRows) * 4);   // deferred RMSNorm sums per row and tile
   L.q = take(M * QD * 2);
   L.o = take(M * QD * 2);
   L.z = take(M * F * 2);
@@ -191,6 +192,11 @@ struct kvr_ctx {
   float2* rope = nullptr;
   float* h = nullptr;
   __nv_bfloat16 *a = nullptr, *q = nullptr, *o = nullptr, *z = nullptr;
+  // a holds bf16(h * gain) with each row's sum of h^2 per 128-column tile in
+  // ss (the small-m GEMV applies the RMSNorm factor after projecting), not
+  // finished RMSNorm rows; tracked in stream order by the host
+  float* ss = nullptr;
+  bool a_deferred = false;
   float* part = nullptr;
   float* opart = nullptr;
   float2* ml = nullptr;
@@ -218,6 +224,11 @@ struct kvr_ctx {
 };
 
 namespace {
+
+// m rows of a 4-bit stack take the GEMV (else the tcgen05 GEMM)
+bool gemv_path(const kvr_ctx* c, int m) {
+  return c->force_gemv || (m <= kGemvMaxCols && !c->force_gemm);
+}
 
 int fail(kvr_ctx* c, int code, const char* fmt, ...) {
   if (c) {
@@ -407,8 +418,9 @@ struct Fused {
   int fmt = -1;                           // WeightFmt; -1: the layers' format
 };
 
-// Small-m int4 passes: the GEMV with its fused epilogue (plus the RMSNorm of
-// the finished rows after a residual projection).
+// Small-m int4 passes: the GEMV with its fused epilogue.  A residual
+// projection with a norm gain leaves the next RMSNorm deferred (a_deferred);
+// a projection of c->a in that form applies it.
 int project_gemv_int4(kvr_ctx* c, cudaStream_t st, const Seg* segs, int nseg, const CUtensorMap* tmx,
                       int K, int m, const Fused& fz) {
   const kvr_config& cfg = c->cfg;
@@ -469,6 +481,15 @@ int project_gemv_int4(kvr_ctx* c, cudaStream_t st, const Seg* segs, int nseg, co
   p.F = cfg.ffn;
   p.slot_stride = kv_offset(c, 1, 0, 0);
   p.best = fz.best;
+  p.nss = (cfg.hidden + kGemvRows - 1) / kGemvRows;
+  p.eps = cfg.rms_eps;
+  if (tmx == c->tm_a && c->a_deferred) p.ss_in = c->ss;
+  const bool norm_out = fz.epi == kGemvEpiResid && fz.norm_gain;
+  if (norm_out) {
+    p.gain = fz.norm_gain;
+    p.a = c->a;
+    p.ss_out = c->ss;
+  }
   for (int c0 = 0; c0 < m; c0 += kGemvMaxCols) {
     const int mb = std::min(kGemvMaxCols, m - c0);
     p.c0 = c0;
@@ -500,12 +521,8 @@ int project_gemv_int4(kvr_ctx* c, cudaStream_t st, const Seg* segs, int nseg, co
       e = launch_gemv_int4(p, nt, st);
     }
     if (e != cudaSuccess) return cuda_fail(c, e, "gemv_int4 launch");
-    if (fz.epi == kGemvEpiResid && fz.norm_gain) {
-      Timed t(c, kEpi, st);
-      e = launch_rmsnorm(c->h, c0, mb, cfg.hidden, fz.norm_gain, cfg.rms_eps, c->a, st);
-      if (e != cudaSuccess) return cuda_fail(c, e, "rmsnorm launch");
-    }
   }
+  if (norm_out) c->a_deferred = true;
   return KVR_OK;
 }
 
@@ -514,11 +531,12 @@ int project(kvr_ctx* c, cudaStream_t st, const Seg* segs, int nseg, Act act, int
             const Fused& fz, bool swiglu = false) {
   const kvr_config& cfg = c->cfg;
   const CUtensorMap* tmx = act == Act::A ? c->tm_a : (act == Act::O ? c->tm_o : c->tm_z);
-  if (packed4(cfg)) {
-    if ((m > kGemvMaxCols || c->force_gemm) && !c->force_gemv)
-      return project_gemm(c, st, segs, nseg, tmx, K, m, swiglu, epi);
-    return project_gemv_int4(c, st, segs, nseg, tmx, K, m, fz);
-  }
+  if (packed4(cfg) && gemv_path(c, m)) return project_gemv_int4(c, st, segs, nseg, tmx, K, m, fz);
+  // the row-wise epilogues below write finished RMSNorm rows
+  if (tmx == c->tm_a && c->a_deferred)
+    return fail(c, KVR_ERR_UNSUPPORTED, "activations in the deferred-norm form reached a row-wise path");
+  if (fz.epi == kGemvEpiResid && fz.norm_gain) c->a_deferred = false;
+  if (packed4(cfg)) return project_gemm(c, st, segs, nseg, tmx, K, m, swiglu, epi);
   // bf16 weights: plain GEMV into partials, then the row-wise epilogue kernel
   GemvParams p;
   memset(&p, 0, sizeof p);
@@ -730,12 +748,16 @@ int run_stack(kvr_ctx* c, const RowMap& rows, const void* hidden,
   }
   if (e != cudaSuccess) return cuda_fail(c, e, "rope table launch");
   if (k.attn_only) {
+    c->a_deferred = false;
     e = cudaMemcpyAsync(c->a, hidden, (size_t)m * H * 2, cudaMemcpyDeviceToDevice, st);
     if (e != cudaSuccess) return cuda_fail(c, e, "input copy");
   } else {
+    // the small-m GEMV takes the first RMSNorm deferred, like every later one
+    c->a_deferred = packed4(k) && gemv_path(c, m);
     Timed t(c, kEpi, st);
     e = launch_embed(static_cast<const __nv_bfloat16*>(hidden), m, H,
-                     static_cast<const __nv_bfloat16*>(w[0].norm_attn), k.rms_eps, c->h, c->a, st);
+                     static_cast<const __nv_bfloat16*>(w[0].norm_attn), k.rms_eps, c->h, c->a,
+                     c->a_deferred ? c->ss : nullptr, (H + kGemvRows - 1) / kGemvRows, st);
     if (e != cudaSuccess) return cuda_fail(c, e, "embed launch");
   }
   auto trace = [&](int entry) -> cudaError_t {
@@ -1144,6 +1166,7 @@ int kvr_ctx_create(const kvr_config* cfg, void* kv_arena, size_t arena_bytes, vo
   c->rope = reinterpret_cast<float2*>(s + c->sl.rope);
   c->h = reinterpret_cast<float*>(s + c->sl.h);
   c->a = reinterpret_cast<__nv_bfloat16*>(s + c->sl.a);
+  c->ss = reinterpret_cast<float*>(s + c->sl.ss);
   c->q = reinterpret_cast<__nv_bfloat16*>(s + c->sl.q);
   c->o = reinterpret_cast<__nv_bfloat16*>(s + c->sl.o);
   c->z = reinterpret_cast<__nv_bfloat16*>(s + c->sl.z);

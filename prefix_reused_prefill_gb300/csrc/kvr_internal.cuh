@@ -145,6 +145,17 @@ struct GemvParams {
   __nv_bfloat16* z;     // Swiglu: [max_rows][F]
   int F;
   float2* best;         // Argmax: [token][tiles] (value, row)
+  // Deferred RMSNorm of the small-m path.  A residual epilogue with a gain
+  // writes a = bf16(h * gain) and, per row and 128-column tile, the sum of
+  // h^2; a launch that reads those rows scales each row's results by
+  // rsqrt(sum / H + eps), which is RMSNorm applied after the (linear)
+  // projection instead of before it.
+  const __nv_bfloat16* gain;  // Resid: the next RMSNorm's gain, or null
+  __nv_bfloat16* a;           // Resid with gain: bf16 [max_rows][H]
+  float* ss_out;              // Resid with gain: [max_rows][nss]
+  const float* ss_in;         // the input rows' sums [max_rows][nss], or null (rows already normed)
+  int nss;                    // ceil(H / 128)
+  float eps;
 };
 
 struct GemmSeg {
@@ -252,16 +263,17 @@ cudaError_t launch_attention_tc(const AttnParams& p, int d, cudaStream_t st);
 cudaError_t launch_attn_combine(const AttnParams& p, int d, cudaStream_t st);
 cudaError_t launch_rope_table(const RowMap& rows, int d, float theta, float2* table,
                               cudaStream_t st);
+// h = float(hidden) and the first RMSNorm: a = bf16(RMSNorm(h) * gain), or,
+// with ss_out (the deferred form read by the small-m GEMV), a = bf16(h * gain)
+// and ss_out[row][0] = sum of h^2 (the row's other nss - 1 entries zero)
 cudaError_t launch_embed(const __nv_bfloat16* hidden, int m, int H, const __nv_bfloat16* gain,
-                         float eps, float* h, __nv_bfloat16* a, cudaStream_t st);
+                         float eps, float* h, __nv_bfloat16* a, float* ss_out, int nss,
+                         cudaStream_t st);
 // out[t] = the row of the largest value over the tiles' bests of token t
 // (lowest row on ties), t < m
 // one device-side wait that runs out (the failure path, without a fault)
 cudaError_t launch_wait_probe(int* status, cudaStream_t st);
 cudaError_t launch_head_argmax(const float2* best, int tiles, int m, int32_t* out, cudaStream_t st);
-// a[c0 + t] = bf16(RMSNorm(h[c0 + t]) * gain) for t < mb
-cudaError_t launch_rmsnorm(const float* h, int c0, int mb, int H, const __nv_bfloat16* gain,
-                           float eps, __nv_bfloat16* a, cudaStream_t st);
 cudaError_t launch_epi_qkv(const float* part, long long plane, int ksplit, int ldo, int c0,
                            int mb, const RowMap& rows, int Hq, int Hkv, int d,
                            const float2* rope, __nv_bfloat16* q, __nv_bfloat16* arena,
