@@ -250,165 +250,119 @@ __device__ __forceinline__ void epi_argmax(const GemvParams& p, const GemvSeg& s
   }
 }
 
-// two CTAs per SM for up to 16 tokens (the host sizes the grid for it)
-template <int NT, int EPI, int FMT>
-__global__ void __launch_bounds__(kThreads, NT == 4 ? 1 : 2) gemv_int4_kernel(const __grid_constant__ GemvParams p) {
+// segment and first weight row of a tile
+template <bool kPair>
+__device__ __forceinline__ int tile_seg(const GemvParams& p, int tile) {
+  int s = 0;
+  if (!kPair)
+    while (s + 1 < p.nseg && tile >= p.seg[s + 1].tile0) ++s;
+  return s;
+}
+template <bool kPair>
+__device__ __forceinline__ int tile_row0(const GemvParams& p, int tile, int s) {
+  return kPair ? tile * 64 : (tile - p.seg[s].tile0) * kGemvRows;
+}
+// Producer (one lane): the weight and scale tiles of units [u0, u0 + nk) and
+// their activation tiles through the stage ring.
+template <int NT, bool kPair>
+__device__ __forceinline__ void gemv_produce(const GemvParams& p, uint32_t base, uint64_t* full_bar,
+                                             uint64_t* empty_bar, volatile int* abort_v, int u0, int nk) {
   using C = GemvCfg<NT>;
-  constexpr bool kPair = EPI == kGemvEpiSwiglu;   // tile = 64 gate rows + 64 up rows
-  extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t full_bar[C::kStages];
-  __shared__ __align__(8) uint64_t empty_bar[C::kStages];
-  __shared__ int abort_flag;
-  __shared__ int n_own;
-  __shared__ int own_tiles[kMaxOwnTiles];
-  // K-quant: per warp and stage, (d*sc, dmin*mn) of its 16 rows x 8 sub-blocks
-  __shared__ float2 q4k_tab[FMT == kFmtQ4K ? kConsumerWarps * 128 : 1];
-  __shared__ float row_scale[kGemvMaxCols];   // deferred RMSNorm of the input rows
-  volatile int* abort_v = &abort_flag;
-
-  const uint32_t base = (dev::smem_u32(smem_raw) + 1023u) & ~1023u;
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-
-  // this CTA's contiguous range of (tile, k-step) units
-  const int units = p.tiles * p.ksteps;
-  const int u0 = (int)((long long)blockIdx.x * units / p.ctas);
-  const int u1 = (int)((long long)(blockIdx.x + 1) * units / p.ctas);
-  const int nk = u1 - u0;
-  // segment and first weight row of a tile
-  auto tile_seg = [&](int tile) {
-    int s = 0;
-    if (!kPair)
-      while (s + 1 < p.nseg && tile >= p.seg[s + 1].tile0) ++s;
-    return s;
+  for (int i = 0; i < p.nseg; ++i) {
+    dev::prefetch_tmap(&p.seg[i].tw);
+    dev::prefetch_tmap(&p.seg[i].ts);
+  }
+  if (kPair) {
+    dev::prefetch_tmap(&p.seg[1].tw);
+    dev::prefetch_tmap(&p.seg[1].ts);
+  }
+  dev::prefetch_tmap(&p.tx);
+  const uint64_t pol = dev::policy_evict_first();
+  auto load_w = [&](uint32_t sb, uint32_t fb, int u) {
+    const int tile = u / p.ksteps, ks = u % p.ksteps;
+    const int s = tile_seg<kPair>(p, tile);
+    const int row0 = tile_row0<kPair>(p, tile, s);
+    const uint32_t sc = sb + kWTileBytes + C::kXTileBytes;
+    if (kPair) {
+      dev::tma_load_2d_hint(sb, &p.seg[0].tw, ks * 128, row0, fb, pol);
+      dev::tma_load_2d_hint(sb + kWTileBytes / 2, &p.seg[1].tw, ks * 128, row0, fb, pol);
+      dev::tma_load_2d_hint(sc, &p.seg[0].ts, ks * 8, row0, fb, pol);
+      dev::tma_load_2d_hint(sc + kSTileBytes / 2, &p.seg[1].ts, ks * 8, row0, fb, pol);
+    } else {
+      dev::tma_load_2d_hint(sb, &p.seg[s].tw, ks * 128, row0, fb, pol);
+      dev::tma_load_2d_hint(sc, &p.seg[s].ts, ks * 8, row0, fb, pol);
+    }
   };
-  auto tile_row0 = [&](int tile, int s) { return kPair ? tile * 64 : (tile - p.seg[s].tile0) * kGemvRows; };
-
-  dev::pdl_trigger();
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < C::kStages; ++i) {
-      dev::mbar_init(dev::smem_u32(&full_bar[i]), 1);
-      dev::mbar_init(dev::smem_u32(&empty_bar[i]), kConsumerWarps);
+  auto prefetch_w = [&](int u) {
+    const int tile = u / p.ksteps, ks = u % p.ksteps;
+    const int s = tile_seg<kPair>(p, tile);
+    const int row0 = tile_row0<kPair>(p, tile, s);
+    if (kPair) {
+      dev::tma_prefetch_2d(&p.seg[0].tw, ks * 128, row0);
+      dev::tma_prefetch_2d(&p.seg[1].tw, ks * 128, row0);
+      dev::tma_prefetch_2d(&p.seg[0].ts, ks * 8, row0);
+      dev::tma_prefetch_2d(&p.seg[1].ts, ks * 8, row0);
+    } else {
+      dev::tma_prefetch_2d(&p.seg[s].tw, ks * 128, row0);
+      dev::tma_prefetch_2d(&p.seg[s].ts, ks * 8, row0);
     }
-    *abort_v = 0;
-    n_own = 0;
-    dev::fence_mbar_init();
-  }
-  __syncthreads();
-
-  if (warp == kConsumerWarps) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      for (int i = 0; i < p.nseg; ++i) {
-        dev::prefetch_tmap(&p.seg[i].tw);
-        dev::prefetch_tmap(&p.seg[i].ts);
-      }
-      if (kPair) {
-        dev::prefetch_tmap(&p.seg[1].tw);
-        dev::prefetch_tmap(&p.seg[1].ts);
-      }
-      dev::prefetch_tmap(&p.tx);
-      const uint64_t pol = dev::policy_evict_first();
-      auto load_w = [&](uint32_t sb, uint32_t fb, int u) {
-        const int tile = u / p.ksteps, ks = u % p.ksteps;
-        const int s = tile_seg(tile);
-        const int row0 = tile_row0(tile, s);
-        const uint32_t sc = sb + kWTileBytes + C::kXTileBytes;
-        if (kPair) {
-          dev::tma_load_2d_hint(sb, &p.seg[0].tw, ks * 128, row0, fb, pol);
-          dev::tma_load_2d_hint(sb + kWTileBytes / 2, &p.seg[1].tw, ks * 128, row0, fb, pol);
-          dev::tma_load_2d_hint(sc, &p.seg[0].ts, ks * 8, row0, fb, pol);
-          dev::tma_load_2d_hint(sc + kSTileBytes / 2, &p.seg[1].ts, ks * 8, row0, fb, pol);
-        } else {
-          dev::tma_load_2d_hint(sb, &p.seg[s].tw, ks * 128, row0, fb, pol);
-          dev::tma_load_2d_hint(sc, &p.seg[s].ts, ks * 8, row0, fb, pol);
-        }
-      };
-      auto prefetch_w = [&](int u) {
-        const int tile = u / p.ksteps, ks = u % p.ksteps;
-        const int s = tile_seg(tile);
-        const int row0 = tile_row0(tile, s);
-        if (kPair) {
-          dev::tma_prefetch_2d(&p.seg[0].tw, ks * 128, row0);
-          dev::tma_prefetch_2d(&p.seg[1].tw, ks * 128, row0);
-          dev::tma_prefetch_2d(&p.seg[0].ts, ks * 8, row0);
-          dev::tma_prefetch_2d(&p.seg[1].ts, ks * 8, row0);
-        } else {
-          dev::tma_prefetch_2d(&p.seg[s].tw, ks * 128, row0);
-          dev::tma_prefetch_2d(&p.seg[s].ts, ks * 8, row0);
-        }
-      };
-      auto load_x = [&](uint32_t sb, uint32_t fb, int u) {
-        const int ks = u % p.ksteps;
+  };
+  auto load_x = [&](uint32_t sb, uint32_t fb, int u) {
+    const int ks = u % p.ksteps;
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-          dev::tma_load_2d(sb + kWTileBytes + j * C::kXBoxBytes, &p.tx, ks * kGemvKStep + 64 * j, p.c0, fb);
-      };
-      // Weights do not depend on earlier launches: fill the ring's weight and
-      // scale tiles and pull the rest of this CTA's weights toward L2 before
-      // waiting for the previous launch; the activations follow the wait.
-      const int pre = nk < C::kStages ? nk : C::kStages;
-      for (int it = 0; it < pre; ++it) {
-        const uint32_t fb = dev::smem_u32(&full_bar[it]);
-        dev::mbar_arrive_expect_tx(fb, C::kStageBytes);
-        load_w(base + it * C::kStageBytes, fb, u0 + it);
-      }
-      for (int it = pre; it < nk; ++it) prefetch_w(u0 + it);
-      dev::pdl_wait();
-      for (int it = 0; it < pre; ++it)
-        load_x(base + it * C::kStageBytes, dev::smem_u32(&full_bar[it]), u0 + it);
-      int issued = pre;
-      for (int it = pre; it < nk; ++it) {
-        const int st = it % C::kStages;
-        const uint32_t use = (uint32_t)(it / C::kStages);
-        if (!dev::mbar_wait(dev::smem_u32(&empty_bar[st]), (use - 1) & 1, p.status) || *abort_v) {
-          *abort_v = 1;
-          break;
-        }
-        const uint32_t sb = base + st * C::kStageBytes;
-        const uint32_t fb = dev::smem_u32(&full_bar[st]);
-        dev::mbar_arrive_expect_tx(fb, C::kStageBytes);
-        load_w(sb, fb, u0 + it);
-        load_x(sb, fb, u0 + it);
-        ++issued;
-      }
-      // never leave the CTA with copies in flight: wait (bounded) for the last
-      // use of every stage that was filled
-      for (int st = 0; st < C::kStages && st < issued; ++st) {
-        const int last = ((issued - 1 - st) / C::kStages) * C::kStages + st;
-        dev::mbar_wait(dev::smem_u32(&full_bar[st]), (uint32_t)(last / C::kStages) & 1, nullptr);
-      }
-    }
-    return;
+    for (int j = 0; j < 4; ++j)
+      dev::tma_load_2d(sb + kWTileBytes + j * C::kXBoxBytes, &p.tx, ks * kGemvKStep + 64 * j, p.c0, fb);
+  };
+  // Weights do not depend on earlier launches: fill the ring's weight and
+  // scale tiles and pull the rest of this CTA's weights toward L2 before
+  // waiting for the previous launch; the activations follow the wait.
+  const int pre = nk < C::kStages ? nk : C::kStages;
+  for (int it = 0; it < pre; ++it) {
+    const uint32_t fb = dev::smem_u32(&full_bar[it]);
+    dev::mbar_arrive_expect_tx(fb, C::kStageBytes);
+    load_w(base + it * C::kStageBytes, fb, u0 + it);
   }
-
-  // -------------------------------------------------------------- consumers
-  dev::pdl_wait();                  // results are written below
-  const int tid = threadIdx.x;      // 0..255 over the consumer warps
-  // Input rows in the deferred form: each row's RMSNorm factor from its tile
-  // sums (fixed order), used when the tile's contributions are added.  The
-  // loads overlap the first activation copies.
-  if (p.ss_in)
-    for (int t = warp; t < p.mb; t += kConsumerWarps) {
-      float v = 0.f;
-      for (int j = lane; j < p.nss; j += 32) v += p.ss_in[(long long)(p.c0 + t) * p.nss + j];
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-      if (lane == 0) row_scale[t] = rsqrtf(v / p.H + p.eps);
+  for (int it = pre; it < nk; ++it) prefetch_w(u0 + it);
+  dev::pdl_wait();
+  for (int it = 0; it < pre; ++it)
+    load_x(base + it * C::kStageBytes, dev::smem_u32(&full_bar[it]), u0 + it);
+  int issued = pre;
+  for (int it = pre; it < nk; ++it) {
+    const int st = it % C::kStages;
+    const uint32_t use = (uint32_t)(it / C::kStages);
+    if (!dev::mbar_wait(dev::smem_u32(&empty_bar[st]), (use - 1) & 1, p.status) || *abort_v) {
+      *abort_v = 1;
+      break;
     }
+    const uint32_t sb = base + st * C::kStageBytes;
+    const uint32_t fb = dev::smem_u32(&full_bar[st]);
+    dev::mbar_arrive_expect_tx(fb, C::kStageBytes);
+    load_w(sb, fb, u0 + it);
+    load_x(sb, fb, u0 + it);
+    ++issued;
+  }
+  // never leave the CTA with copies in flight: wait (bounded) for the last
+  // use of every stage that was filled
+  for (int st = 0; st < C::kStages && st < issued; ++st) {
+    const int last = ((issued - 1 - st) / C::kStages) * C::kStages + st;
+    dev::mbar_wait(dev::smem_u32(&full_bar[st]), (uint32_t)(last / C::kStages) & 1, nullptr);
+  }
+}
+
+// Consumers (8 warps, tid 0..255): units [u0, u0 + nk) into acc; at the end
+// of each tile's run of units, seg_end(tile, acc, ok, last) takes the
+// accumulators (and zeroes them).  A wait that gives up marks the CTA aborted;
+// from then on the warps skip the work and the waits.  Returns ok.
+template <int NT, int FMT, class SegEnd>
+__device__ __forceinline__ bool gemv_consume(const GemvParams& p, uint32_t base, uint64_t* full_bar,
+                                             uint64_t* empty_bar, volatile int* abort_v, float2* q4k_tab,
+                                             int u0, int nk, float (&acc)[NT][4], SegEnd&& seg_end) {
+  using C = GemvCfg<NT>;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = lane >> 2;          // fragment row 0..7
   const int c = lane & 3;           // fragment column pair
   const int rho0 = warp * 16 + r;   // tile rows of this thread: rho0 and rho0+8
-  float acc[NT][4];
-#pragma unroll
-  for (int t = 0; t < NT; ++t)
-#pragma unroll
-    for (int e = 0; e < 4; ++e) acc[t][e] = 0.f;
-
   const float zero4[4] = {0.f, 0.f, 0.f, 0.f};
-  // A wait that gives up marks the CTA aborted; from then on the warps skip
-  // the work and the waits but still pass every consumer barrier, so no warp
-  // is left waiting for one that has stopped.
   bool ok = true;                   // warp-uniform
   for (int it = 0; it < nk; ++it) {
     const int st = it % C::kStages;
@@ -466,63 +420,136 @@ __global__ void __launch_bounds__(kThreads, NT == 4 ? 1 : 2) gemv_int4_kernel(co
           }
         }
       } else {
-      // (removing the offset with two extra MMAs instead of the subtraction
-      // measured slower here: the MMA issue, not the ALU, is the tighter limit)
-      const uint4 sc0 = dev::lds128(stile + rho0 * 16);
-      const uint4 sc1 = dev::lds128(stile + (rho0 + 8) * 16);
-      const __half* s0h = reinterpret_cast<const __half*>(&sc0);
-      const __half* s1h = reinterpret_cast<const __half*>(&sc1);
+        // (removing the offset with two extra MMAs instead of the subtraction
+        // measured slower here: the MMA issue, not the ALU, is the tighter limit)
+        const uint4 sc0 = dev::lds128(stile + rho0 * 16);
+        const uint4 sc1 = dev::lds128(stile + (rho0 + 8) * 16);
+        const __half* s0h = reinterpret_cast<const __half*>(&sc0);
+        const __half* s1h = reinterpret_cast<const __half*>(&sc1);
 #pragma unroll
-      for (int g = 0; g < 8; ++g) {
-        const uint32_t w0 = dev::lds32(wt + dev::swz128(rho0, g) + 4 * c);
-        const uint32_t w1 = dev::lds32(wt + dev::swz128(rho0 + 8, g) + 4 * c);
-        uint32_t q0[4], q1[4];
-        code_word(w0, q0);
-        code_word(w1, q1);
-        const uint32_t a_lo[4] = {q0[0], q1[0], q0[1], q1[1]};  // inputs 0..15 of the group
-        const uint32_t a_hi[4] = {q0[2], q1[2], q0[3], q1[3]};  // inputs 16..31
-        const float sr0 = __half2float(s0h[g]);
-        const float sr1 = __half2float(s1h[g]);
+        for (int g = 0; g < 8; ++g) {
+          const uint32_t w0 = dev::lds32(wt + dev::swz128(rho0, g) + 4 * c);
+          const uint32_t w1 = dev::lds32(wt + dev::swz128(rho0 + 8, g) + 4 * c);
+          uint32_t q0[4], q1[4];
+          code_word(w0, q0);
+          code_word(w1, q1);
+          const uint32_t a_lo[4] = {q0[0], q1[0], q0[1], q1[1]};  // inputs 0..15 of the group
+          const uint32_t a_hi[4] = {q0[2], q1[2], q0[3], q1[3]};  // inputs 16..31
+          const float sr0 = __half2float(s0h[g]);
+          const float sr1 = __half2float(s1h[g]);
 #pragma unroll
-        for (int t = 0; t < NT; ++t) {
-          // B fragments: tokens t*8 .. t*8+7, inputs 32g + 8q .. +7 for q = 0..3
-          const int n = t * 8 + (lane & 7);
-          const int q = lane >> 3;
-          const int box = g >> 1;
-          const int chunk = 4 * (g & 1) + q;
-          uint32_t b0, b1, b2, b3;
-          dev::ldmatrix_x4(xt + box * C::kXBoxBytes + dev::swz128(n, chunk), b0, b1, b2, b3);
-          float tmp[4];
-          dev::mma_bf16_16816(tmp, a_lo, b0, b1, zero4);
-          dev::mma_bf16_16816(tmp, a_hi, b2, b3, tmp);
-          acc[t][0] = fmaf(sr0, tmp[0], acc[t][0]);
-          acc[t][1] = fmaf(sr0, tmp[1], acc[t][1]);
-          acc[t][2] = fmaf(sr1, tmp[2], acc[t][2]);
-          acc[t][3] = fmaf(sr1, tmp[3], acc[t][3]);
+          for (int t = 0; t < NT; ++t) {
+            // B fragments: tokens t*8 .. t*8+7, inputs 32g + 8q .. +7 for q = 0..3
+            const int n = t * 8 + (lane & 7);
+            const int q = lane >> 3;
+            const int box = g >> 1;
+            const int chunk = 4 * (g & 1) + q;
+            uint32_t b0, b1, b2, b3;
+            dev::ldmatrix_x4(xt + box * C::kXBoxBytes + dev::swz128(n, chunk), b0, b1, b2, b3);
+            float tmp[4];
+            dev::mma_bf16_16816(tmp, a_lo, b0, b1, zero4);
+            dev::mma_bf16_16816(tmp, a_hi, b2, b3, tmp);
+            acc[t][0] = fmaf(sr0, tmp[0], acc[t][0]);
+            acc[t][1] = fmaf(sr0, tmp[1], acc[t][1]);
+            acc[t][2] = fmaf(sr1, tmp[2], acc[t][2]);
+            acc[t][3] = fmaf(sr1, tmp[3], acc[t][3]);
+          }
         }
-      }
       }
       __syncwarp();
       if (lane == 0) dev::mbar_arrive(dev::smem_u32(&empty_bar[st]));
     }
-
-    // end of this CTA's part of a tile: store it as one contribution (the
-    // arrivals are counted once, after the loop)
     const int u = u0 + it;
-    const int tile = u / p.ksteps;
-    if (u % p.ksteps == p.ksteps - 1 || it == nk - 1) {
-      const int first = unit_owner((long long)tile * p.ksteps, units, p.ctas);
-      float* tp = p.part + ((long long)tile * p.maxc + (blockIdx.x - first)) * (kGemvMaxCols * kGemvRows);
-#pragma unroll
-      for (int t = 0; t < NT; ++t)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int tok = t * 8 + 2 * c + (e & 1);
-          if (ok && tok < p.mb) tp[tok * kGemvRows + rho0 + (e >> 1) * 8] = acc[t][e];
-          acc[t][e] = 0.f;
-        }
-    }
+    if (u % p.ksteps == p.ksteps - 1 || it == nk - 1) seg_end(u / p.ksteps, acc, ok, it == nk - 1);
   }
+  return ok;
+}
+
+// Input rows in the deferred-RMSNorm form: each row's factor from its sums
+// (fixed order), applied when the tile's contributions are added.  The loads
+// overlap the first activation copies.
+__device__ __forceinline__ void row_scales(const GemvParams& p, float* row_scale) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (!p.ss_in) return;
+  for (int t = warp; t < p.mb; t += kConsumerWarps) {
+    float v = 0.f;
+    for (int j = lane; j < p.nss; j += 32) v += p.ss_in[(long long)(p.c0 + t) * p.nss + j];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if (lane == 0) row_scale[t] = rsqrtf(v / p.H + p.eps);
+  }
+}
+
+// Stream-K: a CTA takes an equal run of (tile, k-step) units of the whole
+// launch (the host sizes the grid to one resident wave: two CTAs per SM for
+// up to 16 tokens, one beyond).
+template <int NT, int EPI, int FMT>
+__global__ void __launch_bounds__(kThreads, NT == 4 ? 1 : 2) gemv_int4_kernel(const __grid_constant__ GemvParams p) {
+  using C = GemvCfg<NT>;
+  constexpr bool kPair = EPI == kGemvEpiSwiglu;   // tile = 64 gate rows + 64 up rows
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t full_bar[C::kStages];
+  __shared__ __align__(8) uint64_t empty_bar[C::kStages];
+  __shared__ int abort_flag;
+  __shared__ int n_own;
+  __shared__ int own_tiles[kMaxOwnTiles];
+  // K-quant: per warp and stage, (d*sc, dmin*mn) of its 16 rows x 8 sub-blocks
+  __shared__ float2 q4k_tab[FMT == kFmtQ4K ? kConsumerWarps * 128 : 1];
+  __shared__ float row_scale[kGemvMaxCols];   // deferred RMSNorm of the input rows
+  volatile int* abort_v = &abort_flag;
+
+  const uint32_t base = (dev::smem_u32(smem_raw) + 1023u) & ~1023u;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // this CTA's contiguous range of (tile, k-step) units
+  const int units = p.tiles * p.ksteps;
+  const int u0 = (int)((long long)blockIdx.x * units / p.ctas);
+  const int u1 = (int)((long long)(blockIdx.x + 1) * units / p.ctas);
+  const int nk = u1 - u0;
+
+  dev::pdl_trigger();
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::kStages; ++i) {
+      dev::mbar_init(dev::smem_u32(&full_bar[i]), 1);
+      dev::mbar_init(dev::smem_u32(&empty_bar[i]), kConsumerWarps);
+    }
+    *abort_v = 0;
+    n_own = 0;
+    dev::fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == kConsumerWarps) {
+    if (lane == 0) gemv_produce<NT, kPair>(p, base, full_bar, empty_bar, abort_v, u0, nk);
+    return;
+  }
+
+  dev::pdl_wait();                  // results are written below
+  const int tid = threadIdx.x;      // 0..255 over the consumer warps
+  row_scales(p, row_scale);
+  const int r = lane >> 2, c = lane & 3;
+  const int rho0 = warp * 16 + r;
+  float acc[NT][4];
+#pragma unroll
+  for (int t = 0; t < NT; ++t)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc[t][e] = 0.f;
+  // end of this CTA's part of a tile: store it as one contribution (the
+  // arrivals are counted once, after the loop)
+  gemv_consume<NT, FMT>(p, base, full_bar, empty_bar, abort_v, q4k_tab, u0, nk, acc,
+                        [&](int tile, float (&a)[NT][4], bool ok, bool) {
+    const int first = unit_owner((long long)tile * p.ksteps, units, p.ctas);
+    float* tp = p.part + ((long long)tile * p.maxc + (blockIdx.x - first)) * (kGemvMaxCols * kGemvRows);
+#pragma unroll
+    for (int t = 0; t < NT; ++t)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int tok = t * 8 + 2 * c + (e & 1);
+        if (ok && tok < p.mb) tp[tok * kGemvRows + rho0 + (e >> 1) * 8] = a[t][e];
+        a[t][e] = 0.f;
+      }
+  });
   // publish every contribution of this CTA, then count one arrival per tile
   // touched (one thread per tile); the last arrival owns the tile's epilogue.
   // The barrier orders every consumer's partial stores before the counting
@@ -582,8 +609,8 @@ __global__ void __launch_bounds__(kThreads, NT == 4 ? 1 : 2) gemv_int4_kernel(co
       *reinterpret_cast<float4*>(ct + tok * kTileLd + r4) = v;
     }
     consumers_sync();
-    const int s = tile_seg(tile);
-    const int row0 = tile_row0(tile, s);
+    const int s = tile_seg<kPair>(p, tile);
+    const int row0 = tile_row0<kPair>(p, tile, s);
     if (EPI == kGemvEpiQKV) epi_qkv(p, p.seg[s], s, row0, ct, tid);
     else if (EPI == kGemvEpiResid) epi_resid(p, row0, ct, tid);
     else if (EPI == kGemvEpiSwiglu) epi_swiglu(p, row0, ct, tid);

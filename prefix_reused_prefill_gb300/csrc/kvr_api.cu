@@ -103,6 +103,9 @@ struct ScratchLayout {
   size_t part_floats, opart_floats, ml_count;
 };
 
+// deferred-RMSNorm sums per row: one per 128-column tile of the hidden width
+size_t ss_per_row(size_t H) { return (H + kGemvRows - 1) / kGemvRows; }
+
 ScratchLayout scratch_layout(const kvr_config* c) {
   ScratchLayout L{};
   const int S = std::max(c->n_slots, 1);
@@ -118,7 +121,7 @@ ScratchLayout scratch_layout(const kvr_config* c) {
   L.rope = take(M * (c->head_dim / 2) * 8);
   L.h = take(M * H * 4);
   L.a = take(M * H * 2);
-  L.ss = take(M * ((H + kGemvRows - 1) / kGemvRows) * 4);   // deferred RMSNorm sums per row and tile
+  L.ss = take(M * ss_per_row(H) * 4);   // deferred RMSNorm sums per row
   L.q = take(M * QD * 2);
   L.o = take(M * QD * 2);
   L.z = take(M * F * 2);
@@ -481,7 +484,7 @@ int project_gemv_int4(kvr_ctx* c, cudaStream_t st, const Seg* segs, int nseg, co
   p.F = cfg.ffn;
   p.slot_stride = kv_offset(c, 1, 0, 0);
   p.best = fz.best;
-  p.nss = (cfg.hidden + kGemvRows - 1) / kGemvRows;
+  p.nss = (int)ss_per_row(cfg.hidden);
   p.eps = cfg.rms_eps;
   if (tmx == c->tm_a && c->a_deferred) p.ss_in = c->ss;
   const bool norm_out = fz.epi == kGemvEpiResid && fz.norm_gain;
@@ -496,6 +499,7 @@ int project_gemv_int4(kvr_ctx* c, cudaStream_t st, const Seg* segs, int nseg, co
     p.mb = mb;
     const int nt = mb <= 8 ? 1 : (mb <= 16 ? 2 : 4);
     const int per_sm = nt == 4 ? 1 : 2;   // CTAs resident per SM (shared memory, registers)
+    p.tx = tmx[nt == 1 ? 0 : (nt == 2 ? 1 : 2)];
     // one resident wave of CTAs, each an equal run of (tile, k-step) units
     const int units = tiles * p.ksteps;
     int ctas = std::min(units, c->n_sms * per_sm);
@@ -514,7 +518,6 @@ int project_gemv_int4(kvr_ctx* c, cudaStream_t st, const Seg* segs, int nseg, co
     p.ctas = ctas;
     p.maxc = maxc;
     p.ksplit = 1;
-    p.tx = tmx[nt == 1 ? 0 : (nt == 2 ? 1 : 2)];
     cudaError_t e;
     {
       Timed t(c, kProj, st);
@@ -757,7 +760,7 @@ int run_stack(kvr_ctx* c, const RowMap& rows, const void* hidden,
     Timed t(c, kEpi, st);
     e = launch_embed(static_cast<const __nv_bfloat16*>(hidden), m, H,
                      static_cast<const __nv_bfloat16*>(w[0].norm_attn), k.rms_eps, c->h, c->a,
-                     c->a_deferred ? c->ss : nullptr, (H + kGemvRows - 1) / kGemvRows, st);
+                     c->a_deferred ? c->ss : nullptr, (int)ss_per_row(H), st);
     if (e != cudaSuccess) return cuda_fail(c, e, "embed launch");
   }
   auto trace = [&](int entry) -> cudaError_t {
