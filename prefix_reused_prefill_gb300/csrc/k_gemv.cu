@@ -33,7 +33,8 @@
 //     pair (j, j + d/2) is in the tile: RoPE at the row's position, bf16,
 //     q to the KV-head-major q buffer, K rows and V^T columns to the slot
 //     (goinfer "What goinfer does": one key and one value row per token and layer);
-//   * Resid: h += y in fp32, and on the last layer out = bf16(h).  The
+//   * Resid (applied as the contributions are added, with the residual row
+//     loaded alongside them): h += y in fp32, and on the last layer out = bf16(h).  The
 //     RMSNorm that follows needs the whole row, which no tile has; it is
 //     deferred instead: the tile writes a = bf16(h * gain) and its share of
 //     sum(h^2) per row, and the next projection, linear in a, multiplies its
@@ -154,46 +155,38 @@ __device__ __forceinline__ void epi_qkv(const GemvParams& p, const GemvSeg& seg,
   }
 }
 
-// h += y; with a gain, also the deferred RMSNorm input of the next projection:
-// a = bf16(h * gain) and this tile's sum of h^2 per row.  A warp covers one
-// row's 128 columns per pass, so the tile's sum is one warp reduction in a
-// fixed order.
-__device__ __forceinline__ void epi_resid(const GemvParams& p, int row0, const float* ct, int tid) {
-  static_assert(kGemvRows / 4 == 32, "one warp per row of the tile");
-  const int nv = min(kGemvRows, p.H - row0);
-  for (int idx = tid; idx < p.mb * (kGemvRows / 4); idx += kConsumers) {
-    const int t = idx / (kGemvRows / 4), c4 = (idx % (kGemvRows / 4)) * 4;
-    const long long i = p.c0 + t;
-    float ss = 0.f;
-    if (c4 < nv) {
-      float4* hp = reinterpret_cast<float4*>(p.h + i * p.H + row0 + c4);
-      const float4 y = *reinterpret_cast<const float4*>(ct + t * kTileLd + c4);
-      float4 hv = *hp;
-      hv.x += y.x; hv.y += y.y; hv.z += y.z; hv.w += y.w;
-      *hp = hv;
-      if (p.out) {
-        uint2 o;
-        o.x = dev::pack_bf16x2(hv.x, hv.y);
-        o.y = dev::pack_bf16x2(hv.z, hv.w);
-        *reinterpret_cast<uint2*>(p.out + i * p.ldout + row0 + c4) = o;
-      }
-      if (p.gain) {
-        const uint2 gw = *reinterpret_cast<const uint2*>(p.gain + row0 + c4);
-        const __nv_bfloat162 g01 = *reinterpret_cast<const __nv_bfloat162*>(&gw.x);
-        const __nv_bfloat162 g23 = *reinterpret_cast<const __nv_bfloat162*>(&gw.y);
-        uint2 o;
-        o.x = dev::pack_bf16x2(hv.x * __bfloat162float(g01.x), hv.y * __bfloat162float(g01.y));
-        o.y = dev::pack_bf16x2(hv.z * __bfloat162float(g23.x), hv.w * __bfloat162float(g23.y));
-        *reinterpret_cast<uint2*>(p.a + i * p.H + row0 + c4) = o;
-        ss = hv.x * hv.x + hv.y * hv.y + hv.z * hv.z + hv.w * hv.w;
-      }
-    }
-    if (p.gain) {
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-      if ((tid & 31) == 0) p.ss_out[i * p.nss + row0 / kGemvRows] = ss;
-    }
+// Resid, one float4 of row i (columns row0 + c4 .. +3): h = h_old + y, the
+// final bf16 output on the last layer, and with a gain the deferred RMSNorm
+// input of the next projection, a = bf16(h * gain); returns the float4's
+// share of sum(h^2) (0 without a gain).  The tile's sum per row is one warp
+// reduction in a fixed order (a warp covers one row's 128 columns).
+__device__ __forceinline__ float resid_apply(const GemvParams& p, int row0, long long i, int c4, float4 hv,
+                                             const float4& y) {
+  hv.x += y.x; hv.y += y.y; hv.z += y.z; hv.w += y.w;
+  *reinterpret_cast<float4*>(p.h + i * p.H + row0 + c4) = hv;
+  if (p.out) {
+    uint2 o;
+    o.x = dev::pack_bf16x2(hv.x, hv.y);
+    o.y = dev::pack_bf16x2(hv.z, hv.w);
+    *reinterpret_cast<uint2*>(p.out + i * p.ldout + row0 + c4) = o;
   }
+  if (!p.gain) return 0.f;
+  const uint2 gw = *reinterpret_cast<const uint2*>(p.gain + row0 + c4);
+  const __nv_bfloat162 g01 = *reinterpret_cast<const __nv_bfloat162*>(&gw.x);
+  const __nv_bfloat162 g23 = *reinterpret_cast<const __nv_bfloat162*>(&gw.y);
+  uint2 o;
+  o.x = dev::pack_bf16x2(hv.x * __bfloat162float(g01.x), hv.y * __bfloat162float(g01.y));
+  o.y = dev::pack_bf16x2(hv.z * __bfloat162float(g23.x), hv.w * __bfloat162float(g23.y));
+  *reinterpret_cast<uint2*>(p.a + i * p.H + row0 + c4) = o;
+  return hv.x * hv.x + hv.y * hv.y + hv.z * hv.z + hv.w * hv.w;
+}
+
+__device__ __forceinline__ void resid_tile_sum(const GemvParams& p, int row0, long long i, float ss, int lane) {
+  static_assert(kGemvRows / 4 == 32, "one warp per row of the tile");
+  if (!p.gain) return;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  if (lane == 0) p.ss_out[i * p.nss + row0 / kGemvRows] = ss;
 }
 
 __device__ __forceinline__ void epi_swiglu(const GemvParams& p, int row0, const float* ct, int tid) {
@@ -553,7 +546,9 @@ __global__ void __launch_bounds__(kThreads, NT == 4 ? 1 : 2) gemv_int4_kernel(co
   // publish every contribution of this CTA, then count one arrival per tile
   // touched (one thread per tile); the last arrival owns the tile's epilogue.
   // The barrier orders every consumer's partial stores before the counting
-  // threads' gpu-scope fence (fences are cumulative), so only they fence.
+  // thread's acquire-release add (release is cumulative); its acquire side,
+  // passed on by the barriers below, orders the other CTAs' partials before
+  // this CTA's reads of them.
   consumers_sync();
   {
     const int t_first = u0 / p.ksteps, t_last = (u1 - 1) / p.ksteps;
@@ -561,8 +556,7 @@ __global__ void __launch_bounds__(kThreads, NT == 4 ? 1 : 2) gemv_int4_kernel(co
     if (tile <= t_last && !*abort_v) {
       const long long tu0 = (long long)tile * p.ksteps;
       const int ncon = unit_owner(tu0 + p.ksteps - 1, units, p.ctas) - unit_owner(tu0, units, p.ctas) + 1;
-      __threadfence();
-      const int done = atomicAdd(p.counters + tile, 1) + 1;
+      const int done = dev::atom_add_acq_rel(p.counters + tile, 1) + 1;
       if (done == ncon) {
         p.counters[tile] = 0;   // ready for the next launch
         const int k = atomicAdd(&n_own, 1);
@@ -582,11 +576,17 @@ __global__ void __launch_bounds__(kThreads, NT == 4 ? 1 : 2) gemv_int4_kernel(co
     const long long tu0 = (long long)tile * p.ksteps;
     const int first = unit_owner(tu0, units, p.ctas);
     const int ncon = unit_owner(tu0 + p.ksteps - 1, units, p.ctas) - first + 1;
-    __threadfence();
+    const int s = tile_seg<kPair>(p, tile);
+    const int row0 = tile_row0<kPair>(p, tile, s);
+    const int nv_h = EPI == kGemvEpiResid ? min(kGemvRows, p.H - row0) : 0;
     const float* t0p = p.part + (long long)tile * p.maxc * (kGemvMaxCols * kGemvRows);
     for (int idx = tid; idx < p.mb * (kGemvRows / 4); idx += kConsumers) {
       const int tok = idx / (kGemvRows / 4), r4 = (idx % (kGemvRows / 4)) * 4;
       const float* src = t0p + tok * kGemvRows + r4;
+      // Resid: the residual row's float4 travels with the contributions
+      float4 h_old = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (EPI == kGemvEpiResid && r4 < nv_h)
+        h_old = __ldcg(reinterpret_cast<const float4*>(p.h + (long long)(p.c0 + tok) * p.H + row0 + r4));
       // all contributions in flight at once, then added in contributor order
       // (the sum does not depend on which CTA arrived last)
       float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -606,13 +606,16 @@ __global__ void __launch_bounds__(kThreads, NT == 4 ? 1 : 2) gemv_int4_kernel(co
         const float f = row_scale[tok];
         v.x *= f; v.y *= f; v.z *= f; v.w *= f;
       }
-      *reinterpret_cast<float4*>(ct + tok * kTileLd + r4) = v;
+      if (EPI == kGemvEpiResid) {   // epilogue in place: no trip through shared memory
+        const float ss = r4 < nv_h ? resid_apply(p, row0, p.c0 + tok, r4, h_old, v) : 0.f;
+        resid_tile_sum(p, row0, p.c0 + tok, ss, lane);
+      } else {
+        *reinterpret_cast<float4*>(ct + tok * kTileLd + r4) = v;
+      }
     }
+    if (EPI == kGemvEpiResid) continue;
     consumers_sync();
-    const int s = tile_seg<kPair>(p, tile);
-    const int row0 = tile_row0<kPair>(p, tile, s);
     if (EPI == kGemvEpiQKV) epi_qkv(p, p.seg[s], s, row0, ct, tid);
-    else if (EPI == kGemvEpiResid) epi_resid(p, row0, ct, tid);
     else if (EPI == kGemvEpiSwiglu) epi_swiglu(p, row0, ct, tid);
     else if (EPI == kGemvEpiArgmax) epi_argmax(p, p.seg[s], tile, row0, ct, tid);
     else epi_cast(p, p.seg[s], row0, ct, tid);
