@@ -96,6 +96,65 @@ __device__ __forceinline__ bool visible(const RowInfo& ri, int j) {
   return ri.tok >= 0 && (j < ri.pre || (j >= ri.lo && j <= ri.hi));
 }
 
+// One warp merges the key splits' (O, max, sum) partials of one (token, head)
+// row: lane s holds split s's (max, sum) (lane s-32 split s for ns > 32), the
+// split weights are broadcast with shuffles, and each lane accumulates D/32
+// consecutive elements over the splits in split order, NS splits' slices in
+// flight at a time.  rows: rows per split plane; rowidx: this row's index.
+template <int D, int NS>
+__device__ __forceinline__ void merge_splits(const float* opart, const float2* mlp, long long rows,
+                                             long long rowidx, int ns, __nv_bfloat16* dst, int lane) {
+  constexpr int E = D / 32;
+  static_assert(kMaxSplits <= 64, "two split records per lane");
+  const float* src = opart + rowidx * D + lane * E;
+  const long long sstride = rows * D;
+  // the first batch is requested before the split weights are formed
+  float v[NS][E];
+  auto load = [&](int s0) {
+#pragma unroll
+    for (int j = 0; j < NS; ++j)
+      if (s0 + j < ns) {
+        if (E == 4) {
+          const float4 x = __ldcg(reinterpret_cast<const float4*>(src + (s0 + j) * sstride));
+          v[j][0] = x.x; v[j][1 % E] = x.y; v[j][2 % E] = x.z; v[j][3 % E] = x.w;
+        } else {
+          const float2 x = __ldcg(reinterpret_cast<const float2*>(src + (s0 + j) * sstride));
+          v[j][0] = x.x; v[j][1 % E] = x.y;
+        }
+      }
+  };
+  load(0);
+  const float2 ml0 = lane < ns ? __ldcg(mlp + lane * rows + rowidx) : make_float2(-INFINITY, 0.f);
+  const float2 ml1 = lane + 32 < ns ? __ldcg(mlp + (lane + 32) * rows + rowidx) : make_float2(-INFINITY, 0.f);
+  float M = fmaxf(ml0.x, ml1.x);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  const float w0 = ml0.x == -INFINITY ? 0.f : exp2f(ml0.x - M);
+  const float w1 = ml1.x == -INFINITY ? 0.f : exp2f(ml1.x - M);
+  float den = w0 * ml0.y + w1 * ml1.y;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+  float acc[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) acc[e] = 0.f;
+  for (int s0 = 0; s0 < ns; s0 += NS) {
+    if (s0 > 0) load(s0);
+#pragma unroll
+    for (int j = 0; j < NS; ++j)
+      if (s0 + j < ns) {
+        const int sp = s0 + j;
+        const float w = __shfl_sync(0xffffffffu, sp < 32 ? w0 : w1, sp & 31);
+#pragma unroll
+        for (int e = 0; e < E; ++e) acc[e] += w * v[j][e];
+      }
+  }
+  const float inv = 1.f / den;
+  dst += rowidx * D + lane * E;
+#pragma unroll
+  for (int e = 0; e < E; e += 2)
+    *reinterpret_cast<uint32_t*>(dst + e) = dev::pack_bf16x2(acc[e] * inv, acc[e + 1] * inv);
+}
+
 template <int D, int RW, int KW>
 __global__ void __launch_bounds__((RW * KW + 1) * 32) attn_kernel(const __grid_constant__ AttnParams p) {
   static_assert(KW == 1 || RW == 1, "key-parallel warps serve one row tile");
@@ -338,7 +397,10 @@ __global__ void __launch_bounds__((RW * KW + 1) * 32) attn_kernel(const __grid_c
       }
     }
     asm volatile("bar.sync 1, %0;" ::"r"(kCons * 32) : "memory");
-    if (kw != 0 || *abort_v) return;
+    // with p.counters the other warps stay for the merge of the splits below
+    // (every warp then reaches its barriers, aborted or not)
+    if (kw != 0 && !(p.counters && v.nsplit > 1)) return;
+    if (kw == 0 && !*abort_v)
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int row = r + 8 * h;
@@ -369,11 +431,11 @@ __global__ void __launch_bounds__((RW * KW + 1) * 32) attn_kernel(const __grid_c
       lrow[h] = L;
     }
   }
-  if (*abort_v) return;
+  if (KW == 1 && *abort_v) return;
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     const RowInfo& ri = h == 0 ? ri0 : ri1;
-    if (ri.tok < 0) continue;
+    if (kw != 0 || ri.tok < 0 || *abort_v) continue;
     const long long rowidx = (long long)ri.tok * p.Hq + ri.head;
     if (v.nsplit == 1) {
       const float inv = 1.f / lrow[h];
@@ -389,6 +451,33 @@ __global__ void __launch_bounds__((RW * KW + 1) * 32) attn_kernel(const __grid_c
       for (int i = 0; i < D / 8; ++i)
         *reinterpret_cast<float2*>(dst + 8 * i + 2 * c) = make_float2(o[i][2 * h], o[i][2 * h + 1]);
       if (c == 0) v.ml[split * plane + rowidx] = make_float2(mrow[h], lrow[h]);
+    }
+  }
+  if constexpr (KW > 1) {
+    // The last split to finish this (row tile, KV head) merges every split's
+    // partials (split order, as the combine kernel does), the KW warps taking
+    // alternate rows.  The barrier orders warp 0's partial stores before the
+    // counting thread's acquire-release add; its acquire side, passed on by
+    // the second barrier, orders the other splits' partials before the loads.
+    if (!p.counters || v.nsplit == 1) return;
+    __shared__ int last_split;
+    asm volatile("bar.sync 1, %0;" ::"r"(kCons * 32) : "memory");
+    if (threadIdx.x == 0) {   // an aborted CTA does not count: its row tile is left unmerged
+      last_split = 0;
+      if (!*abort_v) {
+        int* ctr = p.counters + (long long)blockIdx.x * p.Hkv + kv;
+        const int done = dev::atom_add_acq_rel(ctr, 1) + 1;
+        last_split = done == v.nsplit;
+        if (done == v.nsplit) *ctr = 0;   // ready for the next launch
+      }
+    }
+    asm volatile("bar.sync 1, %0;" ::"r"(kCons * 32) : "memory");
+    if (!last_split) return;
+    const long long plane = (long long)v.m * p.Hq;
+    for (int rho = row_lo + kw; rho < row_hi; rho += KW) {
+      const RowInfo ri = row_info(p, v, kv, rho);
+      if (ri.tok < 0) continue;
+      merge_splits<D, 16>(v.opart, v.ml, plane, (long long)ri.tok * p.Hq + ri.head, v.nsplit, v.o, lane);
     }
   }
 }
@@ -421,57 +510,8 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const __grid_constant
     opart += cv.part0;
     mlp += cv.part0 / D;
   }
-  const int lane = threadIdx.x & 31;
-  constexpr int E = D / 32;
-  static_assert(kMaxSplits <= 64, "two split records per lane");
-  const float* src = opart + rowidx * D + lane * E;
-  const long long sstride = rows * D;
-  // NS splits' slices in flight at a time, added in split order; the first
-  // batch is requested before the split weights are formed
-  float v[NS][E];
-  auto load = [&](int s0) {
-#pragma unroll
-    for (int j = 0; j < NS; ++j)
-      if (s0 + j < ns) {
-        if (E == 4) {
-          const float4 x = __ldcg(reinterpret_cast<const float4*>(src + (s0 + j) * sstride));
-          v[j][0] = x.x; v[j][1 % E] = x.y; v[j][2 % E] = x.z; v[j][3 % E] = x.w;
-        } else {
-          const float2 x = __ldcg(reinterpret_cast<const float2*>(src + (s0 + j) * sstride));
-          v[j][0] = x.x; v[j][1 % E] = x.y;
-        }
-      }
-  };
-  load(0);
-  const float2 ml0 = lane < ns ? mlp[lane * rows + rowidx] : make_float2(-INFINITY, 0.f);
-  const float2 ml1 = lane + 32 < ns ? mlp[(lane + 32) * rows + rowidx] : make_float2(-INFINITY, 0.f);
-  float M = fmaxf(ml0.x, ml1.x);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-  const float w0 = ml0.x == -INFINITY ? 0.f : exp2f(ml0.x - M);
-  const float w1 = ml1.x == -INFINITY ? 0.f : exp2f(ml1.x - M);
-  float den = w0 * ml0.y + w1 * ml1.y;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
-  float acc[E];
-#pragma unroll
-  for (int e = 0; e < E; ++e) acc[e] = 0.f;
-  for (int s0 = 0; s0 < ns; s0 += NS) {
-    if (s0 > 0) load(s0);
-#pragma unroll
-    for (int j = 0; j < NS; ++j)
-      if (s0 + j < ns) {
-        const int sp = s0 + j;
-        const float w = __shfl_sync(0xffffffffu, sp < 32 ? w0 : w1, sp & 31);
-#pragma unroll
-        for (int e = 0; e < E; ++e) acc[e] += w * v[j][e];
-      }
-  }
-  const float inv = 1.f / den;
-  __nv_bfloat16* dst = p.o + grow * D + lane * E;
-#pragma unroll
-  for (int e = 0; e < E; e += 2)
-    *reinterpret_cast<uint32_t*>(dst + e) = dev::pack_bf16x2(acc[e] * inv, acc[e + 1] * inv);
+  // row rowidx of the conversation's planes is row grow of the call's o
+  merge_splits<D, NS>(opart, mlp, rows, rowidx, ns, p.o + (grow - rowidx) * D, threadIdx.x & 31);
 }
 
 template <int D, int RW, int KW = 1>

@@ -34,6 +34,8 @@ namespace {
 
 constexpr size_t kAlign = 256;
 constexpr int kCounters = 16384;   // per-tile arrival counters of the fused GEMV epilogues
+// then per (row tile, KV head) arrival counters of the split-KV attention's own merge
+constexpr int kAttnCounters = 4096;
 constexpr int kVerifyMaxRows = 64; // rows of one verify call
 inline size_t align_up(size_t x, size_t a = kAlign) { return (x + a - 1) / a * a; }
 
@@ -114,7 +116,7 @@ ScratchLayout scratch_layout(const kvr_config* c) {
   size_t off = 0;
   auto take = [&](size_t bytes) { size_t at = off; off = align_up(off + std::max<size_t>(bytes, 1)); return at; };
   L.status = take(64);
-  L.counters = take(kCounters * 4);
+  L.counters = take((kCounters + kAttnCounters) * 4);
   L.prompt = take((size_t)c->capacity * 4);
   L.slot_len = take(KVR_MAX_SLOTS * 4);
   L.match_out = take((size_t)(S + 1) * S * 4);
@@ -212,12 +214,16 @@ struct kvr_ctx {
   // slot table
   SlotState slots[KVR_MAX_SLOTS];
   unsigned long long clock = 0;
-  std::vector<int32_t> host_match;
+  // the match lengths read back by kvr_slot_match, [(slots + 1) * slots]; pinned,
+  // so the read-back is one DMA straight into it
+  int32_t* host_match = nullptr;
+  size_t host_match_n = 0;
   // profiling
   bool prof = false;
   float* trace = nullptr;   // [n_layers + 1][max_rows][hidden] float32, or null
   bool force_gemv = false;  // KVR_FORCE_GEMV=1: keep every m on the GEMV path
   bool force_gemm = false;  // KVR_FORCE_GEMM=1: every m on the tcgen05 GEMM (a GEMV-free process)
+  bool attn_combine = false; // KVR_ATTN_COMBINE=1: small-m split-KV partials merged by the combine launch
   int attn_splits = 0;      // KVR_ATTN_SPLITS=n: fixed key-split count of the tcgen05 attention
   std::vector<EventPair> pending;
   std::vector<cudaEvent_t> free_events;
@@ -593,6 +599,17 @@ int vt_row(const kvr_ctx* c, int slot, int layer) {
 
 // Attention of one slot's rows (tokens tok0 .. tok0 + rows.m of the call; a
 // batch runs one of these per conversation).
+// The split-KV kernel with one row tile per CTA (rw == 1: four key-parallel
+// warps) merges its own splits when a row tile has at most one row per warp
+// (R <= 4): the last split of each (row tile, KV head) does it, so no combine
+// launch follows.  With more rows each warp would merge them one after the
+// other, and the combine launch (a warp per row) is faster (measured at 12
+// and 16 rows: 2.57 / 2.63 ms per verify call against 2.50).
+bool own_merge(const kvr_ctx* c, int rw, int row_tiles, int rows_per_tile) {
+  return rw == 1 && rows_per_tile <= attn_key_warps(1) && !c->attn_combine &&
+         (long long)row_tiles * c->cfg.n_kv_heads <= kAttnCounters;
+}
+
 int attention(kvr_ctx* c, cudaStream_t st, int slot, int layer, const RowMap& rows, int tok0 = 0) {
   const kvr_config& k = c->cfg;
   AttnParams p;
@@ -635,6 +652,7 @@ int attention(kvr_ctx* c, cudaStream_t st, int slot, int layer, const RowMap& ro
   }
   while (ns > 1 && (size_t)ns * rows.m * k.n_q_heads * k.head_dim > c->sl.opart_floats) --ns;
   p.nsplit = ns;
+  p.counters = own_merge(c, tc ? 0 : attn_row_warps(R), p.row_tiles, R) ? c->counters + kCounters : nullptr;
   cudaError_t e;
   {
     Timed t(c, kAttn, st);
@@ -642,7 +660,7 @@ int attention(kvr_ctx* c, cudaStream_t st, int slot, int layer, const RowMap& ro
            : launch_attention(p, k.head_dim, attn_row_warps(R), st);
   }
   if (e != cudaSuccess) return cuda_fail(c, e, "attention launch");
-  if (ns > 1) {
+  if (ns > 1 && !p.counters) {
     Timed t(c, kAttn, st);
     e = launch_attn_combine(p, k.head_dim, st);
     if (e != cudaSuccess) return cuda_fail(c, e, "attention combine launch");
@@ -721,13 +739,14 @@ int attention_batch(kvr_ctx* c, cudaStream_t st, int layer, const RowMap& rows, 
     }
     p.nsplit = std::max(p.nsplit, p.conv[i].nsplit);
   }
+  p.counters = own_merge(c, rw, tiles, rmax) ? c->counters + kCounters : nullptr;
   cudaError_t e;
   {
     Timed t(c, kAttn, st);
     e = launch_attention(p, k.head_dim, rw, st);
   }
   if (e != cudaSuccess) return cuda_fail(c, e, "attention launch");
-  if (combine) {
+  if (combine && !p.counters) {
     Timed t(c, kAttn, st);
     e = launch_attn_combine(p, k.head_dim, st);
     if (e != cudaSuccess) return cuda_fail(c, e, "attention combine launch");
@@ -1144,6 +1163,8 @@ int kvr_ctx_create(const kvr_config* cfg, void* kv_arena, size_t arena_bytes, vo
   c->force_gemv = fg && fg[0] == '1';
   const char* fm = getenv("KVR_FORCE_GEMM");
   c->force_gemm = fm && fm[0] == '1';
+  const char* ac = getenv("KVR_ATTN_COMBINE");
+  c->attn_combine = ac && ac[0] == '1';
   const char* as = getenv("KVR_ATTN_SPLITS");
   c->attn_splits = as ? atoi(as) : 0;
   c->requested = cfg->n_slots;
@@ -1220,14 +1241,18 @@ int kvr_ctx_create(const kvr_config* cfg, void* kv_arena, size_t arena_bytes, vo
   // Positions past a slot's length are read (and multiplied by a zero weight)
   // when a key block is partly visible; zero the arena once so they are finite.
   e = cudaMemset(c->status, 0, 64);
-  if (e == cudaSuccess) e = cudaMemset(c->counters, 0, kCounters * 4);
+  if (e == cudaSuccess) e = cudaMemset(c->counters, 0, (kCounters + kAttnCounters) * 4);
   if (e == cudaSuccess) e = cudaMemset(c->arena, 0, (size_t)c->granted * slot_kv_bytes(cfg));
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e != cudaSuccess) {
     delete c;
     return KVR_ERR_CUDA;
   }
-  c->host_match.resize((size_t)(c->granted + 1) * c->granted);
+  c->host_match_n = (size_t)(c->granted + 1) * c->granted;
+  if (cudaHostAlloc(&c->host_match, c->host_match_n * 4, cudaHostAllocDefault) != cudaSuccess) {
+    delete c;
+    return KVR_ERR_CUDA;
+  }
   *out = c;
   return KVR_OK;
 }
@@ -1247,6 +1272,7 @@ int kvr_ctx_destroy(kvr_ctx* c) {
     cudaEventDestroy(p.b);
   }
   for (auto e : c->free_events) cudaEventDestroy(e);
+  if (c->host_match) cudaFreeHost(c->host_match);
   delete c;
   return KVR_OK;
 }
@@ -1276,7 +1302,7 @@ int kvr_slot_match(kvr_ctx* c, const int32_t* tokens, int n, int* slot, int* reu
                             c->match_out, st);
   }
   if (e != cudaSuccess) return cuda_fail(c, e, "prefix match launch");
-  e = cudaMemcpyAsync(c->host_match.data(), c->match_out, c->host_match.size() * 4,
+  e = cudaMemcpyAsync(c->host_match, c->match_out, c->host_match_n * 4,
                       cudaMemcpyDeviceToHost, st);
   if (e == cudaSuccess) e = cudaStreamSynchronize(st);
   if (e != cudaSuccess) return cuda_fail(c, e, "match readback");
@@ -1543,7 +1569,7 @@ int kvr_sync_status(kvr_ctx* c, void* stream) {
   if (e != cudaSuccess) return cuda_fail(c, e, "status readback");
   if (word) {
     // a launch that gave up may have left tile counters behind
-    cudaMemsetAsync(c->counters, 0, kCounters * 4, st);
+    cudaMemsetAsync(c->counters, 0, (kCounters + kAttnCounters) * 4, st);
     cudaMemsetAsync(c->status, 0, 4, st);
     cudaStreamSynchronize(st);
     return fail(c, KVR_ERR_TIMEOUT, "a device-side wait gave up (status %d)", word);

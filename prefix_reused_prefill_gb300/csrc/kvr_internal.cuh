@@ -216,6 +216,10 @@ struct AttnParams {
   int row_tiles;
   float scale_log2;          // log2(e) / sqrt(d)
   int* status;
+  // split-KV kernel with one row tile (R <= 16): arrival counters per (row
+  // tile, KV head), zero between launches; the last split merges the splits
+  // and writes o itself (no combine launch).  Null: the combine kernel merges.
+  int* counters;
   // batched conversations (split-KV kernel and combine only): n_conv > 0
   // replaces rows/kbase/vtbase/nsplit/q/o by each CTA's conversation
   int n_conv;

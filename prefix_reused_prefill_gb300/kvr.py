@@ -6,10 +6,12 @@ library is not built this module raises on first use -- there is no fallback.
 """
 from __future__ import annotations
 
+import array
 import ctypes
 import os
 from typing import Dict, List, Optional, Sequence, Tuple
 
+import numpy as np
 import torch
 
 HERE = os.path.dirname(os.path.abspath(__file__))
@@ -159,8 +161,22 @@ def head_weight_struct(head: Dict[str, object]):
 
 
 def _i32(tokens) -> ctypes.Array:
-    t = [int(x) for x in tokens]
-    return (ctypes.c_int32 * max(len(t), 1))(*t)
+    """Token ids as a C int32 array (at least one element) that shares memory
+    with one contiguous copy: an int32 numpy array is passed as it is, a list
+    goes through array('i') (a per-element ctypes constructor costs ~60 us for
+    254 tokens, on the path between a match and the prefill it decides)."""
+    if isinstance(tokens, np.ndarray):
+        a = np.ascontiguousarray(tokens, dtype=np.int32)
+        if a.size == 0:
+            a = np.zeros(1, np.int32)
+        return (ctypes.c_int32 * a.size).from_buffer(a)
+    a = array.array("i", tokens)
+    if not a:
+        a.append(0)
+    return (ctypes.c_int32 * len(a)).from_buffer(a)
+
+
+assert array.array("i").itemsize == 4, "C int must be 32 bits"
 
 
 class Kvr:

@@ -118,6 +118,38 @@ def test_suffix_prefill_matches_oracle(shape_name, P, ms, cap):
     assert kv.kvr_slot_len(0) == P + ms[-1]
 
 
+@pytest.mark.parametrize("combine", ["0", "1"])
+@pytest.mark.parametrize("shape_name", ["small", "small_d128"])
+def test_split_kv_merge_matches_oracle(monkeypatch, shape_name, combine):
+    """A 700-token prefix gives the small-m split-KV kernel several key splits per
+    KV head.  With at most four rows per KV head (m = 1 here: G = 4 and 3) the
+    last split of each (row tile, KV head) merges them; more rows, or
+    KVR_ATTN_COMBINE=1, leave the merge to the combine launch.  Both against
+    the oracle, with the new rows' K/V."""
+    monkeypatch.setenv("KVR_ATTN_COMBINE", combine)
+    shape, kv, w, W, _ = make(shape_name, 1, 1024, 256)
+    monkeypatch.delenv("KVR_ATTN_COMBINE")
+    dims = oracle_dims(shape)
+    P = 700
+    toks = list(range(2000, 2000 + P + 8))
+    x = hidden(toks, shape)
+    cache = om.SlotKV(shape.n_layers, shape.n_kv_heads, 1024, shape.head_dim)
+    whole = om.prefill(dims, W, cache, workloads.bf16_to_f64(x), 0)
+    kv.kvr_slot_match(toks[:1])
+    for a in range(0, P, 256):
+        b = min(P, a + 256)
+        kv.kvr_prefill_suffix(0, toks[a:b], x[a:b].cuda(), w)
+    for m in (1, 3, 8):
+        kv.kvr_slot_truncate(0, P)
+        out = kv.kvr_prefill_suffix(0, toks[P:P + m], x[P:P + m].cuda(), w)
+        kv.kvr_sync_status()
+        close(workloads.bf16_to_f64(out), whole[P:P + m], f"{shape_name} merge {combine} m={m}")
+        for l in range(shape.n_layers):
+            k, v = slot_kv_f64(kv, 0, l, P + m)
+            close(k[:, P:], cache.K[l][:, P:P + m], f"{shape_name} m={m} new K layer {l}")
+            close(v[:, P:], cache.V[l][:, P:P + m], f"{shape_name} m={m} new V layer {l}")
+
+
 @pytest.mark.parametrize("shape_name", ["small", "small_q4k"])
 def test_small_m_on_the_tensor_core_gemm_matches_oracle(monkeypatch, shape_name):
     """KVR_FORCE_GEMM=1 sends every m to the tcgen05 GEMM (N = 16 for up to 16 rows)."""
