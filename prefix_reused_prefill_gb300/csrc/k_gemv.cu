@@ -117,8 +117,10 @@ __device__ __forceinline__ void consumers_sync() { asm volatile("bar.sync 1, 256
 // ---------------------------------------------------------------- epilogues
 // ct: the tile's fp32 results [token][kTileLd] for tokens < p.mb
 
+// rope_s: the pass's rows of the RoPE table, [token][d/2] (staged in shared
+// memory at the start of the launch)
 __device__ __forceinline__ void epi_qkv(const GemvParams& p, const GemvSeg& seg, int s, int row0,
-                                        const float* ct, int tid) {
+                                        const float* ct, const float2* rope_s, int tid) {
   const int d = p.d, half = d >> 1;
   const int nv = min(kGemvRows, seg.N - row0);
   const int hd0 = row0 / d;
@@ -132,7 +134,7 @@ __device__ __forceinline__ void epi_qkv(const GemvParams& p, const GemvSeg& seg,
       const float x1 = ct[t * kTileLd + col];
       const float x2 = ct[t * kTileLd + col + half];
       const int i = p.c0 + t;
-      const float2 cs = p.rope[(long long)i * half + j];
+      const float2 cs = rope_s[t * half + j];
       const float y1 = x1 * cs.x - x2 * cs.y;
       const float y2 = x2 * cs.x + x1 * cs.y;
       const int hd = hd0 + hh;
@@ -489,6 +491,10 @@ __global__ void __launch_bounds__(kThreads, NT == 4 ? 1 : 2) gemv_int4_kernel(co
   // K-quant: per warp and stage, (d*sc, dmin*mn) of its 16 rows x 8 sub-blocks
   __shared__ float2 q4k_tab[FMT == kFmtQ4K ? kConsumerWarps * 128 : 1];
   __shared__ float row_scale[kGemvMaxCols];   // deferred RMSNorm of the input rows
+  // QKV up to 8 tokens: the rows' (cos, sin), d <= 128 (more rows would cost
+  // the second CTA per SM its shared memory; they read the table directly)
+  constexpr bool kRopeS = EPI == kGemvEpiQKV && NT == 1;
+  __shared__ float2 rope_s[kRopeS ? C::kXRows * 64 : 1];
   volatile int* abort_v = &abort_flag;
 
   const uint32_t base = (dev::smem_u32(smem_raw) + 1023u) & ~1023u;
@@ -521,6 +527,9 @@ __global__ void __launch_bounds__(kThreads, NT == 4 ? 1 : 2) gemv_int4_kernel(co
   dev::pdl_wait();                  // results are written below
   const int tid = threadIdx.x;      // 0..255 over the consumer warps
   row_scales(p, row_scale);
+  if (kRopeS)   // off the epilogue's path: loaded while the activations arrive
+    for (int idx = tid; idx < p.mb * (p.d >> 1); idx += kConsumers)
+      rope_s[idx] = p.rope[(long long)p.c0 * (p.d >> 1) + idx];
   const int r = lane >> 2, c = lane & 3;
   const int rho0 = warp * 16 + r;
   float acc[NT][4];
@@ -615,7 +624,7 @@ __global__ void __launch_bounds__(kThreads, NT == 4 ? 1 : 2) gemv_int4_kernel(co
     }
     if (EPI == kGemvEpiResid) continue;
     consumers_sync();
-    if (EPI == kGemvEpiQKV) epi_qkv(p, p.seg[s], s, row0, ct, tid);
+    if (EPI == kGemvEpiQKV) epi_qkv(p, p.seg[s], s, row0, ct, kRopeS ? rope_s : p.rope + (long long)p.c0 * (p.d >> 1), tid);
     else if (EPI == kGemvEpiSwiglu) epi_swiglu(p, row0, ct, tid);
     else if (EPI == kGemvEpiArgmax) epi_argmax(p, p.seg[s], tile, row0, ct, tid);
     else epi_cast(p, p.seg[s], row0, ct, tid);
@@ -668,6 +677,15 @@ __global__ void __launch_bounds__(256) gemv_bf16_kernel(const __grid_constant__ 
 
 }  // namespace
 
+namespace {
+// resident CTAs per SM of each (NT, EPI, FMT) variant, from the occupancy API
+int g_per_sm[3][5][2];
+}  // namespace
+
+int gemv_int4_per_sm(int nt, int epi, int fmt) {
+  return g_per_sm[nt == 1 ? 0 : (nt == 2 ? 1 : 2)][epi][fmt == kFmtQ4K ? 1 : 0];
+}
+
 int gemv_int4_smem(int nt) {
   switch (nt) {
     case 1: return GemvCfg<1>::kSmem;
@@ -685,9 +703,13 @@ cudaError_t setup_nt() {
       gemv_int4_kernel<NT, 3, kFmtInt4>, gemv_int4_kernel<NT, 4, kFmtInt4>, gemv_int4_kernel<NT, 0, kFmtQ4K>,
       gemv_int4_kernel<NT, 1, kFmtQ4K>, gemv_int4_kernel<NT, 2, kFmtQ4K>, gemv_int4_kernel<NT, 3, kFmtQ4K>,
       gemv_int4_kernel<NT, 4, kFmtQ4K>};
-  for (auto k : ks) {
-    const cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, GemvCfg<NT>::kSmem);
+  const int ni = NT == 1 ? 0 : (NT == 2 ? 1 : 2);
+  for (int i = 0; i < 10; ++i) {
+    cudaError_t e = cudaFuncSetAttribute(ks[i], cudaFuncAttributeMaxDynamicSharedMemorySize, GemvCfg<NT>::kSmem);
+    int n = 0;
+    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, ks[i], kThreads, GemvCfg<NT>::kSmem);
     if (e != cudaSuccess) return e;
+    g_per_sm[ni][i % 5][i / 5] = n;
   }
   return cudaSuccess;
 }

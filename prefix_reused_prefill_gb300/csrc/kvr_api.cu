@@ -504,7 +504,9 @@ int project_gemv_int4(kvr_ctx* c, cudaStream_t st, const Seg* segs, int nseg, co
     p.c0 = c0;
     p.mb = mb;
     const int nt = mb <= 8 ? 1 : (mb <= 16 ? 2 : 4);
-    const int per_sm = nt == 4 ? 1 : 2;   // CTAs resident per SM (shared memory, registers)
+    // CTAs resident per SM (shared memory, registers): 2 up to 16 tokens, 1
+    // beyond, and 1 where a variant's shared memory leaves no room for a second
+    const int per_sm = std::max(1, gemv_int4_per_sm(nt, p.epi, p.fmt));
     p.tx = tmx[nt == 1 ? 0 : (nt == 2 ? 1 : 2)];
     // one resident wave of CTAs, each an equal run of (tile, k-step) units
     const int units = tiles * p.ksteps;

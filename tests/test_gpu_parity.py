@@ -118,6 +118,34 @@ def test_suffix_prefill_matches_oracle(shape_name, P, ms, cap):
     assert kv.kvr_slot_len(0) == P + ms[-1]
 
 
+@pytest.mark.parametrize("shape_name", ["small", "small_q4k"])
+def test_many_rows_on_the_gemv_match_oracle(monkeypatch, shape_name):
+    """KVR_FORCE_GEMV=1 keeps every m on the GEMV (32-row passes) and the split-KV
+    attention: the deferred RMSNorm then spans passes (each pass reads and
+    writes its own rows' sums)."""
+    monkeypatch.setenv("KVR_FORCE_GEMV", "1")
+    shape, kv, w, W, _ = make(shape_name, 1, 256, 128)
+    monkeypatch.delenv("KVR_FORCE_GEMV")
+    dims = oracle_dims(shape)
+    P = 50
+    toks = list(range(3000, 3000 + P + 70))
+    x = hidden(toks, shape)
+    cache = om.SlotKV(shape.n_layers, shape.n_kv_heads, 256, shape.head_dim)
+    whole = om.prefill(dims, W, cache, workloads.bf16_to_f64(x), 0)
+    kv.kvr_slot_match(toks[:1])
+    pre = kv.kvr_prefill_suffix(0, toks[:P], x[:P].cuda(), w)
+    close(workloads.bf16_to_f64(pre), whole[:P], f"{shape_name} GEMV prefix rows")
+    for m in (1, 40, 70):
+        kv.kvr_slot_truncate(0, P)
+        out = kv.kvr_prefill_suffix(0, toks[P:P + m], x[P:P + m].cuda(), w)
+        kv.kvr_sync_status()
+        close(workloads.bf16_to_f64(out), whole[P:P + m], f"{shape_name} GEMV m={m}")
+        for l in range(shape.n_layers):
+            k, v = slot_kv_f64(kv, 0, l, P + m)
+            close(k, cache.K[l][:, :P + m], f"{shape_name} GEMV m={m} K layer {l}")
+            close(v, cache.V[l][:, :P + m], f"{shape_name} GEMV m={m} V layer {l}")
+
+
 @pytest.mark.parametrize("combine", ["0", "1"])
 @pytest.mark.parametrize("shape_name", ["small", "small_d128"])
 def test_split_kv_merge_matches_oracle(monkeypatch, shape_name, combine):
