@@ -169,6 +169,8 @@ def _i32(tokens) -> ctypes.Array:
         a = np.ascontiguousarray(tokens, dtype=np.int32)
         if a.size == 0:
             a = np.zeros(1, np.int32)
+        elif not a.flags.writeable:   # from_buffer needs a writable buffer
+            a = a.copy()
         return (ctypes.c_int32 * a.size).from_buffer(a)
     a = array.array("i", tokens)
     if not a:

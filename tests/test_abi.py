@@ -154,3 +154,27 @@ def test_binding_fails_loudly_without_library(tmp_path):
             kvr.load_library(str(tmp_path / "missing.so"))
     finally:
         kvr._lib = saved
+
+
+def test_token_ids_marshal_to_int32_arrays():
+    """The binding hands token ids to the C ABI as one int32 array: a list goes
+    through a single array copy, an int32 numpy array is passed as it is, other
+    integer arrays are converted, an empty list still gives a valid pointer, and
+    ids outside int32 are refused rather than wrapped."""
+    import numpy as np
+    from prefix_reused_prefill_gb300.kvr import _i32
+    a = _i32([5, 0, 151935, 2**31 - 1])
+    assert isinstance(a, ctypes.Array) and ctypes.sizeof(a._type_) == 4
+    assert list(a) == [5, 0, 151935, 2**31 - 1]
+    assert list(_i32([np.int64(7), np.int32(3)])) == [7, 3]
+    assert list(_i32([])) == [0]
+    n32 = np.arange(10, 20, dtype=np.int32)
+    b = _i32(n32)
+    assert list(b) == list(range(10, 20))
+    assert ctypes.addressof(b) == n32.ctypes.data          # no copy
+    assert list(_i32(np.array([[1, 2], [3, 4]], dtype=np.int64))) == [1, 2, 3, 4]
+    ro = np.arange(3, dtype=np.int32)
+    ro.flags.writeable = False
+    assert list(_i32(ro)) == [0, 1, 2]
+    with pytest.raises(OverflowError):
+        _i32([2**31])
