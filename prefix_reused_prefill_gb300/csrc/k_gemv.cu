@@ -686,14 +686,6 @@ int gemv_int4_per_sm(int nt, int epi, int fmt) {
   return g_per_sm[nt == 1 ? 0 : (nt == 2 ? 1 : 2)][epi][fmt == kFmtQ4K ? 1 : 0];
 }
 
-int gemv_int4_smem(int nt) {
-  switch (nt) {
-    case 1: return GemvCfg<1>::kSmem;
-    case 2: return GemvCfg<2>::kSmem;
-    default: return GemvCfg<4>::kSmem;
-  }
-}
-
 namespace {
 
 template <int NT>

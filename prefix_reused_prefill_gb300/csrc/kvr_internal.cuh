@@ -292,7 +292,6 @@ cudaError_t launch_epi_cast(const float* part, long long plane, int ksplit, int 
                             int mb, int N, __nv_bfloat16* out, cudaStream_t st);
 
 // dynamic shared memory the launchers need (for cudaFuncSetAttribute at setup)
-int gemv_int4_smem(int nt);
 // resident CTAs per SM of the int4 GEMV for nt token tiles, epilogue and weight format
 int gemv_int4_per_sm(int nt, int epi, int fmt);
 int attn_key_warps(int row_warps);   // consumer warps per row tile taking alternate key blocks
