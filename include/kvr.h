@@ -360,7 +360,8 @@ int kvr_prefill_batch(kvr_ctx* ctx, int n_seq, const int* slots, const int* lens
 
 /* Wait for `stream` and check the device status word that kernels set when a
  * bounded device-side wait gives up.  Returns KVR_ERR_TIMEOUT (and clears the
- * word) if one did. */
+ * word and the kernels' arrival counters, so the next call starts clean) if
+ * one did; the outputs of the call that timed out are not to be used. */
 int kvr_sync_status(kvr_ctx* ctx, void* stream);
 
 /* Per-layer trace for checking a long stack one layer at a time.  While a
@@ -418,7 +419,8 @@ int kvr_verify_accept_batch(kvr_ctx* ctx, int n_seq, const int* slots, const int
  * wait on an mbarrier that nothing completes.  Like every wait in the
  * library's kernels it gives up after 1 s and records the timeout in the
  * status word; the next kvr_sync_status returns KVR_ERR_TIMEOUT, clears the
- * word and the GEMV arrival counters, and the context stays usable. */
+ * word and the arrival counters (projection tiles and attention splits), and
+ * the context stays usable. */
 int kvr_selftest_wait(kvr_ctx* ctx, void* stream);
 
 /* Per-kernel-class timing with CUDA events recorded on the launch stream.
