@@ -239,7 +239,11 @@ int kvr_slot_match(kvr_ctx* ctx, const int32_t* tokens, int n, int* slot, int* r
  *    KVR_ERR_CAPACITY and a message saying so; nothing is launched.
  *  - The first call on a device looks up the array's device address
  *    (cudaGetSymbolAddress) with that device current; make that first call
- *    before any stream capture on the device.
+ *    before any stream capture on the device.  The address is cached per
+ *    device for the life of the process: it does not survive a
+ *    cudaDeviceReset or any other teardown of the device's primary context.
+ *    After one, the next call returns a stale address; do not call this
+ *    entry point again in that process.
  *  - Every call, from every context on the device, shares the one array and
  *    leaves its contents behind.  Each call writes every word it reads
  *    before reading it, so nothing needs clearing; but calls that overlap on

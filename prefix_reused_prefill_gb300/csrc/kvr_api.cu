@@ -1009,6 +1009,66 @@ int greedy_accept(const int32_t* tokens, const int32_t* next, int m) {
   return a;
 }
 
+// ---------------------------------------------------------------- slot policy
+// The slot choice of goinfer "How it works" applied to the match kernel's
+// result res ([S][S+1]: res[s][S] = LCP of slot s with the prompt, res[a][b]
+// for a < b = LCP of slots a and b): the longest match wins if it is longer
+// than what that slot shares with any other occupied slot (and, with an empty
+// slot free, if it would not cut its conversation back); otherwise the lowest
+// empty slot, else the least recently used one, starts from zero.  The chosen
+// slot keeps min(match, n - 1) tokens and is touched.
+void apply_slot_policy(kvr_ctx* c, const int32_t* res, int n, int* slot, int* reused) {
+  const int S = c->granted;
+  const int W = S + 1;
+  auto pair = [&](int a, int b) { return a < b ? res[a * W + b] : res[b * W + a]; };
+  int l[KVR_MAX_SLOTS];
+  int best = -1;
+  bool any_empty = false;
+  for (int s = 0; s < S; ++s) {
+    l[s] = c->slots[s].occupied ? res[s * W + S] : 0;
+    if (!c->slots[s].occupied) any_empty = true;
+    if (c->slots[s].occupied && (best < 0 || l[s] > l[best])) best = s;
+  }
+  bool accept = best >= 0 && l[best] > 0;
+  if (accept && c->cfg.match_threshold) {
+    int o = 0;
+    for (int t = 0; t < S; ++t)
+      if (t != best && c->slots[t].occupied) o = std::max(o, pair(best, t));
+    accept = l[best] > o;
+    if (accept && any_empty && l[best] < (int)c->slots[best].tokens.size()) accept = false;
+  }
+  if (accept) {
+    const int r = std::min(l[best], n - 1);
+    c->slots[best].tokens.resize(r);
+    touch(c, best);
+    *slot = best;
+    *reused = r;
+    return;
+  }
+  int pick = -1;
+  for (int s = 0; s < S && pick < 0; ++s)
+    if (!c->slots[s].occupied) pick = s;
+  if (pick < 0) {
+    pick = 0;
+    for (int s = 1; s < S; ++s)
+      if (c->slots[s].stamp < c->slots[pick].stamp) pick = s;
+  }
+  c->slots[pick].occupied = true;
+  c->slots[pick].tokens.clear();
+  touch(c, pick);
+  *slot = pick;
+  *reused = 0;
+}
+
+// n_slots = 0 ("0 turns reuse off"): one working slot, cleared by every match
+void match_without_reuse(kvr_ctx* c, int* slot, int* reused) {
+  c->slots[0].occupied = true;
+  c->slots[0].tokens.clear();
+  touch(c, 0);
+  *slot = 0;
+  *reused = 0;
+}
+
 // ---------------------------------------------------------------- spill/restore
 struct SpillHeader {
   char magic[8];      // "KVRSLOT1"
@@ -1286,11 +1346,7 @@ int kvr_slot_match(kvr_ctx* c, const int32_t* tokens, int n, int* slot, int* reu
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int S = c->granted;
   if (!c->reuse) {
-    c->slots[0].occupied = true;
-    c->slots[0].tokens.clear();
-    touch(c, 0);
-    *slot = 0;
-    *reused = 0;
+    match_without_reuse(c, slot, reused);
     return KVR_OK;
   }
   int lens[KVR_MAX_SLOTS];
@@ -1308,45 +1364,7 @@ int kvr_slot_match(kvr_ctx* c, const int32_t* tokens, int n, int* slot, int* reu
                       cudaMemcpyDeviceToHost, st);
   if (e == cudaSuccess) e = cudaStreamSynchronize(st);
   if (e != cudaSuccess) return cuda_fail(c, e, "match readback");
-  const int W = S + 1;
-  auto pair = [&](int a, int b) { return a < b ? c->host_match[a * W + b] : c->host_match[b * W + a]; };
-  int l[KVR_MAX_SLOTS];
-  int best = -1;
-  bool any_empty = false;
-  for (int s = 0; s < S; ++s) {
-    l[s] = c->slots[s].occupied ? c->host_match[s * W + S] : 0;
-    if (!c->slots[s].occupied) any_empty = true;
-    if (c->slots[s].occupied && (best < 0 || l[s] > l[best])) best = s;
-  }
-  bool accept = best >= 0 && l[best] > 0;
-  if (accept && c->cfg.match_threshold) {
-    int o = 0;
-    for (int t = 0; t < S; ++t)
-      if (t != best && c->slots[t].occupied) o = std::max(o, pair(best, t));
-    accept = l[best] > o;
-    if (accept && any_empty && l[best] < (int)c->slots[best].tokens.size()) accept = false;
-  }
-  if (accept) {
-    const int r = std::min(l[best], n - 1);
-    c->slots[best].tokens.resize(r);
-    touch(c, best);
-    *slot = best;
-    *reused = r;
-    return KVR_OK;
-  }
-  int pick = -1;
-  for (int s = 0; s < S && pick < 0; ++s)
-    if (!c->slots[s].occupied) pick = s;
-  if (pick < 0) {
-    pick = 0;
-    for (int s = 1; s < S; ++s)
-      if (c->slots[s].stamp < c->slots[pick].stamp) pick = s;
-  }
-  c->slots[pick].occupied = true;
-  c->slots[pick].tokens.clear();
-  touch(c, pick);
-  *slot = pick;
-  *reused = 0;
+  apply_slot_policy(c, c->host_match, n, slot, reused);
   return KVR_OK;
 }
 
@@ -1570,10 +1588,12 @@ int kvr_sync_status(kvr_ctx* c, void* stream) {
   if (e == cudaSuccess) e = cudaStreamSynchronize(st);
   if (e != cudaSuccess) return cuda_fail(c, e, "status readback");
   if (word) {
-    // a launch that gave up may have left tile counters behind
-    cudaMemsetAsync(c->counters, 0, (kCounters + kAttnCounters) * 4, st);
-    cudaMemsetAsync(c->status, 0, 4, st);
-    cudaStreamSynchronize(st);
+    // a launch that gave up may have left arrival counters behind: clear
+    // every one of them (GEMV tiles and split-KV merges) and the status word
+    e = cudaMemsetAsync(c->counters, 0, (kCounters + kAttnCounters) * 4, st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(c->status, 0, 4, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_fail(c, e, "clearing the counters after a timeout");
     return fail(c, KVR_ERR_TIMEOUT, "a device-side wait gave up (status %d)", word);
   }
   return KVR_OK;
@@ -1658,11 +1678,7 @@ int kvr_slot_match_static(kvr_ctx* c, const int32_t* tokens, int n, int* slot, i
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int S = c->granted;
   if (!c->reuse) {
-    c->slots[0].occupied = true;
-    c->slots[0].tokens.clear();
-    touch(c, 0);
-    *slot = 0;
-    *reused = 0;
+    match_without_reuse(c, slot, reused);
     return KVR_OK;
   }
   int32_t *d_prompt = nullptr, *d_out = nullptr;
@@ -1683,45 +1699,7 @@ int kvr_slot_match_static(kvr_ctx* c, const int32_t* tokens, int n, int* slot, i
   e = cudaMemcpyAsync(res.data(), d_out, res.size() * 4, cudaMemcpyDeviceToHost, st);
   if (e == cudaSuccess) e = cudaStreamSynchronize(st);
   if (e != cudaSuccess) return cuda_fail(c, e, "static match readback");
-  const int W = S + 1;
-  auto pair = [&](int a, int b) { return a < b ? res[a * W + b] : res[b * W + a]; };
-  int l[KVR_MAX_SLOTS];
-  int best = -1;
-  bool any_empty = false;
-  for (int s = 0; s < S; ++s) {
-    l[s] = c->slots[s].occupied ? res[s * W + S] : 0;
-    if (!c->slots[s].occupied) any_empty = true;
-    if (c->slots[s].occupied && (best < 0 || l[s] > l[best])) best = s;
-  }
-  bool accept = best >= 0 && l[best] > 0;
-  if (accept && c->cfg.match_threshold) {
-    int o = 0;
-    for (int t = 0; t < S; ++t)
-      if (t != best && c->slots[t].occupied) o = std::max(o, pair(best, t));
-    accept = l[best] > o;
-    if (accept && any_empty && l[best] < (int)c->slots[best].tokens.size()) accept = false;
-  }
-  if (accept) {
-    const int r = std::min(l[best], n - 1);
-    c->slots[best].tokens.resize(r);
-    touch(c, best);
-    *slot = best;
-    *reused = r;
-    return KVR_OK;
-  }
-  int pick = -1;
-  for (int s = 0; s < S && pick < 0; ++s)
-    if (!c->slots[s].occupied) pick = s;
-  if (pick < 0) {
-    pick = 0;
-    for (int s = 1; s < S; ++s)
-      if (c->slots[s].stamp < c->slots[pick].stamp) pick = s;
-  }
-  c->slots[pick].occupied = true;
-  c->slots[pick].tokens.clear();
-  touch(c, pick);
-  *slot = pick;
-  *reused = 0;
+  apply_slot_policy(c, res.data(), n, slot, reused);
   return KVR_OK;
 }
 

@@ -68,4 +68,15 @@ def test_static_match_refuses_prompts_beyond_its_limit():
     with pytest.raises(KvrError) as e:
         b.kvr_slot_match_static(list(range(16385)))
     assert e.value.code == -2 and "static match limit" in str(e.value)
-    assert b.kvr_slot_match_static(list(range(16384)))[1] == 0
+    # at the limit, with a slot that matches the prompt up to its last token:
+    # the kernel reads every word of the fixed prompt region
+    # (slot 0 holds another conversation, so no empty slot takes the prompt)
+    prompt = list(range(16384))
+    held = prompt[:16383] + [99999]
+    for kv in (a, b):
+        kv.kvr_slot_assign(0, [7, 7, 7])
+        kv.kvr_slot_assign(1, held)
+    want = a.kvr_slot_match(prompt)
+    assert want == (1, 16383)
+    assert b.kvr_slot_match_static(prompt) == want
+    assert b.kvr_slot_tokens(1) == a.kvr_slot_tokens(1) == prompt[:16383]
