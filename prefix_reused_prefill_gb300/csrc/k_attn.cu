@@ -103,7 +103,8 @@ __device__ __forceinline__ bool visible(const RowInfo& ri, int j) {
 // flight at a time.  rows: rows per split plane; rowidx: this row's index.
 template <int D, int NS>
 __device__ __forceinline__ void merge_splits(const float* opart, const float2* mlp, long long rows,
-                                             long long rowidx, int ns, __nv_bfloat16* dst, int lane) {
+                                             long long rowidx, int ns, __nv_bfloat16* dst, int lane,
+                                             bool o16) {
   constexpr int E = D / 32;
   static_assert(kMaxSplits <= 64, "two split records per lane");
   const float* src = opart + rowidx * D + lane * E;
@@ -152,7 +153,7 @@ __device__ __forceinline__ void merge_splits(const float* opart, const float2* m
   dst += rowidx * D + lane * E;
 #pragma unroll
   for (int e = 0; e < E; e += 2)
-    *reinterpret_cast<uint32_t*>(dst + e) = dev::pack_bf16x2(acc[e] * inv, acc[e + 1] * inv);
+    *reinterpret_cast<uint32_t*>(dst + e) = dev::pack_act2(acc[e] * inv, acc[e + 1] * inv, o16);
 }
 
 template <int D, int RW, int KW>
@@ -443,7 +444,7 @@ __global__ void __launch_bounds__((RW * KW + 1) * 32) attn_kernel(const __grid_c
 #pragma unroll
       for (int i = 0; i < D / 8; ++i)
         *reinterpret_cast<uint32_t*>(dst + 8 * i + 2 * c) =
-            dev::pack_bf16x2(o[i][2 * h] * inv, o[i][2 * h + 1] * inv);
+            dev::pack_act2(o[i][2 * h] * inv, o[i][2 * h + 1] * inv, p.o16);
     } else {
       const long long plane = (long long)v.m * p.Hq;
       float* dst = v.opart + ((long long)split * plane + rowidx) * D;
@@ -477,7 +478,7 @@ __global__ void __launch_bounds__((RW * KW + 1) * 32) attn_kernel(const __grid_c
     for (int rho = row_lo + kw; rho < row_hi; rho += KW) {
       const RowInfo ri = row_info(p, v, kv, rho);
       if (ri.tok < 0) continue;
-      merge_splits<D, 16>(v.opart, v.ml, plane, (long long)ri.tok * p.Hq + ri.head, v.nsplit, v.o, lane);
+      merge_splits<D, 16>(v.opart, v.ml, plane, (long long)ri.tok * p.Hq + ri.head, v.nsplit, v.o, lane, p.o16);
     }
   }
 }
@@ -511,7 +512,7 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const __grid_constant
     mlp += cv.part0 / D;
   }
   // row rowidx of the conversation's planes is row grow of the call's o
-  merge_splits<D, NS>(opart, mlp, rows, rowidx, ns, p.o + (grow - rowidx) * D, threadIdx.x & 31);
+  merge_splits<D, NS>(opart, mlp, rows, rowidx, ns, p.o + (grow - rowidx) * D, threadIdx.x & 31, p.o16);
 }
 
 template <int D, int RW, int KW = 1>

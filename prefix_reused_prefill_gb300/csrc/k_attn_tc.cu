@@ -487,10 +487,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
 #pragma unroll
             for (int c8 = 0; c8 < 4; ++c8) {
               uint4 w;
-              w.x = dev::pack_bf16x2(v[8 * c8] * inv, v[8 * c8 + 1] * inv);
-              w.y = dev::pack_bf16x2(v[8 * c8 + 2] * inv, v[8 * c8 + 3] * inv);
-              w.z = dev::pack_bf16x2(v[8 * c8 + 4] * inv, v[8 * c8 + 5] * inv);
-              w.w = dev::pack_bf16x2(v[8 * c8 + 6] * inv, v[8 * c8 + 7] * inv);
+              w.x = dev::pack_act2(v[8 * c8] * inv, v[8 * c8 + 1] * inv, p.o16);
+              w.y = dev::pack_act2(v[8 * c8 + 2] * inv, v[8 * c8 + 3] * inv, p.o16);
+              w.z = dev::pack_act2(v[8 * c8 + 4] * inv, v[8 * c8 + 5] * inv, p.o16);
+              w.w = dev::pack_act2(v[8 * c8 + 6] * inv, v[8 * c8 + 7] * inv, p.o16);
               dst[c8] = w;
             }
           } else {

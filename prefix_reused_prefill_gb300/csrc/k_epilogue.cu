@@ -52,11 +52,16 @@ __global__ void rope_table_kernel(RowMap rows, int d, double theta, float2* tabl
 }
 
 __global__ void embed_kernel(const __nv_bfloat16* hidden, int H, const __nv_bfloat16* gain,
-                             float eps, float* h, __nv_bfloat16* a, float* ss_out, int nss) {
+                             float eps, float* h, __nv_bfloat16* a, float* ss_out, int nss, bool a16) {
   dev::pdl_trigger();
   dev::pdl_wait();
   __shared__ float red[32];
   const long long row = blockIdx.x;
+  if (!gain) {   // attention-only layer: the input rows are the projection's input
+    for (int k = threadIdx.x; k < H; k += blockDim.x)
+      dev::store_act(a + row * H + k, __bfloat162float(hidden[row * H + k]), a16);
+    return;
+  }
   float ss = 0.f;
   for (int k = threadIdx.x; k < H; k += blockDim.x) {
     const float v = __bfloat162float(hidden[row * H + k]);
@@ -71,7 +76,7 @@ __global__ void embed_kernel(const __nv_bfloat16* hidden, int H, const __nv_bflo
   }
   const float rs = rsqrtf(sum / H + eps);
   for (int k = threadIdx.x; k < H; k += blockDim.x)
-    a[row * H + k] = __float2bfloat16_rn(h[row * H + k] * rs * __bfloat162float(gain[k]));
+    dev::store_act(a + row * H + k, h[row * H + k] * rs * __bfloat162float(gain[k]), a16);
 }
 
 // One CTA per (tile of tokens, head): sum the split partials, rotate q/k
@@ -169,7 +174,8 @@ template <int V>  // float4 per thread (H <= 4 * 512 * V)
 __global__ void __launch_bounds__(kResidThreads) epi_resid_kernel(const float* part, long long plane, int ksplit,
                                                                   int ldo, int c0, int H, float* h,
                                                                   const __nv_bfloat16* gain, float eps,
-                                                                  __nv_bfloat16* a_out, __nv_bfloat16* final_out) {
+                                                                  __nv_bfloat16* a_out, bool a16,
+                                                                  __nv_bfloat16* final_out) {
   dev::pdl_trigger();
   dev::pdl_wait();
   __shared__ float red[32];
@@ -231,8 +237,8 @@ __global__ void __launch_bounds__(kResidThreads) epi_resid_kernel(const float* p
         const __nv_bfloat162 g01 = *reinterpret_cast<const __nv_bfloat162*>(&gw.x);
         const __nv_bfloat162 g23 = *reinterpret_cast<const __nv_bfloat162*>(&gw.y);
         uint2 o;
-        o.x = dev::pack_bf16x2(v[u].x * rs * __bfloat162float(g01.x), v[u].y * rs * __bfloat162float(g01.y));
-        o.y = dev::pack_bf16x2(v[u].z * rs * __bfloat162float(g23.x), v[u].w * rs * __bfloat162float(g23.y));
+        o.x = dev::pack_act2(v[u].x * rs * __bfloat162float(g01.x), v[u].y * rs * __bfloat162float(g01.y), a16);
+        o.y = dev::pack_act2(v[u].z * rs * __bfloat162float(g23.x), v[u].w * rs * __bfloat162float(g23.y), a16);
         reinterpret_cast<uint2*>(a_out + i * H)[k4] = o;
       }
     }
@@ -253,14 +259,13 @@ __global__ void epi_swiglu_kernel(const float* part, long long plane, int ksplit
 }
 
 __global__ void epi_cast_kernel(const float* part, long long plane, int ksplit, int ldo, int c0,
-                                int mb, int N, __nv_bfloat16* out) {
+                                int mb, int N, __nv_bfloat16* out, bool f16) {
   dev::pdl_trigger();
   dev::pdl_wait();
   const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= (long long)mb * N) return;
   const int t = (int)(idx / N), n = (int)(idx % N);
-  out[(long long)(c0 + t) * N + n] =
-      __float2bfloat16_rn(split_sum(part, plane, ksplit, (long long)t * ldo + n));
+  dev::store_act(out + (long long)(c0 + t) * N + n, split_sum(part, plane, ksplit, (long long)t * ldo + n), f16);
 }
 
 inline unsigned blocks_for(long long n, int threads) { return (unsigned)((n + threads - 1) / threads); }
@@ -273,9 +278,9 @@ cudaError_t launch_rope_table(const RowMap& rows, int d, float theta, float2* ta
 }
 
 cudaError_t launch_embed(const __nv_bfloat16* hidden, int m, int H, const __nv_bfloat16* gain,
-                         float eps, float* h, __nv_bfloat16* a, float* ss_out, int nss,
+                         float eps, float* h, __nv_bfloat16* a, float* ss_out, int nss, bool a16,
                          cudaStream_t st) {
-  return launch_k(embed_kernel, m, 256, 0, st, hidden, H, gain, eps, h, a, ss_out, nss);
+  return launch_k(embed_kernel, m, 256, 0, st, hidden, H, gain, eps, h, a, ss_out, nss, a16);
 }
 
 // One warp per token: the largest of the tiles' bests, lowest row on ties.
@@ -338,18 +343,18 @@ cudaError_t launch_epi_qkv(const float* part, long long plane, int ksplit, int l
 
 cudaError_t launch_epi_resid(const float* part, long long plane, int ksplit, int ldo, int c0,
                              int mb, int H, float* h, const __nv_bfloat16* gain, float eps,
-                             __nv_bfloat16* a_out, __nv_bfloat16* final_out, cudaStream_t st) {
+                             __nv_bfloat16* a_out, bool a16, __nv_bfloat16* final_out, cudaStream_t st) {
   if (ksplit > kGemmMaxSplit) return cudaErrorInvalidValue;
   const int v = (H / 4 + kResidThreads - 1) / kResidThreads;
   if (v <= 1)
     return launch_k(epi_resid_kernel<1>, mb, kResidThreads, 0, st, part, plane, ksplit, ldo, c0, H, h, gain,
-                    eps, a_out, final_out);
+                    eps, a_out, a16, final_out);
   if (v <= 2)
     return launch_k(epi_resid_kernel<2>, mb, kResidThreads, 0, st, part, plane, ksplit, ldo, c0, H, h, gain,
-                    eps, a_out, final_out);
+                    eps, a_out, a16, final_out);
   if (v <= 4)
     return launch_k(epi_resid_kernel<4>, mb, kResidThreads, 0, st, part, plane, ksplit, ldo, c0, H, h, gain,
-                    eps, a_out, final_out);
+                    eps, a_out, a16, final_out);
   return cudaErrorInvalidValue;
 }
 
@@ -360,9 +365,9 @@ cudaError_t launch_epi_swiglu(const float* part, long long plane, int ksplit, in
 }
 
 cudaError_t launch_epi_cast(const float* part, long long plane, int ksplit, int ldo, int c0,
-                            int mb, int N, __nv_bfloat16* out, cudaStream_t st) {
+                            int mb, int N, __nv_bfloat16* out, bool f16, cudaStream_t st) {
   return launch_k(epi_cast_kernel, blocks_for((long long)mb * N, 256), 256, 0, st, part, plane,
-                  ksplit, ldo, c0, mb, N, out);
+                  ksplit, ldo, c0, mb, N, out, f16);
 }
 
 }  // namespace kvr

@@ -1,5 +1,9 @@
 // Large-m projections on the 5th-generation tensor cores: Y = X W^T with int4
-// group-32 weights, X bf16 [tokens][K], fp32 accumulation in tensor memory.
+// group-32 weights, fp32 accumulation in tensor memory.  Both operands are
+// fp16: X [tokens][K] holds the activations' bf16 values (the model's rounding
+// point) in fp16, which represents them exactly, and each dequantised weight
+// code * scale is rounded once to fp16 (relative error at most 2^-12; the
+// product of a 4-bit code and an 11-bit fp16 scale can need 14 bits).
 //
 // thinkspread, "The economics of speculative decoding" (cost model): each
 // weight streams once for all m rows.  At the m = 254 rows of goinfer's
@@ -20,9 +24,9 @@
 //              K-major atoms, 3 stages); the two rings are independent;
 //   warp 1     allocates the TMEM accumulator; one thread issues tcgen05.mma
 //              and tcgen05.commit (which frees the smem stages it read);
-//   warps 2-17 converters: int4 codes -> bf16 weights (code * scale, exact for
-//              scales with at most 8 significant bits; the fp16 scales are read
-//              from global memory) stored straight into a TMEM A stage with one
+//   warps 2-17 converters: int4 codes -> fp16 weights (code * scale rounded
+//              once; the fp16 scales are read from global memory) stored
+//              straight into a TMEM A stage with one
 //              tcgen05.st per thread (thread = TMEM lane / tile row, one
 //              64-input half of the stage).  Two groups of eight warps take
 //              alternate stages of a 4-deep A ring in TMEM.
@@ -71,9 +75,10 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
          (2ull << 61);
 }
 
-// kind::f16 instruction descriptor: D fp32, A and B bf16, both K-major.
-__device__ __forceinline__ uint32_t idesc_bf16(int M, int N) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+// kind::f16 instruction descriptor: D fp32, A and B fp16 (format fields 0),
+// both K-major.
+__device__ __forceinline__ uint32_t idesc_f16(int M, int N) {
+  return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
 // D (TMEM) += A (TMEM) * B (shared memory)
@@ -122,31 +127,34 @@ __device__ __forceinline__ void named_sync(int id, int n) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 
-// 8 codes of one 32-bit word -> 4 bf16x2 code values (field i low, field i+4 high)
-__device__ __forceinline__ void codes_of_word(uint32_t w, __nv_bfloat162 out[4]) {
-  const uint32_t magic = 0x43004300u;
-  const __nv_bfloat162 bias = __floats2bfloat162_rn(136.0f, 136.0f);
+// 8 codes of one 32-bit word -> 4 fp16x2 code values (field i low, field i+4
+// high): the field OR'd into the mantissa of fp16 1024.0 is 1024 + field
+// (the fp16 step is 1 there), and 1024 + field - 1032 = code, exactly.
+__device__ __forceinline__ void codes_of_word(uint32_t w, __half2 out[4]) {
+  const uint32_t magic = 0x64006400u;
+  const __half2 bias = __floats2half2_rn(1032.0f, 1032.0f);
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     uint32_t v;
     asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(v) : "r"(w >> (4 * i)), "r"(0x000F000Fu), "r"(magic));
-    out[i] = __hsub2(*reinterpret_cast<__nv_bfloat162*>(&v), bias);
+    out[i] = __hsub2(*reinterpret_cast<__half2*>(&v), bias);
   }
 }
 
-// K-quant: 8 unsigned 4-bit codes of one word -> 4 bf16x2 weights
-// bf16(d*sc*q - dmin*mn) (pair i: fields i and i+4, as codes_of_word).  The
+// K-quant: 8 unsigned 4-bit codes of one word -> 4 fp16x2 weights
+// fp16(d*sc*q - dmin*mn) (pair i: fields i and i+4, as codes_of_word).  The
 // codes become exact fp32 values 128 + q (the bf16 pattern 128 + q shifted
 // into the high half), so w = (128 + q)*a + c with a = d*sc and
 // c = -(128*a + dmin*mn), one fp32 FMA per weight on the full-rate pipe (c
-// carries at most one fp32 rounding, far below the bf16 rounding that follows).
+// carries at most one fp32 rounding, far below the fp16 rounding that follows).
 __device__ __forceinline__ void q4k_weights_of_word(uint32_t w, float a, float c, uint32_t out[4]) {
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     uint32_t v;
     asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(v) : "r"(w >> (4 * i)), "r"(0x000F000Fu), "r"(0x43004300u));
     const float ql = __uint_as_float(v << 16), qh = __uint_as_float(v & 0xFFFF0000u);
-    out[i] = dev::pack_bf16x2(fmaf(ql, a, c), fmaf(qh, a, c));
+    __half2 hv = __floats2half2_rn(fmaf(ql, a, c), fmaf(qh, a, c));
+    out[i] = *reinterpret_cast<uint32_t*>(&hv);
   }
 }
 
@@ -289,7 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_int4_tc_kernel(const __grid_
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      const uint32_t idesc = idesc_bf16(128, p.n_tok);
+      const uint32_t idesc = idesc_f16(128, p.n_tok);
       bool ok = true;
       for (int i = 0; i < nkc; ++i) {
         const int xs = i % kStages, as = i % kAStages;
@@ -353,7 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_int4_tc_kernel(const __grid_
       const uint32_t sw = (uint32_t)((t >> 1) & 3);  // 64-byte swizzle of this row
       const uint4 w0 = dev::lds128(rb + (((uint32_t)(2 * hq) ^ sw) << 4));
       const uint4 w1 = dev::lds128(rb + (((uint32_t)(2 * hq + 1) ^ sw) << 4));
-      uint32_t outv[32];   // 64 bf16 inputs of this row, k order, two per column
+      uint32_t outv[32];   // 64 fp16 weights of this row, k order, two per column
       if (p.fmt == kFmtQ4K) {
         const float d = __half2float(__ushort_as_half((unsigned short)(rec.x & 0xFFFFu)));
         const float dmin = __half2float(__ushort_as_half((unsigned short)(rec.x >> 16)));
@@ -381,9 +389,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_int4_tc_kernel(const __grid_
       for (int h = 0; h < 2; ++h) {
         const uint4 wv = h ? w1 : w0;
         const uint16_t sbits = (uint16_t)(h ? (scw >> 16) : (scw & 0xFFFFu));
-        const float sf = __half2float(__ushort_as_half(sbits));
-        const __nv_bfloat162 s2 = __floats2bfloat162_rn(sf, sf);
-        __nv_bfloat162 c0[4], c1[4], c2[4], c3[4];
+        const __half2 s2 = __half2half2(__ushort_as_half(sbits));
+        __half2 c0[4], c1[4], c2[4], c3[4];
         codes_of_word(wv.x, c0);
         codes_of_word(wv.y, c1);
         codes_of_word(wv.z, c2);
@@ -391,8 +398,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_int4_tc_kernel(const __grid_
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj) {
           // inputs 8*jj .. 8*jj+7 of this 32-input group: words 0..3 give pairs (2w, 2w+1)
-          __nv_bfloat162 v0 = __hmul2(c0[jj], s2), v1 = __hmul2(c1[jj], s2);
-          __nv_bfloat162 v2 = __hmul2(c2[jj], s2), v3 = __hmul2(c3[jj], s2);
+          // code * scale: the exact product rounded once to fp16
+          __half2 v0 = __hmul2(c0[jj], s2), v1 = __hmul2(c1[jj], s2);
+          __half2 v2 = __hmul2(c2[jj], s2), v3 = __hmul2(c3[jj], s2);
           outv[16 * h + 4 * jj + 0] = *reinterpret_cast<uint32_t*>(&v0);
           outv[16 * h + 4 * jj + 1] = *reinterpret_cast<uint32_t*>(&v1);
           outv[16 * h + 4 * jj + 2] = *reinterpret_cast<uint32_t*>(&v2);
@@ -457,7 +465,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_int4_tc_kernel(const __grid_
                 const float g = xch[r * 33 + k];
                 const float u = xch[(64 + r) * 33 + k];
                 const float sg = __fdividef(g, 1.f + __expf(-g));
-                p.z[(long long)(p.t0 + c0 + k) * p.F + n] = __float2bfloat16_rn(sg * u);
+                dev::store_act(p.z + (long long)(p.t0 + c0 + k) * p.F + n, sg * u, p.z16 != 0);
               }
             }
           }

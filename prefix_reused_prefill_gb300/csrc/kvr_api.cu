@@ -202,6 +202,9 @@ struct kvr_ctx {
   // finished RMSNorm rows; tracked in stream order by the host
   float* ss = nullptr;
   bool a_deferred = false;
+  // the call's projections run on the tcgen05 GEMM, whose operands are fp16:
+  // a, o and z then hold their bf16-rounded values in fp16
+  bool act16 = false;
   float* part = nullptr;
   float* opart = nullptr;
   float2* ml = nullptr;
@@ -351,6 +354,7 @@ int project_gemm(kvr_ctx* c, cudaStream_t st, const Seg* segs, int nseg, const C
   p.status = c->status;
   p.part = c->part;
   p.z = c->z;
+  p.z16 = 1;   // z feeds the down projection, on this GEMM as well
   p.F = c->cfg.ffn;
   int col = 0, tiles = 0;
   if (swiglu) {
@@ -634,6 +638,7 @@ int attention(kvr_ctx* c, cudaStream_t st, int slot, int layer, const RowMap& ro
   p.cap = k.capacity;
   p.scale_log2 = 1.4426950408889634f / sqrtf((float)k.head_dim);
   p.status = c->status;
+  p.o16 = c->act16 ? 1 : 0;
   const int R = p.G * rows.m;
   const int kend = rows.P + rows.m;
   const bool tc = R > kAttnTcMinRows && !c->force_gemv;
@@ -692,6 +697,7 @@ int attention_batch(kvr_ctx* c, cudaStream_t st, int layer, const RowMap& rows, 
   p.cap = k.capacity;
   p.scale_log2 = 1.4426950408889634f / sqrtf((float)k.head_dim);
   p.status = c->status;
+  p.o16 = c->act16 ? 1 : 0;
   int rmax = 0;
   for (int i = 0; i < nbs; ++i) rmax = std::max(rmax, p.G * (rows.off[bs[i] + 1] - rows.off[bs[i]]));
   const int rw = attn_row_warps(rmax);
@@ -771,17 +777,20 @@ int run_stack(kvr_ctx* c, const RowMap& rows, const void* hidden,
     e = launch_rope_table(rows, d, k.rope_theta, c->rope, st);
   }
   if (e != cudaSuccess) return cuda_fail(c, e, "rope table launch");
+  c->act16 = packed4(k) && !gemv_path(c, m);
   if (k.attn_only) {
     c->a_deferred = false;
-    e = cudaMemcpyAsync(c->a, hidden, (size_t)m * H * 2, cudaMemcpyDeviceToDevice, st);
-    if (e != cudaSuccess) return cuda_fail(c, e, "input copy");
+    Timed t(c, kEpi, st);
+    e = launch_embed(static_cast<const __nv_bfloat16*>(hidden), m, H, nullptr, 0.f, nullptr, c->a, nullptr, 0,
+                     c->act16, st);
+    if (e != cudaSuccess) return cuda_fail(c, e, "input copy launch");
   } else {
     // the small-m GEMV takes the first RMSNorm deferred, like every later one
     c->a_deferred = packed4(k) && gemv_path(c, m);
     Timed t(c, kEpi, st);
     e = launch_embed(static_cast<const __nv_bfloat16*>(hidden), m, H,
                      static_cast<const __nv_bfloat16*>(w[0].norm_attn), k.rms_eps, c->h, c->a,
-                     c->a_deferred ? c->ss : nullptr, (int)ss_per_row(H), st);
+                     c->a_deferred ? c->ss : nullptr, (int)ss_per_row(H), c->act16, st);
     if (e != cudaSuccess) return cuda_fail(c, e, "embed launch");
   }
   auto trace = [&](int entry) -> cudaError_t {
@@ -846,7 +855,7 @@ int run_stack(kvr_ctx* c, const RowMap& rows, const void* hidden,
         fz.out = dst;
         rc = project(c, st, &so, 1, Act::O, Hq * d, m,
                      [&](const float* part, long long plane, int ks, int ldo, int c0, int mb) {
-                       return launch_epi_cast(part, plane, ks, ldo, c0, mb, H, dst, st);
+                       return launch_epi_cast(part, plane, ks, ldo, c0, mb, H, dst, c->act16 && !last, st);
                      }, fz);
         if (rc) return rc;
         continue;
@@ -858,7 +867,7 @@ int run_stack(kvr_ctx* c, const RowMap& rows, const void* hidden,
                    [&](const float* part, long long plane, int ks, int ldo, int c0, int mb) {
                      return launch_epi_resid(part, plane, ks, ldo, c0, mb, H, c->h,
                                              static_cast<const __nv_bfloat16*>(W.norm_ffn),
-                                             k.rms_eps, c->a, nullptr, st);
+                                             k.rms_eps, c->a, c->act16, nullptr, st);
                    }, fz);
       if (rc) return rc;
     }
@@ -885,8 +894,9 @@ int run_stack(kvr_ctx* c, const RowMap& rows, const void* hidden,
       fz.out = last ? static_cast<__nv_bfloat16*>(out) : nullptr;
       rc = project(c, st, &sd, 1, Act::Z, F, m,
                    [&](const float* part, long long plane, int ks, int ldo, int c0, int mb) {
+                     // the output head's input stays bf16 (the head runs on the GEMV)
                      return launch_epi_resid(part, plane, ks, ldo, c0, mb, H, c->h, gain, k.rms_eps,
-                                             gain ? c->a : nullptr,
+                                             gain ? c->a : nullptr, c->act16 && !last,
                                              last ? static_cast<__nv_bfloat16*>(out) : nullptr, st);
                    }, fz);
       if (rc) return rc;

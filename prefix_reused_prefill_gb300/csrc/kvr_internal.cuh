@@ -185,6 +185,7 @@ struct GemmParams {
   long long plane;
   float* part;      // [ksplit][256][ldo]
   __nv_bfloat16* z; // [max_rows][F]
+  int z16;          // z holds fp16 (the next GEMM's operand type)
   int* status;
 };
 
@@ -215,6 +216,7 @@ struct AttnParams {
   int nsplit;
   int row_tiles;
   float scale_log2;          // log2(e) / sqrt(d)
+  int o16;                   // o holds fp16 (the O projection runs on the tcgen05 GEMM)
   int* status;
   // split-KV kernel with one row tile (R <= 16): arrival counters per (row
   // tile, KV head), zero between launches; the last split merges the splits
@@ -269,9 +271,11 @@ cudaError_t launch_rope_table(const RowMap& rows, int d, float theta, float2* ta
                               cudaStream_t st);
 // h = float(hidden) and the first RMSNorm: a = bf16(RMSNorm(h) * gain), or,
 // with ss_out (the deferred form read by the small-m GEMV), a = bf16(h * gain)
-// and ss_out[row][0] = sum of h^2 (the row's other nss - 1 entries zero)
+// and ss_out[row][0] = sum of h^2 (the row's other nss - 1 entries zero).
+// Without a gain, a = hidden (attention-only layers; h untouched).  a16: a
+// holds the bf16-rounded values as fp16 (the tcgen05 GEMM's operand type).
 cudaError_t launch_embed(const __nv_bfloat16* hidden, int m, int H, const __nv_bfloat16* gain,
-                         float eps, float* h, __nv_bfloat16* a, float* ss_out, int nss,
+                         float eps, float* h, __nv_bfloat16* a, float* ss_out, int nss, bool a16,
                          cudaStream_t st);
 // out[t] = the row of the largest value over the tiles' bests of token t
 // (lowest row on ties), t < m
@@ -283,13 +287,15 @@ cudaError_t launch_epi_qkv(const float* part, long long plane, int ksplit, int l
                            const float2* rope, __nv_bfloat16* q, __nv_bfloat16* arena,
                            long long k_off, long long v_off, long long slot_stride, int cap,
                            cudaStream_t st);
+// a16: a_out holds fp16 (as launch_embed); final_out is always bf16
 cudaError_t launch_epi_resid(const float* part, long long plane, int ksplit, int ldo, int c0,
                              int mb, int H, float* h, const __nv_bfloat16* gain, float eps,
-                             __nv_bfloat16* a_out, __nv_bfloat16* final_out, cudaStream_t st);
+                             __nv_bfloat16* a_out, bool a16, __nv_bfloat16* final_out, cudaStream_t st);
 cudaError_t launch_epi_swiglu(const float* part, long long plane, int ksplit, int ldo, int c0,
                               int mb, int F, __nv_bfloat16* z, cudaStream_t st);
+// f16: out holds fp16 (a later layer's tcgen05 GEMM input)
 cudaError_t launch_epi_cast(const float* part, long long plane, int ksplit, int ldo, int c0,
-                            int mb, int N, __nv_bfloat16* out, cudaStream_t st);
+                            int mb, int N, __nv_bfloat16* out, bool f16, cudaStream_t st);
 
 // dynamic shared memory the launchers need (for cudaFuncSetAttribute at setup)
 // resident CTAs per SM of the int4 GEMV for nt token tiles, epilogue and weight format
@@ -450,6 +456,27 @@ __device__ __forceinline__ void mma_bf16_16816(float d[4], const uint32_t a[4], 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// An activation pair rounded to bf16 (the model's rounding point), stored as
+// bf16 or, for the tcgen05 GEMM's fp16 operands (f16), as the same two values
+// in fp16: every bf16 number of magnitude 2^-14 .. 65504 is an fp16 number,
+// so the conversion is exact there (smaller ones lose at most 2^-25).
+__device__ __forceinline__ uint32_t pack_act2(float lo, float hi, bool f16) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  if (f16) {
+    const float2 f = __bfloat1622float2(v);
+    __half2 h = __floats2half2_rn(f.x, f.y);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// one activation, as pack_act2
+__device__ __forceinline__ void store_act(__nv_bfloat16* dst, float x, bool f16) {
+  const __nv_bfloat16 b = __float2bfloat16_rn(x);
+  if (f16) *reinterpret_cast<__half*>(dst) = __float2half_rn(__bfloat162float(b));
+  else *dst = b;
 }
 
 // *p += v at gpu scope with acquire-release semantics; returns the old value
