@@ -58,13 +58,29 @@ def test_decode_inverts_pack(rng):
     np.testing.assert_array_equal(formats.int4_codes(packed, 256), q.numpy().astype(np.int64))
 
 
-def test_quantized_weights_are_exact_in_bf16(rng):
-    # the synthetic quantiser's 5-bit scales make every code*scale a bf16 value
+def test_quantizer_scales_and_error(rng):
+    # the format as stated: scale = absmax/7 rounded to the nearest fp16
+    # (numpy's own float16 cast pins the rounding), codes within [-8, 7], and
+    # the quantisation error is what int4 allows: |w - deq| <= scale/2
     w = torch.from_numpy(rng.standard_normal((64, 512)).astype(np.float32) * 0.02)
     m = workloads.make_int4(w)
+    amax = np.abs(w.numpy().reshape(64, 16, 32)).max(axis=-1)
+    np.testing.assert_array_equal(m.scales.numpy(), (amax / np.float32(7.0)).astype(np.float16))
+    deq = formats.dequant_int4(m.packed.numpy(), m.scales.numpy())
+    s = m.scales.numpy().astype(np.float64).repeat(32, axis=1)
+    assert np.all(np.abs(w.numpy() - deq) <= s / 2 + 1e-12)
+    # general fp16 scales carry up to 11 significant bits: some code*scale is
+    # not a bf16 number (the case the projections must handle exactly)
+    assert np.any(round_bf16(deq) != deq)
+
+
+def test_five_bit_scales_give_bf16_weights(rng):
+    # the named extra case: scales rounded up to 5 significant bits make every
+    # code*scale exactly a bf16 (and fp16) number
+    w = torch.from_numpy(rng.standard_normal((64, 512)).astype(np.float32) * 0.02)
+    m = workloads.make_int4(w, scales="5bit")
     deq = formats.dequant_int4(m.packed.numpy(), m.scales.numpy())
     np.testing.assert_array_equal(round_bf16(deq), deq)
-    # and the quantisation error is what int4 allows: |w - deq| <= scale/2
     s = m.scales.numpy().astype(np.float64).repeat(32, axis=1)
     assert np.all(np.abs(w.numpy() - deq) <= s / 2 + 1e-12)
 

@@ -7,7 +7,8 @@ an input has to be *in* the library's formats before anyone can read it:
 
 * round N(0, 1) / N(0, 0.02) draws to bf16 (through torch's own cast);
 * quantise N(0, 0.02) draws to the int4 group-32 format with fp16 scales and
-  pack the 4-bit codes into the byte layout that ``include/kvr.h`` documents.
+  pack the 4-bit codes into the byte layout that ``include/kvr.h`` documents;
+* draw the RMSNorm gains, bf16 in [0.5, 1.5), one set per norm.
 
 The shapes are the ones the pages' workloads name (goinfer's turn-9 replay of
 Qwen2.5-7B served as int4; the dense 9B of the speculative-decoding post; the
@@ -123,25 +124,34 @@ def hidden_for_tokens(tokens: Sequence[int], hidden: int, seed: int) -> torch.Te
 def _scale_up_5bit(s: torch.Tensor) -> torch.Tensor:
     """Round positive scales UP to 5 significant bits (then exact in fp16).
 
-    With at most 5 significant bits in the scale, q*scale is exact in bf16
-    for every code q in [-8, 7]; see the precision readings of the design.
+    A named extra case only: with such scales every code*scale has at most 8
+    significant bits, a number both fp16 and bf16 hold exactly.
     """
     m, e = torch.frexp(s)                       # s = m * 2**e, m in [0.5, 1)
     m = torch.ceil(m * 32.0) / 32.0
     return torch.ldexp(m, e)
 
 
-def quantize_int4(w: torch.Tensor) -> tuple:
+SCALES = ("fp16", "5bit")
+
+
+def quantize_int4(w: torch.Tensor, scales: str = "fp16") -> tuple:
     """Symmetric int4 with one fp16 scale per 32 inputs.  w: float32 [N][K].
 
     Returns (codes int8 [N][K] in [-8, 7], scales fp16 [N][K/32]).
-    scale = absmax/7 rounded up to 5 significant bits; code = clamp(rne(w/scale)).
+    scales="fp16" (the format as stated): scale = fp16(absmax / 7), round to
+    nearest; scales="5bit": absmax / 7 rounded up to 5 significant bits.
+    code = clamp(rne(w / scale), -8, 7) with the stored scale.
     """
+    if scales not in SCALES:
+        raise ValueError(f"scales must be one of {SCALES}")
     N, K = w.shape
     assert K % GROUP == 0
     g = w.reshape(N, K // GROUP, GROUP).to(torch.float32)
     amax = g.abs().amax(dim=-1)
-    s = _scale_up_5bit(torch.clamp(amax / 7.0, min=2.0 ** -14))
+    s = torch.clamp(amax / 7.0, min=2.0 ** -14)
+    if scales == "5bit":
+        s = _scale_up_5bit(s)
     s = s.to(torch.float16)
     q = torch.round(g / s.to(torch.float32).unsqueeze(-1)).clamp_(-8, 7).to(torch.int8)
     return q.reshape(N, K), s
@@ -175,8 +185,8 @@ class Int4Matrix:
     codes: Optional[torch.Tensor] = None  # int8 [N][K], kept only for small shapes
 
 
-def make_int4(w: torch.Tensor, keep_codes: bool = False) -> Int4Matrix:
-    q, s = quantize_int4(w)
+def make_int4(w: torch.Tensor, keep_codes: bool = False, scales: str = "fp16") -> Int4Matrix:
+    q, s = quantize_int4(w, scales)
     return Int4Matrix(pack_int4(q), s.contiguous(), q if keep_codes else None)
 
 
@@ -255,11 +265,20 @@ def make_q4k(w: torch.Tensor) -> Q4KMatrix:
 _MAT_ORDER = ["wq", "wk", "wv", "wo", "wg", "wu", "wd"]
 
 
-def layer_weights(shape: ModelShape, seed: int, layer: int, device="cpu",
-                  keep_codes: bool = False, std: float = 0.02) -> Dict[str, object]:
-    """Weights of one layer.  bf16: tensors [N][K]; int4: Int4Matrix per matrix.
+def norm_gain(hidden: int, seed: int, layer: int, which: int, device="cpu") -> torch.Tensor:
+    """An RMSNorm gain: bf16 of U[0.5, 1.5) per element from PCG64([seed, layer,
+    200 + which]) (which: 0 attention norm, 1 FFN norm, 2 the output head's),
+    so a dropped, misplaced or swapped gain changes the result."""
+    g = np.random.Generator(np.random.PCG64([seed, layer, 200 + which])).uniform(0.5, 1.5, hidden)
+    return torch.from_numpy(g.astype(np.float32)).to(torch.bfloat16).to(device)
 
-    Also 'norm_attn' and 'norm_ffn' (bf16 ones, the RMSNorm gains).
+
+def layer_weights(shape: ModelShape, seed: int, layer: int, device="cpu",
+                  keep_codes: bool = False, std: float = 0.02, scales: str = "fp16") -> Dict[str, object]:
+    """Weights of one layer.  bf16: tensors [N][K]; int4: Int4Matrix per matrix
+    (scales: "fp16" or the named "5bit" case, see quantize_int4).
+
+    Also 'norm_attn' and 'norm_ffn', the RMSNorm gains (norm_gain).
     """
     out: Dict[str, object] = {}
     for name, (n, k) in shape.matrices().items():
@@ -276,18 +295,18 @@ def layer_weights(shape: ModelShape, seed: int, layer: int, device="cpu",
         elif shape.weight_format == "q4k":
             out[name] = make_q4k(w)
         else:
-            out[name] = make_int4(w, keep_codes=keep_codes)
+            out[name] = make_int4(w, keep_codes=keep_codes, scales=scales)
         del w
     H = shape.hidden
     if not shape.attn_only:
-        out["norm_attn"] = torch.ones(H, dtype=torch.bfloat16, device=device)
-        out["norm_ffn"] = torch.ones(H, dtype=torch.bfloat16, device=device)
+        out["norm_attn"] = norm_gain(H, seed, layer, 0, device)
+        out["norm_ffn"] = norm_gain(H, seed, layer, 1, device)
     return out
 
 
 def head_weights(shape: ModelShape, seed: int, device="cpu", vocab: int = VOCAB, keep_codes: bool = False,
                  std: float = 0.02) -> Dict[str, object]:
-    """The output head: 'norm' (bf16 ones, the final RMSNorm gain) and 'lm', the
+    """The output head: 'norm' (the final RMSNorm gain, norm_gain) and 'lm', the
     LM head [vocab][H] in the shape's weight format (int4 g32 or bf16)."""
     H = shape.hidden
     if str(device) == "cpu":
@@ -298,13 +317,13 @@ def head_weights(shape: ModelShape, seed: int, device="cpu", vocab: int = VOCAB,
         g.manual_seed(seed * 1_000_003 + 10_000 * 101)
         w = torch.randn((vocab, H), generator=g, device=device, dtype=torch.float32) * std
     lm = w.to(torch.bfloat16).contiguous() if shape.weight_format == "bf16" else make_int4(w, keep_codes=keep_codes)
-    return {"norm": torch.ones(H, dtype=torch.bfloat16, device=device), "lm": lm}
+    return {"norm": norm_gain(H, seed, 10_000, 2, device), "lm": lm}
 
 
 def stack_weights(shape: ModelShape, seed: int, device="cpu", keep_codes=False,
-                  n_layers: Optional[int] = None) -> List[Dict[str, object]]:
+                  n_layers: Optional[int] = None, scales: str = "fp16") -> List[Dict[str, object]]:
     L = shape.n_layers if n_layers is None else n_layers
-    return [layer_weights(shape, seed, l, device, keep_codes) for l in range(L)]
+    return [layer_weights(shape, seed, l, device, keep_codes, scales=scales) for l in range(L)]
 
 
 def weights_to(ws: List[Dict[str, object]], device) -> List[Dict[str, object]]:
