@@ -52,7 +52,7 @@ __global__ void rope_table_kernel(RowMap rows, int d, double theta, float2* tabl
 }
 
 __global__ void embed_kernel(const __nv_bfloat16* hidden, int H, const __nv_bfloat16* gain,
-                             float eps, float* h, __nv_bfloat16* a, float* ss_out, int nss, bool a16) {
+                             float eps, float* h, __nv_bfloat16* a, bool a16) {
   dev::pdl_trigger();
   dev::pdl_wait();
   __shared__ float red[32];
@@ -67,16 +67,53 @@ __global__ void embed_kernel(const __nv_bfloat16* hidden, int H, const __nv_bflo
     const float v = __bfloat162float(hidden[row * H + k]);
     h[row * H + k] = v;
     ss += v * v;
-    if (ss_out) a[row * H + k] = __float2bfloat16_rn(v * __bfloat162float(gain[k]));
   }
   const float sum = block_sum(ss, red);
-  if (ss_out) {
-    for (int j = threadIdx.x; j < nss; j += blockDim.x) ss_out[row * nss + j] = j == 0 ? sum : 0.f;
-    return;
-  }
   const float rs = rsqrtf(sum / H + eps);
   for (int k = threadIdx.x; k < H; k += blockDim.x)
     dev::store_act(a + row * H + k, h[row * H + k] * rs * __bfloat162float(gain[k]), a16);
+}
+
+// One CTA per row: a = bf16(h * rsqrt(mean(h^2) + eps) * gain), the RMSNorm
+// of a row of the fp32 residual stream (float4 loads; the row stays in
+// registers between the sum and the scaling for H <= 4096).
+__global__ void __launch_bounds__(256) norm_kernel(const float* h, int H, const __nv_bfloat16* gain, float eps,
+                                                   __nv_bfloat16* a) {
+  dev::pdl_trigger();
+  dev::pdl_wait();
+  __shared__ float red[32];
+  constexpr int kV = 4;   // float4 per thread held in registers
+  const long long row = blockIdx.x;
+  const float4* src = reinterpret_cast<const float4*>(h + row * H);
+  const int H4 = H >> 2;
+  float4 v[kV];
+  float ss = 0.f;
+#pragma unroll
+  for (int u = 0; u < kV; ++u) {
+    const int k4 = threadIdx.x + u * 256;
+    v[u] = k4 < H4 ? src[k4] : make_float4(0.f, 0.f, 0.f, 0.f);
+    ss += v[u].x * v[u].x + v[u].y * v[u].y + v[u].z * v[u].z + v[u].w * v[u].w;
+  }
+  for (int k4 = threadIdx.x + kV * 256; k4 < H4; k4 += 256) {
+    const float4 x = src[k4];
+    ss += x.x * x.x + x.y * x.y + x.z * x.z + x.w * x.w;
+  }
+  const float rs = rsqrtf(block_sum(ss, red) / H + eps);
+  auto put = [&](const float4& x, int k4) {
+    const uint2 gw = reinterpret_cast<const uint2*>(gain)[k4];
+    const __nv_bfloat162 g01 = *reinterpret_cast<const __nv_bfloat162*>(&gw.x);
+    const __nv_bfloat162 g23 = *reinterpret_cast<const __nv_bfloat162*>(&gw.y);
+    uint2 o;
+    o.x = dev::pack_bf16x2(x.x * rs * __bfloat162float(g01.x), x.y * rs * __bfloat162float(g01.y));
+    o.y = dev::pack_bf16x2(x.z * rs * __bfloat162float(g23.x), x.w * rs * __bfloat162float(g23.y));
+    reinterpret_cast<uint2*>(a + row * H)[k4] = o;
+  };
+#pragma unroll
+  for (int u = 0; u < kV; ++u) {
+    const int k4 = threadIdx.x + u * 256;
+    if (k4 < H4) put(v[u], k4);
+  }
+  for (int k4 = threadIdx.x + kV * 256; k4 < H4; k4 += 256) put(src[k4], k4);
 }
 
 // One CTA per (tile of tokens, head): sum the split partials, rotate q/k
@@ -278,9 +315,14 @@ cudaError_t launch_rope_table(const RowMap& rows, int d, float theta, float2* ta
 }
 
 cudaError_t launch_embed(const __nv_bfloat16* hidden, int m, int H, const __nv_bfloat16* gain,
-                         float eps, float* h, __nv_bfloat16* a, float* ss_out, int nss, bool a16,
-                         cudaStream_t st) {
-  return launch_k(embed_kernel, m, 256, 0, st, hidden, H, gain, eps, h, a, ss_out, nss, a16);
+                         float eps, float* h, __nv_bfloat16* a, bool a16, cudaStream_t st) {
+  return launch_k(embed_kernel, m, 256, 0, st, hidden, H, gain, eps, h, a, a16);
+}
+
+cudaError_t launch_norm(const float* h, int m, int H, const __nv_bfloat16* gain, float eps,
+                        __nv_bfloat16* a, cudaStream_t st) {
+  if (H % 4) return cudaErrorInvalidValue;
+  return launch_k(norm_kernel, m, 256, 0, st, h, H, gain, eps, a);
 }
 
 // One warp per token: the largest of the tiles' bests, lowest row on ties.

@@ -34,11 +34,9 @@
 //     q to the KV-head-major q buffer, K rows and V^T columns to the slot
 //     (goinfer "What goinfer does": one key and one value row per token and layer);
 //   * Resid (applied as the contributions are added, with the residual row
-//     loaded alongside them): h += y in fp32, and on the last layer out = bf16(h).  The
-//     RMSNorm that follows needs the whole row, which no tile has; it is
-//     deferred instead: the tile writes a = bf16(h * gain) and its share of
-//     sum(h^2) per row, and the next projection, linear in a, multiplies its
-//     results by rsqrt(sum / H + eps) when it adds the tile's contributions;
+//     loaded alongside them): h += y in fp32, and on the last layer out = bf16(h)
+//     (the RMSNorm that follows needs the whole row, which no tile has: a
+//     one-row-per-CTA launch forms it);
 //   * Swiglu: the tile holds gate rows n0..n0+63 and the same up rows, so
 //     z = bf16(silu(g) * u) is local to the tile;
 //   * Cast: out = bf16(y) (attention-only layers);
@@ -157,13 +155,10 @@ __device__ __forceinline__ void epi_qkv(const GemvParams& p, const GemvSeg& seg,
   }
 }
 
-// Resid, one float4 of row i (columns row0 + c4 .. +3): h = h_old + y, the
-// final bf16 output on the last layer, and with a gain the deferred RMSNorm
-// input of the next projection, a = bf16(h * gain); returns the float4's
-// share of sum(h^2) (0 without a gain).  The tile's sum per row is one warp
-// reduction in a fixed order (a warp covers one row's 128 columns).
-__device__ __forceinline__ float resid_apply(const GemvParams& p, int row0, long long i, int c4, float4 hv,
-                                             const float4& y) {
+// Resid, one float4 of row i (columns row0 + c4 .. +3): h = h_old + y, and
+// the final bf16 output on the last layer.
+__device__ __forceinline__ void resid_apply(const GemvParams& p, int row0, long long i, int c4, float4 hv,
+                                            const float4& y) {
   hv.x += y.x; hv.y += y.y; hv.z += y.z; hv.w += y.w;
   *reinterpret_cast<float4*>(p.h + i * p.H + row0 + c4) = hv;
   if (p.out) {
@@ -172,23 +167,6 @@ __device__ __forceinline__ float resid_apply(const GemvParams& p, int row0, long
     o.y = dev::pack_bf16x2(hv.z, hv.w);
     *reinterpret_cast<uint2*>(p.out + i * p.ldout + row0 + c4) = o;
   }
-  if (!p.gain) return 0.f;
-  const uint2 gw = *reinterpret_cast<const uint2*>(p.gain + row0 + c4);
-  const __nv_bfloat162 g01 = *reinterpret_cast<const __nv_bfloat162*>(&gw.x);
-  const __nv_bfloat162 g23 = *reinterpret_cast<const __nv_bfloat162*>(&gw.y);
-  uint2 o;
-  o.x = dev::pack_bf16x2(hv.x * __bfloat162float(g01.x), hv.y * __bfloat162float(g01.y));
-  o.y = dev::pack_bf16x2(hv.z * __bfloat162float(g23.x), hv.w * __bfloat162float(g23.y));
-  *reinterpret_cast<uint2*>(p.a + i * p.H + row0 + c4) = o;
-  return hv.x * hv.x + hv.y * hv.y + hv.z * hv.z + hv.w * hv.w;
-}
-
-__device__ __forceinline__ void resid_tile_sum(const GemvParams& p, int row0, long long i, float ss, int lane) {
-  static_assert(kGemvRows / 4 == 32, "one warp per row of the tile");
-  if (!p.gain) return;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-  if (lane == 0) p.ss_out[i * p.nss + row0 / kGemvRows] = ss;
 }
 
 __device__ __forceinline__ void epi_swiglu(const GemvParams& p, int row0, const float* ct, int tid) {
@@ -460,21 +438,6 @@ __device__ __forceinline__ bool gemv_consume(const GemvParams& p, uint32_t base,
   return ok;
 }
 
-// Input rows in the deferred-RMSNorm form: each row's factor from its sums
-// (fixed order), applied when the tile's contributions are added.  The loads
-// overlap the first activation copies.
-__device__ __forceinline__ void row_scales(const GemvParams& p, float* row_scale) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (!p.ss_in) return;
-  for (int t = warp; t < p.mb; t += kConsumerWarps) {
-    float v = 0.f;
-    for (int j = lane; j < p.nss; j += 32) v += p.ss_in[(long long)(p.c0 + t) * p.nss + j];
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    if (lane == 0) row_scale[t] = rsqrtf(v / p.H + p.eps);
-  }
-}
-
 // Stream-K: a CTA takes an equal run of (tile, k-step) units of the whole
 // launch (the host sizes the grid to one resident wave: two CTAs per SM for
 // up to 16 tokens, one beyond).
@@ -490,7 +453,6 @@ __global__ void __launch_bounds__(kThreads, NT == 4 ? 1 : 2) gemv_int4_kernel(co
   __shared__ int own_tiles[kMaxOwnTiles];
   // K-quant: per warp and stage, (d*sc, dmin*mn) of its 16 rows x 8 sub-blocks
   __shared__ float2 q4k_tab[FMT == kFmtQ4K ? kConsumerWarps * 128 : 1];
-  __shared__ float row_scale[kGemvMaxCols];   // deferred RMSNorm of the input rows
   // QKV up to 8 tokens: the rows' (cos, sin), d <= 128 (more rows would cost
   // the second CTA per SM its shared memory; they read the table directly)
   constexpr bool kRopeS = EPI == kGemvEpiQKV && NT == 1;
@@ -526,7 +488,6 @@ __global__ void __launch_bounds__(kThreads, NT == 4 ? 1 : 2) gemv_int4_kernel(co
 
   dev::pdl_wait();                  // results are written below
   const int tid = threadIdx.x;      // 0..255 over the consumer warps
-  row_scales(p, row_scale);
   if (kRopeS)   // off the epilogue's path: loaded while the activations arrive
     for (int idx = tid; idx < p.mb * (p.d >> 1); idx += kConsumers)
       rope_s[idx] = p.rope[(long long)p.c0 * (p.d >> 1) + idx];
@@ -611,13 +572,8 @@ __global__ void __launch_bounds__(kThreads, NT == 4 ? 1 : 2) gemv_int4_kernel(co
             v.x += w[j].x; v.y += w[j].y; v.z += w[j].z; v.w += w[j].w;
           }
       }
-      if (p.ss_in) {
-        const float f = row_scale[tok];
-        v.x *= f; v.y *= f; v.z *= f; v.w *= f;
-      }
       if (EPI == kGemvEpiResid) {   // epilogue in place: no trip through shared memory
-        const float ss = r4 < nv_h ? resid_apply(p, row0, p.c0 + tok, r4, h_old, v) : 0.f;
-        resid_tile_sum(p, row0, p.c0 + tok, ss, lane);
+        if (r4 < nv_h) resid_apply(p, row0, p.c0 + tok, r4, h_old, v);
       } else {
         *reinterpret_cast<float4*>(ct + tok * kTileLd + r4) = v;
       }

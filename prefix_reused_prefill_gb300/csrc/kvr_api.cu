@@ -101,12 +101,9 @@ int attn_nsplit(int Hkv, int R, int kend_max, int target) {
 }
 
 struct ScratchLayout {
-  size_t status, counters, prompt, slot_len, match_out, rope, h, a, ss, q, o, z, part, opart, ml, best, next, total;
+  size_t status, counters, prompt, slot_len, match_out, rope, h, a, q, o, z, part, opart, ml, best, next, total;
   size_t part_floats, opart_floats, ml_count;
 };
-
-// deferred-RMSNorm sums per row: one per 128-column tile of the hidden width
-size_t ss_per_row(size_t H) { return (H + kGemvRows - 1) / kGemvRows; }
 
 ScratchLayout scratch_layout(const kvr_config* c) {
   ScratchLayout L{};
@@ -123,7 +120,6 @@ ScratchLayout scratch_layout(const kvr_config* c) {
   L.rope = take(M * (c->head_dim / 2) * 8);
   L.h = take(M * H * 4);
   L.a = take(M * H * 2);
-  L.ss = take(M * ss_per_row(H) * 4);   // deferred RMSNorm sums per row
   L.q = take(M * QD * 2);
   L.o = take(M * QD * 2);
   L.z = take(M * F * 2);
@@ -197,11 +193,6 @@ struct kvr_ctx {
   float2* rope = nullptr;
   float* h = nullptr;
   __nv_bfloat16 *a = nullptr, *q = nullptr, *o = nullptr, *z = nullptr;
-  // a holds bf16(h * gain) with each row's sum of h^2 per 128-column tile in
-  // ss (the small-m GEMV applies the RMSNorm factor after projecting), not
-  // finished RMSNorm rows; tracked in stream order by the host
-  float* ss = nullptr;
-  bool a_deferred = false;
   // the call's projections run on the tcgen05 GEMM, whose operands are fp16:
   // a, o and z then hold their bf16-rounded values in fp16
   bool act16 = false;
@@ -432,8 +423,8 @@ struct Fused {
 };
 
 // Small-m int4 passes: the GEMV with its fused epilogue.  A residual
-// projection with a norm gain leaves the next RMSNorm deferred (a_deferred);
-// a projection of c->a in that form applies it.
+// projection with a norm gain is followed by the row-wise RMSNorm launch that
+// forms the next projection's input a.
 int project_gemv_int4(kvr_ctx* c, cudaStream_t st, const Seg* segs, int nseg, const CUtensorMap* tmx,
                       int K, int m, const Fused& fz) {
   const kvr_config& cfg = c->cfg;
@@ -494,15 +485,6 @@ int project_gemv_int4(kvr_ctx* c, cudaStream_t st, const Seg* segs, int nseg, co
   p.F = cfg.ffn;
   p.slot_stride = kv_offset(c, 1, 0, 0);
   p.best = fz.best;
-  p.nss = (int)ss_per_row(cfg.hidden);
-  p.eps = cfg.rms_eps;
-  if (tmx == c->tm_a && c->a_deferred) p.ss_in = c->ss;
-  const bool norm_out = fz.epi == kGemvEpiResid && fz.norm_gain;
-  if (norm_out) {
-    p.gain = fz.norm_gain;
-    p.a = c->a;
-    p.ss_out = c->ss;
-  }
   for (int c0 = 0; c0 < m; c0 += kGemvMaxCols) {
     const int mb = std::min(kGemvMaxCols, m - c0);
     p.c0 = c0;
@@ -537,7 +519,11 @@ int project_gemv_int4(kvr_ctx* c, cudaStream_t st, const Seg* segs, int nseg, co
     }
     if (e != cudaSuccess) return cuda_fail(c, e, "gemv_int4 launch");
   }
-  if (norm_out) c->a_deferred = true;
+  if (fz.epi == kGemvEpiResid && fz.norm_gain) {
+    Timed t(c, kEpi, st);
+    const cudaError_t e = launch_norm(c->h, m, cfg.hidden, fz.norm_gain, cfg.rms_eps, c->a, st);
+    if (e != cudaSuccess) return cuda_fail(c, e, "norm launch");
+  }
   return KVR_OK;
 }
 
@@ -547,10 +533,6 @@ int project(kvr_ctx* c, cudaStream_t st, const Seg* segs, int nseg, Act act, int
   const kvr_config& cfg = c->cfg;
   const CUtensorMap* tmx = act == Act::A ? c->tm_a : (act == Act::O ? c->tm_o : c->tm_z);
   if (packed4(cfg) && gemv_path(c, m)) return project_gemv_int4(c, st, segs, nseg, tmx, K, m, fz);
-  // the row-wise epilogues below write finished RMSNorm rows
-  if (tmx == c->tm_a && c->a_deferred)
-    return fail(c, KVR_ERR_UNSUPPORTED, "activations in the deferred-norm form reached a row-wise path");
-  if (fz.epi == kGemvEpiResid && fz.norm_gain) c->a_deferred = false;
   if (packed4(cfg)) return project_gemm(c, st, segs, nseg, tmx, K, m, swiglu, epi);
   // bf16 weights: plain GEMV into partials, then the row-wise epilogue kernel
   GemvParams p;
@@ -778,19 +760,12 @@ int run_stack(kvr_ctx* c, const RowMap& rows, const void* hidden,
   }
   if (e != cudaSuccess) return cuda_fail(c, e, "rope table launch");
   c->act16 = packed4(k) && !gemv_path(c, m);
-  if (k.attn_only) {
-    c->a_deferred = false;
-    Timed t(c, kEpi, st);
-    e = launch_embed(static_cast<const __nv_bfloat16*>(hidden), m, H, nullptr, 0.f, nullptr, c->a, nullptr, 0,
-                     c->act16, st);
-    if (e != cudaSuccess) return cuda_fail(c, e, "input copy launch");
-  } else {
-    // the small-m GEMV takes the first RMSNorm deferred, like every later one
-    c->a_deferred = packed4(k) && gemv_path(c, m);
+  {
+    // attention-only layers take the input rows as they are (no norm)
     Timed t(c, kEpi, st);
     e = launch_embed(static_cast<const __nv_bfloat16*>(hidden), m, H,
-                     static_cast<const __nv_bfloat16*>(w[0].norm_attn), k.rms_eps, c->h, c->a,
-                     c->a_deferred ? c->ss : nullptr, (int)ss_per_row(H), c->act16, st);
+                     k.attn_only ? nullptr : static_cast<const __nv_bfloat16*>(w[0].norm_attn), k.rms_eps,
+                     c->h, c->a, c->act16, st);
     if (e != cudaSuccess) return cuda_fail(c, e, "embed launch");
   }
   auto trace = [&](int entry) -> cudaError_t {
@@ -1262,7 +1237,6 @@ int kvr_ctx_create(const kvr_config* cfg, void* kv_arena, size_t arena_bytes, vo
   c->rope = reinterpret_cast<float2*>(s + c->sl.rope);
   c->h = reinterpret_cast<float*>(s + c->sl.h);
   c->a = reinterpret_cast<__nv_bfloat16*>(s + c->sl.a);
-  c->ss = reinterpret_cast<float*>(s + c->sl.ss);
   c->q = reinterpret_cast<__nv_bfloat16*>(s + c->sl.q);
   c->o = reinterpret_cast<__nv_bfloat16*>(s + c->sl.o);
   c->z = reinterpret_cast<__nv_bfloat16*>(s + c->sl.z);

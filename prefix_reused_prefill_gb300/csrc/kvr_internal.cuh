@@ -145,17 +145,6 @@ struct GemvParams {
   __nv_bfloat16* z;     // Swiglu: [max_rows][F]
   int F;
   float2* best;         // Argmax: [token][tiles] (value, row)
-  // Deferred RMSNorm of the small-m path.  A residual epilogue with a gain
-  // writes a = bf16(h * gain) and, per row and 128-column tile, the sum of
-  // h^2; a launch that reads those rows scales each row's results by
-  // rsqrt(sum / H + eps), which is RMSNorm applied after the (linear)
-  // projection instead of before it.
-  const __nv_bfloat16* gain;  // Resid: the next RMSNorm's gain, or null
-  __nv_bfloat16* a;           // Resid with gain: bf16 [max_rows][H]
-  float* ss_out;              // Resid with gain: [max_rows][nss]
-  const float* ss_in;         // the input rows' sums [max_rows][nss], or null (rows already normed)
-  int nss;                    // ceil(H / 128)
-  float eps;
 };
 
 struct GemmSeg {
@@ -269,14 +258,15 @@ cudaError_t launch_attention_tc(const AttnParams& p, int d, cudaStream_t st);
 cudaError_t launch_attn_combine(const AttnParams& p, int d, cudaStream_t st);
 cudaError_t launch_rope_table(const RowMap& rows, int d, float theta, float2* table,
                               cudaStream_t st);
-// h = float(hidden) and the first RMSNorm: a = bf16(RMSNorm(h) * gain), or,
-// with ss_out (the deferred form read by the small-m GEMV), a = bf16(h * gain)
-// and ss_out[row][0] = sum of h^2 (the row's other nss - 1 entries zero).
+// h = float(hidden) and the first RMSNorm: a = bf16(RMSNorm(h) * gain).
 // Without a gain, a = hidden (attention-only layers; h untouched).  a16: a
 // holds the bf16-rounded values as fp16 (the tcgen05 GEMM's operand type).
 cudaError_t launch_embed(const __nv_bfloat16* hidden, int m, int H, const __nv_bfloat16* gain,
-                         float eps, float* h, __nv_bfloat16* a, float* ss_out, int nss, bool a16,
-                         cudaStream_t st);
+                         float eps, float* h, __nv_bfloat16* a, bool a16, cudaStream_t st);
+// a = bf16(RMSNorm(h) * gain) for rows [0, m) of the fp32 residual stream
+// (after a small-m residual projection, whose tiles each hold part of a row)
+cudaError_t launch_norm(const float* h, int m, int H, const __nv_bfloat16* gain, float eps,
+                        __nv_bfloat16* a, cudaStream_t st);
 // out[t] = the row of the largest value over the tiles' bests of token t
 // (lowest row on ties), t < m
 // one device-side wait that runs out (the failure path, without a fault)
