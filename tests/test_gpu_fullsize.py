@@ -4,17 +4,11 @@ The oracle cannot run a 28- or 36-layer stack over thousands of rows, so each
 test runs the CUDA path at full size and checks it layer by layer: the
 library's per-layer trace gives the GPU's input to layer l, the slot gives
 the cached prefix K/V, and the oracle evaluates layer l for sampled rows
-(oracle.model.layer_rows) and for the K/V of every new row.  
-Tolerances.  K/V rows and unit-scale outputs: |gpu - oracle| <= 1e-2 +
-2e-2 |oracle| elementwise, as in test_gpu_parity; for rotated K the relative
-term takes the larger magnitude of the element's rotate-half pair (RoPE mixes
-the pair, so a large partner's rounding error reaches a small element).  Residual-stream rows
-(float32, rms 2.5-10 at these widths): per row, max |gpu - oracle| <= 1e-2 *
-max |oracle| and ||gpu - oracle|| <= 2e-2 ||oracle||.  An elementwise 1e-2
-absolute bound is below one bf16 step of such values; the per-element error of
-a sum over 4-19 thousand bf16-rounded terms follows the row's scale (an fp32
-CPU evaluation with the same rounding points is already max 0.0115 away from
-the float64 oracle on a 9B layer).  NaN fails every check.
+(oracle.model.layer_rows) and for the K/V of every new row.
+
+Tolerance: the stated bf16 bar, |gpu - oracle| <= 1e-2 + 2e-2 |oracle|
+elementwise, on the K/V rows and on the residual-stream rows alike.  NaN
+fails every check.
 """
 import gc
 
@@ -62,41 +56,6 @@ def close(got, ref, what):
     return float(err.max())
 
 
-def close_rope(got, ref, what):
-    """Rotated K rows [head][row][d]: RoPE turns each rotate-half pair (j, j + d/2)
-    as one 2-vector, so the error of either input lands on both outputs; the
-    relative part of the elementwise bound uses the pair's larger magnitude."""
-    got = np.asarray(got, dtype=np.float64)
-    ref = np.asarray(ref, dtype=np.float64)
-    half = ref.shape[-1] // 2
-    pair = np.maximum(np.abs(ref), np.abs(np.roll(ref, half, axis=-1)))
-    err = np.abs(got - ref)
-    bad = ~(err <= ATOL + RTOL * pair)   # NaN fails
-    detail = ""
-    if bad.any():
-        w = np.unravel_index(np.argmax(err - (ATOL + RTOL * pair)), err.shape)
-        p = w[:-1] + ((w[-1] + half) % (2 * half),)
-        detail = (f" worst at {w}: gpu {got[w]:.5g} oracle {ref[w]:.5g}, partner oracle {ref[p]:.5g}")
-    print(f"[parity] {what}: max err {err.max():.3g}, rms err {np.sqrt(np.mean(err ** 2)):.3g}, "
-          f"rms ref {np.sqrt(np.mean(ref ** 2)):.3g}")
-    assert not bad.any(), f"{what}: {int(bad.sum())}/{bad.size} out of tolerance, max err {err.max():.4g};" + detail
-    return float(err.max())
-
-
-def close_rows(got, ref, what):
-    """Per row: max-abs error <= 1e-2 * max-abs of the row, norm-relative <= 2e-2."""
-    got = np.asarray(got, dtype=np.float64)
-    ref = np.asarray(ref, dtype=np.float64)
-    assert np.isfinite(got).all(), f"{what}: non-finite values"
-    err = np.abs(got - ref)
-    rel_max = err.max(axis=1) / np.abs(ref).max(axis=1)
-    rel_norm = np.linalg.norm(got - ref, axis=1) / np.linalg.norm(ref, axis=1)
-    print(f"[parity] {what}: max-abs/row-max {rel_max.max():.3g}, norm-relative {rel_norm.max():.3g}, "
-          f"max err {err.max():.3g}, rms ref {np.sqrt(np.mean(ref ** 2)):.3g}")
-    assert (rel_max <= 1e-2).all() and (rel_norm <= 2e-2).all(), (
-        f"{what}: per-row max-abs/row-max {rel_max.tolist()}, norm-relative {rel_norm.tolist()}")
-
-
 def oracle_layer_weights(lw):
     """Decode one layer's device weights on the CPU (the oracle's own decoding)."""
     W = {}
@@ -131,9 +90,9 @@ def check_layer(shape, lw, kv, slot, layer, trace, P, rows, out_rows, what):
     h_in = trace[layer, :m].astype(np.float64)
     ref = om.layer_rows(dims, W, h_in, K, V, rows, out_rows)
     Kg, Vg = slot_prefix(kv, slot, layer, cap)
-    close_rope(Kg[:, P:cap], K[:, P:cap], f"{what} layer {layer} new K")
+    close(Kg[:, P:cap], K[:, P:cap], f"{what} layer {layer} new K")
     close(Vg[:, P:cap], V[:, P:cap], f"{what} layer {layer} new V")
-    close_rows(trace[layer + 1, out_rows], ref, f"{what} layer {layer} rows {list(out_rows)}")
+    close(trace[layer + 1, out_rows], ref, f"{what} layer {layer} rows {list(out_rows)}")
 
 
 def make_ctx(shape, n_slots, cap, max_rows):
@@ -242,9 +201,9 @@ def test_batch_full_size_four_conversations():
             h_in = tr[layer, at:at + lens[j]].astype(np.float64)
             ref = om.layer_rows(dims, W, h_in, K, V, om.plain_rows(4096, lens[j]), list(range(lens[j])))
             Kg, Vg = slot_prefix(kv, j, layer, 4096 + lens[j])
-            close_rope(Kg[:, 4096:], K[:, 4096:], f"batch conversation {j} layer {layer} new K")
+            close(Kg[:, 4096:], K[:, 4096:], f"batch conversation {j} layer {layer} new K")
             close(Vg[:, 4096:], V[:, 4096:], f"batch conversation {j} layer {layer} new V")
-            close_rows(tr[layer + 1, at:at + lens[j]], ref, f"batch conversation {j} layer {layer}")
+            close(tr[layer + 1, at:at + lens[j]], ref, f"batch conversation {j} layer {layer}")
         at += lens[j]
     kv.close()
 
@@ -324,7 +283,7 @@ def test_priming_full_size_equals_separate_runs():
         ta = trace.cpu().numpy()
         assert kv.kvr_slot_len(0) == P + n
         assert torch.isfinite(alone.float()).all()
-        close_rows(ta[1, :n], tr[1, off:off + n], f"branch {b} layer 0 batched vs alone")
+        close(ta[1, :n], tr[1, off:off + n], f"branch {b} layer 0 batched vs alone")
         if b == len(lens) - 1:
             for layer in (0, 35):
                 check_layer(shape, lws[layer], kv, 0, layer, ta, P, om.plain_rows(P, n),
@@ -365,6 +324,6 @@ def test_attention_layer_at_capacity(m):
     ref = om.layer_rows(dims, W, workloads.bf16_to_f64(x), K, V, om.plain_rows(P, m), sel)
     close(workloads.bf16_to_f64(out)[sel], ref, f"attention layer m={m}")
     Kg, Vg = slot_prefix(kv, 3, 0, P + m)
-    close_rope(Kg[:, P:], K[:, P:], "new K")
+    close(Kg[:, P:], K[:, P:], "new K")
     close(Vg[:, P:], V[:, P:], "new V")
     kv.close()

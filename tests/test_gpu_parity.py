@@ -34,10 +34,10 @@ def close(got, ref, what=""):
     return float(err.max())
 
 
-def make(shape_name, n_slots, cap, max_rows, seed=21, threshold=True):
+def make(shape_name, n_slots, cap, max_rows, seed=21, threshold=True, scales="fp16"):
     from prefix_reused_prefill_gb300 import Kvr, config_for_shape
     shape = workloads.SHAPES[shape_name]
-    lws = workloads.stack_weights(shape, seed)
+    lws = workloads.stack_weights(shape, seed, scales=scales)
     kv = Kvr(config_for_shape(shape, n_slots, cap, max_rows, threshold), device="cuda")
     gw = workloads.weights_to(lws, "cuda")
     w = kv.weights(gw)
@@ -121,8 +121,7 @@ def test_suffix_prefill_matches_oracle(shape_name, P, ms, cap):
 @pytest.mark.parametrize("shape_name", ["small", "small_q4k"])
 def test_many_rows_on_the_gemv_match_oracle(monkeypatch, shape_name):
     """KVR_FORCE_GEMV=1 keeps every m on the GEMV (32-row passes) and the split-KV
-    attention: the deferred RMSNorm then spans passes (each pass reads and
-    writes its own rows' sums)."""
+    attention: the residual epilogue and the RMSNorm launch then span passes."""
     monkeypatch.setenv("KVR_FORCE_GEMV", "1")
     shape, kv, w, W, _ = make(shape_name, 1, 256, 128)
     monkeypatch.delenv("KVR_FORCE_GEMV")
@@ -196,6 +195,102 @@ def test_small_m_on_the_tensor_core_gemm_matches_oracle(monkeypatch, shape_name)
         out = kv.kvr_prefill_suffix(0, toks[40:40 + m], x[40:40 + m].cuda(), w)
         kv.kvr_sync_status()
         close(workloads.bf16_to_f64(out), whole[40:40 + m], f"{shape_name} m={m} on the GEMM")
+
+
+def test_five_bit_scales_named_case():
+    """The named extra input case: scales with at most 5 significant bits, where
+    every code*scale is exactly a bf16 (and fp16) number, through the GEMV
+    (m = 3) and the tcgen05 GEMM (m = 40)."""
+    shape, kv, w, W, _ = make("small", 1, 256, 64, scales="5bit")
+    dims = oracle_dims(shape)
+    toks = list(range(4000, 4000 + 120))
+    x = hidden(toks, shape)
+    cache = om.SlotKV(shape.n_layers, shape.n_kv_heads, 256, shape.head_dim)
+    whole = om.prefill(dims, W, cache, workloads.bf16_to_f64(x), 0)
+    kv.kvr_slot_match(toks[:1])
+    pre = kv.kvr_prefill_suffix(0, toks[:70], x[:70].cuda(), w)
+    close(workloads.bf16_to_f64(pre), whole[:70], "5-bit scales, 70 rows")
+    for m in (3, 40):
+        kv.kvr_slot_truncate(0, 70)
+        out = kv.kvr_prefill_suffix(0, toks[70:70 + m], x[70:70 + m].cuda(), w)
+        kv.kvr_sync_status()
+        close(workloads.bf16_to_f64(out), whole[70:70 + m], f"5-bit scales m={m}")
+
+
+@pytest.mark.parametrize("m", [3, 40])
+def test_swapped_norm_gains_are_caught(m):
+    """The two RMSNorm gains of a layer are distinct bf16 draws in [0.5, 1.5):
+    the GPU output matches the oracle with the gains in place and fails the
+    same bound against an oracle whose first layer has them swapped (the
+    mistake is planted in the oracle's weights, on the CPU).  m = 3 takes the
+    GEMV path, m = 40 the tcgen05 GEMM and its row-wise norms."""
+    shape, kv, w, W, _ = make("small", 1, 256, 64)
+    dims = oracle_dims(shape)
+    toks = list(range(6000, 6000 + 50 + m))
+    x = hidden(toks, shape)
+    kv.kvr_slot_match(toks[:1])
+    kv.kvr_prefill_suffix(0, toks[:50], x[:50].cuda(), w)
+    out = workloads.bf16_to_f64(kv.kvr_prefill_suffix(0, toks[50:], x[50:].cuda(), w))
+    kv.kvr_sync_status()
+    cache = om.SlotKV(shape.n_layers, shape.n_kv_heads, 256, shape.head_dim)
+    ref = om.prefill(dims, W, cache, workloads.bf16_to_f64(x), 0)[50:]
+    close(out, ref, f"gains in place m={m}")
+    Ws = [dict(lw) for lw in W]
+    Ws[0]["norm_attn"], Ws[0]["norm_ffn"] = W[0]["norm_ffn"], W[0]["norm_attn"]
+    cache = om.SlotKV(shape.n_layers, shape.n_kv_heads, 256, shape.head_dim)
+    swapped = om.prefill(dims, Ws, cache, workloads.bf16_to_f64(x), 0)[50:]
+    with pytest.raises(AssertionError):
+        close(out, swapped, f"gains swapped m={m}")
+
+
+def peaked_kv(n_kv_heads, P, d, alpha_max, seed):
+    """Cached K/V for a sharply peaked, steadily sharpening softmax: key j is
+    alpha_j * z_j with z_j ~ N(0, I) and alpha_j rising linearly from
+    0.05*alpha_max to alpha_max over the prefix, so a row's scores spread
+    wider block after block and its running maximum keeps growing; V ~ N(0, 1).
+    Both rounded to bf16, [Hkv][P][d]."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    z = rng.standard_normal((n_kv_heads, P, d), dtype=np.float32)
+    alpha = (alpha_max * (0.05 + 0.95 * np.arange(P) / max(P - 1, 1))).astype(np.float32)
+    v = rng.standard_normal((n_kv_heads, P, d), dtype=np.float32)
+    return workloads.to_bf16(z * alpha[None, :, None]), workloads.to_bf16(v)
+
+
+@pytest.mark.parametrize("combine", ["0", "1"])
+@pytest.mark.parametrize("shape_name,P,alpha,ms", [
+    ("small_attn", 1000, 40.0, [1, 3, 8, 40]),     # split-KV up to 24 rows, tcgen05 from 25
+    ("qwen7b_attn", 2000, 16.0, [1, 4, 16, 64]),   # split-KV up to 13 rows, tcgen05 from 14
+])
+def test_peaked_attention_matches_oracle(monkeypatch, shape_name, P, alpha, ms, combine):
+    """Scores with std >= 10 whose row maximum grows across the prefix: the
+    tcgen05 kernel must move its lazy reference maximum (and rescale O) many
+    times, and the split-KV kernel must merge splits whose maxima differ by
+    many units, by the last split (one row per warp) or by the combine launch
+    (KVR_ATTN_COMBINE=1).  Cached K/V given through kvr_slot_kv."""
+    monkeypatch.setenv("KVR_ATTN_COMBINE", combine)
+    shape, kv, w, W, _ = make(shape_name, 2, 2176, 64, seed=workloads.config_seed(5))
+    monkeypatch.delenv("KVR_ATTN_COMBINE")
+    dims = oracle_dims(shape)
+    kk, vv = peaked_kv(shape.n_kv_heads, P, shape.head_dim, alpha, 91)
+    k, v = kv.kvr_slot_kv(1, 0)
+    k[:, :P] = kk.cuda()
+    v[:, :, :P] = vv.transpose(1, 2).cuda()
+    kv.kvr_slot_assign(1, list(range(P)))
+    cache = om.SlotKV(1, shape.n_kv_heads, 2176, shape.head_dim)
+    cache.K[0][:, :P] = workloads.bf16_to_f64(kk)
+    cache.V[0][:, :P] = workloads.bf16_to_f64(vv)
+    new = list(range(9000, 9000 + max(ms)))
+    x = hidden(new, shape)
+    ref = om.prefill(dims, W, cache, workloads.bf16_to_f64(x), P)
+    # the inputs really are peaked: the last rows' score spread over the prefix
+    q = workloads.bf16_to_f64(x[-1:]) @ W[0]["wq"].T
+    s = (q.reshape(shape.n_q_heads, shape.head_dim)[0] @ cache.K[0][0, :P].T) / np.sqrt(shape.head_dim)
+    assert s[-256:].std() >= 10.0 and s[-256:].max() > s[:256].max() + 20.0
+    for m in ms:
+        kv.kvr_slot_truncate(1, P)
+        out = kv.kvr_prefill_suffix(1, new[:m], x[:m].cuda(), w)
+        kv.kvr_sync_status()
+        close(workloads.bf16_to_f64(out), ref[:m], f"{shape_name} peaked m={m} combine={combine}")
 
 
 def test_verify_then_truncate_equals_single_steps():
