@@ -365,7 +365,11 @@ int kvr_prefill_batch(kvr_ctx* ctx, int n_seq, const int* slots, const int* lens
 /* Wait for `stream` and check the device status word that kernels set when a
  * bounded device-side wait gives up.  Returns KVR_ERR_TIMEOUT (and clears the
  * word and the kernels' arrival counters, so the next call starts clean) if
- * one did; the outputs of the call that timed out are not to be used. */
+ * one did; the outputs of the call that timed out are not to be used.
+ * While the word is set, every kernel the library launches leaves at entry
+ * and every pending wait gives up within microseconds: the calls issued after
+ * a timeout and before this check compute nothing (their outputs, and the
+ * K/V rows they were to append, are not to be used either). */
 int kvr_sync_status(kvr_ctx* ctx, void* stream);
 
 /* Per-layer trace for checking a long stack one layer at a time.  While a

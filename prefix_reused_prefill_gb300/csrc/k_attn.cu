@@ -189,10 +189,12 @@ __global__ void __launch_bounds__((RW * KW + 1) * 32) attn_kernel(const __grid_c
       dev::mbar_init(dev::smem_u32(&full_bar[i]), 1);
       dev::mbar_init(dev::smem_u32(&empty_bar[i]), RW);
     }
-    *abort_v = 0;
+    // a wait has given up earlier in the call: leave before any copy
+    *abort_v = dev::status_set(p.status) ? 1 : 0;
     dev::fence_mbar_init();
   }
   __syncthreads();
+  if (*abort_v) return;
 
   if (warp == kCons) {
     // ------------------------------------------------------------ producer
@@ -237,9 +239,10 @@ __global__ void __launch_bounds__((RW * KW + 1) * 32) attn_kernel(const __grid_c
         dev::tma_load_2d(sb + C::kTileBytes, &p.tvt, key0, v.vtbase + kv * D, fb);
         ++issued;
       }
+      const unsigned long long deadline = dev::globaltimer_ns() + kWaitLimitNs;
       for (int st = 0; st < C::kStages && st < issued; ++st) {
         const int last = ((issued - 1 - st) / C::kStages) * C::kStages + st;
-        dev::mbar_wait(dev::smem_u32(&full_bar[st]), (uint32_t)(last / C::kStages) & 1, nullptr);
+        dev::mbar_wait_until(dev::smem_u32(&full_bar[st]), (uint32_t)(last / C::kStages) & 1, deadline);
       }
     }
     return;

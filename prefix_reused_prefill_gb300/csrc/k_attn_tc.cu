@@ -201,9 +201,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       dev::mbar_init(dev::smem_u32(&p_full[i]), kSoftmaxWarps);
       dev::mbar_init(dev::smem_u32(&pv_done[i]), 1);
     }
-    *abort_v = 0;
+    // a wait has given up earlier in the call: leave before any copy or
+    // tensor-memory allocation (one decision for the whole CTA)
+    *abort_v = dev::status_set(p.status) ? 1 : 0;
     dev::fence_mbar_init();
   }
+  __syncthreads();
+  if (*abort_v) return;
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      dev::smem_u32(&tmem_slot)),
@@ -289,10 +293,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         load(j, ring + st * bytes, fb);
         ++issued;
       }
-      if (is_k) dev::mbar_wait(qb, 0, nullptr);
+      const unsigned long long deadline = dev::globaltimer_ns() + kWaitLimitNs;
+      if (is_k) dev::mbar_wait_until(qb, 0, deadline);
       for (int st = 0; st < stages && st < issued; ++st) {
         const int last = ((issued - 1 - st) / stages) * stages + st;
-        dev::mbar_wait(dev::smem_u32(&fullb[st]), (uint32_t)(last / stages) & 1, nullptr);
+        dev::mbar_wait_until(dev::smem_u32(&fullb[st]), (uint32_t)(last / stages) & 1, deadline);
       }
     }
   } else if (warp == 1) {

@@ -209,10 +209,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_int4_tc_kernel(const __grid_
       dev::mbar_init(dev::smem_u32(&x_empty[i]), 1);
     }
     dev::mbar_init(dev::smem_u32(&acc_full), 1);
-    *abort_v = 0;
+    // a wait has given up earlier in the call: leave before any copy or
+    // tensor-memory allocation (one decision for the whole CTA)
+    *abort_v = dev::status_set(p.status) ? 1 : 0;
     epi_bad = 0;
     dev::fence_mbar_init();
   }
+  __syncthreads();
+  if (*abort_v) return;
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      dev::smem_u32(&tmem_slot)),
@@ -268,9 +272,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_int4_tc_kernel(const __grid_
         }
         ++issued;
       }
+      const unsigned long long deadline = dev::globaltimer_ns() + kWaitLimitNs;
       for (int st = 0; st < kRawStages && st < issued; ++st) {
         const int last = ((issued - 1 - st) / kRawStages) * kRawStages + st;
-        dev::mbar_wait(dev::smem_u32(&raw_full[st]), (uint32_t)(last / kRawStages) & 1, nullptr);
+        dev::mbar_wait_until(dev::smem_u32(&raw_full[st]), (uint32_t)(last / kRawStages) & 1, deadline);
       }
     } else if (lane == 1) {
       dev::prefetch_tmap(&p.tx);
@@ -289,9 +294,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_int4_tc_kernel(const __grid_
         dev::tma_load_2d(dst + kXAtom, &p.tx, (kc0 + i) * 128 + 64, p.t0, xb);
         ++issued;
       }
+      const unsigned long long deadline = dev::globaltimer_ns() + kWaitLimitNs;
       for (int st = 0; st < kStages && st < issued; ++st) {
         const int last = ((issued - 1 - st) / kStages) * kStages + st;
-        dev::mbar_wait(dev::smem_u32(&x_full[st]), (uint32_t)(last / kStages) & 1, nullptr);
+        dev::mbar_wait_until(dev::smem_u32(&x_full[st]), (uint32_t)(last / kStages) & 1, deadline);
       }
     }
   } else if (warp == 1) {

@@ -314,11 +314,12 @@ __device__ __forceinline__ void gemv_produce(const GemvParams& p, uint32_t base,
     load_x(sb, fb, u0 + it);
     ++issued;
   }
-  // never leave the CTA with copies in flight: wait (bounded) for the last
-  // use of every stage that was filled
+  // never leave the CTA with copies in flight: wait for the last use of
+  // every stage that was filled, all within one bounded wait
+  const unsigned long long deadline = dev::globaltimer_ns() + kWaitLimitNs;
   for (int st = 0; st < C::kStages && st < issued; ++st) {
     const int last = ((issued - 1 - st) / C::kStages) * C::kStages + st;
-    dev::mbar_wait(dev::smem_u32(&full_bar[st]), (uint32_t)(last / C::kStages) & 1, nullptr);
+    dev::mbar_wait_until(dev::smem_u32(&full_bar[st]), (uint32_t)(last / C::kStages) & 1, deadline);
   }
 }
 
@@ -475,11 +476,14 @@ __global__ void __launch_bounds__(kThreads, NT == 4 ? 1 : 2) gemv_int4_kernel(co
       dev::mbar_init(dev::smem_u32(&full_bar[i]), 1);
       dev::mbar_init(dev::smem_u32(&empty_bar[i]), kConsumerWarps);
     }
-    *abort_v = 0;
+    // a wait of this or an earlier launch has given up: the call has failed,
+    // and the whole CTA leaves before it issues a copy
+    *abort_v = dev::status_set(p.status) ? 1 : 0;
     n_own = 0;
     dev::fence_mbar_init();
   }
   __syncthreads();
+  if (*abort_v) return;
 
   if (warp == kConsumerWarps) {
     if (lane == 0) gemv_produce<NT, kPair>(p, base, full_bar, empty_bar, abort_v, u0, nk);

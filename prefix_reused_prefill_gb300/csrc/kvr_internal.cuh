@@ -352,18 +352,35 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// The device status word: non-zero once any wait of any launch has given up.
+__device__ __forceinline__ bool status_set(const int* status) {
+  return status && *reinterpret_cast<const volatile int*>(status) != 0;
+}
+
 // Wait for the phase of `parity` to complete; give up after kWaitLimitNs,
-// record the timeout in the device status word and return false.
+// record the timeout in the device status word and return false.  A wait
+// that finds the status word already set (another CTA, or an earlier launch,
+// gave up) returns false at once, so one stall ends every CTA's waits
+// within microseconds instead of one limit per wait.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* status) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer_ns();
-  while (true) {
+  for (unsigned n = 0;; ++n) {
     if (mbar_try_wait(bar, parity)) return true;
+    if ((n & 31u) == 31u && status_set(status)) return false;
     if (globaltimer_ns() - t0 > kWaitLimitNs) {
       if (status) atomicExch(status, kStatusTimeout);
       return false;
     }
   }
+}
+
+// Drain: wait for a phase until an absolute globaltimer deadline (one limit
+// shared by all the stages a CTA drains before it exits).
+__device__ __forceinline__ bool mbar_wait_until(uint32_t bar, uint32_t parity, unsigned long long deadline) {
+  while (!mbar_try_wait(bar, parity))
+    if (globaltimer_ns() > deadline) return false;
+  return true;
 }
 
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* m) {

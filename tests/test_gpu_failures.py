@@ -75,11 +75,28 @@ def test_device_wait_that_runs_out_is_reported_and_the_context_recovers():
         kv.kvr_sync_status()
     assert e.value.code == -4
     kv.kvr_sync_status()   # cleared
-    # the context still computes the right thing
+    # with the status word set, every later kernel of the call leaves at entry
+    # (or at its next wait): a whole stack behind a wait that ran out costs
+    # about one wait limit, not one per CTA and launch
+    import time
     toks = list(range(300, 340))
     x = workloads.hidden_for_tokens(toks, shape.hidden, 5)
+    t0 = time.time()
+    kv.kvr_selftest_wait()
     kv.kvr_slot_match(toks)
-    out = kv.kvr_prefill_suffix(0, toks, x.cuda(), w)
+    kv.kvr_prefill_suffix(0, toks, x.cuda(), w)   # 40 rows: GEMM, attention, epilogues
+    kv.kvr_prefill_suffix(0, toks[:3], x[:3].cuda(), w)   # 3 rows: GEMV, split-KV
+    with pytest.raises(KvrError) as e:
+        kv.kvr_sync_status()
+    assert e.value.code == -4
+    assert time.time() - t0 < 5.0
+    kv.kvr_sync_status()   # cleared
+    # the context still computes the right thing (the skipped calls' rows are
+    # cut away first)
+    kv.kvr_slot_truncate(0, 0)
+    s, reused = kv.kvr_slot_match(toks)
+    assert reused == 0
+    out = kv.kvr_prefill_suffix(s, toks, x.cuda(), w)
     kv.kvr_sync_status()
     dims = oracle_dims(shape)
     W = [oracle_weights(shape, lw) for lw in lws]
