@@ -11,11 +11,17 @@ cut back, prefill) and no state is reset between steps.
 value       = suffix rows/s over the timed steps (device time, inputs resident).
 e2e         = the same through the public API with pinned host buffers: the
               step's hidden rows copied in, the output copied back.
-roofline    = the projection kernels (the dominant class) against the measured
-              bf16 tensor peak; attended-KV GB/s of the attention kernels is
-              reported beside it.
+roofline    = the projection kernels (the dominant class, each launch timed by
+              its own event pair) against the measured burst bf16 tensor peak;
+              attended-KV GB/s of the attention kernels is reported beside it,
+              and the whole step's causal flops against the same peak.
+verify      = the m <= 16 half of the metric in the same run: a speculative
+              verify of m = 1 and m = 8 rows on the dense 9B-class shape over a
+              4096-token slot, ms per call and the fraction of measured HBM
+              bandwidth its algorithmic bytes reach.
 cpu_baseline= the oracle (float64 numpy) on a bounded sample of the same
-              workload: one layer, the 254 suffix rows, over a 1668-row prefix.
+              workload: one layer, the 254 suffix rows, over a 1668-row prefix,
+              extrapolated to the 28-layer stack.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl kvr|reference]
 For N > 1, launch under torch.distributed.run: each rank runs an independent
@@ -150,6 +156,13 @@ class ClockSampler:
 FORMAT_LABEL = {"int4": "int4-g32", "q4k": "K-quant 4-bit superblocks"}
 
 
+def turn9_config(world, fmt="int4"):
+    return {"workload": f"turn-9 suffix prefill: Qwen2.5-7B-shaped 28-layer {FORMAT_LABEL[fmt]} "
+                        "stack, 1922-token prompt, 1668 cached, 254 suffix rows, 4 slots x 16384",
+            "global_batch": M_ROWS * world, "seq_len": PROMPT, "parallelism": f"replicas{world}",
+            "l2": "inputs larger than L2: 3.67 GB of 4-bit weights streamed per step"}
+
+
 def build_turn9(device, steps_total, layers=None, fmt="int4"):
     import dataclasses
     from prefix_reused_prefill_gb300 import Kvr, config_for_shape
@@ -261,11 +274,12 @@ def run_gpu(args, rank, world):
     proj_ms = cls_ms[0] / args.steps
     n_proj = cls_n[0] / args.steps
     achieved_tf = proj_flops / (proj_ms / 1e3) / 1e12
-    peak_tf = pk.get("bf16_tflops_sustained", pk.get("bf16_tflops"))
     attn_bytes = (P_CACHED + M_ROWS) * shape.n_kv_heads * shape.head_dim * 2 * 2 * L
     attn_ms = cls_ms[1] / args.steps
     attn_gbs = attn_bytes / (attn_ms / 1e3) / 1e9
     attn_flops = 4.0 * shape.head_dim * shape.n_q_heads * sum(P_CACHED + i + 1 for i in range(M_ROWS)) * L
+    # each projection launch is timed alone, inside ~0.1 s of steps at full clock: the burst peak
+    peak_tf = pk.get("bf16_tflops", FALLBACK["bf16_tflops"])
     weight_bytes = shape.params_per_layer() * L * 0.5625
     line = {
         "metric": "suffix-prefill rows/s",
@@ -280,10 +294,7 @@ def run_gpu(args, rank, world):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": f"turn-9 suffix prefill: Qwen2.5-7B-shaped 28-layer {FORMAT_LABEL[args.format]} "
-                               "stack, 1922-token prompt, 1668 cached, 254 suffix rows, 4 slots x 16384",
-                   "global_batch": M_ROWS * world, "seq_len": PROMPT, "parallelism": f"replicas{world}",
-                   "l2": "inputs larger than L2: 3.67 GB of 4-bit weights streamed per step"},
+        "config": turn9_config(world, args.format),
         "attended_kv_gbs": round(attn_gbs, 1),
         "attended_kv_frac_hbm": round(attn_gbs / pk["hbm_gbs"], 4),
         "attention_causal_tflops": round(attn_flops / (attn_ms / 1e3) / 1e12, 1),
@@ -294,10 +305,14 @@ def run_gpu(args, rank, world):
                      # DRAM bytes from an ncu capture of the int4 kernels
                      "traffic": None if args.layers or args.format != "int4" else round(PROJ_TRAFFIC_PER_LAYER * L),
                      "traffic_per": "step (the class's 112 launches)",
-                     "peak_kind": f"bf16 sustained ({pk_kind})",
+                     "peak_kind": f"bf16 burst ({pk_kind})",
                      "kernel": "projections (gemv_int4 / gemm_int4)",
                      "launches_per_step": n_proj, "ms_per_step": round(proj_ms, 4),
                      "weight_gbs": round(weight_bytes / (proj_ms / 1e3) / 1e9, 1)},
+        # the whole step (every launch, PDL overlap included): projection and causal attention flops
+        "step_tensor": {"tflops": round((proj_flops + attn_flops) / (ms_step / 1e3) / 1e12, 1),
+                        "frac": round((proj_flops + attn_flops) / (ms_step / 1e3) / 1e12 / peak_tf, 4),
+                        "peak": peak_tf, "peak_kind": f"bf16 burst ({pk_kind})"},
         "kernel_ms_per_step": {"projections": round(cls_ms[0] / args.steps, 4),
                                "attention": round(cls_ms[1] / args.steps, 4),
                                "epilogues": round(cls_ms[2] / args.steps, 4),
@@ -310,9 +325,58 @@ def run_gpu(args, rank, world):
     }
     if args.layers:
         line["config"]["workload"] += f" (REDUCED to {args.layers} layers: profiling case, not the bench line)"
+    del kv, w, xs_dev
+    torch.cuda.empty_cache()
+    if not args.no_verify and not args.layers:
+        line["verify"] = verify_summary(args, pk, pk_kind)
     if rank == 0 and not args.no_cpu:
         line["cpu_baseline"] = cpu_baseline(args.cpu_rows)
     return line, rank
+
+
+def verify_summary(args, pk, pk_kind, ms_rows=(1, 8)):
+    """The m <= 16 half of the metric in the bench run itself: kvr_verify of
+    m rows on the dense 9B-class shape (36 x (H 4096, 32/8 heads, F 12288),
+    4096 cached tokens), median of CUDA-event times per call with the slot cut
+    back after each (outside the timed call), clocks sampled meanwhile.
+    Algorithmic bytes per call: the weights once (0.5625 B per int4 weight),
+    the slot's K/V once per KV head, the appended rows."""
+    from prefix_reused_prefill_gb300 import Kvr, config_for_shape
+    device = torch.device("cuda", torch.cuda.current_device())
+    shape = workloads.SHAPES["dense9b" if args.format == "int4" else "dense9b_q4k"]
+    seed = workloads.config_seed(3)
+    tk = workloads.verify_tokens(seed)
+    P = len(tk["state"])
+    lws = workloads.stack_weights(shape, seed, device=device)
+    kv = Kvr(config_for_shape(shape, 1, P + 256, 256), device=device)
+    w = kv.weights(lws)
+    assert kv.kvr_slot_match(tk["state"][:1]) == (0, 0)
+    _prefill_state(kv, 0, tk["state"], shape, seed, w, device)
+    L = shape.n_layers
+    reps = max(args.steps, 20)
+    out = {}
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    for m in ms_rows:
+        draft = tk["draft"][:m]
+        x = workloads.hidden_for_tokens(draft, shape.hidden, seed).to(device)
+        o = torch.empty((m, shape.hidden), dtype=torch.bfloat16, device=device)
+        ms = _event_ms(lambda: kv.kvr_verify(0, draft, x, w, out=o), reps, args.warmup,
+                       after=lambda: kv.kvr_slot_truncate(0, P))
+        nbytes = (shape.params_per_layer() * 0.5625 * L
+                  + (P + m) * shape.n_kv_heads * shape.head_dim * 2 * 2 * L
+                  + m * shape.n_kv_heads * shape.head_dim * 4 * L)
+        gbs = nbytes / (ms / 1e3) / 1e9
+        out[f"m{m}"] = {"ms": round(ms, 4), "algorithmic_gb": round(nbytes / 1e9, 4), "gbs": round(gbs, 1),
+                        "frac_hbm": round(gbs / pk["hbm_gbs"], 4)}
+    out["clocks"] = clocks.stop()
+    kv.kvr_sync_status()
+    kv.close()
+    out.update({"workload": f"speculative verify: 36 x (H 4096, 32/8 heads, F 12288) {FORMAT_LABEL[args.format]}, "
+                            "4096 cached tokens, m = k+1 rows",
+                "peak_hbm_gbs": pk["hbm_gbs"], "peak_kind": pk_kind, "reps": reps,
+                "l2": "inputs larger than L2 (3.9 GB of weights and 0.6 GB of K/V per call)"})
+    return out
 
 
 # ---------------------------------------------------------------------------
@@ -658,13 +722,17 @@ def cpu_baseline(rows: int, min_seconds: float = 10.0):
     per_row_stack = dt / (n_eval * rows) * shape.n_layers
     cores = int(os.environ.get("OMP_NUM_THREADS", 0)) or os.cpu_count()
     return {"value": round(1.0 / per_row_stack, 3), "unit": "rows/s", "cores": cores,
-            "kind": "oracle",
+            "kind": "oracle", "extrapolated": f"one layer timed, scaled x{shape.n_layers} to the stack",
+            "layer_s": round(dt / n_eval, 3),
             "sample": f"{n_eval} layer evaluation(s) of {rows} suffix rows over 1668 cached rows "
-                      f"(float64 numpy, {dt:.1f} s), scaled to the 28-layer stack"}
+                      f"(float64 numpy, {dt:.1f} s), extrapolated to the 28-layer stack"}
 
 
 def run_reference(args, rank, world):
-    """--impl reference: the oracle as the reference arm (host cores)."""
+    """--impl reference: the oracle as the reference arm (host cores).  A timed
+    step is one layer of the turn-9 workload (254 suffix rows over the
+    1668-row prefix): ms_per_step is that measured time, and value is the
+    rate of the whole 28-layer stack extrapolated from it (named beside it)."""
     if rank != 0:
         return None, rank
     vals = []
@@ -675,13 +743,17 @@ def run_reference(args, rank, world):
         vals.append(cpu_baseline(args.cpu_rows, min_seconds=0.0))
     dt = time.perf_counter() - t0
     v = statistics.median(x["value"] for x in vals)
-    cb = dict(vals[0]); cb["value"] = v
+    layer_ms = 1000.0 * statistics.median(x["layer_s"] for x in vals)
+    n_layers = workloads.SHAPES["qwen7b"].n_layers
+    cb = dict(vals[0]); cb["value"] = v; cb["layer_s"] = round(layer_ms / 1e3, 3)
     line = {"impl": "reference", "metric": "suffix-prefill rows/s", "value": v, "unit": "rows/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": round(1000 * M_ROWS / v, 1), "higher_is_better": True, "scaling": "weak",
+            "ms_per_step": round(layer_ms, 1),
+            "step": "one layer of the stack (the timed unit); value extrapolates it to all layers",
+            "stack_ms_extrapolated": round(layer_ms * n_layers, 1),
+            "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": "turn-9 suffix prefill: Qwen2.5-7B-shaped 28-layer int4-g32 stack, "
-                                   "1922-token prompt, 1668 cached, 254 suffix rows, 4 slots x 16384"},
+            "config": turn9_config(world),
             "cpu_baseline": cb, "e2e": {"value": v, "unit": "rows/s", "h2d_bytes_per_step": 0,
                                         "d2h_bytes_per_step": 0},
             "wall_s": round(dt, 1)}
@@ -696,6 +768,7 @@ def main():
     ap.add_argument("--impl", default="kvr", choices=["kvr", "reference"])
     ap.add_argument("--cpu-rows", type=int, default=M_ROWS)
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-verify", action="store_true", help="turn9: skip the verify object")
     ap.add_argument("--workload", default="turn9", choices=["turn9", "verify", "priming", "crossover", "batch"],
                     help="turn9 is the bench line; the others print their own measurement line")
     ap.add_argument("--format", default="int4", choices=["int4", "q4k"],
