@@ -89,3 +89,92 @@ def test_rounding_points_against_the_elementwise_bound(block):
     assert gemm < 0.5                      # fp16 weights: inside the bound with margin
     assert bf16w > 0.6 and deferred > 0.6  # the rejected forms: near the bound already
     assert bf16w_rms > 2.5 * gemm_rms and deferred_rms > 2.5 * gemm_rms
+
+
+# ----------------------------------------------------------------------------
+# one whole 7B-width layer: the rounding points cascade
+# ----------------------------------------------------------------------------
+# Each bf16 rounding point (q/k/v, the attention output o, the normed rows,
+# the SwiGLU product z) turns a perturbation far below one bf16 step into
+# one-step flips with probability ~ perturbation / step, and every flip
+# perturbs the next stage: a float32 evaluation differs from float64 in 0.5 %
+# of o, ~1 % of the normed rows and ~15 % of z, and z feeds an 18944-input
+# down projection.  At this width the residual stream (rms ~3) therefore
+# carries errors of a few 1e-3 from float32 arithmetic alone, near an
+# absolute 1e-2 per element; the residual rows of the full-size parity tests
+# take the same bound with its absolute term in units of the row's rms.
+
+H7, F7, HQ7, HKV7, D7, P7, M7 = 3584, 18944, 28, 4, 128, 1668, 8
+
+
+@pytest.fixture(scope="module")
+def layer7b():
+    def mat(n, k, idx):
+        rng = np.random.Generator(np.random.PCG64([11, idx]))
+        w = torch.from_numpy(rng.standard_normal((n, k), dtype=np.float32) * np.float32(0.02))
+        m = workloads.make_int4(w)
+        return formats.dequant_int4(m.packed.numpy(), m.scales.numpy()).astype(np.float32)
+    W32 = {"wq": mat(HQ7 * D7, H7, 0), "wk": mat(HKV7 * D7, H7, 1), "wv": mat(HKV7 * D7, H7, 2),
+           "wo": mat(H7, HQ7 * D7, 3), "wg": mat(F7, H7, 4), "wu": mat(F7, H7, 5), "wd": mat(H7, F7, 6),
+           "norm_attn": workloads.norm_gain(H7, 11, 0, 0).float().numpy(),
+           "norm_ffn": workloads.norm_gain(H7, 11, 0, 1).float().numpy()}
+    kk, vv = workloads.random_kv(HKV7, P7, D7, 12)
+    x = workloads.bf16_to_f64(workloads.hidden_for_tokens(list(range(100, 100 + M7)), H7, 13))
+    return W32, workloads.bf16_to_f64(kk), workloads.bf16_to_f64(vv), x
+
+
+def _layer_f32(W32, Kp, Vp, x, rows, bf16_p):
+    """The decoder layer in float32 with the oracle's rounding points; with
+    bf16_p the softmax numerators enter the P V product rounded to bf16 (the
+    row sum keeps their float32 values), as the tensor-core attention does."""
+    G = HQ7 // HKV7
+    h = x.astype(np.float32)
+
+    def norm(v, g):
+        r = (1.0 / np.sqrt(np.mean(v * v, axis=-1, keepdims=True) + np.float32(1e-6))).astype(np.float32)
+        return _bf16_32(v * r * g)
+
+    a = norm(h, W32["norm_attn"])
+    k = (a @ W32["wk"].T).reshape(-1, HKV7, D7)
+    v = (a @ W32["wv"].T).reshape(-1, HKV7, D7)
+    K = np.zeros((HKV7, P7 + M7, D7), np.float32)
+    V = np.zeros_like(K)
+    K[:, :P7], V[:, :P7] = Kp, Vp
+    for i, r in enumerate(rows):
+        K[:, r.store] = _bf16_32(om.rope(k[i].astype(np.float64), r.pos, 1e6))
+        V[:, r.store] = _bf16_32(v[i])
+    q = (a @ W32["wq"].T).reshape(-1, HQ7, D7)
+    o = np.empty((M7, HQ7, D7), np.float32)
+    for i, r in enumerate(rows):
+        qq = _bf16_32(om.rope(q[i].astype(np.float64), r.pos, 1e6))
+        for hh in range(HQ7):
+            s = (K[hh // G, r.visible] @ qq[hh]) / np.float32(np.sqrt(D7))
+            e = np.exp(s - s.max()).astype(np.float32)
+            o[i, hh] = ((_bf16_32(e) if bf16_p else e) @ V[hh // G, r.visible]) / e.sum()
+    hs = h + _bf16_32(o).reshape(M7, -1) @ W32["wo"].T
+    b = norm(hs, W32["norm_ffn"])
+    g, u = b @ W32["wg"].T, b @ W32["wu"].T
+    z = _bf16_32(g / (np.float32(1) + np.exp(-g)) * u)
+    return (hs + z @ W32["wd"].T).astype(np.float64)
+
+
+def test_full_width_layer_cascade(layer7b):
+    W32, Kp, Vp, x = layer7b
+    W = {k: v.astype(np.float64) for k, v in W32.items()}
+    dims = om.Dims(H7, HQ7, HKV7, D7, F7, False, 1e6, 1e-6)
+    rows = om.plain_rows(P7, M7)
+    K = np.zeros((HKV7, P7 + M7, D7))
+    V = np.zeros_like(K)
+    K[:, :P7], V[:, :P7] = Kp, Vp
+    ref = om.layer_rows(dims, W, x, K, V, rows, list(range(M7)))
+    rms = np.sqrt(np.mean(ref ** 2, axis=1, keepdims=True))
+    plain, scaled = {}, {}
+    for bf16_p in (False, True):
+        err = np.abs(_layer_f32(W32, Kp, Vp, x, rows, bf16_p) - ref)
+        plain[bf16_p] = err / (1e-2 + 2e-2 * np.abs(ref))
+        scaled[bf16_p] = float((err / (1e-2 * rms + 2e-2 * np.abs(ref))).max())
+    print(f"exact P: plain {plain[False].max():.3f} scaled {scaled[False]:.3f}; "
+          f"bf16 P: plain {plain[True].max():.3f} ({int((plain[True] > 1).sum())} over) scaled {scaled[True]:.3f}")
+    assert plain[False].max() > 0.5        # float32 arithmetic alone uses most of an absolute 1e-2
+    assert (plain[True] > 1).sum() > 0     # with bf16 P (the tensor cores' operand) some elements exceed it
+    assert scaled[False] < 0.5 and scaled[True] < 0.8   # the rms-scaled form holds with margin
