@@ -137,6 +137,16 @@ typedef struct kvr_config {
  *   counted from the least significant bits.  A field holds code + 8 with
  *   code in [-8, 7].
  *   s* are fp16 [N][K/32] row-major; weight(n, k) = code(n, k) * s[n][k/32].
+ *   Any positive finite fp16 scale is accepted (no requirement on its
+ *   significant bits).  Precision of the arithmetic: calls with up to 32 rows
+ *   (the GEMV) use code * scale exactly (fp32 sums of code * x per group,
+ *   scaled in fp32).  Calls with more rows (the tcgen05 GEMM, fp16 operands)
+ *   keep the Q, K and V projections exact too (each weight as two fp16
+ *   terms, two MMAs) and round each O, gate, up and down weight once to fp16
+ *   (relative error at most 2^-12); their activations are the model's bf16
+ *   values, which fp16 holds exactly for magnitudes 2^-14 .. 65504, so an
+ *   activation above 65504 (not produced by these random-weight workloads,
+ *   and unusual for real ones) would overflow that path.
  *   (The field order lets one 32-bit shared-memory load give a tensor-core
  *   fragment its eight inputs of one group.)
  * KVR_WEIGHTS_Q4K (K-quant 4-bit superblocks; Tempo9 docs, "Models and
@@ -149,8 +159,9 @@ typedef struct kvr_config {
  *   field f at bits 6f: fields 0-7 the scales sc_j, fields 8-15 the mins mn_j
  *   of sub-block j (inputs 256s + 32j .. +31).
  *   weight(n, k) = d*sc_j*q - dmin*mn_j.  The small-m GEMV applies d*sc_j
- *   and dmin*mn_j to fp32 sums; the tcgen05 GEMM rounds each weight to the
- *   nearest bf16 once.
+ *   and dmin*mn_j to fp32 sums; the tcgen05 GEMM forms each weight in fp32
+ *   and, as for int4, keeps it as two fp16 terms for Q, K and V and rounds
+ *   it once to fp16 for the other projections.
  *   Every projection input width must be a multiple of 256 (as for int4).
  * norm_attn, norm_ffn: bf16 [H] RMSNorm gains (unused when attn_only).
  * Every pointer must be 16-byte aligned.

@@ -3,7 +3,11 @@
 // fp16: X [tokens][K] holds the activations' bf16 values (the model's rounding
 // point) in fp16, which represents them exactly, and each dequantised weight
 // code * scale is rounded once to fp16 (relative error at most 2^-12; the
-// product of a 4-bit code and an 11-bit fp16 scale can need 14 bits).
+// product of a 4-bit code and an 11-bit fp16 scale can need 14 bits).  The
+// exact variant (the QKV projection, whose q and k feed a softmax that can
+// amplify their errors) carries each weight as two fp16 terms, hi = fp16(w)
+// and lo = fp16(w - hi) (the remainder has at most 4 significant bits), and
+// issues both MMAs: twice the tensor work for exact weights.
 //
 // thinkspread, "The economics of speculative decoding" (cost model): each
 // weight streams once for all m rows.  At the m = 254 rows of goinfer's
@@ -52,13 +56,13 @@ constexpr int kThreads = 64 + 32 * kConvWarps;   // + producer warp + MMA warp
 // the other group, which the mbarrier phase parity could not tell apart).
 constexpr int kRawStages = 4;
 constexpr int kStages = 3;                       // activation stages (shared memory)
-constexpr int kAStages = 4;                      // A stages (tensor memory)
+constexpr int kAStages = 4;                      // A stages (tensor memory); 2 hi|lo stages when exact
 constexpr int kPrefetch = 2;                     // int4 stages prefetched into L2 ahead
 constexpr int kRawBytes = 128 * 64;              // 128 rows x 128 inputs of int4
 constexpr int kXAtom = 256 * 128;                // one 64-input atom of up to 256 tokens
 constexpr int kXBytes = 2 * kXAtom;
 constexpr int kTmemCols = 512;                   // accumulator 256 + 4 A stages x 64 columns
-constexpr uint32_t kACol = 256;                  // first A stage column; stage s at kACol + 64 s
+constexpr uint32_t kACol = 256;                  // first A stage column; stage s at kACol + 64 s (128 s exact)
 constexpr int kSmem = kRawStages * kRawBytes + kStages * kXBytes + 1024;
 
 __device__ __forceinline__ void tc_fence_before() {
@@ -158,6 +162,23 @@ __device__ __forceinline__ void q4k_weights_of_word(uint32_t w, float a, float c
   }
 }
 
+// Exact variant: 8 4-bit fields of one word -> 4 pairs of weights w = (128 + f)*a + c
+// formed in fp32 (exact for int4: a = scale, c = -136*scale gives code*scale)
+// and split into fp16 hi = fp16(w) and lo = fp16(w - hi) (pair i: fields i, i+4).
+__device__ __forceinline__ void hilo_weights_of_word(uint32_t w, float a, float c, uint32_t hi[4], uint32_t lo[4]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint32_t v;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(v) : "r"(w >> (4 * i)), "r"(0x000F000Fu), "r"(0x43004300u));
+    const float wl = fmaf(__uint_as_float(v << 16), a, c), wh = fmaf(__uint_as_float(v & 0xFFFF0000u), a, c);
+    __half2 h = __floats2half2_rn(wl, wh);
+    const float2 f = __half22float2(h);
+    __half2 l = __floats2half2_rn(wl - f.x, wh - f.y);
+    hi[i] = *reinterpret_cast<uint32_t*>(&h);
+    lo[i] = *reinterpret_cast<uint32_t*>(&l);
+  }
+}
+
 __device__ __forceinline__ uint32_t q4k_field6(const uint4& r, int f) {
   const int p = 6 * f, word = p >> 5, off = p & 31;
   const uint32_t lo = word == 0 ? r.y : (word == 1 ? r.z : r.w);
@@ -165,7 +186,10 @@ __device__ __forceinline__ uint32_t q4k_field6(const uint4& r, int f) {
   return (off > 26 && word < 2 ? __funnelshift_r(lo, hi, off) : lo >> off) & 63u;
 }
 
+template <bool kExact>
 __global__ void __launch_bounds__(kThreads, 1) gemm_int4_tc_kernel(const __grid_constant__ GemmParams p) {
+  constexpr int kAS = kExact ? 2 : kAStages;            // A stages in flight
+  constexpr uint32_t kAW = kExact ? 128u : 64u;         // TMEM columns per A stage (hi, then lo)
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t raw_full[kRawStages], raw_empty[kRawStages];
   __shared__ __align__(8) uint64_t a_full[kAStages], a_empty[kAStages];
@@ -200,7 +224,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_int4_tc_kernel(const __grid_
       dev::mbar_init(dev::smem_u32(&raw_full[i]), 1);
       dev::mbar_init(dev::smem_u32(&raw_empty[i]), kGroupWarps);
     }
-    for (int i = 0; i < kAStages; ++i) {
+    for (int i = 0; i < kAS; ++i) {
       dev::mbar_init(dev::smem_u32(&a_full[i]), kGroupWarps);
       dev::mbar_init(dev::smem_u32(&a_empty[i]), 1);
     }
@@ -306,21 +330,23 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_int4_tc_kernel(const __grid_
       const uint32_t idesc = idesc_f16(128, p.n_tok);
       bool ok = true;
       for (int i = 0; i < nkc; ++i) {
-        const int xs = i % kStages, as = i % kAStages;
-        if (!dev::mbar_wait(dev::smem_u32(&a_full[as]), (i / kAStages) & 1, p.status) ||
+        const int xs = i % kStages, as = i % kAS;
+        if (!dev::mbar_wait(dev::smem_u32(&a_full[as]), (i / kAS) & 1, p.status) ||
             !dev::mbar_wait(dev::smem_u32(&x_full[xs]), (i / kStages) & 1, p.status) || *abort_v) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t ta = tmem + kACol + 64u * (uint32_t)as;
+        const uint32_t ta = tmem + kACol + kAW * (uint32_t)as;
 #pragma unroll
         for (int atom = 0; atom < 2; ++atom) {
           const uint64_t bd = sw128_desc(x_base + xs * kXBytes + atom * kXAtom);
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
+          for (int kk = 0; kk < 4; ++kk) {
             mma_f16_ta(tmem, ta + 32u * atom + 8u * kk, bd + 2 * kk, idesc,
                        (i > 0 || atom > 0 || kk > 0) ? 1u : 0u);
+            if (kExact) mma_f16_ta(tmem, ta + 64u + 32u * atom + 8u * kk, bd + 2 * kk, idesc, 1u);
+          }
         }
         mma_commit(dev::smem_u32(&a_empty[as]));
         mma_commit(dev::smem_u32(&x_empty[xs]));
@@ -346,7 +372,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_int4_tc_kernel(const __grid_
     const uint32_t tlane = (uint32_t)(32 * q) << 16;
     bool ok = true;
     for (int i = grp; i < nkc; i += kConvGroups) {
-      const int rs = i % kRawStages, as = i % kAStages;
+      const int rs = i % kRawStages, as = i % kAS;
       // scales of groups 4*(kc0+i) + 2*hq and +1 (one aligned 32-bit load), or
       // the K-quant record of superblock (kc0+i)/2 (sub-blocks 4*((kc0+i)&1) + 2*hq, +1)
       uint32_t scw = 0u;
@@ -357,8 +383,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_int4_tc_kernel(const __grid_
         scw = srow_ok ? __ldg(sptr + 2 * (kc0 + i) + hq) : 0u;
       }
       ok = dev::mbar_wait(dev::smem_u32(&raw_full[rs]), (i / kRawStages) & 1, p.status) && !*abort_v;
-      if (ok && i >= kAStages)
-        ok = dev::mbar_wait(dev::smem_u32(&a_empty[as]), ((i / kAStages) - 1) & 1, p.status) && !*abort_v;
+      if (ok && i >= kAS)
+        ok = dev::mbar_wait(dev::smem_u32(&a_empty[as]), ((i / kAS) - 1) & 1, p.status) && !*abort_v;
       if (!__all_sync(0xffffffffu, ok)) {
         ok = false;
         break;
@@ -367,54 +393,89 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_int4_tc_kernel(const __grid_
       const uint32_t sw = (uint32_t)((t >> 1) & 3);  // 64-byte swizzle of this row
       const uint4 w0 = dev::lds128(rb + (((uint32_t)(2 * hq) ^ sw) << 4));
       const uint4 w1 = dev::lds128(rb + (((uint32_t)(2 * hq + 1) ^ sw) << 4));
-      uint32_t outv[32];   // 64 fp16 weights of this row, k order, two per column
-      if (p.fmt == kFmtQ4K) {
+      const uint32_t abase = tmem + tlane + kACol + kAW * (uint32_t)as + 32u * (uint32_t)hq;
+      if constexpr (kExact) {
+        // hi and lo of the 64 weights of this row (k order, two per column)
+        uint32_t hi[32], lo[32];
         const float d = __half2float(__ushort_as_half((unsigned short)(rec.x & 0xFFFFu)));
         const float dmin = __half2float(__ushort_as_half((unsigned short)(rec.x >> 16)));
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           const uint4 wv = h ? w1 : w0;
-          const int j = 4 * ((kc0 + i) & 1) + 2 * hq + h;   // sub-block of the superblock
-          const float a = d * (float)q4k_field6(rec, j);
-          const float c = -fmaf(128.f, a, dmin * (float)q4k_field6(rec, 8 + j));
-          uint32_t c0[4], c1[4], c2[4], c3[4];
-          q4k_weights_of_word(wv.x, a, c, c0);
-          q4k_weights_of_word(wv.y, a, c, c1);
-          q4k_weights_of_word(wv.z, a, c, c2);
-          q4k_weights_of_word(wv.w, a, c, c3);
+          float a, c;
+          if (p.fmt == kFmtQ4K) {
+            const int j = 4 * ((kc0 + i) & 1) + 2 * hq + h;
+            a = d * (float)q4k_field6(rec, j);
+            c = -fmaf(128.f, a, dmin * (float)q4k_field6(rec, 8 + j));
+          } else {
+            a = __half2float(__ushort_as_half((uint16_t)(h ? (scw >> 16) : (scw & 0xFFFFu))));
+            c = -136.f * a;
+          }
+          uint32_t h4[4][4], l4[4][4];
+          hilo_weights_of_word(wv.x, a, c, h4[0], l4[0]);
+          hilo_weights_of_word(wv.y, a, c, h4[1], l4[1]);
+          hilo_weights_of_word(wv.z, a, c, h4[2], l4[2]);
+          hilo_weights_of_word(wv.w, a, c, h4[3], l4[3]);
 #pragma unroll
+          for (int jj = 0; jj < 4; ++jj)
+#pragma unroll
+            for (int wi = 0; wi < 4; ++wi) {
+              hi[16 * h + 4 * jj + wi] = h4[wi][jj];
+              lo[16 * h + 4 * jj + wi] = l4[wi][jj];
+            }
+        }
+        tmem_st32(abase, hi);
+        tmem_st32(abase + 64u, lo);
+      } else {
+        uint32_t outv[32];   // 64 fp16 weights of this row, k order, two per column
+        if (p.fmt == kFmtQ4K) {
+          const float d = __half2float(__ushort_as_half((unsigned short)(rec.x & 0xFFFFu)));
+          const float dmin = __half2float(__ushort_as_half((unsigned short)(rec.x >> 16)));
+  #pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const uint4 wv = h ? w1 : w0;
+            const int j = 4 * ((kc0 + i) & 1) + 2 * hq + h;   // sub-block of the superblock
+            const float a = d * (float)q4k_field6(rec, j);
+            const float c = -fmaf(128.f, a, dmin * (float)q4k_field6(rec, 8 + j));
+            uint32_t c0[4], c1[4], c2[4], c3[4];
+            q4k_weights_of_word(wv.x, a, c, c0);
+            q4k_weights_of_word(wv.y, a, c, c1);
+            q4k_weights_of_word(wv.z, a, c, c2);
+            q4k_weights_of_word(wv.w, a, c, c3);
+  #pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+              outv[16 * h + 4 * jj + 0] = c0[jj];
+              outv[16 * h + 4 * jj + 1] = c1[jj];
+              outv[16 * h + 4 * jj + 2] = c2[jj];
+              outv[16 * h + 4 * jj + 3] = c3[jj];
+            }
+          }
+        } else {
+  #pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const uint4 wv = h ? w1 : w0;
+          const uint16_t sbits = (uint16_t)(h ? (scw >> 16) : (scw & 0xFFFFu));
+          const __half2 s2 = __half2half2(__ushort_as_half(sbits));
+          __half2 c0[4], c1[4], c2[4], c3[4];
+          codes_of_word(wv.x, c0);
+          codes_of_word(wv.y, c1);
+          codes_of_word(wv.z, c2);
+          codes_of_word(wv.w, c3);
+  #pragma unroll
           for (int jj = 0; jj < 4; ++jj) {
-            outv[16 * h + 4 * jj + 0] = c0[jj];
-            outv[16 * h + 4 * jj + 1] = c1[jj];
-            outv[16 * h + 4 * jj + 2] = c2[jj];
-            outv[16 * h + 4 * jj + 3] = c3[jj];
+            // inputs 8*jj .. 8*jj+7 of this 32-input group: words 0..3 give pairs (2w, 2w+1)
+            // code * scale: the exact product rounded once to fp16
+            __half2 v0 = __hmul2(c0[jj], s2), v1 = __hmul2(c1[jj], s2);
+            __half2 v2 = __hmul2(c2[jj], s2), v3 = __hmul2(c3[jj], s2);
+            outv[16 * h + 4 * jj + 0] = *reinterpret_cast<uint32_t*>(&v0);
+            outv[16 * h + 4 * jj + 1] = *reinterpret_cast<uint32_t*>(&v1);
+            outv[16 * h + 4 * jj + 2] = *reinterpret_cast<uint32_t*>(&v2);
+            outv[16 * h + 4 * jj + 3] = *reinterpret_cast<uint32_t*>(&v3);
           }
         }
-      } else {
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const uint4 wv = h ? w1 : w0;
-        const uint16_t sbits = (uint16_t)(h ? (scw >> 16) : (scw & 0xFFFFu));
-        const __half2 s2 = __half2half2(__ushort_as_half(sbits));
-        __half2 c0[4], c1[4], c2[4], c3[4];
-        codes_of_word(wv.x, c0);
-        codes_of_word(wv.y, c1);
-        codes_of_word(wv.z, c2);
-        codes_of_word(wv.w, c3);
-#pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-          // inputs 8*jj .. 8*jj+7 of this 32-input group: words 0..3 give pairs (2w, 2w+1)
-          // code * scale: the exact product rounded once to fp16
-          __half2 v0 = __hmul2(c0[jj], s2), v1 = __hmul2(c1[jj], s2);
-          __half2 v2 = __hmul2(c2[jj], s2), v3 = __hmul2(c3[jj], s2);
-          outv[16 * h + 4 * jj + 0] = *reinterpret_cast<uint32_t*>(&v0);
-          outv[16 * h + 4 * jj + 1] = *reinterpret_cast<uint32_t*>(&v1);
-          outv[16 * h + 4 * jj + 2] = *reinterpret_cast<uint32_t*>(&v2);
-          outv[16 * h + 4 * jj + 3] = *reinterpret_cast<uint32_t*>(&v3);
         }
+        tmem_st32(abase, outv);
       }
-      }
-      tmem_st32(tmem + tlane + kACol + 64u * (uint32_t)as + 32u * (uint32_t)hq, outv);
       asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       tc_fence_before();
       __syncwarp();
@@ -494,12 +555,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_int4_tc_kernel(const __grid_
 int gemm_tc_smem() { return kSmem; }
 
 cudaError_t gemm_tc_setup() {
-  return cudaFuncSetAttribute(gemm_int4_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  cudaError_t e = cudaFuncSetAttribute(gemm_int4_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(gemm_int4_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  return e;
 }
 
 cudaError_t launch_gemm_int4_tc(const GemmParams& p, int total_tiles, cudaStream_t st) {
   const dim3 grid(total_tiles, p.ksplit);
-  return launch_k(gemm_int4_tc_kernel, grid, kThreads, kSmem, st, p);
+  return p.exact ? launch_k(gemm_int4_tc_kernel<true>, grid, kThreads, kSmem, st, p)
+                 : launch_k(gemm_int4_tc_kernel<false>, grid, kThreads, kSmem, st, p);
 }
 
 }  // namespace kvr

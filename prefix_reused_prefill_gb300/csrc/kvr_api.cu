@@ -334,10 +334,12 @@ struct Seg {
 
 enum class Act { A, O, Z };
 
-// Large-m passes on the tcgen05 GEMM; swiglu = 1 fuses silu(gate)*up into its epilogue.
+// Large-m passes on the tcgen05 GEMM; swiglu = 1 fuses silu(gate)*up into its
+// epilogue; exact = 1 carries each weight as two fp16 terms (the QKV projection:
+// q and k feed the softmax, which can amplify a weight's fp16 rounding).
 template <class Epi>
 int project_gemm(kvr_ctx* c, cudaStream_t st, const Seg* segs, int nseg, const CUtensorMap* tmx,
-                 int K, int m, bool swiglu, Epi epi) {
+                 int K, int m, bool swiglu, bool exact, Epi epi) {
   GemmParams p;
   memset(&p, 0, sizeof p);
   p.K = K;
@@ -375,6 +377,7 @@ int project_gemm(kvr_ctx* c, cudaStream_t st, const Seg* segs, int nseg, const C
   p.ldo = col;
   p.plane = (long long)kGemmMaxTok * p.ldo;
   p.swiglu = swiglu ? 1 : 0;
+  p.exact = exact ? 1 : 0;
   p.fmt = weight_fmt(c->cfg);
   int ks = 1;
   if (!swiglu) {
@@ -529,11 +532,11 @@ int project_gemv_int4(kvr_ctx* c, cudaStream_t st, const Seg* segs, int nseg, co
 
 template <class Epi>
 int project(kvr_ctx* c, cudaStream_t st, const Seg* segs, int nseg, Act act, int K, int m, Epi epi,
-            const Fused& fz, bool swiglu = false) {
+            const Fused& fz, bool swiglu = false, bool exact = false) {
   const kvr_config& cfg = c->cfg;
   const CUtensorMap* tmx = act == Act::A ? c->tm_a : (act == Act::O ? c->tm_o : c->tm_z);
   if (packed4(cfg) && gemv_path(c, m)) return project_gemv_int4(c, st, segs, nseg, tmx, K, m, fz);
-  if (packed4(cfg)) return project_gemm(c, st, segs, nseg, tmx, K, m, swiglu, epi);
+  if (packed4(cfg)) return project_gemm(c, st, segs, nseg, tmx, K, m, swiglu, exact, epi);
   // bf16 weights: plain GEMV into partials, then the row-wise epilogue kernel
   GemvParams p;
   memset(&p, 0, sizeof p);
@@ -794,7 +797,7 @@ int run_stack(kvr_ctx* c, const RowMap& rows, const void* hidden,
                                                           int ldo, int c0, int mb) {
         return launch_epi_qkv(part, plane, ks, ldo, c0, mb, rows, Hq, Hkv, d, c->rope, c->q, arena,
                               koff, voff, sstride, k.capacity, st);
-      }, fz);
+      }, fz, /*swiglu=*/false, /*exact=*/true);
       if (rc) return rc;
     }
     int rc = KVR_OK;

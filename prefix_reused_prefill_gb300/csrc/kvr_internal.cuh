@@ -169,6 +169,7 @@ struct GemmParams {
   int t0;           // first token of this pass
   int swiglu;       // 1: write z = silu(gate) * up; 0: write fp32 partial sums
   int fmt;          // WeightFmt (scales: fp16 group scales or K-quant records)
+  int exact;        // weights as two fp16 terms (hi + lo, two MMAs): exact code * scale
   int ldo;
   int F;
   long long plane;

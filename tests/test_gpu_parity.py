@@ -201,7 +201,7 @@ def test_five_bit_scales_named_case():
     """The named extra input case: scales with at most 5 significant bits, where
     every code*scale is exactly a bf16 (and fp16) number, through the GEMV
     (m = 3) and the tcgen05 GEMM (m = 40)."""
-    shape, kv, w, W, _ = make("small", 1, 256, 64, scales="5bit")
+    shape, kv, w, W, _ = make("small", 1, 256, 128, scales="5bit")
     dims = oracle_dims(shape)
     toks = list(range(4000, 4000 + 120))
     x = hidden(toks, shape)
