@@ -101,7 +101,8 @@ int attn_nsplit(int Hkv, int R, int kend_max, int target) {
 }
 
 struct ScratchLayout {
-  size_t status, counters, prompt, slot_len, match_out, rope, h, a, q, o, z, part, opart, ml, best, next, total;
+  size_t status, counters, prompt, slot_len, match_out, rope, h, a, q, o, z, part, opart, ml, best, next;
+  size_t pass_layers, pass_done, pass_ss, total;
   size_t part_floats, opart_floats, ml_count;
 };
 
@@ -145,6 +146,11 @@ ScratchLayout scratch_layout(const kvr_config* c) {
   L.ml = take(L.ml_count * 8);
   L.best = take((size_t)kVerifyMaxRows * head_tiles * 8);
   L.next = take((size_t)kVerifyMaxRows * 4);
+  // the persistent small-m pass: per-layer weight descriptors, completion
+  // counters, per-tile sums of squares of its rows
+  L.pass_layers = take((size_t)c->n_layers * sizeof(PassLayer));
+  L.pass_done = take(((size_t)c->n_layers * kPassPhases + 8) * 4);
+  L.pass_ss = take((size_t)kPassRows * ((H + kGemvRows - 1) / kGemvRows) * 4);
   L.total = off;
   return L;
 }
@@ -196,6 +202,15 @@ struct kvr_ctx {
   // the call's projections run on the tcgen05 GEMM, whose operands are fp16:
   // a, o and z then hold their bf16-rounded values in fp16
   bool act16 = false;
+  // the persistent small-m pass: device layer table (and the host copy last
+  // uploaded, pinned), completion counters and this context's call count
+  PassLayer* pass_layers = nullptr;
+  PassLayer* pass_host = nullptr;
+  bool pass_uploaded = false;
+  int* pass_done = nullptr;
+  float* pass_ss = nullptr;
+  unsigned pass_epoch = 0;
+  bool use_pass = true;     // KVR_PASS=0 keeps small m on the per-step launches
   float* part = nullptr;
   float* opart = nullptr;
   float2* ml = nullptr;
@@ -747,12 +762,153 @@ int attention_batch(kvr_ctx* c, cudaStream_t st, int layer, const RowMap& rows, 
   return KVR_OK;
 }
 
+// ---------------------------------------------------------------------------
+// the persistent small-m pass
+// ---------------------------------------------------------------------------
+// It serves a call with int4 group-32 weights, whole decoder layers, one slot,
+// up to kPassRows rows (and G * rows <= kPassMaxAttnRows) and head_dim 128.
+bool pass_fits(const kvr_ctx* c, const RowMap& rows) {
+  const kvr_config& k = c->cfg;
+  return c->use_pass && !c->force_gemv && !c->force_gemm && pass_ctas() > 0 &&
+         k.weight_format == KVR_WEIGHTS_INT4_G32 && !k.attn_only && !rows.batch && rows.m <= kPassRows &&
+         (k.n_q_heads / k.n_kv_heads) * rows.m <= kPassMaxAttnRows && k.head_dim == 128 &&
+         k.hidden % kGemvRows == 0 && k.n_kv_heads <= pass_ctas();
+}
+
+// contributors of the most shared tile, and whether every CTA touches at most
+// kMaxOwnTiles tiles, for `tiles` tiles of `ks` units over `ctas` CTAs
+bool pass_split(int tiles, int ks, int ctas, int* maxc) {
+  const long long units = (long long)tiles * ks;
+  auto owner = [&](long long u) { return (int)(((u + 1) * ctas - 1) / units); };
+  int mc = 1;
+  for (int t = 0; t < tiles; ++t) mc = std::max(mc, owner((long long)t * ks + ks - 1) - owner((long long)t * ks) + 1);
+  for (int b = 0; b < ctas; ++b) {
+    const long long u0 = b * units / ctas, u1 = (b + 1) * units / ctas;
+    if (u1 > u0 && (u1 - 1) / ks - u0 / ks + 1 > 16) return false;
+  }
+  *maxc = mc;
+  return true;
+}
+
+int run_pass(kvr_ctx* c, const RowMap& rows, const void* hidden, const kvr_layer_weights* w, void* out,
+             cudaStream_t st, const __nv_bfloat16* head_gain) {
+  const kvr_config& k = c->cfg;
+  const int L = k.n_layers, H = k.hidden, F = k.ffn, d = k.head_dim;
+  const int Hq = k.n_q_heads, Hkv = k.n_kv_heads, m = rows.m;
+  const int ctas = pass_ctas();
+  // per-layer weight descriptors (the cached tensor maps), uploaded when they change
+  std::vector<PassLayer> tab(L);
+  for (int l = 0; l < L; ++l) {
+    const kvr_layer_weights& W = w[l];
+    const void* ws[7] = {W.wq, W.wk, W.wv, W.wo, W.wg, W.wu, W.wd};
+    const void* ss[7] = {W.sq, W.sk, W.sv, W.so, W.sg, W.su, W.sd};
+    const int N[7] = {Hq * d, Hkv * d, Hkv * d, H, F, F, H};
+    const int K[7] = {H, H, H, Hq * d, H, H, F};
+    PassLayer& T = tab[l];
+    memset(&T, 0, sizeof T);
+    for (int i = 0; i < 7; ++i) {
+      const WMap* wm = weight_map(c, ws[i], ss[i], N[i], K[i], (i == 4 || i == 5) ? 64 : kGemvRows);
+      if (!wm) return fail(c, KVR_ERR_CUDA, "cuTensorMapEncodeTiled failed for a weight matrix");
+      T.tw[i] = wm->w;
+      T.ts[i] = wm->s;
+    }
+    T.norm_attn = static_cast<const __nv_bfloat16*>(W.norm_attn);
+    T.norm_ffn = static_cast<const __nv_bfloat16*>(W.norm_ffn);
+  }
+  const size_t tab_bytes = (size_t)L * sizeof(PassLayer);
+  cudaError_t e = cudaSuccess;
+  if (!c->pass_uploaded || memcmp(c->pass_host, tab.data(), tab_bytes) != 0) {
+    // the pinned copy may still feed an earlier upload
+    e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_fail(c, e, "pass table upload");
+    memcpy(c->pass_host, tab.data(), tab_bytes);
+    e = cudaMemcpyAsync(c->pass_layers, c->pass_host, tab_bytes, cudaMemcpyHostToDevice, st);
+    if (e != cudaSuccess) return cuda_fail(c, e, "pass table upload");
+    c->pass_uploaded = true;
+  }
+  PassParams p;
+  memset(&p, 0, sizeof p);
+  p.layers = c->pass_layers;
+  p.L = L; p.H = H; p.F = F; p.Hq = Hq; p.Hkv = Hkv; p.d = d; p.G = Hq / Hkv; p.cap = k.capacity;
+  p.m = m;
+  p.rows = rows;
+  p.slot = rows.slot[0];
+  p.tkv = c->tm_kv;
+  p.tvt = c->tm_vt;
+  p.arena = reinterpret_cast<__nv_bfloat16*>(c->arena);
+  p.kv_slot = kv_offset(c, rows.slot[0], 0, 0);
+  p.kbase0 = k_row(c, rows.slot[0], 0);
+  p.vtbase0 = vt_row(c, rows.slot[0], 0);
+  p.ctas = ctas;
+  const int ksH = H / kGemvKStep, ksQ = Hq * d / kGemvKStep, ksF = F / kGemvKStep;
+  const int tq = (Hq * d + kGemvRows - 1) / kGemvRows + 2 * ((Hkv * d + kGemvRows - 1) / kGemvRows);
+  const int th = (H + kGemvRows - 1) / kGemvRows, tgu = (F + 63) / 64;
+  const int tiles[kPassPhases] = {tq, 0, th, tgu, th};
+  const int ks[kPassPhases] = {ksH, 0, ksQ, ksH, ksF};
+  for (int ph = 0; ph < kPassPhases; ++ph) {
+    if (ph == 1) continue;
+    if (tiles[ph] > kCounters || !pass_split(tiles[ph], ks[ph], ctas, &p.maxc[ph]) ||
+        (size_t)tiles[ph] * p.maxc[ph] * kGemvMaxCols * kGemvRows > c->sl.part_floats)
+      return fail(c, KVR_ERR_UNSUPPORTED, "no split of the small-m pass fits its buffers");
+  }
+  p.nb = (rows.P + m + kAttnKeys - 1) / kAttnKeys;
+  p.nsplit = std::max(1, std::min(std::min(ctas / Hkv, p.nb), kMaxSplits));   // the merge holds 64
+  while (p.nsplit > 1 && ((size_t)Hkv * p.nsplit * kPassMaxAttnRows * d > c->sl.opart_floats ||
+                          (size_t)Hkv * p.nsplit * kPassMaxAttnRows > c->sl.ml_count))
+    --p.nsplit;
+  if ((size_t)Hkv * p.nsplit * kPassMaxAttnRows * d > c->sl.opart_floats)
+    return fail(c, KVR_ERR_UNSUPPORTED, "attention partials of the small-m pass do not fit");
+  p.hidden = static_cast<const __nv_bfloat16*>(hidden);
+  p.h = c->h;
+  p.ss = c->pass_ss;
+  p.nss = H / kGemvRows;
+  p.rope = c->rope;
+  p.q = c->q;
+  p.o = c->o;
+  p.z = c->z;
+  p.part = c->part;
+  p.opart = c->opart;
+  p.ml = c->ml;
+  p.tile_cnt = c->counters;
+  p.head_cnt = c->counters + kCounters;
+  p.done = c->pass_done;
+  // completion counters grow by one call's count per call; restart them
+  // before the products could overflow
+  if (c->pass_epoch >= (1u << 20)) {
+    e = cudaMemsetAsync(c->pass_done, 0, ((size_t)L * kPassPhases + 8) * 4, st);
+    if (e != cudaSuccess) return cuda_fail(c, e, "pass counter reset");
+    c->pass_epoch = 0;
+  }
+  p.epoch = ++c->pass_epoch;
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.head_gain = head_gain;
+  p.a_head = c->a;
+  p.trace = c->trace;
+  p.trace_rows = k.max_rows;
+  p.eps = k.rms_eps;
+  p.scale_log2 = 1.4426950408889634f / sqrtf((float)d);
+  p.status = c->status;
+  c->act16 = false;
+  {
+    Timed t(c, kEpi, st);
+    e = launch_rope_table(rows, d, k.rope_theta, c->rope, st);
+  }
+  if (e != cudaSuccess) return cuda_fail(c, e, "rope table launch");
+  {
+    Timed t(c, kProj, st);
+    e = launch_pass(p, m <= 8 ? 1 : 2, st);
+  }
+  if (e != cudaSuccess) return cuda_fail(c, e, "small-m pass launch");
+  return KVR_OK;
+}
+
 // The layer stack for the rows of one call.
 // out (bf16 [m][hidden]) may be null; head_gain: RMSNorm the last layer's rows
 // with it into c->a (the output head's input)
 int run_stack(kvr_ctx* c, const RowMap& rows, const void* hidden,
               const kvr_layer_weights* w, void* out, cudaStream_t st,
               const __nv_bfloat16* head_gain = nullptr) {
+  if (pass_fits(c, rows)) return run_pass(c, rows, hidden, w, out, st, head_gain);
   const kvr_config& k = c->cfg;
   const int m = rows.m, H = k.hidden, d = k.head_dim;
   const int Hq = k.n_q_heads, Hkv = k.n_kv_heads, F = k.ffn;
@@ -1217,6 +1373,8 @@ int kvr_ctx_create(const kvr_config* cfg, void* kv_arena, size_t arena_bytes, vo
   c->attn_combine = ac && ac[0] == '1';
   const char* as = getenv("KVR_ATTN_SPLITS");
   c->attn_splits = as ? atoi(as) : 0;
+  const char* ps = getenv("KVR_PASS");
+  c->use_pass = !(ps && ps[0] == '0');
   c->requested = cfg->n_slots;
   c->reuse = cfg->n_slots > 0;
   const int want = std::max(cfg->n_slots, 1);
@@ -1248,6 +1406,9 @@ int kvr_ctx_create(const kvr_config* cfg, void* kv_arena, size_t arena_bytes, vo
   c->ml = reinterpret_cast<float2*>(s + c->sl.ml);
   c->best = reinterpret_cast<float2*>(s + c->sl.best);
   c->next = reinterpret_cast<int32_t*>(s + c->sl.next);
+  c->pass_layers = reinterpret_cast<PassLayer*>(s + c->sl.pass_layers);
+  c->pass_done = reinterpret_cast<int*>(s + c->sl.pass_done);
+  c->pass_ss = reinterpret_cast<float*>(s + c->sl.pass_ss);
 
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -1256,6 +1417,12 @@ int kvr_ctx_create(const kvr_config* cfg, void* kv_arena, size_t arena_bytes, vo
   if (e == cudaSuccess) e = gemm_tc_setup();
   if (e == cudaSuccess) e = attn_setup();
   if (e == cudaSuccess) e = attn_tc_setup();
+  // the persistent pass is optional: without room for it, small m keeps the
+  // per-step launches
+  if (e == cudaSuccess && pass_setup() != cudaSuccess) {
+    (void)cudaGetLastError();
+    c->use_pass = false;
+  }
   if (e == cudaSuccess && !g_encode) {
     cudaDriverEntryPointQueryResult q;
     void* fn = nullptr;
@@ -1291,6 +1458,12 @@ int kvr_ctx_create(const kvr_config* cfg, void* kv_arena, size_t arena_bytes, vo
   // when a key block is partly visible; zero the arena once so they are finite.
   e = cudaMemset(c->status, 0, 64);
   if (e == cudaSuccess) e = cudaMemset(c->counters, 0, (kCounters + kAttnCounters) * 4);
+  if (e == cudaSuccess) e = cudaMemset(c->pass_done, 0, ((size_t)k.n_layers * kPassPhases + 8) * 4);
+  if (e == cudaSuccess && cudaHostAlloc(&c->pass_host, (size_t)k.n_layers * sizeof(PassLayer), cudaHostAllocDefault) != cudaSuccess) {
+    (void)cudaGetLastError();
+    c->pass_host = nullptr;
+    c->use_pass = false;
+  }
   if (e == cudaSuccess) e = cudaMemset(c->arena, 0, (size_t)c->granted * slot_kv_bytes(cfg));
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e != cudaSuccess) {
@@ -1322,6 +1495,7 @@ int kvr_ctx_destroy(kvr_ctx* c) {
   }
   for (auto e : c->free_events) cudaEventDestroy(e);
   if (c->host_match) cudaFreeHost(c->host_match);
+  if (c->pass_host) cudaFreeHost(c->pass_host);
   delete c;
   return KVR_OK;
 }
@@ -1578,6 +1752,9 @@ int kvr_sync_status(kvr_ctx* c, void* stream) {
     // a launch that gave up may have left arrival counters behind: clear
     // every one of them (GEMV tiles and split-KV merges) and the status word
     e = cudaMemsetAsync(c->counters, 0, (kCounters + kAttnCounters) * 4, st);
+    if (e == cudaSuccess)
+      e = cudaMemsetAsync(c->pass_done, 0, ((size_t)c->cfg.n_layers * kPassPhases + 8) * 4, st);
+    c->pass_epoch = 0;
     if (e == cudaSuccess) e = cudaMemsetAsync(c->status, 0, 4, st);
     if (e == cudaSuccess) e = cudaStreamSynchronize(st);
     if (e != cudaSuccess) return cuda_fail(c, e, "clearing the counters after a timeout");

@@ -218,6 +218,59 @@ struct AttnParams {
   AttnConv conv[KVR_MAX_BRANCHES];
 };
 
+// Persistent small-m pass: the whole stack for up to kPassRows rows in one
+// cooperative launch (k_pass.cu).
+constexpr int kPassRows = 16;       // rows of a call (two tensor-core n-tiles)
+constexpr int kPassMaxAttnRows = 64;   // G * rows: four 16-row attention tiles
+constexpr int kPassPhases = 5;      // QKV, attention, O, gate|up, down per layer
+
+// per-layer weight descriptors, in device memory (tensor maps 64-byte aligned)
+struct PassLayer {
+  CUtensorMap tw[7];   // int4 bytes of wq wk wv wo wg wu wd: 128-row boxes (wg, wu: 64-row boxes)
+  CUtensorMap ts[7];   // their fp16 scales, same row boxes
+  const __nv_bfloat16* norm_attn;
+  const __nv_bfloat16* norm_ffn;
+};
+static_assert(alignof(PassLayer) >= 64 && sizeof(PassLayer) % 64 == 0,
+              "every layer's tensor maps stay 64-byte aligned in the device table");
+
+struct PassParams {
+  const PassLayer* layers;
+  int L, H, F, Hq, Hkv, d, G, cap;
+  int m;                   // rows of the call
+  RowMap rows;             // one slot (batch == 0); branches allowed
+  int slot;
+  CUtensorMap tkv, tvt;    // the arena as the attention kernels see it
+  __nv_bfloat16* arena;
+  long long kv_slot;       // arena elements before (slot, layer 0, K)
+  int kbase0, vtbase0;     // [rows][d] / [rows][cap] view rows of (slot, layer 0)
+  int ctas;
+  int maxc[kPassPhases];   // partial slots per tile of each projection phase
+  int nsplit, nb;          // attention: key splits per KV head, 64-key blocks over [0, P + m)
+  const __nv_bfloat16* hidden;
+  float* h;                // [m][H] residual stream
+  float* ss;               // [m][nss] sum of h^2 per 128-column tile
+  int nss;
+  const float2* rope;      // (cos, sin) [m][d/2]
+  __nv_bfloat16* q;        // [Hkv][m][G][d]
+  __nv_bfloat16* o;        // [m][Hq*d]
+  __nv_bfloat16* z;        // [m][F]
+  float* part;             // projection partials [tiles][maxc][32][128]
+  float* opart;            // attention partials [Hkv*nsplit][64][d]
+  float2* ml;              // [Hkv*nsplit][64] (max in log2 units, sum)
+  int* tile_cnt;           // per-tile arrivals (zero between uses)
+  int* head_cnt;           // per-KV-head split arrivals (zero between uses)
+  int* done;               // [L*5 + 1] completion counters, growing by one call's count per call
+  unsigned epoch;          // this call: a counter is complete at epoch * its count
+  __nv_bfloat16* out;      // bf16 [m][H] (last layer), or null
+  const __nv_bfloat16* head_gain;  // output head's RMSNorm: a_head = bf16(RMSNorm(h) * gain), or null
+  __nv_bfloat16* a_head;
+  float* trace;            // [L + 1][trace_rows][H] layer inputs (float32), or null
+  int trace_rows;
+  float eps, scale_log2;
+  int* status;
+};
+
 // ----------------------------------------------------------------------------
 // launchers (each returns the error of its launch)
 // ----------------------------------------------------------------------------
@@ -272,6 +325,10 @@ cudaError_t launch_norm(const float* h, int m, int H, const __nv_bfloat16* gain,
 // (lowest row on ties), t < m
 // one device-side wait that runs out (the failure path, without a fault)
 cudaError_t launch_wait_probe(int* status, cudaStream_t st);
+// the persistent small-m pass (nt: tensor-core n-tiles of 8 rows, 1 or 2)
+cudaError_t launch_pass(const PassParams& p, int nt, cudaStream_t st);
+cudaError_t pass_setup();
+int pass_ctas();   // CTAs of the pass (one per SM), 0 before pass_setup
 cudaError_t launch_head_argmax(const float2* best, int tiles, int m, int32_t* out, cudaStream_t st);
 cudaError_t launch_epi_qkv(const float* part, long long plane, int ksplit, int ldo, int c0,
                            int mb, const RowMap& rows, int Hq, int Hkv, int d,
