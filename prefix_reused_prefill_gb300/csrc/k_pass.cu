@@ -122,13 +122,19 @@ __device__ __forceinline__ int rows_of(const Proj& j, int s) { return j.ph == kP
 __device__ __forceinline__ int mat_of(const Proj& j, int s) {
   return j.ph == kPhQKV ? s : (j.ph == kPhO ? 3 : (j.ph == kPhGU ? 4 + s : 6));
 }
+// A projection's units are split over its first min(ctas, units) CTAs, each
+// an equal run of at least one unit, so the CTAs that touch a tile are
+// consecutive and each contributes one partial.
+__device__ __forceinline__ int proj_ctas(int units, int ctas) { return units < ctas ? units : ctas; }
 // this CTA's units [u0, u1) of a projection with `units` units
 __device__ __forceinline__ void unit_range(int units, int ctas, int cta, int& u0, int& u1) {
-  u0 = (int)((long long)cta * units / ctas);
-  u1 = (int)((long long)(cta + 1) * units / ctas);
+  const int n = proj_ctas(units, ctas);
+  u0 = cta < n ? (int)((long long)cta * units / n) : units;
+  u1 = cta < n ? (int)((long long)(cta + 1) * units / n) : units;
 }
 __device__ __forceinline__ int owner_of(long long u, int units, int ctas) {
-  return (int)(((u + 1) * ctas - 1) / units);
+  const int n = proj_ctas(units, ctas);
+  return (int)(((u + 1) * n - 1) / units);
 }
 
 // ------------------------------------------------------------ attention items
@@ -164,16 +170,46 @@ __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
+// The first wait of a pass to give up records where in the status word:
+// bit 0 set, the wait site in bits 1-3, a site detail (the counter index or
+// the ring use) in bits 4-15 and the CTA in bits 16-30.
+__device__ __forceinline__ int site_code(int site, int detail) {
+  return kStatusTimeout | (site << 1) | ((detail & 0xFFF) << 4) | ((int)(blockIdx.x & 0x7FFF) << 16);
+}
+__device__ __forceinline__ void give_up(int* status, int* diag, int site, int detail, int seen) {
+  const int code = site_code(site, detail);
+  atomicCAS(status, 0, code);
+  if (diag && blockIdx.x < kPassMaxCtas) {
+    diag[2 * blockIdx.x] = code;
+    diag[2 * blockIdx.x + 1] = seen;
+  }
+}
+constexpr int kSiteProdCount = 1, kSiteConsCount = 2, kSiteProdRing = 3, kSiteConsRing = 4;
+
 // Wait (bounded) until *ctr reaches target (counters only grow within a call).
 // Returns false on a timeout or when another wait has given up.
-__device__ __forceinline__ bool wait_count(const int* ctr, int target, int* status) {
+__device__ __forceinline__ bool wait_count(const int* ctr, int target, int* status, int* diag, int site, int detail) {
   if (ld_acquire(ctr) - target >= 0) return true;
   const unsigned long long t0 = dev::globaltimer_ns();
   for (unsigned n = 0;; ++n) {
     if (ld_acquire(ctr) - target >= 0) return true;
     if ((n & 15u) == 15u && dev::status_set(status)) return false;
     if (dev::globaltimer_ns() - t0 > kWaitLimitNs) {
-      atomicExch(status, kStatusTimeout);
+      give_up(status, diag, site, detail, ld_acquire(ctr));
+      return false;
+    }
+  }
+}
+
+// An mbarrier phase wait of the pass: as dev::mbar_wait, with its site recorded
+__device__ __forceinline__ bool ring_wait(uint32_t bar, uint32_t parity, int* status, int* diag, int site, int detail) {
+  if (dev::mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = dev::globaltimer_ns();
+  for (unsigned n = 0;; ++n) {
+    if (dev::mbar_try_wait(bar, parity)) return true;
+    if ((n & 31u) == 31u && dev::status_set(status)) return false;
+    if (dev::globaltimer_ns() - t0 > kWaitLimitNs) {
+      give_up(status, diag, site, detail, (int)parity);
       return false;
     }
   }
@@ -235,7 +271,7 @@ __device__ void produce(const PassParams& p, Shared& sh, uint32_t ring) {
   auto next_stage = [&](uint32_t bytes) -> uint32_t {
     const int st = (int)(it % kStages);
     if (it >= (unsigned)kStages) {
-      if (!dev::mbar_wait(dev::smem_u32(&sh.empty[st]), ((it / kStages) - 1) & 1, p.status) ||
+      if (!ring_wait(dev::smem_u32(&sh.empty[st]), ((it / kStages) - 1) & 1, p.status, p.diag, kSiteProdRing, (int)it) ||
           *reinterpret_cast<volatile int*>(&sh.abort)) {
         ok = false;
         return 0;
@@ -257,7 +293,8 @@ __device__ void produce(const PassParams& p, Shared& sh, uint32_t ring) {
         for (int b = item.b0; b < item.b1 && ok; ++b) {
           if ((b + 1) * kAttnKeys > P && !waited) {
             // this block holds rows of this call: their K/V come from the QKV step
-            if (!wait_count(p.done + done_index(l, kPhQKV), (int)p.epoch * done_count(p, kPhQKV), p.status)) {
+            if (!wait_count(p.done + done_index(l, kPhQKV), (int)p.epoch * done_count(p, kPhQKV), p.status,
+                            p.diag, kSiteProdCount, done_index(l, kPhQKV))) {
               ok = false;
               break;
             }
@@ -337,7 +374,7 @@ struct Cons {
   // one thread waits for a counter; everyone learns the outcome at the barrier
   __device__ __forceinline__ bool wait_dep(int idx, int count) {
     if (tid == 0 && !abort_flag()) {
-      if (!wait_count(p.done + idx, (int)p.epoch * count, p.status)) abort_flag() = 1;
+      if (!wait_count(p.done + idx, (int)p.epoch * count, p.status, p.diag, kSiteConsCount, idx)) abort_flag() = 1;
     }
     ok = !cons_sync_any(abort_flag() != 0);
     return ok;
@@ -349,7 +386,7 @@ struct Cons {
   __device__ __forceinline__ uint32_t wait_use(unsigned u, bool& good) {
     const int st = (int)(u % kStages);
     const bool got = !abort_flag() &&
-                     dev::mbar_wait(dev::smem_u32(&sh.full[st]), (u / kStages) & 1, p.status);
+                     ring_wait(dev::smem_u32(&sh.full[st]), (u / kStages) & 1, p.status, p.diag, kSiteConsRing, (int)u);
     good = __all_sync(0xffffffffu, got);
     if (!good && lane == 0) abort_flag() = 1;
     return ring + st * kStage;

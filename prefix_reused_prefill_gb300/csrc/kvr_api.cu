@@ -102,7 +102,7 @@ int attn_nsplit(int Hkv, int R, int kend_max, int target) {
 
 struct ScratchLayout {
   size_t status, counters, prompt, slot_len, match_out, rope, h, a, q, o, z, part, opart, ml, best, next;
-  size_t pass_layers, pass_done, pass_ss, total;
+  size_t pass_layers, pass_done, pass_ss, pass_diag, total;
   size_t part_floats, opart_floats, ml_count;
 };
 
@@ -151,6 +151,7 @@ ScratchLayout scratch_layout(const kvr_config* c) {
   L.pass_layers = take((size_t)c->n_layers * sizeof(PassLayer));
   L.pass_done = take(((size_t)c->n_layers * kPassPhases + 8) * 4);
   L.pass_ss = take((size_t)kPassRows * ((H + kGemvRows - 1) / kGemvRows) * 4);
+  L.pass_diag = take((size_t)kPassMaxCtas * 2 * 4);
   L.total = off;
   return L;
 }
@@ -209,6 +210,7 @@ struct kvr_ctx {
   bool pass_uploaded = false;
   int* pass_done = nullptr;
   float* pass_ss = nullptr;
+  int* pass_diag = nullptr;   // [kPassMaxCtas][2] where the pass's waits gave up
   unsigned pass_epoch = 0;
   bool use_pass = true;     // KVR_PASS=0 keeps small m on the per-step launches
   float* part = nullptr;
@@ -776,9 +778,11 @@ bool pass_fits(const kvr_ctx* c, const RowMap& rows) {
 }
 
 // contributors of the most shared tile, and whether every CTA touches at most
-// kMaxOwnTiles tiles, for `tiles` tiles of `ks` units over `ctas` CTAs
+// 16 tiles, for `tiles` tiles of `ks` units over min(ctas, units) CTAs (the
+// split of k_pass.cu)
 bool pass_split(int tiles, int ks, int ctas, int* maxc) {
   const long long units = (long long)tiles * ks;
+  ctas = (int)std::min<long long>(ctas, units);
   auto owner = [&](long long u) { return (int)(((u + 1) * ctas - 1) / units); };
   int mc = 1;
   for (int t = 0; t < tiles; ++t) mc = std::max(mc, owner((long long)t * ks + ks - 1) - owner((long long)t * ks) + 1);
@@ -885,6 +889,7 @@ int run_pass(kvr_ctx* c, const RowMap& rows, const void* hidden, const kvr_layer
   p.a_head = c->a;
   p.trace = c->trace;
   p.trace_rows = k.max_rows;
+  p.diag = c->pass_diag;
   p.eps = k.rms_eps;
   p.scale_log2 = 1.4426950408889634f / sqrtf((float)d);
   p.status = c->status;
@@ -1409,6 +1414,7 @@ int kvr_ctx_create(const kvr_config* cfg, void* kv_arena, size_t arena_bytes, vo
   c->pass_layers = reinterpret_cast<PassLayer*>(s + c->sl.pass_layers);
   c->pass_done = reinterpret_cast<int*>(s + c->sl.pass_done);
   c->pass_ss = reinterpret_cast<float*>(s + c->sl.pass_ss);
+  c->pass_diag = reinterpret_cast<int*>(s + c->sl.pass_diag);
 
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -1459,6 +1465,7 @@ int kvr_ctx_create(const kvr_config* cfg, void* kv_arena, size_t arena_bytes, vo
   e = cudaMemset(c->status, 0, 64);
   if (e == cudaSuccess) e = cudaMemset(c->counters, 0, (kCounters + kAttnCounters) * 4);
   if (e == cudaSuccess) e = cudaMemset(c->pass_done, 0, ((size_t)k.n_layers * kPassPhases + 8) * 4);
+  if (e == cudaSuccess) e = cudaMemset(c->pass_diag, 0, (size_t)kPassMaxCtas * 2 * 4);
   if (e == cudaSuccess && cudaHostAlloc(&c->pass_host, (size_t)k.n_layers * sizeof(PassLayer), cudaHostAllocDefault) != cudaSuccess) {
     (void)cudaGetLastError();
     c->pass_host = nullptr;
@@ -1749,16 +1756,38 @@ int kvr_sync_status(kvr_ctx* c, void* stream) {
   if (e == cudaSuccess) e = cudaStreamSynchronize(st);
   if (e != cudaSuccess) return cuda_fail(c, e, "status readback");
   if (word) {
+    // where the small-m pass's waits gave up, if it ran: (site, detail, CTA)
+    // of the first few CTAs that recorded one
+    std::string where;
+    std::vector<int> diag((size_t)kPassMaxCtas * 2);
+    e = cudaMemcpyAsync(diag.data(), c->pass_diag, diag.size() * 4, cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_fail(c, e, "status detail readback");
+    int shown = 0, total = 0;
+    for (int b = 0; b < kPassMaxCtas; ++b) {
+      const int code = diag[2 * b];
+      if (!code) continue;
+      ++total;
+      if (shown < 6) {
+        char buf[96];
+        snprintf(buf, sizeof buf, "%s[cta %d site %d detail %d seen %d]", shown ? " " : "; pass waits: ",
+                 (code >> 16) & 0x7FFF, (code >> 1) & 7, (code >> 4) & 0xFFF, diag[2 * b + 1]);
+        where += buf;
+        ++shown;
+      }
+    }
+    if (total > shown) where += " ... (" + std::to_string(total) + " CTAs)";
     // a launch that gave up may have left arrival counters behind: clear
     // every one of them (GEMV tiles and split-KV merges) and the status word
     e = cudaMemsetAsync(c->counters, 0, (kCounters + kAttnCounters) * 4, st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(c->pass_diag, 0, (size_t)kPassMaxCtas * 2 * 4, st);
     if (e == cudaSuccess)
       e = cudaMemsetAsync(c->pass_done, 0, ((size_t)c->cfg.n_layers * kPassPhases + 8) * 4, st);
     c->pass_epoch = 0;
     if (e == cudaSuccess) e = cudaMemsetAsync(c->status, 0, 4, st);
     if (e == cudaSuccess) e = cudaStreamSynchronize(st);
     if (e != cudaSuccess) return cuda_fail(c, e, "clearing the counters after a timeout");
-    return fail(c, KVR_ERR_TIMEOUT, "a device-side wait gave up (status %d)", word);
+    return fail(c, KVR_ERR_TIMEOUT, "a device-side wait gave up (status %d)%s", word, where.c_str());
   }
   return KVR_OK;
 }

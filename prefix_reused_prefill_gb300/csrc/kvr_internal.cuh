@@ -223,6 +223,7 @@ struct AttnParams {
 constexpr int kPassRows = 16;       // rows of a call (two tensor-core n-tiles)
 constexpr int kPassMaxAttnRows = 64;   // G * rows: four 16-row attention tiles
 constexpr int kPassPhases = 5;      // QKV, attention, O, gate|up, down per layer
+constexpr int kPassMaxCtas = 512;   // per-CTA records of a wait that gave up
 
 // per-layer weight descriptors, in device memory (tensor maps 64-byte aligned)
 struct PassLayer {
@@ -267,6 +268,7 @@ struct PassParams {
   __nv_bfloat16* a_head;
   float* trace;            // [L + 1][trace_rows][H] layer inputs (float32), or null
   int trace_rows;
+  int* diag;               // [kPassMaxCtas][2]: a CTA's wait that gave up (code, value seen)
   float eps, scale_log2;
   int* status;
 };
