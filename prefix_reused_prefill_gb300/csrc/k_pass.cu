@@ -10,11 +10,15 @@
 // Separate launches per projection leave the weight stream idle at every
 // step boundary (a launch edge, the activations' first load, the split-K
 // tail, the slowest CTA).  Here each CTA keeps one ring of shared-memory
-// stages filled by one producer thread that walks the whole call's schedule
-// -- its share of every projection's (tile, 256-input step) units and its
-// attention item's 64-key blocks, layer after layer -- and never waits for a
-// result, only for a free stage.  The weights of the next steps therefore
-// stream while the consumers wait for the current step's inputs.
+// stages that a producer warp fills: it walks the whole call's schedule --
+// its share of every projection's (tile, 256-input step) units and its
+// attention item's 64-key blocks, layer after layer -- and issues the copy of
+// each use as soon as its stage is free.  The weights of the next steps
+// therefore stream while the consumers wait for the current step's inputs.
+// The producer is a warp of its own: copies issued from inside a consumer's
+// wait loop are issued late (that warp's other lanes sleep on the barrier,
+// and the issuing lane moves on before the last consumer frees a stage), and
+// the stream then runs at about 60% of the rate a free-running producer gets.
 //
 // Steps of a layer and what each waits for (counters in global memory that
 // grow by one call's count per call, read with acquire loads):
@@ -32,28 +36,29 @@
 // Each projection is split stream-K over all CTAs as in the GEMV kernel: a
 // CTA stores its partial tile, and the last contributor of a tile to arrive
 // adds the partials in contributor order (the result does not depend on
-// timing) and applies the epilogue.  Sixteen consumer warps share a unit:
-// eight row groups of 16 weight rows times two halves of the 256 inputs.
-// The activations of a unit are staged by the consumers (bf16, swizzled as
-// the GEMV's TMA tiles) one unit ahead of its weights.
+// timing) and applies the epilogue.  The eight consumer warps share a unit,
+// one 16-row group of the 128-row tile each, over all 256 inputs (nine warps
+// leave 224 registers a thread).  The activations of a unit are staged by the
+// consumers (bf16, swizzled as the GEMV's TMA tiles) one unit ahead of its
+// weights.
 //
 // Every wait is bounded (1 s) and reports through the status word; a CTA that
 // finds the word set stops, drains its copies and leaves.
-#include <cooperative_groups.h>
-
 #include "kvr_internal.cuh"
 
 namespace kvr {
 
 namespace {
 
-constexpr int kWarps = 16;                    // consumer warps
+constexpr int kWarps = 8;                     // consumer warps (one 16-row group of a tile each)
 constexpr int kCons = kWarps * 32;
-constexpr int kThreads = kCons + 32;          // + the producer warp
+constexpr int kThreads = kCons + 64;          // the producer warp and the L2 prefetch warp
+constexpr int kPfAhead = 16;                  // uses the L2 prefetch runs ahead of the copies
 constexpr int kStage = 18 * 1024;             // int4 tile 16 KB + scales 2 KB, or one K / V^T tile
-constexpr int kStages = 10;
-constexpr int kXBox = kPassRows * 128;        // one 64-input box of 16 activation rows
-constexpr int kXBytes = 4 * kXBox;            // the 256 inputs of one unit
+constexpr int kStages = 8;
+// activations of a projection step, staged for up to kXArea / (4 * 1 KB * NT)
+// units at a time: per unit four 64-input boxes of 8 * NT rows (GEMV layout)
+constexpr int kXArea = 64 * 1024;
 constexpr int kCtLd = kGemvRows + 4;          // tile buffer row stride (floats)
 constexpr int kCtBytes = kPassRows * kCtLd * 4;
 constexpr int kAttnD = 128;
@@ -63,7 +68,8 @@ constexpr int kMergeBytes = 8 * kMergeState * 4;
 // rows; three or four tiles (one warp each) keep only the query rows
 constexpr int kAttnWork = kMergeBytes + 2 * 16 * kAttnD * 2;
 static_assert(kPassMaxAttnRows * kAttnD * 2 <= kAttnWork, "query rows of four tiles fit");
-constexpr int kWork = (2 * kXBytes + kCtBytes > kAttnWork ? 2 * kXBytes + kCtBytes : kAttnWork);
+static_assert(kCtBytes <= kXArea, "the epilogue's tile buffer fits the staging area");
+constexpr int kWork = (kXArea > kAttnWork ? kXArea : kAttnWork);
 constexpr int kSmem = kStages * kStage + kWork + 1024;
 constexpr int kMaxOwn = 16;                   // tiles one CTA may finish per projection
 static_assert(kSmem <= 232448, "shared memory of one CTA");
@@ -170,6 +176,12 @@ __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
+// Polls of global words (the completion counters, the status word) are spaced
+// in time: thousands of threads reading one L2 line back to back slow every
+// other request that line's L2 slice serves, the weight copies included.
+constexpr unsigned long long kPollNs = 4000;
+constexpr unsigned kCountBackoffNs = 100;
+
 // The first wait of a pass to give up records where in the status word:
 // bit 0 set, the wait site in bits 1-3, a site detail (the counter index or
 // the ring use) in bits 4-15 and the CTA in bits 16-30.
@@ -184,48 +196,39 @@ __device__ __forceinline__ void give_up(int* status, int* diag, int site, int de
     diag[2 * blockIdx.x + 1] = seen;
   }
 }
-constexpr int kSiteProdCount = 1, kSiteConsCount = 2, kSiteProdRing = 3, kSiteConsRing = 4;
-
-// Wait (bounded) until *ctr reaches target (counters only grow within a call).
-// Returns false on a timeout or when another wait has given up.
-__device__ __forceinline__ bool wait_count(const int* ctr, int target, int* status, int* diag, int site, int detail) {
-  if (ld_acquire(ctr) - target >= 0) return true;
-  const unsigned long long t0 = dev::globaltimer_ns();
-  for (unsigned n = 0;; ++n) {
-    if (ld_acquire(ctr) - target >= 0) return true;
-    if ((n & 15u) == 15u && dev::status_set(status)) return false;
-    if (dev::globaltimer_ns() - t0 > kWaitLimitNs) {
-      give_up(status, diag, site, detail, ld_acquire(ctr));
-      return false;
-    }
-  }
-}
+constexpr int kSiteConsCount = 2, kSiteConsRing = 4, kSiteProdRing = 5, kSiteProdCount = 6;
 
 // An mbarrier phase wait of the pass: as dev::mbar_wait, with its site recorded
 __device__ __forceinline__ bool ring_wait(uint32_t bar, uint32_t parity, int* status, int* diag, int site, int detail) {
   if (dev::mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = dev::globaltimer_ns();
-  for (unsigned n = 0;; ++n) {
+  unsigned long long next_check = t0 + kPollNs;
+  for (;;) {
     if (dev::mbar_try_wait(bar, parity)) return true;
-    if ((n & 31u) == 31u && dev::status_set(status)) return false;
-    if (dev::globaltimer_ns() - t0 > kWaitLimitNs) {
+    const unsigned long long t = dev::globaltimer_ns();
+    if (t > next_check) {   // another wait may have given up (checked every few microseconds)
+      if (dev::status_set(status)) return false;
+      next_check = t + kPollNs;
+    }
+    if (t - t0 > kWaitLimitNs) {
       give_up(status, diag, site, detail, (int)parity);
       return false;
     }
   }
 }
 
-__device__ __forceinline__ void cons_sync() { asm volatile("bar.sync 1, 512;" ::: "memory"); }
+// (the non-aligned barrier forms: thread 0 reaches them from its own loops)
+__device__ __forceinline__ void cons_sync() { asm volatile("barrier.sync 1, 256;" ::: "memory"); }
 
-// Barrier of the consumer warps that also ORs one flag over all of them: every
-// consumer thread gets the same answer, so a decision taken on it is uniform
-// (the abort flag itself may change at any time; the producer sets it too).
+// Barrier of the CTA's warps that also ORs one flag over all of them: every
+// thread gets the same answer, so a decision taken on it is uniform (the
+// abort flag itself may be set by any warp at any time).
 __device__ __forceinline__ bool cons_sync_any(bool v) {
   uint32_t r;
   asm volatile(
       "{\n\t.reg .pred p, q;\n\t"
       "setp.ne.u32 p, %1, 0;\n\t"
-      "bar.red.or.pred q, 1, 512, p;\n\t"
+      "barrier.red.or.pred q, 1, 256, p;\n\t"
       "selp.u32 %0, 1, 0, q;\n\t}\n"
       : "=r"(r)
       : "r"((uint32_t)v)
@@ -250,119 +253,261 @@ __device__ __forceinline__ void codes_bf16(uint32_t w, uint32_t r[4]) {
 struct Shared {
   uint64_t full[kStages];
   uint64_t empty[kStages];
+  Item item;                              // this CTA's attention item
+  int u0[kPassPhases], u1[kPassPhases];   // this CTA's units of each projection step
+  unsigned issued;                        // uses the producer has issued
   int abort;
   int n_own;
   int own[kMaxOwn];
   float rscale[kPassRows];
   int merge_last;
 };
+__shared__ Shared sh;
 
 // ============================================================== the producer
-// One thread walks the call's schedule in the consumers' order and fills the
-// ring.  Only the key blocks that hold this call's rows wait for a result
-// (the QKV step of their layer).
-template <int NT>
-__device__ void produce(const PassParams& p, Shared& sh, uint32_t ring) {
+// Lane 0 of the producer warp walks the call's schedule of ring uses -- this
+// CTA's units of every projection step and its attention item's key blocks
+// (a K tile, then a V^T tile), layer after layer -- and issues the copy of
+// each use as soon as its stage is free, so the weights of later steps stream
+// while the consumers wait for a step's inputs.  Key blocks that hold this
+// call's rows are issued once the layer's QKV step is complete, after a proxy
+// fence, since the consumers' generic stores wrote them.  Everything that
+// needs a division is worked out once per step; an issue only advances the
+// step's (tile, k-step) cursor.
+struct Cursor {
+  int l, ph;              // step: layer, phase
+  int k, n;               // index within the step's uses, their count
+  int tile, ks, ksteps;
+  int seg, seg_end, t2;   // QKV segment (0 q, 1 k, 2 v), its end tile, the first v tile
+  int row0, rstep;        // weight row of the tile, rows from one tile to the next
+  int wi;                 // PassLayer matrix of the segment (gate|up: 4 and 5)
+  bool pair;
+  const PassLayer* Ly;
+  int kb, vb, b;          // attention: view rows of the layer's K and V^T, the block
+};
+
+__device__ __forceinline__ void cursor_enter(const PassParams& p, Cursor& c) {
+  c.k = 0;
+  if (c.ph == kPhAttn) {
+    const Item& item = sh.item;
+    c.n = 2 * (item.b1 - item.b0);
+    c.b = item.b0;
+    c.kb = p.kbase0 + c.l * 2 * p.Hkv * p.cap + item.kv * p.cap;
+    c.vb = p.vtbase0 + c.l * 2 * p.Hkv * p.d + item.kv * p.d;
+    return;
+  }
+  const Proj j = proj_of(p, c.ph);
+  const int u0 = sh.u0[c.ph];
+  c.n = sh.u1[c.ph] - u0;
+  if (c.n <= 0) return;
+  c.ksteps = j.ksteps;
+  c.tile = u0 / j.ksteps;
+  c.ks = u0 % j.ksteps;
+  c.seg = seg_of(j, c.tile);
+  c.t2 = j.t2;
+  c.seg_end = c.seg == 0 ? j.t1 : (c.seg == 1 ? j.t2 : (1 << 30));
+  c.row0 = row0_of(j, c.tile, c.seg);
+  c.rstep = j.pair ? 64 : kGemvRows;
+  c.pair = j.pair;
+  c.wi = mat_of(j, c.seg);
+  c.Ly = p.layers + c.l;
+  for (int s = 0; s < (j.pair ? 2 : 1); ++s) {
+    dev::prefetch_tmap(&c.Ly->tw[c.wi + s]);
+    dev::prefetch_tmap(&c.Ly->ts[c.wi + s]);
+  }
+}
+
+// advance a projection cursor past one use: the next k-step, the next tile,
+// the next QKV segment
+__device__ __forceinline__ void cursor_next_unit(Cursor& c) {
+  if (++c.ks == c.ksteps) {
+    c.ks = 0;
+    c.row0 += c.rstep;
+    if (++c.tile == c.seg_end) {
+      ++c.seg;
+      c.wi = c.seg;   // QKV: matrices 0, 1, 2
+      c.row0 = 0;
+      c.seg_end = c.seg == 1 ? c.t2 : (1 << 30);
+      dev::prefetch_tmap(&c.Ly->tw[c.wi]);
+      dev::prefetch_tmap(&c.Ly->ts[c.wi]);
+    }
+  }
+}
+
+// Wait (bounded) for an mbarrier phase on the producer's side: gives up when
+// the consumers have aborted, when the status word is set, or after the limit.
+__device__ __forceinline__ bool producer_wait(const PassParams& p, uint32_t bar, uint32_t parity, int detail) {
+  if (dev::mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = dev::globaltimer_ns();
+  unsigned long long next_check = t0 + kPollNs;
+  for (;;) {
+    if (dev::mbar_try_wait(bar, parity)) return true;
+    if (*reinterpret_cast<volatile int*>(&sh.abort)) return false;
+    const unsigned long long t = dev::globaltimer_ns();
+    if (t > next_check) {
+      if (dev::status_set(p.status)) return false;
+      next_check = t + kPollNs;
+    }
+    if (t - t0 > kWaitLimitNs) {
+      give_up(p.status, p.diag, kSiteProdRing, detail, (int)parity);
+      return false;
+    }
+  }
+}
+
+__device__ __noinline__ void producer(const PassParams& p, uint32_t ring) {
   const uint64_t pol = dev::policy_evict_first();
   dev::prefetch_tmap(&p.tkv);
   dev::prefetch_tmap(&p.tvt);
-  unsigned it = 0;
-  bool ok = true;
-  auto next_stage = [&](uint32_t bytes) -> uint32_t {
+  Cursor c;
+  c.l = 0;
+  c.ph = 0;
+  cursor_enter(p, c);
+  int qkv_l = -1;   // last layer whose QKV step is known complete
+  unsigned it = 0;  // uses issued
+  bool live = true;
+  while (live) {
+    if (c.k >= c.n) {   // the step is exhausted: the next one
+      if (++c.ph == kPassPhases) {
+        c.ph = 0;
+        if (++c.l == p.L) break;
+      }
+      cursor_enter(p, c);
+      continue;
+    }
     const int st = (int)(it % kStages);
-    if (it >= (unsigned)kStages) {
-      if (!ring_wait(dev::smem_u32(&sh.empty[st]), ((it / kStages) - 1) & 1, p.status, p.diag, kSiteProdRing, (int)it) ||
-          *reinterpret_cast<volatile int*>(&sh.abort)) {
-        ok = false;
-        return 0;
-      }
-    }
-    dev::mbar_arrive_expect_tx(dev::smem_u32(&sh.full[st]), bytes);
-    ++it;
-    return (uint32_t)st;
-  };
-  const Item item = item_of(p, blockIdx.x);
-  const int P = p.rows.P;
-  for (int l = 0; l < p.L && ok; ++l) {
-    const PassLayer* Ly = p.layers + l;
-    for (int ph = 0; ph < kPassPhases && ok; ++ph) {
-      if (ph == kPhAttn) {
-        const int kb = p.kbase0 + l * 2 * p.Hkv * p.cap + item.kv * p.cap;
-        const int vb = p.vtbase0 + l * 2 * p.Hkv * p.d + item.kv * p.d;
-        bool waited = false;
-        for (int b = item.b0; b < item.b1 && ok; ++b) {
-          if ((b + 1) * kAttnKeys > P && !waited) {
-            // this block holds rows of this call: their K/V come from the QKV step
-            if (!wait_count(p.done + done_index(l, kPhQKV), (int)p.epoch * done_count(p, kPhQKV), p.status,
-                            p.diag, kSiteProdCount, done_index(l, kPhQKV))) {
-              ok = false;
-              break;
-            }
-            fence_proxy_async_global();
-            waited = true;
+    if (it >= (unsigned)kStages && !producer_wait(p, dev::smem_u32(&sh.empty[st]), ((it / kStages) - 1) & 1, (int)it))
+      break;
+    const uint32_t sb = ring + st * kStage;
+    const uint32_t fb = dev::smem_u32(&sh.full[st]);
+    if (c.ph == kPhAttn) {
+      if ((c.b + 1) * kAttnKeys > p.rows.P && qkv_l < c.l) {
+        // this block holds rows of this call, appended by the layer's QKV step
+        const int* ctr = p.done + done_index(c.l, kPhQKV);
+        const int target = (int)p.epoch * done_count(p, kPhQKV);
+        const unsigned long long t0 = dev::globaltimer_ns();
+        for (unsigned n = 0; ld_acquire(ctr) - target < 0; ++n) {
+          __nanosleep(kCountBackoffNs);
+          if (*reinterpret_cast<volatile int*>(&sh.abort) || ((n & 15u) == 15u && dev::status_set(p.status))) {
+            live = false;
+            break;
           }
-          const uint32_t sk = next_stage(kAttnKeys * kAttnD * 2);
-          if (!ok) break;
-          const uint32_t fk = dev::smem_u32(&sh.full[sk]);
-          dev::tma_load_2d(ring + sk * kStage, &p.tkv, 0, kb + b * kAttnKeys, fk);
-          dev::tma_load_2d(ring + sk * kStage + kAttnKeys * 128, &p.tkv, 64, kb + b * kAttnKeys, fk);
-          const uint32_t sv = next_stage(kAttnKeys * kAttnD * 2);
-          if (!ok) break;
-          dev::tma_load_2d(ring + sv * kStage, &p.tvt, b * kAttnKeys, vb, dev::smem_u32(&sh.full[sv]));
+          if (dev::globaltimer_ns() - t0 > kWaitLimitNs) {
+            give_up(p.status, p.diag, kSiteProdCount, done_index(c.l, kPhQKV), ld_acquire(ctr));
+            live = false;
+            break;
+          }
         }
-        continue;
+        if (!live) break;
+        fence_proxy_async_global();
+        qkv_l = c.l;
       }
-      const Proj j = proj_of(p, ph);
-      const int units = j.tiles * j.ksteps;
-      int u0, u1;
-      unit_range(units, p.ctas, blockIdx.x, u0, u1);
-      for (int s = 0; s < (j.pair ? 2 : j.nseg); ++s) {
-        dev::prefetch_tmap(&Ly->tw[mat_of(j, s)]);
-        dev::prefetch_tmap(&Ly->ts[mat_of(j, s)]);
+      dev::mbar_arrive_expect_tx(fb, kAttnKeys * kAttnD * 2);
+      if ((c.k & 1) == 0) {
+        const int kr = c.kb + c.b * kAttnKeys;
+        dev::tma_load_2d(sb, &p.tkv, 0, kr, fb);
+        dev::tma_load_2d(sb + kAttnKeys * 128, &p.tkv, 64, kr, fb);
+      } else {
+        dev::tma_load_2d(sb, &p.tvt, c.b * kAttnKeys, c.vb, fb);
+        ++c.b;
       }
-      for (int u = u0; u < u1 && ok; ++u) {
-        const uint32_t st = next_stage(kStage);
-        if (!ok) break;
-        const uint32_t sb = ring + st * kStage;
-        const uint32_t fb = dev::smem_u32(&sh.full[st]);
-        const int tile = u / j.ksteps, ks = u % j.ksteps;
-        const int s = seg_of(j, tile);
-        const int row0 = row0_of(j, tile, s);
-        if (j.pair) {
-          dev::tma_load_2d_hint(sb, &Ly->tw[4], ks * 128, row0, fb, pol);
-          dev::tma_load_2d_hint(sb + 64 * 128, &Ly->tw[5], ks * 128, row0, fb, pol);
-          dev::tma_load_2d_hint(sb + 128 * 128, &Ly->ts[4], ks * 8, row0, fb, pol);
-          dev::tma_load_2d_hint(sb + 128 * 128 + 64 * 16, &Ly->ts[5], ks * 8, row0, fb, pol);
-        } else {
-          dev::tma_load_2d_hint(sb, &Ly->tw[mat_of(j, s)], ks * 128, row0, fb, pol);
-          dev::tma_load_2d_hint(sb + 128 * 128, &Ly->ts[mat_of(j, s)], ks * 8, row0, fb, pol);
-        }
+    } else {
+      const CUtensorMap* tw = &c.Ly->tw[c.wi];
+      const CUtensorMap* ts = &c.Ly->ts[c.wi];
+      const int x = c.ks * 128, xs = c.ks * 8, y = c.row0;
+      dev::mbar_arrive_expect_tx(fb, kStage);
+      if (c.pair) {
+        dev::tma_load_2d_hint(sb, tw, x, y, fb, pol);
+        dev::tma_load_2d_hint(sb + 64 * 128, tw + 1, x, y, fb, pol);
+        dev::tma_load_2d_hint(sb + 128 * 128, ts, xs, y, fb, pol);
+        dev::tma_load_2d_hint(sb + 128 * 128 + 64 * 16, ts + 1, xs, y, fb, pol);
+      } else {
+        dev::tma_load_2d_hint(sb, tw, x, y, fb, pol);
+        dev::tma_load_2d_hint(sb + 128 * 128, ts, xs, y, fb, pol);
+      }
+      cursor_next_unit(c);
+    }
+    ++it;
+    ++c.k;
+    *reinterpret_cast<volatile unsigned*>(&sh.issued) = it;
+  }
+  // never leave with copies in flight: the last uses issued (whether or not
+  // the consumers took them) have landed before the producer returns, all
+  // within one bounded wait
+  const unsigned long long deadline = dev::globaltimer_ns() + kWaitLimitNs;
+  for (unsigned u = it > (unsigned)kStages ? it - kStages : 0u; u < it; ++u)
+    dev::mbar_wait_until(dev::smem_u32(&sh.full[u % kStages]), (u / kStages) & 1, deadline);
+}
+
+// ============================================================== the L2 prefetch
+// Lane 0 of the prefetch warp walks the same schedule kPfAhead uses ahead of
+// the producer and pulls each use's boxes toward L2.  A wait for a step's
+// inputs then does not stop the HBM stream: the ring's copies after it read
+// L2.  (Key blocks that hold this call's rows are not written yet and are
+// skipped.)  It runs in a warp of its own: a lane sharing the producer's warp
+// would sleep while the producer sleeps on a stage.
+__device__ __noinline__ void prefetcher(const PassParams& p) {
+  Cursor c;
+  c.l = 0;
+  c.ph = 0;
+  cursor_enter(p, c);
+  unsigned it = 0;
+  for (;;) {
+    if (c.k >= c.n) {
+      if (++c.ph == kPassPhases) {
+        c.ph = 0;
+        if (++c.l == p.L) return;
+      }
+      cursor_enter(p, c);
+      continue;
+    }
+    // stay kPfAhead uses ahead of the copies, no further (L2 holds the window)
+    if (it >= *reinterpret_cast<volatile unsigned*>(&sh.issued) + kPfAhead) {
+      const unsigned long long t0 = dev::globaltimer_ns();
+      while (it >= *reinterpret_cast<volatile unsigned*>(&sh.issued) + kPfAhead) {
+        if (*reinterpret_cast<volatile int*>(&sh.abort) || dev::globaltimer_ns() - t0 > kWaitLimitNs) return;
+        __nanosleep(100);
       }
     }
-  }
-  if (!ok) *reinterpret_cast<volatile int*>(&sh.abort) = 1;
-  // never leave with copies in flight: the last use of every filled stage,
-  // all within one bounded wait
-  const unsigned long long deadline = dev::globaltimer_ns() + kWaitLimitNs;
-  for (int st = 0; st < kStages && (unsigned)st < it; ++st) {
-    const unsigned last = ((it - 1 - st) / kStages) * kStages + st;
-    dev::mbar_wait_until(dev::smem_u32(&sh.full[st]), (last / kStages) & 1, deadline);
+    if (c.ph == kPhAttn) {
+      if ((c.b + 1) * kAttnKeys <= p.rows.P) {
+        if ((c.k & 1) == 0) {
+          dev::tma_prefetch_2d(&p.tkv, 0, c.kb + c.b * kAttnKeys);
+          dev::tma_prefetch_2d(&p.tkv, 64, c.kb + c.b * kAttnKeys);
+        } else {
+          dev::tma_prefetch_2d(&p.tvt, c.b * kAttnKeys, c.vb);
+        }
+      }
+      if (c.k & 1) ++c.b;
+    } else {
+      const CUtensorMap* tw = &c.Ly->tw[c.wi];
+      const CUtensorMap* ts = &c.Ly->ts[c.wi];
+      const int x = c.ks * 128, xs = c.ks * 8, y = c.row0;
+      dev::tma_prefetch_2d(tw, x, y);
+      dev::tma_prefetch_2d(ts, xs, y);
+      if (c.pair) {
+        dev::tma_prefetch_2d(tw + 1, x, y);
+        dev::tma_prefetch_2d(ts + 1, xs, y);
+      }
+      cursor_next_unit(c);
+    }
+    ++it;
+    ++c.k;
   }
 }
 
 // ============================================================== consumers
 struct Cons {
   const PassParams& p;
-  Shared& sh;
   uint32_t ring;
   uint8_t* work;        // generic pointer to the work area
   uint32_t work_s;      // its shared address
-  unsigned it;          // ring uses consumed so far (same count as the producer)
+  unsigned it;          // ring uses taken so far (the producer issues them in the same order)
   int tid, warp, lane;
   bool ok;              // uniform after each cons_sync
 
-  __device__ Cons(const PassParams& pp, Shared& s, uint32_t r, uint8_t* w, uint32_t ws)
-      : p(pp), sh(s), ring(r), work(w), work_s(ws), it(0) {
+  __device__ __forceinline__ Cons(const PassParams& pp, uint32_t r, uint8_t* w, uint32_t ws)
+      : p(pp), ring(r), work(w), work_s(ws), it(0) {
     tid = threadIdx.x;
     warp = tid >> 5;
     lane = tid & 31;
@@ -374,7 +519,22 @@ struct Cons {
   // one thread waits for a counter; everyone learns the outcome at the barrier
   __device__ __forceinline__ bool wait_dep(int idx, int count) {
     if (tid == 0 && !abort_flag()) {
-      if (!wait_count(p.done + idx, (int)p.epoch * count, p.status, p.diag, kSiteConsCount, idx)) abort_flag() = 1;
+      const int* ctr = p.done + idx;
+      const int target = (int)p.epoch * count;
+      const unsigned long long t0 = dev::globaltimer_ns();
+      for (unsigned n = 0;; ++n) {
+        if (ld_acquire(ctr) - target >= 0) break;
+        __nanosleep(kCountBackoffNs);
+        if ((n & 15u) == 15u && dev::status_set(p.status)) {
+          abort_flag() = 1;
+          break;
+        }
+        if (dev::globaltimer_ns() - t0 > kWaitLimitNs) {
+          give_up(p.status, p.diag, kSiteConsCount, idx, ld_acquire(ctr));
+          abort_flag() = 1;
+          break;
+        }
+      }
     }
     ok = !cons_sync_any(abort_flag() != 0);
     return ok;
@@ -385,8 +545,10 @@ struct Cons {
   // every use, so the ring's phases stay in step)
   __device__ __forceinline__ uint32_t wait_use(unsigned u, bool& good) {
     const int st = (int)(u % kStages);
-    const bool got = !abort_flag() &&
-                     ring_wait(dev::smem_u32(&sh.full[st]), (u / kStages) & 1, p.status, p.diag, kSiteConsRing, (int)u);
+    const uint32_t bar = dev::smem_u32(&sh.full[st]);
+    const uint32_t parity = (u / kStages) & 1;
+    bool got = false;
+    if (!abort_flag()) got = ring_wait(bar, parity, p.status, p.diag, kSiteConsRing, (int)u);
     good = __all_sync(0xffffffffu, got);
     if (!good && lane == 0) abort_flag() = 1;
     return ring + st * kStage;
@@ -398,14 +560,14 @@ struct Cons {
 
   // ---------------------------------------------------------- activations
   // x for the unit at k-step ks: rows [0, m) of 256 inputs, bf16, in the
-  // GEMV's swizzled box layout; thread = (row, 8-input chunk)
+  // GEMV's swizzled box layout; a warp stages rows warp and warp + 8, a lane
+  // one 8-input chunk of each
   struct Chunk {
     float4 h0, h1;
     uint4 g;
   };
-  __device__ __forceinline__ bool chunk_live(int NT) const { return (tid >> 5) < p.m && tid < 8 * NT * 32; }
-  __device__ __forceinline__ void chunk_load(int ph, const __nv_bfloat16* gain, int ks, Chunk& c) const {
-    const int n = tid >> 5, k = ks * kGemvKStep + 8 * (tid & 31);
+  __device__ __forceinline__ void chunk_load(int ph, const __nv_bfloat16* gain, int ks, int n, Chunk& c) const {
+    const int k = ks * kGemvKStep + 8 * lane;
     if (ph == kPhQKV || ph == kPhGU) {
       const float4* hp = reinterpret_cast<const float4*>(p.h + (long long)n * p.H + k);
       c.h0 = __ldcg(hp);
@@ -416,8 +578,9 @@ struct Cons {
       c.g = __ldcg(reinterpret_cast<const uint4*>(src + k));
     }
   }
-  __device__ __forceinline__ void chunk_store(int ph, const Chunk& c, uint32_t xbuf) const {
-    const int n = tid >> 5, k8 = tid & 31;
+  template <int NT>
+  __device__ __forceinline__ void chunk_store(int ph, const Chunk& c, int n, uint32_t xbuf) const {
+    const int k8 = lane;
     uint4 v = c.g;
     if (ph == kPhQKV || ph == kPhGU) {
       const float r = sh.rscale[n];
@@ -429,10 +592,11 @@ struct Cons {
       v.z = dev::pack_bf16x2(c.h1.x * r * g2f.x, c.h1.y * r * g2f.y);
       v.w = dev::pack_bf16x2(c.h1.z * r * g3.x, c.h1.w * r * g3.y);
     }
-    const uint32_t addr = xbuf + (k8 >> 3) * kXBox + dev::swz128((uint32_t)n, (uint32_t)(k8 & 7));
+    const uint32_t addr = xbuf + (k8 >> 3) * (NT * 1024) + dev::swz128((uint32_t)n, (uint32_t)(k8 & 7));
+    // no memory clobber: the next items' global loads may be issued before
+    // this store; the barrier after the staging orders it before the reads
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z),
-                 "r"(v.w)
-                 : "memory");
+                 "r"(v.w));
   }
 
   // RMSNorm factors of the call's rows from the per-tile sums (fixed order)
@@ -446,9 +610,42 @@ struct Cons {
     }
   }
 
+  // stage x of nslot units from unit ua on (slot i: unit ua + i): a warp per
+  // (unit, row), a lane per 8 inputs.  O and DOWN copy bf16 rows of o and z
+  // with asynchronous copies, all in flight at once; QKV and GU convert
+  // RMSNorm(h) * g two items at a time (both items' loads in flight before
+  // the first store).  Rows from m to 8 * NT are left as they are: they feed
+  // output columns that are never stored.
+  template <int NT>
+  __device__ __forceinline__ void stage(int ph, const __nv_bfloat16* gain, int ua, int nslot, int ksteps) {
+    constexpr int kUnitX = 4 * NT * 1024;
+    const int items = nslot * p.m;
+    if (ph == kPhO || ph == kPhDown) {
+      for (int sn = warp; sn < items; sn += kWarps) {
+        const int slot = sn / p.m, n = sn - slot * p.m;
+        const int k = ((ua + slot) % ksteps) * kGemvKStep + 8 * lane;
+        const __nv_bfloat16* src = ph == kPhO ? p.o + (long long)n * p.Hq * p.d : p.z + (long long)n * p.F;
+        const uint32_t dst = work_s + slot * kUnitX + (lane >> 3) * (NT * 1024) + dev::swz128((uint32_t)n, (uint32_t)(lane & 7));
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src + k) : "memory");
+      }
+      asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+      return;
+    }
+    for (int sn = warp; sn < items; sn += 2 * kWarps) {
+      Chunk c0, c1;
+      const int sn1 = sn + kWarps;
+      const int slot0 = sn / p.m, n0 = sn - slot0 * p.m;
+      const int slot1 = sn1 / p.m, n1 = sn1 - slot1 * p.m;
+      chunk_load(ph, gain, (ua + slot0) % ksteps, n0, c0);
+      if (sn1 < items) chunk_load(ph, gain, (ua + slot1) % ksteps, n1, c1);
+      chunk_store<NT>(ph, c0, n0, work_s + slot0 * kUnitX);
+      if (sn1 < items) chunk_store<NT>(ph, c1, n1, work_s + slot1 * kUnitX);
+    }
+  }
+
   // ---------------------------------------------------------- one projection step
   template <int NT>
-  __device__ __noinline__ void projection(int l, int ph) {
+  __device__ __forceinline__ void projection(int l, int ph) {
     const Proj j = proj_of(p, ph);
     const int units = j.tiles * j.ksteps;
     int u0, u1;
@@ -467,96 +664,85 @@ struct Cons {
       row_scales();
       cons_sync();
     }
-    const uint32_t xb0 = work_s, xb1 = work_s + kXBytes;
-    float* ct = reinterpret_cast<float*>(work + 2 * kXBytes);
-    const bool live = chunk_live(NT);
-    Chunk ch;
-    if (live) {
-      chunk_load(ph, gain, u0 % j.ksteps, ch);
-      chunk_store(ph, ch, xb0);
-    }
-    cons_sync();
-    // warp roles: 16 weight rows (rg) x half of the 8 input groups (kh)
-    const int rg = warp & 7, kh = warp >> 3;
+    float* ct = reinterpret_cast<float*>(work);   // the epilogue's tile buffer (after the units)
+    constexpr int kUnitX = 4 * NT * 1024;          // staged activations of one unit
+    constexpr int kChunk = kXArea / kUnitX;        // units staged at a time (16 or 8)
+    // warp role: 16 weight rows of the tile, all 256 inputs of a unit
     const int r = lane >> 2, c = lane & 3;
-    const int rho0 = rg * 16 + r;
+    const int rho0 = warp * 16 + r;
     float acc[NT][4];
 #pragma unroll
     for (int t = 0; t < NT; ++t)
 #pragma unroll
       for (int e = 0; e < 4; ++e) acc[t][e] = 0.f;
     const float zero4[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int i = 0; i < nk; ++i) {
-      const int u = u0 + i;
-      const uint32_t xb = (i & 1) ? xb1 : xb0;
-      if (i + 1 < nk && live) chunk_load(ph, gain, (u + 1) % j.ksteps, ch);
-      bool good;
-      const uint32_t wt = wait_use(it, good);
-      if (good) {
-        const uint32_t stile = wt + 128 * 128;
-        const uint4 sc0 = dev::lds128(stile + rho0 * 16);
-        const uint4 sc1 = dev::lds128(stile + (rho0 + 8) * 16);
-        const __half* s0h = reinterpret_cast<const __half*>(&sc0);
-        const __half* s1h = reinterpret_cast<const __half*>(&sc1);
+    // a unit's activations depend on its k-step alone: when the step has at
+    // most kChunk k-steps, each is staged once and the units that repeat it
+    // reuse its slot; otherwise the units go kChunk at a time
+    const bool once = j.ksteps <= kChunk;
+    const int span = once ? nk : kChunk;
+    for (int c0 = 0; c0 < nk; c0 += span) {
+      const int cn = min(span, nk - c0);
+      const int nslot = once ? min(nk, j.ksteps) : cn;
+      if (c0 > 0) cons_sync();   // the previous chunk's activations are read
+      stage<NT>(ph, gain, u0 + c0, nslot, j.ksteps);
+      cons_sync();
+      for (int i = c0; i < c0 + cn; ++i) {
+        const int u = u0 + i;
+        const uint32_t xb = work_s + (once ? i % j.ksteps : i - c0) * kUnitX;
+        bool good;
+        const uint32_t wt = wait_use(it, good);
+        if (good) {
+          const uint32_t stile = wt + 128 * 128;
+          const uint4 sc0 = dev::lds128(stile + rho0 * 16);
+          const uint4 sc1 = dev::lds128(stile + (rho0 + 8) * 16);
+          const __half* s0h = reinterpret_cast<const __half*>(&sc0);
+          const __half* s1h = reinterpret_cast<const __half*>(&sc1);
 #pragma unroll
-        for (int gq = 0; gq < 4; ++gq) {
-          const int g = 4 * kh + gq;
-          const uint32_t w0 = dev::lds32(wt + dev::swz128(rho0, g) + 4 * c);
-          const uint32_t w1 = dev::lds32(wt + dev::swz128(rho0 + 8, g) + 4 * c);
-          uint32_t q0[4], q1[4];
-          codes_bf16(w0, q0);
-          codes_bf16(w1, q1);
-          const uint32_t a_lo[4] = {q0[0], q1[0], q0[1], q1[1]};
-          const uint32_t a_hi[4] = {q0[2], q1[2], q0[3], q1[3]};
-          const float sr0 = __half2float(s0h[g]);
-          const float sr1 = __half2float(s1h[g]);
+          for (int g = 0; g < 8; ++g) {
+            const uint32_t w0 = dev::lds32(wt + dev::swz128(rho0, g) + 4 * c);
+            const uint32_t w1 = dev::lds32(wt + dev::swz128(rho0 + 8, g) + 4 * c);
+            uint32_t q0[4], q1[4];
+            codes_bf16(w0, q0);
+            codes_bf16(w1, q1);
+            const uint32_t a_lo[4] = {q0[0], q1[0], q0[1], q1[1]};
+            const uint32_t a_hi[4] = {q0[2], q1[2], q0[3], q1[3]};
+            const float sr0 = __half2float(s0h[g]);
+            const float sr1 = __half2float(s1h[g]);
 #pragma unroll
-          for (int t = 0; t < NT; ++t) {
-            const int n = t * 8 + (lane & 7);
-            const int q = lane >> 3;
-            uint32_t b0, b1, b2, b3;
-            dev::ldmatrix_x4(xb + (g >> 1) * kXBox + dev::swz128(n, 4 * (g & 1) + q), b0, b1, b2, b3);
-            float tmp[4];
-            dev::mma_bf16_16816(tmp, a_lo, b0, b1, zero4);
-            dev::mma_bf16_16816(tmp, a_hi, b2, b3, tmp);
-            acc[t][0] = fmaf(sr0, tmp[0], acc[t][0]);
-            acc[t][1] = fmaf(sr0, tmp[1], acc[t][1]);
-            acc[t][2] = fmaf(sr1, tmp[2], acc[t][2]);
-            acc[t][3] = fmaf(sr1, tmp[3], acc[t][3]);
+            for (int t = 0; t < NT; ++t) {
+              const int n = t * 8 + (lane & 7);
+              const int q = lane >> 3;
+              uint32_t b0, b1, b2, b3;
+              dev::ldmatrix_x4(xb + (g >> 1) * (NT * 1024) + dev::swz128(n, 4 * (g & 1) + q), b0, b1, b2, b3);
+              float tmp[4];
+              dev::mma_bf16_16816(tmp, a_lo, b0, b1, zero4);
+              dev::mma_bf16_16816(tmp, a_hi, b2, b3, tmp);
+              acc[t][0] = fmaf(sr0, tmp[0], acc[t][0]);
+              acc[t][1] = fmaf(sr0, tmp[1], acc[t][1]);
+              acc[t][2] = fmaf(sr1, tmp[2], acc[t][2]);
+              acc[t][3] = fmaf(sr1, tmp[3], acc[t][3]);
+            }
           }
         }
+        release_use(it);
+        ++it;
+        // the tile's partial of this CTA: each warp stores its 16 rows
+        if (u % j.ksteps == j.ksteps - 1 || i == nk - 1) {
+          const int tile = u / j.ksteps;
+          const int first = owner_of((long long)tile * j.ksteps, units, p.ctas);
+          float* tp = p.part + ((long long)tile * p.maxc[ph] + (blockIdx.x - first)) * (kGemvMaxCols * kGemvRows);
+#pragma unroll
+          for (int t = 0; t < NT; ++t)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int tok = t * 8 + 2 * c + (e & 1);
+              const int row = rho0 + (e >> 1) * 8;
+              if (tok < p.m) tp[tok * kGemvRows + row] = acc[t][e];
+              acc[t][e] = 0.f;
+            }
+        }
       }
-      release_use(it);
-      ++it;
-      const bool tile_end = u % j.ksteps == j.ksteps - 1 || i == nk - 1;
-      // the second input half hands its sums to the first through shared memory
-      if (tile_end && kh == 1) {
-#pragma unroll
-        for (int t = 0; t < NT; ++t)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            ct[(t * 8 + 2 * c + (e & 1)) * kCtLd + rho0 + (e >> 1) * 8] = acc[t][e];
-            acc[t][e] = 0.f;
-          }
-      }
-      if (i + 1 < nk && live) chunk_store(ph, ch, (i & 1) ? xb0 : xb1);
-      cons_sync();
-      if (tile_end && kh == 0) {
-        const int tile = u / j.ksteps;
-        const int first = owner_of((long long)tile * j.ksteps, units, p.ctas);
-        float* tp = p.part + ((long long)tile * p.maxc[ph] + (blockIdx.x - first)) * (kGemvMaxCols * kGemvRows);
-#pragma unroll
-        for (int t = 0; t < NT; ++t)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int tok = t * 8 + 2 * c + (e & 1);
-            const int row = rho0 + (e >> 1) * 8;
-            const float v = acc[t][e] + ct[tok * kCtLd + row];
-            if (tok < p.m) tp[tok * kGemvRows + row] = v;
-            acc[t][e] = 0.f;
-          }
-      }
-      if (tile_end) cons_sync();   // ct is free again; the partial is stored
     }
     // one arrival per tile this CTA touched; the last arrival owns the epilogue
     if (tid == 0) sh.n_own = 0;
@@ -587,7 +773,7 @@ struct Cons {
   }
 
   // add a tile's partials in contributor order, then the step's epilogue
-  __device__ __noinline__ void epilogue(int l, int ph, const Proj& j, int units, int tile, float* ct) {
+  __device__ __forceinline__ void epilogue(int l, int ph, const Proj& j, int units, int tile, float* ct) {
     const long long tu0 = (long long)tile * j.ksteps;
     const int first = owner_of(tu0, units, p.ctas);
     const int ncon = owner_of(tu0 + j.ksteps - 1, units, p.ctas) - first + 1;
@@ -603,13 +789,13 @@ struct Cons {
       float4 hv = make_float4(0.f, 0.f, 0.f, 0.f);
       if (resid && r4 < nv_h) hv = __ldcg(reinterpret_cast<const float4*>(p.h + (long long)tok * p.H + row0 + r4));
       float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int j0 = 0; j0 < ncon; j0 += 8) {
-        float4 w[8];
+      for (int j0 = 0; j0 < ncon; j0 += 4) {
+        float4 w[4];
 #pragma unroll
-        for (int q = 0; q < 8; ++q)
+        for (int q = 0; q < 4; ++q)
           if (j0 + q < ncon) w[q] = __ldcg(reinterpret_cast<const float4*>(src + (long long)(j0 + q) * (kGemvMaxCols * kGemvRows)));
 #pragma unroll
-        for (int q = 0; q < 8; ++q)
+        for (int q = 0; q < 4; ++q)
           if (j0 + q < ncon) {
             v.x += w[q].x; v.y += w[q].y; v.z += w[q].z; v.w += w[q].w;
           }
@@ -717,7 +903,7 @@ struct Cons {
   }
 
   // ---------------------------------------------------------- attention
-  __device__ __noinline__ void attention(int l) {
+  __device__ __forceinline__ void attention(int l) {
     const Item item = item_of(p, blockIdx.x);
     if (!item.any) return;
     if (!wait_dep(done_index(l, kPhQKV), done_count(p, kPhQKV))) return;
@@ -960,10 +1146,20 @@ struct Cons {
 #pragma unroll
       for (int o2 = 16; o2 > 0; o2 >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o2);
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int sp = 0; sp < p.nsplit; ++sp) {
-        const float w = __shfl_sync(0xffffffffu, sp < 32 ? w0 : w1, sp & 31);
-        const float4 x = __ldcg(reinterpret_cast<const float4*>(src + sp * stride * D));
-        acc.x += w * x.x; acc.y += w * x.y; acc.z += w * x.z; acc.w += w * x.w;
+      // four splits' loads in flight at a time; added in split order
+      for (int sp0 = 0; sp0 < p.nsplit; sp0 += 4) {
+        float4 x[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          if (sp0 + q < p.nsplit) x[q] = __ldcg(reinterpret_cast<const float4*>(src + (sp0 + q) * stride * D));
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int sp = sp0 + q;
+          if (sp < p.nsplit) {
+            const float w = __shfl_sync(0xffffffffu, sp < 32 ? w0 : w1, sp & 31);
+            acc.x += w * x[q].x; acc.y += w * x[q].y; acc.z += w * x[q].z; acc.w += w * x[q].w;
+          }
+        }
       }
       const float inv = 1.f / den;
       const int tok = row / p.G, head = kv * p.G + row % p.G;
@@ -999,13 +1195,11 @@ struct Cons {
 template <int NT>
 __global__ void __launch_bounds__(kThreads, 1) pass_kernel(const __grid_constant__ PassParams p) {
   extern __shared__ uint8_t smem_raw[];
-  __shared__ Shared sh;
   const uint32_t raw = dev::smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   const uint32_t ring = base;
   const uint32_t work_s = base + kStages * kStage;
   uint8_t* work = smem_raw + (work_s - raw);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
       dev::mbar_init(dev::smem_u32(&sh.full[i]), 1);
@@ -1015,28 +1209,36 @@ __global__ void __launch_bounds__(kThreads, 1) pass_kernel(const __grid_constant
     sh.abort = dev::status_set(p.status) ? 1 : 0;
     sh.n_own = 0;
     sh.merge_last = 0;
+    sh.issued = 0;
+    sh.item = item_of(p, blockIdx.x);
+    for (int ph = 0; ph < kPassPhases; ++ph) {
+      sh.u0[ph] = sh.u1[ph] = 0;
+      if (ph == kPhAttn) continue;
+      const Proj j = proj_of(p, ph);
+      unit_range(j.tiles * j.ksteps, p.ctas, blockIdx.x, sh.u0[ph], sh.u1[ph]);
+    }
     dev::fence_mbar_init();
   }
   __syncthreads();
   if (sh.abort) return;
-  if (warp == kWarps) {
-    if (lane == 0) produce<NT>(p, sh, ring);
+  if (threadIdx.x >= kCons) {
+    // the producer and prefetch warps: one lane each, the others have no work
+    if (threadIdx.x == kCons) producer(p, ring);
+    if (threadIdx.x == kCons + 32) prefetcher(p);
     return;
   }
-  // activation rows past the call's rows stay zero in both unit buffers
-  for (int i = threadIdx.x; i < 2 * kXBytes / 16; i += kCons)
-    asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(work_s + 16 * i), "r"(0u) : "memory");
-  cons_sync();
-  Cons cs(p, sh, ring, work, work_s);
+  Cons cs(p, ring, work, work_s);
   cs.embed();
   for (int l = 0; l < p.L && cs.ok; ++l) {
-    cs.template projection<NT>(l, kPhQKV);
-    if (cs.ok) cs.attention(l);
-    if (cs.ok) cs.template projection<NT>(l, kPhO);
-    if (cs.ok) cs.template projection<NT>(l, kPhGU);
-    if (cs.ok) cs.template projection<NT>(l, kPhDown);
+#pragma unroll 1
+    for (int ph = 0; ph < kPassPhases && cs.ok; ++ph) {
+      if (ph == kPhAttn) cs.attention(l);
+      else cs.template projection<NT>(l, ph);
+    }
   }
   if (cs.ok) cs.head_norm();
+  // a consumer that stops early tells the producer, which then stops issuing
+  if (!cs.ok && threadIdx.x == 0) *reinterpret_cast<volatile int*>(&sh.abort) = 1;
 }
 
 int g_ctas = 0;
@@ -1052,6 +1254,8 @@ cudaError_t pass_setup() {
   if (e == cudaSuccess) e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, pass_kernel<2>, kThreads, kSmem);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(pass_kernel<1>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(pass_kernel<2>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
   if (e == cudaSuccess) g_ctas = per >= 1 ? sms : 0;
   return e;
 }

@@ -411,6 +411,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// Non-blocking test of a phase: try_wait may suspend the thread until the
+// phase completes or a hardware time limit passes, so a thread that must go
+// on with other work when the phase is not complete (and may itself be the
+// one that completes it later) tests with test_wait instead.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
 
 // The device status word: non-zero once any wait of any launch has given up.
 __device__ __forceinline__ bool status_set(const int* status) {

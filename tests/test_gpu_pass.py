@@ -1,8 +1,8 @@
 """The persistent small-m pass against the oracle and against the per-step launches.
 
-Calls with up to 16 rows of an int4 stack with head_dim 128 run as one
-cooperative launch (k_pass.cu); KVR_PASS=0 keeps them on the per-step GEMV and
-attention launches.  Both are checked against the oracle with the stated
+With KVR_PASS=1, calls with up to 16 rows of an int4 stack with head_dim 128
+run as one cooperative launch (k_pass.cu); by default (KVR_PASS unset or 0)
+they stay on the per-step GEMV and attention launches.  Both are checked against the oracle with the stated
 elementwise bound, and against each other, over a prefix of several 64-key
 blocks (several key splits per KV head), for row counts across the one- and
 two-n-tile variants, branch rows, consecutive calls with changing row counts,
