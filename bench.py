@@ -30,6 +30,7 @@ replica (slots shard by conversation; no collective on the data path).
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import os
 import statistics
@@ -164,7 +165,6 @@ def turn9_config(world, fmt="int4"):
 
 
 def build_turn9(device, steps_total, layers=None, fmt="int4"):
-    import dataclasses
     from prefix_reused_prefill_gb300 import Kvr, config_for_shape
     shape = workloads.SHAPES["qwen7b" if fmt == "int4" else "qwen7b_q4k"]
     if layers:
@@ -422,6 +422,8 @@ def run_verify(args):
     device = torch.device("cuda", torch.cuda.current_device())
     pk, pk_kind = peaks()
     shape = workloads.SHAPES["dense9b" if args.format == "int4" else "dense9b_q4k"]
+    if args.layers:   # profiling aid: a reduced stack
+        shape = dataclasses.replace(shape, n_layers=args.layers)
     seed = workloads.config_seed(3)
     tk = workloads.verify_tokens(seed)
     P = len(tk["state"])
@@ -483,8 +485,9 @@ def run_verify(args):
     ts = np.array([r["ms"] for r in table])
     b, a = np.polyfit(ms_, ts, 1)
     kv.close()
+    reduced = f" (REDUCED to {args.layers} layers: profiling case)" if args.layers else ""
     return {"metric": "verify ms per call", "workload": "speculative verify: 36 x (H 4096, 32/8 heads, F 12288) "
-            f"{FORMAT_LABEL[args.format]}, 4096 cached tokens, m = k+1 rows", "unit": "ms", "higher_is_better": False,
+            f"{FORMAT_LABEL[args.format]}, 4096 cached tokens, m = k+1 rows" + reduced, "unit": "ms", "higher_is_better": False,
             "fit_ms": {"a": round(float(a), 4), "b_per_row": round(float(b), 4)},
             "accept": {"vocab": workloads.VOCAB, "what": "accept_ms: kvr_verify_accept (verify + final "
                        "RMSNorm + int4 LM head + argmax + acceptance, read back to the host), device events; "
