@@ -687,9 +687,10 @@ struct Cons {
       if (c0 > 0) cons_sync();   // the previous chunk's activations are read
       stage<NT>(ph, gain, u0 + c0, nslot, j.ksteps);
       cons_sync();
+      // running (tile, k-step) of the unit and its activation slot
+      int ks_c = (u0 + c0) % j.ksteps, tile_c = (u0 + c0) / j.ksteps, slot = 0;
       for (int i = c0; i < c0 + cn; ++i) {
-        const int u = u0 + i;
-        const uint32_t xb = work_s + (once ? i % j.ksteps : i - c0) * kUnitX;
+        const uint32_t xb = work_s + slot * kUnitX;
         bool good;
         const uint32_t wt = wait_use(it, good);
         if (good) {
@@ -728,8 +729,8 @@ struct Cons {
         release_use(it);
         ++it;
         // the tile's partial of this CTA: each warp stores its 16 rows
-        if (u % j.ksteps == j.ksteps - 1 || i == nk - 1) {
-          const int tile = u / j.ksteps;
+        if (ks_c == j.ksteps - 1 || i == nk - 1) {
+          const int tile = tile_c;
           const int first = owner_of((long long)tile * j.ksteps, units, p.ctas);
           float* tp = p.part + ((long long)tile * p.maxc[ph] + (blockIdx.x - first)) * (kGemvMaxCols * kGemvRows);
 #pragma unroll
@@ -742,6 +743,11 @@ struct Cons {
               acc[t][e] = 0.f;
             }
         }
+        if (++ks_c == j.ksteps) {
+          ks_c = 0;
+          ++tile_c;
+        }
+        if (++slot == j.ksteps && once) slot = 0;
       }
     }
     // one arrival per tile this CTA touched; the last arrival owns the epilogue
@@ -899,6 +905,80 @@ struct Cons {
       }
       __syncwarp();
       if (lane == 0) red_release_add(p.done + p.L * kPassPhases, 1);
+    }
+  }
+
+  // ---------------------------------------------------------- split merge
+  // The last split of a KV head to finish merges every split's partial (O,
+  // max, sum) of the head's R rows into o, in split order.  First the weights
+  // 2^(m_s - M) and 1 / sum_s w_s l_s of every row (a warp per row, a lane per
+  // split, the rows of a warp's loads in flight together), into shared memory;
+  // then rows in chunks that fit the work area: every (row, split) partial of
+  // the chunk copied in with asynchronous copies, all in flight at once, and a
+  // thread per (row, four head dims) adds them up.
+  __device__ __forceinline__ void merge(int kv, int R) {
+    constexpr int D = kAttnD;
+    const int ns = p.nsplit;
+    const long long stride = (long long)kPassMaxAttnRows;   // rows per split partial
+    float* wsm = reinterpret_cast<float*>(work);            // [R][ns] weights
+    float* inv = wsm + kPassMaxAttnRows * kMaxSplits;       // [R] 1 / denominator
+    const uint32_t stage_s = work_s + (kPassMaxAttnRows * kMaxSplits + kPassMaxAttnRows) * 4;
+    const float* stage = reinterpret_cast<const float*>(work + (stage_s - work_s));
+    constexpr int kStageBytes = kWork - (kPassMaxAttnRows * kMaxSplits + kPassMaxAttnRows) * 4;
+    const float2* mlk = p.ml + (long long)kv * ns * stride;
+    constexpr int kRowsW = kPassMaxAttnRows / kWarps;        // rows of one warp (at most)
+    float2 a[kRowsW], b[kRowsW];
+#pragma unroll
+    for (int q = 0; q < kRowsW; ++q) {
+      const int row = warp + q * kWarps;
+      a[q] = row < R && lane < ns ? __ldcg(mlk + lane * stride + row) : make_float2(-INFINITY, 0.f);
+      b[q] = row < R && lane + 32 < ns ? __ldcg(mlk + (lane + 32) * stride + row) : make_float2(-INFINITY, 0.f);
+    }
+#pragma unroll
+    for (int q = 0; q < kRowsW; ++q) {
+      const int row = warp + q * kWarps;
+      if (row >= R) continue;
+      float M = fmaxf(a[q].x, b[q].x);
+#pragma unroll
+      for (int o2 = 16; o2 > 0; o2 >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o2));
+      const float w0 = a[q].x == -INFINITY ? 0.f : exp2f(a[q].x - M);
+      const float w1 = b[q].x == -INFINITY ? 0.f : exp2f(b[q].x - M);
+      float den = w0 * a[q].y + w1 * b[q].y;
+#pragma unroll
+      for (int o2 = 16; o2 > 0; o2 >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o2);
+      if (lane < ns) wsm[row * ns + lane] = w0;
+      if (lane + 32 < ns) wsm[row * ns + lane + 32] = w1;
+      if (lane == 0) inv[row] = 1.f / den;
+    }
+    const int rows_chunk = max(1, min(R, kStageBytes / (ns * D * 4)));
+    for (int r0 = 0; r0 < R; r0 += rows_chunk) {
+      const int rc = min(rows_chunk, R - r0);
+      cons_sync();   // weights written; the previous chunk's partials read
+      // (row, split, 16-byte piece): 32 pieces per 512-byte partial row
+      for (int idx = tid; idx < rc * ns * (D / 4); idx += kCons) {
+        const int pc = idx % (D / 4), rs = idx / (D / 4);
+        const int sp = rs % ns, row = r0 + rs / ns;
+        const float* src = p.opart + (((long long)kv * ns + sp) * stride + row) * D + 4 * pc;
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(stage_s + 16u * (uint32_t)idx), "l"(src)
+                     : "memory");
+      }
+      asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+      cons_sync();
+      for (int idx = tid; idx < rc * (D / 4); idx += kCons) {
+        const int pc = idx % (D / 4), rr = idx / (D / 4), row = r0 + rr;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int sp = 0; sp < ns; ++sp) {
+          const float w = wsm[row * ns + sp];
+          const float4 x = reinterpret_cast<const float4*>(stage)[(rr * ns + sp) * (D / 4) + pc];
+          acc.x += w * x.x; acc.y += w * x.y; acc.z += w * x.z; acc.w += w * x.w;
+        }
+        const float iv = inv[row];
+        const int tok = row / p.G, head = kv * p.G + row % p.G;
+        uint2 v;
+        v.x = dev::pack_bf16x2(acc.x * iv, acc.y * iv);
+        v.y = dev::pack_bf16x2(acc.z * iv, acc.w * iv);
+        *reinterpret_cast<uint2*>(p.o + (long long)tok * p.Hq * D + head * D + 4 * pc) = v;
+      }
     }
   }
 
@@ -1131,43 +1211,7 @@ struct Cons {
     cons_sync();
     if (!sh.merge_last) return;
     // the last split merges every split's rows in split order into o
-    for (int row = warp; row < R; row += kWarps) {
-      const long long stride = (long long)kPassMaxAttnRows;   // rows per split partial
-      const float* src = p.opart + ((long long)kv * p.nsplit * stride + row) * D + lane * 4;
-      const float2* mls = p.ml + (long long)kv * p.nsplit * stride + row;
-      const float2 ml0 = lane < p.nsplit ? __ldcg(mls + lane * stride) : make_float2(-INFINITY, 0.f);
-      const float2 ml1 = lane + 32 < p.nsplit ? __ldcg(mls + (lane + 32) * stride) : make_float2(-INFINITY, 0.f);
-      float M = fmaxf(ml0.x, ml1.x);
-#pragma unroll
-      for (int o2 = 16; o2 > 0; o2 >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o2));
-      const float w0 = ml0.x == -INFINITY ? 0.f : exp2f(ml0.x - M);
-      const float w1 = ml1.x == -INFINITY ? 0.f : exp2f(ml1.x - M);
-      float den = w0 * ml0.y + w1 * ml1.y;
-#pragma unroll
-      for (int o2 = 16; o2 > 0; o2 >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o2);
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-      // four splits' loads in flight at a time; added in split order
-      for (int sp0 = 0; sp0 < p.nsplit; sp0 += 4) {
-        float4 x[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-          if (sp0 + q < p.nsplit) x[q] = __ldcg(reinterpret_cast<const float4*>(src + (sp0 + q) * stride * D));
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int sp = sp0 + q;
-          if (sp < p.nsplit) {
-            const float w = __shfl_sync(0xffffffffu, sp < 32 ? w0 : w1, sp & 31);
-            acc.x += w * x[q].x; acc.y += w * x[q].y; acc.z += w * x[q].z; acc.w += w * x[q].w;
-          }
-        }
-      }
-      const float inv = 1.f / den;
-      const int tok = row / p.G, head = kv * p.G + row % p.G;
-      uint2 v;
-      v.x = dev::pack_bf16x2(acc.x * inv, acc.y * inv);
-      v.y = dev::pack_bf16x2(acc.z * inv, acc.w * inv);
-      *reinterpret_cast<uint2*>(p.o + (long long)tok * p.Hq * D + head * D + lane * 4) = v;
-    }
+    merge(kv, R);
     cons_sync();
     if (tid == 0) red_release_add(p.done + done_index(l, kPhAttn), 1);
   }

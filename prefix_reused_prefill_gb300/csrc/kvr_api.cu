@@ -857,6 +857,7 @@ int run_pass(kvr_ctx* c, const RowMap& rows, const void* hidden, const kvr_layer
   }
   p.nb = (rows.P + m + kAttnKeys - 1) / kAttnKeys;
   p.nsplit = std::max(1, std::min(std::min(ctas / Hkv, p.nb), kMaxSplits));   // the merge holds 64
+  if (c->attn_splits > 0) p.nsplit = std::max(1, std::min(c->attn_splits, p.nsplit));
   while (p.nsplit > 1 && ((size_t)Hkv * p.nsplit * kPassMaxAttnRows * d > c->sl.opart_floats ||
                           (size_t)Hkv * p.nsplit * kPassMaxAttnRows > c->sl.ml_count))
     --p.nsplit;
