@@ -62,6 +62,7 @@ struct TcCfg {
   static __device__ __forceinline__ uint32_t scol(int b) { return (uint32_t)(128 * b); }
   static constexpr uint32_t kOCol = 384;
   static constexpr int kTmemCols = 512;
+  static_assert(128 * (D + 4) * 4 <= kKStages * kKBytes, "the O tile fits the K ring");
 };
 
 __device__ __forceinline__ void tc_fence_before() {
@@ -395,13 +396,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
         float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
         // raw scores here; the log2-domain scale is applied inside the
         // exponent's FMA below (the scale is positive, so the max commutes)
-        if (tok >= 0 && pe == 64) {
-          // wholly inside the cached prefix: every key visible
+        if (pe == 64) {
+          // wholly inside the cached prefix: every key visible.  (pe is the same
+          // for every row, so the warp takes one path; a row past the tile's
+          // last token keeps its scores but a block max of -inf, so its O row,
+          // never stored, moves no reference and rescales nothing.)
 #pragma unroll
           for (int k = 0; k < 64; ++k) {
             sv[k] = __uint_as_float(sr[k]);
             m4[k & 3] = fmaxf(m4[k & 3], sv[k]);
           }
+          if (tok < 0) m4[0] = m4[1] = m4[2] = m4[3] = -INFINITY;
         } else {
 #pragma unroll
           for (int k = 0; k < 64; ++k) {
@@ -472,11 +477,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     xsum[half][r] = l;
     named_sync(pair_bar, 64);
     l += xsum[half ^ 1][r];
+    // O (divided by l with one key split; the unnormalised partial with
+    // several) through shared memory, so that the stores to global memory go
+    // a whole row per warp instruction: [128 rows][kOStride floats] over the K
+    // ring, which the last S product has finished reading (the last P V is
+    // complete, and the tensor core completes its products in order).  The
+    // stride keeps both the row-wise v4 writes and the row reads conflict-free.
+    constexpr int kOStride = D + 4;
+    float* ost = reinterpret_cast<float*>(smem_raw + (k_base - dev::smem_u32(smem_raw)));
     if (ok) {
       tc_fence_after();
-      const long long rowidx = (long long)tok * p.Hq + head;
-      const long long plane = (long long)p.rows.m * p.Hq;
-      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const float sc = p.nsplit == 1 ? (l > 0.f ? 1.f / l : 0.f) : 1.f;
 #pragma unroll
       for (int c0 = (D / 2) * half; c0 < (D / 2) * (half + 1); c0 += 32) {
         float v[32];
@@ -486,27 +497,39 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
 #pragma unroll
           for (int k = 0; k < 32; ++k) v[k] = 0.f;
         }
-        if (tok >= 0) {
+#pragma unroll
+        for (int c4 = 0; c4 < 8; ++c4)
+          *reinterpret_cast<float4*>(ost + r * kOStride + c0 + 4 * c4) =
+              make_float4(v[4 * c4] * sc, v[4 * c4 + 1] * sc, v[4 * c4 + 2] * sc, v[4 * c4 + 3] * sc);
+      }
+      if (tok >= 0 && p.nsplit > 1 && half == 0) {
+        const long long plane = (long long)p.rows.m * p.Hq;
+        p.ml[split * plane + (long long)tok * p.Hq + head] = make_float2(m_ref, l);
+      }
+    }
+    named_sync(5, 32 * kSoftmaxWarps);
+    if (ok) {
+      // warp w of the softmax warps writes rows 16 w .. 16 w + 15, a lane per
+      // four head dims
+      const int sw = warp - 2;
+      const long long plane = (long long)p.rows.m * p.Hq;
+      for (int rr = 16 * sw; rr < 16 * sw + 16; ++rr) {
+        const int rho2 = row_lo + rr;
+        if (rho2 >= R) break;
+        const int tk = rho2 / p.G, hd = kv * p.G + rho2 % p.G;
+        const long long ridx = (long long)tk * p.Hq + hd;
+        for (int c = 4 * lane; c < D; c += 128) {
+          const float4 x = *reinterpret_cast<const float4*>(ost + rr * kOStride + c);
           if (p.nsplit == 1) {
-            uint4* dst = reinterpret_cast<uint4*>(p.o + rowidx * D + c0);
-#pragma unroll
-            for (int c8 = 0; c8 < 4; ++c8) {
-              uint4 w;
-              w.x = dev::pack_act2(v[8 * c8] * inv, v[8 * c8 + 1] * inv, p.o16);
-              w.y = dev::pack_act2(v[8 * c8 + 2] * inv, v[8 * c8 + 3] * inv, p.o16);
-              w.z = dev::pack_act2(v[8 * c8 + 4] * inv, v[8 * c8 + 5] * inv, p.o16);
-              w.w = dev::pack_act2(v[8 * c8 + 6] * inv, v[8 * c8 + 7] * inv, p.o16);
-              dst[c8] = w;
-            }
+            uint2 w;
+            w.x = dev::pack_act2(x.x, x.y, p.o16);
+            w.y = dev::pack_act2(x.z, x.w, p.o16);
+            *reinterpret_cast<uint2*>(p.o + ridx * D + c) = w;
           } else {
-            float4* dst = reinterpret_cast<float4*>(p.opart + ((long long)split * plane + rowidx) * D + c0);
-#pragma unroll
-            for (int c4 = 0; c4 < 8; ++c4)
-              dst[c4] = make_float4(v[4 * c4], v[4 * c4 + 1], v[4 * c4 + 2], v[4 * c4 + 3]);
+            *reinterpret_cast<float4*>(p.opart + ((long long)split * plane + ridx) * D + c) = x;
           }
         }
       }
-      if (tok >= 0 && p.nsplit > 1 && half == 0) p.ml[split * plane + rowidx] = make_float2(m_ref, l);
     }
   }
 
