@@ -256,20 +256,25 @@ def peaked_kv(n_kv_heads, P, d, alpha_max, seed):
     return workloads.to_bf16(z * alpha[None, :, None]), workloads.to_bf16(v)
 
 
+@pytest.mark.parametrize("splits", ["0", "2"])
 @pytest.mark.parametrize("combine", ["0", "1"])
 @pytest.mark.parametrize("shape_name,P,alpha,ms", [
     ("small_attn", 1000, 40.0, [1, 3, 8, 40]),     # split-KV up to 24 rows, tcgen05 from 25
     ("qwen7b_attn", 2000, 16.0, [1, 4, 16, 64]),   # split-KV up to 13 rows, tcgen05 from 14
 ])
-def test_peaked_attention_matches_oracle(monkeypatch, shape_name, P, alpha, ms, combine):
+def test_peaked_attention_matches_oracle(monkeypatch, shape_name, P, alpha, ms, combine, splits):
     """Scores with std >= 10 whose row maximum grows across the prefix: the
     tcgen05 kernel must move its lazy reference maximum (and rescale O) many
     times, and the split-KV kernel must merge splits whose maxima differ by
     many units, by the last split (one row per warp) or by the combine launch
-    (KVR_ATTN_COMBINE=1).  Cached K/V given through kvr_slot_kv."""
+    (KVR_ATTN_COMBINE=1).  KVR_ATTN_SPLITS=2 runs the tcgen05 kernel with the
+    two key splits of the turn-9 shape instead of its default four here.
+    Cached K/V given through kvr_slot_kv."""
     monkeypatch.setenv("KVR_ATTN_COMBINE", combine)
+    monkeypatch.setenv("KVR_ATTN_SPLITS", splits)
     shape, kv, w, W, _ = make(shape_name, 2, 2176, 64, seed=workloads.config_seed(5))
     monkeypatch.delenv("KVR_ATTN_COMBINE")
+    monkeypatch.delenv("KVR_ATTN_SPLITS")
     dims = oracle_dims(shape)
     kk, vv = peaked_kv(shape.n_kv_heads, P, shape.head_dim, alpha, 91)
     k, v = kv.kvr_slot_kv(1, 0)
