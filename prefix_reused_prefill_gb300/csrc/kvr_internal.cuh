@@ -432,6 +432,7 @@ __device__ __forceinline__ bool status_set(const int* status) {
   return status && *reinterpret_cast<const volatile int*>(status) != 0;
 }
 
+constexpr unsigned long long kStatusPollNs = 4000;
 // Wait for the phase of `parity` to complete; give up after kWaitLimitNs,
 // record the timeout in the device status word and return false.  A wait
 // that finds the status word already set (another CTA, or an earlier launch,
@@ -440,10 +441,17 @@ __device__ __forceinline__ bool status_set(const int* status) {
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* status) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer_ns();
-  for (unsigned n = 0;; ++n) {
+  // the status word is read once every few microseconds of waiting: a global
+  // load in the loop would otherwise delay noticing the phase
+  unsigned long long next_check = t0 + kStatusPollNs;
+  for (;;) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((n & 31u) == 31u && status_set(status)) return false;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+    const unsigned long long t = globaltimer_ns();
+    if (t > next_check) {
+      if (status_set(status)) return false;
+      next_check = t + kStatusPollNs;
+    }
+    if (t - t0 > kWaitLimitNs) {
       if (status) atomicExch(status, kStatusTimeout);
       return false;
     }
