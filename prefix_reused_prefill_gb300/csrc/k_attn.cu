@@ -32,7 +32,9 @@ struct AttnCfg {
   static constexpr int kHalves = D / 64;                 // 64-element TMA boxes per row
   static constexpr int kTileBytes = kAttnKeys * D * 2;   // one K tile ([64 keys][D]) or V^T tile ([D][64 keys])
   static constexpr int kStageBytes = 2 * kTileBytes;
-  static constexpr int kStages = KW > 1 ? (D == 128 ? 6 : 8) : (D == 128 ? 3 : 4);
+  // key-parallel (one row tile, a split of a few blocks): enough stages for
+  // every block of a typical split to be requested at once (7 x 32 KB fits)
+  static constexpr int kStages = KW > 1 ? (D == 128 ? 7 : 8) : (D == 128 ? 3 : 4);
   static constexpr int kSmem = kStages * kStageBytes + 1024;
   static_assert(KW * (16 * D + 32) * 4 <= kStages * kStageBytes, "warp merge buffer fits the ring");
 };
@@ -67,6 +69,14 @@ __device__ __forceinline__ AttnView attn_view(const AttnParams& p, int bx) {
   v.q = p.q + qd; v.o = p.o + qd;
   v.opart = p.opart + cv.part0; v.ml = p.ml + cv.part0 / D;
   return v;
+}
+
+// 2^x with the PTX approximate base-2 exponential (ex2.approx.ftz.f32; 2^-inf
+// = 0): one instruction on the per-element softmax chain
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 struct RowInfo {
@@ -334,7 +344,7 @@ __global__ void __launch_bounds__((RW * KW + 1) * 32) attn_kernel(const __grid_c
       mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 2));
       const float mnew = fmaxf(mrow[h], mx[h]);
       muse[h] = mnew == -INFINITY ? 0.f : mnew;
-      corr[h] = exp2f(mrow[h] - muse[h]);
+      corr[h] = ex2_approx(mrow[h] - muse[h]);
       mrow[h] = mnew;
       lrow[h] *= corr[h];
     }
@@ -347,7 +357,7 @@ __global__ void __launch_bounds__((RW * KW + 1) * 32) attn_kernel(const __grid_c
     for (int nt = 0; nt < 8; ++nt) {
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const float pv = exp2f(s[nt][e] - muse[e >> 1]);
+        const float pv = ex2_approx(s[nt][e] - muse[e >> 1]);
         s[nt][e] = pv;
         lrow[e >> 1] += pv;
       }
