@@ -202,13 +202,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
       dev::mbar_init(dev::smem_u32(&p_full[i]), kSoftmaxWarps);
       dev::mbar_init(dev::smem_u32(&pv_done[i]), 1);
     }
-    // a wait has given up earlier in the call: leave before any copy or
-    // tensor-memory allocation (one decision for the whole CTA)
+    // a wait has given up earlier in the call: the CTA issues no copy and
+    // runs no role (one decision for the whole CTA, read after the
+    // allocation's barrier rather than behind a barrier of its own)
     *abort_v = dev::status_set(p.status) ? 1 : 0;
     dev::fence_mbar_init();
   }
-  __syncthreads();
-  if (*abort_v) return;
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      dev::smem_u32(&tmem_slot)),
@@ -219,6 +218,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
+  if (*abort_v) goto teardown;
   // q and this call's K/V come from the previous launch; only the producers'
   // loads of cached-prefix K/V may run ahead of it.
   if (warp != 0 || lane > 1) dev::pdl_wait();
@@ -533,6 +533,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(const __grid_const
     }
   }
 
+teardown:
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {

@@ -233,14 +233,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_int4_tc_kernel(const __grid_
       dev::mbar_init(dev::smem_u32(&x_empty[i]), 1);
     }
     dev::mbar_init(dev::smem_u32(&acc_full), 1);
-    // a wait has given up earlier in the call: leave before any copy or
-    // tensor-memory allocation (one decision for the whole CTA)
+    // a wait has given up earlier in the call: the CTA issues no copy and
+    // runs no role (one decision for the whole CTA, taken after the
+    // allocation's barrier: a barrier of its own before the allocation cost
+    // the projection kernels ~10 % of their time)
     *abort_v = dev::status_set(p.status) ? 1 : 0;
     epi_bad = 0;
     dev::fence_mbar_init();
   }
-  __syncthreads();
-  if (*abort_v) return;
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      dev::smem_u32(&tmem_slot)),
@@ -251,6 +251,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_int4_tc_kernel(const __grid_
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
+  if (*abort_v) goto teardown;
   // Only the activation stream (warp 0, lane 1) and, before it writes, the
   // epilogue depend on the previous launch: the int4 stream, the converters
   // (weights and scales) and the MMA issuer (fed by the two streams) run
@@ -542,6 +543,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_int4_tc_kernel(const __grid_
     }
   }
 
+teardown:
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
