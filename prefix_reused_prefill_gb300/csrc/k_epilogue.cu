@@ -37,41 +37,95 @@ __device__ __forceinline__ float split_sum(const float* part, long long plane, i
 }
 
 // cos/sin of pos * theta^(-2j/d), evaluated in double and rounded once.
-__global__ void rope_table_kernel(RowMap rows, int d, double theta, float2* table) {
+__device__ __forceinline__ float2 rope_pair(const RowMap& rows, int i, int j, const RopeFreq& fr) {
+  const double ang = (double)row_pos(rows, i) * fr.inv[j];
+  double sn, cs;
+  sincos(ang, &sn, &cs);
+  return make_float2((float)cs, (float)sn);
+}
+
+__global__ void rope_table_kernel(RowMap rows, int d, RopeFreq fr, float2* table) {
   dev::pdl_trigger();
   dev::pdl_wait();
   const int half = d / 2;
   const int idx = blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= rows.m * half) return;
-  const int i = idx / half, j = idx % half;
-  const double pos = (double)row_pos(rows, i);
-  const double ang = pos * pow(theta, -2.0 * j / d);
-  double sn, cs;
-  sincos(ang, &sn, &cs);
-  table[idx] = make_float2((float)cs, (float)sn);
+  table[idx] = rope_pair(rows, idx / half, idx % half, fr);
 }
 
-__global__ void embed_kernel(const __nv_bfloat16* hidden, int H, const __nv_bfloat16* gain,
-                             float eps, float* h, __nv_bfloat16* a, bool a16) {
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// One CTA (256 threads) per row i: the row's RoPE pairs (threads j < d/2), h =
+// float(hidden) and a = act(h * rsqrt(mean(h^2) + eps) * gain).  Each thread
+// holds its 8-element vectors of the row in registers between the sum and the
+// scaling (all of the row for H <= 4096; beyond that the rest is re-read).
+__global__ void __launch_bounds__(256) embed_kernel(const __nv_bfloat16* hidden, int H, const __nv_bfloat16* gain,
+                                                    float eps, float* h, __nv_bfloat16* a, bool a16, RowMap rows,
+                                                    int half, RopeFreq fr, float2* table) {
   dev::pdl_trigger();
   dev::pdl_wait();
   __shared__ float red[32];
-  const long long row = blockIdx.x;
+  constexpr int kV = 2;
+  const int i = blockIdx.x;
+  const long long row = i;
+  if (table && (int)threadIdx.x < half) table[row * half + threadIdx.x] = rope_pair(rows, i, threadIdx.x, fr);
+  const uint4* src = reinterpret_cast<const uint4*>(hidden + row * H);
+  uint4* dst = reinterpret_cast<uint4*>(a + row * H);
+  const int H8 = H >> 3;
+  uint4 v[kV];
+  float ss = 0.f;
+  auto sq = [](const uint4& x) {
+    float t = 0.f;
+    const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) t += bf16_lo(w[q]) * bf16_lo(w[q]) + bf16_hi(w[q]) * bf16_hi(w[q]);
+    return t;
+  };
+#pragma unroll
+  for (int u = 0; u < kV; ++u) {
+    const int k8 = threadIdx.x + u * 256;
+    v[u] = k8 < H8 ? src[k8] : make_uint4(0u, 0u, 0u, 0u);
+    ss += sq(v[u]);
+  }
   if (!gain) {   // attention-only layer: the input rows are the projection's input
-    for (int k = threadIdx.x; k < H; k += blockDim.x)
-      dev::store_act(a + row * H + k, __bfloat162float(hidden[row * H + k]), a16);
+    auto copy = [&](const uint4& x, int k8) {
+      uint4 o;
+      o.x = dev::pack_act2(bf16_lo(x.x), bf16_hi(x.x), a16);
+      o.y = dev::pack_act2(bf16_lo(x.y), bf16_hi(x.y), a16);
+      o.z = dev::pack_act2(bf16_lo(x.z), bf16_hi(x.z), a16);
+      o.w = dev::pack_act2(bf16_lo(x.w), bf16_hi(x.w), a16);
+      dst[k8] = o;
+    };
+#pragma unroll
+    for (int u = 0; u < kV; ++u)
+      if ((int)threadIdx.x + u * 256 < H8) copy(v[u], threadIdx.x + u * 256);
+    for (int k8 = threadIdx.x + kV * 256; k8 < H8; k8 += 256) copy(src[k8], k8);
     return;
   }
-  float ss = 0.f;
-  for (int k = threadIdx.x; k < H; k += blockDim.x) {
-    const float v = __bfloat162float(hidden[row * H + k]);
-    h[row * H + k] = v;
-    ss += v * v;
-  }
-  const float sum = block_sum(ss, red);
-  const float rs = rsqrtf(sum / H + eps);
-  for (int k = threadIdx.x; k < H; k += blockDim.x)
-    dev::store_act(a + row * H + k, h[row * H + k] * rs * __bfloat162float(gain[k]), a16);
+  for (int k8 = threadIdx.x + kV * 256; k8 < H8; k8 += 256) ss += sq(src[k8]);
+  const float rs = rsqrtf(block_sum(ss, red) / H + eps);
+  const uint4* g8 = reinterpret_cast<const uint4*>(gain);
+  float4* h4 = reinterpret_cast<float4*>(h + row * H);
+  auto put = [&](const uint4& x, int k8) {
+    const uint4 g = g8[k8];
+    const float f[8] = {bf16_lo(x.x), bf16_hi(x.x), bf16_lo(x.y), bf16_hi(x.y),
+                        bf16_lo(x.z), bf16_hi(x.z), bf16_lo(x.w), bf16_hi(x.w)};
+    const float gf[8] = {bf16_lo(g.x), bf16_hi(g.x), bf16_lo(g.y), bf16_hi(g.y),
+                         bf16_lo(g.z), bf16_hi(g.z), bf16_lo(g.w), bf16_hi(g.w)};
+    h4[2 * k8] = make_float4(f[0], f[1], f[2], f[3]);
+    h4[2 * k8 + 1] = make_float4(f[4], f[5], f[6], f[7]);
+    uint4 o;
+    o.x = dev::pack_act2(f[0] * rs * gf[0], f[1] * rs * gf[1], a16);
+    o.y = dev::pack_act2(f[2] * rs * gf[2], f[3] * rs * gf[3], a16);
+    o.z = dev::pack_act2(f[4] * rs * gf[4], f[5] * rs * gf[5], a16);
+    o.w = dev::pack_act2(f[6] * rs * gf[6], f[7] * rs * gf[7], a16);
+    dst[k8] = o;
+  };
+#pragma unroll
+  for (int u = 0; u < kV; ++u)
+    if ((int)threadIdx.x + u * 256 < H8) put(v[u], threadIdx.x + u * 256);
+  for (int k8 = threadIdx.x + kV * 256; k8 < H8; k8 += 256) put(src[k8], k8);
 }
 
 // One CTA per row: a = bf16(h * rsqrt(mean(h^2) + eps) * gain), the RMSNorm
@@ -309,14 +363,22 @@ inline unsigned blocks_for(long long n, int threads) { return (unsigned)((n + th
 
 }  // namespace
 
-cudaError_t launch_rope_table(const RowMap& rows, int d, float theta, float2* table, cudaStream_t st) {
+RopeFreq rope_freq(float theta, int d) {
+  RopeFreq fr;
+  for (int j = 0; j < 64; ++j) fr.inv[j] = j < d / 2 ? pow((double)theta, -2.0 * j / d) : 0.0;
+  return fr;
+}
+
+cudaError_t launch_rope_table(const RowMap& rows, int d, const RopeFreq& fr, float2* table, cudaStream_t st) {
   const long long n = (long long)rows.m * (d / 2);
-  return launch_k(rope_table_kernel, blocks_for(n, 256), 256, 0, st, rows, d, (double)theta, table);
+  return launch_k(rope_table_kernel, blocks_for(n, 256), 256, 0, st, rows, d, fr, table);
 }
 
 cudaError_t launch_embed(const __nv_bfloat16* hidden, int m, int H, const __nv_bfloat16* gain,
-                         float eps, float* h, __nv_bfloat16* a, bool a16, cudaStream_t st) {
-  return launch_k(embed_kernel, m, 256, 0, st, hidden, H, gain, eps, h, a, a16);
+                         float eps, float* h, __nv_bfloat16* a, bool a16, const RowMap& rows, int d,
+                         const RopeFreq& fr, float2* table, cudaStream_t st) {
+  if (H % 8 || d / 2 > 64) return cudaErrorInvalidValue;
+  return launch_k(embed_kernel, m, 256, 0, st, hidden, H, gain, eps, h, a, a16, rows, d / 2, fr, table);
 }
 
 cudaError_t launch_norm(const float* h, int m, int H, const __nv_bfloat16* gain, float eps,

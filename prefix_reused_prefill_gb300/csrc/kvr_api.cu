@@ -198,6 +198,7 @@ struct kvr_ctx {
   int* slot_len = nullptr;
   int32_t* match_out = nullptr;
   float2* rope = nullptr;
+  RopeFreq rope_fr;   // theta^(-2j/d) in double, from the configuration
   float* h = nullptr;
   __nv_bfloat16 *a = nullptr, *q = nullptr, *o = nullptr, *z = nullptr;
   // the call's projections run on the tcgen05 GEMM, whose operands are fp16:
@@ -897,7 +898,7 @@ int run_pass(kvr_ctx* c, const RowMap& rows, const void* hidden, const kvr_layer
   c->act16 = false;
   {
     Timed t(c, kEpi, st);
-    e = launch_rope_table(rows, d, k.rope_theta, c->rope, st);
+    e = launch_rope_table(rows, d, c->rope_fr, c->rope, st);
   }
   if (e != cudaSuccess) return cuda_fail(c, e, "rope table launch");
   {
@@ -919,18 +920,14 @@ int run_stack(kvr_ctx* c, const RowMap& rows, const void* hidden,
   const int m = rows.m, H = k.hidden, d = k.head_dim;
   const int Hq = k.n_q_heads, Hkv = k.n_kv_heads, F = k.ffn;
   cudaError_t e;
-  {
-    Timed t(c, kEpi, st);
-    e = launch_rope_table(rows, d, k.rope_theta, c->rope, st);
-  }
-  if (e != cudaSuccess) return cuda_fail(c, e, "rope table launch");
   c->act16 = packed4(k) && !gemv_path(c, m);
   {
-    // attention-only layers take the input rows as they are (no norm)
+    // the rows' RoPE table and the first RMSNorm in one launch; attention-only
+    // layers take the input rows as they are (no norm)
     Timed t(c, kEpi, st);
     e = launch_embed(static_cast<const __nv_bfloat16*>(hidden), m, H,
                      k.attn_only ? nullptr : static_cast<const __nv_bfloat16*>(w[0].norm_attn), k.rms_eps,
-                     c->h, c->a, c->act16, st);
+                     c->h, c->a, c->act16, rows, d, c->rope_fr, c->rope, st);
     if (e != cudaSuccess) return cuda_fail(c, e, "embed launch");
   }
   auto trace = [&](int entry) -> cudaError_t {
@@ -1404,6 +1401,7 @@ int kvr_ctx_create(const kvr_config* cfg, void* kv_arena, size_t arena_bytes, vo
   c->slot_len = reinterpret_cast<int*>(s + c->sl.slot_len);
   c->match_out = reinterpret_cast<int32_t*>(s + c->sl.match_out);
   c->rope = reinterpret_cast<float2*>(s + c->sl.rope);
+  c->rope_fr = rope_freq(cfg->rope_theta, cfg->head_dim);
   c->h = reinterpret_cast<float*>(s + c->sl.h);
   c->a = reinterpret_cast<__nv_bfloat16*>(s + c->sl.a);
   c->q = reinterpret_cast<__nv_bfloat16*>(s + c->sl.q);

@@ -312,13 +312,23 @@ cudaError_t launch_gemm_int4_tc(const GemmParams& p, int total_tiles, cudaStream
 cudaError_t launch_attention(const AttnParams& p, int d, int row_warps, cudaStream_t st);
 cudaError_t launch_attention_tc(const AttnParams& p, int d, cudaStream_t st);
 cudaError_t launch_attn_combine(const AttnParams& p, int d, cudaStream_t st);
-cudaError_t launch_rope_table(const RowMap& rows, int d, float theta, float2* table,
+// RoPE inverse frequencies theta^(-2j/d), j < d/2, in double (computed once
+// per context on the host; d <= 128)
+struct RopeFreq {
+  double inv[64];
+};
+RopeFreq rope_freq(float theta, int d);
+// table[i][j] = (cos, sin) of pos_i * inv[j], in double, rounded once to float
+cudaError_t launch_rope_table(const RowMap& rows, int d, const RopeFreq& fr, float2* table,
                               cudaStream_t st);
 // h = float(hidden) and the first RMSNorm: a = bf16(RMSNorm(h) * gain).
 // Without a gain, a = hidden (attention-only layers; h untouched).  a16: a
 // holds the bf16-rounded values as fp16 (the tcgen05 GEMM's operand type).
+// The same launch writes the rows' RoPE table as launch_rope_table does.
+// H must be a multiple of 8 (hidden, h and a rows 16-byte aligned).
 cudaError_t launch_embed(const __nv_bfloat16* hidden, int m, int H, const __nv_bfloat16* gain,
-                         float eps, float* h, __nv_bfloat16* a, bool a16, cudaStream_t st);
+                         float eps, float* h, __nv_bfloat16* a, bool a16, const RowMap& rows, int d,
+                         const RopeFreq& fr, float2* table, cudaStream_t st);
 // a = bf16(RMSNorm(h) * gain) for rows [0, m) of the fp32 residual stream
 // (after a small-m residual projection, whose tiles each hold part of a row)
 cudaError_t launch_norm(const float* h, int m, int H, const __nv_bfloat16* gain, float eps,
