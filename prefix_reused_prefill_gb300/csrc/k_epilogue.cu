@@ -175,7 +175,7 @@ __global__ void __launch_bounds__(256) norm_kernel(const float* h, int H, const 
 // K rows to the slot, and V through a shared-memory transpose to the slot's
 // V^T rows so every global write is contiguous.  Thread = (token, 8-pair chunk).
 template <int D>
-__global__ void __launch_bounds__(256) epi_qkv_kernel(const float* part, long long plane, int ksplit,
+__global__ void __launch_bounds__(256, 4) epi_qkv_kernel(const float* part, long long plane, int ksplit,
                                                       int ldo, int c0, int mb, RowMap rows, int Hq,
                                                       int Hkv, const float2* rope, __nv_bfloat16* q,
                                                       __nv_bfloat16* arena, long long k_off,
@@ -195,6 +195,14 @@ __global__ void __launch_bounds__(256) epi_qkv_kernel(const float* part, long lo
   float x1[8], x2[8];
 #pragma unroll
   for (int e = 0; e < 8; ++e) x1[e] = x2[e] = 0.f;
+  // (cos, sin) of pairs j0 .. j0+7, loaded alongside the split partials
+  float4 cs[4];
+  const bool rotate = live && hd < Hq + Hkv;
+  if (rotate) {
+    const float4* cs4 = reinterpret_cast<const float4*>(rope + (long long)i * kHalf + j0);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) cs[e] = cs4[e];
+  }
   if (live) {
     const float* src = part + (long long)t * ldo + (long long)hd * D + j0;
 #pragma unroll 4
@@ -210,16 +218,15 @@ __global__ void __launch_bounds__(256) epi_qkv_kernel(const float* part, long lo
     }
   }
   if (hd < Hq + Hkv) {
-    if (live) {
-      const float4* cs4 = reinterpret_cast<const float4*>(rope + (long long)i * kHalf + j0);
+    if (rotate) {
       float y1[8], y2[8];
 #pragma unroll
       for (int e = 0; e < 8; e += 2) {
-        const float4 cs = cs4[e / 2];   // (cos, sin) of pairs j0+e and j0+e+1
-        y1[e] = x1[e] * cs.x - x2[e] * cs.y;
-        y2[e] = x2[e] * cs.x + x1[e] * cs.y;
-        y1[e + 1] = x1[e + 1] * cs.z - x2[e + 1] * cs.w;
-        y2[e + 1] = x2[e + 1] * cs.z + x1[e + 1] * cs.w;
+        const float4 c = cs[e / 2];   // (cos, sin) of pairs j0+e and j0+e+1
+        y1[e] = x1[e] * c.x - x2[e] * c.y;
+        y2[e] = x2[e] * c.x + x1[e] * c.y;
+        y1[e + 1] = x1[e + 1] * c.z - x2[e + 1] * c.w;
+        y2[e + 1] = x2[e + 1] * c.z + x1[e + 1] * c.w;
       }
       __nv_bfloat16* dst;
       if (hd < Hq) {
@@ -262,7 +269,7 @@ __global__ void __launch_bounds__(256) epi_qkv_kernel(const float* part, long lo
 // registers between the two passes.
 constexpr int kResidThreads = 512;
 template <int V>  // float4 per thread (H <= 4 * 512 * V)
-__global__ void __launch_bounds__(kResidThreads) epi_resid_kernel(const float* part, long long plane, int ksplit,
+__global__ void __launch_bounds__(kResidThreads, V <= 2 ? 2 : 1) epi_resid_kernel(const float* part, long long plane, int ksplit,
                                                                   int ldo, int c0, int H, float* h,
                                                                   const __nv_bfloat16* gain, float eps,
                                                                   __nv_bfloat16* a_out, bool a16,
@@ -276,8 +283,10 @@ __global__ void __launch_bounds__(kResidThreads) epi_resid_kernel(const float* p
   const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
   const float4* pp = reinterpret_cast<const float4*>(part + (long long)t * ldo);
   const long long pl4 = plane >> 2;
-  // splits in flight at once: all of them for up to two float4 per thread
-  constexpr int kB = V <= 2 ? kGemmMaxSplit : kGemmMaxSplit / 2;
+  // splits in flight at once: five (a 5-way k-split in one round) for up to
+  // two float4 per thread, which keeps two CTAs on an SM (62 registers), so
+  // one wave covers 304 rows
+  constexpr int kB = V <= 2 ? 5 : kGemmMaxSplit / 2;
   float4 v[V];
 #pragma unroll
   for (int u = 0; u < V; ++u) {
