@@ -218,6 +218,32 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_int4_tc_kernel(const __grid_
   const int nkc = kc1 - kc0;
   const uint32_t xbytes = 2u * (uint32_t)p.xrows * 128u;
 
+  // the int4 stream of stage i (thread 0: the weight producer)
+  auto prefetch_stage = [&](int i) {
+    const int x = (kc0 + i) * 64;
+    if (p.swiglu) {
+      dev::tma_prefetch_2d(&p.seg[0].tw, x, row0);
+      dev::tma_prefetch_2d(&p.seg[1].tw, x, row0);
+    } else {
+      dev::tma_prefetch_2d(&seg.tw, x, row0);
+    }
+  };
+  auto load_stage = [&](int i, uint64_t pol) {
+    const int rs = i % kRawStages;
+    const uint32_t rb = raw_base + rs * kRawBytes;
+    const uint32_t fb = dev::smem_u32(&raw_full[rs]);
+    dev::mbar_arrive_expect_tx(fb, kRawBytes);
+    const int x = (kc0 + i) * 64;
+    if (p.swiglu) {
+      dev::tma_load_2d_hint(rb, &p.seg[0].tw, x, row0, fb, pol);
+      dev::tma_load_2d_hint(rb + kRawBytes / 2, &p.seg[1].tw, x, row0, fb, pol);
+    } else {
+      dev::tma_load_2d_hint(rb, &seg.tw, x, row0, fb, pol);
+    }
+  };
+  // int4 stages the weight producer issues before the CTA's barrier
+  const int early = nkc < kRawStages ? nkc : kRawStages;
+
   dev::pdl_trigger();
   if (threadIdx.x == 0) {
     for (int i = 0; i < kRawStages; ++i) {
@@ -240,6 +266,18 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_int4_tc_kernel(const __grid_
     *abort_v = dev::status_set(p.status) ? 1 : 0;
     epi_bad = 0;
     dev::fence_mbar_init();
+    // Thread 0 is also the weight producer: it fills the int4 ring now (its
+    // barriers are initialised and fenced), while warp 1 allocates TMEM, so the
+    // first stage's HBM latency overlaps the CTA's set-up.  Weights depend on
+    // no earlier launch.
+    if (!*abort_v) {
+      dev::prefetch_tmap(&p.seg[0].tw);
+      if (p.swiglu) dev::prefetch_tmap(&p.seg[1].tw);
+      else dev::prefetch_tmap(&seg.tw);
+      const uint64_t pol = dev::policy_evict_first();
+      for (int i = 0; i < early; ++i) load_stage(i, pol);
+      for (int i = early; i < early + kPrefetch && i < nkc; ++i) prefetch_stage(i);
+    }
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -261,22 +299,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_int4_tc_kernel(const __grid_
   if (warp == 0) {
     // ---------------------------------------------------------------- producers
     if (lane == 0) {
-      dev::prefetch_tmap(&p.seg[0].tw);
-      if (p.swiglu) dev::prefetch_tmap(&p.seg[1].tw);
-      else dev::prefetch_tmap(&seg.tw);
+      // stages 0 .. early-1 went out before the CTA's barrier (thread 0)
       const uint64_t pol = dev::policy_evict_first();
-      auto prefetch_stage = [&](int i) {
-        const int x = (kc0 + i) * 64;
-        if (p.swiglu) {
-          dev::tma_prefetch_2d(&p.seg[0].tw, x, row0);
-          dev::tma_prefetch_2d(&p.seg[1].tw, x, row0);
-        } else {
-          dev::tma_prefetch_2d(&seg.tw, x, row0);
-        }
-      };
-      for (int i = 0; i < kPrefetch && i < nkc; ++i) prefetch_stage(i);
-      int issued = 0;
-      for (int i = 0; i < nkc; ++i) {
+      int issued = early;
+      for (int i = early; i < nkc; ++i) {
         if (i + kPrefetch < nkc) prefetch_stage(i + kPrefetch);
         const int rs = i % kRawStages;
         if (i >= kRawStages &&
@@ -285,16 +311,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_int4_tc_kernel(const __grid_
           *abort_v = 1;
           break;
         }
-        const uint32_t rb = raw_base + rs * kRawBytes;
-        const uint32_t fb = dev::smem_u32(&raw_full[rs]);
-        dev::mbar_arrive_expect_tx(fb, kRawBytes);
-        const int x = (kc0 + i) * 64;
-        if (p.swiglu) {
-          dev::tma_load_2d_hint(rb, &p.seg[0].tw, x, row0, fb, pol);
-          dev::tma_load_2d_hint(rb + kRawBytes / 2, &p.seg[1].tw, x, row0, fb, pol);
-        } else {
-          dev::tma_load_2d_hint(rb, &seg.tw, x, row0, fb, pol);
-        }
+        load_stage(i, pol);
         ++issued;
       }
       const unsigned long long deadline = dev::globaltimer_ns() + kWaitLimitNs;
