@@ -52,9 +52,9 @@ FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1
 
 P_CACHED, M_ROWS, PROMPT = 1668, 254, 1922
 # DRAM bytes (read + write) of the four projection GEMMs of one layer of this workload, from one
-# ncu capture (dram__bytes_read.sum + dram__bytes_write.sum, cold L2): 11.17 + 9.11 + 80.39 + 48.34 MB.
+# ncu capture (dram__bytes_read.sum + dram__bytes_write.sum, cold L2): 11.17 + 9.11 + 80.23 + 48.35 MB.
 # Re-take the capture whenever gemm_int4_tc_kernel changes.
-PROJ_TRAFFIC_PER_LAYER = 149.01e6
+PROJ_TRAFFIC_PER_LAYER = 148.85e6
 
 
 def peaks():
