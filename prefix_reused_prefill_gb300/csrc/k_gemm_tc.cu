@@ -23,7 +23,9 @@
 // operand) live in tensor memory, which keeps shared memory for a 3-deep
 // activation ring.  Warp roles:
 //   warp 0     lane 0 streams int4 tiles (128 inputs x 128 rows, 64B-swizzled,
-//              4 stages, prefetched into L2 two stages ahead), lane 1 streams
+//              4 stages, prefetched into L2 two stages ahead; it is thread 0,
+//              which fills the ring as soon as it has initialised the
+//              barriers, before the CTA's barrier), lane 1 streams
 //              activation tiles (128 inputs x N tokens as two 128B-swizzled
 //              K-major atoms, 3 stages); the two rings are independent;
 //   warp 1     allocates the TMEM accumulator; one thread issues tcgen05.mma
