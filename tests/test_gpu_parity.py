@@ -94,6 +94,7 @@ def test_tiny_config_exact():
     ("small_bf16", 33, [2, 11, 35], 256),
     ("small", 150, [300], 512),
     ("small_q4k", 70, [1, 3, 9, 17, 40, 130], 256),   # K-quant: GEMV at 8/16/32 tokens, tcgen05 GEMM
+    ("wide", 40, [1, 9, 40], 256),                     # hidden 4352: row kernels past 4096 elements
 ])
 def test_suffix_prefill_matches_oracle(shape_name, P, ms, cap):
     shape, kv, w, W, _ = make(shape_name, 2, cap, min(cap, 320))

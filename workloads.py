@@ -89,6 +89,8 @@ SHAPES: Dict[str, ModelShape] = {
     "small_q4k": ModelShape("small_q4k", 512, 8, 2, 64, 1024, 2, "q4k"),
     # head_dim 128 with four query heads per KV head (the small-m pass's shape class)
     "small_g4": ModelShape("small_g4", 512, 8, 2, 128, 1024, 3, "int4"),
+    # hidden above 4096 (the row kernels' loops past the first 4096 elements of a row)
+    "wide": ModelShape("wide", 4352, 8, 2, 64, 512, 1, "int4"),
     # the turn-9 and verify shapes with K-quant superblock weights
     "qwen7b_q4k": ModelShape("qwen7b_q4k", 3584, 28, 4, 128, 18944, 28, "q4k"),
     "dense9b_q4k": ModelShape("dense9b_q4k", 4096, 32, 8, 128, 12288, 36, "q4k"),
