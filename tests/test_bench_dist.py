@@ -36,7 +36,7 @@ def _rank_main(rank, world, port, q):
 
         class Args:
             steps, warmup, cpu_rows = 1, 0, 4
-        ref_line = bench.run_reference(Args, r, w)[0] if r != 0 else "rank0-skipped"
+        ref_line = bench.run_reference(Args, r, w)[0]   # rank 0: 4 suffix rows of one layer
         q.put((r, w, dist.get_backend(), slowest, rate, ref_line))
     finally:
         dist.destroy_process_group()
@@ -58,3 +58,17 @@ def test_two_gloo_ranks_agree_on_the_slowest_rank_and_only_rank0_reports():
         assert r[3] == pytest.approx(20.0)                       # max over ranks of 10, 20 ms
         assert r[4] == pytest.approx(2 * 254 * 4 / 0.020)        # whole-job rows/s
     assert results[1][5] is None                                 # rank 1 of the reference arm: no work, no line
+    # rank 0's reference line: the contract's keys, the GPU arm's config and metric, e2e without copies
+    line = results[0][5]
+    for k in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+              "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert k in line, k
+    sys.path.insert(0, ROOT)
+    import bench
+    assert line["impl"] == "reference" and line["metric"] == "suffix-prefill rows/s" and line["unit"] == "rows/s"
+    assert line["config"] == bench.turn9_config(2) and line["n_gpus"] == 2
+    assert line["value"] > 0 and line["higher_is_better"] is True
+    assert line["e2e"] == {"value": line["value"], "unit": "rows/s", "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}
+    cb = line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == line["value"] and "4 suffix rows" in cb["sample"]
