@@ -134,12 +134,20 @@ __global__ void __launch_bounds__(256) embed_kernel(const __nv_bfloat16* hidden,
 __global__ void __launch_bounds__(256) norm_kernel(const float* h, int H, const __nv_bfloat16* gain, float eps,
                                                    __nv_bfloat16* a) {
   dev::pdl_trigger();
-  dev::pdl_wait();
   __shared__ float red[32];
   constexpr int kV = 4;   // float4 per thread held in registers
   const long long row = blockIdx.x;
   const float4* src = reinterpret_cast<const float4*>(h + row * H);
   const int H4 = H >> 2;
+  // the gains are weights (no launch writes them): requested before the wait
+  const uint2* g2 = reinterpret_cast<const uint2*>(gain);
+  uint2 gw[kV];
+#pragma unroll
+  for (int u = 0; u < kV; ++u) {
+    const int k4 = threadIdx.x + u * 256;
+    gw[u] = k4 < H4 ? g2[k4] : make_uint2(0u, 0u);
+  }
+  dev::pdl_wait();
   float4 v[kV];
   float ss = 0.f;
 #pragma unroll
@@ -153,10 +161,9 @@ __global__ void __launch_bounds__(256) norm_kernel(const float* h, int H, const 
     ss += x.x * x.x + x.y * x.y + x.z * x.z + x.w * x.w;
   }
   const float rs = rsqrtf(block_sum(ss, red) / H + eps);
-  auto put = [&](const float4& x, int k4) {
-    const uint2 gw = reinterpret_cast<const uint2*>(gain)[k4];
-    const __nv_bfloat162 g01 = *reinterpret_cast<const __nv_bfloat162*>(&gw.x);
-    const __nv_bfloat162 g23 = *reinterpret_cast<const __nv_bfloat162*>(&gw.y);
+  auto put = [&](const float4& x, const uint2& g, int k4) {
+    const __nv_bfloat162 g01 = *reinterpret_cast<const __nv_bfloat162*>(&g.x);
+    const __nv_bfloat162 g23 = *reinterpret_cast<const __nv_bfloat162*>(&g.y);
     uint2 o;
     o.x = dev::pack_bf16x2(x.x * rs * __bfloat162float(g01.x), x.y * rs * __bfloat162float(g01.y));
     o.y = dev::pack_bf16x2(x.z * rs * __bfloat162float(g23.x), x.w * rs * __bfloat162float(g23.y));
@@ -165,9 +172,9 @@ __global__ void __launch_bounds__(256) norm_kernel(const float* h, int H, const 
 #pragma unroll
   for (int u = 0; u < kV; ++u) {
     const int k4 = threadIdx.x + u * 256;
-    if (k4 < H4) put(v[u], k4);
+    if (k4 < H4) put(v[u], gw[u], k4);
   }
-  for (int k4 = threadIdx.x + kV * 256; k4 < H4; k4 += 256) put(src[k4], k4);
+  for (int k4 = threadIdx.x + kV * 256; k4 < H4; k4 += 256) put(src[k4], g2[k4], k4);
 }
 
 // One CTA per (tile of tokens, head): sum the split partials, rotate q/k
@@ -275,11 +282,18 @@ __global__ void __launch_bounds__(kResidThreads, V <= 2 ? 2 : 1) epi_resid_kerne
                                                                   __nv_bfloat16* a_out, bool a16,
                                                                   __nv_bfloat16* final_out) {
   dev::pdl_trigger();
-  dev::pdl_wait();
   __shared__ float red[32];
   const int t = blockIdx.x;
   const long long i = c0 + t;
   const int H4 = H >> 2;
+  // the norm gains are weights (no launch writes them): requested before the wait
+  uint2 gw[V];
+#pragma unroll
+  for (int u = 0; u < V; ++u) {
+    const int k4 = threadIdx.x + u * kResidThreads;
+    gw[u] = a_out && k4 < H4 ? reinterpret_cast<const uint2*>(gain)[k4] : make_uint2(0u, 0u);
+  }
+  dev::pdl_wait();
   const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
   const float4* pp = reinterpret_cast<const float4*>(part + (long long)t * ldo);
   const long long pl4 = plane >> 2;
@@ -333,9 +347,8 @@ __global__ void __launch_bounds__(kResidThreads, V <= 2 ? 2 : 1) epi_resid_kerne
     for (int u = 0; u < V; ++u) {
       const int k4 = threadIdx.x + u * kResidThreads;
       if (k4 < H4) {
-        const uint2 gw = reinterpret_cast<const uint2*>(gain)[k4];
-        const __nv_bfloat162 g01 = *reinterpret_cast<const __nv_bfloat162*>(&gw.x);
-        const __nv_bfloat162 g23 = *reinterpret_cast<const __nv_bfloat162*>(&gw.y);
+        const __nv_bfloat162 g01 = *reinterpret_cast<const __nv_bfloat162*>(&gw[u].x);
+        const __nv_bfloat162 g23 = *reinterpret_cast<const __nv_bfloat162*>(&gw[u].y);
         uint2 o;
         o.x = dev::pack_act2(v[u].x * rs * __bfloat162float(g01.x), v[u].y * rs * __bfloat162float(g01.y), a16);
         o.y = dev::pack_act2(v[u].z * rs * __bfloat162float(g23.x), v[u].w * rs * __bfloat162float(g23.y), a16);
