@@ -64,15 +64,23 @@ __global__ void __launch_bounds__(256) embed_kernel(const __nv_bfloat16* hidden,
                                                     float eps, float* h, __nv_bfloat16* a, bool a16, RowMap rows,
                                                     int half, RopeFreq fr, float2* table) {
   dev::pdl_trigger();
-  dev::pdl_wait();
   __shared__ float red[32];
   constexpr int kV = 2;
   const int i = blockIdx.x;
   const long long row = i;
+  const int H8 = H >> 3;
+  // the norm gains are weights (no launch writes them): requested before the wait
+  const uint4* g8 = reinterpret_cast<const uint4*>(gain);
+  uint4 gv[kV];
+#pragma unroll
+  for (int u = 0; u < kV; ++u) {
+    const int k8 = threadIdx.x + u * 256;
+    gv[u] = gain && k8 < H8 ? g8[k8] : make_uint4(0u, 0u, 0u, 0u);
+  }
+  dev::pdl_wait();
   if (table && (int)threadIdx.x < half) table[row * half + threadIdx.x] = rope_pair(rows, i, threadIdx.x, fr);
   const uint4* src = reinterpret_cast<const uint4*>(hidden + row * H);
   uint4* dst = reinterpret_cast<uint4*>(a + row * H);
-  const int H8 = H >> 3;
   uint4 v[kV];
   float ss = 0.f;
   auto sq = [](const uint4& x) {
@@ -105,10 +113,8 @@ __global__ void __launch_bounds__(256) embed_kernel(const __nv_bfloat16* hidden,
   }
   for (int k8 = threadIdx.x + kV * 256; k8 < H8; k8 += 256) ss += sq(src[k8]);
   const float rs = rsqrtf(block_sum(ss, red) / H + eps);
-  const uint4* g8 = reinterpret_cast<const uint4*>(gain);
   float4* h4 = reinterpret_cast<float4*>(h + row * H);
-  auto put = [&](const uint4& x, int k8) {
-    const uint4 g = g8[k8];
+  auto put = [&](const uint4& x, const uint4& g, int k8) {
     const float f[8] = {bf16_lo(x.x), bf16_hi(x.x), bf16_lo(x.y), bf16_hi(x.y),
                         bf16_lo(x.z), bf16_hi(x.z), bf16_lo(x.w), bf16_hi(x.w)};
     const float gf[8] = {bf16_lo(g.x), bf16_hi(g.x), bf16_lo(g.y), bf16_hi(g.y),
@@ -124,8 +130,8 @@ __global__ void __launch_bounds__(256) embed_kernel(const __nv_bfloat16* hidden,
   };
 #pragma unroll
   for (int u = 0; u < kV; ++u)
-    if ((int)threadIdx.x + u * 256 < H8) put(v[u], threadIdx.x + u * 256);
-  for (int k8 = threadIdx.x + kV * 256; k8 < H8; k8 += 256) put(src[k8], k8);
+    if ((int)threadIdx.x + u * 256 < H8) put(v[u], gv[u], threadIdx.x + u * 256);
+  for (int k8 = threadIdx.x + kV * 256; k8 < H8; k8 += 256) put(src[k8], g8[k8], k8);
 }
 
 // One CTA per row: a = bf16(h * rsqrt(mean(h^2) + eps) * gain), the RMSNorm
